@@ -1,0 +1,491 @@
+// CPU oracle for the per-layer MoE expert step.  TEST INFRASTRUCTURE ONLY.
+//
+// This file is a plain, slow, scalar restatement of what the step computes.
+// It exists so the CUDA path can be checked against an independent program:
+// it shares no code, header, table or constant generator with the CUDA
+// library, and only the test suite, the smoke check and the timed CPU
+// baseline of the benchmark may load it.  The product never calls it.
+//
+// Sources (FreeToken paper summary "paper.rainbus.top/paper/2608.16157",
+// FreeToken reader "paperglide.net ... freetoken", Edge0 translation
+// "bittide.aicompass.dev ... arXiv 2609.18063"):
+//   * routing families          - Edge0 §2 "MoE routing"
+//   * int4 affine group-64      - Edge0 §2 "Quantisation", §3.1 "executor paths"
+//   * expert math               - Edge0 §3.1 "math convention":
+//                                 down(silu(gate(x)) * up(x))
+//   * lE+e bank ids, dedup, hit classification, q* split, single-pass
+//     K-victim choice           - FreeToken "core method", "method steps",
+//                                 "novelty"; reader "Semantic-Aware Expert
+//                                 Caching" and "Elastic Memory Management"
+//   * exact merge of partials   - FreeToken "core method"
+//
+// Readings where the pages are silent (each is listed in the design notes):
+//   * blob byte layout and nibble order (low nibble = even column)
+//   * dequant w = s*q + b with q unsigned 0..15 (additive "bias")
+//   * router dot product order (CANON-DOT below), own exp (ORACLE-EXP below)
+//   * softmax-top-k weights computed over the selected k only
+//   * sigmoid-group tie rules and normalise-then-scale order
+//   * q rounding half-up, F = lowest-id misses, q capped by K
+//   * clock advanced once per control call; victims exclude slots hit now
+//   * shared expert added with weight 1
+//
+// Parity status: every function below is pinned by the not-gpu tests
+// (worked examples from the pages, closed forms, brute force, float64).
+//
+// Build: g++ -std=c++17 -O2 -ffp-contract=off -fPIC -shared (no -ffast-math).
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+namespace {
+
+const int kGroup = 64;
+
+float bf16_to_float(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return f;
+}
+
+float bits_to_float(uint32_t u) {
+  float f;
+  std::memcpy(&f, &u, 4);
+  return f;
+}
+
+// Byte offsets of the nine sections of an expert blob (the layout reading).
+struct BlobLayout {
+  int64_t gq, uq, dq, gs, gb, us, ub, ds, db, total;
+};
+
+BlobLayout layout_of(int64_t H, int64_t I) {
+  BlobLayout L;
+  int64_t codes_gu = I * H / 2;       // [I][H] nibbles
+  int64_t codes_d = H * I / 2;        // [H][I] nibbles
+  int64_t sb_gu = I * (H / kGroup) * 2;  // bf16 [I][H/64]
+  int64_t sb_d = H * (I / kGroup) * 2;   // bf16 [H][I/64]
+  L.gq = 0;
+  L.uq = L.gq + codes_gu;
+  L.dq = L.uq + codes_gu;
+  L.gs = L.dq + codes_d;
+  L.gb = L.gs + sb_gu;
+  L.us = L.gb + sb_gu;
+  L.ub = L.us + sb_gu;
+  L.ds = L.ub + sb_gu;
+  L.db = L.ds + sb_d;
+  int64_t end = L.db + sb_d;
+  L.total = (end + 255) / 256 * 256;
+  return L;
+}
+
+// Code of column c in a packed row: two codes per byte, low nibble = even c.
+int code_at(const uint8_t* row, int64_t c) {
+  uint8_t byte = row[c / 2];
+  return (c % 2 == 0) ? (byte & 0x0F) : (byte >> 4);
+}
+
+// Dequantised weight of a [rows][cols] matrix: w = s*q + b in fp32, with s
+// and b the bf16 scale and bias of the 64-column group holding column c.
+float weight_at(const uint8_t* codes, const uint16_t* s, const uint16_t* b, int64_t cols,
+                int64_t r, int64_t c) {
+  int q = code_at(codes + r * (cols / 2), c);
+  int64_t g = r * (cols / kGroup) + c / kGroup;
+  float sf = bf16_to_float(s[g]);
+  float bf = bf16_to_float(b[g]);
+  float prod = sf * (float)q;  // exact: 8-bit x 4-bit significands
+  return prod + bf;
+}
+
+}  // namespace
+
+extern "C" {
+
+// ------------------------------------------------------------------ layout
+int64_t or_expert_bytes(int H, int I) {
+  if (H <= 0 || I <= 0 || H % kGroup || I % kGroup) return -1;
+  return layout_of(H, I).total;
+}
+
+// off[0..9] = gq uq dq gs gb us ub ds db total
+void or_blob_offsets(int H, int I, int64_t* off) {
+  BlobLayout L = layout_of(H, I);
+  int64_t v[10] = {L.gq, L.uq, L.dq, L.gs, L.gb, L.us, L.ub, L.ds, L.db, L.total};
+  for (int i = 0; i < 10; ++i) off[i] = v[i];
+}
+
+// ----------------------------------------------------------------- dequant
+// Edge0 §2 "Quantisation" / §3.1: int4 affine group-64 weights with a scale
+// and a bias per group.  out[r][c] = s[r][c/64] * q[r][c] + b[r][c/64].
+void or_dequant(const uint8_t* codes, const uint16_t* s, const uint16_t* b, int rows, int cols,
+                float* out) {
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c) out[r * cols + c] = weight_at(codes, s, b, cols, r, c);
+}
+
+// Dequantise matrix `which` (0 = gate [I][H], 1 = up [I][H], 2 = down [H][I])
+// straight out of an expert blob.
+void or_blob_matrix(const uint8_t* blob, int H, int I, int which, float* out) {
+  BlobLayout L = layout_of(H, I);
+  const uint8_t* q;
+  const uint16_t *s, *b;
+  int rows, cols;
+  if (which == 0) {
+    q = blob + L.gq; s = (const uint16_t*)(blob + L.gs); b = (const uint16_t*)(blob + L.gb);
+    rows = I; cols = H;
+  } else if (which == 1) {
+    q = blob + L.uq; s = (const uint16_t*)(blob + L.us); b = (const uint16_t*)(blob + L.ub);
+    rows = I; cols = H;
+  } else {
+    q = blob + L.dq; s = (const uint16_t*)(blob + L.ds); b = (const uint16_t*)(blob + L.db);
+    rows = H; cols = I;
+  }
+  or_dequant(q, s, b, rows, cols, out);
+}
+
+// --------------------------------------------------------------- ORACLE-EXP
+// Own single-precision exp (not any library's): Cody-Waite reduction
+// x = n*ln2 + r with ln2 split into a short high part and a low part,
+// |r| <= ln2/2, then the degree-7 Taylor polynomial of e^r in Horner form with
+// fused multiply-adds, then exact scaling by 2^n built from exponent bits.
+// x is clamped to [-87, 88] so 2^n stays a normal number.
+float or_exp(float x) {
+  const float kLog2e = 1.44269504088896341f;
+  const float kLn2Hi = 0.693145751953125f;        // 0x3F317200, 15 significant bits
+  const float kLn2Lo = 1.42860682030941723e-06f;  // ln2 - kLn2Hi
+  if (x < -87.0f) x = -87.0f;
+  if (x > 88.0f) x = 88.0f;
+  float t = x * kLog2e;
+  float n = std::nearbyint(t);  // round half to even (default rounding mode)
+  float r = std::fma(n, -kLn2Hi, x);
+  r = std::fma(n, -kLn2Lo, r);
+  // Taylor coefficients 1/j! for j = 7 .. 0.
+  float p = 1.0f / 5040.0f;
+  p = std::fma(p, r, 1.0f / 720.0f);
+  p = std::fma(p, r, 1.0f / 120.0f);
+  p = std::fma(p, r, 1.0f / 24.0f);
+  p = std::fma(p, r, 1.0f / 6.0f);
+  p = std::fma(p, r, 0.5f);
+  p = std::fma(p, r, 1.0f);
+  p = std::fma(p, r, 1.0f);
+  int ni = (int)n;
+  float scale = bits_to_float((uint32_t)(ni + 127) << 23);
+  return p * scale;
+}
+
+// Logistic sigmoid 1 / (1 + exp(-z)) with the exp above and IEEE division.
+float or_sigmoid(float z) {
+  float e = or_exp(-z);
+  float d = 1.0f + e;
+  return 1.0f / d;
+}
+
+// -------------------------------------------------------------- CANON-DOT
+// Router logits l[t][e] = sum_h x[t][h] * W[e][h] in fp32, in one fixed order:
+// H is cut into 8-element chunks; lane j (0..31) accumulates chunks
+// c = j, j+32, j+64, ... in ascending order, elements in order, with fma from
+// 0; then the 32 lane sums are combined by a butterfly: for d = 16, 8, 4, 2, 1
+// every lane adds the value of lane (j xor d).  The result is lane 0's value.
+// Requires H % 8 == 0.  Edge0 §2 "MoE routing" (logits feed both families).
+int or_router_logits(const uint16_t* x, const uint16_t* w, int T, int E, int H, float* logits) {
+  if (H % 8) return -1;
+  const int chunks = H / 8;
+  for (int t = 0; t < T; ++t) {
+    for (int e = 0; e < E; ++e) {
+      float lane[32];
+      for (int j = 0; j < 32; ++j) {
+        float acc = 0.0f;
+        for (int c = j; c < chunks; c += 32)
+          for (int i = 0; i < 8; ++i) {
+            int64_t h = (int64_t)c * 8 + i;
+            acc = std::fma(bf16_to_float(x[(int64_t)t * H + h]),
+                           bf16_to_float(w[(int64_t)e * H + h]), acc);
+          }
+        lane[j] = acc;
+      }
+      for (int d = 16; d >= 1; d /= 2) {
+        float nxt[32];
+        for (int j = 0; j < 32; ++j) nxt[j] = lane[j] + lane[j ^ d];
+        std::memcpy(lane, nxt, sizeof(lane));
+      }
+      logits[(int64_t)t * E + e] = lane[0];
+    }
+  }
+  return 0;
+}
+
+// ------------------------------------------------------------ routing
+// Softmax-top-k (Edge0 §2, Qwen family): softmax over the logits, keep the
+// top k, renormalise.  The full softmax denominator cancels in the
+// renormalisation, so the weights are w_i = e_i / S with
+// e_i = exp(l_i - l_max) over the selected experts and S their sum taken in
+// rank order.  Rank order: logit descending, lower expert index first on ties.
+int or_route_softmax_topk(const float* logits, int T, int E, int k, int32_t* ids, float* wts) {
+  if (k <= 0 || k > E) return -1;
+  std::vector<int> idx(E);
+  for (int t = 0; t < T; ++t) {
+    const float* l = logits + (int64_t)t * E;
+    for (int e = 0; e < E; ++e) idx[e] = e;
+    std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) {
+      if (l[a] != l[b]) return l[a] > l[b];
+      return a < b;
+    });
+    float top = l[idx[0]];
+    std::vector<float> ex(k);
+    float S = 0.0f;
+    for (int i = 0; i < k; ++i) {
+      ex[i] = or_exp(l[idx[i]] - top);
+      S = S + ex[i];
+    }
+    for (int i = 0; i < k; ++i) {
+      ids[(int64_t)t * k + i] = idx[i];
+      wts[(int64_t)t * k + i] = ex[i] / S;
+    }
+  }
+  return 0;
+}
+
+// Sigmoid-group (Edge0 §2, DeepSeek-V3 / Ling family): s = sigmoid(logit);
+// selection score sel = s + bias (bias steers selection only); each of the
+// n_groups contiguous expert groups is scored by the sum of its two largest
+// sel values; the topk_groups best groups are kept (lower group index first on
+// ties); inside them the k best sel are taken (lower expert index first on
+// ties); weights are the raw sigmoid values renormalised over the k, then
+// multiplied by `scale`:  w_i = (s_i / S) * scale, S summed in rank order.
+int or_route_sigmoid_group(const float* logits, const float* bias, int T, int E, int n_groups,
+                           int topk_groups, int k, float scale, int32_t* ids, float* wts) {
+  if (n_groups <= 0 || E % n_groups) return -1;
+  const int gsz = E / n_groups;
+  if (gsz < 2 || topk_groups <= 0 || topk_groups > n_groups) return -1;
+  if (k <= 0 || k > topk_groups * gsz) return -1;
+  std::vector<float> s(E), sel(E), gscore(n_groups);
+  std::vector<int> gidx(n_groups), cand;
+  for (int t = 0; t < T; ++t) {
+    const float* l = logits + (int64_t)t * E;
+    for (int e = 0; e < E; ++e) {
+      s[e] = or_sigmoid(l[e]);
+      sel[e] = s[e] + (bias ? bias[e] : 0.0f);
+    }
+    for (int g = 0; g < n_groups; ++g) {
+      std::vector<float> v(sel.begin() + g * gsz, sel.begin() + (g + 1) * gsz);
+      std::sort(v.begin(), v.end(), [](float a, float b) { return a > b; });
+      gscore[g] = v[0] + v[1];
+      gidx[g] = g;
+    }
+    std::stable_sort(gidx.begin(), gidx.end(), [&](int a, int b) {
+      if (gscore[a] != gscore[b]) return gscore[a] > gscore[b];
+      return a < b;
+    });
+    cand.clear();
+    for (int i = 0; i < topk_groups; ++i)
+      for (int e = gidx[i] * gsz; e < (gidx[i] + 1) * gsz; ++e) cand.push_back(e);
+    std::stable_sort(cand.begin(), cand.end(), [&](int a, int b) {
+      if (sel[a] != sel[b]) return sel[a] > sel[b];
+      return a < b;
+    });
+    float S = 0.0f;
+    for (int i = 0; i < k; ++i) S = S + s[cand[i]];
+    for (int i = 0; i < k; ++i) {
+      ids[(int64_t)t * k + i] = cand[i];
+      float r = s[cand[i]] / S;
+      wts[(int64_t)t * k + i] = r * scale;
+    }
+  }
+  return 0;
+}
+
+// ------------------------------------------------------------------ q*
+// FreeToken "core method": equating T_fill(q) = qS/B_P with
+// T_cpu(m-q) = (m-q)S/(B_H-B_P) gives q* ~= m*B_P/B_H; as B_H -> B_P the split
+// degenerates to pure fill, and with B_H < B_P (no residual host bandwidth)
+// it stays pure fill.  Integer form with bandwidths in MB/s and round half up:
+// q = floor((2*m*bp + bh) / (2*bh)), clamped to [0, m].
+int or_q_star(int m, int bp, int bh) {
+  if (m <= 0) return 0;
+  if (bh <= bp) return m;
+  int64_t num = 2 * (int64_t)m * bp + bh;
+  int64_t q = num / (2 * (int64_t)bh);
+  if (q < 0) q = 0;
+  if (q > m) q = m;
+  return (int)q;
+}
+
+// ------------------------------------------------------------ control step
+// One decode control step for one MoE layer (FreeToken "method steps",
+// "novelty"; reader "Semantic-Aware Expert Caching", "Elastic Memory
+// Management"):
+//   1. now = ++clock
+//   2. U = ascending unique {layer*E + id} over the n routed ids
+//   3. H = members of U with a slot; their slot gets ts = now (recency moves
+//      only when the router selects an expert)
+//   4. M = U \ H ascending, m = |M|, q from or_q_star
+//   5. victims = the K smallest keys (ts, slot) over slots with ts != now
+//      (empty slots have ts 0 and come first), one pass, ascending
+//   6. n_fill = min(q, K, #victims); F = M[0:n_fill]; C = M[n_fill:]
+//   7. for i < n_fill: slot v = victims[i] drops its old id and takes F[i]
+//      with ts = now.
+// counts = {n_uniq, n_hit, n_miss, q, n_fill, n_direct, n_victims, now}.
+// Returns 0, or -1 on an id outside [0, E).
+int or_cache_step(int E, int layer, const int32_t* ids, int n_ids, int S, int K, int bp, int bh,
+                  int32_t* slot_of_id, int32_t* id_of_slot, uint32_t* ts, uint32_t* clock,
+                  int32_t* uniq, int32_t* hit_ids, int32_t* hit_slots, int32_t* fill_ids,
+                  int32_t* fill_slots, int32_t* evicted_ids, int32_t* direct_ids, int32_t* victims,
+                  int32_t* counts) {
+  for (int i = 0; i < n_ids; ++i)
+    if (ids[i] < 0 || ids[i] >= E) return -1;
+  uint32_t now = *clock + 1;
+  *clock = now;
+
+  std::vector<int32_t> U;
+  for (int i = 0; i < n_ids; ++i) U.push_back(layer * E + ids[i]);
+  std::sort(U.begin(), U.end());
+  U.erase(std::unique(U.begin(), U.end()), U.end());
+
+  std::vector<int32_t> H, Hs, M;
+  for (int32_t u : U) {
+    int32_t s = slot_of_id[u];
+    if (s >= 0) {
+      H.push_back(u);
+      Hs.push_back(s);
+      ts[s] = now;
+    } else {
+      M.push_back(u);
+    }
+  }
+  int m = (int)M.size();
+  int q = or_q_star(m, bp, bh);
+
+  std::vector<std::pair<uint32_t, int32_t>> keys;
+  for (int32_t v = 0; v < S; ++v)
+    if (ts[v] != now) keys.push_back({ts[v], v});
+  std::sort(keys.begin(), keys.end());
+  int nv = std::min<int>(K, (int)keys.size());
+
+  int n_fill = std::min(q, nv);
+  for (int i = 0; i < K; ++i) victims[i] = (i < nv) ? keys[i].second : -1;
+
+  for (int i = 0; i < n_fill; ++i) {
+    int32_t v = keys[i].second;
+    int32_t old = id_of_slot[v];
+    if (old >= 0) slot_of_id[old] = -1;
+    id_of_slot[v] = M[i];
+    slot_of_id[M[i]] = v;
+    ts[v] = now;
+    fill_ids[i] = M[i];
+    fill_slots[i] = v;
+    evicted_ids[i] = old;
+  }
+  int n_direct = m - n_fill;
+  for (int i = 0; i < n_direct; ++i) direct_ids[i] = M[n_fill + i];
+  for (size_t i = 0; i < U.size(); ++i) uniq[i] = U[i];
+  for (size_t i = 0; i < H.size(); ++i) {
+    hit_ids[i] = H[i];
+    hit_slots[i] = Hs[i];
+  }
+  counts[0] = (int32_t)U.size();
+  counts[1] = (int32_t)H.size();
+  counts[2] = m;
+  counts[3] = q;
+  counts[4] = n_fill;
+  counts[5] = n_direct;
+  counts[6] = nv;
+  counts[7] = (int32_t)now;
+  return 0;
+}
+
+// -------------------------------------------------------------- expert FFN
+}  // extern "C"
+
+namespace {
+
+struct DenseExpert {
+  int H = 0, I = 0;
+  std::vector<float> wg, wu, wd;  // dequantised fp32 [I][H], [I][H], [H][I]
+};
+
+DenseExpert dense_of(const uint8_t* blob, int H, int I) {
+  DenseExpert d;
+  d.H = H;
+  d.I = I;
+  d.wg.resize((size_t)I * H);
+  d.wu.resize((size_t)I * H);
+  d.wd.resize((size_t)H * I);
+  or_blob_matrix(blob, H, I, 0, d.wg.data());
+  or_blob_matrix(blob, H, I, 1, d.wu.data());
+  or_blob_matrix(blob, H, I, 2, d.wd.data());
+  return d;
+}
+
+// g = Wg x, u = Wu x, h = silu(g) * u, y = Wd h in float64 for one token.
+void dense_forward(const DenseExpert& d, const uint16_t* x, double* y) {
+  const int H = d.H, I = d.I;
+  std::vector<double> xv(H), h(I);
+  for (int c = 0; c < H; ++c) xv[c] = bf16_to_float(x[c]);
+  for (int i = 0; i < I; ++i) {
+    double g = 0.0, u = 0.0;
+    for (int c = 0; c < H; ++c) {
+      g += (double)d.wg[(size_t)i * H + c] * xv[c];
+      u += (double)d.wu[(size_t)i * H + c] * xv[c];
+    }
+    double silu = g / (1.0 + std::exp(-g));
+    h[i] = silu * u;
+  }
+  for (int o = 0; o < H; ++o) {
+    double acc = 0.0;
+    for (int i = 0; i < I; ++i) acc += (double)d.wd[(size_t)o * I + i] * h[i];
+    y[o] = acc;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+// One expert on T tokens in float64 (Edge0 §3.1 "math convention"):
+//   g = Wg x, u = Wu x, h = silu(g) * u, y = Wd h, silu(z) = z / (1 + e^-z),
+// weights dequantised in fp32 (w = s*q + b) and widened, x widened from bf16.
+// x is [T][H] bf16 bits, y is [T][H].
+void or_expert_forward(const uint8_t* blob, int H, int I, const uint16_t* x, int T, double* y) {
+  DenseExpert d = dense_of(blob, H, I);
+  for (int t = 0; t < T; ++t) dense_forward(d, x + (int64_t)t * H, y + (int64_t)t * H);
+}
+
+// Whole-layer expert output (FreeToken "core method": the partial sums of the
+// cached set G and the direct set C merge exactly, so the layer output is the
+// plain routed sum):  y[t] = sum_j w[t][j] * expert_{ids[t][j]}(x[t])
+//                            + shared(x[t])   (shared expert weight 1),
+// the routed terms added in rank order j = 0..k-1, then the shared term.
+// blobs[e] points at expert e's blob for this layer; shared_blob may be null.
+// Each distinct expert is dequantised once and reused for all its tokens.
+void or_moe_ffn(const uint8_t* const* blobs, int E, int H, int I, const uint16_t* x, int T,
+                const int32_t* ids, const float* wts, int k, const uint8_t* shared_blob,
+                int shared_I, double* y) {
+  std::vector<DenseExpert> cache(E);
+  std::vector<char> have(E, 0);
+  DenseExpert shared;
+  if (shared_blob) shared = dense_of(shared_blob, H, shared_I);
+  std::vector<double> ye(H);
+  for (int t = 0; t < T; ++t) {
+    double* yt = y + (int64_t)t * H;
+    const uint16_t* xt = x + (int64_t)t * H;
+    for (int o = 0; o < H; ++o) yt[o] = 0.0;
+    for (int j = 0; j < k; ++j) {
+      int e = ids[(int64_t)t * k + j];
+      if (!have[e]) {
+        cache[e] = dense_of(blobs[e], H, I);
+        have[e] = 1;
+      }
+      dense_forward(cache[e], xt, ye.data());
+      double w = wts[(int64_t)t * k + j];
+      for (int o = 0; o < H; ++o) yt[o] += w * ye[o];
+    }
+    if (shared_blob) {
+      dense_forward(shared, xt, ye.data());
+      for (int o = 0; o < H; ++o) yt[o] += ye[o];
+    }
+  }
+}
+
+}  // extern "C"
