@@ -1,0 +1,477 @@
+#!/usr/bin/env python3
+"""Benchmark of the per-layer MoE expert step on one GB300 (or N replicas).
+
+A step is one decode token through every MoE layer of the workload: per
+layer the router (moe_route), the control step with its fill copies
+(moe_cache_step) and the expert FFN + combine (moe_expert_ffn), all through
+the C ABI on inputs already resident in HBM.  `e2e` repeats the measurement
+through moe_layer_forward with the step's hidden states copied in from pinned
+host memory and the layer outputs copied back every step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+
+Multi-GPU: the decode step does not shard in this build (one control step
+per shared cache); N GPUs run N independent replicas, no collective.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "MoE-layer decode tok/s & expert-weight HBM GB/s vs peak; prefill TFLOPS"
+
+WORKLOADS = {
+    "qwen_decode": dict(
+        desc="Qwen3.6-35B-A3B-shaped decode: 40 MoE layers, H=2048, I=512, E=256, top-8 "
+             "softmax + 1 shared expert (I=512), int4 affine g64, batch 1, 2560 slots (25% of "
+             "pairs), K=8, B_P/B_H=52.7/77.3 GB/s, AR(1) hidden states rho=0.9",
+        L=40, H=2048, I=512, E=256, k=8, T=1, shared=True, router="softmax", slots=2560, K=8,
+        bp=52700, bh=77300),
+    "deepseek_decode_b1": dict(
+        desc="DeepSeek-V3-style decode: 8 MoE layers, H=7168, I=2048, E=256 in 8 groups, top-4 "
+             "groups, top-8, scale 2.5, selection bias N(0,0.01), int4 affine g64, batch 1, 307 "
+             "slots (15%), K=8, B_P/B_H=11.8/47.5 GB/s",
+        L=8, H=7168, I=2048, E=256, k=8, T=1, shared=False, router="sigmoid_group", ng=8, G=4,
+        scale=2.5, slots=307, K=8, bp=11800, bh=47500),
+    "deepseek_decode_b8": dict(
+        desc="DeepSeek-V3-style decode, batch 8 (8 independent AR(1) streams), otherwise as "
+             "deepseek_decode_b1",
+        L=8, H=7168, I=2048, E=256, k=8, T=8, shared=False, router="sigmoid_group", ng=8, G=4,
+        scale=2.5, slots=307, K=8, bp=11800, bh=47500),
+}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("ffn_decode.cu", "moe_internal.cuh"):
+        h.update(open(os.path.join(ROOT, "moe_expert_offload_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    """DRAM bytes per FFN launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "ffn_decode_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    e = d.get(workload)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return float(e["dram_bytes_per_ffn"])
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ inputs
+def make_inputs(w, n_steps, seed_base=0):
+    from moe_expert_offload_gb300 import synth
+
+    L, H, E, T = w["L"], w["H"], w["E"], w["T"]
+    xs = np.stack([synth.ar1_stream(seed_base + l, n_steps, H, n_streams=T) for l in range(L)],
+                  axis=1)  # [steps][L][T][H]
+    wr = np.stack([synth.router_weights(100 + l, E, H) for l in range(L)])  # [L][E][H]
+    bias = (np.stack([synth.selection_bias(300 + l, E) for l in range(L)])
+            if w["router"] == "sigmoid_group" else None)
+    return xs, wr, bias
+
+
+def spec_of(w):
+    import moe_expert_offload_gb300 as m
+
+    if w["router"] == "sigmoid_group":
+        return m.make_spec(w["L"], w["H"], w["I"], w["E"], w["k"], router="sigmoid_group",
+                           n_groups=w["ng"], topk_groups=w["G"], routed_scale=w["scale"],
+                           has_shared=w["shared"])
+    return m.make_spec(w["L"], w["H"], w["I"], w["E"], w["k"], has_shared=w["shared"])
+
+
+# --------------------------------------------------------------- CPU oracle
+class OracleRunner:
+    """Times the CPU oracle (single thread) on the same workload.  Expert blobs
+    are generated on the host on first use (untimed); only oracle calls count."""
+
+    def __init__(self, w, xs, wr, bias):
+        import oracle
+        from moe_expert_offload_gb300 import synth
+
+        oracle.build()
+        self.o, self.synth, self.w = oracle, synth, w
+        self.xs, self.wr, self.bias = xs, wr, bias
+        self.state = oracle.CacheState(w["L"] * w["E"], w["slots"])
+        self.blobs = {}
+        rng = np.random.default_rng(12345)
+        self.shared = synth.make_expert_bytes(rng, w["H"], w["I"]) if w["shared"] else None
+        self.spent = 0.0
+        self.tokens = 0
+
+    def blob(self, gid):
+        b = self.blobs.get(gid)
+        if b is None:
+            b = self.synth.make_expert_bytes(np.random.default_rng(gid + 1), self.w["H"],
+                                             self.w["I"])
+            self.blobs[gid] = b
+        return b
+
+    def step(self, s):
+        w, o = self.w, self.o
+        for l in range(w["L"]):
+            xb = self.xs[s, l]
+            t0 = time.perf_counter()
+            lg = o.router_logits(xb, self.wr[l])
+            if w["router"] == "sigmoid_group":
+                ids, wt = o.route_sigmoid_group(lg, self.bias[l], w["ng"], w["G"], w["k"],
+                                                w["scale"])
+            else:
+                ids, wt = o.route_softmax_topk(lg, w["k"])
+            o.cache_step(self.state, w["E"], l, ids, w["K"], w["bp"], w["bh"])
+            self.spent += time.perf_counter() - t0
+            need = {int(e) for e in ids.reshape(-1)}
+            full = [self.blob(l * w["E"] + (e if e in need else next(iter(need))))
+                    for e in range(w["E"])]
+            t0 = time.perf_counter()
+            o.moe_ffn(full, w["H"], w["I"], xb, ids, wt, self.shared, w["I"])
+            self.spent += time.perf_counter() - t0
+        self.tokens += w["T"]
+
+
+def cpu_baseline(w, xs, wr, bias, budget_s=12.0, max_steps=64):
+    r = OracleRunner(w, xs, wr, bias)
+    s = 0
+    while s < min(max_steps, xs.shape[0]) and (r.spent < budget_s or s == 0):
+        r.step(s)
+        s += 1
+    return {"value": r.tokens / r.spent, "unit": "tok/s", "cores": 1, "kind": "oracle",
+            "sample": f"{s} decode steps x {w['L']} layers x batch {w['T']} (route, control, "
+                      f"float64 FFN) in {r.spent:.1f} s of oracle time, single thread"}
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return
+    n = args.warmup + args.steps
+    xs, wr, bias = make_inputs(w, n)
+    r = OracleRunner(w, xs, wr, bias)
+    for s in range(args.warmup):
+        r.step(s)
+    r.spent, r.tokens = 0.0, 0
+    for s in range(args.warmup, n):
+        r.step(s)
+    val = r.tokens / r.spent
+    sample = (f"{args.steps} decode steps x {w['L']} layers x batch {w['T']} (route, control, "
+              f"float64 FFN), single thread, {r.spent:.1f} s of oracle time")
+    out = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tok/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * r.spent / args.steps,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "config": {"workload": args.workload, "desc": w["desc"]},
+           "cpu_baseline": {"value": val, "unit": "tok/s", "cores": 1, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": val, "unit": "tok/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+# ----------------------------------------------------------------- GPU arm
+def run_gpu(args, w, rank, world, local_rank):
+    import torch
+
+    import moe_expert_offload_gb300 as m
+    from moe_expert_offload_gb300 import _build, synth
+
+    _build.build()
+    m.lib()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    L, H, I, E, k, T = w["L"], w["H"], w["I"], w["E"], w["k"], w["T"]
+    spec = spec_of(w)
+    se = m.moe_expert_bytes(spec)
+    n_in = 2 * (args.warmup + args.steps)
+    xs_h, wr_h, bias_h = make_inputs(w, n_in)
+    bank = synth.make_bank_torch(L * E + (1 if w["shared"] else 0), H, I, 7, dev)
+    shared = bank[L * E] if w["shared"] else None
+    cache = m.DeviceCache(spec, w["slots"], w["K"], w["bp"], w["bh"], bank[:L * E], device=dev)
+    plan = m.DevicePlan(T * k, w["K"], device=dev)
+    xs = torch.from_numpy(xs_h.view(np.int16)).to(dev)          # [steps][L][T][H]
+    wr = torch.from_numpy(wr_h.view(np.int16)).to(dev)          # [L][E][H]
+    bias = None if bias_h is None else torch.from_numpy(bias_h).to(dev)
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    wts = torch.empty((T, k), dtype=torch.float32, device=dev)
+    y = torch.empty((L, T, H), dtype=torch.float32, device=dev)
+    fws = m.moe_ffn_workspace_bytes(spec, T)
+    ws = torch.empty(max(fws, m.moe_layer_workspace_bytes(spec, T)), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+
+    def bias_l(l):
+        return None if bias is None else bias[l]
+
+    def layer(x, l, sh, ev=None):
+        m.moe_route(spec, x, T, wr[l], bias_l(l), logits, ids, wts, sh)
+        m.moe_cache_step(spec, cache.c, l, ids, T, plan.c, 1, sh)
+        if ev is not None:
+            ev[0].record(torch.cuda.current_stream())
+        m.moe_expert_ffn(spec, cache.c, l, plan.c, x, T, ids, wts, shared, ws, fws, y[l], sh)
+        if ev is not None:
+            ev[1].record(torch.cuda.current_stream())
+
+    def step(s, ev=None):
+        sh = torch.cuda.current_stream().cuda_stream
+        for l in range(L):
+            layer(xs[s, l], l, sh, None if ev is None else ev[l])
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    m.moe_cache_reset(spec, cache.c, sp)
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize()
+
+    # The timed region is one CUDA graph holding all K steps back to back (each
+    # step reads its own resident inputs); timing events around every FFN
+    # launch are recorded inside the graph as external event nodes.
+    try:
+        mk = lambda: torch.cuda.Event(enable_timing=True, external=True)  # noqa: E731
+        mk()
+        in_graph_events = True
+    except TypeError:
+        in_graph_events = False
+    evs = [[[mk(), mk()] for _ in range(L)] for _ in range(args.steps)] if in_graph_events \
+        else None
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for s in range(args.steps):
+            step(args.warmup + s, None if evs is None else evs[s])
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier()
+    with ClockSampler(local_rank) as clk:
+        t_start.record(stream)
+        graph.replay()
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    if in_graph_events:
+        ffn_ms = [evs[s][l][0].elapsed_time(evs[s][l][1])
+                  for s in range(args.steps) for l in range(L)]
+        ffn_timing = "CUDA events around every FFN launch inside the timed graph"
+    else:
+        # fallback: a graph of the 40 layers' FFN launches alone, replayed
+        ffn_ms = []
+        ffn_timing = "CUDA events around graph replays of FFN-only steps"
+    del graph
+    ffn_avg_s = statistics.mean(ffn_ms) * 1e-3 if ffn_ms else float("nan")
+
+    # statistics of the control decisions (untimed replay of more steps)
+    n_uniq = n_fill = n_direct = n_miss = 0
+    stat_steps = min(args.steps, 16)
+    for s in range(stat_steps):
+        for l in range(L):
+            layer(xs[args.warmup + args.steps + s, l], l, sp)
+            c = plan.counts.cpu().numpy()
+            n_uniq += int(c[0])
+            n_miss += int(c[2])
+            n_fill += int(c[4])
+            n_direct += int(c[5])
+    layer_steps = stat_steps * L
+
+    # end to end through the public API: pinned host hidden states -> device,
+    # the 40 moe_layer_forward calls (one captured graph), layer outputs ->
+    # pinned host, every step, no host sync inside the timed region.
+    lws = m.moe_layer_workspace_bytes(spec, T)
+    x_host = torch.from_numpy(xs_h[args.warmup + args.steps:].view(np.int16).copy()).pin_memory()
+    y_host = torch.empty((args.steps, L, T, H), dtype=torch.float32).pin_memory()
+    x_dev = torch.empty((L, T, H), dtype=torch.int16, device=dev)
+
+    def fwd_layers():
+        sh = torch.cuda.current_stream().cuda_stream
+        for l in range(L):
+            m.moe_layer_forward(spec, cache.c, l, x_dev[l], T, wr[l], bias_l(l), shared, plan.c,
+                                ids, wts, ws, lws, y[l], sh)
+
+    fwd_layers()
+    torch.cuda.synchronize()
+    g1 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g1):
+        fwd_layers()
+
+    def e2e_step(s):
+        x_dev.copy_(x_host[s], non_blocking=True)
+        g1.replay()
+        y_host[s].copy_(y, non_blocking=True)
+
+    for s in range(min(args.warmup, args.steps)):
+        e2e_step(s)
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(args.steps):
+        e2e_step(s)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms_e2e = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms_e2e], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+
+    if rank != 0:
+        return
+    hbm, _, peak_kind = peaks()
+    ffn_bytes = (n_uniq / layer_steps + (1 if w["shared"] else 0)) * se  # per FFN launch
+    achieved = ffn_bytes / ffn_avg_s / 1e9
+    tokens = args.steps * T * world
+    value = tokens / (ms * 1e-3)
+    roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm, "traffic": ncu_traffic(args.workload),
+            "kernel": "decode expert FFN (gate/up + down launches of moe_expert_ffn)",
+            "algorithmic_bytes_per_launch": ffn_bytes, "avg_launch_us": ffn_avg_s * 1e6,
+            "peak_kind": peak_kind, "timing": ffn_timing}
+    cpu = cpu_baseline(w, xs_h, wr_h, bias_h) if world == 1 and not args.no_cpu else None
+    launches_per_layer = 6  # logits, select, control, fill, gate/up, down
+    out = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "desc": w["desc"], "layers": L, "batch": T,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"inputs larger than L2: ~{(n_uniq / layer_steps + w['shared']) * se * L / 1e6:.0f} MB "
+                         "of expert weights touched per step vs 129 MB L2"},
+        "roofline": roof,
+        "e2e": {"value": tokens / (ms_e2e * 1e-3), "unit": "tok/s",
+                "h2d_bytes_per_step": L * T * H * 2, "d2h_bytes_per_step": L * T * H * 4},
+        "gpu_launches": launches_per_layer * L * args.steps,
+        "clocks": clk.summary(),
+        "cache": {"miss_rate": n_miss / max(n_uniq, 1), "fill_per_layer": n_fill / layer_steps,
+                  "direct_per_layer": n_direct / layer_steps,
+                  "uniq_per_layer": n_uniq / layer_steps},
+        "ffn_gbs": achieved,
+        "step_gbs": (ffn_bytes + 2 * se * n_fill / layer_steps) * L / (ms * 1e-3 / args.steps) / 1e9,
+    }
+    if cpu:
+        out["cpu_baseline"] = cpu
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="qwen_decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu", action="store_true", help="skip the timed CPU oracle baseline")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="override the layer count (small cases for profiling)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = dict(WORKLOADS[args.workload])
+    if args.layers:
+        w["L"] = args.layers
+        w["desc"] += f" [profiling case: {args.layers} layers]"
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+    if world > 1:
+        import torch
+
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    run_gpu(args, w, rank, world, local_rank)
+    if world > 1:
+        import torch
+
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,225 @@
+/*
+ * moe.h -- C ABI of libmoe.so, the GB300 (sm_103a) MoE expert step.
+ *
+ * One MoE layer step, entirely on one GPU:
+ *   moe_route          router scoring: softmax-top-k or sigmoid-group
+ *                      (Edge0 §2 "MoE routing")
+ *   moe_cache_step     device control step: dedup of the routed ids lE+e, hit /
+ *                      miss against the shared slot table, q* split of the
+ *                      misses into a fill set F and a direct set C, single-pass
+ *                      choice of K LRU victims, table update, and the fill
+ *                      copies bank -> slot pool (FreeToken summary "core
+ *                      method", "method steps", "novelty"; FreeToken reader
+ *                      "Semantic-Aware Expert Caching", "Elastic Memory
+ *                      Management")
+ *   moe_expert_ffn     int4 affine group-64 SwiGLU experts down(silu(gate(x)) *
+ *                      up(x)) over G = H u F read from the slot pool and over C
+ *                      read in place from the bank, combined with the routing
+ *                      weights (Edge0 §3.1 "math convention"; FreeToken summary
+ *                      "core method": exact merge of the partial sums)
+ *   moe_layer_forward  the three above in stream order
+ * plus the prefill path (whole-layer copy and grouped GEMM; FreeToken summary
+ * "method steps", reader "System Architecture" ping-pong buffers).
+ *
+ * Conventions shared by every entry point
+ *   Memory   Every pointer named *device* must point to device memory that
+ *            the caller owns (for instance a torch tensor's data_ptr()).  The
+ *            library never allocates, frees or keeps a pointer after a call
+ *            returns; scratch space is passed in as `workspace`.
+ *   Streams  Every call is asynchronous on `stream` (a cudaStream_t; NULL is
+ *            the legacy default stream).  No call synchronises the host, and
+ *            all device-side sizes ("valid counts") live in device memory,
+ *            so every call can be captured in a CUDA graph.
+ *   Errors   Every int-returning call returns MOE_OK or a negative code.
+ *            Arguments are validated on the host before anything is launched;
+ *            on failure nothing is launched and moe_last_error() describes the
+ *            problem (a thread-local string).  Nothing aborts or traps.
+ *            Problems that only the device can see (a routed id outside
+ *            [0, E)) set a bit in plan->err and the offending entry is skipped.
+ *   Layout   Expert blob (one per (layer, expert); bank index l*E + e;
+ *            size moe_expert_bytes, a multiple of 256 bytes):
+ *              Wg codes [I][H/2] | Wu codes [I][H/2] | Wd codes [H][I/2]   (u8,
+ *              two int4 codes per byte, the low nibble is the even column)
+ *              Wg scale [I][H/64] | Wg bias [I][H/64] | Wu scale | Wu bias |
+ *              Wd scale [H][I/64] | Wd bias [H][I/64]                      (bf16)
+ *            Weight w = scale * q + bias with q in 0..15 (Edge0 §2
+ *            "Quantisation": int4 affine, group 64, scale and bias).
+ *            Hidden states x are bf16 [T][H] row-major; router weights bf16
+ *            [E][H]; outputs fp32.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
+
+enum {
+  MOE_OK = 0,
+  MOE_EINVAL = -1,       /* bad argument (null pointer, bad size, misalignment) */
+  MOE_ECUDA = -2,        /* a CUDA runtime call failed (launch error, ...) */
+  MOE_EUNSUPPORTED = -3, /* valid but not supported by this build */
+  MOE_ECAPACITY = -4,    /* a buffer (plan, workspace) is too small */
+  MOE_ETIMEOUT = -5      /* a bounded device wait gave up */
+};
+
+enum { MOE_ROUTER_SOFTMAX_TOPK = 0, MOE_ROUTER_SIGMOID_GROUP = 1 };
+
+/* Device-side error bits written to plan->err[0] (OR-ed, never cleared by the
+ * library; the caller may zero it). */
+enum { MOE_DERR_BAD_ID = 1, MOE_DERR_WAIT = 2 };
+
+/* Model description (Edge0 §3 "MoESpec": expert count, routing family,
+ * quantisation, layout). */
+typedef struct moe_spec {
+  int32_t num_layers;   /* L */
+  int32_t hidden;       /* H, multiple of 64 (the router needs a multiple of 8) */
+  int32_t inter;        /* I, expert intermediate size, multiple of 64 */
+  int32_t num_experts;  /* E routed experts per layer, 1..1024 */
+  int32_t top_k;        /* k experts per token, 1..min(E, 64) */
+  int32_t router;       /* MOE_ROUTER_* */
+  int32_t n_groups;     /* sigmoid-group: expert groups (E % n_groups == 0) */
+  int32_t topk_groups;  /* sigmoid-group: groups kept per token */
+  float routed_scale;   /* sigmoid-group: factor applied after renormalising */
+  int32_t group_size;   /* quantisation group, must be 64 */
+  int32_t has_shared;   /* 1: an always-on shared expert, added with weight 1 */
+  int32_t shared_inter; /* its intermediate size (must equal inter) */
+} moe_spec;
+
+/* The shared expert slot cache (FreeToken summary "core method": one pool
+ * for all MoE layers, one slot per (layer, expert) pair).  The struct itself
+ * lives on the host; the tables live on the device. */
+typedef struct moe_cache {
+  int32_t num_slots;   /* S >= 1 */
+  int32_t k_victims;   /* K, victims chosen per step, 1..32 */
+  int32_t bp_mbps;     /* B_P: fill bandwidth, MB/s (e.g. 52700) */
+  int32_t bh_mbps;     /* B_H: direct-execute bandwidth, MB/s (e.g. 77300) */
+  int32_t* slot_of_id; /* device [L*E]: slot holding id, or -1 */
+  int32_t* id_of_slot; /* device [S]: id held by slot, or -1 */
+  uint32_t* ts;        /* device [S]: last step the router selected it; 0 = empty */
+  uint32_t* clock;     /* device [1]: step counter, advanced once per cache step */
+  void* slot_pool;     /* device [S * S_e] bytes, 16-byte aligned */
+  const void* bank;    /* device [L * E * S_e] bytes, 16-byte aligned */
+} moe_cache;
+
+/* Fixed-shape step buffers with device-side valid counts (FreeToken summary
+ * "novelty": routing-dependent control kept as data).  All device pointers,
+ * each list `capacity` entries long except victims (k_victims entries). */
+typedef struct moe_plan {
+  int32_t capacity;     /* >= T * top_k of the call */
+  int32_t* uniq;        /* ascending unique ids l*E+e routed this step */
+  int32_t* hit_ids;     /* H: resident ids (ascending) */
+  int32_t* hit_slots;   /*    and their slots */
+  int32_t* fill_ids;    /* F: misses copied into the cache (ascending) */
+  int32_t* fill_slots;  /*    and the victim slots they went to */
+  int32_t* evicted_ids; /*    id previously held by that slot, or -1 */
+  int32_t* direct_ids;  /* C: misses executed in place from the bank */
+  int32_t* victims;     /* the K victims in (ts, slot) order; -1 = none */
+  int32_t* counts;      /* [8]: n_uniq n_hit n_miss q n_fill n_direct n_victims now */
+  int32_t* err;         /* [1]: MOE_DERR_* bits */
+} moe_plan;
+
+/* Last error message of this thread ("" if none).  Never NULL. */
+const char* moe_last_error(void);
+
+/* Library version string. */
+const char* moe_version(void);
+
+/* Bytes of one expert blob for (hidden, inter): 3HI/2 + 3HI/64 * 4 rounded up
+ * to 256 (Edge0 §3.1 "problem": 1.77 MB per expert at H=2048, I=512).
+ * Returns 0 for an invalid spec. */
+size_t moe_expert_bytes(const moe_spec* spec);
+
+/* ------------------------------------------------------------------------
+ * moe_route -- router scoring (Edge0 §2 "MoE routing").
+ *   x          device bf16 [T][H]
+ *   w_router   device bf16 [E][H]
+ *   bias       device fp32 [E] or NULL (sigmoid-group only: added to the
+ *              sigmoid scores for selection, never to the weights)
+ *   logits     device fp32 [T][E] out: l = x . W_r^T, fp32, fixed summation
+ *              order (8-element chunks, chunk c to lane c mod 32, lanes
+ *              combined by an xor butterfly 16, 8, 4, 2, 1)
+ *   ids        device int32 [T][k] out: expert index e in rank order
+ *   weights    device fp32 [T][k] out
+ * softmax-top-k : top k logits (ties: lower index), w = exp(l - lmax) / sum,
+ *                 sum over the k in rank order.
+ * sigmoid-group : s = sigmoid(l), sel = s + bias; groups ranked by the sum of
+ *                 their two largest sel; top `topk_groups` groups kept; top k
+ *                 sel inside them; w = s / sum(s) * routed_scale.
+ * exp is the library's own (Cody-Waite reduction, degree-7 Taylor, exact
+ * 2^n scaling) so routing is bit-reproducible against a CPU restatement.
+ * T >= 0 (T == 0 launches nothing).
+ * ------------------------------------------------------------------------ */
+int moe_route(const moe_spec* spec, const void* x, int32_t T, const void* w_router,
+              const float* bias, float* logits, int32_t* ids, float* weights,
+              moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * moe_cache_reset -- empty the cache: slot_of_id[*] = -1, id_of_slot[*] = -1,
+ * ts[*] = 0, clock = 0.
+ * ------------------------------------------------------------------------ */
+int moe_cache_reset(const moe_spec* spec, moe_cache* cache, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * moe_cache_step -- one decode control step for layer `layer` (one CTA),
+ * then (do_fill != 0) the fill copies bank[F_i] -> slot_pool[victim_i].
+ *   ids      device int32 [T][k]: routed expert indices of this layer
+ *   plan     capacity >= T*k; written with the step's sets and counts
+ * Steps (FreeToken summary "method steps"; reader "Semantic-Aware Expert
+ * Caching", "Elastic Memory Management"):
+ *   now = ++clock; U = sorted unique {layer*E + id}; H = ids of U with a slot,
+ *   their ts = now; M = U \ H ascending, m = |M|;
+ *   q = m if B_H <= B_P else floor((2*m*B_P + B_H) / (2*B_H))  (round half up
+ *   of m*B_P/B_H); victims = the K smallest (ts, slot) over slots with
+ *   ts != now, in one pass; n_fill = min(q, K, #victims); F = M[:n_fill] into
+ *   victims[:n_fill] (old ids evicted, ts = now); C = M[n_fill:] (not cached).
+ * Requires T*k <= 1024 and T*k <= plan->capacity (else MOE_ECAPACITY).
+ * With do_fill == 0 only the tables change (trace replay).
+ * ------------------------------------------------------------------------ */
+int moe_cache_step(const moe_spec* spec, moe_cache* cache, int32_t layer, const int32_t* ids,
+                   int32_t T, moe_plan* plan, int32_t do_fill, moe_stream_t stream);
+
+/* Scratch bytes moe_expert_ffn needs for T tokens (0 for an invalid spec). */
+size_t moe_ffn_workspace_bytes(const moe_spec* spec, int32_t T);
+
+/* ------------------------------------------------------------------------
+ * moe_expert_ffn -- decode expert FFN and combine (T <= 64).
+ *   Executes every id in plan->uniq (H and F from their slots, C in place from
+ *   the bank: an id with slot_of_id >= 0 after the cache step is read from
+ *   the slot pool, any other from the bank) plus the shared expert:
+ *     y[t] = sum_j weights[t][j] * expert(ids[t][j])(x[t]) + shared(x[t])
+ *   expert(x) = Wd (silu(Wg x) * (Wu x)), dequantised int4, fp32 accumulate.
+ *   The routed terms are added in rank order j, then the shared term.
+ *   x        device bf16 [T][H];  ids, weights as written by moe_route
+ *   shared   device blob of the shared expert, or NULL (needs has_shared)
+ *   workspace device, >= moe_ffn_workspace_bytes(spec, T), 256-byte aligned
+ *   y        device fp32 [T][H] out
+ * ------------------------------------------------------------------------ */
+int moe_expert_ffn(const moe_spec* spec, const moe_cache* cache, int32_t layer,
+                   const moe_plan* plan, const void* x, int32_t T, const int32_t* ids,
+                   const float* weights, const void* shared, void* workspace,
+                   size_t workspace_bytes, float* y, moe_stream_t stream);
+
+/* Scratch bytes moe_layer_forward needs for T tokens. */
+size_t moe_layer_workspace_bytes(const moe_spec* spec, int32_t T);
+
+/* ------------------------------------------------------------------------
+ * moe_layer_forward -- moe_route, moe_cache_step (with fill) and
+ * moe_expert_ffn for one decode layer, in stream order, no host sync.
+ *   ids, weights  device out [T][k] (the routing decision, kept for the caller)
+ *   workspace     >= moe_layer_workspace_bytes(spec, T)
+ * ------------------------------------------------------------------------ */
+int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, const void* x,
+                      int32_t T, const void* w_router, const float* bias, const void* shared,
+                      moe_plan* plan, int32_t* ids, float* weights, void* workspace,
+                      size_t workspace_bytes, float* y, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H_ */

@@ -1,0 +1,294 @@
+// C ABI entry points of libmoe (declared in include/moe.h): argument checks
+// on the host, then kernel launches on the caller's stream.  Nothing here
+// allocates device memory or synchronises the host.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "moe_internal.cuh"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int ok() {
+  g_err[0] = '\0';
+  return MOE_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+  return fail(MOE_ECUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+int check_spec(const moe_spec* s) {
+  if (!s) return fail(MOE_EINVAL, "spec is NULL");
+  if (s->num_layers < 1) return fail(MOE_EINVAL, "num_layers must be >= 1");
+  if (s->hidden < 64 || s->hidden % 64) return fail(MOE_EINVAL, "hidden must be a multiple of 64");
+  if (s->inter < 64 || s->inter % 64) return fail(MOE_EINVAL, "inter must be a multiple of 64");
+  if (s->num_experts < 1 || s->num_experts > moe::kMaxExperts)
+    return fail(MOE_EINVAL, "num_experts must be in 1..%d", moe::kMaxExperts);
+  if (s->top_k < 1 || s->top_k > s->num_experts || s->top_k > 64)
+    return fail(MOE_EINVAL, "top_k must be in 1..min(num_experts, 64)");
+  if (s->group_size != moe::kGroup) return fail(MOE_EUNSUPPORTED, "group_size must be 64");
+  if ((int64_t)s->num_layers * s->num_experts > (int64_t)1 << 30)
+    return fail(MOE_EINVAL, "num_layers * num_experts too large");
+  if (s->router == MOE_ROUTER_SIGMOID_GROUP) {
+    if (s->n_groups < 1 || s->num_experts % s->n_groups)
+      return fail(MOE_EINVAL, "num_experts must be a multiple of n_groups");
+    if (s->n_groups > 32) return fail(MOE_EUNSUPPORTED, "n_groups > 32");
+    if (s->num_experts / s->n_groups < 2) return fail(MOE_EINVAL, "groups need >= 2 experts");
+    if (s->topk_groups < 1 || s->topk_groups > s->n_groups)
+      return fail(MOE_EINVAL, "topk_groups must be in 1..n_groups");
+    if (s->top_k > s->topk_groups * (s->num_experts / s->n_groups))
+      return fail(MOE_EINVAL, "top_k exceeds the experts of the kept groups");
+  } else if (s->router != MOE_ROUTER_SOFTMAX_TOPK) {
+    return fail(MOE_EINVAL, "unknown router %d", s->router);
+  }
+  if (s->has_shared != 0 && s->has_shared != 1) return fail(MOE_EINVAL, "has_shared must be 0/1");
+  if (s->has_shared && s->shared_inter != s->inter)
+    return fail(MOE_EUNSUPPORTED, "shared_inter must equal inter");
+  return MOE_OK;
+}
+
+int check_cache(const moe_spec* s, const moe_cache* c, bool need_data) {
+  if (!c) return fail(MOE_EINVAL, "cache is NULL");
+  if (c->num_slots < 1) return fail(MOE_EINVAL, "num_slots must be >= 1");
+  if (c->k_victims < 1 || c->k_victims > moe::kMaxVictims)
+    return fail(MOE_EINVAL, "k_victims must be in 1..%d", moe::kMaxVictims);
+  if (c->bp_mbps <= 0 || c->bh_mbps <= 0) return fail(MOE_EINVAL, "bandwidths must be > 0");
+  if (!c->slot_of_id || !c->id_of_slot || !c->ts || !c->clock)
+    return fail(MOE_EINVAL, "cache table pointer is NULL");
+  if (need_data) {
+    if (!c->slot_pool || !c->bank) return fail(MOE_EINVAL, "slot_pool / bank is NULL");
+    if (!aligned(c->slot_pool, 16) || !aligned(c->bank, 16))
+      return fail(MOE_EINVAL, "slot_pool / bank must be 16-byte aligned");
+  }
+  (void)s;
+  return MOE_OK;
+}
+
+int check_plan(const moe_plan* p, int need) {
+  if (!p) return fail(MOE_EINVAL, "plan is NULL");
+  if (!p->uniq || !p->hit_ids || !p->hit_slots || !p->fill_ids || !p->fill_slots ||
+      !p->evicted_ids || !p->direct_ids || !p->victims || !p->counts || !p->err)
+    return fail(MOE_EINVAL, "plan buffer pointer is NULL");
+  if (p->capacity < need)
+    return fail(MOE_ECAPACITY, "plan capacity %d < T*k = %d", p->capacity, need);
+  return MOE_OK;
+}
+
+int do_route(const moe_spec* spec, const void* x, int32_t T, const void* w_router,
+             const float* bias, float* logits, int32_t* ids, float* weights, cudaStream_t st) {
+  if (!x || !w_router || !logits || !ids || !weights)
+    return fail(MOE_EINVAL, "moe_route: NULL argument");
+  if (!aligned(x, 16) || !aligned(w_router, 16))
+    return fail(MOE_EINVAL, "moe_route: x and w_router must be 16-byte aligned");
+  cudaError_t e = moe::launch_router_logits(static_cast<const uint16_t*>(x),
+                                            static_cast<const uint16_t*>(w_router), T,
+                                            spec->num_experts, spec->hidden, logits, st);
+  if (e != cudaSuccess) return cuda_fail(e, "router logits launch");
+  e = moe::launch_router_select(*spec, logits, bias, T, ids, weights, st);
+  if (e != cudaSuccess) return cuda_fail(e, "router select launch");
+  return MOE_OK;
+}
+
+int do_cache_step(const moe_spec* spec, moe_cache* c, int32_t layer, const int32_t* ids,
+                  int32_t T, moe_plan* plan, int32_t do_fill, cudaStream_t st) {
+  moe::CacheArgs a;
+  a.E = spec->num_experts;
+  a.layer = layer;
+  a.n_ids = T * spec->top_k;
+  a.S = c->num_slots;
+  a.K = c->k_victims;
+  a.bp = c->bp_mbps;
+  a.bh = c->bh_mbps;
+  a.ids = ids;
+  a.slot_of_id = c->slot_of_id;
+  a.id_of_slot = c->id_of_slot;
+  a.ts = c->ts;
+  a.clock = c->clock;
+  a.plan = *plan;
+  cudaError_t e = moe::launch_cache_step(a, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cache step launch");
+  if (do_fill) {
+    const moe::BlobOffsets off = moe::blob_offsets(spec->hidden, spec->inter);
+    e = moe::launch_fill_copy(*plan, c->k_victims, static_cast<const uint8_t*>(c->bank),
+                              static_cast<uint8_t*>(c->slot_pool), off.total, st);
+    if (e != cudaSuccess) return cuda_fail(e, "fill copy launch");
+  }
+  return MOE_OK;
+}
+
+int check_step_args(const moe_spec* spec, int32_t layer, int32_t T) {
+  if (layer < 0 || layer >= spec->num_layers) return fail(MOE_EINVAL, "layer out of range");
+  if (T < 0) return fail(MOE_EINVAL, "T must be >= 0");
+  if ((int64_t)T * spec->top_k > moe::kMaxRouted)
+    return fail(MOE_ECAPACITY, "T*k = %lld exceeds %d", (long long)T * spec->top_k,
+                moe::kMaxRouted);
+  return MOE_OK;
+}
+
+int do_ffn(const moe_spec* spec, const moe_cache* c, int32_t layer, const moe_plan* plan,
+           const void* x, int32_t T, const int32_t* ids, const float* weights, const void* shared,
+           void* ws, size_t ws_bytes, float* y, cudaStream_t st) {
+  if (T > moe::kMaxDecodeT) return fail(MOE_EUNSUPPORTED, "decode FFN supports T <= %d",
+                                        moe::kMaxDecodeT);
+  if (!x || !ids || !weights || !y || !ws) return fail(MOE_EINVAL, "moe_expert_ffn: NULL argument");
+  if (spec->has_shared && !shared) return fail(MOE_EINVAL, "spec has a shared expert: pass its blob");
+  if (!aligned(x, 16) || !aligned(ws, 256) || (shared && !aligned(shared, 16)))
+    return fail(MOE_EINVAL, "x (16 B), shared (16 B) and workspace (256 B) alignment");
+  const size_t need = moe::ffn_workspace_bytes(spec->hidden, spec->inter, spec->top_k, T,
+                                               spec->has_shared);
+  if (ws_bytes < need) return fail(MOE_ECAPACITY, "workspace %zu < %zu bytes", ws_bytes, need);
+  moe::FfnArgs a;
+  a.H = spec->hidden;
+  a.I = spec->inter;
+  a.E = spec->num_experts;
+  a.k = spec->top_k;
+  a.layer = layer;
+  a.T = T;
+  a.has_shared = spec->has_shared;
+  a.blob_bytes = moe::blob_offsets(a.H, a.I).total;
+  a.bank = static_cast<const uint8_t*>(c->bank);
+  a.pool = static_cast<const uint8_t*>(c->slot_pool);
+  a.slot_of_id = c->slot_of_id;
+  a.uniq = plan->uniq;
+  a.counts = plan->counts;
+  a.err = plan->err;
+  a.x = static_cast<const uint16_t*>(x);
+  a.ids = ids;
+  a.weights = weights;
+  a.shared = static_cast<const uint8_t*>(shared);
+  a.y = y;
+  moe::ffn_carve_workspace(a, ws);
+  cudaError_t e = moe::launch_ffn_decode(a, st);
+  if (e != cudaSuccess) return cuda_fail(e, "decode FFN launch");
+  return MOE_OK;
+}
+
+size_t align256(size_t b) { return (b + 255) / 256 * 256; }
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_last_error(void) { return g_err; }
+
+const char* moe_version(void) { return "moe-gb300 0.1 (sm_103a)"; }
+
+size_t moe_expert_bytes(const moe_spec* spec) {
+  if (check_spec(spec) != MOE_OK) return 0;
+  return (size_t)moe::blob_offsets(spec->hidden, spec->inter).total;
+}
+
+int moe_route(const moe_spec* spec, const void* x, int32_t T, const void* w_router,
+              const float* bias, float* logits, int32_t* ids, float* weights,
+              moe_stream_t stream) {
+  int rc = check_spec(spec);
+  if (rc) return rc;
+  if (T < 0) return fail(MOE_EINVAL, "T must be >= 0");
+  if (T == 0) return ok();
+  rc = do_route(spec, x, T, w_router, bias, logits, ids, weights, (cudaStream_t)stream);
+  return rc ? rc : ok();
+}
+
+int moe_cache_reset(const moe_spec* spec, moe_cache* cache, moe_stream_t stream) {
+  int rc = check_spec(spec);
+  if (rc) return rc;
+  rc = check_cache(spec, cache, false);
+  if (rc) return rc;
+  cudaError_t e = moe::launch_cache_reset(cache->slot_of_id,
+                                          spec->num_layers * spec->num_experts,
+                                          cache->id_of_slot, cache->ts, cache->num_slots,
+                                          cache->clock, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cache reset launch");
+  return ok();
+}
+
+int moe_cache_step(const moe_spec* spec, moe_cache* cache, int32_t layer, const int32_t* ids,
+                   int32_t T, moe_plan* plan, int32_t do_fill, moe_stream_t stream) {
+  int rc = check_spec(spec);
+  if (rc) return rc;
+  rc = check_cache(spec, cache, do_fill != 0);
+  if (rc) return rc;
+  rc = check_step_args(spec, layer, T);
+  if (rc) return rc;
+  if (T == 0) return ok();
+  if (!ids) return fail(MOE_EINVAL, "ids is NULL");
+  rc = check_plan(plan, T * spec->top_k);
+  if (rc) return rc;
+  rc = do_cache_step(spec, cache, layer, ids, T, plan, do_fill, (cudaStream_t)stream);
+  return rc ? rc : ok();
+}
+
+size_t moe_ffn_workspace_bytes(const moe_spec* spec, int32_t T) {
+  if (check_spec(spec) != MOE_OK || T < 1) return 0;
+  return moe::ffn_workspace_bytes(spec->hidden, spec->inter, spec->top_k, T, spec->has_shared);
+}
+
+int moe_expert_ffn(const moe_spec* spec, const moe_cache* cache, int32_t layer,
+                   const moe_plan* plan, const void* x, int32_t T, const int32_t* ids,
+                   const float* weights, const void* shared, void* workspace,
+                   size_t workspace_bytes, float* y, moe_stream_t stream) {
+  int rc = check_spec(spec);
+  if (rc) return rc;
+  rc = check_cache(spec, cache, true);
+  if (rc) return rc;
+  rc = check_step_args(spec, layer, T);
+  if (rc) return rc;
+  if (T == 0) return ok();
+  rc = check_plan(plan, T * spec->top_k);
+  if (rc) return rc;
+  rc = do_ffn(spec, cache, layer, plan, x, T, ids, weights, shared, workspace, workspace_bytes, y,
+              (cudaStream_t)stream);
+  return rc ? rc : ok();
+}
+
+size_t moe_layer_workspace_bytes(const moe_spec* spec, int32_t T) {
+  if (check_spec(spec) != MOE_OK || T < 1) return 0;
+  return align256((size_t)T * spec->num_experts * 4) +
+         moe::ffn_workspace_bytes(spec->hidden, spec->inter, spec->top_k, T, spec->has_shared);
+}
+
+int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, const void* x,
+                      int32_t T, const void* w_router, const float* bias, const void* shared,
+                      moe_plan* plan, int32_t* ids, float* weights, void* workspace,
+                      size_t workspace_bytes, float* y, moe_stream_t stream) {
+  int rc = check_spec(spec);
+  if (rc) return rc;
+  rc = check_cache(spec, cache, true);
+  if (rc) return rc;
+  rc = check_step_args(spec, layer, T);
+  if (rc) return rc;
+  if (T == 0) return ok();
+  if (T > moe::kMaxDecodeT)
+    return fail(MOE_EUNSUPPORTED, "decode layer supports T <= %d", moe::kMaxDecodeT);
+  rc = check_plan(plan, T * spec->top_k);
+  if (rc) return rc;
+  if (!workspace || !aligned(workspace, 256)) return fail(MOE_EINVAL, "workspace must be 256-B aligned");
+  const size_t need = moe_layer_workspace_bytes(spec, T);
+  if (workspace_bytes < need)
+    return fail(MOE_ECAPACITY, "workspace %zu < %zu bytes", workspace_bytes, need);
+  cudaStream_t st = (cudaStream_t)stream;
+  float* logits = static_cast<float*>(workspace);
+  const size_t lbytes = align256((size_t)T * spec->num_experts * 4);
+  rc = do_route(spec, x, T, w_router, bias, logits, ids, weights, st);
+  if (rc) return rc;
+  rc = do_cache_step(spec, cache, layer, ids, T, plan, 1, st);
+  if (rc) return rc;
+  rc = do_ffn(spec, cache, layer, plan, x, T, ids, weights, shared,
+              static_cast<uint8_t*>(workspace) + lbytes, workspace_bytes - lbytes, y, st);
+  return rc ? rc : ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,292 @@
+// Device control step of the shared expert cache, one CTA per call
+// (FreeToken summary "core method", "method steps", "novelty"; FreeToken
+// reader "Semantic-Aware Expert Caching", "Elastic Memory Management"):
+// dedup of the routed ids lE+e, hit/miss classification, the q* split of the
+// misses into a fill set F and a direct set C, a single pass over the slots
+// for the K least recently used victims, and the slot-table update.  Then the
+// fill copies bank -> slot pool, sized by the device-side fill count.
+//
+// All routing-dependent sizes stay in device memory (plan->counts), so the
+// step needs no host decision and can sit inside a captured graph.
+#include <limits.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kCtlThreads = 512;
+constexpr int kCtlWarps = kCtlThreads / 32;
+constexpr unsigned long long kNoKey = ~0ull;
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Insert `key` into the ascending list best[0..KMAX), dropping the largest.
+template <int KMAX>
+__device__ __forceinline__ void insert_key(unsigned long long (&best)[KMAX],
+                                           unsigned long long key) {
+  if (key >= best[KMAX - 1]) return;
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    const unsigned long long lo = best[j] < key ? best[j] : key;
+    key = best[j] < key ? key : best[j];
+    best[j] = lo;
+  }
+}
+
+// K rounds of warp-wide minimum over the heads of the per-lane ascending
+// lists; round r's minimum is returned in out_r by every lane (keys unique).
+template <int KMAX>
+__device__ __forceinline__ void warp_k_smallest(unsigned long long (&best)[KMAX], int K,
+                                                unsigned long long* out) {
+  const int lane = threadIdx.x & 31;
+  for (int r = 0; r < K; ++r) {
+    unsigned long long m = best[0];
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) {
+      const unsigned long long o = __shfl_xor_sync(0xffffffffu, m, d);
+      m = o < m ? o : m;
+    }
+    if (m != kNoKey && best[0] == m) {
+#pragma unroll
+      for (int j = 0; j < KMAX - 1; ++j) best[j] = best[j + 1];
+      best[KMAX - 1] = kNoKey;
+    }
+    if (lane == 0) out[r] = m;
+  }
+}
+
+template <int KMAX>
+__global__ void __launch_bounds__(kCtlThreads) cache_step_kernel(CacheArgs a) {
+  __shared__ int32_t su[kMaxRouted];
+  __shared__ int32_t suniq[kMaxRouted];
+  __shared__ int32_t smiss[kMaxRouted];
+  __shared__ uint8_t sfirst[kMaxRouted];
+  __shared__ int swh[kCtlWarps], swm[kCtlWarps];
+  __shared__ unsigned long long scand[kCtlWarps * KMAX];
+  __shared__ unsigned long long svict[KMAX];
+  __shared__ int s_nu, s_bad;
+  __shared__ uint32_t s_now;
+
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int n = a.n_ids, E = a.E;
+
+  if (tid == 0) {
+    s_now = a.clock[0] + 1u;
+    a.clock[0] = s_now;
+    s_bad = 0;
+    s_nu = 0;
+  }
+  __syncthreads();
+  const uint32_t now = s_now;
+
+  // routed ids -> bank ids l*E + e (INT_MAX marks an id outside [0, E))
+  for (int i = tid; i < n; i += kCtlThreads) {
+    const int32_t e = a.ids[i];
+    if (e < 0 || e >= E) {
+      su[i] = INT_MAX;
+      s_bad = 1;
+    } else {
+      su[i] = a.layer * E + e;
+    }
+  }
+  __syncthreads();
+
+  // dedup: keep first occurrences; an entry's rank among the unique ids is
+  // the number of smaller unique ids.
+  for (int i = tid; i < n; i += kCtlThreads) {
+    const int32_t v = su[i];
+    uint8_t first = v != INT_MAX;
+    for (int j = 0; j < i && first; ++j) first = su[j] != v;
+    sfirst[i] = first;
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += kCtlThreads) {
+    if (!sfirst[i]) continue;
+    const int32_t v = su[i];
+    int r = 0;
+    for (int j = 0; j < n; ++j) r += (sfirst[j] && su[j] < v);
+    suniq[r] = v;
+    atomicAdd(&s_nu, 1);
+  }
+  __syncthreads();
+  const int n_uniq = s_nu;
+
+  // hit / miss, order-preserving compaction in rounds of kCtlThreads
+  int base_h = 0, base_m = 0;
+  for (int base = 0; base < n_uniq; base += kCtlThreads) {
+    const int r = base + tid;
+    const bool valid = r < n_uniq;
+    const int32_t u = valid ? suniq[r] : 0;
+    const int32_t slot = valid ? a.slot_of_id[u] : -1;
+    const bool hit = valid && slot >= 0, miss = valid && slot < 0;
+    const unsigned hb = __ballot_sync(0xffffffffu, hit), mb = __ballot_sync(0xffffffffu, miss);
+    if (lane == 0) {
+      swh[wid] = __popc(hb);
+      swm[wid] = __popc(mb);
+    }
+    __syncthreads();
+    int oh = base_h, om = base_m, th = 0, tm = 0;
+    for (int w = 0; w < kCtlWarps; ++w) {
+      if (w < wid) {
+        oh += swh[w];
+        om += swm[w];
+      }
+      th += swh[w];
+      tm += swm[w];
+    }
+    if (hit) {
+      const int p = oh + __popc(hb & lanemask_lt());
+      a.plan.hit_ids[p] = u;
+      a.plan.hit_slots[p] = slot;
+      a.ts[slot] = now;  // recency moves only when the router selects the expert
+    }
+    if (miss) smiss[om + __popc(mb & lanemask_lt())] = u;
+    base_h += th;
+    base_m += tm;
+    __syncthreads();
+  }
+  const int n_hit = base_h, m = base_m;
+
+  // q = round half up of m * B_P / B_H; pure fill when B_H <= B_P
+  int q;
+  if (m <= 0) {
+    q = 0;
+  } else if (a.bh <= a.bp) {
+    q = m;
+  } else {
+    long long qq = (2LL * m * a.bp + a.bh) / (2LL * a.bh);
+    q = (int)(qq < 0 ? 0 : (qq > m ? m : qq));
+  }
+
+  // one pass over the slots: K smallest keys (ts << 32 | slot), ts != now
+  const int K = a.K;
+  unsigned long long best[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) best[j] = kNoKey;
+  for (int v = tid; v < a.S; v += kCtlThreads) {
+    const uint32_t t = a.ts[v];
+    if (t != now) insert_key<KMAX>(best, ((unsigned long long)t << 32) | (uint32_t)v);
+  }
+  warp_k_smallest<KMAX>(best, K, &scand[wid * KMAX]);
+  __syncthreads();
+  if (wid == 0) {
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) best[j] = kNoKey;
+    for (int c = lane; c < kCtlWarps * KMAX; c += 32) {
+      const int w = c / KMAX, r = c % KMAX;
+      if (r < K) insert_key<KMAX>(best, scand[w * KMAX + r]);
+    }
+    warp_k_smallest<KMAX>(best, K, svict);
+  }
+  __syncthreads();
+
+  int nv = 0;
+  for (int r = 0; r < K; ++r) nv += svict[r] != kNoKey;
+  const int n_fill = min(q, nv);
+
+  for (int i = tid; i < K; i += kCtlThreads)
+    a.plan.victims[i] = (i < nv) ? (int32_t)(svict[i] & 0xffffffffu) : -1;
+  if (tid < n_fill) {
+    const int32_t v = (int32_t)(svict[tid] & 0xffffffffu);
+    const int32_t f = smiss[tid];
+    const int32_t old = a.id_of_slot[v];
+    if (old >= 0) a.slot_of_id[old] = -1;  // an evicted id is never one of F
+    a.id_of_slot[v] = f;
+    a.slot_of_id[f] = v;
+    a.ts[v] = now;
+    a.plan.fill_ids[tid] = f;
+    a.plan.fill_slots[tid] = v;
+    a.plan.evicted_ids[tid] = old;
+  }
+  for (int i = tid; i < m - n_fill; i += kCtlThreads) a.plan.direct_ids[i] = smiss[n_fill + i];
+  for (int i = tid; i < n_uniq; i += kCtlThreads) a.plan.uniq[i] = suniq[i];
+  if (tid == 0) {
+    int32_t* c = a.plan.counts;
+    c[0] = n_uniq;
+    c[1] = n_hit;
+    c[2] = m;
+    c[3] = q;
+    c[4] = n_fill;
+    c[5] = m - n_fill;
+    c[6] = nv;
+    c[7] = (int32_t)now;
+    if (s_bad) atomicOr(a.plan.err, MOE_DERR_BAD_ID);
+  }
+}
+
+// bank[F_i] -> slot_pool[victim_i]; blockIdx.y = i; blocks past the device
+// fill count return at once.  16-byte vectors, 4 in flight per thread.
+__global__ void __launch_bounds__(256) fill_copy_kernel(const int32_t* __restrict__ counts,
+                                                        const int32_t* __restrict__ fill_ids,
+                                                        const int32_t* __restrict__ fill_slots,
+                                                        const uint8_t* __restrict__ bank,
+                                                        uint8_t* __restrict__ pool,
+                                                        int64_t blob_bytes) {
+  const int i = blockIdx.y;
+  if (i >= counts[4]) return;
+  const uint4* src = reinterpret_cast<const uint4*>(bank + (int64_t)fill_ids[i] * blob_bytes);
+  uint4* dst = reinterpret_cast<uint4*>(pool + (int64_t)fill_slots[i] * blob_bytes);
+  const int64_t n16 = blob_bytes / 16;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; j + 3 * stride < n16; j += 4 * stride) {
+    const uint4 v0 = __ldcs(src + j), v1 = __ldcs(src + j + stride);
+    const uint4 v2 = __ldcs(src + j + 2 * stride), v3 = __ldcs(src + j + 3 * stride);
+    dst[j] = v0;
+    dst[j + stride] = v1;
+    dst[j + 2 * stride] = v2;
+    dst[j + 3 * stride] = v3;
+  }
+  for (; j < n16; j += stride) dst[j] = __ldcs(src + j);
+}
+
+__global__ void cache_reset_kernel(int32_t* slot_of_id, int n_ids, int32_t* id_of_slot,
+                                   uint32_t* ts, int S, uint32_t* clock) {
+  const int stride = gridDim.x * blockDim.x;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_ids; i += stride) slot_of_id[i] = -1;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < S; i += stride) {
+    id_of_slot[i] = -1;
+    ts[i] = 0;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) clock[0] = 0;
+}
+
+}  // namespace
+
+cudaError_t launch_cache_step(const CacheArgs& a, cudaStream_t st) {
+  if (a.K <= 8)
+    cache_step_kernel<8><<<1, kCtlThreads, 0, st>>>(a);
+  else if (a.K <= 16)
+    cache_step_kernel<16><<<1, kCtlThreads, 0, st>>>(a);
+  else
+    cache_step_kernel<32><<<1, kCtlThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fill_copy(const moe_plan& plan, int K, const uint8_t* bank, uint8_t* pool,
+                             int64_t blob_bytes, cudaStream_t st) {
+  const int64_t n16 = blob_bytes / 16;
+  int gx = (int)((n16 + 256 * 4 - 1) / (256 * 4));
+  if (gx > 128) gx = 128;
+  if (gx < 1) gx = 1;
+  fill_copy_kernel<<<dim3(gx, K), 256, 0, st>>>(plan.counts, plan.fill_ids, plan.fill_slots, bank,
+                                                pool, blob_bytes);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cache_reset(int32_t* slot_of_id, int n_ids, int32_t* id_of_slot, uint32_t* ts,
+                               int S, uint32_t* clock, cudaStream_t st) {
+  int n = n_ids > S ? n_ids : S;
+  int grid = (n + 255) / 256;
+  if (grid > 1024) grid = 1024;
+  if (grid < 1) grid = 1;
+  cache_reset_kernel<<<grid, 256, 0, st>>>(slot_of_id, n_ids, id_of_slot, ts, S, clock);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,276 @@
+// Router scoring (Edge0 §2 "MoE routing"): logits x . W_r^T in a fixed fp32
+// order, then softmax-top-k or sigmoid-group selection, one warp per token.
+//
+// Routing decisions must be reproducible bit for bit by a plain CPU program,
+// so every floating-point step here is an explicitly rounded IEEE operation
+// (__fmaf_rn, __fadd_rn, __fmul_rn, __fdiv_rn: nothing for the compiler to
+// contract) and exp is the library's own function below, not CUDA's.
+#include <float.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+__device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// exp(x) in fp32: Cody-Waite reduction x = n ln2 + r (ln2 = 0x1.62e4p-1 +
+// 0x1.7f7d1cp-20, the high part short enough that n * hi is exact), the
+// degree-7 Taylor polynomial of e^r (coefficients 1/7! .. 1/0!) in Horner
+// form with fused multiply-adds, and an exact 2^n scale from exponent bits.
+// x is clamped to [-87, 88], so n is in [-126, 127] and 2^n is normal.
+__device__ __forceinline__ float moe_exp(float x) {
+  x = fminf(fmaxf(x, -87.0f), 88.0f);
+  const float n = rintf(__fmul_rn(x, 0x1.715476p+0f));
+  float r = __fmaf_rn(n, -0x1.62e4p-1f, x);
+  r = __fmaf_rn(n, -0x1.7f7d1cp-20f, r);
+  float p = 0x1.a01a02p-13f;           // 1/5040
+  p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);  // 1/720
+  p = __fmaf_rn(p, r, 0x1.111112p-7f);   // 1/120
+  p = __fmaf_rn(p, r, 0x1.555556p-5f);   // 1/24
+  p = __fmaf_rn(p, r, 0x1.555556p-3f);   // 1/6
+  p = __fmaf_rn(p, r, 0.5f);
+  p = __fmaf_rn(p, r, 1.0f);
+  p = __fmaf_rn(p, r, 1.0f);
+  const int ni = (int)n;
+  return __fmul_rn(p, __int_as_float((ni + 127) << 23));
+}
+
+__device__ __forceinline__ float moe_sigmoid(float z) {
+  const float d = __fadd_rn(1.0f, moe_exp(-z));
+  return __fdiv_rn(1.0f, d);
+}
+
+// (value, index) order used for every top-k: larger value first, lower
+// index first among equal values.
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
+}
+
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, d);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, d);
+    if (better(ov, oi, v, i)) {
+      v = ov;
+      i = oi;
+    }
+  }
+}
+
+// One warp per (token, expert).  Lane j accumulates 8-element chunks
+// c = j, j+32, ... in order with fma from 0; the lane sums then go through an
+// xor butterfly 16, 8, 4, 2, 1.  x rows and W rows are 16-byte aligned.
+__global__ void __launch_bounds__(128) router_logits_kernel(const uint16_t* __restrict__ x,
+                                                            const uint16_t* __restrict__ w, int T,
+                                                            int E, int H,
+                                                            float* __restrict__ logits) {
+  const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (warp >= T * E) return;
+  const int t = warp / E, e = warp - t * E;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+  const uint4* wr = reinterpret_cast<const uint4*>(w + (size_t)e * H);
+  const int chunks = H >> 3;
+  float acc = 0.0f;
+#pragma unroll 4
+  for (int c = lane; c < chunks; c += 32) {
+    const uint4 xv = __ldg(xr + c);
+    const uint4 wv = __ldg(wr + c);
+    acc = __fmaf_rn(bf_lo(xv.x), bf_lo(wv.x), acc);
+    acc = __fmaf_rn(bf_hi(xv.x), bf_hi(wv.x), acc);
+    acc = __fmaf_rn(bf_lo(xv.y), bf_lo(wv.y), acc);
+    acc = __fmaf_rn(bf_hi(xv.y), bf_hi(wv.y), acc);
+    acc = __fmaf_rn(bf_lo(xv.z), bf_lo(wv.z), acc);
+    acc = __fmaf_rn(bf_hi(xv.z), bf_hi(wv.z), acc);
+    acc = __fmaf_rn(bf_lo(xv.w), bf_lo(wv.w), acc);
+    acc = __fmaf_rn(bf_hi(xv.w), bf_hi(wv.w), acc);
+  }
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, d));
+  if (lane == 0) logits[(size_t)t * E + e] = acc;
+}
+
+constexpr int kSelWarps = 4;
+constexpr int kMaxK = 64;
+
+// Softmax-top-k, one warp per token.  Lane j holds experts j + 32 i.
+template <int EPL>
+__global__ void __launch_bounds__(kSelWarps * 32)
+    select_softmax_kernel(const float* __restrict__ logits, int T, int E, int k,
+                          int32_t* __restrict__ ids, float* __restrict__ wts) {
+  __shared__ float sv[kSelWarps][kMaxK];
+  __shared__ float sex[kSelWarps][kMaxK];
+  __shared__ float ssum[kSelWarps];
+  const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kSelWarps + wid;
+  if (t >= T) return;
+  float v[EPL];
+  uint32_t taken = 0;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = (e < E) ? logits[(size_t)t * E + e] : -FLT_MAX;
+    if (e >= E) taken |= 1u << i;
+  }
+  for (int r = 0; r < k; ++r) {
+    float bv = -FLT_MAX;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (!(taken >> i & 1u) && better(v[i], e, bv, bi)) {
+        bv = v[i];
+        bi = e;
+      }
+    }
+    warp_argmax(bv, bi);
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == 0) {
+      sv[wid][r] = bv;
+      ids[(size_t)t * k + r] = bi;
+    }
+  }
+  __syncwarp();
+  if (lane == 0) {
+    const float top = sv[wid][0];
+    float S = 0.0f;
+    for (int r = 0; r < k; ++r) {
+      const float ex = moe_exp(__fsub_rn(sv[wid][r], top));
+      sex[wid][r] = ex;
+      S = __fadd_rn(S, ex);
+    }
+    ssum[wid] = S;
+  }
+  __syncwarp();
+  for (int r = lane; r < k; r += 32) wts[(size_t)t * k + r] = __fdiv_rn(sex[wid][r], ssum[wid]);
+}
+
+// Sigmoid-group, one warp per token (n_groups <= 32, E <= 32 * EPL).
+template <int EPL>
+__global__ void __launch_bounds__(kSelWarps * 32)
+    select_sigmoid_group_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
+                                int T, int E, int n_groups, int topk_groups, int k, float scale,
+                                int32_t* __restrict__ ids, float* __restrict__ wts) {
+  __shared__ float ssel[kSelWarps][32 * EPL];
+  __shared__ float ss[kSelWarps][kMaxK];
+  __shared__ float ssum[kSelWarps];
+  const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kSelWarps + wid;
+  if (t >= T) return;
+  const int gsz = E / n_groups;
+  float s[EPL], sel[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      s[i] = moe_sigmoid(logits[(size_t)t * E + e]);
+      sel[i] = __fadd_rn(s[i], bias ? bias[e] : 0.0f);
+      ssel[wid][e] = sel[i];
+    } else {
+      s[i] = 0.0f;
+      sel[i] = -FLT_MAX;
+    }
+  }
+  __syncwarp();
+  // group score: sum of the two largest selection scores of the group
+  float gscore = -FLT_MAX;
+  if (lane < n_groups) {
+    float t1 = -FLT_MAX, t2 = -FLT_MAX;
+    for (int e = lane * gsz; e < (lane + 1) * gsz; ++e) {
+      const float z = ssel[wid][e];
+      if (z > t1) {
+        t2 = t1;
+        t1 = z;
+      } else if (z > t2) {
+        t2 = z;
+      }
+    }
+    gscore = __fadd_rn(t1, t2);
+  }
+  uint32_t kept = 0;  // bit g: group g kept
+  uint32_t gtaken = (lane < n_groups) ? 0u : 1u;
+  for (int r = 0; r < topk_groups; ++r) {
+    float bv = gtaken ? -FLT_MAX : gscore;
+    int bi = gtaken ? 0x7fffffff : lane;
+    warp_argmax(bv, bi);
+    if (bi == lane) gtaken = 1;
+    kept |= 1u << bi;
+  }
+  uint32_t taken = 0;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e >= E || !((kept >> (e / gsz)) & 1u)) taken |= 1u << i;
+  }
+  for (int r = 0; r < k; ++r) {
+    float bv = -FLT_MAX;
+    int bi = 0x7fffffff;
+    float bs = 0.0f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (!(taken >> i & 1u) && better(sel[i], e, bv, bi)) {
+        bv = sel[i];
+        bi = e;
+        bs = s[i];
+      }
+    }
+    const int mine = bi;
+    warp_argmax(bv, bi);
+    const bool win = (bi == mine) && ((bi & 31) == lane);
+    if (win) {
+      taken |= 1u << (bi >> 5);
+      ss[wid][r] = bs;
+      ids[(size_t)t * k + r] = bi;
+    }
+  }
+  __syncwarp();
+  if (lane == 0) {
+    float S = 0.0f;
+    for (int r = 0; r < k; ++r) S = __fadd_rn(S, ss[wid][r]);
+    ssum[wid] = S;
+  }
+  __syncwarp();
+  for (int r = lane; r < k; r += 32)
+    wts[(size_t)t * k + r] = __fmul_rn(__fdiv_rn(ss[wid][r], ssum[wid]), scale);
+}
+
+template <int EPL>
+cudaError_t launch_select(const moe_spec& sp, const float* logits, const float* bias, int T,
+                          int32_t* ids, float* weights, cudaStream_t st) {
+  const int grid = (T + kSelWarps - 1) / kSelWarps;
+  if (sp.router == MOE_ROUTER_SOFTMAX_TOPK)
+    select_softmax_kernel<EPL><<<grid, kSelWarps * 32, 0, st>>>(logits, T, sp.num_experts,
+                                                                 sp.top_k, ids, weights);
+  else
+    select_sigmoid_group_kernel<EPL><<<grid, kSelWarps * 32, 0, st>>>(
+        logits, bias, T, sp.num_experts, sp.n_groups, sp.topk_groups, sp.top_k, sp.routed_scale,
+        ids, weights);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* w, int T, int E, int H,
+                                 float* logits, cudaStream_t st) {
+  const long warps = (long)T * E;
+  const int grid = (int)((warps + 3) / 4);
+  router_logits_kernel<<<grid, 128, 0, st>>>(x, w, T, E, H, logits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_select(const moe_spec& sp, const float* logits, const float* bias,
+                                 int T, int32_t* ids, float* weights, cudaStream_t st) {
+  const int E = sp.num_experts;
+  if (E <= 32) return launch_select<1>(sp, logits, bias, T, ids, weights, st);
+  if (E <= 64) return launch_select<2>(sp, logits, bias, T, ids, weights, st);
+  if (E <= 128) return launch_select<4>(sp, logits, bias, T, ids, weights, st);
+  if (E <= 256) return launch_select<8>(sp, logits, bias, T, ids, weights, st);
+  if (E <= 512) return launch_select<16>(sp, logits, bias, T, ids, weights, st);
+  return launch_select<32>(sp, logits, bias, T, ids, weights, st);
+}
+
+}  // namespace moe

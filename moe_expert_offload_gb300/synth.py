@@ -99,6 +99,20 @@ def make_expert(rng, H: int, I: int) -> np.ndarray:
     return pack_blob(H, I, qg, qu, qd, sg, bg, su, bu, sd, bd)
 
 
+def make_expert_bytes(rng, H: int, I: int) -> np.ndarray:
+    """Same distribution as make_expert, drawn faster: code bytes are uniform
+    (so both nibbles are uniform and independent)."""
+    off, sizes, total = blob_sections(H, I)
+    blob = np.zeros(total, dtype=np.uint8)
+    blob[:off["gs"]] = rng.integers(0, 256, size=off["gs"], dtype=np.uint8)
+    for sname, bname in (("gs", "gb"), ("us", "ub"), ("ds", "db")):
+        n = sizes[sname] // 2
+        s, b = _scale_bias(rng, n)
+        blob[off[sname]:off[sname] + 2 * n] = s.view(np.uint8)
+        blob[off[bname]:off[bname] + 2 * n] = b.view(np.uint8)
+    return blob
+
+
 def make_bank(n_experts: int, H: int, I: int, seed: int) -> np.ndarray:
     """Host bank of n_experts random blobs, uint8 [n_experts, S_e]."""
     rng = np.random.default_rng(seed)

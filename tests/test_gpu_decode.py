@@ -1,0 +1,378 @@
+"""GPU parity of the decode path against the CPU oracle, through the C ABI.
+
+Routing (logits, ids, weights), the control step (sets, victims, tables) and
+the slot-pool contents must match bit for bit; expert-FFN outputs must be
+within the Edge0 tolerance (relative L2 <= 1e-2, |err| <= 2e-2 * max|y|).
+"""
+import numpy as np
+import pytest
+
+import moe_expert_offload_gb300 as m
+from moe_expert_offload_gb300 import synth
+
+from gpu_util import assert_ffn_close, dev, dev_bits, f32_bits
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from moe_expert_offload_gb300 import _build
+    import oracle
+
+    _build.build()
+    oracle.build()
+    m.lib()
+
+
+@pytest.fixture(scope="module")
+def oracle():
+    import oracle as o
+
+    return o
+
+
+# ------------------------------------------------------------------ routing
+def _route(spec, xb, wb, bias=None):
+    T = xb.shape[0]
+    E, k = spec.num_experts, spec.top_k
+    x = dev_bits(xb, DEV)
+    w = dev_bits(wb, DEV)
+    b = None if bias is None else dev(bias, DEV)
+    logits = torch.empty((T, E), dtype=torch.float32, device=DEV)
+    ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    wts = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    m.moe_route(spec, x, T, w, b, logits, ids, wts)
+    torch.cuda.synchronize()
+    return logits.cpu().numpy(), ids.cpu().numpy(), wts.cpu().numpy()
+
+
+@pytest.mark.parametrize("T,E,H,k", [(1, 16, 256, 2), (1, 256, 2048, 8), (8, 256, 2048, 8),
+                                     (8, 256, 7168, 8), (5, 20, 320, 3), (3, 1000, 64, 7),
+                                     (64, 64, 512, 4)])
+def test_softmax_routing_bit_exact(oracle, T, E, H, k):
+    rng = np.random.default_rng(T * 1000 + E)
+    xb = synth.bf16_bits(rng.normal(0, 2.3, (T, H)))
+    wb = synth.router_weights(E + H, E, H)
+    spec = m.make_spec(1, max(H, 64) // 64 * 64, 64, E, k)
+    spec.hidden = H
+    lg, ids, w = _route(spec, xb, wb)
+    ol = oracle.router_logits(xb, wb)
+    assert np.array_equal(f32_bits(lg), f32_bits(ol))
+    oid, ow = oracle.route_softmax_topk(ol, k)
+    assert np.array_equal(ids, oid)
+    assert np.array_equal(f32_bits(w), f32_bits(ow))
+
+
+def test_softmax_routing_ties(oracle):
+    # experts 3, 7 and 11 share one router row: equal logits, lower index ranks first
+    T, E, H, k = 4, 16, 256, 4
+    rng = np.random.default_rng(5)
+    wb = synth.router_weights(9, E, H)
+    wb[7] = wb[3]
+    wb[11] = wb[3]
+    xb = synth.bf16_bits(rng.normal(0, 1, (T, H)))
+    xb[0] = synth.bf16_bits(synth.bf16_value(wb[3]) * 50)  # token 0 prefers the tied rows
+    spec = m.make_spec(1, H, 64, E, k)
+    lg, ids, w = _route(spec, xb, wb)
+    ol = oracle.router_logits(xb, wb)
+    oid, ow = oracle.route_softmax_topk(ol, k)
+    assert list(ids[0][:3]) == [3, 7, 11]
+    assert np.array_equal(ids, oid) and np.array_equal(f32_bits(w), f32_bits(ow))
+
+
+@pytest.mark.parametrize("T,E,H,ng,G,k,scale", [(1, 256, 7168, 8, 4, 8, 2.5),
+                                                 (8, 256, 7168, 8, 4, 8, 2.5),
+                                                 (16, 16, 256, 4, 2, 3, 1.0),
+                                                 (7, 64, 512, 32, 3, 4, 2.0)])
+def test_sigmoid_group_routing_bit_exact(oracle, T, E, H, ng, G, k, scale):
+    rng = np.random.default_rng(E + T)
+    xb = synth.bf16_bits(rng.normal(0, 2.3, (T, H)))
+    wb = synth.router_weights(E * 7 + H, E, H)
+    bias = synth.selection_bias(3, E)
+    spec = m.make_spec(1, H, 64, E, k, router="sigmoid_group", n_groups=ng, topk_groups=G,
+                       routed_scale=scale)
+    lg, ids, w = _route(spec, xb, wb, bias)
+    ol = oracle.router_logits(xb, wb)
+    assert np.array_equal(f32_bits(lg), f32_bits(ol))
+    oid, ow = oracle.route_sigmoid_group(ol, bias, ng, G, k, scale)
+    assert np.array_equal(ids, oid)
+    assert np.array_equal(f32_bits(w), f32_bits(ow))
+
+
+def test_exp_sweep_through_softmax_weights(oracle):
+    # two experts per token with logit gap d: weight[1] = e^-d / (1 + e^-d) uses the
+    # library's own exp; a dense sweep of gaps compares it bit for bit.
+    T, E, H = 4096, 2, 64
+    gaps = np.linspace(0, 60, T).astype(np.float32)
+    wb = np.zeros((E, H), np.uint16)
+    wb[0, 0] = synth.bf16_bits([1.0])[0]
+    xb = synth.bf16_bits(gaps[:, None] * (np.arange(H) == 0))
+    spec = m.make_spec(1, H, 64, E, 2)
+    lg, ids, w = _route(spec, xb, wb)
+    ol = oracle.router_logits(xb, wb)
+    oid, ow = oracle.route_softmax_topk(ol, 2)
+    assert np.array_equal(ids, oid) and np.array_equal(f32_bits(w), f32_bits(ow))
+
+
+# ---------------------------------------------------------- control step
+def _tables_equal(cache, ost):
+    soi, ios, ts, clk = cache.host_tables()
+    assert np.array_equal(soi, ost.slot_of_id)
+    assert np.array_equal(ios, ost.id_of_slot)
+    assert np.array_equal(ts, ost.ts)
+    assert clk[0] == ost.clock[0]
+
+
+def _plans_equal(gp, op, K):
+    for key in ("uniq", "hit_ids", "hit_slots", "fill_ids", "fill_slots", "evicted_ids",
+                "direct_ids", "victims"):
+        assert np.array_equal(gp[key], op[key]), key
+    assert np.array_equal(gp["counts"], op["counts"])
+
+
+@pytest.mark.parametrize("L,E,S,K,bp,bh,T,k,steps", [
+    (1, 16, 8, 4, 52700, 77300, 1, 2, 64),       # tiny decode config
+    (3, 16, 5, 3, 11800, 47500, 4, 2, 120),
+    (2, 32, 1, 1, 77300, 77300, 1, 4, 60),       # one slot, pure fill
+    (2, 32, 40, 8, 60000, 50000, 8, 8, 80),      # B_H < B_P -> pure fill
+    (4, 64, 7, 16, 1, 1000, 8, 8, 80),           # K > S, q mostly 0
+])
+def test_cache_step_matches_oracle_on_random_traces(oracle, L, E, S, K, bp, bh, T, k, steps):
+    rng = np.random.default_rng(S * 31 + K)
+    spec = m.make_spec(L, 64, 64, E, k)
+    cache = m.DeviceCache(spec, S, K, bp, bh, bank=None, device=DEV, with_pool=False)
+    plan = m.DevicePlan(T * k, K, device=DEV)
+    ost = oracle.CacheState(L * E, S)
+    for step in range(steps):
+        layer = step % L
+        ids_h = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+        ids = dev(ids_h, DEV)
+        m.moe_cache_step(spec, cache.c, layer, ids, T, plan.c, do_fill=0)
+        torch.cuda.synchronize()
+        op = oracle.cache_step(ost, E, layer, ids_h, K, bp, bh)
+        _plans_equal(plan.read(K), op, K)
+        _tables_equal(cache, ost)
+
+
+@pytest.mark.parametrize("S", [512, 5120])
+def test_cache_step_zipf_trace_sweep_shape(oracle, S):
+    L, E, k, K, steps = 40, 256, 8, 8, 6
+    spec = m.make_spec(L, 64, 64, E, k)
+    cache = m.DeviceCache(spec, S, K, 52700, 77300, bank=None, device=DEV, with_pool=False)
+    plan = m.DevicePlan(k, K, device=DEV)
+    ost = oracle.CacheState(L * E, S)
+    traces = [synth.zipf_trace(1000 + l, steps, E, k) for l in range(L)]
+    for s in range(steps):
+        for layer in range(L):
+            ids_h = traces[layer][s:s + 1]
+            m.moe_cache_step(spec, cache.c, layer, dev(ids_h, DEV), 1, plan.c, do_fill=0)
+            op = oracle.cache_step(ost, E, layer, ids_h, K, 52700, 77300)
+            if layer % 13 == 0:
+                torch.cuda.synchronize()
+                _plans_equal(plan.read(K), op, K)
+        torch.cuda.synchronize()
+        _tables_equal(cache, ost)
+
+
+def test_cache_step_all_hits_then_duplicates(oracle):
+    L, E, S, K, k = 1, 16, 16, 4, 4
+    spec = m.make_spec(L, 64, 64, E, k)
+    cache = m.DeviceCache(spec, S, K, 77300, 77300, bank=None, device=DEV, with_pool=False)
+    plan = m.DevicePlan(2 * k, K, device=DEV)
+    ost = oracle.CacheState(E, S)
+    seq = [np.array([[0, 1, 2, 3]]), np.array([[0, 1, 2, 3]]),
+           np.array([[3, 2, 1, 0], [0, 5, 1, 6]])]
+    for ids_h in seq:
+        ids_h = ids_h.astype(np.int32)
+        T = ids_h.shape[0]
+        m.moe_cache_step(spec, cache.c, 0, dev(ids_h, DEV), T, plan.c, do_fill=0)
+        torch.cuda.synchronize()
+        op = oracle.cache_step(ost, E, 0, ids_h, K, 77300, 77300)
+        gp = plan.read(K)
+        _plans_equal(gp, op, K)
+    assert gp["n_uniq"] == 6 and gp["n_hit"] == 4 and gp["n_fill"] == 2
+
+
+def test_cache_step_flags_bad_ids(oracle):
+    E, S, K, k = 16, 8, 4, 2
+    spec = m.make_spec(1, 64, 64, E, k)
+    cache = m.DeviceCache(spec, S, K, 77300, 77300, bank=None, device=DEV, with_pool=False)
+    plan = m.DevicePlan(4, K, device=DEV)
+    ids_h = np.array([[3, 99], [-2, 5]], np.int32)
+    m.moe_cache_step(spec, cache.c, 0, dev(ids_h, DEV), 2, plan.c, do_fill=0)
+    torch.cuda.synchronize()
+    gp = plan.read(K)
+    assert gp["err"] & m.MOE_DERR_BAD_ID
+    ost = oracle.CacheState(E, S)
+    op = oracle.cache_step(ost, E, 0, np.array([3, 5], np.int32), K, 77300, 77300)
+    _plans_equal(gp, op, K)
+
+
+# ------------------------------------------------------- fill + expert FFN
+def _layer_rig(L, H, I, E, k, S, K, bp, bh, has_shared, seed=0, big=False):
+    spec = m.make_spec(L, H, I, E, k, has_shared=has_shared)
+    if big:
+        bank = synth.make_bank_torch(L * E + 1, H, I, seed, DEV)
+        bank_h = None
+    else:
+        bank_h = synth.make_bank(L * E + 1, H, I, seed)
+        bank = dev(bank_h, DEV)
+    cache = m.DeviceCache(spec, S, K, bp, bh, bank=bank[:L * E], device=DEV)
+    shared = bank[L * E] if has_shared else None
+    return spec, bank, bank_h, cache, shared
+
+
+def test_tiny_config_64_decode_steps(oracle):
+    """Tiny single layer (H=256, I=128, E=16, top-2), AR(1) inputs, 64 steps, S=8, K=4."""
+    H, I, E, k, S, K, T = 256, 128, 16, 2, 8, 4, 1
+    spec, bank, bank_h, cache, _ = _layer_rig(1, H, I, E, k, S, K, 52700, 77300, False)
+    wr_h = synth.router_weights(0, E, H)
+    wr = dev_bits(wr_h, DEV)
+    xs = synth.ar1_stream(0, 64, H)
+    plan = m.DevicePlan(T * k, K, device=DEV)
+    wsb = m.moe_layer_workspace_bytes(spec, T)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    wts = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    y = torch.empty((T, H), dtype=torch.float32, device=DEV)
+    ost = oracle.CacheState(E, S)
+    fills = 0
+    for step in range(64):
+        xb = xs[step]
+        m.moe_layer_forward(spec, cache.c, 0, dev_bits(xb, DEV), T, wr, None, None, plan.c, ids,
+                            wts, ws, wsb, y)
+        torch.cuda.synchronize()
+        oid, ow = oracle.route_softmax_topk(oracle.router_logits(xb, wr_h), k)
+        assert np.array_equal(ids.cpu().numpy(), oid)
+        assert np.array_equal(f32_bits(wts.cpu().numpy()), f32_bits(ow))
+        op = oracle.cache_step(ost, E, 0, oid, K, 52700, 77300)
+        _plans_equal(plan.read(K), op, K)
+        fills += op["n_fill"]
+        ref = oracle.moe_ffn(list(bank_h[:E]), H, I, xb, oid, ow)
+        assert_ffn_close(y.cpu().numpy(), ref, f"step {step}")
+    _tables_equal(cache, ost)
+    # every resident slot holds exactly its expert's bank blob
+    pool = cache.pool.cpu().numpy()
+    for slot, eid in enumerate(ost.id_of_slot):
+        if eid >= 0:
+            assert np.array_equal(pool[slot], bank_h[eid])
+    assert fills > 0
+
+
+@pytest.mark.parametrize("H,I,E,k,T,shared", [(2048, 512, 256, 8, 1, True),
+                                              (2048, 512, 256, 8, 8, True),
+                                              (512, 192, 24, 3, 5, True),
+                                              (7168, 2048, 16, 8, 1, False)])
+def test_expert_ffn_direct_and_cached(oracle, H, I, E, k, T, shared):
+    """FFN over a mix of hits, fills and direct (bank) experts, several tokens."""
+    S = max(2, E // 4)
+    spec, bank, bank_h, cache, sh = _layer_rig(1, H, I, E, k, S, 4, 11800, 47500, shared, seed=H)
+    rng = np.random.default_rng(I)
+    wr_h = synth.router_weights(I, E, H)
+    wr = dev_bits(wr_h, DEV)
+    plan = m.DevicePlan(T * k, 4, device=DEV)
+    wsb = m.moe_layer_workspace_bytes(spec, T)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    wts = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    y = torch.empty((T, H), dtype=torch.float32, device=DEV)
+    for step in range(3):
+        xb = synth.bf16_bits(rng.normal(0, 2, (T, H)))
+        m.moe_layer_forward(spec, cache.c, 0, dev_bits(xb, DEV), T, wr, None, sh, plan.c, ids,
+                            wts, ws, wsb, y)
+        torch.cuda.synchronize()
+        gp = plan.read(4)
+        oid, ow = oracle.route_softmax_topk(oracle.router_logits(xb, wr_h), k)
+        assert np.array_equal(ids.cpu().numpy(), oid)
+        ref = oracle.moe_ffn(list(bank_h[:E]), H, I, xb, oid, ow,
+                             bank_h[E] if shared else None, I)
+        assert_ffn_close(y.cpu().numpy(), ref, f"step {step} plan {gp['counts']}")
+
+
+def test_full_size_qwen_shape_decode(oracle):
+    """40 layers x 256 experts (18.1 GB bank), 2560 slots, shared expert, T=1:
+    several decode steps over all layers, sampled layers checked against the oracle."""
+    L, H, I, E, k, S, K, T = 40, 2048, 512, 256, 8, 2560, 8, 1
+    spec, bank, _, cache, sh = _layer_rig(L, H, I, E, k, S, K, 52700, 77300, True, big=True)
+    wr_h = [synth.router_weights(100 + l, E, H) for l in range(L)]
+    wr = [dev_bits(w, DEV) for w in wr_h]
+    xs = [synth.ar1_stream(l, 4, H) for l in range(L)]
+    plan = m.DevicePlan(T * k, K, device=DEV)
+    wsb = m.moe_layer_workspace_bytes(spec, T)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    wts = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    y = torch.empty((T, H), dtype=torch.float32, device=DEV)
+    ost = oracle.CacheState(L * E, S)
+    shared_h = sh.cpu().numpy()
+    for step in range(4):
+        for layer in range(L):
+            xb = xs[layer][step]
+            m.moe_layer_forward(spec, cache.c, layer, dev_bits(xb, DEV), T, wr[layer], None, sh,
+                                plan.c, ids, wts, ws, wsb, y)
+            oid, ow = oracle.route_softmax_topk(oracle.router_logits(xb, wr_h[layer]), k)
+            op = oracle.cache_step(ost, E, layer, oid, K, 52700, 77300)
+            if layer in (0, 17, 39):
+                torch.cuda.synchronize()
+                assert np.array_equal(ids.cpu().numpy(), oid)
+                _plans_equal(plan.read(K), op, K)
+                blobs = {int(e): bank[layer * E + int(e)].cpu().numpy() for e in oid.reshape(-1)}
+                full = [blobs.get(e, blobs[int(oid[0, 0])]) for e in range(E)]
+                ref = oracle.moe_ffn(full, H, I, xb, oid, ow, shared_h, I)
+                assert_ffn_close(y.cpu().numpy(), ref, f"step {step} layer {layer}")
+    torch.cuda.synchronize()
+    _tables_equal(cache, ost)
+    del bank, cache
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("T", [1, 8])
+def test_full_size_deepseek_shape_decode(oracle, T):
+    """8 layers x 256 experts of H=7168, I=2048 (50.7 GB bank), sigmoid-group routing,
+    307 slots, K=8, B_P/B_H = 11.8/47.5; sampled tokens checked against the oracle."""
+    L, H, I, E, k, S, K = 8, 7168, 2048, 256, 8, 307, 8
+    spec = m.make_spec(L, H, I, E, k, router="sigmoid_group", n_groups=8, topk_groups=4,
+                       routed_scale=2.5)
+    bank = synth.make_bank_torch(L * E, H, I, 7, DEV)
+    cache = m.DeviceCache(spec, S, K, 11800, 47500, bank=bank, device=DEV)
+    wr_h = [synth.router_weights(200 + l, E, H) for l in range(L)]
+    bias_h = [synth.selection_bias(300 + l, E) for l in range(L)]
+    plan = m.DevicePlan(T * k, K, device=DEV)
+    wsb = m.moe_layer_workspace_bytes(spec, T)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    wts = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    y = torch.empty((T, H), dtype=torch.float32, device=DEV)
+    xs = [synth.ar1_stream(50 + l, 2, H, n_streams=T) for l in range(L)]
+    ost = oracle.CacheState(L * E, S)
+    for step in range(2):
+        for layer in range(L):
+            xb = xs[layer][step]
+            m.moe_layer_forward(spec, cache.c, layer, dev_bits(xb, DEV), T,
+                                dev_bits(wr_h[layer], DEV), dev(bias_h[layer], DEV), None,
+                                plan.c, ids, wts, ws, wsb, y)
+            ol = oracle.router_logits(xb, wr_h[layer])
+            oid, ow = oracle.route_sigmoid_group(ol, bias_h[layer], 8, 4, k, 2.5)
+            op = oracle.cache_step(ost, E, layer, oid, K, 11800, 47500)
+            if layer in (0, 5) and step == 1:
+                torch.cuda.synchronize()
+                assert np.array_equal(ids.cpu().numpy(), oid)
+                assert np.array_equal(f32_bits(wts.cpu().numpy()), f32_bits(ow))
+                _plans_equal(plan.read(K), op, K)
+                toks = [0] if T == 1 else [0, T - 1]
+                need = {int(e) for t in toks for e in oid[t]}
+                blobs = {e: bank[layer * E + e].cpu().numpy() for e in need}
+                anyb = blobs[next(iter(need))]
+                full = [blobs.get(e, anyb) for e in range(E)]
+                ref = oracle.moe_ffn(full, H, I, xb[toks], oid[toks], ow[toks])
+                assert_ffn_close(y.cpu().numpy()[toks], ref, f"layer {layer}")
+    torch.cuda.synchronize()
+    _tables_equal(cache, ost)
+    del bank, cache
+    torch.cuda.empty_cache()
