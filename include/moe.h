@@ -219,6 +219,37 @@ int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, con
                       moe_plan* plan, int32_t* ids, float* weights, void* workspace,
                       size_t workspace_bytes, float* y, moe_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * moe_expert_ffn_noalloc -- moe_expert_ffn for callers that cannot allocate
+ * device memory.  No counterpart on the pages: this is a library addition.
+ *
+ * Some callers of the decode FFN cannot call cudaMalloc or any allocating
+ * routine: code that runs inside a host application's fixed device-memory
+ * budget (an inference server or game engine whose pools own all device
+ * memory), real-time loops that forbid allocation on the token path, and
+ * plugins that are handed only input and output buffers.  For them this entry
+ * point takes the same inputs and output as moe_expert_ffn but no workspace:
+ * its scratch is one file-scope device array of MOE_NOALLOC_SCRATCH_BYTES
+ * inside libmoe.so, which every GPU that loads the library holds until the
+ * process exits.
+ *   - Sizes whose scratch need (moe_ffn_workspace_bytes(spec, T)) exceeds
+ *     MOE_NOALLOC_SCRATCH_BYTES are rejected with MOE_ECAPACITY.
+ *   - The first call on a device looks up the array's device address for the
+ *     current device (cudaGetSymbolAddress); make that first call before any
+ *     stream capture.
+ *   - All calls share the one array, which keeps the last call's contents
+ *     (the arrival counters are cleared by every call).  Calls whose
+ *     execution overlaps on the GPU (different streams, or different host
+ *     threads) race on it and must not be issued; order them on one stream.
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine.
+ * Results equal moe_expert_ffn's for the same inputs.
+ * ------------------------------------------------------------------------ */
+#define MOE_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+int moe_expert_ffn_noalloc(const moe_spec* spec, const moe_cache* cache, int32_t layer,
+                           const moe_plan* plan, const void* x, int32_t T, const int32_t* ids,
+                           const float* weights, const void* shared, float* y,
+                           moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

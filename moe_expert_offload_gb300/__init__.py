@@ -31,8 +31,9 @@ MOE_DERR_WAIT = 2
 EXPORTED = (
     "moe_last_error", "moe_version", "moe_expert_bytes", "moe_route", "moe_cache_reset",
     "moe_cache_step", "moe_ffn_workspace_bytes", "moe_expert_ffn", "moe_layer_workspace_bytes",
-    "moe_layer_forward",
+    "moe_layer_forward", "moe_expert_ffn_noalloc",
 )
+MOE_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class MoeError(RuntimeError):
@@ -98,6 +99,8 @@ def lib():
         L.moe_layer_forward.restype = C.c_int
         L.moe_layer_forward.argtypes = [sp, cp, i32, vp, i32, vp, vp, vp, pp, vp, vp, vp, sz,
                                         vp, vp]
+        L.moe_expert_ffn_noalloc.restype = C.c_int
+        L.moe_expert_ffn_noalloc.argtypes = [sp, cp, i32, pp, vp, i32, vp, vp, vp, vp, vp]
         _lib = L
     return _lib
 
@@ -163,6 +166,15 @@ def moe_expert_ffn(spec, cache, layer, plan, x, T, ids, weights, shared, workspa
                                        _ptr(x), T, _ptr(ids), _ptr(weights), _ptr(shared),
                                        _ptr(workspace), workspace_bytes, _ptr(y),
                                        _stream(stream)))
+
+
+def moe_expert_ffn_noalloc(spec, cache, layer, plan, x, T, ids, weights, shared, y, stream=None):
+    """moe_expert_ffn without a workspace, for callers that cannot allocate device
+    memory: the scratch is the library's built-in device array (see moe.h)."""
+    return _check(lib().moe_expert_ffn_noalloc(C.byref(spec), C.byref(cache), layer,
+                                               C.byref(plan), _ptr(x), T, _ptr(ids),
+                                               _ptr(weights), _ptr(shared), _ptr(y),
+                                               _stream(stream)))
 
 
 def moe_layer_workspace_bytes(spec, T) -> int:

@@ -292,3 +292,64 @@ int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, con
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// moe_expert_ffn_noalloc: the decode FFN with its scratch in a file-scope
+// device array instead of a caller workspace, for callers that may not
+// allocate device memory.  The array's device address is looked up once per
+// device (host code cannot use the symbol itself as a device pointer).
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kNoAllocMaxDevices = 64;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kNoAllocMaxDevices)
+    return fail(MOE_EUNSUPPORTED, "device ordinal %d >= %d", dev, kNoAllocMaxDevices);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" int moe_expert_ffn_noalloc(const moe_spec* spec, const moe_cache* cache,
+                                      int32_t layer, const moe_plan* plan, const void* x,
+                                      int32_t T, const int32_t* ids, const float* weights,
+                                      const void* shared, float* y, moe_stream_t stream) {
+  int rc = check_spec(spec);
+  if (rc) return rc;
+  rc = check_cache(spec, cache, true);
+  if (rc) return rc;
+  rc = check_step_args(spec, layer, T);
+  if (rc) return rc;
+  if (T == 0) return ok();
+  rc = check_plan(plan, T * spec->top_k);
+  if (rc) return rc;
+  if (T > moe::kMaxDecodeT)
+    return fail(MOE_EUNSUPPORTED, "decode FFN supports T <= %d", moe::kMaxDecodeT);
+  const size_t need = moe::ffn_workspace_bytes(spec->hidden, spec->inter, spec->top_k, T,
+                                               spec->has_shared);
+  if (need > MOE_NOALLOC_SCRATCH_BYTES)
+    return fail(MOE_ECAPACITY,
+                "moe_expert_ffn_noalloc: this size needs %zu scratch bytes, the built-in "
+                "array holds %zu; use moe_expert_ffn with a workspace",
+                need, (size_t)MOE_NOALLOC_SCRATCH_BYTES);
+  void* ws = nullptr;
+  rc = noalloc_scratch(&ws);
+  if (rc) return rc;
+  rc = do_ffn(spec, cache, layer, plan, x, T, ids, weights, shared, ws,
+              (size_t)MOE_NOALLOC_SCRATCH_BYTES, y, (cudaStream_t)stream);
+  return rc ? rc : ok();
+}
+
