@@ -51,6 +51,13 @@ WORKLOADS = {
              "deepseek_decode_b1",
         L=8, H=7168, I=2048, E=256, k=8, T=8, shared=False, router="sigmoid_group", ng=8, G=4,
         scale=2.5, slots=307, K=8, bp=11800, bh=47500),
+    "qwen_prefill": dict(
+        desc="Whole-layer prefill, Qwen3.6-35B-A3B layer shape: H=2048, I=512, E=256, top-8 "
+             "softmax + shared expert, 8192 tokens of N(0,1) bf16 hidden states with the router "
+             "logit of expert (t mod 256) raised by 3 (routing union = all 256 experts), int4 "
+             "affine g64 dequantised to bf16 into tcgen05 grouped GEMMs; 2 layers alternating, "
+             "the next layer copied bank -> buffer on a second stream (double buffer)",
+        L=2, H=2048, I=512, E=256, k=8, T=8192, shared=True, router="softmax", prefill=True),
 }
 
 
@@ -438,6 +445,189 @@ def run_gpu(args, w, rank, world, local_rank):
     print(json.dumps(out), flush=True)
 
 
+def prefill_flops(w):
+    """Algorithmic flops of the expert FFN per layer: 6*H*I per (token, expert)."""
+    return 6.0 * w["H"] * w["I"] * w["T"] * (w["k"] + (1 if w["shared"] else 0))
+
+
+def run_prefill(args, w, rank, world, local_rank):
+    import torch
+
+    import moe_expert_offload_gb300 as m
+    from moe_expert_offload_gb300 import _build, synth
+
+    _build.build()
+    m.lib()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    L, H, I, E, k, T = w["L"], w["H"], w["I"], w["E"], w["k"], w["T"]
+    spec = spec_of(w)
+    se = m.moe_expert_bytes(spec)
+    bank = synth.make_bank_torch(L * E + 1, H, I, 7, dev)
+    shared = bank[L * E]
+    bufs = [torch.empty((E, se), dtype=torch.uint8, device=dev) for _ in range(2)]
+    wr_h = [synth.router_weights(100 + l, E, H) for l in range(L)]
+    x_h = [synth.prefill_hidden(500 + l, T, H, wr_h[l]) for l in range(L)]
+    wr = [torch.from_numpy(a.view(np.int16)).to(dev) for a in wr_h]
+    xs = [torch.from_numpy(a.view(np.int16)).to(dev) for a in x_h]
+    wsb = m.moe_prefill_workspace_bytes(spec, T)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    wts = torch.empty((T, k), dtype=torch.float32, device=dev)
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    y = torch.empty((T, H), dtype=torch.float32, device=dev)
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    copy_done = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+    fws = m.moe_prefill_workspace_bytes(spec, T)
+
+    def compute(s, buf, ev=None):
+        l = s % L
+        sp = main.cuda_stream
+        if ev is not None:
+            ev[0].record(main)
+        m.moe_route(spec, xs[l], T, wr[l], None, logits, ids, wts, sp)
+        if ev is not None:
+            ev[1].record(main)
+        m.moe_expert_ffn_prefill(spec, buf, xs[l], T, ids, wts, shared, err, ws, fws, y, sp)
+        if ev is not None:
+            ev[2].record(main)
+
+    def step_overlap(s, ev=None):
+        # layer s % L computes from bufs[s % 2] while layer (s+1) % L streams into the other
+        main.wait_event(copy_done[s % 2])
+        side.wait_event(comp_done[(s + 1) % 2])
+        m.moe_layer_prefetch(spec, bank, (s + 1) % L, bufs[(s + 1) % 2], side.cuda_stream)
+        copy_done[(s + 1) % 2].record(side)
+        compute(s, bufs[s % 2], ev)
+        comp_done[s % 2].record(main)
+
+    def step_serial(s, ev=None):
+        m.moe_layer_prefetch(spec, bank, s % L, bufs[0], main.cuda_stream)
+        compute(s, bufs[0], ev)
+
+    def timed(fn, n, with_ev):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(main)
+        for s in range(n):
+            fn(s, evs[s] if with_ev else None)
+        b.record(main)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b), evs
+
+    m.moe_layer_prefetch(spec, bank, 0, bufs[0], main.cuda_stream)
+    copy_done[0].record(main)
+    comp_done[1].record(main)
+    for s in range(args.warmup):
+        step_overlap(s)
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        ms, evs = timed(step_overlap, args.steps, True)
+    route_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    ffn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    for s in range(min(args.warmup, 3)):
+        step_serial(s)
+    ms_serial, _ = timed(step_serial, args.steps, False)
+    assert int(err.cpu()[0]) == 0, "device error flag set"
+
+    # end to end: hidden states in from pinned host memory, y back, every step
+    x_host = [torch.from_numpy(a.view(np.int16)).pin_memory() for a in x_h]
+    y_host = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    x_dev = torch.empty((T, H), dtype=torch.int16, device=dev)
+    lws = m.moe_prefill_workspace_bytes(spec, T)
+
+    def e2e_step(s, ev=None):
+        l = s % L
+        main.wait_event(copy_done[s % 2])
+        side.wait_event(comp_done[(s + 1) % 2])
+        m.moe_layer_prefetch(spec, bank, (s + 1) % L, bufs[(s + 1) % 2], side.cuda_stream)
+        copy_done[(s + 1) % 2].record(side)
+        x_dev.copy_(x_host[l], non_blocking=True)
+        m.moe_layer_forward_prefill(spec, bufs[s % 2], x_dev, T, wr[l], None, shared, ids, wts,
+                                    err, ws, lws, y, main.cuda_stream)
+        y_host.copy_(y, non_blocking=True)
+        comp_done[s % 2].record(main)
+
+    m.moe_layer_prefetch(spec, bank, 0, bufs[0], main.cuda_stream)
+    copy_done[0].record(main)
+    comp_done[1].record(main)
+    for s in range(min(args.warmup, 3)):
+        e2e_step(s)
+    ms_e2e, _ = timed(e2e_step, args.steps, False)
+    if rank != 0:
+        return
+    _, bf16_peak, peak_kind = peaks()
+    sustained = None
+    pp = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pp):
+        sustained = json.load(open(pp)).get("bf16_tflops_sustained")
+    peak = float(sustained or bf16_peak)
+    flops = prefill_flops(w)
+    tflops = flops / (ffn_ms * 1e-3) / 1e12
+    step_ms = ms / args.steps
+    tokens = args.steps * T * world
+    out = {
+        "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "desc": w["desc"], "tokens": T, "layers": L,
+                   "l2": "inputs larger than L2: 453 MB of int4 experts per layer + 32 MB x"},
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": tflops / peak, "traffic": None,
+                     "kernel": "prefill expert FFN (moe_expert_ffn_prefill: permute, 2 grouped "
+                               "tcgen05 GEMMs, combine)",
+                     "algorithmic_flops_per_launch": flops, "avg_launch_us": ffn_ms * 1e3,
+                     "peak_kind": f"{peak_kind} bf16 dense, sustained"},
+        "prefill_tok_s": tokens / (ms * 1e-3),
+        "layer_ms": {"overlapped_copy": step_ms, "serial_copy": ms_serial / args.steps,
+                     "route": route_ms, "ffn": ffn_ms},
+        "e2e": {"value": tokens / (ms_e2e * 1e-3), "unit": "tok/s",
+                "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 4},
+        "gpu_launches": 10 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if world == 1 and not args.no_cpu:
+        out["cpu_baseline"] = cpu_baseline_prefill(w, x_h, wr_h)
+    print(json.dumps(out), flush=True)
+
+
+def cpu_baseline_prefill(w, x_h, wr_h, budget_s=12.0):
+    """The oracle (single thread) on a bounded sample of the prefill layer: routing and the
+    float64 FFN for successive tokens until the budget is spent; reported as TFLOP/s."""
+    import oracle
+    from moe_expert_offload_gb300 import synth
+
+    oracle.build()
+    H, I, E, k = w["H"], w["I"], w["E"], w["k"]
+    blobs = {}
+    shared = synth.make_expert_bytes(np.random.default_rng(12345), H, I)
+    spent, n, t = 0.0, 0, 0
+    while spent < budget_s and t < w["T"]:
+        xb = x_h[0][t:t + 1]
+        t0 = time.perf_counter()
+        ids, wt = oracle.route_softmax_topk(oracle.router_logits(xb, wr_h[0]), k)
+        spent += time.perf_counter() - t0
+        for e in ids.reshape(-1):
+            if int(e) not in blobs:
+                blobs[int(e)] = synth.make_expert_bytes(np.random.default_rng(int(e) + 1), H, I)
+        anyb = blobs[int(ids[0, 0])]
+        full = [blobs.get(e, anyb) for e in range(E)]
+        t0 = time.perf_counter()
+        oracle.moe_ffn(full, H, I, xb, ids, wt, shared, I)
+        spent += time.perf_counter() - t0
+        n += 1
+        t += 1
+    per_tok = 6.0 * H * I * (k + 1)
+    return {"value": per_tok * n / spent / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} prefill tokens (route + float64 FFN, experts dequantised per call) in "
+                      f"{spent:.1f} s, single thread"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -466,7 +656,10 @@ def main():
 
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
-    run_gpu(args, w, rank, world, local_rank)
+    if w.get("prefill"):
+        run_prefill(args, w, rank, world, local_rank)
+    else:
+        run_gpu(args, w, rank, world, local_rank)
     if world > 1:
         import torch
 

@@ -220,6 +220,47 @@ int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, con
                       size_t workspace_bytes, float* y, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Prefill (FreeToken summary "method steps": the GPU computes layer l from
+ * one whole-layer buffer while the next layer is copied into the other; the
+ * reader's "System Architecture" ping-pong buffers).  In prefill the routing
+ * union covers nearly every expert, so the experts run as grouped GEMMs on
+ * the tensor cores instead of through the slot cache.
+ * Requires hidden % 256 == 0, inter % 128 == 0, num_experts <= 1023.
+ * ------------------------------------------------------------------------ */
+
+/* Scratch bytes moe_expert_ffn_prefill / moe_layer_forward_prefill need. */
+size_t moe_prefill_workspace_bytes(const moe_spec* spec, int32_t T);
+
+/* Copy the E expert blobs of `layer` (E * S_e bytes, contiguous in the bank)
+ * into `dst` (device, 16-byte aligned) on `stream`: the whole-layer fill of the
+ * double buffer.  Issue it on a second stream to overlap the previous layer. */
+int moe_layer_prefetch(const moe_spec* spec, const void* bank, int32_t layer, void* dst,
+                       moe_stream_t stream);
+
+/* Prefill expert FFN + combine for T tokens (T >= 1).
+ *   layer_experts  device, the E blobs of this layer (bank slice or a buffer
+ *                  filled by moe_layer_prefetch)
+ *   x              device bf16 [T][H];  ids int32 [T][k], weights fp32 [T][k]
+ *   shared         shared expert blob or NULL (needs has_shared)
+ *   err            device int32 [1] or NULL: MOE_DERR_* bits are OR-ed in
+ *   y              device fp32 [T][H] out:  sum_j w[t][j] expert_{ids[t][j]}(x[t])
+ *                  + shared(x[t]); each routed term is rounded to bf16 before
+ *                  the fixed-order fp32 sum; h is bf16.
+ * Steps: stable counting sort of the T*k assignments by expert, grouped GEMM
+ * gate/up with SwiGLU, grouped GEMM down with the routing weight, combine. */
+int moe_expert_ffn_prefill(const moe_spec* spec, const void* layer_experts, const void* x,
+                           int32_t T, const int32_t* ids, const float* weights,
+                           const void* shared, int32_t* err, void* workspace,
+                           size_t workspace_bytes, float* y, moe_stream_t stream);
+
+/* moe_route + moe_expert_ffn_prefill for one layer (ids / weights are outputs). */
+int moe_layer_forward_prefill(const moe_spec* spec, const void* layer_experts, const void* x,
+                              int32_t T, const void* w_router, const float* bias,
+                              const void* shared, int32_t* ids, float* weights, int32_t* err,
+                              void* workspace, size_t workspace_bytes, float* y,
+                              moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * moe_expert_ffn_noalloc -- moe_expert_ffn for callers that cannot allocate
  * device memory.  No counterpart on the pages: this is a library addition.
  *

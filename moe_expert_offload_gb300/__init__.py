@@ -31,7 +31,8 @@ MOE_DERR_WAIT = 2
 EXPORTED = (
     "moe_last_error", "moe_version", "moe_expert_bytes", "moe_route", "moe_cache_reset",
     "moe_cache_step", "moe_ffn_workspace_bytes", "moe_expert_ffn", "moe_layer_workspace_bytes",
-    "moe_layer_forward", "moe_expert_ffn_noalloc",
+    "moe_layer_forward", "moe_expert_ffn_noalloc", "moe_prefill_workspace_bytes",
+    "moe_layer_prefetch", "moe_expert_ffn_prefill", "moe_layer_forward_prefill",
 )
 MOE_NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -99,6 +100,15 @@ def lib():
         L.moe_layer_forward.restype = C.c_int
         L.moe_layer_forward.argtypes = [sp, cp, i32, vp, i32, vp, vp, vp, pp, vp, vp, vp, sz,
                                         vp, vp]
+        L.moe_prefill_workspace_bytes.restype = sz
+        L.moe_prefill_workspace_bytes.argtypes = [sp, i32]
+        L.moe_layer_prefetch.restype = C.c_int
+        L.moe_layer_prefetch.argtypes = [sp, vp, i32, vp, vp]
+        L.moe_expert_ffn_prefill.restype = C.c_int
+        L.moe_expert_ffn_prefill.argtypes = [sp, vp, vp, i32, vp, vp, vp, vp, vp, sz, vp, vp]
+        L.moe_layer_forward_prefill.restype = C.c_int
+        L.moe_layer_forward_prefill.argtypes = [sp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, sz,
+                                                vp, vp]
         L.moe_expert_ffn_noalloc.restype = C.c_int
         L.moe_expert_ffn_noalloc.argtypes = [sp, cp, i32, pp, vp, i32, vp, vp, vp, vp, vp]
         _lib = L
@@ -187,6 +197,32 @@ def moe_layer_forward(spec, cache, layer, x, T, w_router, bias, shared, plan, id
                                           _ptr(w_router), _ptr(bias), _ptr(shared), C.byref(plan),
                                           _ptr(ids), _ptr(weights), _ptr(workspace),
                                           workspace_bytes, _ptr(y), _stream(stream)))
+
+
+def moe_prefill_workspace_bytes(spec, T) -> int:
+    return int(lib().moe_prefill_workspace_bytes(C.byref(spec), T))
+
+
+def moe_layer_prefetch(spec, bank, layer, dst, stream=None):
+    return _check(lib().moe_layer_prefetch(C.byref(spec), _ptr(bank), layer, _ptr(dst),
+                                           _stream(stream)))
+
+
+def moe_expert_ffn_prefill(spec, layer_experts, x, T, ids, weights, shared, err, workspace,
+                           workspace_bytes, y, stream=None):
+    return _check(lib().moe_expert_ffn_prefill(C.byref(spec), _ptr(layer_experts), _ptr(x), T,
+                                               _ptr(ids), _ptr(weights), _ptr(shared), _ptr(err),
+                                               _ptr(workspace), workspace_bytes, _ptr(y),
+                                               _stream(stream)))
+
+
+def moe_layer_forward_prefill(spec, layer_experts, x, T, w_router, bias, shared, ids, weights,
+                              err, workspace, workspace_bytes, y, stream=None):
+    return _check(lib().moe_layer_forward_prefill(C.byref(spec), _ptr(layer_experts), _ptr(x), T,
+                                                  _ptr(w_router), _ptr(bias), _ptr(shared),
+                                                  _ptr(ids), _ptr(weights), _ptr(err),
+                                                  _ptr(workspace), workspace_bytes, _ptr(y),
+                                                  _stream(stream)))
 
 
 # ------------------------------------------------- device memory (plumbing)

@@ -294,6 +294,115 @@ int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, con
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
+// Prefill entry points.
+namespace {
+
+int check_prefill(const moe_spec* s, int32_t T) {
+  if (T < 0) return fail(MOE_EINVAL, "T must be >= 0");
+  if (s->hidden % 256 || s->inter % 128)
+    return fail(MOE_EUNSUPPORTED, "prefill needs hidden %% 256 == 0 and inter %% 128 == 0");
+  if (s->num_experts > 1023) return fail(MOE_EUNSUPPORTED, "prefill supports num_experts <= 1023");
+  if ((int64_t)T * (s->top_k + 1) > ((int64_t)1 << 30)) return fail(MOE_EINVAL, "T too large");
+  return MOE_OK;
+}
+
+size_t prefill_ws(const moe_spec* s, int32_t T) {
+  return align256((size_t)T * s->num_experts * 4) +
+         moe::prefill_workspace_bytes(s->hidden, s->inter, s->num_experts, s->top_k, T);
+}
+
+int do_prefill(const moe_spec* spec, const void* experts, const void* x, int32_t T,
+               const int32_t* ids, const float* weights, const void* shared, int32_t* err,
+               void* ws, size_t ws_bytes, float* y, cudaStream_t st) {
+  if (!experts || !x || !ids || !weights || !y || !ws)
+    return fail(MOE_EINVAL, "prefill: NULL argument");
+  if (spec->has_shared && !shared) return fail(MOE_EINVAL, "spec has a shared expert: pass its blob");
+  if (!aligned(experts, 16) || !aligned(x, 16) || !aligned(y, 16) || !aligned(ws, 256) ||
+      (shared && !aligned(shared, 16)))
+    return fail(MOE_EINVAL, "prefill: experts/x/y/shared need 16 B, workspace 256 B alignment");
+  const size_t need = moe::prefill_workspace_bytes(spec->hidden, spec->inter, spec->num_experts,
+                                                   spec->top_k, T);
+  if (ws_bytes < need) return fail(MOE_ECAPACITY, "workspace %zu < %zu bytes", ws_bytes, need);
+  moe::PrefillBufs b;
+  moe::prefill_carve(b, ws, spec->hidden, spec->inter, spec->num_experts, spec->top_k, T);
+  moe::GemmArgs a = {};
+  a.H = spec->hidden;
+  a.I = spec->inter;
+  a.E = spec->num_experts;
+  a.k = spec->top_k;
+  a.T = T;
+  a.blob_bytes = moe::blob_offsets(a.H, a.I).total;
+  a.experts = static_cast<const uint8_t*>(experts);
+  a.shared = static_cast<const uint8_t*>(shared);
+  a.weights = weights;
+  a.err = err;
+  cudaError_t e = moe::launch_prefill_ffn(a, b, static_cast<const uint16_t*>(x), ids,
+                                          spec->has_shared, y, st);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" size_t moe_prefill_workspace_bytes(const moe_spec* spec, int32_t T) {
+  if (check_spec(spec) != MOE_OK || T < 1 || check_prefill(spec, T) != MOE_OK) return 0;
+  return prefill_ws(spec, T);
+}
+
+extern "C" int moe_layer_prefetch(const moe_spec* spec, const void* bank, int32_t layer,
+                                  void* dst, moe_stream_t stream) {
+  int rc = check_spec(spec);
+  if (rc) return rc;
+  if (layer < 0 || layer >= spec->num_layers) return fail(MOE_EINVAL, "layer out of range");
+  if (!bank || !dst) return fail(MOE_EINVAL, "moe_layer_prefetch: NULL argument");
+  const size_t se = (size_t)moe::blob_offsets(spec->hidden, spec->inter).total;
+  const size_t bytes = se * spec->num_experts;
+  const uint8_t* src = static_cast<const uint8_t*>(bank) + (size_t)layer * bytes;
+  cudaError_t e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "layer copy");
+  return ok();
+}
+
+extern "C" int moe_expert_ffn_prefill(const moe_spec* spec, const void* layer_experts,
+                                      const void* x, int32_t T, const int32_t* ids,
+                                      const float* weights, const void* shared, int32_t* err,
+                                      void* workspace, size_t workspace_bytes, float* y,
+                                      moe_stream_t stream) {
+  int rc = check_spec(spec);
+  if (rc) return rc;
+  rc = check_prefill(spec, T);
+  if (rc) return rc;
+  if (T == 0) return ok();
+  rc = do_prefill(spec, layer_experts, x, T, ids, weights, shared, err, workspace,
+                  workspace_bytes, y, (cudaStream_t)stream);
+  return rc ? rc : ok();
+}
+
+extern "C" int moe_layer_forward_prefill(const moe_spec* spec, const void* layer_experts,
+                                         const void* x, int32_t T, const void* w_router,
+                                         const float* bias, const void* shared, int32_t* ids,
+                                         float* weights, int32_t* err, void* workspace,
+                                         size_t workspace_bytes, float* y, moe_stream_t stream) {
+  int rc = check_spec(spec);
+  if (rc) return rc;
+  rc = check_prefill(spec, T);
+  if (rc) return rc;
+  if (T == 0) return ok();
+  if (!workspace || !aligned(workspace, 256))
+    return fail(MOE_EINVAL, "workspace must be 256-B aligned");
+  if (workspace_bytes < prefill_ws(spec, T))
+    return fail(MOE_ECAPACITY, "workspace %zu < %zu bytes", workspace_bytes, prefill_ws(spec, T));
+  cudaStream_t st = (cudaStream_t)stream;
+  float* logits = static_cast<float*>(workspace);
+  const size_t lb = align256((size_t)T * spec->num_experts * 4);
+  rc = do_route(spec, x, T, w_router, bias, logits, ids, weights, st);
+  if (rc) return rc;
+  rc = do_prefill(spec, layer_experts, x, T, ids, weights, shared, err,
+                  static_cast<uint8_t*>(workspace) + lb, workspace_bytes - lb, y, st);
+  return rc ? rc : ok();
+}
+
+// ---------------------------------------------------------------------------
 // moe_expert_ffn_noalloc: the decode FFN with its scratch in a file-scope
 // device array instead of a caller workspace, for callers that may not
 // allocate device memory.  The array's device address is looked up once per

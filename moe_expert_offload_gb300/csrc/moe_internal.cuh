@@ -79,4 +79,44 @@ size_t ffn_workspace_bytes(int H, int I, int k, int T, int has_shared);
 void ffn_carve_workspace(FfnArgs& a, void* ws);
 cudaError_t launch_ffn_decode(const FfnArgs& a, cudaStream_t st);
 
+// ------------------------------------------------------------------ prefill
+constexpr int kPrefillTileRows = 256;  // rows of one grouped-GEMM m-tile
+
+struct GemmArgs {
+  int H, I, E, k, T;
+  int64_t blob_bytes;
+  const uint8_t* experts;   // E blobs of this layer, contiguous
+  const uint8_t* shared;    // shared expert blob (group E) or null
+  const uint16_t* a_src;    // mode 1: x_perm [T][H]; mode 2: h_perm [R][I]
+  const int32_t* perm;      // permuted row -> assignment (t*k + j, or T*k + t)
+  const int32_t* tile_g;    // m-tile -> group (expert, or E for the shared one)
+  const int32_t* tile_row0; // m-tile -> first permuted row
+  const int32_t* tile_rows; // m-tile -> rows (<= kPrefillTileRows)
+  const int32_t* n_tiles;   // device count of m-tiles
+  const float* weights;     // [T][k]
+  uint16_t* h_out;          // mode 1 output: h_perm [R][I], K-permuted
+  uint16_t* y_out;          // mode 2 output: y_assign [T][k+1][H]
+  int32_t* err;             // device error bits (MOE_DERR_*), may be null
+};
+
+struct PrefillBufs {
+  uint16_t* x_perm;
+  int32_t* counts;          // [E + 1]
+  int32_t* offsets;         // [E + 2]
+  int32_t* perm;            // [T*k + T]
+  int32_t* tile_g;
+  int32_t* tile_row0;
+  int32_t* tile_rows;
+  int32_t* n_tiles;
+  uint16_t* h_perm;         // [T*k + T][I]
+  uint16_t* y_assign;       // [T][k + 1][H]
+  int max_tiles;
+};
+
+size_t prefill_workspace_bytes(int H, int I, int E, int k, int T);
+void prefill_carve(PrefillBufs& b, void* ws, int H, int I, int E, int k, int T);
+cudaError_t launch_prefill_ffn(const GemmArgs& base, const PrefillBufs& b, const uint16_t* x,
+                               const int32_t* ids, int has_shared, float* y, cudaStream_t st);
+cudaError_t launch_grouped_gemm(int mode, const GemmArgs& a, int max_tiles, cudaStream_t st);
+
 }  // namespace moe

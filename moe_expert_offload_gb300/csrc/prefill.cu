@@ -1,0 +1,256 @@
+// Prefill path around the grouped GEMMs (FreeToken summary "method steps":
+// prefill computes layer l from one whole-layer buffer while the next layer
+// streams into the other; reader "System Architecture" ping-pong buffers).
+//
+//   1. x -> x_perm: each 8-element chunk reordered 0,4,1,5,2,6,3,7 (the K
+//      order of the GEMM operands).
+//   2. routing permute: a stable counting sort of the T*k (token, rank)
+//      assignments by expert; the shared expert (if any) is one more group
+//      holding every token in order.  Offsets, and 256-row m-tiles per group.
+//   3. GEMM1 (gate/up + SwiGLU) and GEMM2 (down, weighted per assignment).
+//   4. combine: y[t] = sum over j = 0..k of y_assign[t][j], in j order.
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kTileRows = kPrefillTileRows;
+
+__global__ void permute_x_kernel(const uint4* __restrict__ x, uint4* __restrict__ xp, int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 v = __ldg(x + i);
+    uint4 o;
+    o.x = __byte_perm(v.x, v.z, 0x5410);
+    o.y = __byte_perm(v.x, v.z, 0x7632);
+    o.z = __byte_perm(v.y, v.w, 0x5410);
+    o.w = __byte_perm(v.y, v.w, 0x7632);
+    xp[i] = o;
+  }
+}
+
+__global__ void zero_i32_kernel(int32_t* p, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = 0;
+}
+
+// Per-expert assignment counts (ids outside [0, E) are flagged and skipped).
+__global__ void hist_kernel(const int32_t* __restrict__ ids, int n, int E, int32_t* counts,
+                            int32_t* err) {
+  extern __shared__ int32_t h[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
+  __syncthreads();
+  bool bad = false;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const int e = ids[i];
+    if (e >= 0 && e < E)
+      atomicAdd(&h[e], 1);
+    else
+      bad = true;
+  }
+  if (bad && err) atomicOr(err, MOE_DERR_BAD_ID);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    if (h[e]) atomicAdd(&counts[e], h[e]);
+}
+
+// One CTA: group offsets (exclusive scan of counts, group E = shared expert
+// with T rows) and the m-tile table (256 rows per tile, ragged last tile).
+__global__ void __launch_bounds__(1024) plan_kernel(int32_t* counts, int E, int T,
+                                                    int has_shared, int32_t* offsets,
+                                                    int32_t* tile_g, int32_t* tile_row0,
+                                                    int32_t* tile_rows, int32_t* n_tiles,
+                                                    int max_tiles) {
+  __shared__ int s_wr[32], s_wt[32];
+  const int G = E + 1;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  if (tid == E) counts[E] = has_shared ? T : 0;
+  // each thread owns one group (G = E + 1 <= 1024)
+  int c = 0, t = 0;
+  if (tid < G) {
+    c = (tid == E) ? (has_shared ? T : 0) : counts[tid];
+    t = (c + kTileRows - 1) / kTileRows;
+  }
+  // block exclusive scans of rows and tiles
+  int ir = c, it = t;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int vr = __shfl_up_sync(0xffffffffu, ir, d), vt = __shfl_up_sync(0xffffffffu, it, d);
+    if (lane >= d) {
+      ir += vr;
+      it += vt;
+    }
+  }
+  if (lane == 31) {
+    s_wr[wid] = ir;
+    s_wt[wid] = it;
+  }
+  __syncthreads();
+  if (wid == 0) {
+    int wr = s_wr[lane], wt = s_wt[lane];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int vr = __shfl_up_sync(0xffffffffu, wr, d), vt = __shfl_up_sync(0xffffffffu, wt, d);
+      if (lane >= d) {
+        wr += vr;
+        wt += vt;
+      }
+    }
+    s_wr[lane] = wr;
+    s_wt[lane] = wt;
+  }
+  __syncthreads();
+  const int base_r = (wid > 0 ? s_wr[wid - 1] : 0) + ir - c;
+  const int base_t = (wid > 0 ? s_wt[wid - 1] : 0) + it - t;
+  if (tid < G) {
+    offsets[tid] = base_r;
+    for (int j = 0; j < t; ++j) {
+      const int m = base_t + j;
+      if (m < max_tiles) {
+        tile_g[m] = tid;
+        tile_row0[m] = base_r + j * kTileRows;
+        tile_rows[m] = min(kTileRows, c - j * kTileRows);
+      }
+    }
+  }
+  if (tid == G - 1) {
+    offsets[G] = base_r + c;
+    *n_tiles = min(base_t + t, max_tiles);
+  }
+}
+
+// CTA g: the assignments routed to expert g, in ascending (t, j) order, to
+// perm[offsets[g] ...]; CTA E (shared expert) writes T*k + t for every token.
+__global__ void __launch_bounds__(256) scatter_kernel(const int32_t* __restrict__ ids, int n,
+                                                      int T, const int32_t* __restrict__ offsets,
+                                                      int32_t* __restrict__ perm, int E) {
+  __shared__ int s_w[8];
+  const int g = blockIdx.x;
+  const int base = offsets[g];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  if (g == E) {
+    for (int t = tid; t < T; t += blockDim.x) perm[base + t] = n + t;
+    return;
+  }
+  int run = 0;
+  for (int i0 = 0; i0 < n; i0 += blockDim.x) {
+    const int i = i0 + tid;
+    const bool m = i < n && ids[i] == g;
+    const unsigned b = __ballot_sync(0xffffffffu, m);
+    if (lane == 0) s_w[wid] = __popc(b);
+    __syncthreads();
+    int pre = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      pre += (w < wid) ? s_w[w] : 0;
+      tot += s_w[w];
+    }
+    if (m) perm[base + run + pre + __popc(b & ((1u << lane) - 1u))] = i;
+    run += tot;
+    __syncthreads();
+  }
+}
+
+// y[t][o] = sum_{j=0..k} y_assign[t][j][o] (bf16 terms, fp32 sum, j order);
+// routed terms whose id was invalid are skipped.
+__global__ void combine_kernel(const uint16_t* __restrict__ ya, const int32_t* __restrict__ ids,
+                               int T, int k, int E, int H, int has_shared, float* __restrict__ y) {
+  const int nslot = k + 1;
+  const int64_t n = (int64_t)T * H / 8;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = (i * 8) / H, o = (i * 8) % H;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < nslot; ++j) {
+      if (j < k) {
+        const int e = ids[t * k + j];
+        if (e < 0 || e >= E) continue;
+      } else if (!has_shared) {
+        continue;
+      }
+      const uint4 v = __ldcs(reinterpret_cast<const uint4*>(ya + (t * nslot + j) * H + o));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[2 * q] += __uint_as_float(w[q] << 16);
+        acc[2 * q + 1] += __uint_as_float(w[q] & 0xFFFF0000u);
+      }
+    }
+    float4* dst = reinterpret_cast<float4*>(y + t * H + o);
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+}
+
+size_t al256(size_t b) { return (b + 255) / 256 * 256; }
+
+int max_tiles_for(int E, int k, int T) {
+  return (int)(((int64_t)T * k + T + kTileRows - 1) / kTileRows) + E + 1;
+}
+
+}  // namespace
+
+size_t prefill_workspace_bytes(int H, int I, int E, int k, int T) {
+  const size_t R = (size_t)T * k + T;
+  const size_t mt = max_tiles_for(E, k, T);
+  return al256((size_t)T * H * 2) + al256((size_t)(E + 1) * 4) + al256((size_t)(E + 2) * 4) +
+         al256(R * 4) + 3 * al256(mt * 4) + al256(4) + al256(R * I * 2) +
+         al256((size_t)T * (k + 1) * H * 2);
+}
+
+void prefill_carve(PrefillBufs& b, void* ws, int H, int I, int E, int k, int T) {
+  const size_t R = (size_t)T * k + T;
+  const size_t mt = max_tiles_for(E, k, T);
+  uint8_t* p = static_cast<uint8_t*>(ws);
+  auto take = [&](size_t n) {
+    uint8_t* q = p;
+    p += al256(n);
+    return q;
+  };
+  b.x_perm = reinterpret_cast<uint16_t*>(take((size_t)T * H * 2));
+  b.counts = reinterpret_cast<int32_t*>(take((size_t)(E + 1) * 4));
+  b.offsets = reinterpret_cast<int32_t*>(take((size_t)(E + 2) * 4));
+  b.perm = reinterpret_cast<int32_t*>(take(R * 4));
+  b.tile_g = reinterpret_cast<int32_t*>(take(mt * 4));
+  b.tile_row0 = reinterpret_cast<int32_t*>(take(mt * 4));
+  b.tile_rows = reinterpret_cast<int32_t*>(take(mt * 4));
+  b.n_tiles = reinterpret_cast<int32_t*>(take(4));
+  b.h_perm = reinterpret_cast<uint16_t*>(take(R * I * 2));
+  b.y_assign = reinterpret_cast<uint16_t*>(take((size_t)T * (k + 1) * H * 2));
+  b.max_tiles = (int)mt;
+}
+
+cudaError_t launch_prefill_ffn(const GemmArgs& base, const PrefillBufs& b, const uint16_t* x,
+                               const int32_t* ids, int has_shared, float* y, cudaStream_t st) {
+  const int H = base.H, E = base.E, k = base.k, T = base.T;
+  const int n = T * k;
+  cudaError_t e;
+  const int64_t nx = (int64_t)T * H / 8;
+  permute_x_kernel<<<(int)((nx + 255) / 256 < 4096 ? (nx + 255) / 256 : 4096), 256, 0, st>>>(
+      reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(b.x_perm), nx);
+  zero_i32_kernel<<<1, 256, 0, st>>>(b.counts, E + 1);
+  const int hb = (n + 1023) / 1024 < 256 ? (n + 1023) / 1024 : 256;
+  hist_kernel<<<hb > 0 ? hb : 1, 256, E * 4, st>>>(ids, n, E, b.counts, base.err);
+  plan_kernel<<<1, 1024, 0, st>>>(b.counts, E, T, has_shared, b.offsets, b.tile_g, b.tile_row0,
+                                  b.tile_rows, b.n_tiles, b.max_tiles);
+  scatter_kernel<<<E + (has_shared ? 1 : 0), 256, 0, st>>>(ids, n, T, b.offsets, b.perm, E);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  GemmArgs a = base;
+  a.perm = b.perm;
+  a.tile_g = b.tile_g;
+  a.tile_row0 = b.tile_row0;
+  a.tile_rows = b.tile_rows;
+  a.n_tiles = b.n_tiles;
+  a.a_src = b.x_perm;
+  a.h_out = b.h_perm;
+  a.y_out = b.y_assign;
+  if ((e = launch_grouped_gemm(1, a, b.max_tiles, st)) != cudaSuccess) return e;
+  a.a_src = b.h_perm;
+  if ((e = launch_grouped_gemm(2, a, b.max_tiles, st)) != cudaSuccess) return e;
+  const int64_t nc = (int64_t)T * H / 8;
+  combine_kernel<<<(int)((nc + 255) / 256 < 8192 ? (nc + 255) / 256 : 8192), 256, 0, st>>>(
+      b.y_assign, ids, T, k, E, H, has_shared, y);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -166,3 +166,24 @@ def test_layer_forward_argument_checks(L):
         m.moe_layer_forward(s, _cache(), 5, 256, 1, 256, None, None, _plan(), 256, 256, 4096,
                             need, 256, stream=0)
     assert e.value.code == m.MOE_EINVAL
+
+
+def test_prefill_argument_checks(L):
+    s = _spec(hidden=320 // 64 * 64)
+    s.hidden = 320
+    assert m.moe_prefill_workspace_bytes(s, 16) == 0  # hidden % 256 != 0
+    s2 = _spec()
+    assert m.moe_prefill_workspace_bytes(s2, 16) > 0
+    with pytest.raises(m.MoeError) as e:
+        m.moe_expert_ffn_prefill(s2, 4096, 4096, 16, 256, 256, None, None, 4096, 16, 4096,
+                                 stream=0)
+    assert e.value.code == m.MOE_ECAPACITY
+    with pytest.raises(m.MoeError) as e:
+        m.moe_expert_ffn_prefill(s2, None, 4096, 16, 256, 256, None, None, 4096, 1 << 30, 4096,
+                                 stream=0)
+    assert e.value.code == m.MOE_EINVAL
+    with pytest.raises(m.MoeError) as e:
+        m.moe_layer_prefetch(s2, 4096, 7, 4096, stream=0)
+    assert e.value.code == m.MOE_EINVAL
+    assert m.moe_expert_ffn_prefill(s2, None, None, 0, None, None, None, None, None, 0, None,
+                                    stream=0) == m.MOE_OK
