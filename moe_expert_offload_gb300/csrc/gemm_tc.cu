@@ -13,14 +13,20 @@
 //
 // One CTA computes a 256 x 256 tile (BM x BN) with K in blocks of 64, as two
 // M=128 MMAs per K step that share one dequantised B tile:
-//   * A (256 rows x 64 bf16) is gathered row by row with cp.async into a
-//     4-deep ring, two blocks ahead; rows past the expert's count are zero and
-//     a tile of at most 128 rows skips its second half entirely.
-//   * The raw int4 codes and group scales/biases of B (256 rows) are loaded
-//     straight into registers, also two blocks ahead (three named register
-//     sets in rotation); 16 warps dequantise them (one LOP3 per nibble pair
-//     gives (128+q) as bf16x2, then q = v - 128 and w = s*q + b by bf16x2 fma)
-//     into a double-buffered B operand.
+//   * Warp-specialised, stages handed over with mbarriers (no block-wide
+//     barrier inside the K loop):
+//       warps 0-3 gather A (256 rows x 64 bf16) row by row with cp.async into
+//                 a 4-deep ring (each lane owns 16 fixed rows, addresses kept
+//                 in registers); cp.async.mbarrier.arrive marks a stage full.
+//                 Rows past the group's count are zero-filled, and a tile of at
+//                 most 128 rows skips its second half entirely.
+//       warps 5-12 one B row per thread: int4 codes and the group scale / bias
+//                 prefetched into registers three blocks ahead, dequantised (one
+//                 LOP3 per nibble pair gives (128+q) as bf16x2, then q = v - 128
+//                 and w = s*q + b by bf16x2 fma) into a 2-deep B ring.
+//       warp 4    one thread waits for both stages, issues the MMAs and frees
+//                 the stages with tcgen05.commit.
+//     Warps 5-12 then read the accumulators (tcgen05.ld) for the epilogue.
 //   * Both operands are K-major bf16 in the 128-byte swizzled layout; one
 //     thread issues tcgen05.mma (M=128, N=256, K=16) into two TMEM
 //     accumulators (512 columns) and tcgen05.commit signals an mbarrier when
@@ -30,7 +36,8 @@
 //     stored in the same order (x is permuted once, GEMM1 writes h in it), so
 //     every dot product is unchanged.
 // Every mbarrier wait is bounded: on time-out the CTA records MOE_DERR_WAIT,
-// drains its own copies, frees its TMEM and returns.
+// every role leaves its loop, the loader drains its own copies, and the CTA
+// frees its TMEM and returns.
 #include <cuda_bf16.h>
 
 #include "moe_internal.cuh"
@@ -40,9 +47,12 @@ namespace {
 
 constexpr int kBM = kPrefillTileRows;            // 256 rows: two M=128 accumulators
 constexpr int kBN = 256, kBK = 64;
-constexpr int kThreads = 512;
-constexpr int kStages = 4;                       // A ring depth
-constexpr int kAhead = 2;                        // blocks loaded ahead (A and B codes)
+// warp roles: 0-3 gather A, 4 issues MMAs (one thread), 5-12 dequantise B and
+// then drain the accumulators
+constexpr int kLoadWarps = 4, kMmaWarp = 4, kDqWarp0 = 5, kDqWarps = 8;
+constexpr int kThreads = (kDqWarp0 + kDqWarps) * 32;
+constexpr int kStagesA = 4;                      // A ring depth
+constexpr int kStagesB = 2;                      // B operand ring depth
 constexpr int kHalfBytes = 128 * kBK * 2;        // 16 KB: one 128-row half of A
 constexpr int kABytes = kBM * kBK * 2;           // 32 KB
 constexpr int kBBytes = kBN * kBK * 2;           // 32 KB
@@ -58,14 +68,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool v
   const int n = valid ? 16 : 0;  // 0: zero-fill the destination
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
                : "memory");
-}
-
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
 template <int N>
@@ -168,11 +170,27 @@ __device__ __forceinline__ uint32_t bf2(float lo, float hi) {
 }
 
 
+__device__ __forceinline__ void mbar_arrive(uint32_t addr) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}" ::"r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_arrive(uint32_t addr) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(addr) : "memory");
+}
+
+struct BRegs {
+  uint4 q0, q1;   // the B row's 32 code bytes of one k-block
+  uint32_t s, b;  // scale / bias words holding groups kb & ~1 and kb | 1
+};
+
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(GemmArgs g) {
   extern __shared__ unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t mbar[2];
+  __shared__ __align__(8) uint64_t full_a[kStagesA], empty_a[kStagesA];
+  __shared__ __align__(8) uint64_t full_b[kStagesB], empty_b[kStagesB], acc_full;
   __shared__ uint32_t tmem_slot;
+  __shared__ volatile int s_fail;
   __shared__ const uint16_t* arow_s[kBM];
   const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
   const int mt = blockIdx.x, nt = blockIdx.y;
@@ -180,14 +198,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(GemmArgs g) {
   const int grp = g.tile_g[mt], row0 = g.tile_row0[mt], rows = g.tile_rows[mt];
   const int H = g.H, I = g.I;
   const int K = (MODE == 1) ? H : I, nk = K / kBK;
+  const bool two = rows > 128;  // second 128-row half in use
 
-  // shared memory: A ring | B double buffer | raw ring (1024-aligned base)
+  // shared memory: A ring | B ring (1024-aligned base)
   const uint32_t s0 = smem_u32(smem_raw);
   const uint32_t sbase = (s0 + 1023u) & ~1023u;
   unsigned char* gbase = smem_raw + (sbase - s0);
   const uint32_t a_addr = sbase;
-  const uint32_t b_addr = sbase + kStages * kABytes;
-  unsigned char* b_ptr = gbase + (b_addr - sbase);
+  const uint32_t b_addr = sbase + kStagesA * kABytes;
+  unsigned char* b_ptr = gbase + kStagesA * kABytes;
 
   // A source row of every tile row (null past the group's rows)
   for (int r = tid; r < kBM; r += kThreads) {
@@ -212,8 +231,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(GemmArgs g) {
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (tid == 0) {
-    mbar_init(smem_u32(&mbar[0]), 1);
-    mbar_init(smem_u32(&mbar[1]), 1);
+    for (int i = 0; i < kStagesA; ++i) {
+      mbar_init(smem_u32(&full_a[i]), 32 * kLoadWarps);  // one cp.async arrive per loader lane
+      mbar_init(smem_u32(&empty_a[i]), 1);  // tcgen05.commit
+    }
+    for (int i = 0; i < kStagesB; ++i) {
+      mbar_init(smem_u32(&full_b[i]), kDqWarps);  // one arrive per dequant warp
+      mbar_init(smem_u32(&empty_b[i]), 1);
+    }
+    mbar_init(smem_u32(&acc_full), 1);
+    s_fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   tc_fence_before();
@@ -221,195 +248,213 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(GemmArgs g) {
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  // B row r of the tile -> its codes / scale / bias rows
-  const uint8_t* blob = (grp < g.E) ? g.experts + (int64_t)grp * g.blob_bytes : g.shared;
-  const BlobOffsets off = blob_offsets(H, I);
-  auto brow = [&](int r, int which) -> const uint8_t* {  // which: 0 codes, 1 scale, 2 bias
-    int64_t row, o;
+  if (wid < kLoadWarps) {
+    // ---------------------------------------------------------- A loader
+    // lane: rows wid*64 + lane/8 + 4j (j < 16), 16-byte chunk lane % 8
+    constexpr int kRowsPerLane = kBM / (kLoadWarps * 4);
+    const int c = lane & 7;
+    const uint16_t* src[kRowsPerLane];
+    uint32_t doff[kRowsPerLane];
+    uint32_t vmask = 0;
+#pragma unroll
+    for (int j = 0; j < kRowsPerLane; ++j) {
+      const int r = wid * (kBM / kLoadWarps) + (lane >> 3) + 4 * j;
+      const uint16_t* p = arow_s[r];
+      src[j] = p ? p + c * 8 : g.a_src;
+      doff[j] = (r >> 7) * kHalfBytes + swz(r & 127, c);
+      if (p) vmask |= 1u << j;
+    }
+    const bool active = two || wid * (kBM / kLoadWarps) < 128;
+    for (int kb = 0; kb < nk; ++kb) {
+      const int st = kb % kStagesA, use = kb / kStagesA;
+      if (use > 0 && !mbar_wait(smem_u32(&empty_a[st]), (use - 1) & 1)) s_fail = 1;
+      if (s_fail) break;
+      const uint32_t ab = a_addr + st * kABytes;
+      if (active) {
+#pragma unroll
+        for (int j = 0; j < kRowsPerLane; ++j)
+          cp_async16(ab + doff[j], src[j] + kb * kBK, (vmask >> j) & 1u);
+      }
+      cp_async_arrive(smem_u32(&full_a[st]));
+    }
+    cp_async_wait<0>();
+  } else if (wid == kMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      bool ok = true;
+      for (int kb = 0; kb < nk && ok; ++kb) {
+        const int sa = kb % kStagesA, sb = kb % kStagesB;
+        ok = mbar_wait(smem_u32(&full_a[sa]), (kb / kStagesA) & 1) &&
+             mbar_wait(smem_u32(&full_b[sb]), (kb / kStagesB) & 1);
+        if (!ok || s_fail) {
+          ok = false;
+          break;
+        }
+        fence_async_smem();
+        tc_fence_after();
+        const uint32_t ab = a_addr + sa * kABytes;
+        const uint32_t bb = b_addr + sb * kBBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          const uint64_t bd = smem_desc(bb + kk * 32);
+          mma_bf16(tmem, smem_desc(ab + kk * 32), bd, (kb | kk) != 0);
+          if (two)
+            mma_bf16(tmem + kBN, smem_desc(ab + kHalfBytes + kk * 32), bd, (kb | kk) != 0);
+        }
+        mma_commit(smem_u32(&empty_a[sa]));
+        mma_commit(smem_u32(&empty_b[sb]));
+      }
+      if (ok)
+        mma_commit(smem_u32(&acc_full));
+      else
+        s_fail = 1;
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------- B dequantisation (row t)
+    const int t = tid - kDqWarp0 * 32;
+    const uint8_t* blob = (grp < g.E) ? g.experts + (int64_t)grp * g.blob_bytes : g.shared;
+    const BlobOffsets off = blob_offsets(H, I);
+    int64_t row, qo, so, bo;
     if (MODE == 1) {
-      const bool up = r >= kBN / 2;
-      row = (int64_t)nt * (kBN / 2) + (up ? r - kBN / 2 : r);
-      o = which == 0 ? (up ? off.uq : off.gq) : which == 1 ? (up ? off.us : off.gs)
-                                                           : (up ? off.ub : off.gb);
+      const bool up = t >= kBN / 2;
+      row = (int64_t)nt * (kBN / 2) + (up ? t - kBN / 2 : t);
+      qo = up ? off.uq : off.gq;
+      so = up ? off.us : off.gs;
+      bo = up ? off.ub : off.gb;
     } else {
-      row = (int64_t)nt * kBN + r;
-      o = which == 0 ? off.dq : which == 1 ? off.ds : off.db;
+      row = (int64_t)nt * kBN + t;
+      qo = off.dq;
+      so = off.ds;
+      bo = off.db;
     }
-    return which == 0 ? blob + o + row * (K / 2) : blob + o + row * (K / kGroup) * 2;
-  };
-  // this thread's B items: half a code row (16 bytes) plus the row's scale
-  // and bias words (groups kb & ~1 and kb | 1)
-  const int lr = tid >> 1, lh = tid & 1;
-  const uint8_t* qsrc = brow(lr, 0) + lh * 16;
-  const uint8_t* ssrc = brow(lr, 1);
-  const uint8_t* bsrc = brow(lr, 2);
-  const bool two = rows > 128;  // second 128-row half in use
-
-  struct BRegs {
-    uint4 q;
-    uint32_t s, b;
-  };
-  auto load_b = [&](int kb, BRegs& r) {
-    r.q = __ldg(reinterpret_cast<const uint4*>(qsrc + kb * 32));
-    r.s = __ldg(reinterpret_cast<const uint32_t*>(ssrc + (kb & ~1) * 2));
-    r.b = __ldg(reinterpret_cast<const uint32_t*>(bsrc + (kb & ~1) * 2));
-  };
-  auto load_a = [&](int kb) {
-    const uint32_t ab = a_addr + (kb % kStages) * kABytes;
+    const uint8_t* qrow = blob + qo + row * (K / 2);
+    const uint8_t* srow = blob + so + row * (K / kGroup) * 2;
+    const uint8_t* brw = blob + bo + row * (K / kGroup) * 2;
+    auto load_b = [&](int kb, BRegs& r) {
+      r.q0 = __ldg(reinterpret_cast<const uint4*>(qrow + kb * 32));
+      r.q1 = __ldg(reinterpret_cast<const uint4*>(qrow + kb * 32 + 16));
+      r.s = __ldg(reinterpret_cast<const uint32_t*>(srow + (kb & ~1) * 2));
+      r.b = __ldg(reinterpret_cast<const uint32_t*>(brw + (kb & ~1) * 2));
+    };
+    auto dequant = [&](int kb, const BRegs& r) {
+      const uint32_t sh = (kb & 1) ? (r.s >> 16) : (r.s & 0xFFFFu);
+      const uint32_t bh = (kb & 1) ? (r.b >> 16) : (r.b & 0xFFFFu);
+      const uint32_t s2u = sh | (sh << 16), b2u = bh | (bh << 16);
+      const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162*>(&s2u);
+      const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&b2u);
+      const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.0f, 128.0f);
+      const uint32_t words[8] = {r.q0.x, r.q0.y, r.q0.z, r.q0.w, r.q1.x, r.q1.y, r.q1.z, r.q1.w};
+      unsigned char* bb = b_ptr + (kb % kStagesB) * kBBytes;
 #pragma unroll
-    for (int j = 0; j < (kBM * 8) / kThreads; ++j) {
-      const int i = tid + j * kThreads, r = i >> 3, c = i & 7;
-      if (r < 128 || two) {
-        const uint16_t* p = arow_s[r];
-        const uint32_t dst = ab + (r >> 7) * kHalfBytes + swz(r & 127, c);
-        cp_async16(dst, p ? p + kb * kBK + c * 8 : g.a_src, p != nullptr);
+      for (int c = 0; c < 8; ++c) {
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t v = ((words[c] >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
+          const __nv_bfloat162 q = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v), k128);
+          const __nv_bfloat162 w = __hfma2(q, s2, b2);
+          o[i] = *reinterpret_cast<const uint32_t*>(&w);
+        }
+        *reinterpret_cast<uint4*>(bb + swz(t, c)) = make_uint4(o[0], o[1], o[2], o[3]);
       }
-    }
-  };
-  // registers of block kb -> B operand buffer kb % 2 (chunks 4lh..4lh+3 of row lr)
-  auto dequant = [&](int kb, const BRegs& r) {
-    const uint32_t sh = (kb & 1) ? (r.s >> 16) : (r.s & 0xFFFFu);
-    const uint32_t bh = (kb & 1) ? (r.b >> 16) : (r.b & 0xFFFFu);
-    const uint32_t s2u = sh | (sh << 16), b2u = bh | (bh << 16);
-    const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162*>(&s2u);
-    const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&b2u);
-    const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.0f, 128.0f);
-    const uint32_t words[4] = {r.q.x, r.q.y, r.q.z, r.q.w};
-    unsigned char* bb = b_ptr + (kb & 1) * kBBytes;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t o[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t v = ((words[c] >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
-        const __nv_bfloat162 q = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v), k128);
-        const __nv_bfloat162 w = __hfma2(q, s2, b2);
-        o[i] = *reinterpret_cast<const uint32_t*>(&w);
+    };
+    // one B stage: wait until the MMAs of its previous use are done (lane 0,
+    // broadcast), prefetch block kb+3, dequantise block kb, mark the stage full
+    auto step = [&](int kb, const BRegs& cur, BRegs& nxt) -> bool {
+      const int sb = kb % kStagesB, use = kb / kStagesB;
+      int ok = 1;
+      if (lane == 0) {
+        if (use > 0 && !mbar_wait(smem_u32(&empty_b[sb]), (use - 1) & 1)) s_fail = 1;
+        ok = !s_fail;
       }
-      *reinterpret_cast<uint4*>(bb + swz(lr, 4 * lh + c)) = make_uint4(o[0], o[1], o[2], o[3]);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+      if (kb + 3 < nk) load_b(kb + 3, nxt);
+      dequant(kb, cur);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&full_b[sb]));
+      return true;
+    };
+    BRegs r0, r1, r2, r3;  // four named sets in rotation: block kb lives in set kb % 4
+    load_b(0, r0);
+    if (nk > 1) load_b(1, r1);
+    if (nk > 2) load_b(2, r2);
+    for (int kb = 0; kb < nk; kb += 4) {
+      if (!step(kb, r0, r3)) break;
+      if (kb + 1 < nk && !step(kb + 1, r1, r0)) break;
+      if (kb + 2 < nk && !step(kb + 2, r2, r1)) break;
+      if (kb + 3 < nk && !step(kb + 3, r3, r2)) break;
     }
-  };
 
-  // ---- main loop: blocks kb+1, kb+2 load while block kb is dequantised and
-  // block kb-1's MMAs run; buffers of block kb-2 are reused once its MMAs end.
-  bool failed = false;
-  BRegs r0, r1, r2;
-  load_a(0);
-  cp_async_commit();
-  load_b(0, r0);
-  if (nk > 1) {
-    load_a(1);
-    load_b(1, r1);
-  }
-  cp_async_commit();
-  auto iteration = [&](int kb, const BRegs& cur, BRegs& nxt) -> bool {
-    bool ok = true;
-    if (kb >= 2) ok = mbar_wait(smem_u32(&mbar[kb & 1]), ((kb - 2) >> 1) & 1);
-    if (__syncthreads_or(!ok)) return false;
-    tc_fence_after();
-    if (kb + kAhead < nk) {
-      load_a(kb + kAhead);
-      load_b(kb + kAhead, nxt);
+    // ---------------------------------------------------------- epilogue
+    int ok = 1;
+    if (lane == 0) {
+      if (!mbar_wait(smem_u32(&acc_full), 0)) s_fail = 1;
+      ok = !s_fail;
     }
-    cp_async_commit();
-    cp_async_wait<kAhead>();
-    __syncthreads();
-    dequant(kb, cur);
-    fence_async_smem();
-    __syncthreads();
-    if (tid == 0) {
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) {
       tc_fence_after();
-      const uint32_t ab = a_addr + (kb % kStages) * kABytes;
-      const uint32_t bb = b_addr + (kb & 1) * kBBytes;
+      const int q = wid & 3, ch = (wid - kDqWarp0) >> 2;
 #pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk) {
-        const uint64_t bd = smem_desc(bb + kk * 32);
-        mma_bf16(tmem, smem_desc(ab + kk * 32), bd, (kb | kk) != 0);
-        if (two) mma_bf16(tmem + kBN, smem_desc(ab + kHalfBytes + kk * 32), bd, (kb | kk) != 0);
-      }
-      mma_commit(smem_u32(&mbar[kb & 1]));
-    }
-    return true;
-  };
-  int kb = 0;
-  for (; kb < nk; kb += 3) {
-    if (!iteration(kb, r0, r2)) break;
-    if (kb + 1 < nk && !iteration(kb + 1, r1, r0)) {
-      kb += 1;
-      break;
-    }
-    if (kb + 2 < nk && !iteration(kb + 2, r2, r1)) {
-      kb += 2;
-      break;
-    }
-  }
-  failed = kb < nk;
-  // the last block's commit covers every MMA issued before it
-  const int last = failed ? kb - 1 : nk - 1;
-  bool done = true;
-  if (last >= 0) done = mbar_wait(smem_u32(&mbar[last & 1]), (last >> 1) & 1);
-  cp_async_wait<0>();
-  if (__syncthreads_or(!done)) failed = true;
-  tc_fence_after();
-
-  if (!failed) {
-    // 16 warps: TMEM lane quarter q = warp % 4, column quarter cq = warp / 4
-    const int q = wid & 3, cq = wid >> 2;
+      for (int hm = 0; hm < 2; ++hm) {
+        if (hm == 1 && !two) break;
+        const int r = hm * 128 + 32 * q + lane;
+        const uint32_t trow = tmem + hm * kBN + ((uint32_t)(32 * q) << 16);
+        if (MODE == 1) {
 #pragma unroll
-    for (int hm = 0; hm < 2; ++hm) {
-      if (hm == 1 && !two) break;
-      const int r = hm * 128 + 32 * q + lane;
-      const uint32_t trow = tmem + hm * kBN + ((uint32_t)(32 * q) << 16);
-      if (MODE == 1) {
-        float gv[32], uv[32];
-        tmem_ld32(trow + 32 * cq, gv);
-        tmem_ld32(trow + kBN / 2 + 32 * cq, uv);
-        if (r < rows) {
-          uint16_t* dst = g.h_out + (int64_t)(row0 + r) * I + nt * (kBN / 2) + 32 * cq;
+          for (int c = 0; c < 64; c += 32) {
+            float gv[32], uv[32];
+            tmem_ld32(trow + 64 * ch + c, gv);
+            tmem_ld32(trow + kBN / 2 + 64 * ch + c, uv);
+            if (r < rows) {
+              uint16_t* dst = g.h_out + (int64_t)(row0 + r) * I + nt * (kBN / 2) + 64 * ch + c;
 #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            float h[8];
+              for (int e = 0; e < 32; e += 8) {
+                float h[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) h[i] = silu(gv[e + i]) * uv[e + i];
-            *reinterpret_cast<uint4*>(dst + e) =
-                make_uint4(bf2(h[0], h[4]), bf2(h[1], h[5]), bf2(h[2], h[6]), bf2(h[3], h[7]));
+                for (int i = 0; i < 8; ++i) h[i] = silu(gv[e + i]) * uv[e + i];
+                *reinterpret_cast<uint4*>(dst + e) = make_uint4(
+                    bf2(h[0], h[4]), bf2(h[1], h[5]), bf2(h[2], h[6]), bf2(h[3], h[7]));
+              }
+            }
           }
-        }
-      } else {
-        int64_t dst_row = 0;
-        float wgt = 0.0f;
-        if (r < rows) {
-          const int a = g.perm[row0 + r];
-          const int Tk = g.T * g.k;
-          if (a < Tk) {
-            dst_row = (int64_t)(a / g.k) * (g.k + 1) + a % g.k;
-            wgt = g.weights[a];
-          } else {
-            dst_row = (int64_t)(a - Tk) * (g.k + 1) + g.k;
-            wgt = 1.0f;
-          }
-        }
-#pragma unroll
-        for (int c = 0; c < 64; c += 32) {
-          float v[32];
-          tmem_ld32(trow + 64 * cq + c, v);
+        } else {
+          int64_t dst_row = 0;
+          float wgt = 0.0f;
           if (r < rows) {
-            uint16_t* dst = g.y_out + dst_row * H + nt * kBN + 64 * cq + c;
+            const int a = g.perm[row0 + r];
+            const int Tk = g.T * g.k;
+            if (a < Tk) {
+              dst_row = (int64_t)(a / g.k) * (g.k + 1) + a % g.k;
+              wgt = g.weights[a];
+            } else {
+              dst_row = (int64_t)(a - Tk) * (g.k + 1) + g.k;
+              wgt = 1.0f;
+            }
+          }
 #pragma unroll
-            for (int e = 0; e < 32; e += 8)
-              *reinterpret_cast<uint4*>(dst + e) = make_uint4(
-                  bf2(wgt * v[e], wgt * v[e + 1]), bf2(wgt * v[e + 2], wgt * v[e + 3]),
-                  bf2(wgt * v[e + 4], wgt * v[e + 5]), bf2(wgt * v[e + 6], wgt * v[e + 7]));
+          for (int c = 0; c < kBN / 2; c += 32) {
+            float v[32];
+            tmem_ld32(trow + (kBN / 2) * ch + c, v);
+            if (r < rows) {
+              uint16_t* dst = g.y_out + dst_row * H + nt * kBN + (kBN / 2) * ch + c;
+#pragma unroll
+              for (int e = 0; e < 32; e += 8)
+                *reinterpret_cast<uint4*>(dst + e) = make_uint4(
+                    bf2(wgt * v[e], wgt * v[e + 1]), bf2(wgt * v[e + 2], wgt * v[e + 3]),
+                    bf2(wgt * v[e + 4], wgt * v[e + 5]), bf2(wgt * v[e + 6], wgt * v[e + 7]));
+            }
           }
         }
       }
     }
-  } else if (tid == 0 && g.err) {
-    atomicOr(g.err, MOE_DERR_WAIT);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (tid == 0 && s_fail && g.err) atomicOr(g.err, MOE_DERR_WAIT);
   if (wid == 0)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
@@ -420,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(GemmArgs g) {
 
 cudaError_t launch_grouped_gemm(int mode, const GemmArgs& a, int max_tiles, cudaStream_t st) {
   static bool attr_done[2][64] = {};
-  const size_t smem = 1024 + (size_t)kStages * kABytes + 2 * (size_t)kBBytes;
+  const size_t smem = 1024 + (size_t)kStagesA * kABytes + (size_t)kStagesB * kBBytes;
   int d = 0;
   cudaError_t e = cudaGetDevice(&d);
   if (e != cudaSuccess) return e;
