@@ -93,6 +93,95 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const uint16_t* __re
   if (lane == 0) logits[(size_t)t * E + e] = acc;
 }
 
+// Tiled logits for many tokens, same order as router_logits_kernel: CTA =
+// 16 tokens x 16 experts, 8 warps of 4 tokens x 8 experts.  H goes through
+// shared memory in 256-column slices; in slice s lane j owns chunk 32 s + j,
+// so each lane still accumulates chunks j, j+32, ... in ascending order with
+// fma from 0.  The 32 sums of a lane are then combined by a reduce-scatter
+// over the same xor partners 16, 8, 4, 2, 1 (each add pairs the same two
+// lane partials as the butterfly, and fp addition is commutative, so every
+// logit is bit-identical); lane j ends with pair j.  Needs H % 256 == 0.
+constexpr int kTileTok = 16, kTileExp = 16;
+
+__global__ void __launch_bounds__(256) router_logits_tiled_kernel(const uint16_t* __restrict__ x,
+                                                                  const uint16_t* __restrict__ w,
+                                                                  int T, int E, int H,
+                                                                  float* __restrict__ logits) {
+  __shared__ __align__(16) uint4 xs[kTileTok][32];  // 16 rows x 256 bf16
+  __shared__ __align__(16) uint4 ws[kTileExp][32];
+  const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
+  const int t0 = blockIdx.x * kTileTok, e0 = blockIdx.y * kTileExp;
+  const int tw = (wid >> 1) * 4, ew = (wid & 1) * 8;
+  float acc[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+  // staging: 32 rows (16 x, 16 W) x 32 chunks = 1024 uint4, 4 per thread
+  uint4 nx[4];
+  auto fetch = [&](int s) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = tid + 256 * j, row = i >> 5, c = i & 31;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (row < kTileTok) {
+        if (t0 + row < T)
+          v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + row) * H + s * 256) + c);
+      } else if (e0 + row - kTileTok < E) {
+        v = __ldg(reinterpret_cast<const uint4*>(w + (size_t)(e0 + row - kTileTok) * H +
+                                                 s * 256) + c);
+      }
+      nx[j] = v;
+    }
+  };
+  const int ns = H / 256;
+  fetch(0);
+  for (int s = 0; s < ns; ++s) {
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = tid + 256 * j, row = i >> 5, c = i & 31;
+      if (row < kTileTok)
+        xs[row][c] = nx[j];
+      else
+        ws[row - kTileTok][c] = nx[j];
+    }
+    __syncthreads();
+    if (s + 1 < ns) fetch(s + 1);
+    uint4 xv[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) xv[a] = xs[tw + a][lane];
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const uint4 wv = ws[ew + b][lane];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        float& r = acc[a * 8 + b];
+        r = __fmaf_rn(bf_lo(xv[a].x), bf_lo(wv.x), r);
+        r = __fmaf_rn(bf_hi(xv[a].x), bf_hi(wv.x), r);
+        r = __fmaf_rn(bf_lo(xv[a].y), bf_lo(wv.y), r);
+        r = __fmaf_rn(bf_hi(xv[a].y), bf_hi(wv.y), r);
+        r = __fmaf_rn(bf_lo(xv[a].z), bf_lo(wv.z), r);
+        r = __fmaf_rn(bf_hi(xv[a].z), bf_hi(wv.z), r);
+        r = __fmaf_rn(bf_lo(xv[a].w), bf_lo(wv.w), r);
+        r = __fmaf_rn(bf_hi(xv[a].w), bf_hi(wv.w), r);
+      }
+    }
+  }
+  // reduce-scatter: after the step of width d the lane keeps the half of its
+  // values selected by (lane & d); finally lane j holds pair j = a*8 + b
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) {
+#pragma unroll
+    for (int i = 0; i < d; ++i) {
+      const bool upper = lane & d;
+      const float send = upper ? acc[i] : acc[i + d];
+      const float keep = upper ? acc[i + d] : acc[i];
+      acc[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, d));
+    }
+  }
+  const int t = t0 + tw + (lane >> 3), e = e0 + ew + (lane & 7);
+  if (t < T && e < E) logits[(size_t)t * E + e] = acc[0];
+}
+
 constexpr int kSelWarps = 4;
 constexpr int kMaxK = 64;
 
@@ -256,6 +345,11 @@ cudaError_t launch_select(const moe_spec& sp, const float* logits, const float* 
 
 cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* w, int T, int E, int H,
                                  float* logits, cudaStream_t st) {
+  if (H % 256 == 0 && T >= kTileTok) {
+    const dim3 grid((T + kTileTok - 1) / kTileTok, (E + kTileExp - 1) / kTileExp);
+    router_logits_tiled_kernel<<<grid, 256, 0, st>>>(x, w, T, E, H, logits);
+    return cudaGetLastError();
+  }
   const long warps = (long)T * E;
   const int grid = (int)((warps + 3) / 4);
   router_logits_kernel<<<grid, 128, 0, st>>>(x, w, T, E, H, logits);

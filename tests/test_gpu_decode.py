@@ -54,7 +54,7 @@ def _route(spec, xb, wb, bias=None):
 
 @pytest.mark.parametrize("T,E,H,k", [(1, 16, 256, 2), (1, 256, 2048, 8), (8, 256, 2048, 8),
                                      (8, 256, 7168, 8), (5, 20, 320, 3), (3, 1000, 64, 7),
-                                     (64, 64, 512, 4)])
+                                     (64, 64, 512, 4), (37, 40, 512, 5), (512, 256, 2048, 8)])
 def test_softmax_routing_bit_exact(oracle, T, E, H, k):
     rng = np.random.default_rng(T * 1000 + E)
     xb = synth.bf16_bits(rng.normal(0, 2.3, (T, H)))
@@ -87,6 +87,7 @@ def test_softmax_routing_ties(oracle):
 
 
 @pytest.mark.parametrize("T,E,H,ng,G,k,scale", [(1, 256, 7168, 8, 4, 8, 2.5),
+                                                 (40, 256, 7168, 8, 4, 8, 2.5),
                                                  (8, 256, 7168, 8, 4, 8, 2.5),
                                                  (16, 16, 256, 4, 2, 3, 1.0),
                                                  (7, 64, 512, 32, 3, 4, 2.0)])
