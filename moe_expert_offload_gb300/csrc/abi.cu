@@ -161,6 +161,8 @@ int do_ffn(const moe_spec* spec, const moe_cache* c, int32_t layer, const moe_pl
   a.blob_bytes = moe::blob_offsets(a.H, a.I).total;
   a.bank = static_cast<const uint8_t*>(c->bank);
   a.pool = static_cast<const uint8_t*>(c->slot_pool);
+  a.n_bank = spec->num_layers * spec->num_experts;
+  a.n_pool = c->num_slots;
   a.slot_of_id = c->slot_of_id;
   a.uniq = plan->uniq;
   a.counts = plan->counts;

@@ -602,7 +602,9 @@ cudaError_t launch_ffn_decode(const FfnArgs& a, cudaStream_t st) {
   int tok_rows = a.T < kTokA * ntile_a ? a.T : kTokA * ntile_a;
   while (tok_rows > 1 && fixed_a + tok_rows * row_a > 100 * 1024) --tok_rows;
   const size_t sa = fixed_a + tok_rows * row_a;
-  if (ntile_a == 1) {
+  if (a.max_entries <= 128 && ffn_stream_smem(a.H, a.T) != SIZE_MAX) {
+    if ((e = launch_ffn_gate_up_stream(a, nblk, st)) != cudaSuccess) return e;
+  } else if (ntile_a == 1) {
     if ((e = raise_smem(ffn_gate_up_kernel<1>, sa, done_a1)) != cudaSuccess) return e;
     ffn_gate_up_kernel<1><<<grid_a, kWarpsA * 32, sa, st>>>(a, nblk, tok_rows);
   } else {

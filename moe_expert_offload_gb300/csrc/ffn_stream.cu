@@ -1,0 +1,553 @@
+// Decode expert FFN, streaming gate/up phase: the same math as ffn_decode.cu
+// (Edge0 §3.1 "math convention"; int4 affine group-64 weights, register-built
+// (128+q) bf16 fragments into mma.sync m16n8k16, group scale and bias applied
+// to the fp32 accumulator), organised so that HBM never waits on the SMs:
+//
+//  * one persistent CTA per SM owns a contiguous range of (entry, 16-row tile)
+//    units of all executed experts;
+//  * a producer warp streams each unit's gate and up code tiles through a
+//    ring of shared-memory stages with tiled TMA loads (a few 4 KB boxes per
+//    stage, completion counted in bytes on the stage's mbarrier), and the
+//    unit's four scale / bias blocks into a separate buffer with bulk copies;
+//  * each of the eight consumer warps owns a fixed K slice (GPW 64-column
+//    groups of every stage): it stages the activations and converts the
+//    scales of its own slice only, so no CTA-wide barrier sits on the path --
+//    warps meet only at the stage mbarriers;
+//  * the warps' partial sums go to a two-deep ring in shared memory and one
+//    designated warp per unit (rotating) adds them in warp order and writes
+//    h = silu(g) * u: the sum order is fixed, the result deterministic.
+// Every wait is bounded; on a time-out the kernel sets MOE_DERR_WAIT in the
+// plan's error word, the producer still waits (bounded) for the copies it
+// issued, and every warp returns.
+#include <cuda_bf16.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kCW = 8;                     // consumer warps
+constexpr int kSThreads = (kCW + 1) * 32;  // + producer warp (warp kCW)
+constexpr int kTokS = 8;                   // tokens per MMA N tile (one per column)
+constexpr int kRing = 2;                   // partial-sum ring depth
+constexpr int kMaxStages = 8;
+constexpr int kStreamMaxEntries = 128;
+constexpr uint32_t kSpin = 1u << 20;
+constexpr size_t kStreamSmemBudget = 220 * 1024;
+
+__device__ __forceinline__ uint32_t su32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void bar_init(uint32_t a, uint32_t n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ bool bar_wait(uint32_t a, uint32_t parity) {
+  for (uint32_t i = 0; i < kSpin; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+// the whole warp waits; true only if every lane saw the phase complete
+__device__ __forceinline__ bool warp_wait(uint32_t a, uint32_t parity) {
+  return __all_sync(0xffffffffu, bar_wait(a, parity));
+}
+
+__device__ __forceinline__ void bar_arrive(uint32_t a) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}" ::"r"(a)
+               : "memory");
+}
+
+__device__ __forceinline__ void bar_expect(uint32_t a, uint32_t bytes) {
+  asm volatile(
+      "{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}" ::"r"(a),
+      "r"(bytes)
+      : "memory");
+}
+
+// global -> shared bulk copy (16-byte aligned, size a multiple of 16)
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t nib_pair(uint32_t w, int i) {
+  return ((w >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 16 rows x one 64-column group: lo / hi are the lane's 8 code bytes of rows
+// g and g + 8, b the group's 8 B-fragment registers (same k order as
+// ffn_decode.cu: MMA jj takes nibble pairs (i, i+4), (i+1, i+5) of word jj/2).
+__device__ __forceinline__ void group_mma(float (&d)[4], uint2 lo, uint2 hi,
+                                          const uint32_t (&b)[8]) {
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    const uint32_t wl = (jj < 2) ? lo.x : lo.y, wh = (jj < 2) ? hi.x : hi.y;
+    const int i = 2 * (jj & 1);
+    mma16816(d, nib_pair(wl, i), nib_pair(wh, i), nib_pair(wl, i + 1), nib_pair(wh, i + 1),
+             b[2 * jj], b[2 * jj + 1]);
+  }
+}
+
+__device__ __forceinline__ void frag_order(const uint32_t (&w)[8], uint4& o0, uint4& o1) {
+  o0.x = __byte_perm(w[0], w[2], 0x5410);
+  o0.y = __byte_perm(w[0], w[2], 0x7632);
+  o0.z = __byte_perm(w[1], w[3], 0x5410);
+  o0.w = __byte_perm(w[1], w[3], 0x7632);
+  o1.x = __byte_perm(w[4], w[6], 0x5410);
+  o1.y = __byte_perm(w[4], w[6], 0x7632);
+  o1.z = __byte_perm(w[5], w[7], 0x5410);
+  o1.w = __byte_perm(w[5], w[7], 0x7632);
+}
+
+__device__ __forceinline__ float bf(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// Code tiles arrive through a 4-D tensor map per blob array (bank, slot
+// pool, shared expert): u32 words [blob][gate/up][row of I][word of H/8],
+// box = 32 words (128 B) x 16 rows x both matrices = one 4 KB sub-tile,
+// 128-byte swizzled: 16-byte chunk c of line L lands at chunk c ^ (L & 7), so
+// the eight rows a warp reads at once fall in distinct banks.
+struct CodeMaps {
+  CUtensorMap m[3];
+};
+
+// Shared-memory plan of one CTA.  GPW 64-column groups per consumer warp per
+// stage, so a stage spans KC = 8 * GPW * 64 columns of H (KC / 256 sub-tiles);
+// each warp owns gtot = H / 512 groups of a unit (its slice of every stage).
+struct StreamGeom {
+  int gpw, KC, nch, gtot, nsub;
+  int stage;     // bytes: 32 rows (16 gate + 16 up) x KC / 2
+  int nst;       // stages in the ring
+  int tr;        // token rows staged per warp (min(T, 8))
+  int xrow;      // bytes per staged token row of one warp: gtot * 128 + 16
+  size_t o_raw, o_sbt, o_x, o_xsum, o_red, smem;
+};
+
+__host__ __device__ inline StreamGeom stream_geom(int H, int T, int nst) {
+  StreamGeom g;
+  const int ng = H / kGroup;
+  g.gpw = (H % 1024 == 0) ? 2 : 1;
+  g.KC = kCW * g.gpw * kGroup;
+  g.nch = H / g.KC;
+  g.gtot = ng / kCW;
+  g.nsub = g.KC / 256;
+  g.stage = 16 * g.KC;
+  g.tr = T < kTokS ? T : kTokS;
+  g.xrow = g.gtot * 128 + 16;
+  g.nst = nst;
+  g.o_raw = (size_t)nst * g.stage;                       // 4 blocks [16][ng] bf16
+  g.o_sbt = g.o_raw + (size_t)4 * 16 * ng * 2;           // per warp [gtot][32] float2
+  g.o_x = g.o_sbt + (size_t)kCW * g.gtot * 32 * 8;       // per warp [tr][xrow]
+  g.o_xsum = g.o_x + (size_t)kCW * g.tr * g.xrow;        // per warp [gtot][8] fp32
+  g.o_red = g.o_xsum + (size_t)kCW * g.gtot * kTokS * 4; // [ring][warp][32 rows][tr] fp32
+  g.smem = g.o_red + (size_t)kRing * kCW * 32 * g.tr * 4 + 1024;  // + base alignment
+  return g;
+}
+
+// Deepest ring that fits the budget (0 if not even two stages fit).
+inline StreamGeom stream_plan(int H, int T) {
+  StreamGeom g = stream_geom(H, T, 0);
+  int nst = (int)((kStreamSmemBudget - (g.smem < kStreamSmemBudget ? g.smem : kStreamSmemBudget)) /
+                  g.stage);
+  if (nst > kMaxStages) nst = kMaxStages;
+  if (nst < 2) nst = 0;
+  return stream_geom(H, T, nst);
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, int w, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+template <int GPW>
+__global__ void __launch_bounds__(kSThreads, 1)
+    ffn_gate_up_stream_kernel(FfnArgs a, int n_tick, StreamGeom geo,
+                              const __grid_constant__ CodeMaps maps) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages], sfull, sempty;
+  __shared__ __align__(8) uint64_t rfull[kRing], rfree[kRing];
+  __shared__ const uint8_t* sblob[kStreamMaxEntries];
+  __shared__ int smap[kStreamMaxEntries], sbi[kStreamMaxEntries];
+  __shared__ int wtok[kCW][kTokS];
+  __shared__ int s_fail;
+  const int H = a.H, I = a.I, ng = H / kGroup;
+  const int nst = geo.nst, nch = geo.nch, gtot = geo.gtot;
+  // swizzled tiles need a 1024-byte aligned base
+  unsigned char* smem = smem_raw + ((1024u - (su32(smem_raw) & 1023u)) & 1023u);
+  constexpr int G = kCW * GPW;  // groups per stage
+  const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int i = 0; i < nst; ++i) {
+      bar_init(su32(&full[i]), 1);
+      bar_init(su32(&empty[i]), kCW);
+    }
+    bar_init(su32(&sfull), 1);
+    bar_init(su32(&sempty), kCW);
+    for (int i = 0; i < kRing; ++i) {
+      bar_init(su32(&rfull[i]), kCW);
+      bar_init(su32(&rfree[i]), 1);
+    }
+    s_fail = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (blockIdx.x == 0)
+    for (int i = tid; i < n_tick; i += blockDim.x) a.tick[i] = 0u;
+  const int n_uniq = a.counts[0];
+  const int n_exec = n_uniq + a.has_shared;
+  if (wid == kCW) {
+    if (lane < 3) tma_prefetch_map(&maps.m[lane]);
+    for (int r = lane; r < n_exec; r += 32) {
+      // blob pointer (scale copies) and (tensor map, blob index) of entry r
+      int mi = 2, bi = 0;
+      if (r < n_uniq) {
+        const int32_t id = a.uniq[r];
+        const int32_t slot = a.slot_of_id[id];
+        mi = slot >= 0 ? 1 : 0;
+        bi = slot >= 0 ? slot : id;
+      }
+      smap[r] = mi;
+      sbi[r] = bi;
+      sblob[r] = (mi == 2 ? a.shared : mi == 1 ? a.pool : a.bank) + (int64_t)bi * a.blob_bytes;
+    }
+  }
+  __syncthreads();
+
+  const int tpe = I / 16;
+  const int n_units = n_exec * tpe;
+  const int u_lo = (int)((int64_t)blockIdx.x * n_units / gridDim.x);
+  const int u_hi = (int)((int64_t)(blockIdx.x + 1) * n_units / gridDim.x);
+  const BlobOffsets off = blob_offsets(H, I);
+  unsigned char* stages = smem;
+  unsigned char* sraw = smem + geo.o_raw;
+  const int sblk = 16 * ng * 2;
+
+  if (wid == kCW) {
+    // -------------------------------------------------------- producer
+    int s = 0, rnd = 0, nq = 0, nu = 0;
+    bool ok = true;
+    for (int u = u_lo; ok && u < u_hi; ++u) {
+      const int i = u - u_lo;
+      const uint8_t* blob = sblob[u / tpe];
+      const CUtensorMap* map = &maps.m[smap[u / tpe]];
+      const int bidx = sbi[u / tpe];
+      const int row0 = (u % tpe) * 16;
+      // scales: single buffer, refilled once every warp converted the last unit
+      if (lane == 0) {
+        ok = i == 0 || bar_wait(su32(&sempty), (i - 1) & 1);
+        if (ok) bar_expect(su32(&sfull), 4 * sblk);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      ++nu;
+      if (lane < 4) {
+        const int64_t so = lane == 0 ? off.gs : lane == 1 ? off.gb : lane == 2 ? off.us : off.ub;
+        bulk_g2s(su32(sraw + lane * sblk), blob + so + (int64_t)row0 * ng * 2, sblk,
+                 su32(&sfull));
+      }
+      for (int kc = 0; kc < nch; ++kc) {
+        if (lane == 0) {
+          ok = rnd == 0 || bar_wait(su32(&empty[s]), (rnd - 1) & 1);
+          if (ok) bar_expect(su32(&full[s]), geo.stage);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        // sub-tile c: words [kc * KC/8 + 32c, +32) of the 16 gate and 16 up rows
+        if (lane < geo.nsub)
+          tma_load_4d(su32(stages + s * geo.stage + lane * 4096), map,
+                      kc * (geo.KC / 8) + 32 * lane, row0, 0, bidx, su32(&full[s]));
+        ++nq;
+        if (++s == nst) {
+          s = 0;
+          ++rnd;
+        }
+      }
+    }
+    // wait (bounded) until every copy this warp issued has landed
+    if (lane < nst) {
+      const int uses = nq > lane ? (nq - lane + nst - 1) / nst : 0;
+      if (uses > 0 && !bar_wait(su32(&full[lane]), (uses - 1) & 1)) ok = false;
+    }
+    if (lane == 31 && nu > 0 && !bar_wait(su32(&sfull), (nu - 1) & 1)) ok = false;
+    if (!__all_sync(0xffffffffu, ok)) s_fail = 1;
+    if (lane == 0 && s_fail && a.err) atomicOr(a.err, MOE_DERR_WAIT);
+    return;
+  }
+
+  // ---------------------------------------------------------- consumers
+  const int w = wid, gid = lane >> 2, t4 = lane & 3;
+  float2* sbt = reinterpret_cast<float2*>(smem + geo.o_sbt) + (size_t)w * gtot * 32;
+  unsigned char* xw = smem + geo.o_x + (size_t)w * geo.tr * geo.xrow;
+  float* xsum = reinterpret_cast<float*>(smem + geo.o_xsum) + (size_t)w * gtot * kTokS;
+  float* red = reinterpret_cast<float*>(smem + geo.o_red);
+  const int tr = geo.tr;
+  const uint16_t* raw = reinterpret_cast<const uint16_t*>(sraw);
+  int prev_r = -1, ntok = 0, s = 0, rnd = 0;
+  bool ok = true;
+  for (int u = u_lo; ok && u < u_hi; ++u) {
+    const int i = u - u_lo, r = u / tpe, row0 = (u % tpe) * 16;
+    if (r != prev_r) {
+      // tokens routed to entry r (ascending; this warp's own copy of the list)
+      int cnt;
+      if (r < n_uniq) {
+        const int32_t id = a.uniq[r];
+        const int base = a.layer * a.E, n = a.T * a.k;
+        cnt = 0;
+        for (int n0 = 0; n0 < n; n0 += 32) {
+          const int ii = n0 + lane;
+          bool mt = ii < n && base + a.ids[ii] == id;
+          // a token listing the id twice is staged once (h is per token)
+          for (int jj = mt ? ii - ii % a.k : ii; jj < ii; ++jj)
+            if (base + a.ids[jj] == id) mt = false;
+          const unsigned b = __ballot_sync(0xffffffffu, mt);
+          const int pos = cnt + __popc(b & ((1u << lane) - 1u));
+          if (mt && pos < kTokS) wtok[w][pos] = ii / a.k;
+          cnt += __popc(b);
+        }
+      } else {
+        if (lane < a.T && lane < kTokS) wtok[w][lane] = lane;
+        cnt = a.T;
+      }
+      ntok = cnt < tr ? cnt : tr;
+      __syncwarp();
+      // x of those tokens on this warp's groups, in fragment order, + group sums
+      const int per_tok = gtot * 4;
+      const int n_items = ntok * per_tok;
+      for (int it0 = 0; it0 < n_items; it0 += 32) {
+        const int it = it0 + lane;
+        const bool in = it < n_items;
+        const int n = in ? it / per_tok : 0, rem = it - n * per_tok, gi = rem >> 2, qq = rem & 3;
+        const int g = (gi / GPW) * G + w * GPW + (gi % GPW);
+        uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
+        float sx = 0.0f;
+        if (in) {
+          const uint4* px =
+              reinterpret_cast<const uint4*>(a.x + (int64_t)wtok[w][n] * H + g * 64 + qq * 16);
+          const uint4 v0 = __ldg(px), v1 = __ldg(px + 1);
+          const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            sx += __uint_as_float(wv[j] << 16) + __uint_as_float(wv[j] & 0xFFFF0000u);
+          frag_order(wv, o0, o1);
+        }
+        sx += __shfl_xor_sync(0xffffffffu, sx, 1);
+        sx += __shfl_xor_sync(0xffffffffu, sx, 2);
+        if (in) {
+          uint4* d = reinterpret_cast<uint4*>(xw + (size_t)n * geo.xrow + gi * 128 + qq * 32);
+          d[0] = o0;
+          d[1] = o1;
+          if (qq == 0) xsum[gi * kTokS + n] = sx;
+        }
+      }
+      __syncwarp();
+      prev_r = r;
+    }
+
+    // this warp's groups of the unit's scales -> (s, b - 128 s), lane = row
+    if (!warp_wait(su32(&sfull), i & 1)) {
+      ok = false;
+      break;
+    }
+    {
+      const int m = lane >> 4, row = lane & 15;
+      const uint16_t* rs = raw + (2 * m) * 16 * ng + row * ng;
+      const uint16_t* rb = raw + (2 * m + 1) * 16 * ng + row * ng;
+      for (int kc = 0; kc < nch; ++kc) {
+#pragma unroll
+        for (int j = 0; j < GPW; ++j) {
+          const int g = kc * G + w * GPW + j;
+          const float sv = bf(rs[g]);
+          sbt[(kc * GPW + j) * 32 + lane] = make_float2(sv, fmaf(-128.0f, sv, bf(rb[g])));
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) bar_arrive(su32(&sempty));
+
+    float acc[2][4];
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[m][e] = 0.0f;
+    const unsigned char* xg = xw + (size_t)gid * geo.xrow + t4 * 32;
+    const bool has_tok = gid < ntok;
+    for (int kc = 0; kc < nch; ++kc) {
+      if (!warp_wait(su32(&full[s]), rnd & 1)) {
+        ok = false;
+        break;
+      }
+      const unsigned char* st = stages + s * geo.stage + gid * 128 + (t4 & 1) * 8;
+#pragma unroll
+      for (int j = 0; j < GPW; ++j) {
+        const int gl = w * GPW + j, gi = kc * GPW + j;
+        // group gl = 32 bytes of sub-tile gl / 4; the lane's 8 bytes sit in
+        // 16-byte chunk 2 (gl % 4) + t4 / 2, swizzled by the row (gid)
+        const unsigned char* cg =
+            st + (gl >> 2) * 4096 + ((((gl & 3) << 1) | (t4 >> 1)) ^ gid) * 16;
+        const uint2 g0 = *reinterpret_cast<const uint2*>(cg);
+        const uint2 g1 = *reinterpret_cast<const uint2*>(cg + 8 * 128);
+        const uint2 u0 = *reinterpret_cast<const uint2*>(cg + 16 * 128);
+        const uint2 u1 = *reinterpret_cast<const uint2*>(cg + 24 * 128);
+        uint32_t bfr[8];
+        if (has_tok) {
+          const uint4* px = reinterpret_cast<const uint4*>(xg + gi * 128);
+          const uint4 v0 = px[0], v1 = px[1];
+          bfr[0] = v0.x; bfr[1] = v0.y; bfr[2] = v0.z; bfr[3] = v0.w;
+          bfr[4] = v1.x; bfr[5] = v1.y; bfr[6] = v1.z; bfr[7] = v1.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) bfr[e] = 0u;
+        }
+        float dg[4] = {0.f, 0.f, 0.f, 0.f}, du[4] = {0.f, 0.f, 0.f, 0.f};
+        group_mma(dg, g0, g1, bfr);
+        group_mma(du, u0, u1, bfr);
+        const float2 X = *reinterpret_cast<const float2*>(xsum + gi * kTokS + 2 * t4);
+        const float2* sb = sbt + gi * 32;
+        const float2 sg0 = sb[gid], sg1 = sb[8 + gid], su0 = sb[16 + gid], su1 = sb[24 + gid];
+        acc[0][0] = fmaf(sg0.x, dg[0], fmaf(sg0.y, X.x, acc[0][0]));
+        acc[0][1] = fmaf(sg0.x, dg[1], fmaf(sg0.y, X.y, acc[0][1]));
+        acc[0][2] = fmaf(sg1.x, dg[2], fmaf(sg1.y, X.x, acc[0][2]));
+        acc[0][3] = fmaf(sg1.x, dg[3], fmaf(sg1.y, X.y, acc[0][3]));
+        acc[1][0] = fmaf(su0.x, du[0], fmaf(su0.y, X.x, acc[1][0]));
+        acc[1][1] = fmaf(su0.x, du[1], fmaf(su0.y, X.y, acc[1][1]));
+        acc[1][2] = fmaf(su1.x, du[2], fmaf(su1.y, X.x, acc[1][2]));
+        acc[1][3] = fmaf(su1.x, du[3], fmaf(su1.y, X.y, acc[1][3]));
+      }
+      __syncwarp();
+      if (lane == 0) bar_arrive(su32(&empty[s]));
+      if (++s == nst) {
+        s = 0;
+        ++rnd;
+      }
+    }
+    if (!ok) break;
+
+    // partial sums -> ring slot p; the unit's designated warp adds them
+    const int p = i % kRing, pr = i / kRing;
+    if (pr > 0 && !warp_wait(su32(&rfree[p]), (pr - 1) & 1)) {
+      ok = false;
+      break;
+    }
+    float* rp = red + (size_t)p * kCW * 32 * tr;
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int row = m * 16 + gid + 8 * (e >> 1), n = 2 * t4 + (e & 1);
+        if (n < ntok) rp[((size_t)w * 32 + row) * tr + n] = acc[m][e];
+      }
+    __syncwarp();
+    if (lane == 0) bar_arrive(su32(&rfull[p]));
+    if (w == i % kCW) {
+      if (!warp_wait(su32(&rfull[p]), pr & 1)) {
+        ok = false;
+        break;
+      }
+      for (int it = lane; it < 16 * ntok; it += 32) {
+        const int row = it / ntok, n = it - row * ntok;
+        float gs = 0.0f, us = 0.0f;
+#pragma unroll
+        for (int ww = 0; ww < kCW; ++ww) {
+          gs += rp[((size_t)ww * 32 + row) * tr + n];
+          us += rp[((size_t)ww * 32 + 16 + row) * tr + n];
+        }
+        const float silu = gs / (1.0f + __expf(-gs));
+        a.h[((int64_t)r * a.T + wtok[w][n]) * I + row0 + row] = silu * us;
+      }
+      __syncwarp();
+      if (lane == 0) bar_arrive(su32(&rfree[p]));
+    }
+  }
+  if (!ok && lane == 0) {
+    s_fail = 1;
+    if (a.err) atomicOr(a.err, MOE_DERR_WAIT);
+  }
+}
+
+}  // namespace
+
+size_t ffn_stream_smem(int H, int T) {
+  if (H % 512 != 0 || T < 1 || T > kTokS) return SIZE_MAX;
+  const StreamGeom g = stream_plan(H, T);
+  return g.nst ? g.smem : SIZE_MAX;
+}
+
+cudaError_t launch_ffn_gate_up_stream(const FfnArgs& a, int n_tick, cudaStream_t st) {
+  static size_t done1[64], done2[64];
+  static int sms[64];
+  if (a.max_entries > kStreamMaxEntries) return cudaErrorInvalidValue;
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) return e;
+  if (d < 0 || d >= 64) return cudaErrorInvalidDevice;
+  if (!sms[d]) {
+    e = cudaDeviceGetAttribute(&sms[d], cudaDevAttrMultiProcessorCount, d);
+    if (e != cudaSuccess) return e;
+  }
+  const StreamGeom geo = stream_plan(a.H, a.T);
+  if (!geo.nst) return cudaErrorInvalidValue;
+  // gate and up code matrices of every blob: [blob][matrix][row][word]
+  CodeMaps maps;
+  const uint64_t strides[3] = {(uint64_t)a.H / 2, (uint64_t)a.I * a.H / 2,
+                               (uint64_t)a.blob_bytes};
+  const uint32_t box[4] = {32, 16, 2, 1};
+  const uint8_t* bases[3] = {a.bank, a.pool, a.shared ? a.shared : a.bank};
+  const int nblob[3] = {a.n_bank, a.n_pool, a.shared ? 1 : a.n_bank};
+  for (int i = 0; i < 3; ++i) {
+    const uint64_t dims[4] = {(uint64_t)a.H / 8, (uint64_t)a.I, 2, (uint64_t)nblob[i]};
+    if ((e = encode_tiled_u32(&maps.m[i], bases[i], 4, dims, strides, box)) != cudaSuccess)
+      return e;
+  }
+  const int units = a.max_entries * (a.I / 16);
+  const int grid = units < sms[d] ? units : sms[d];
+  if (geo.gpw == 2) {
+    if (done2[d] < geo.smem) {
+      e = cudaFuncSetAttribute(ffn_gate_up_stream_kernel<2>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.smem);
+      if (e != cudaSuccess) return e;
+      done2[d] = geo.smem;
+    }
+    ffn_gate_up_stream_kernel<2><<<grid, kSThreads, geo.smem, st>>>(a, n_tick, geo, maps);
+  } else {
+    if (done1[d] < geo.smem) {
+      e = cudaFuncSetAttribute(ffn_gate_up_stream_kernel<1>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.smem);
+      if (e != cudaSuccess) return e;
+      done1[d] = geo.smem;
+    }
+    ffn_gate_up_stream_kernel<1><<<grid, kSThreads, geo.smem, st>>>(a, n_tick, geo, maps);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

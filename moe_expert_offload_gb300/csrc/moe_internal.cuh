@@ -1,6 +1,7 @@
 // Internal declarations of libmoe (not part of the C ABI).
 #pragma once
 
+#include <cuda.h>  // CUtensorMap and its enums (types only)
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -35,6 +36,12 @@ __host__ __device__ inline BlobOffsets blob_offsets(int64_t H, int64_t I) {
   o.total = ((o.db + sd) + 255) / 256 * 256;
   return o;
 }
+
+// Tiled TMA descriptor over u32 elements, 128-byte swizzle, rank <= 5:
+// dims[0] innermost, strides[i] = bytes between consecutive indices of
+// dimension i + 1.  Returns cudaErrorNotSupported without a driver encoder.
+cudaError_t encode_tiled_u32(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                             const uint64_t* strides, const uint32_t* box);
 
 // ---------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error.
@@ -74,10 +81,16 @@ struct FfnArgs {
   uint32_t* tick;   // [H / rows per down block] arrival counters
   float* y;         // [T][H]
   int max_entries;
+  int n_bank;       // blobs in the bank (num_layers * E)
+  int n_pool;       // slots in the pool
 };
 size_t ffn_workspace_bytes(int H, int I, int k, int T, int has_shared);
 void ffn_carve_workspace(FfnArgs& a, void* ws);
 cudaError_t launch_ffn_decode(const FfnArgs& a, cudaStream_t st);
+// streaming gate/up phase (T <= 8, H % 256 == 0): persistent CTAs fed by
+// cp.async.bulk stages
+cudaError_t launch_ffn_gate_up_stream(const FfnArgs& a, int n_tick, cudaStream_t st);
+size_t ffn_stream_smem(int H, int T);
 
 // ------------------------------------------------------------------ prefill
 constexpr int kPrefillTileRows = 256;  // rows of one grouped-GEMM m-tile

@@ -377,3 +377,30 @@ def test_full_size_deepseek_shape_decode(oracle, T):
     _tables_equal(cache, ost)
     del bank, cache
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("H,I,T", [(1024, 256, 4), (1536, 128, 3), (512, 192, 12)])
+def test_expert_ffn_repeated_ids(oracle, H, I, T):
+    """Routing given by the caller in which one token lists an expert twice and
+    several tokens share experts: each (token, rank) pair contributes once."""
+    E, k = 8, 3
+    spec, bank, bank_h, cache, _ = _layer_rig(1, H, I, E, k, 2, 2, 11800, 47500, False, seed=I)
+    rng = np.random.default_rng(H + T)
+    ids_h = rng.integers(0, E, (T, k)).astype(np.int32)
+    ids_h[0] = [5, 5, 2]
+    ids_h[1, 0] = 5
+    w_h = rng.uniform(0.1, 1.0, (T, k)).astype(np.float32)
+    xb = synth.bf16_bits(rng.normal(0, 1, (T, H)))
+    plan = m.DevicePlan(T * k, 2, device=DEV)
+    fws = m.moe_ffn_workspace_bytes(spec, T)
+    ws = torch.empty(fws, dtype=torch.uint8, device=DEV)
+    y = torch.empty((T, H), dtype=torch.float32, device=DEV)
+    ids = dev(ids_h, DEV)
+    for step in range(2):  # second pass runs with the slots filled by the first
+        m.moe_cache_step(spec, cache.c, 0, ids, T, plan.c, 1)
+        m.moe_expert_ffn(spec, cache.c, 0, plan.c, dev_bits(xb, DEV), T, ids, dev(w_h, DEV), None,
+                         ws, fws, y)
+        torch.cuda.synchronize()
+        assert plan.read(2)["err"] == 0
+        ref = oracle.moe_ffn(list(bank_h[:E]), H, I, xb, ids_h, w_h)
+        assert_ffn_close(y.cpu().numpy(), ref, f"step {step}")
