@@ -573,8 +573,8 @@ cudaError_t raise_smem(Kern kernel, size_t bytes, size_t (&done)[64]) {
 size_t ffn_workspace_bytes(int H, int I, int k, int T, int has_shared) {
   auto al = [](size_t b) { return (b + 255) / 256 * 256; };
   const size_t max_entries = (size_t)T * k + has_shared;
-  const size_t nblk = (H + kRowsBlkB - 1) / kRowsBlkB;
-  return al(max_entries * T * I * 4) + al((size_t)T * (k + has_shared) * H * 4) + al(nblk * 4);
+  const size_t ntick = (H + 15) / 16;  // one arrival counter per 16-row tile of H
+  return al(max_entries * T * I * 4) + al((size_t)T * (k + has_shared) * H * 4) + al(ntick * 4);
 }
 
 void ffn_carve_workspace(FfnArgs& a, void* ws) {
@@ -602,17 +602,20 @@ cudaError_t launch_ffn_decode(const FfnArgs& a, cudaStream_t st) {
   int tok_rows = a.T < kTokA * ntile_a ? a.T : kTokA * ntile_a;
   while (tok_rows > 1 && fixed_a + tok_rows * row_a > 100 * 1024) --tok_rows;
   const size_t sa = fixed_a + tok_rows * row_a;
+  const int ntick = (a.H + 15) / 16;
   if (a.max_entries <= 128 && ffn_stream_smem(a.H, a.T) != SIZE_MAX) {
-    if ((e = launch_ffn_gate_up_stream(a, nblk, st)) != cudaSuccess) return e;
+    if ((e = launch_ffn_gate_up_stream(a, ntick, st)) != cudaSuccess) return e;
   } else if (ntile_a == 1) {
     if ((e = raise_smem(ffn_gate_up_kernel<1>, sa, done_a1)) != cudaSuccess) return e;
-    ffn_gate_up_kernel<1><<<grid_a, kWarpsA * 32, sa, st>>>(a, nblk, tok_rows);
+    ffn_gate_up_kernel<1><<<grid_a, kWarpsA * 32, sa, st>>>(a, ntick, tok_rows);
   } else {
     if ((e = raise_smem(ffn_gate_up_kernel<2>, sa, done_a2)) != cudaSuccess) return e;
-    ffn_gate_up_kernel<2><<<grid_a, kWarpsA * 32, sa, st>>>(a, nblk, tok_rows);
+    ffn_gate_up_kernel<2><<<grid_a, kWarpsA * 32, sa, st>>>(a, ntick, tok_rows);
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (a.T <= kTokB) {
+  if (a.max_entries <= 128 && ffn_down_stream_smem(a.H, a.I, a.T) != SIZE_MAX) {
+    return launch_ffn_down_stream(a, st);
+  } else if (a.T <= kTokB) {
     const size_t sb = smem_b(a.I, 1);
     if ((e = raise_smem(ffn_down_kernel<1>, sb, done_b1)) != cudaSuccess) return e;
     ffn_down_kernel<1><<<grid_b, kWarpsB * 32, sb, st>>>(a);

@@ -242,6 +242,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
     }
   }
   __syncthreads();
+  // the down kernel may now take SMs as this grid's CTAs retire
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int tpe = I / 16;
   const int n_units = n_exec * tpe;
@@ -494,6 +496,375 @@ __global__ void __launch_bounds__(kSThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------ phase B
+// Down projection, streamed the same way.  Unit = (entry, 128 output rows);
+// warp w owns rows 16w..16w+15 over the whole K = I, so a unit needs no
+// cross-warp sum.  A stage is one 128-row x 256-column tile of Wd codes (a
+// 16 KB TMA box of a 3-D map [blob][row of H][word of I/8], 128-byte
+// swizzled).  The B operand is h of the entry's tokens, each fp32 value split
+// into a bf16 hi / lo column pair (~2^-17 relative), four tokens per MMA.
+// Each warp writes  w[t][j] * (Wd h)  into partial[t][j][rows]; the last entry
+// to finish a 16-row tile (arrival counter) adds partial[t][0..k] in j order
+// into y.  The kernel is launched as a programmatic dependent of the gate/up
+// kernel: its producer starts streaming weights while that kernel drains and
+// its consumers wait for it (griddepcontrol.wait) before reading h.
+constexpr int kTokB = 4;     // tokens per MMA N tile (hi / lo column pairs)
+constexpr int kRowsB = 128;  // output rows per unit (kCW warps x 16)
+constexpr int kStageB = kRowsB * 128;
+
+struct DownGeom {
+  int ngi, nch;  // 64-column groups of I, stages per unit (I / 256)
+  int nst;
+  int tr;        // distinct tokens staged (min(T, 8))
+  int hrow;      // bytes per staged h row (one bf16 half of one token): 2 I + 16
+  size_t o_raw, o_sbt, o_h, o_hsum, smem;
+};
+
+__host__ __device__ inline DownGeom down_geom(int I, int T, int nst) {
+  DownGeom g;
+  g.ngi = I / kGroup;
+  g.nch = I / 256;
+  g.nst = nst;
+  g.tr = T < kTokS ? T : kTokS;
+  const int nt = (g.tr + kTokB - 1) / kTokB;
+  g.hrow = 2 * I + 16;
+  g.o_raw = (size_t)nst * kStageB;                      // ds, db blocks [128][ngi] bf16
+  g.o_sbt = g.o_raw + (size_t)2 * kRowsB * g.ngi * 2;   // per warp [16][ngi + 1] float2
+  g.o_h = g.o_sbt + (size_t)kCW * 16 * (g.ngi + 1) * 8; // [8 nt][hrow]
+  g.o_hsum = g.o_h + (size_t)8 * nt * g.hrow;           // [ngi][4 nt] fp32
+  g.smem = g.o_hsum + (size_t)g.ngi * kTokB * nt * 4 + 1024;
+  return g;
+}
+
+inline DownGeom down_plan(int I, int T) {
+  DownGeom g = down_geom(I, T, 0);
+  int nst = (int)((kStreamSmemBudget - (g.smem < kStreamSmemBudget ? g.smem : kStreamSmemBudget)) /
+                  kStageB);
+  if (nst > kMaxStages) nst = kMaxStages;
+  if (nst < 2) nst = 0;
+  return down_geom(I, T, nst);
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void load_frag(const unsigned char* p, bool valid, uint32_t (&b)[8]) {
+  if (valid) {
+    const uint4 v0 = reinterpret_cast<const uint4*>(p)[0];
+    const uint4 v1 = reinterpret_cast<const uint4*>(p)[1];
+    b[0] = v0.x; b[1] = v0.y; b[2] = v0.z; b[3] = v0.w;
+    b[4] = v1.x; b[5] = v1.y; b[6] = v1.z; b[7] = v1.w;
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) b[e] = 0u;
+  }
+}
+
+// named barrier over the consumer warps only
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kCW * 32) : "memory");
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kSThreads, 1)
+    ffn_down_stream_kernel(FfnArgs a, DownGeom geo, const __grid_constant__ CodeMaps maps) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages], sfull, sempty;
+  __shared__ const uint8_t* sblob[kStreamMaxEntries];
+  __shared__ int smap[kStreamMaxEntries], sbi[kStreamMaxEntries];
+  __shared__ int utok[kTokS], s_ntok;
+  constexpr int NTOK = kTokB * NT;
+  const int H = a.H, I = a.I, ngi = geo.ngi, nst = geo.nst, nch = geo.nch;
+  unsigned char* smem = smem_raw + ((1024u - (su32(smem_raw) & 1023u)) & 1023u);
+  const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int i = 0; i < nst; ++i) {
+      bar_init(su32(&full[i]), 1);
+      bar_init(su32(&empty[i]), kCW);
+    }
+    bar_init(su32(&sfull), 1);
+    bar_init(su32(&sempty), kCW);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // the routing plan is complete before the gate/up kernel starts; only h
+  // (and the arrival counters it resets) need that kernel to finish
+  const int n_uniq = a.counts[0];
+  const int n_exec = n_uniq + a.has_shared;
+  if (wid == kCW) {
+    if (lane < 3) tma_prefetch_map(&maps.m[lane]);
+    for (int r = lane; r < n_exec; r += 32) {
+      int mi = 2, bi = 0;
+      if (r < n_uniq) {
+        const int32_t id = a.uniq[r];
+        const int32_t slot = a.slot_of_id[id];
+        mi = slot >= 0 ? 1 : 0;
+        bi = slot >= 0 ? slot : id;
+      }
+      smap[r] = mi;
+      sbi[r] = bi;
+      sblob[r] = (mi == 2 ? a.shared : mi == 1 ? a.pool : a.bank) + (int64_t)bi * a.blob_bytes;
+    }
+  }
+  __syncthreads();
+
+  const int upe = H / kRowsB;
+  const int n_units = n_exec * upe;
+  const int u_lo = (int)((int64_t)blockIdx.x * n_units / gridDim.x);
+  const int u_hi = (int)((int64_t)(blockIdx.x + 1) * n_units / gridDim.x);
+  const BlobOffsets off = blob_offsets(H, I);
+  unsigned char* stages = smem;
+  unsigned char* sraw = smem + geo.o_raw;
+  const int rblk = kRowsB * ngi * 2;
+
+  if (wid == kCW) {
+    // -------------------------------------------------------- producer
+    int s = 0, rnd = 0, nq = 0, nu = 0;
+    bool ok = true;
+    for (int u = u_lo; ok && u < u_hi; ++u) {
+      const int i = u - u_lo, r = u / upe, o0 = (u % upe) * kRowsB;
+      const uint8_t* blob = sblob[r];
+      const CUtensorMap* map = &maps.m[smap[r]];
+      if (lane == 0) {
+        ok = i == 0 || bar_wait(su32(&sempty), (i - 1) & 1);
+        if (ok) bar_expect(su32(&sfull), 2 * rblk);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      ++nu;
+      if (lane < 2)
+        bulk_g2s(su32(sraw + lane * rblk), blob + (lane ? off.db : off.ds) + (int64_t)o0 * ngi * 2,
+                 rblk, su32(&sfull));
+      for (int kc = 0; kc < nch; ++kc) {
+        if (lane == 0) {
+          ok = rnd == 0 || bar_wait(su32(&empty[s]), (rnd - 1) & 1);
+          if (ok) {
+            bar_expect(su32(&full[s]), kStageB);
+            tma_load_3d(su32(stages + s * kStageB), map, kc * 32, o0, sbi[r], su32(&full[s]));
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        ++nq;
+        if (++s == nst) {
+          s = 0;
+          ++rnd;
+        }
+      }
+    }
+    if (lane < nst) {
+      const int uses = nq > lane ? (nq - lane + nst - 1) / nst : 0;
+      if (uses > 0 && !bar_wait(su32(&full[lane]), (uses - 1) & 1)) ok = false;
+    }
+    if (lane == 31 && nu > 0 && !bar_wait(su32(&sfull), (nu - 1) & 1)) ok = false;
+    if (!__all_sync(0xffffffffu, ok) && lane == 0 && a.err) atomicOr(a.err, MOE_DERR_WAIT);
+    return;
+  }
+
+  // ---------------------------------------------------------- consumers
+  // h is written by the gate/up kernel: wait for it to complete
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int w = wid, gid = lane >> 2, t4 = lane & 3;
+  const int ctid = tid;  // 0 .. kCW * 32 - 1
+  float2* sbt = reinterpret_cast<float2*>(smem + geo.o_sbt) + (size_t)w * 16 * (ngi + 1);
+  unsigned char* hf = smem + geo.o_h;
+  float* hsum = reinterpret_cast<float*>(smem + geo.o_hsum);
+  const uint16_t* raw = reinterpret_cast<const uint16_t*>(sraw);
+  const int nslot = a.k + a.has_shared, hrow = geo.hrow;
+  int prev_r = -1, ntok = 0, s = 0, rnd = 0;
+  bool ok = true;  // after a failed wait the warp keeps walking the loop (no waits,
+                   // no math) so that every consumer warp meets the same barriers
+  for (int u = u_lo; u < u_hi; ++u) {
+    const int i = u - u_lo, r = u / upe, o0 = (u % upe) * kRowsB;
+    if (r != prev_r) {
+      consumers_sync();  // every warp is done with the previous entry's h
+      if (w == 0) {
+        // distinct tokens routed to entry r, ascending
+        int cnt;
+        if (r < n_uniq) {
+          const int32_t id = a.uniq[r];
+          const int base = a.layer * a.E, n = a.T * a.k;
+          cnt = 0;
+          for (int n0 = 0; n0 < n; n0 += 32) {
+            const int ii = n0 + lane;
+            bool mt = ii < n && base + a.ids[ii] == id;
+            for (int jj = mt ? ii - ii % a.k : ii; jj < ii; ++jj)
+              if (base + a.ids[jj] == id) mt = false;
+            const unsigned b = __ballot_sync(0xffffffffu, mt);
+            const int pos = cnt + __popc(b & ((1u << lane) - 1u));
+            if (mt && pos < kTokS) utok[pos] = ii / a.k;
+            cnt += __popc(b);
+          }
+        } else {
+          if (lane < a.T && lane < kTokS) utok[lane] = lane;
+          cnt = a.T;
+        }
+        if (lane == 0) s_ntok = cnt < geo.tr ? cnt : geo.tr;
+      }
+      consumers_sync();
+      ntok = s_ntok;
+      // h of those tokens as hi / lo bf16 column pairs in fragment order
+      const int n_items = ntok * ngi * 4;
+      for (int it0 = 0; it0 < n_items; it0 += kCW * 32) {
+        const int it = it0 + ctid;
+        const bool in = it < n_items;
+        const int n = in ? it / (ngi * 4) : 0, rem = it - n * ngi * 4, g = rem >> 2, qq = rem & 3;
+        float v[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = 0.0f;
+        if (in) {
+          const float4* p =
+              reinterpret_cast<const float4*>(a.h + ((int64_t)r * a.T + utok[n]) * I + g * 64 + qq * 16);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float4 f = __ldcg(p + e);
+            v[4 * e] = f.x;
+            v[4 * e + 1] = f.y;
+            v[4 * e + 2] = f.z;
+            v[4 * e + 3] = f.w;
+          }
+        }
+        uint32_t whi[8], wlo[8];
+        float sx = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float h0 = v[2 * j], h1 = v[2 * j + 1];
+          sx += h0 + h1;
+          const __nv_bfloat162 hi = __floats2bfloat162_rn(h0, h1);
+          const float2 hb = __bfloat1622float2(hi);
+          whi[j] = *reinterpret_cast<const uint32_t*>(&hi);
+          wlo[j] = pack_bf16(h0 - hb.x, h1 - hb.y);
+        }
+        sx += __shfl_xor_sync(0xffffffffu, sx, 1);
+        sx += __shfl_xor_sync(0xffffffffu, sx, 2);
+        if (in) {
+          uint4 o0h, o1h, o0l, o1l;
+          frag_order(whi, o0h, o1h);
+          frag_order(wlo, o0l, o1l);
+          uint4* dh = reinterpret_cast<uint4*>(hf + (size_t)(2 * n) * hrow + g * 128 + qq * 32);
+          uint4* dl = reinterpret_cast<uint4*>(hf + (size_t)(2 * n + 1) * hrow + g * 128 + qq * 32);
+          dh[0] = o0h;
+          dh[1] = o1h;
+          dl[0] = o0l;
+          dl[1] = o1l;
+          if (qq == 0) hsum[g * NTOK + n] = sx;
+        }
+      }
+      consumers_sync();
+      prev_r = r;
+    }
+
+    // this warp's 16 rows of the unit's scales -> (s, b - 128 s), lane = group
+    ok = ok && warp_wait(su32(&sfull), i & 1);
+    if (ok) {
+      const uint16_t* rs = raw + (size_t)(16 * w) * ngi;
+      const uint16_t* rb = rs + kRowsB * ngi;
+      for (int row = 0; row < 16; ++row)
+        for (int g = lane; g < ngi; g += 32) {
+          const float sv = bf(rs[row * ngi + g]);
+          sbt[row * (ngi + 1) + g] = make_float2(sv, fmaf(-128.0f, sv, bf(rb[row * ngi + g])));
+        }
+      __syncwarp();
+      if (lane == 0) bar_arrive(su32(&sempty));
+    }
+
+    float acc[NT][2];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = 0.0f;
+    for (int kc = 0; ok && kc < nch; ++kc) {
+      ok = warp_wait(su32(&full[s]), rnd & 1);
+      if (!ok) break;
+      const unsigned char* st = stages + s * kStageB + (16 * w + gid) * 128 + (t4 & 1) * 8;
+#pragma unroll
+      for (int gs = 0; gs < 4; ++gs) {
+        const int g = kc * 4 + gs;
+        const unsigned char* cg = st + ((((gs << 1) | (t4 >> 1)) ^ gid) * 16);
+        const uint2 lo = *reinterpret_cast<const uint2*>(cg);
+        const uint2 hi = *reinterpret_cast<const uint2*>(cg + 8 * 128);
+        const float2 s0 = sbt[gid * (ngi + 1) + g], s1 = sbt[(gid + 8) * (ngi + 1) + g];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          const int col = j * 2 * kTokB + gid;  // = 2 * token + (0 hi / 1 lo)
+          uint32_t bfr[8];
+          load_frag(hf + (size_t)col * hrow + g * 128 + t4 * 32, (col >> 1) < ntok, bfr);
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
+          group_mma(d, lo, hi, bfr);
+          const float X = hsum[g * NTOK + j * kTokB + t4];
+          acc[j][0] = fmaf(s0.x, d[0] + d[1], fmaf(s0.y, X, acc[j][0]));
+          acc[j][1] = fmaf(s1.x, d[2] + d[3], fmaf(s1.y, X, acc[j][1]));
+        }
+      }
+      __syncwarp();
+      if (lane == 0) bar_arrive(su32(&empty[s]));
+      if (++s == nst) {
+        s = 0;
+        ++rnd;
+      }
+    }
+    if (!ok) continue;
+
+    // lane (gid, t4) holds rows orow, orow + 8 of token utok[j * 4 + t4]:
+    // weighted into every routing slot of that token that names this expert
+    const int orow = o0 + 16 * w + gid;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const int n = j * kTokB + t4;
+      if (n < ntok) {
+        const int t = utok[n];
+        if (r < n_uniq) {
+          const int32_t id = a.uniq[r];
+          for (int jj = 0; jj < a.k; ++jj) {
+            if (a.layer * a.E + a.ids[t * a.k + jj] != id) continue;
+            const float wt = a.weights[t * a.k + jj];
+            float* dst = a.partial + ((int64_t)t * nslot + jj) * H;
+            dst[orow] = wt * acc[j][0];
+            dst[orow + 8] = wt * acc[j][1];
+          }
+        } else {
+          float* dst = a.partial + ((int64_t)t * nslot + a.k) * H;
+          dst[orow] = acc[j][0];
+          dst[orow + 8] = acc[j][1];
+        }
+      }
+    }
+    // arrival: the last entry to finish this 16-row tile combines it
+    __syncwarp();
+    __threadfence();
+    const int tile = (o0 >> 4) + w;
+    unsigned prev = 0;
+    if (lane == 0) prev = atomicAdd(&a.tick[tile], 1u);
+    prev = __shfl_sync(0xffffffffu, prev, 0);
+    if (prev == (unsigned)(n_exec - 1)) {
+      __threadfence();
+      for (int it = lane; it < 16 * a.T; it += 32) {
+        const int t = it >> 4, o = tile * 16 + (it & 15);
+        float yv = 0.0f;
+        for (int j = 0; j < nslot; ++j) {
+          if (j < a.k) {
+            const int32_t e = a.ids[t * a.k + j];
+            if (e < 0 || e >= a.E) continue;  // skipped by the control step as well
+          }
+          yv += __ldcg(a.partial + ((int64_t)t * nslot + j) * H + o);
+        }
+        a.y[(int64_t)t * H + o] = yv;
+      }
+      __syncwarp();
+      if (lane == 0) a.tick[tile] = 0u;
+    }
+  }
+  if (!ok && lane == 0 && a.err) atomicOr(a.err, MOE_DERR_WAIT);
+}
 }  // namespace
 
 size_t ffn_stream_smem(int H, int T) {
@@ -548,6 +919,68 @@ cudaError_t launch_ffn_gate_up_stream(const FfnArgs& a, int n_tick, cudaStream_t
     ffn_gate_up_stream_kernel<1><<<grid, kSThreads, geo.smem, st>>>(a, n_tick, geo, maps);
   }
   return cudaGetLastError();
+}
+
+size_t ffn_down_stream_smem(int H, int I, int T) {
+  if (I % 256 != 0 || H % kRowsB != 0 || T < 1 || T > kTokS) return SIZE_MAX;
+  const DownGeom g = down_plan(I, T);
+  return g.nst ? g.smem : SIZE_MAX;
+}
+
+cudaError_t launch_ffn_down_stream(const FfnArgs& a, cudaStream_t st) {
+  static size_t done1[64], done2[64];
+  static int sms[64];
+  if (a.max_entries > kStreamMaxEntries) return cudaErrorInvalidValue;
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) return e;
+  if (d < 0 || d >= 64) return cudaErrorInvalidDevice;
+  if (!sms[d]) {
+    e = cudaDeviceGetAttribute(&sms[d], cudaDevAttrMultiProcessorCount, d);
+    if (e != cudaSuccess) return e;
+  }
+  const DownGeom geo = down_plan(a.I, a.T);
+  if (!geo.nst) return cudaErrorInvalidValue;
+  // down code matrix of every blob: [blob][row of H][word of I/8]
+  CodeMaps maps;
+  const BlobOffsets off = blob_offsets(a.H, a.I);
+  const uint64_t strides[2] = {(uint64_t)a.I / 2, (uint64_t)a.blob_bytes};
+  const uint32_t box[3] = {32, kRowsB, 1};
+  const uint8_t* bases[3] = {a.bank, a.pool, a.shared ? a.shared : a.bank};
+  const int nblob[3] = {a.n_bank, a.n_pool, a.shared ? 1 : a.n_bank};
+  for (int i = 0; i < 3; ++i) {
+    const uint64_t dims[3] = {(uint64_t)a.I / 8, (uint64_t)a.H, (uint64_t)nblob[i]};
+    if ((e = encode_tiled_u32(&maps.m[i], bases[i] + off.dq, 3, dims, strides, box)) !=
+        cudaSuccess)
+      return e;
+  }
+  const int units = a.max_entries * (a.H / kRowsB);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(units < sms[d] ? units : sms[d]);
+  cfg.blockDim = dim3(kSThreads);
+  cfg.dynamicSmemBytes = geo.smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (geo.tr <= kTokB) {
+    if (done1[d] < geo.smem) {
+      e = cudaFuncSetAttribute(ffn_down_stream_kernel<1>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.smem);
+      if (e != cudaSuccess) return e;
+      done1[d] = geo.smem;
+    }
+    return cudaLaunchKernelEx(&cfg, ffn_down_stream_kernel<1>, a, geo, maps);
+  }
+  if (done2[d] < geo.smem) {
+    e = cudaFuncSetAttribute(ffn_down_stream_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)geo.smem);
+    if (e != cudaSuccess) return e;
+    done2[d] = geo.smem;
+  }
+  return cudaLaunchKernelEx(&cfg, ffn_down_stream_kernel<2>, a, geo, maps);
 }
 
 }  // namespace moe

@@ -91,6 +91,10 @@ cudaError_t launch_ffn_decode(const FfnArgs& a, cudaStream_t st);
 // cp.async.bulk stages
 cudaError_t launch_ffn_gate_up_stream(const FfnArgs& a, int n_tick, cudaStream_t st);
 size_t ffn_stream_smem(int H, int T);
+// streaming down phase (T <= 8, I % 256 == 0): launched as a programmatic
+// dependent of the gate/up kernel
+cudaError_t launch_ffn_down_stream(const FfnArgs& a, cudaStream_t st);
+size_t ffn_down_stream_smem(int H, int I, int T);
 
 // ------------------------------------------------------------------ prefill
 constexpr int kPrefillTileRows = 256;  // rows of one grouped-GEMM m-tile

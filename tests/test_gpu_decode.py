@@ -379,7 +379,7 @@ def test_full_size_deepseek_shape_decode(oracle, T):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("H,I,T", [(1024, 256, 4), (1536, 128, 3), (512, 192, 12)])
+@pytest.mark.parametrize("H,I,T", [(1024, 256, 4), (1024, 512, 6), (1536, 128, 3), (512, 192, 12)])
 def test_expert_ffn_repeated_ids(oracle, H, I, T):
     """Routing given by the caller in which one token lists an expert twice and
     several tokens share experts: each (token, rank) pair contributes once."""
