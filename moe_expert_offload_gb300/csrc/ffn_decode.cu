@@ -388,6 +388,11 @@ __global__ void __launch_bounds__(kWarpsB * 32) ffn_down_kernel(FfnArgs a) {
   float2* sb = reinterpret_cast<float2*>(hsum + ngi * NTOK);
   const int nblk = (H + kRowsBlkB - 1) / kRowsBlkB;
   const int r = blockIdx.x / nblk, blk = blockIdx.x - r * nblk;
+  if (a.counts[0] + a.has_shared == 0) {  // nothing routed to a valid expert: y = 0
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.T * H; i += gridDim.x * blockDim.x)
+      a.y[i] = 0.0f;
+    return;
+  }
   if (!resolve_entry(a, r, stok, sj, sw, &ent)) return;
 
   const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;

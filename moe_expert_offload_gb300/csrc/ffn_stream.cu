@@ -19,12 +19,11 @@
 // Every wait is bounded; on a time-out the kernel sets MOE_DERR_WAIT in the
 // plan's error word, the producer still waits (bounded) for the copies it
 // issued, and every warp returns.
-#include <cuda_bf16.h>
-
-#include "moe_internal.cuh"
+#include "stream_common.cuh"
 
 namespace moe {
 namespace {
+using namespace sc;
 
 constexpr int kCW = 8;                     // consumer warps
 constexpr int kSThreads = (kCW + 1) * 32;  // + producer warp (warp kCW)
@@ -32,107 +31,14 @@ constexpr int kTokS = 8;                   // tokens per MMA N tile (one per col
 constexpr int kRing = 2;                   // partial-sum ring depth
 constexpr int kMaxStages = 8;
 constexpr int kStreamMaxEntries = 128;
-constexpr uint32_t kSpin = 1u << 20;
 constexpr size_t kStreamSmemBudget = 220 * 1024;
 
-__device__ __forceinline__ uint32_t su32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void bar_init(uint32_t a, uint32_t n) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(n) : "memory");
-}
-
-__device__ __forceinline__ bool bar_wait(uint32_t a, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpin; ++i) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(a), "r"(parity)
-        : "memory");
-    if (done) return true;
-  }
-  return false;
-}
-
-// the whole warp waits; true only if every lane saw the phase complete
-__device__ __forceinline__ bool warp_wait(uint32_t a, uint32_t parity) {
-  return __all_sync(0xffffffffu, bar_wait(a, parity));
-}
-
-__device__ __forceinline__ void bar_arrive(uint32_t a) {
-  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}" ::"r"(a)
-               : "memory");
-}
-
-__device__ __forceinline__ void bar_expect(uint32_t a, uint32_t bytes) {
-  asm volatile(
-      "{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}" ::"r"(a),
-      "r"(bytes)
-      : "memory");
-}
-
-// global -> shared bulk copy (16-byte aligned, size a multiple of 16)
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ uint32_t nib_pair(uint32_t w, int i) {
-  return ((w >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
-}
-
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// 16 rows x one 64-column group: lo / hi are the lane's 8 code bytes of rows
-// g and g + 8, b the group's 8 B-fragment registers (same k order as
-// ffn_decode.cu: MMA jj takes nibble pairs (i, i+4), (i+1, i+5) of word jj/2).
-__device__ __forceinline__ void group_mma(float (&d)[4], uint2 lo, uint2 hi,
-                                          const uint32_t (&b)[8]) {
-#pragma unroll
-  for (int jj = 0; jj < 4; ++jj) {
-    const uint32_t wl = (jj < 2) ? lo.x : lo.y, wh = (jj < 2) ? hi.x : hi.y;
-    const int i = 2 * (jj & 1);
-    mma16816(d, nib_pair(wl, i), nib_pair(wh, i), nib_pair(wl, i + 1), nib_pair(wh, i + 1),
-             b[2 * jj], b[2 * jj + 1]);
-  }
-}
-
-__device__ __forceinline__ void frag_order(const uint32_t (&w)[8], uint4& o0, uint4& o1) {
-  o0.x = __byte_perm(w[0], w[2], 0x5410);
-  o0.y = __byte_perm(w[0], w[2], 0x7632);
-  o0.z = __byte_perm(w[1], w[3], 0x5410);
-  o0.w = __byte_perm(w[1], w[3], 0x7632);
-  o1.x = __byte_perm(w[4], w[6], 0x5410);
-  o1.y = __byte_perm(w[4], w[6], 0x7632);
-  o1.z = __byte_perm(w[5], w[7], 0x5410);
-  o1.w = __byte_perm(w[5], w[7], 0x7632);
-}
-
-__device__ __forceinline__ float bf(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
-
-// Code tiles arrive through a 4-D tensor map per blob array (bank, slot
-// pool, shared expert): u32 words [blob][gate/up][row of I][word of H/8],
+// Gate / up code tiles arrive through a 4-D tensor map per blob array (bank,
+// slot pool, shared expert): u32 words [blob][gate/up][row of I][word of H/8],
 // box = 32 words (128 B) x 16 rows x both matrices = one 4 KB sub-tile,
 // 128-byte swizzled: 16-byte chunk c of line L lands at chunk c ^ (L & 7), so
 // the eight rows a warp reads at once fall in distinct banks.
-struct CodeMaps {
-  CUtensorMap m[3];
-};
-
+//
 // Shared-memory plan of one CTA.  GPW 64-column groups per consumer warp per
 // stage, so a stage spans KC = 8 * GPW * 64 columns of H (KC / 256 sub-tiles);
 // each warp owns gtot = H / 512 groups of a unit (its slice of every stage).
@@ -174,19 +80,6 @@ inline StreamGeom stream_plan(int H, int T) {
   if (nst > kMaxStages) nst = kMaxStages;
   if (nst < 2) nst = 0;
   return stream_geom(H, T, nst);
-}
-
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            int z, int w, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
 
 template <int GPW>
@@ -431,8 +324,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
           for (int e = 0; e < 8; ++e) bfr[e] = 0u;
         }
         float dg[4] = {0.f, 0.f, 0.f, 0.f}, du[4] = {0.f, 0.f, 0.f, 0.f};
-        group_mma(dg, g0, g1, bfr);
-        group_mma(du, u0, u1, bfr);
+        group_mma2(dg, du, g0, g1, u0, u1, bfr);
         const float2 X = *reinterpret_cast<const float2*>(xsum + gi * kTokS + 2 * t4);
         const float2* sb = sbt + gi * 32;
         const float2 sg0 = sb[gid], sg1 = sb[8 + gid], su0 = sb[16 + gid], su1 = sb[24 + gid];
@@ -511,6 +403,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
 constexpr int kTokB = 4;     // tokens per MMA N tile (hi / lo column pairs)
 constexpr int kRowsB = 128;  // output rows per unit (kCW warps x 16)
 constexpr int kStageB = kRowsB * 128;
+constexpr int kMaxMatch = 4;  // routing slots of one token listed per entry
 
 struct DownGeom {
   int ngi, nch;  // 64-column groups of I, stages per unit (I / 256)
@@ -545,35 +438,36 @@ inline DownGeom down_plan(int I, int T) {
   return down_geom(I, T, nst);
 }
 
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            int z, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
-
-__device__ __forceinline__ void load_frag(const unsigned char* p, bool valid, uint32_t (&b)[8]) {
-  if (valid) {
-    const uint4 v0 = reinterpret_cast<const uint4*>(p)[0];
-    const uint4 v1 = reinterpret_cast<const uint4*>(p)[1];
-    b[0] = v0.x; b[1] = v0.y; b[2] = v0.z; b[3] = v0.w;
-    b[4] = v1.x; b[5] = v1.y; b[6] = v1.z; b[7] = v1.w;
-  } else {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) b[e] = 0u;
-  }
-}
-
 // named barrier over the consumer warps only
 __device__ __forceinline__ void consumers_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kCW * 32) : "memory");
+}
+
+// One warp's arrival on a 16-row tile of y after storing its partial rows:
+// the last of the n_exec entries to arrive adds partial[t][0..k] in j order.
+__device__ void arrive_tile(const FfnArgs& a, int tile, int n_exec, int nslot) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+  __threadfence();
+  unsigned prev = 0;
+  if (lane == 0) prev = atomicAdd(&a.tick[tile], 1u);
+  prev = __shfl_sync(0xffffffffu, prev, 0);
+  if (prev != (unsigned)(n_exec - 1)) return;
+  __threadfence();
+  for (int it = lane; it < 16 * a.T; it += 32) {
+    const int t = it >> 4, o = tile * 16 + (it & 15);
+    float yv = 0.0f;
+    for (int j = 0; j < nslot; ++j) {
+      if (j < a.k) {
+        const int32_t e = a.ids[t * a.k + j];
+        if (e < 0 || e >= a.E) continue;  // skipped by the control step as well
+      }
+      yv += __ldcg(a.partial + ((int64_t)t * nslot + j) * a.H + o);
+    }
+    a.y[(int64_t)t * a.H + o] = yv;
+  }
+  __syncwarp();
+  if (lane == 0) a.tick[tile] = 0u;
 }
 
 template <int NT>
@@ -584,6 +478,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
   __shared__ const uint8_t* sblob[kStreamMaxEntries];
   __shared__ int smap[kStreamMaxEntries], sbi[kStreamMaxEntries];
   __shared__ int utok[kTokS], s_ntok;
+  // routing slots j (and weights) of each staged token that name the entry
+  __shared__ int mj[kTokS][kMaxMatch], mcnt[kTokS];
+  __shared__ float mw[kTokS][kMaxMatch];
   constexpr int NTOK = kTokB * NT;
   const int H = a.H, I = a.I, ngi = geo.ngi, nst = geo.nst, nch = geo.nch;
   unsigned char* smem = smem_raw + ((1024u - (su32(smem_raw) & 1023u)) & 1023u);
@@ -602,6 +499,11 @@ __global__ void __launch_bounds__(kSThreads, 1)
   // (and the arrival counters it resets) need that kernel to finish
   const int n_uniq = a.counts[0];
   const int n_exec = n_uniq + a.has_shared;
+  if (n_exec == 0) {  // nothing routed to a valid expert: y = 0
+    for (int i = blockIdx.x * blockDim.x + tid; i < a.T * H; i += gridDim.x * blockDim.x)
+      a.y[i] = 0.0f;
+    return;
+  }
   if (wid == kCW) {
     if (lane < 3) tma_prefetch_map(&maps.m[lane]);
     for (int r = lane; r < n_exec; r += 32) {
@@ -682,7 +584,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   float* hsum = reinterpret_cast<float*>(smem + geo.o_hsum);
   const uint16_t* raw = reinterpret_cast<const uint16_t*>(sraw);
   const int nslot = a.k + a.has_shared, hrow = geo.hrow;
-  int prev_r = -1, ntok = 0, s = 0, rnd = 0;
+  int prev_r = -1, ntok = 0, s = 0, rnd = 0, pend = -1;
   bool ok = true;  // after a failed wait the warp keeps walking the loop (no waits,
                    // no math) so that every consumer warp meets the same barriers
   for (int u = u_lo; u < u_hi; ++u) {
@@ -710,7 +612,29 @@ __global__ void __launch_bounds__(kSThreads, 1)
           if (lane < a.T && lane < kTokS) utok[lane] = lane;
           cnt = a.T;
         }
-        if (lane == 0) s_ntok = cnt < geo.tr ? cnt : geo.tr;
+        const int nt = cnt < geo.tr ? cnt : geo.tr;
+        if (lane == 0) s_ntok = nt;
+        __syncwarp();
+        if (lane < nt) {
+          const int t = utok[lane];
+          int c = 0;
+          if (r < n_uniq) {
+            const int32_t id = a.uniq[r];
+            for (int jj = 0; jj < a.k; ++jj)
+              if (a.layer * a.E + a.ids[t * a.k + jj] == id) {
+                if (c < kMaxMatch) {
+                  mj[lane][c] = jj;
+                  mw[lane][c] = a.weights[t * a.k + jj];
+                }
+                ++c;
+              }
+          } else {
+            mj[lane][0] = a.k;
+            mw[lane][0] = 1.0f;
+            c = 1;
+          }
+          mcnt[lane] = c;
+        }
       }
       consumers_sync();
       ntok = s_ntok;
@@ -814,6 +738,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
     }
     if (!ok) continue;
 
+    // the previous unit's partials were stored long ago: its arrival (fence +
+    // counter) is cheap here and stays off the path of this unit's math
+    if (pend >= 0) arrive_tile(a, pend, n_exec, nslot);
     // lane (gid, t4) holds rows orow, orow + 8 of token utok[j * 4 + t4]:
     // weighted into every routing slot of that token that names this expert
     const int orow = o0 + 16 * w + gid;
@@ -821,48 +748,26 @@ __global__ void __launch_bounds__(kSThreads, 1)
     for (int j = 0; j < NT; ++j) {
       const int n = j * kTokB + t4;
       if (n < ntok) {
-        const int t = utok[n];
-        if (r < n_uniq) {
+        const int t = utok[n], c = mcnt[n];
+        for (int m = 0; m < c && m < kMaxMatch; ++m) {
+          float* dst = a.partial + ((int64_t)t * nslot + mj[n][m]) * H;
+          dst[orow] = mw[n][m] * acc[j][0];
+          dst[orow + 8] = mw[n][m] * acc[j][1];
+        }
+        if (c > kMaxMatch) {  // a token naming this expert more than kMaxMatch times
           const int32_t id = a.uniq[r];
-          for (int jj = 0; jj < a.k; ++jj) {
-            if (a.layer * a.E + a.ids[t * a.k + jj] != id) continue;
-            const float wt = a.weights[t * a.k + jj];
+          for (int jj = 0, m = 0; jj < a.k; ++jj) {
+            if (a.layer * a.E + a.ids[t * a.k + jj] != id || m++ < kMaxMatch) continue;
             float* dst = a.partial + ((int64_t)t * nslot + jj) * H;
-            dst[orow] = wt * acc[j][0];
-            dst[orow + 8] = wt * acc[j][1];
+            dst[orow] = a.weights[t * a.k + jj] * acc[j][0];
+            dst[orow + 8] = a.weights[t * a.k + jj] * acc[j][1];
           }
-        } else {
-          float* dst = a.partial + ((int64_t)t * nslot + a.k) * H;
-          dst[orow] = acc[j][0];
-          dst[orow + 8] = acc[j][1];
         }
       }
     }
-    // arrival: the last entry to finish this 16-row tile combines it
-    __syncwarp();
-    __threadfence();
-    const int tile = (o0 >> 4) + w;
-    unsigned prev = 0;
-    if (lane == 0) prev = atomicAdd(&a.tick[tile], 1u);
-    prev = __shfl_sync(0xffffffffu, prev, 0);
-    if (prev == (unsigned)(n_exec - 1)) {
-      __threadfence();
-      for (int it = lane; it < 16 * a.T; it += 32) {
-        const int t = it >> 4, o = tile * 16 + (it & 15);
-        float yv = 0.0f;
-        for (int j = 0; j < nslot; ++j) {
-          if (j < a.k) {
-            const int32_t e = a.ids[t * a.k + j];
-            if (e < 0 || e >= a.E) continue;  // skipped by the control step as well
-          }
-          yv += __ldcg(a.partial + ((int64_t)t * nslot + j) * H + o);
-        }
-        a.y[(int64_t)t * H + o] = yv;
-      }
-      __syncwarp();
-      if (lane == 0) a.tick[tile] = 0u;
-    }
+    pend = (o0 >> 4) + w;
   }
+  if (ok && pend >= 0) arrive_tile(a, pend, n_exec, nslot);
   if (!ok && lane == 0 && a.err) atomicOr(a.err, MOE_DERR_WAIT);
 }
 }  // namespace

@@ -78,7 +78,7 @@ struct FfnArgs {
   const uint8_t* shared;
   float* h;         // [max_entries][T][I]
   float* partial;   // [T][k + has_shared][H]
-  uint32_t* tick;   // [H / rows per down block] arrival counters
+  uint32_t* tick;   // [ceil(H / 16)] arrival counters, one per 16-row tile of y
   float* y;         // [T][H]
   int max_entries;
   int n_bank;       // blobs in the bank (num_layers * E)
