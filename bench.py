@@ -71,7 +71,7 @@ def peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("ffn_decode.cu", "moe_internal.cuh"):
+    for f in ("ffn_decode.cu", "ffn_stream.cu", "stream_common.cuh", "moe_internal.cuh"):
         h.update(open(os.path.join(ROOT, "moe_expert_offload_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -638,6 +638,9 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the timed CPU oracle baseline")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (small cases for profiling)")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override the experts per layer (small cases for profiling; same expert "
+                         "shape, slot count scaled in proportion)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -645,9 +648,13 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     w = dict(WORKLOADS[args.workload])
-    if args.layers:
-        w["L"] = args.layers
-        w["desc"] += f" [profiling case: {args.layers} layers]"
+    if args.layers or args.experts:
+        L0, E0 = w["L"], w["E"]
+        w["L"] = args.layers or L0
+        w["E"] = args.experts or E0
+        if "slots" in w:
+            w["slots"] = max(2 * w["k"], round(w["slots"] * w["L"] * w["E"] / (L0 * E0)))
+        w["desc"] += f" [profiling case: {w['L']} layers x {w['E']} experts]"
     if args.impl == "reference":
         run_reference(args, w, rank, world)
         return

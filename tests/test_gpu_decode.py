@@ -404,3 +404,24 @@ def test_expert_ffn_repeated_ids(oracle, H, I, T):
         assert plan.read(2)["err"] == 0
         ref = oracle.moe_ffn(list(bank_h[:E]), H, I, xb, ids_h, w_h)
         assert_ffn_close(y.cpu().numpy(), ref, f"step {step}")
+
+
+@pytest.mark.parametrize("H,I", [(1024, 256), (256, 128)])
+def test_expert_ffn_no_valid_expert_writes_zero(oracle, H, I):
+    """Every routed id out of range and no shared expert: the control step flags
+    the ids, nothing executes, and y is all zeros (stale contents are replaced)."""
+    E, k, T = 8, 2, 1
+    spec, bank, bank_h, cache, _ = _layer_rig(1, H, I, E, k, 2, 2, 11800, 47500, False, seed=3)
+    plan = m.DevicePlan(T * k, 2, device=DEV)
+    fws = m.moe_ffn_workspace_bytes(spec, T)
+    ws = torch.empty(fws, dtype=torch.uint8, device=DEV)
+    y = torch.full((T, H), float("nan"), dtype=torch.float32, device=DEV)
+    ids = torch.tensor([[E, -1]], dtype=torch.int32, device=DEV)
+    w = torch.tensor([[0.5, 0.5]], dtype=torch.float32, device=DEV)
+    xb = synth.bf16_bits(np.random.default_rng(0).normal(0, 1, (T, H)))
+    m.moe_cache_step(spec, cache.c, 0, ids, T, plan.c, 1)
+    m.moe_expert_ffn(spec, cache.c, 0, plan.c, dev_bits(xb, DEV), T, ids, w, None, ws, fws, y)
+    torch.cuda.synchronize()
+    gp = plan.read(2)
+    assert gp["err"] & m.MOE_DERR_BAD_ID and gp["n_uniq"] == 0
+    assert torch.count_nonzero(y).item() == 0
