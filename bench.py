@@ -311,20 +311,11 @@ def run_gpu(args, w, rank, world, local_rank):
     torch.cuda.synchronize()
 
     # The timed region is one CUDA graph holding all K steps back to back (each
-    # step reads its own resident inputs); timing events around every FFN
-    # launch are recorded inside the graph as external event nodes.
-    try:
-        mk = lambda: torch.cuda.Event(enable_timing=True, external=True)  # noqa: E731
-        mk()
-        in_graph_events = True
-    except TypeError:
-        in_graph_events = False
-    evs = [[[mk(), mk()] for _ in range(L)] for _ in range(args.steps)] if in_graph_events \
-        else None
+    # step reads its own resident inputs), with nothing between the kernels.
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         for s in range(args.steps):
-            step(args.warmup + s, None if evs is None else evs[s])
+            step(args.warmup + s)
     torch.cuda.synchronize()
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -340,15 +331,30 @@ def run_gpu(args, w, rank, world, local_rank):
         t = torch.tensor([ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
-    if in_graph_events:
-        ffn_ms = [evs[s][l][0].elapsed_time(evs[s][l][1])
-                  for s in range(args.steps) for l in range(L)]
-        ffn_timing = "CUDA events around every FFN launch inside the timed graph"
-    else:
-        # fallback: a graph of the 40 layers' FFN launches alone, replayed
-        ffn_ms = []
-        ffn_timing = "CUDA events around graph replays of FFN-only steps"
     del graph
+
+    # Per-launch FFN duration for the roofline: a second graph of the same
+    # steps with timing events around every FFN launch (event nodes sit
+    # between kernels, so this graph is replayed outside the timed region).
+    ev_steps = min(args.steps, 16)
+    try:
+        mk = lambda: torch.cuda.Event(enable_timing=True, external=True)  # noqa: E731
+        mk()
+        evs = [[[mk(), mk()] for _ in range(L)] for _ in range(ev_steps)]
+        g_ev = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_ev):
+            for s in range(ev_steps):
+                step(args.warmup + s, evs[s])
+        g_ev.replay()
+        torch.cuda.synchronize()
+        ffn_ms = [evs[s][l][0].elapsed_time(evs[s][l][1]) for s in range(ev_steps)
+                  for l in range(L)]
+        ffn_timing = (f"CUDA events around every FFN launch, {ev_steps} steps replayed as a graph "
+                      "outside the timed region")
+        del g_ev
+    except TypeError:
+        ffn_ms = []
+        ffn_timing = "unavailable (this torch build has no external events)"
     ffn_avg_s = statistics.mean(ffn_ms) * 1e-3 if ffn_ms else float("nan")
 
     # statistics of the control decisions (untimed replay of more steps)

@@ -71,6 +71,8 @@ __global__ void __launch_bounds__(kCtlThreads) cache_step_kernel(CacheArgs a) {
   __shared__ unsigned long long svict[KMAX];
   __shared__ int s_nu, s_bad;
   __shared__ uint32_t s_now;
+  griddep_launch();
+  griddep_wait();  // routed ids from the previous kernel
 
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int n = a.n_ids, E = a.E;
@@ -227,6 +229,8 @@ __global__ void __launch_bounds__(256) fill_copy_kernel(const int32_t* __restric
                                                         const uint8_t* __restrict__ bank,
                                                         uint8_t* __restrict__ pool,
                                                         int64_t blob_bytes) {
+  griddep_launch();
+  griddep_wait();  // the plan from the control step
   const int i = blockIdx.y;
   if (i >= counts[4]) return;
   const uint4* src = reinterpret_cast<const uint4*>(bank + (int64_t)fill_ids[i] * blob_bytes);
@@ -259,13 +263,9 @@ __global__ void cache_reset_kernel(int32_t* slot_of_id, int n_ids, int32_t* id_o
 }  // namespace
 
 cudaError_t launch_cache_step(const CacheArgs& a, cudaStream_t st) {
-  if (a.K <= 8)
-    cache_step_kernel<8><<<1, kCtlThreads, 0, st>>>(a);
-  else if (a.K <= 16)
-    cache_step_kernel<16><<<1, kCtlThreads, 0, st>>>(a);
-  else
-    cache_step_kernel<32><<<1, kCtlThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  if (a.K <= 8) return launch_pdl(cache_step_kernel<8>, dim3(1), dim3(kCtlThreads), 0, st, a);
+  if (a.K <= 16) return launch_pdl(cache_step_kernel<16>, dim3(1), dim3(kCtlThreads), 0, st, a);
+  return launch_pdl(cache_step_kernel<32>, dim3(1), dim3(kCtlThreads), 0, st, a);
 }
 
 cudaError_t launch_fill_copy(const moe_plan& plan, int K, const uint8_t* bank, uint8_t* pool,
@@ -274,9 +274,8 @@ cudaError_t launch_fill_copy(const moe_plan& plan, int K, const uint8_t* bank, u
   int gx = (int)((n16 + 256 * 4 - 1) / (256 * 4));
   if (gx > 128) gx = 128;
   if (gx < 1) gx = 1;
-  fill_copy_kernel<<<dim3(gx, K), 256, 0, st>>>(plan.counts, plan.fill_ids, plan.fill_slots, bank,
-                                                pool, blob_bytes);
-  return cudaGetLastError();
+  return launch_pdl(fill_copy_kernel, dim3(gx, K), dim3(256), 0, st, plan.counts, plan.fill_ids,
+                    plan.fill_slots, bank, pool, blob_bytes);
 }
 
 cudaError_t launch_cache_reset(int32_t* slot_of_id, int n_ids, int32_t* id_of_slot, uint32_t* ts,

@@ -114,6 +114,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     s_fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  griddep_wait();  // the plan and the filled slots from the previous kernels
   if (blockIdx.x == 0)
     for (int i = tid; i < n_tick; i += blockDim.x) a.tick[i] = 0u;
   const int n_uniq = a.counts[0];
@@ -576,7 +577,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
 
   // ---------------------------------------------------------- consumers
   // h is written by the gate/up kernel: wait for it to complete
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  griddep_wait();
+  griddep_launch();  // the next kernel may be scheduled (it waits for this one)
   const int w = wid, gid = lane >> 2, t4 = lane & 3;
   const int ctid = tid;  // 0 .. kCW * 32 - 1
   float2* sbt = reinterpret_cast<float2*>(smem + geo.o_sbt) + (size_t)w * 16 * (ngi + 1);
@@ -813,7 +815,8 @@ cudaError_t launch_ffn_gate_up_stream(const FfnArgs& a, int n_tick, cudaStream_t
       if (e != cudaSuccess) return e;
       done2[d] = geo.smem;
     }
-    ffn_gate_up_stream_kernel<2><<<grid, kSThreads, geo.smem, st>>>(a, n_tick, geo, maps);
+    return launch_pdl(ffn_gate_up_stream_kernel<2>, dim3(grid), dim3(kSThreads), geo.smem, st, a,
+                      n_tick, geo, maps);
   } else {
     if (done1[d] < geo.smem) {
       e = cudaFuncSetAttribute(ffn_gate_up_stream_kernel<1>,
@@ -821,9 +824,9 @@ cudaError_t launch_ffn_gate_up_stream(const FfnArgs& a, int n_tick, cudaStream_t
       if (e != cudaSuccess) return e;
       done1[d] = geo.smem;
     }
-    ffn_gate_up_stream_kernel<1><<<grid, kSThreads, geo.smem, st>>>(a, n_tick, geo, maps);
+    return launch_pdl(ffn_gate_up_stream_kernel<1>, dim3(grid), dim3(kSThreads), geo.smem, st, a,
+                      n_tick, geo, maps);
   }
-  return cudaGetLastError();
 }
 
 size_t ffn_down_stream_smem(int H, int I, int T) {

@@ -37,6 +37,33 @@ __host__ __device__ inline BlobOffsets blob_offsets(int64_t H, int64_t I) {
   return o;
 }
 
+// Programmatic dependent launch (the decode layer path).  A kernel launched
+// with launch_pdl may be scheduled while the previous kernel in the stream is
+// still running: it calls griddep_wait() before its first access to memory
+// that a predecessor writes or reads, and griddep_launch() so that its own
+// dependent can be scheduled early.  After a predecessor that never signals
+// (any other kernel) it simply starts when that kernel has finished.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Tiled TMA descriptor over u32 elements, 128-byte swizzle, rank <= 5:
 // dims[0] innermost, strides[i] = bytes between consecutive indices of
 // dimension i + 1.  Returns cudaErrorNotSupported without a driver encoder.

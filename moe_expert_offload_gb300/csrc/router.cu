@@ -67,6 +67,8 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const uint16_t* __re
                                                             const uint16_t* __restrict__ w, int T,
                                                             int E, int H,
                                                             float* __restrict__ logits) {
+  griddep_launch();
+  griddep_wait();  // x may come from the previous kernel
   const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (warp >= T * E) return;
@@ -108,6 +110,8 @@ __global__ void __launch_bounds__(256) router_logits_tiled_kernel(const uint16_t
                                                                   int T, int E, int H,
                                                                   float* __restrict__ logits) {
   __shared__ __align__(16) uint4 xs[kTileTok][32];  // 16 rows x 256 bf16
+  griddep_launch();
+  griddep_wait();
   __shared__ __align__(16) uint4 ws[kTileExp][32];
   const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
   const int t0 = blockIdx.x * kTileTok, e0 = blockIdx.y * kTileExp;
@@ -193,6 +197,8 @@ __global__ void __launch_bounds__(kSelWarps * 32)
   __shared__ float sv[kSelWarps][kMaxK];
   __shared__ float sex[kSelWarps][kMaxK];
   __shared__ float ssum[kSelWarps];
+  griddep_launch();
+  griddep_wait();  // logits from the previous kernel
   const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kSelWarps + wid;
   if (t >= T) return;
@@ -246,6 +252,8 @@ __global__ void __launch_bounds__(kSelWarps * 32)
   __shared__ float ssel[kSelWarps][32 * EPL];
   __shared__ float ss[kSelWarps][kMaxK];
   __shared__ float ssum[kSelWarps];
+  griddep_launch();
+  griddep_wait();  // logits from the previous kernel
   const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kSelWarps + wid;
   if (t >= T) return;
@@ -332,13 +340,11 @@ cudaError_t launch_select(const moe_spec& sp, const float* logits, const float* 
                           int32_t* ids, float* weights, cudaStream_t st) {
   const int grid = (T + kSelWarps - 1) / kSelWarps;
   if (sp.router == MOE_ROUTER_SOFTMAX_TOPK)
-    select_softmax_kernel<EPL><<<grid, kSelWarps * 32, 0, st>>>(logits, T, sp.num_experts,
-                                                                 sp.top_k, ids, weights);
-  else
-    select_sigmoid_group_kernel<EPL><<<grid, kSelWarps * 32, 0, st>>>(
-        logits, bias, T, sp.num_experts, sp.n_groups, sp.topk_groups, sp.top_k, sp.routed_scale,
-        ids, weights);
-  return cudaGetLastError();
+    return launch_pdl(select_softmax_kernel<EPL>, dim3(grid), dim3(kSelWarps * 32), 0, st, logits,
+                      T, sp.num_experts, sp.top_k, ids, weights);
+  return launch_pdl(select_sigmoid_group_kernel<EPL>, dim3(grid), dim3(kSelWarps * 32), 0, st,
+                    logits, bias, T, sp.num_experts, sp.n_groups, sp.topk_groups, sp.top_k,
+                    sp.routed_scale, ids, weights);
 }
 
 }  // namespace
@@ -347,13 +353,11 @@ cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* w, int T, in
                                  float* logits, cudaStream_t st) {
   if (H % 256 == 0 && T >= kTileTok) {
     const dim3 grid((T + kTileTok - 1) / kTileTok, (E + kTileExp - 1) / kTileExp);
-    router_logits_tiled_kernel<<<grid, 256, 0, st>>>(x, w, T, E, H, logits);
-    return cudaGetLastError();
+    return launch_pdl(router_logits_tiled_kernel, grid, dim3(256), 0, st, x, w, T, E, H, logits);
   }
   const long warps = (long)T * E;
   const int grid = (int)((warps + 3) / 4);
-  router_logits_kernel<<<grid, 128, 0, st>>>(x, w, T, E, H, logits);
-  return cudaGetLastError();
+  return launch_pdl(router_logits_kernel, dim3(grid), dim3(128), 0, st, x, w, T, E, H, logits);
 }
 
 cudaError_t launch_router_select(const moe_spec& sp, const float* logits, const float* bias,
