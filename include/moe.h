@@ -13,8 +13,10 @@
  *                      "Semantic-Aware Expert Caching", "Elastic Memory
  *                      Management")
  *   moe_expert_ffn     int4 affine group-64 SwiGLU experts down(silu(gate(x)) *
- *                      up(x)) over G = H u F read from the slot pool and over C
- *                      read in place from the bank, combined with the routing
+ *                      up(x)) over G = H u F (H from the slot pool; F, the
+ *                      experts filled in this step, from their bank bytes,
+ *                      identical to the slot copy) and over C read in place
+ *                      from the bank, combined with the routing
  *                      weights (Edge0 §3.1 "math convention"; FreeToken summary
  *                      "core method": exact merge of the partial sums)
  *   moe_layer_forward  the three above in stream order
@@ -189,9 +191,10 @@ size_t moe_ffn_workspace_bytes(const moe_spec* spec, int32_t T);
 
 /* ------------------------------------------------------------------------
  * moe_expert_ffn -- decode expert FFN and combine (T <= 64).
- *   Executes every id in plan->uniq (H and F from their slots, C in place from
- *   the bank: an id with slot_of_id >= 0 after the cache step is read from
- *   the slot pool, any other from the bank) plus the shared expert:
+ *   Executes every id in plan->uniq (H from its slot; F and C in place from
+ *   the bank: an id cached before this step is read from the slot pool, an id
+ *   in plan->fill_ids or without a slot from the bank, so the FFN does not
+ *   depend on the fill copies) plus the shared expert:
  *     y[t] = sum_j weights[t][j] * expert(ids[t][j])(x[t]) + shared(x[t])
  *   expert(x) = Wd (silu(Wg x) * (Wu x)), dequantised int4, fp32 accumulate.
  *   The routed terms are added in rank order j, then the shared term.
@@ -210,9 +213,14 @@ size_t moe_layer_workspace_bytes(const moe_spec* spec, int32_t T);
 
 /* ------------------------------------------------------------------------
  * moe_layer_forward -- moe_route, moe_cache_step (with fill) and
- * moe_expert_ffn for one decode layer, in stream order, no host sync.
+ * moe_expert_ffn for one decode layer, no host sync.
  *   ids, weights  device out [T][k] (the routing decision, kept for the caller)
  *   workspace     >= moe_layer_workspace_bytes(spec, T)
+ * The fill copies run beside the FFN (which reads the experts being filled
+ * from the bank, byte-identical to their new slots) on a stream owned by the
+ * library; `stream` waits for them before any later work, so everything the
+ * call enqueues is complete, in order, from the caller's stream's view (also
+ * when the stream is being captured into a graph).
  * ------------------------------------------------------------------------ */
 int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, const void* x,
                       int32_t T, const void* w_router, const float* bias, const void* shared,

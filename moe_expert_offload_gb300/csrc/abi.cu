@@ -129,6 +129,40 @@ int do_cache_step(const moe_spec* spec, moe_cache* c, int32_t layer, const int32
   return MOE_OK;
 }
 
+// The fill copy of a decode layer step runs beside the FFN on a side stream
+// owned by the library (one per host thread and device): the FFN reads the
+// experts being filled from the bank, and the caller's stream waits for the
+// copy before its next work.  Fork and join are event record / wait pairs,
+// so they also hold inside a captured graph.  The stream and its events are
+// created on the first call that is not being captured (creation is not
+// allowed during capture); until then the copy stays on the caller's stream.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+SideStream* side_stream(cudaStream_t st) {
+  thread_local SideStream tab[64];
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) return nullptr;
+  SideStream& r = tab[d];
+  if (r.s) return &r;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+    return nullptr;
+  if (cudaStreamCreateWithFlags(&r.s, cudaStreamNonBlocking) != cudaSuccess) {
+    r.s = nullptr;
+    return nullptr;
+  }
+  if (cudaEventCreateWithFlags(&r.fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&r.join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaStreamDestroy(r.s);
+    r.s = nullptr;
+    return nullptr;
+  }
+  return &r;
+}
+
 int check_step_args(const moe_spec* spec, int32_t layer, int32_t T) {
   if (layer < 0 || layer >= spec->num_layers) return fail(MOE_EINVAL, "layer out of range");
   if (T < 0) return fail(MOE_EINVAL, "T must be >= 0");
@@ -166,6 +200,7 @@ int do_ffn(const moe_spec* spec, const moe_cache* c, int32_t layer, const moe_pl
   a.slot_of_id = c->slot_of_id;
   a.uniq = plan->uniq;
   a.counts = plan->counts;
+  a.fill_ids = plan->fill_ids;
   a.err = plan->err;
   a.x = static_cast<const uint16_t*>(x);
   a.ids = ids;
@@ -286,10 +321,25 @@ int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, con
   const size_t lbytes = align256((size_t)T * spec->num_experts * 4);
   rc = do_route(spec, x, T, w_router, bias, logits, ids, weights, st);
   if (rc) return rc;
-  rc = do_cache_step(spec, cache, layer, ids, T, plan, 1, st);
+  SideStream* ss = side_stream(st);
+  rc = do_cache_step(spec, cache, layer, ids, T, plan, ss ? 0 : 1, st);
   if (rc) return rc;
+  if (ss) {  // fill copy beside the FFN
+    cudaError_t e = cudaEventRecord(ss->fork, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->s, ss->fork, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "fill fork");
+    const moe::BlobOffsets off = moe::blob_offsets(spec->hidden, spec->inter);
+    e = moe::launch_fill_copy(*plan, cache->k_victims, static_cast<const uint8_t*>(cache->bank),
+                              static_cast<uint8_t*>(cache->slot_pool), off.total, ss->s);
+    if (e == cudaSuccess) e = cudaEventRecord(ss->join, ss->s);
+    if (e != cudaSuccess) return cuda_fail(e, "fill copy launch");
+  }
   rc = do_ffn(spec, cache, layer, plan, x, T, ids, weights, shared,
               static_cast<uint8_t*>(workspace) + lbytes, workspace_bytes - lbytes, y, st);
+  if (ss) {
+    const cudaError_t e = cudaStreamWaitEvent(st, ss->join, 0);
+    if (e != cudaSuccess && !rc) return cuda_fail(e, "fill join");
+  }
   return rc ? rc : ok();
 }
 

@@ -18,6 +18,8 @@ namespace {
 constexpr int kCtlThreads = 512;
 constexpr int kCtlWarps = kCtlThreads / 32;
 constexpr unsigned long long kNoKey = ~0ull;
+constexpr int kEarlyTs = 8;  // recency stamps per thread loaded before the routed ids
+constexpr int kEarlySlots = kEarlyTs * kCtlThreads;
 
 __device__ __forceinline__ unsigned lanemask_lt() {
   unsigned m;
@@ -71,12 +73,25 @@ __global__ void __launch_bounds__(kCtlThreads) cache_step_kernel(CacheArgs a) {
   __shared__ unsigned long long svict[KMAX];
   __shared__ int s_nu, s_bad;
   __shared__ uint32_t s_now;
+  __shared__ uint32_t shit[kEarlySlots / 32];  // slots hit this step (those < kEarlySlots)
   griddep_launch();
   griddep_wait();  // routed ids from the previous kernel
 
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int n = a.n_ids, E = a.E;
 
+  // The victim scan does not depend on the routed ids: the recency stamps of
+  // this thread's first kEarlyTs slots are loaded now, alongside the ids, and
+  // the slots hit this step are left out through a bitmap (their stamps
+  // become `now`, which the scan excludes).
+  constexpr int NE = KMAX <= 16 ? kEarlyTs : 0;  // (the K <= 32 list needs the registers)
+  uint32_t early[NE > 0 ? NE : 1];
+#pragma unroll
+  for (int j = 0; j < NE; ++j) {
+    const int v = tid + j * kCtlThreads;
+    early[j] = v < a.S ? a.ts[v] : 0u;
+  }
+  for (int i = tid; i < kEarlySlots / 32; i += kCtlThreads) shit[i] = 0u;
   if (tid == 0) {
     s_now = a.clock[0] + 1u;
     a.clock[0] = s_now;
@@ -146,6 +161,7 @@ __global__ void __launch_bounds__(kCtlThreads) cache_step_kernel(CacheArgs a) {
       a.plan.hit_ids[p] = u;
       a.plan.hit_slots[p] = slot;
       a.ts[slot] = now;  // recency moves only when the router selects the expert
+      if (slot < kEarlySlots) atomicOr(&shit[slot >> 5], 1u << (slot & 31));
     }
     if (miss) smiss[om + __popc(mb & lanemask_lt())] = u;
     base_h += th;
@@ -170,7 +186,13 @@ __global__ void __launch_bounds__(kCtlThreads) cache_step_kernel(CacheArgs a) {
   unsigned long long best[KMAX];
 #pragma unroll
   for (int j = 0; j < KMAX; ++j) best[j] = kNoKey;
-  for (int v = tid; v < a.S; v += kCtlThreads) {
+#pragma unroll
+  for (int j = 0; j < NE; ++j) {
+    const int v = tid + j * kCtlThreads;
+    if (v < a.S && !(shit[v >> 5] >> (v & 31) & 1u))
+      insert_key<KMAX>(best, ((unsigned long long)early[j] << 32) | (uint32_t)v);
+  }
+  for (int v = tid + NE * kCtlThreads; v < a.S; v += kCtlThreads) {  // read after the hit updates
     const uint32_t t = a.ts[v];
     if (t != now) insert_key<KMAX>(best, ((unsigned long long)t << 32) | (uint32_t)v);
   }

@@ -130,7 +130,7 @@ __device__ bool resolve_entry(const FfnArgs& a, int r, int* stok, int* sj, float
   if (r < n_uniq) {
     const int32_t id = a.uniq[r];
     if (tid == 0) {
-      const int32_t slot = a.slot_of_id[id];
+      const int32_t slot = ffn_slot(a, id);
       out->blob = slot >= 0 ? a.pool + (int64_t)slot * a.blob_bytes
                             : a.bank + (int64_t)id * a.blob_bytes;
     }

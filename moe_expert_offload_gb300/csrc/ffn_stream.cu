@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       int mi = 2, bi = 0;
       if (r < n_uniq) {
         const int32_t id = a.uniq[r];
-        const int32_t slot = a.slot_of_id[id];
+        const int32_t slot = ffn_slot(a, id);
         mi = slot >= 0 ? 1 : 0;
         bi = slot >= 0 ? slot : id;
       }
@@ -511,7 +511,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       int mi = 2, bi = 0;
       if (r < n_uniq) {
         const int32_t id = a.uniq[r];
-        const int32_t slot = a.slot_of_id[id];
+        const int32_t slot = ffn_slot(a, id);
         mi = slot >= 0 ? 1 : 0;
         bi = slot >= 0 ? slot : id;
       }

@@ -98,6 +98,7 @@ struct FfnArgs {
   const int32_t* slot_of_id;
   const int32_t* uniq;
   const int32_t* counts;
+  const int32_t* fill_ids;  // F of this step (counts[4] entries)
   int32_t* err;
   const uint16_t* x;
   const int32_t* ids;
@@ -111,6 +112,19 @@ struct FfnArgs {
   int n_bank;       // blobs in the bank (num_layers * E)
   int n_pool;       // slots in the pool
 };
+// Where the FFN reads a routed id's weights: its slot when it was cached
+// before this step (H), else in place from the bank (C, and F: an expert being
+// filled in this step is read from the bank, byte-identical to its new slot,
+// so the FFN need not wait for the fill copy).  Returns the slot or -1.
+__device__ __forceinline__ int32_t ffn_slot(const FfnArgs& a, int32_t id) {
+  const int32_t slot = a.slot_of_id[id];
+  if (slot < 0) return -1;
+  const int nf = a.counts[4];
+  for (int i = 0; i < nf; ++i)
+    if (a.fill_ids[i] == id) return -1;
+  return slot;
+}
+
 size_t ffn_workspace_bytes(int H, int I, int k, int T, int has_shared);
 void ffn_carve_workspace(FfnArgs& a, void* ws);
 cudaError_t launch_ffn_decode(const FfnArgs& a, cudaStream_t st);
