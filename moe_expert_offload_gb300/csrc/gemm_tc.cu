@@ -21,7 +21,7 @@
 //                 Rows past the group's count are zero-filled, and a tile of at
 //                 most 128 rows skips its second half entirely.
 //       warps 5-12 one B row per thread: int4 codes and the group scale / bias
-//                 prefetched into registers three blocks ahead, dequantised (one
+//                 prefetched into registers five blocks ahead, dequantised (one
 //                 LOP3 per nibble pair gives (128+q) as bf16x2, then q = v - 128
 //                 and w = s*q + b by bf16x2 fma) into a 2-deep B ring.
 //       warp 4    one thread waits for both stages, issues the MMAs and frees
@@ -57,6 +57,7 @@ constexpr int kHalfBytes = 128 * kBK * 2;        // 16 KB: one 128-row half of A
 constexpr int kABytes = kBM * kBK * 2;           // 32 KB
 constexpr int kBBytes = kBN * kBK * 2;           // 32 KB
 constexpr int kTmemCols = 512;
+constexpr int kAhead = 5;                        // k-blocks of B codes requested ahead
 constexpr uint32_t kWaitIters = 1u << 20;
 
 // ------------------------------------------------------------- PTX wrappers
@@ -193,7 +194,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(GemmArgs g) {
   __shared__ volatile int s_fail;
   __shared__ const uint16_t* arow_s[kBM];
   const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
-  const int mt = blockIdx.x, nt = blockIdx.y;
+  // n-tiles run fastest: the CTAs sharing an m-tile's A rows are resident
+  // together, so A comes from HBM once and from L2 for the other n-tiles
+  const int nt = blockIdx.x, mt = blockIdx.y;
   if (mt >= *g.n_tiles) return;
   const int grp = g.tile_g[mt], row0 = g.tile_row0[mt], rows = g.tile_rows[mt];
   const int H = g.H, I = g.I;
@@ -360,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(GemmArgs g) {
       }
     };
     // one B stage: wait until the MMAs of its previous use are done (lane 0,
-    // broadcast), prefetch block kb+3, dequantise block kb, mark the stage full
+    // broadcast), prefetch block kb+kAhead, dequantise block kb, mark the stage full
     auto step = [&](int kb, const BRegs& cur, BRegs& nxt) -> bool {
       const int sb = kb % kStagesB, use = kb / kStagesB;
       int ok = 1;
@@ -369,22 +372,28 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(GemmArgs g) {
         ok = !s_fail;
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
-      if (kb + 3 < nk) load_b(kb + 3, nxt);
+      if (kb + kAhead < nk) load_b(kb + kAhead, nxt);
       dequant(kb, cur);
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&full_b[sb]));
       return true;
     };
-    BRegs r0, r1, r2, r3;  // four named sets in rotation: block kb lives in set kb % 4
+    // six named sets in rotation: block kb lives in set kb % 6, its codes are
+    // requested five blocks (~5 x 1200 cycles) before they are dequantised
+    BRegs r0, r1, r2, r3, r4, r5;
     load_b(0, r0);
     if (nk > 1) load_b(1, r1);
     if (nk > 2) load_b(2, r2);
-    for (int kb = 0; kb < nk; kb += 4) {
-      if (!step(kb, r0, r3)) break;
+    if (nk > 3) load_b(3, r3);
+    if (nk > 4) load_b(4, r4);
+    for (int kb = 0; kb < nk; kb += 6) {
+      if (!step(kb, r0, r5)) break;
       if (kb + 1 < nk && !step(kb + 1, r1, r0)) break;
       if (kb + 2 < nk && !step(kb + 2, r2, r1)) break;
       if (kb + 3 < nk && !step(kb + 3, r3, r2)) break;
+      if (kb + 4 < nk && !step(kb + 4, r4, r3)) break;
+      if (kb + 5 < nk && !step(kb + 5, r5, r4)) break;
     }
 
     // ---------------------------------------------------------- epilogue
@@ -477,7 +486,7 @@ cudaError_t launch_grouped_gemm(int mode, const GemmArgs& a, int max_tiles, cuda
       if (e != cudaSuccess) return e;
       attr_done[0][d] = true;
     }
-    const dim3 grid(max_tiles, a.I / (kBN / 2));
+    const dim3 grid(a.I / (kBN / 2), max_tiles);
     grouped_gemm_kernel<1><<<grid, kThreads, smem, st>>>(a);
   } else {
     if (!attr_done[1][d]) {
@@ -486,7 +495,7 @@ cudaError_t launch_grouped_gemm(int mode, const GemmArgs& a, int max_tiles, cuda
       if (e != cudaSuccess) return e;
       attr_done[1][d] = true;
     }
-    const dim3 grid(max_tiles, a.H / kBN);
+    const dim3 grid(a.H / kBN, max_tiles);
     grouped_gemm_kernel<2><<<grid, kThreads, smem, st>>>(a);
   }
   return cudaGetLastError();
