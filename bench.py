@@ -58,6 +58,14 @@ WORKLOADS = {
              "affine g64 dequantised to bf16 into tcgen05 grouped GEMMs; 2 layers alternating, "
              "the next layer copied bank -> buffer on a second stream (double buffer)",
         L=2, H=2048, I=512, E=256, k=8, T=8192, shared=True, router="softmax", prefill=True),
+    "cache_sweep": dict(
+        desc="Cache stress sweep: 40 layers x 256 experts, top-8, Zipf(1.1) routing traces of "
+             "2048 steps per layer with 70% step-to-step overlap fed straight to the control "
+             "step (no router, no fill); capacity 5/10/25/50% of pairs x B_P/B_H in "
+             "{52.7/77.3, 11.8/47.5, 77.3/77.3} GB/s, K=8",
+        L=40, H=64, I=64, E=256, k=8, T=1, shared=False, router="softmax", K=8, sweep=True,
+        trace_steps=2048, caps=(0.05, 0.10, 0.25, 0.50),
+        ratios=((52700, 77300), (11800, 47500), (77300, 77300)), slots=2560, bp=52700, bh=77300),
 }
 
 
@@ -226,9 +234,66 @@ def cpu_baseline(w, xs, wr, bias, budget_s=12.0, max_steps=64):
                       f"float64 FFN) in {r.spent:.1f} s of oracle time, single thread"}
 
 
+def reference_line(args, w, world, val, unit, spent, sample, dtype):
+    return {"impl": "reference", "metric": METRIC, "value": val, "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * spent / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
+            "data": "synthetic", "config": {"workload": args.workload, "desc": w["desc"]},
+            "cpu_baseline": {"value": val, "unit": unit, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_reference_prefill(args, w, world):
+    """Each step is one token of the prefill layer through the oracle (route +
+    float64 FFN, the token's experts dequantised per call): a bounded sample."""
+    x_h, wr_h = prefill_inputs(w)
+    r = PrefillOracle(w, x_h, wr_h)
+    for t in range(args.warmup):
+        r.token(t)
+    r.spent, r.n = 0.0, 0
+    for t in range(args.warmup, args.warmup + args.steps):
+        r.token(t % w["T"])
+    val = r.flops_per_token * r.n / r.spent / 1e12
+    sample = (f"{r.n} tokens of the {w['T']}-token prefill layer (route + float64 FFN), "
+              f"single thread, {r.spent:.1f} s of oracle time")
+    print(json.dumps(reference_line(args, w, world, val, "TFLOP/s", r.spent, sample, "f64")),
+          flush=True)
+
+
+def run_reference_sweep(args, w, world):
+    """Each step is one trace step through all layers' oracle control steps at the
+    capacity-25%, B_P/B_H 52.7/77.3 point of the sweep."""
+    import oracle
+    from moe_expert_offload_gb300 import synth
+
+    oracle.build()
+    L, E, K = w["L"], w["E"], w["K"]
+    n = args.warmup + args.steps
+    tr = np.stack([synth.zipf_trace(1000 + l, n, E, w["k"]) for l in range(L)], axis=1)
+    state = oracle.CacheState(L * E, int(round(0.25 * L * E)))
+    spent = 0.0
+    for s in range(n):
+        if s == args.warmup:
+            spent = 0.0
+        for l in range(L):
+            t0 = time.perf_counter()
+            oracle.cache_step(state, E, l, tr[s, l:l + 1], K, 52700, 77300)
+            spent += time.perf_counter() - t0
+    val = args.steps * L / spent
+    sample = (f"{args.steps} trace steps x {L} layers of oracle control steps, single thread, "
+              f"{spent:.3f} s of oracle time")
+    print(json.dumps(reference_line(args, w, world, val, "layer-steps/s", spent, sample, "int32")),
+          flush=True)
+
+
 def run_reference(args, w, rank, world):
     if rank != 0:
         return
+    if w.get("prefill"):
+        return run_reference_prefill(args, w, world)
+    if w.get("sweep"):
+        return run_reference_sweep(args, w, world)
     n = args.warmup + args.steps
     xs, wr, bias = make_inputs(w, n)
     r = OracleRunner(w, xs, wr, bias)
@@ -240,15 +305,8 @@ def run_reference(args, w, rank, world):
     val = r.tokens / r.spent
     sample = (f"{args.steps} decode steps x {w['L']} layers x batch {w['T']} (route, control, "
               f"float64 FFN), single thread, {r.spent:.1f} s of oracle time")
-    out = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tok/s", "n_gpus": world,
-           "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * r.spent / args.steps,
-           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-           "data": "synthetic", "config": {"workload": args.workload, "desc": w["desc"]},
-           "cpu_baseline": {"value": val, "unit": "tok/s", "cores": 1, "kind": "oracle",
-                            "sample": sample},
-           "e2e": {"value": val, "unit": "tok/s", "h2d_bytes_per_step": 0,
-                   "d2h_bytes_per_step": 0}}
-    print(json.dumps(out), flush=True)
+    print(json.dumps(reference_line(args, w, world, val, "tok/s", r.spent, sample, "f64")),
+          flush=True)
 
 
 # ----------------------------------------------------------------- GPU arm
@@ -576,8 +634,11 @@ def run_prefill(args, w, rank, world, local_rank):
     tflops = flops / (ffn_ms * 1e-3) / 1e12
     step_ms = ms / args.steps
     tokens = args.steps * T * world
+    # value: the whole layer step (route + expert FFN with the next layer's copy
+    # overlapped); the roofline entry is the expert FFN call alone
     out = {
-        "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
+        "metric": METRIC, "value": flops / (step_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
@@ -590,9 +651,11 @@ def run_prefill(args, w, rank, world, local_rank):
                      "algorithmic_flops_per_launch": flops, "avg_launch_us": ffn_ms * 1e3,
                      "peak_kind": f"{peak_kind} bf16 dense, sustained"},
         "prefill_tok_s": tokens / (ms * 1e-3),
+        "ffn_tflops": tflops,
         "layer_ms": {"overlapped_copy": step_ms, "serial_copy": ms_serial / args.steps,
                      "route": route_ms, "ffn": ffn_ms},
-        "e2e": {"value": tokens / (ms_e2e * 1e-3), "unit": "tok/s",
+        "e2e": {"value": flops * args.steps * world / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "tok_s": tokens / (ms_e2e * 1e-3),
                 "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 4},
         "gpu_launches": 10 * args.steps,
         "clocks": clk.summary(),
@@ -602,35 +665,213 @@ def run_prefill(args, w, rank, world, local_rank):
     print(json.dumps(out), flush=True)
 
 
-def cpu_baseline_prefill(w, x_h, wr_h, budget_s=12.0):
-    """The oracle (single thread) on a bounded sample of the prefill layer: routing and the
-    float64 FFN for successive tokens until the budget is spent; reported as TFLOP/s."""
-    import oracle
+def prefill_inputs(w):
     from moe_expert_offload_gb300 import synth
 
-    oracle.build()
-    H, I, E, k = w["H"], w["I"], w["E"], w["k"]
-    blobs = {}
-    shared = synth.make_expert_bytes(np.random.default_rng(12345), H, I)
-    spent, n, t = 0.0, 0, 0
-    while spent < budget_s and t < w["T"]:
-        xb = x_h[0][t:t + 1]
+    L, H, E, T = w["L"], w["H"], w["E"], w["T"]
+    wr_h = [synth.router_weights(100 + l, E, H) for l in range(L)]
+    x_h = [synth.prefill_hidden(500 + l, T, H, wr_h[l]) for l in range(L)]
+    return x_h, wr_h
+
+
+class PrefillOracle:
+    """The oracle on single tokens of prefill layer 0: routing and the float64 FFN
+    (the token's experts dequantised per call).  Blob generation is untimed."""
+
+    def __init__(self, w, x_h, wr_h):
+        import oracle
+        from moe_expert_offload_gb300 import synth
+
+        oracle.build()
+        self.o, self.synth, self.w, self.x, self.wr = oracle, synth, w, x_h[0], wr_h[0]
+        self.blobs = {}
+        self.shared = synth.make_expert_bytes(np.random.default_rng(12345), w["H"], w["I"])
+        self.flops_per_token = 6.0 * w["H"] * w["I"] * (w["k"] + 1)
+        self.spent, self.n = 0.0, 0
+
+    def token(self, t):
+        o, w = self.o, self.w
+        xb = self.x[t:t + 1]
         t0 = time.perf_counter()
-        ids, wt = oracle.route_softmax_topk(oracle.router_logits(xb, wr_h[0]), k)
-        spent += time.perf_counter() - t0
+        ids, wt = o.route_softmax_topk(o.router_logits(xb, self.wr), w["k"])
+        self.spent += time.perf_counter() - t0
         for e in ids.reshape(-1):
-            if int(e) not in blobs:
-                blobs[int(e)] = synth.make_expert_bytes(np.random.default_rng(int(e) + 1), H, I)
-        anyb = blobs[int(ids[0, 0])]
-        full = [blobs.get(e, anyb) for e in range(E)]
+            if int(e) not in self.blobs:
+                self.blobs[int(e)] = self.synth.make_expert_bytes(np.random.default_rng(int(e) + 1),
+                                                                  w["H"], w["I"])
+        anyb = self.blobs[int(ids[0, 0])]
+        full = [self.blobs.get(e, anyb) for e in range(w["E"])]
         t0 = time.perf_counter()
-        oracle.moe_ffn(full, H, I, xb, ids, wt, shared, I)
-        spent += time.perf_counter() - t0
-        n += 1
+        o.moe_ffn(full, w["H"], w["I"], xb, ids, wt, self.shared, w["I"])
+        self.spent += time.perf_counter() - t0
+        self.n += 1
+
+
+def cpu_baseline_prefill(w, x_h, wr_h, budget_s=12.0):
+    """The oracle (single thread) on a bounded sample of the prefill layer: successive
+    tokens until the budget is spent; reported as TFLOP/s."""
+    r = PrefillOracle(w, x_h, wr_h)
+    t = 0
+    while r.spent < budget_s and t < w["T"]:
+        r.token(t)
         t += 1
-    per_tok = 6.0 * H * I * (k + 1)
-    return {"value": per_tok * n / spent / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n} prefill tokens (route + float64 FFN, experts dequantised per call) in "
+    return {"value": r.flops_per_token * r.n / r.spent / 1e12, "unit": "TFLOP/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{r.n} prefill tokens (route + float64 FFN, experts dequantised per call) "
+                      f"in {r.spent:.1f} s, single thread"}
+
+
+# ------------------------------------------------------------- cache sweep
+def sweep_traces(w):
+    """Zipf routing traces int32 [steps][L][k], layer l drawn with seed 1000 + l."""
+    from moe_expert_offload_gb300 import synth
+
+    per_layer = [synth.zipf_trace(1000 + l, w["trace_steps"], w["E"], w["k"]) for l in range(w["L"])]
+    return np.ascontiguousarray(np.stack(per_layer, axis=1))
+
+
+def sweep_points(w):
+    return [(cap, int(round(cap * w["L"] * w["E"])), bp, bh)
+            for cap in w["caps"] for bp, bh in w["ratios"]]
+
+
+def run_sweep(args, w, rank, world, local_rank):
+    """Config 5: every (capacity, B_P/B_H) point runs the 2048-step x 40-layer trace
+    through moe_cache_step from a reset cache; one CUDA graph per 64 trace steps.
+    Each call's counts land in their own row of a device array (the plan struct of
+    call i points there), so the statistics cost no extra work in the timed region."""
+    import torch
+
+    import moe_expert_offload_gb300 as m
+    from moe_expert_offload_gb300 import _build
+
+    _build.build()
+    m.lib()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    L, E, k, K, n = w["L"], w["E"], w["k"], w["K"], w["trace_steps"]
+    spec = spec_of(w)
+    tr_h = sweep_traces(w)                                   # [n][L][k]
+    tr = torch.from_numpy(tr_h).to(dev)
+    calls = n * L
+    base = m.DevicePlan(k, K, device=dev)
+    stats = torch.zeros((calls, 8), dtype=torch.int32, device=dev)
+    b = base.buf
+    bp_ = [m._ptr(b[x]) for x in m.DevicePlan.NAMES]
+    plans = [m.MoePlan(k, *bp_, m._ptr(base.victims), stats.data_ptr() + 32 * i,
+                       m._ptr(base.err)) for i in range(calls)]
+    tr_ptr = tr.data_ptr()
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    chunk = 64
+
+    def capture(cache):
+        graphs = []
+        for s0 in range(0, n, chunk):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                sh = torch.cuda.current_stream().cuda_stream
+                for st in range(s0, min(n, s0 + chunk)):
+                    for l in range(L):
+                        i = st * L + l
+                        m.moe_cache_step(spec, cache.c, l, tr_ptr + 4 * k * i, 1, plans[i], 0, sh)
+            graphs.append(g)
+        return graphs
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    rows, head = [], None
+    with ClockSampler(local_rank) as clk:
+        for cap, S, bp, bh in sweep_points(w):
+            cache = m.DeviceCache(spec, S, K, bp, bh, bank=None, device=dev, with_pool=False)
+            graphs = capture(cache)
+            for rep in range(2):          # a warm pass, then the timed pass, each from reset
+                m.moe_cache_reset(spec, cache.c, sp)
+                torch.cuda.synchronize()
+                e0.record(stream)
+                for g in graphs:
+                    g.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            st = stats.cpu().numpy().astype(np.int64)
+            if int(base.err.cpu()[0]) != 0:
+                raise RuntimeError("control step flagged an error in the sweep")
+            row = {"capacity": cap, "slots": S, "bp_bh": f"{bp / 1000:.1f}/{bh / 1000:.1f}",
+                   "miss_rate": float(st[:, 2].sum() / max(st[:, 0].sum(), 1)),
+                   "mean_uniq": float(st[:, 0].mean()), "mean_hits": float(st[:, 1].mean()),
+                   "mean_F": float(st[:, 4].mean()), "mean_C": float(st[:, 5].mean()),
+                   "mean_q": float(st[:, 3].mean()),
+                   "control_us_per_layer": 1e3 * ms / calls}
+            rows.append(row)
+            if cap == 0.25 and (bp, bh) == (52700, 77300):
+                head = (row, ms, cache, graphs)
+            else:
+                del graphs
+            torch.cuda.synchronize()
+    row, ms, cache, graphs = head
+
+    # end to end at the headline point: each 64-step chunk of the trace is copied
+    # in from pinned host memory and its counts copied back, inside the timed region
+    tr_host = torch.from_numpy(tr_h).pin_memory()
+    st_host = torch.empty((calls, 8), dtype=torch.int32).pin_memory()
+    m.moe_cache_reset(spec, cache.c, sp)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for j, g in enumerate(graphs):
+        s0, s1 = j * chunk, min(n, (j + 1) * chunk)
+        tr[s0:s1].copy_(tr_host[s0:s1], non_blocking=True)
+        g.replay()
+        st_host[s0 * L:s1 * L].copy_(stats[s0 * L:s1 * L], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1)
+    if rank != 0:
+        return
+    hbm, _, peak_kind = peaks()
+    t_call = ms * 1e-3 / calls
+    scan = row["slots"] * 8 + (k + K) * 16            # ts + id_of_slot scan, plan rows
+    out = {
+        "metric": METRIC, "value": calls / (ms * 1e-3), "unit": "layer-steps/s",
+        "n_gpus": world, "steps": n, "warmup": 1, "ms_per_step": ms / n,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "desc": w["desc"], "layers": L,
+                   "headline_point": "capacity 25%, B_P/B_H 52.7/77.3",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "integer tables (<1 MB) stay in L2; this is a latency measurement"},
+        "roofline": {"bound": "hbm", "achieved": scan / t_call / 1e9, "peak": hbm, "unit": "GB/s",
+                     "frac": scan / t_call / 1e9 / hbm, "traffic": None,
+                     "kernel": "control step (one CTA, latency-bound)", "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": scan, "avg_launch_us": t_call * 1e6},
+        "sweep": rows,
+        "e2e": {"value": calls / (ms_e2e * 1e-3), "unit": "layer-steps/s",
+                "h2d_bytes_per_step": L * k * 4, "d2h_bytes_per_step": L * 32},
+        "gpu_launches": calls,
+        "clocks": clk.summary(),
+    }
+    if world == 1 and not args.no_cpu:
+        out["cpu_baseline"] = cpu_baseline_sweep(w, tr_h)
+    print(json.dumps(out), flush=True)
+
+
+def cpu_baseline_sweep(w, tr_h, budget_s=10.0):
+    """The oracle control step (single thread) at the headline sweep point, on the
+    first trace steps until the budget is spent; layer-steps/s."""
+    import oracle
+
+    oracle.build()
+    L, E, K = w["L"], w["E"], w["K"]
+    state = oracle.CacheState(L * E, int(round(0.25 * L * E)))
+    spent, calls, s = 0.0, 0, 0
+    while s < tr_h.shape[0] and (spent < budget_s or s == 0):
+        for l in range(L):
+            t0 = time.perf_counter()
+            oracle.cache_step(state, E, l, tr_h[s, l:l + 1], K, 52700, 77300)
+            spent += time.perf_counter() - t0
+            calls += 1
+        s += 1
+    return {"value": calls / spent, "unit": "layer-steps/s", "cores": 1, "kind": "oracle",
+            "sample": f"{s} trace steps x {L} layers at capacity 25%, B_P/B_H 52.7/77.3 in "
                       f"{spent:.1f} s, single thread"}
 
 
@@ -671,6 +912,8 @@ def main():
         torch.distributed.init_process_group("nccl")
     if w.get("prefill"):
         run_prefill(args, w, rank, world, local_rank)
+    elif w.get("sweep"):
+        run_sweep(args, w, rank, world, local_rank)
     else:
         run_gpu(args, w, rank, world, local_rank)
     if world > 1:

@@ -41,6 +41,7 @@
 #include <cuda_bf16.h>
 
 #include "moe_internal.cuh"
+#include "stream_common.cuh"
 
 namespace moe {
 namespace {
@@ -57,7 +58,11 @@ constexpr int kHalfBytes = 128 * kBK * 2;        // 16 KB: one 128-row half of A
 constexpr int kABytes = kBM * kBK * 2;           // 32 KB
 constexpr int kBBytes = kBN * kBK * 2;           // 32 KB
 constexpr int kTmemCols = 512;
-constexpr int kAhead = 5;                        // k-blocks of B codes requested ahead
+// int4 codes reach shared memory by TMA: each dequant warp owns a ring of
+// kCodeStages boxes of its 32 B rows x 32 bytes (one k-block), so the code
+// loads leave the load/store pipe to the A gather and the bf16 stores
+constexpr int kCodeStages = 3;
+constexpr int kCodeBox = 32 * 32;
 constexpr uint32_t kWaitIters = 1u << 20;
 
 // ------------------------------------------------------------- PTX wrappers
@@ -180,16 +185,19 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t addr) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(addr) : "memory");
 }
 
-struct BRegs {
-  uint4 q0, q1;   // the B row's 32 code bytes of one k-block
-  uint32_t s, b;  // scale / bias words holding groups kb & ~1 and kb | 1
+// Code maps of one GEMM: m[0] over the layer's E blobs, m[1] over the shared
+// expert's blob; u32 words [blob][B row][K / 8], boxes of 8 words x 32 rows.
+struct GemmMaps {
+  CUtensorMap m[2];
 };
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(GemmArgs g) {
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(GemmArgs g, const __grid_constant__ GemmMaps maps) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t full_a[kStagesA], empty_a[kStagesA];
   __shared__ __align__(8) uint64_t full_b[kStagesB], empty_b[kStagesB], acc_full;
+  __shared__ __align__(8) uint64_t code_full[kDqWarps][kCodeStages];
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int s_fail;
   __shared__ const uint16_t* arow_s[kBM];
@@ -210,6 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(GemmArgs g) {
   const uint32_t a_addr = sbase;
   const uint32_t b_addr = sbase + kStagesA * kABytes;
   unsigned char* b_ptr = gbase + kStagesA * kABytes;
+  const uint32_t code_addr = b_addr + kStagesB * kBBytes;
+  const unsigned char* code_ptr = b_ptr + kStagesB * kBBytes;
 
   // A source row of every tile row (null past the group's rows)
   for (int r = tid; r < kBM; r += kThreads) {
@@ -243,6 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(GemmArgs g) {
       mbar_init(smem_u32(&empty_b[i]), 1);
     }
     mbar_init(smem_u32(&acc_full), 1);
+    for (int i = 0; i < kDqWarps * kCodeStages; ++i) mbar_init(smem_u32(&code_full[0][0] + i), 1);
     s_fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -315,40 +326,89 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(GemmArgs g) {
     __syncwarp();
   } else {
     // ------------------------------------------- B dequantisation (row t)
-    const int t = tid - kDqWarp0 * 32;
+    const int t = tid - kDqWarp0 * 32, w = wid - kDqWarp0;  // warp w: B rows 32w .. 32w+31
     const uint8_t* blob = (grp < g.E) ? g.experts + (int64_t)grp * g.blob_bytes : g.shared;
     const BlobOffsets off = blob_offsets(H, I);
-    int64_t row, qo, so, bo;
+    int64_t row, so, bo;
+    int my;  // first row of this warp's code box in the map
     if (MODE == 1) {
       const bool up = t >= kBN / 2;
       row = (int64_t)nt * (kBN / 2) + (up ? t - kBN / 2 : t);
-      qo = up ? off.uq : off.gq;
       so = up ? off.us : off.gs;
       bo = up ? off.ub : off.gb;
+      my = (up ? I : 0) + nt * (kBN / 2) + 32 * (w & 3);  // up rows follow the gate rows
     } else {
       row = (int64_t)nt * kBN + t;
-      qo = off.dq;
       so = off.ds;
       bo = off.db;
+      my = nt * kBN + 32 * w;
     }
-    const uint8_t* qrow = blob + qo + row * (K / 2);
-    const uint8_t* srow = blob + so + row * (K / kGroup) * 2;
-    const uint8_t* brw = blob + bo + row * (K / kGroup) * 2;
-    auto load_b = [&](int kb, BRegs& r) {
-      r.q0 = __ldg(reinterpret_cast<const uint4*>(qrow + kb * 32));
-      r.q1 = __ldg(reinterpret_cast<const uint4*>(qrow + kb * 32 + 16));
-      r.s = __ldg(reinterpret_cast<const uint32_t*>(srow + (kb & ~1) * 2));
-      r.b = __ldg(reinterpret_cast<const uint32_t*>(brw + (kb & ~1) * 2));
+    const int G = K / kGroup;
+    const bool g8 = (G & 7) == 0;  // scales fetched 8 groups (16 bytes) at a time, else 2
+    const int span = g8 ? 8 : 2;
+    const uint8_t* srow = blob + so + row * G * 2;
+    const uint8_t* brw = blob + bo + row * G * 2;
+    const CUtensorMap* map = &maps.m[grp < g.E ? 0 : 1];
+    const int mz = grp < g.E ? grp : 0;
+    const uint32_t cbase = code_addr + (uint32_t)(w * kCodeStages * kCodeBox);
+    const unsigned char* cptr = code_ptr + w * kCodeStages * kCodeBox;
+    auto issue = [&](int kb) {  // lane 0: the codes of block kb into slot kb % kCodeStages
+      const uint32_t bar = smem_u32(&code_full[w][kb % kCodeStages]);
+      sc::bar_expect(bar, kCodeBox);
+      sc::tma_load_3d(cbase + (kb % kCodeStages) * kCodeBox, map, kb * 8, my, mz, bar);
     };
-    auto dequant = [&](int kb, const BRegs& r) {
-      const uint32_t sh = (kb & 1) ? (r.s >> 16) : (r.s & 0xFFFFu);
-      const uint32_t bh = (kb & 1) ? (r.b >> 16) : (r.b & 0xFFFFu);
+    int issued = 0;
+    if (lane == 0) {
+      sc::tma_prefetch_map(map);
+      for (; issued < nk && issued < kCodeStages; ++issued) issue(issued);
+    }
+    struct SB { uint32_t s0, s1, s2, s3, b0, b1, b2, b3; };
+    auto load_sb = [&](int kb, SB& v) {
+      if (g8) {
+        const uint4 a = __ldg(reinterpret_cast<const uint4*>(srow + kb * 2));
+        const uint4 b = __ldg(reinterpret_cast<const uint4*>(brw + kb * 2));
+        v = SB{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      } else {
+        v.s0 = __ldg(reinterpret_cast<const uint32_t*>(srow + kb * 2));
+        v.b0 = __ldg(reinterpret_cast<const uint32_t*>(brw + kb * 2));
+      }
+    };
+    SB cur{}, nxt{};
+    load_sb(0, cur);
+    if (span < nk) load_sb(span, nxt);
+    const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.0f, 128.0f);
+    int kb = 0;
+    bool failed = false;
+    for (; kb < nk; ++kb) {
+      const int sb = kb % kStagesB, use = kb / kStagesB, cs = kb % kCodeStages;
+      if (kb > 0 && kb % span == 0) {
+        cur = nxt;
+        if (kb + span < nk) load_sb(kb + span, nxt);
+      }
+      // the stage's previous MMAs are done (lane 0), this block's codes have landed (all lanes)
+      if (lane == 0 && use > 0 && !mbar_wait(smem_u32(&empty_b[sb]), (use - 1) & 1)) s_fail = 1;
+      const bool cok = mbar_wait(smem_u32(&code_full[w][cs]), (kb / kCodeStages) & 1);
+      if (!__all_sync(0xffffffffu, cok) && lane == 0) s_fail = 1;
+      if (__shfl_sync(0xffffffffu, (int)s_fail, 0)) {
+        failed = true;
+        break;
+      }
+      const uint4 q0 = *reinterpret_cast<const uint4*>(cptr + cs * kCodeBox + lane * 32);
+      const uint4 q1 = *reinterpret_cast<const uint4*>(cptr + cs * kCodeBox + lane * 32 + 16);
+      // every lane's reads of the slot come before its refill through the async proxy
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0 && issued < nk) issue(issued++);
+      const int gi = kb % span;  // group within the fetched span
+      const uint32_t sw = gi < 2 ? cur.s0 : gi < 4 ? cur.s1 : gi < 6 ? cur.s2 : cur.s3;
+      const uint32_t bw = gi < 2 ? cur.b0 : gi < 4 ? cur.b1 : gi < 6 ? cur.b2 : cur.b3;
+      const uint32_t sh = (gi & 1) ? (sw >> 16) : (sw & 0xFFFFu);
+      const uint32_t bh = (gi & 1) ? (bw >> 16) : (bw & 0xFFFFu);
       const uint32_t s2u = sh | (sh << 16), b2u = bh | (bh << 16);
       const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162*>(&s2u);
       const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&b2u);
-      const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.0f, 128.0f);
-      const uint32_t words[8] = {r.q0.x, r.q0.y, r.q0.z, r.q0.w, r.q1.x, r.q1.y, r.q1.z, r.q1.w};
-      unsigned char* bb = b_ptr + (kb % kStagesB) * kBBytes;
+      const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+      unsigned char* bb = b_ptr + sb * kBBytes;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         uint32_t o[4];
@@ -356,45 +416,19 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(GemmArgs g) {
         for (int i = 0; i < 4; ++i) {
           uint32_t v = ((words[c] >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
           const __nv_bfloat162 q = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v), k128);
-          const __nv_bfloat162 w = __hfma2(q, s2, b2);
-          o[i] = *reinterpret_cast<const uint32_t*>(&w);
+          const __nv_bfloat162 wv = __hfma2(q, s2, b2);
+          o[i] = *reinterpret_cast<const uint32_t*>(&wv);
         }
         *reinterpret_cast<uint4*>(bb + swz(t, c)) = make_uint4(o[0], o[1], o[2], o[3]);
       }
-    };
-    // one B stage: wait until the MMAs of its previous use are done (lane 0,
-    // broadcast), prefetch block kb+kAhead, dequantise block kb, mark the stage full
-    auto step = [&](int kb, const BRegs& cur, BRegs& nxt) -> bool {
-      const int sb = kb % kStagesB, use = kb / kStagesB;
-      int ok = 1;
-      if (lane == 0) {
-        if (use > 0 && !mbar_wait(smem_u32(&empty_b[sb]), (use - 1) & 1)) s_fail = 1;
-        ok = !s_fail;
-      }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
-      if (kb + kAhead < nk) load_b(kb + kAhead, nxt);
-      dequant(kb, cur);
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&full_b[sb]));
-      return true;
-    };
-    // six named sets in rotation: block kb lives in set kb % 6, its codes are
-    // requested five blocks (~5 x 1200 cycles) before they are dequantised
-    BRegs r0, r1, r2, r3, r4, r5;
-    load_b(0, r0);
-    if (nk > 1) load_b(1, r1);
-    if (nk > 2) load_b(2, r2);
-    if (nk > 3) load_b(3, r3);
-    if (nk > 4) load_b(4, r4);
-    for (int kb = 0; kb < nk; kb += 6) {
-      if (!step(kb, r0, r5)) break;
-      if (kb + 1 < nk && !step(kb + 1, r1, r0)) break;
-      if (kb + 2 < nk && !step(kb + 2, r2, r1)) break;
-      if (kb + 3 < nk && !step(kb + 3, r3, r2)) break;
-      if (kb + 4 < nk && !step(kb + 4, r4, r3)) break;
-      if (kb + 5 < nk && !step(kb + 5, r5, r4)) break;
     }
+    // after a failed wait: let this warp's code copies still in flight land (bounded)
+    if (failed && lane == 0)
+      for (int j = kb; j < issued; ++j)
+        mbar_wait(smem_u32(&code_full[w][j % kCodeStages]), (j / kCodeStages) & 1);
 
     // ---------------------------------------------------------- epilogue
     int ok = 1;
@@ -474,11 +508,29 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(GemmArgs g) {
 
 cudaError_t launch_grouped_gemm(int mode, const GemmArgs& a, int max_tiles, cudaStream_t st) {
   static bool attr_done[2][64] = {};
-  const size_t smem = 1024 + (size_t)kStagesA * kABytes + (size_t)kStagesB * kBBytes;
+  const size_t smem = 1024 + (size_t)kStagesA * kABytes + (size_t)kStagesB * kBBytes +
+                      (size_t)kDqWarps * kCodeStages * kCodeBox;
   int d = 0;
   cudaError_t e = cudaGetDevice(&d);
   if (e != cudaSuccess) return e;
   if (d < 0 || d >= 64) return cudaErrorInvalidDevice;
+  // code maps: mode 1 the gate rows then the up rows ([2I][H/2] bytes, contiguous
+  // in the blob), mode 2 the down rows ([H][I/2] bytes)
+  const BlobOffsets off = blob_offsets(a.H, a.I);
+  const int64_t K = mode == 1 ? a.H : a.I;
+  const uint64_t rows = mode == 1 ? 2 * (uint64_t)a.I : (uint64_t)a.H;
+  const int64_t q0 = mode == 1 ? off.gq : off.dq;
+  GemmMaps maps;
+  const uint8_t* bases[2] = {a.experts, a.shared ? a.shared : a.experts};
+  const uint64_t nblob[2] = {(uint64_t)a.E, 1};
+  for (int i = 0; i < 2; ++i) {
+    const uint64_t dims[3] = {(uint64_t)K / 8, rows, nblob[i]};
+    const uint64_t strides[2] = {(uint64_t)K / 2, (uint64_t)a.blob_bytes};
+    const uint32_t box[3] = {8, 32, 1};
+    if ((e = encode_tiled_u32(&maps.m[i], bases[i] + q0, 3, dims, strides, box, false)) !=
+        cudaSuccess)
+      return e;
+  }
   if (mode == 1) {
     if (!attr_done[0][d]) {
       e = cudaFuncSetAttribute(grouped_gemm_kernel<1>,
@@ -487,7 +539,7 @@ cudaError_t launch_grouped_gemm(int mode, const GemmArgs& a, int max_tiles, cuda
       attr_done[0][d] = true;
     }
     const dim3 grid(a.I / (kBN / 2), max_tiles);
-    grouped_gemm_kernel<1><<<grid, kThreads, smem, st>>>(a);
+    grouped_gemm_kernel<1><<<grid, kThreads, smem, st>>>(a, maps);
   } else {
     if (!attr_done[1][d]) {
       e = cudaFuncSetAttribute(grouped_gemm_kernel<2>,
@@ -496,7 +548,7 @@ cudaError_t launch_grouped_gemm(int mode, const GemmArgs& a, int max_tiles, cuda
       attr_done[1][d] = true;
     }
     const dim3 grid(a.H / kBN, max_tiles);
-    grouped_gemm_kernel<2><<<grid, kThreads, smem, st>>>(a);
+    grouped_gemm_kernel<2><<<grid, kThreads, smem, st>>>(a, maps);
   }
   return cudaGetLastError();
 }

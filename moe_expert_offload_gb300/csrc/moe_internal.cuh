@@ -64,11 +64,12 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-// Tiled TMA descriptor over u32 elements, 128-byte swizzle, rank <= 5:
-// dims[0] innermost, strides[i] = bytes between consecutive indices of
+// Tiled TMA descriptor over u32 elements, rank <= 5, 128-byte swizzle (or
+// none): dims[0] innermost, strides[i] = bytes between consecutive indices of
 // dimension i + 1.  Returns cudaErrorNotSupported without a driver encoder.
 cudaError_t encode_tiled_u32(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                             const uint64_t* strides, const uint32_t* box);
+                             const uint64_t* strides, const uint32_t* box,
+                             bool swizzle128 = true);
 
 // ---------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error.
@@ -168,6 +169,9 @@ struct PrefillBufs {
   int32_t* n_tiles;
   uint16_t* h_perm;         // [T*k + T][I]
   uint16_t* y_assign;       // [T][k + 1][H]
+  int32_t* chunk_cnt;       // [nch][E]: assignments of each expert per chunk of ids
+  int32_t* chunk_base;      // [nch][E]: where each chunk's ids of an expert start in perm
+  int nch;
   int max_tiles;
 };
 

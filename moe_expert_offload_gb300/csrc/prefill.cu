@@ -5,7 +5,7 @@
 //   1. x -> x_perm: each 8-element chunk reordered 0,4,1,5,2,6,3,7 (the K
 //      order of the GEMM operands).
 //   2. routing permute: a stable counting sort of the T*k (token, rank)
-//      assignments by expert; the shared expert (if any) is one more group
+//      assignments by expert, in chunks of 2048 ids; the shared expert (if any) is one more group
 //      holding every token in order.  Offsets, and 256-row m-tiles per group.
 //   3. GEMM1 (gate/up + SwiGLU) and GEMM2 (down, weighted per assignment).
 //   4. combine: y[t] = sum over j = 0..k of y_assign[t][j], in j order.
@@ -29,18 +29,23 @@ __global__ void permute_x_kernel(const uint4* __restrict__ x, uint4* __restrict_
   }
 }
 
-__global__ void zero_i32_kernel(int32_t* p, int n) {
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = 0;
-}
+// Assignments are permuted in chunks of kChunk ids (8 warps x 256): the
+// chunk's per-expert counts, then every chunk's base in each group, then each
+// warp places its ids in order.  The result is the stable counting sort.
+constexpr int kChunk = 2048;
+constexpr int kChunkWarps = 8;
+constexpr int kWarpIds = kChunk / kChunkWarps;
 
-// Per-expert assignment counts (ids outside [0, E) are flagged and skipped).
-__global__ void hist_kernel(const int32_t* __restrict__ ids, int n, int E, int32_t* counts,
-                            int32_t* err) {
+// chunk c: per-expert counts cnt[c][e] (ids outside [0, E) are flagged and skipped)
+__global__ void __launch_bounds__(256) chunk_count_kernel(const int32_t* __restrict__ ids, int n,
+                                                          int E, int32_t* __restrict__ cnt,
+                                                          int32_t* err) {
   extern __shared__ int32_t h[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
   __syncthreads();
   bool bad = false;
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+  const int i0 = blockIdx.x * kChunk, i1 = min(n, i0 + kChunk);
+  for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
     const int e = ids[i];
     if (e >= 0 && e < E)
       atomicAdd(&h[e], 1);
@@ -49,13 +54,14 @@ __global__ void hist_kernel(const int32_t* __restrict__ ids, int n, int E, int32
   }
   if (bad && err) atomicOr(err, MOE_DERR_BAD_ID);
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x)
-    if (h[e]) atomicAdd(&counts[e], h[e]);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[(int64_t)blockIdx.x * E + e] = h[e];
 }
 
 // One CTA: group offsets (exclusive scan of counts, group E = shared expert
 // with T rows) and the m-tile table (256 rows per tile, ragged last tile).
-__global__ void __launch_bounds__(1024) plan_kernel(int32_t* counts, int E, int T,
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ cnt, int nch,
+                                                    int32_t* __restrict__ cbase,
+                                                    int32_t* counts, int E, int T,
                                                     int has_shared, int32_t* offsets,
                                                     int32_t* tile_g, int32_t* tile_row0,
                                                     int32_t* tile_rows, int32_t* n_tiles,
@@ -63,11 +69,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(int32_t* counts, int E, int 
   __shared__ int s_wr[32], s_wt[32];
   const int G = E + 1;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  if (tid == E) counts[E] = has_shared ? T : 0;
-  // each thread owns one group (G = E + 1 <= 1024)
+  // each thread owns one group (G = E + 1 <= 1024); routed group totals from the chunk counts
   int c = 0, t = 0;
+  if (tid < E)
+    for (int ch = 0; ch < nch; ++ch) c += cnt[(int64_t)ch * E + tid];
+  else if (tid == E)
+    c = has_shared ? T : 0;
   if (tid < G) {
-    c = (tid == E) ? (has_shared ? T : 0) : counts[tid];
+    counts[tid] = c;
     t = (c + kTileRows - 1) / kTileRows;
   }
   // block exclusive scans of rows and tiles
@@ -101,6 +110,13 @@ __global__ void __launch_bounds__(1024) plan_kernel(int32_t* counts, int E, int 
   __syncthreads();
   const int base_r = (wid > 0 ? s_wr[wid - 1] : 0) + ir - c;
   const int base_t = (wid > 0 ? s_wt[wid - 1] : 0) + it - t;
+  if (tid < E) {  // where each chunk's ids of group tid start
+    int run = base_r;
+    for (int ch = 0; ch < nch; ++ch) {
+      cbase[(int64_t)ch * E + tid] = run;
+      run += cnt[(int64_t)ch * E + tid];
+    }
+  }
   if (tid < G) {
     offsets[tid] = base_r;
     for (int j = 0; j < t; ++j) {
@@ -118,35 +134,53 @@ __global__ void __launch_bounds__(1024) plan_kernel(int32_t* counts, int E, int 
   }
 }
 
-// CTA g: the assignments routed to expert g, in ascending (t, j) order, to
-// perm[offsets[g] ...]; CTA E (shared expert) writes T*k + t for every token.
-__global__ void __launch_bounds__(256) scatter_kernel(const int32_t* __restrict__ ids, int n,
-                                                      int T, const int32_t* __restrict__ offsets,
-                                                      int32_t* __restrict__ perm, int E) {
-  __shared__ int s_w[8];
-  const int g = blockIdx.x;
-  const int base = offsets[g];
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  if (g == E) {
+// CTA c < nch: chunk c's ids to perm in ascending order within each group.
+// Each warp counts its 256 ids per expert, the warps' starts follow from the
+// chunk base, then each warp walks its ids 32 at a time (lanes of equal
+// expert ranked by lane).  CTA nch (shared expert) writes T*k + t for every t.
+__global__ void __launch_bounds__(kChunkWarps * 32) scatter_kernel(
+    const int32_t* __restrict__ ids, int n, int T, int E, int nch,
+    const int32_t* __restrict__ cbase, const int32_t* __restrict__ offsets,
+    int32_t* __restrict__ perm) {
+  extern __shared__ int32_t wb[];  // [kChunkWarps][E]: per-warp counts, then starts
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  if (blockIdx.x == nch) {
+    const int base = offsets[E];
     for (int t = tid; t < T; t += blockDim.x) perm[base + t] = n + t;
     return;
   }
-  int run = 0;
-  for (int i0 = 0; i0 < n; i0 += blockDim.x) {
-    const int i = i0 + tid;
-    const bool m = i < n && ids[i] == g;
-    const unsigned b = __ballot_sync(0xffffffffu, m);
-    if (lane == 0) s_w[wid] = __popc(b);
-    __syncthreads();
-    int pre = 0, tot = 0;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      pre += (w < wid) ? s_w[w] : 0;
-      tot += s_w[w];
+  for (int i = tid; i < kChunkWarps * E; i += blockDim.x) wb[i] = 0;
+  __syncthreads();
+  const int i0 = blockIdx.x * kChunk + w * kWarpIds, i1 = min(n, i0 + kWarpIds);
+  for (int b = i0; b < i1; b += 32) {
+    const int i = b + lane;
+    int e = i < i1 ? ids[i] : -1;
+    if (e < 0 || e >= E) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) wb[w * E + e] += __popc(peers);
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) {
+    int run = cbase[(int64_t)blockIdx.x * E + e];
+    for (int v = 0; v < kChunkWarps; ++v) {
+      const int c = wb[v * E + e];
+      wb[v * E + e] = run;
+      run += c;
     }
-    if (m) perm[base + run + pre + __popc(b & ((1u << lane) - 1u))] = i;
-    run += tot;
-    __syncthreads();
+  }
+  __syncthreads();
+  for (int b = i0; b < i1; b += 32) {
+    const int i = b + lane;
+    int e = i < i1 ? ids[i] : -1;
+    if (e < 0 || e >= E) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0) {
+      const int start = wb[w * E + e];
+      perm[start + __popc(peers & ((1u << lane) - 1u))] = i;
+    }
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) wb[w * E + e] += __popc(peers);
+    __syncwarp();
   }
 }
 
@@ -192,9 +226,10 @@ int max_tiles_for(int E, int k, int T) {
 size_t prefill_workspace_bytes(int H, int I, int E, int k, int T) {
   const size_t R = (size_t)T * k + T;
   const size_t mt = max_tiles_for(E, k, T);
+  const size_t nch = ((size_t)T * k + kChunk - 1) / kChunk;
   return al256((size_t)T * H * 2) + al256((size_t)(E + 1) * 4) + al256((size_t)(E + 2) * 4) +
          al256(R * 4) + 3 * al256(mt * 4) + al256(4) + al256(R * I * 2) +
-         al256((size_t)T * (k + 1) * H * 2);
+         al256((size_t)T * (k + 1) * H * 2) + 2 * al256(nch * E * 4);
 }
 
 void prefill_carve(PrefillBufs& b, void* ws, int H, int I, int E, int k, int T) {
@@ -216,6 +251,9 @@ void prefill_carve(PrefillBufs& b, void* ws, int H, int I, int E, int k, int T) 
   b.n_tiles = reinterpret_cast<int32_t*>(take(4));
   b.h_perm = reinterpret_cast<uint16_t*>(take(R * I * 2));
   b.y_assign = reinterpret_cast<uint16_t*>(take((size_t)T * (k + 1) * H * 2));
+  b.nch = (int)(((size_t)T * k + kChunk - 1) / kChunk);
+  b.chunk_cnt = reinterpret_cast<int32_t*>(take((size_t)b.nch * E * 4));
+  b.chunk_base = reinterpret_cast<int32_t*>(take((size_t)b.nch * E * 4));
   b.max_tiles = (int)mt;
 }
 
@@ -227,12 +265,12 @@ cudaError_t launch_prefill_ffn(const GemmArgs& base, const PrefillBufs& b, const
   const int64_t nx = (int64_t)T * H / 8;
   permute_x_kernel<<<(int)((nx + 255) / 256 < 4096 ? (nx + 255) / 256 : 4096), 256, 0, st>>>(
       reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(b.x_perm), nx);
-  zero_i32_kernel<<<1, 256, 0, st>>>(b.counts, E + 1);
-  const int hb = (n + 1023) / 1024 < 256 ? (n + 1023) / 1024 : 256;
-  hist_kernel<<<hb > 0 ? hb : 1, 256, E * 4, st>>>(ids, n, E, b.counts, base.err);
-  plan_kernel<<<1, 1024, 0, st>>>(b.counts, E, T, has_shared, b.offsets, b.tile_g, b.tile_row0,
-                                  b.tile_rows, b.n_tiles, b.max_tiles);
-  scatter_kernel<<<E + (has_shared ? 1 : 0), 256, 0, st>>>(ids, n, T, b.offsets, b.perm, E);
+  chunk_count_kernel<<<b.nch, 256, E * 4, st>>>(ids, n, E, b.chunk_cnt, base.err);
+  plan_kernel<<<1, 1024, 0, st>>>(b.chunk_cnt, b.nch, b.chunk_base, b.counts, E, T, has_shared,
+                                  b.offsets, b.tile_g, b.tile_row0, b.tile_rows, b.n_tiles,
+                                  b.max_tiles);
+  scatter_kernel<<<b.nch + (has_shared ? 1 : 0), kChunkWarps * 32, kChunkWarps * E * 4, st>>>(
+      ids, n, T, E, b.nch, b.chunk_base, b.offsets, b.perm);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   GemmArgs a = base;

@@ -26,7 +26,7 @@ EncodeTiledFn encoder() {
 }  // namespace
 
 cudaError_t encode_tiled_u32(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                             const uint64_t* strides, const uint32_t* box) {
+                             const uint64_t* strides, const uint32_t* box, bool swizzle128) {
   EncodeTiledFn fn = encoder();
   if (!fn) return cudaErrorNotSupported;
   cuuint64_t d[5], s[4];
@@ -39,7 +39,8 @@ cudaError_t encode_tiled_u32(CUtensorMap* map, const void* base, int rank, const
   }
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, (cuuint32_t)rank,
                         const_cast<void*>(base), d, s, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
