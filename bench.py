@@ -84,9 +84,10 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload):
+def ncu_traffic(workload, experts_per_ffn):
     """DRAM bytes per FFN launch from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
+    on the current kernel source (else None).  An entry captured on another
+    workload of the same expert shape is scaled by the experts per launch."""
     p = os.path.join(ROOT, "profiles", "ffn_decode_traffic.json")
     if not os.path.exists(p):
         return None
@@ -94,6 +95,8 @@ def ncu_traffic(workload):
     e = d.get(workload)
     if not e or e.get("source_hash") != kernel_source_hash():
         return None
+    if e.get("scaled"):
+        return float(e["bytes_per_expert"]) * experts_per_ffn
     return float(e["dram_bytes_per_ffn"])
 
 
@@ -478,7 +481,8 @@ def run_gpu(args, w, rank, world, local_rank):
     tokens = args.steps * T * world
     value = tokens / (ms * 1e-3)
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-            "frac": achieved / hbm, "traffic": ncu_traffic(args.workload),
+            "frac": achieved / hbm,
+            "traffic": ncu_traffic(args.workload, n_uniq / layer_steps + (1 if w["shared"] else 0)),
             "kernel": "decode expert FFN (gate/up + down launches of moe_expert_ffn)",
             "algorithmic_bytes_per_launch": ffn_bytes, "avg_launch_us": ffn_avg_s * 1e6,
             "peak_kind": peak_kind, "timing": ffn_timing}
