@@ -458,12 +458,25 @@ __device__ void arrive_tile(const FfnArgs& a, int tile, int n_exec, int nslot) {
   for (int it = lane; it < 16 * a.T; it += 32) {
     const int t = it >> 4, o = tile * 16 + (it & 15);
     float yv = 0.0f;
-    for (int j = 0; j < nslot; ++j) {
-      if (j < a.k) {
-        const int32_t e = a.ids[t * a.k + j];
-        if (e < 0 || e >= a.E) continue;  // skipped by the control step as well
+    // eight slots at a time: every load is issued before the first add, the adds
+    // stay in j order; an invalid routed id (skipped by the control step as
+    // well) contributes nothing
+    for (int j0 = 0; j0 < nslot; j0 += 8) {
+      float p[8];
+      bool v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int j = j0 + q;
+        v[q] = j < nslot;
+        if (v[q] && j < a.k) {
+          const int32_t e = a.ids[t * a.k + j];
+          v[q] = e >= 0 && e < a.E;
+        }
+        p[q] = v[q] ? __ldcg(a.partial + ((int64_t)t * nslot + j) * a.H + o) : 0.0f;
       }
-      yv += __ldcg(a.partial + ((int64_t)t * nslot + j) * a.H + o);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (v[q]) yv += p[q];
     }
     a.y[(int64_t)t * a.H + o] = yv;
   }
@@ -576,9 +589,6 @@ __global__ void __launch_bounds__(kSThreads, 1)
   }
 
   // ---------------------------------------------------------- consumers
-  // h is written by the gate/up kernel: wait for it to complete
-  griddep_wait();
-  griddep_launch();  // the next kernel may be scheduled (it waits for this one)
   const int w = wid, gid = lane >> 2, t4 = lane & 3;
   const int ctid = tid;  // 0 .. kCW * 32 - 1
   float2* sbt = reinterpret_cast<float2*>(smem + geo.o_sbt) + (size_t)w * 16 * (ngi + 1);
@@ -586,59 +596,77 @@ __global__ void __launch_bounds__(kSThreads, 1)
   float* hsum = reinterpret_cast<float*>(smem + geo.o_hsum);
   const uint16_t* raw = reinterpret_cast<const uint16_t*>(sraw);
   const int nslot = a.k + a.has_shared, hrow = geo.hrow;
+  // warp 0: the tokens routed to entry r and their routing slots and weights
+  auto lists = [&](int r) {
+    if (w == 0) {
+      // distinct tokens routed to entry r, ascending
+      int cnt;
+      if (r < n_uniq) {
+        const int32_t id = a.uniq[r];
+        const int base = a.layer * a.E, n = a.T * a.k;
+        cnt = 0;
+        for (int n0 = 0; n0 < n; n0 += 32) {
+          const int ii = n0 + lane;
+          bool mt = ii < n && base + a.ids[ii] == id;
+          for (int jj = mt ? ii - ii % a.k : ii; jj < ii; ++jj)
+            if (base + a.ids[jj] == id) mt = false;
+          const unsigned b = __ballot_sync(0xffffffffu, mt);
+          const int pos = cnt + __popc(b & ((1u << lane) - 1u));
+          if (mt && pos < kTokS) utok[pos] = ii / a.k;
+          cnt += __popc(b);
+        }
+      } else {
+        if (lane < a.T && lane < kTokS) utok[lane] = lane;
+        cnt = a.T;
+      }
+      const int nt = cnt < geo.tr ? cnt : geo.tr;
+      if (lane == 0) s_ntok = nt;
+      __syncwarp();
+      if (lane < nt) {
+        const int t = utok[lane];
+        int c = 0;
+        if (r < n_uniq) {
+          const int32_t id = a.uniq[r];
+          for (int jj = 0; jj < a.k; ++jj)
+            if (a.layer * a.E + a.ids[t * a.k + jj] == id) {
+              if (c < kMaxMatch) {
+                mj[lane][c] = jj;
+                mw[lane][c] = a.weights[t * a.k + jj];
+              }
+              ++c;
+            }
+        } else {
+          mj[lane][0] = a.k;
+          mw[lane][0] = 1.0f;
+          c = 1;
+        }
+        mcnt[lane] = c;
+      }
+    }
+  };
+  // the first entry's lists need only the routing plan: built before the wait
+  int listed = -1;
+  if (u_lo < u_hi) {
+    listed = u_lo / upe;
+    lists(listed);
+  }
+  // h is written by the gate/up kernel: wait for it to complete
+  griddep_wait();
+  griddep_launch();  // the next kernel may be scheduled (it waits for this one)
   int prev_r = -1, ntok = 0, s = 0, rnd = 0, pend = -1;
   bool ok = true;  // after a failed wait the warp keeps walking the loop (no waits,
                    // no math) so that every consumer warp meets the same barriers
   for (int u = u_lo; u < u_hi; ++u) {
     const int i = u - u_lo, r = u / upe, o0 = (u % upe) * kRowsB;
     if (r != prev_r) {
-      consumers_sync();  // every warp is done with the previous entry's h
-      if (w == 0) {
-        // distinct tokens routed to entry r, ascending
-        int cnt;
-        if (r < n_uniq) {
-          const int32_t id = a.uniq[r];
-          const int base = a.layer * a.E, n = a.T * a.k;
-          cnt = 0;
-          for (int n0 = 0; n0 < n; n0 += 32) {
-            const int ii = n0 + lane;
-            bool mt = ii < n && base + a.ids[ii] == id;
-            for (int jj = mt ? ii - ii % a.k : ii; jj < ii; ++jj)
-              if (base + a.ids[jj] == id) mt = false;
-            const unsigned b = __ballot_sync(0xffffffffu, mt);
-            const int pos = cnt + __popc(b & ((1u << lane) - 1u));
-            if (mt && pos < kTokS) utok[pos] = ii / a.k;
-            cnt += __popc(b);
-          }
-        } else {
-          if (lane < a.T && lane < kTokS) utok[lane] = lane;
-          cnt = a.T;
-        }
-        const int nt = cnt < geo.tr ? cnt : geo.tr;
-        if (lane == 0) s_ntok = nt;
-        __syncwarp();
-        if (lane < nt) {
-          const int t = utok[lane];
-          int c = 0;
-          if (r < n_uniq) {
-            const int32_t id = a.uniq[r];
-            for (int jj = 0; jj < a.k; ++jj)
-              if (a.layer * a.E + a.ids[t * a.k + jj] == id) {
-                if (c < kMaxMatch) {
-                  mj[lane][c] = jj;
-                  mw[lane][c] = a.weights[t * a.k + jj];
-                }
-                ++c;
-              }
-          } else {
-            mj[lane][0] = a.k;
-            mw[lane][0] = 1.0f;
-            c = 1;
-          }
-          mcnt[lane] = c;
-        }
-      }
+      // every warp is done with the previous entry's h and lists (and sees the
+      // first entry's lists, built before the wait)
       consumers_sync();
+      if (r != listed) {
+        lists(r);
+        listed = r;
+        consumers_sync();
+      }
       ntok = s_ntok;
       // h of those tokens as hi / lo bf16 column pairs in fragment order
       const int n_items = ntok * ngi * 4;

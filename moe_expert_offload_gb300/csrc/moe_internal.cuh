@@ -117,13 +117,20 @@ struct FfnArgs {
 // before this step (H), else in place from the bank (C, and F: an expert being
 // filled in this step is read from the bank, byte-identical to its new slot,
 // so the FFN need not wait for the fill copy).  Returns the slot or -1.
+// The slot, the fill count and the first fill ids are loaded together (no load
+// waits for another's result) since this sits on the FFN's start-up path.
 __device__ __forceinline__ int32_t ffn_slot(const FfnArgs& a, int32_t id) {
   const int32_t slot = a.slot_of_id[id];
-  if (slot < 0) return -1;
   const int nf = a.counts[4];
-  for (int i = 0; i < nf; ++i)
-    if (a.fill_ids[i] == id) return -1;
-  return slot;
+  bool filled = false;
+  for (int i0 = 0; i0 < nf; i0 += 8) {
+    int32_t f[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) f[q] = i0 + q < nf ? a.fill_ids[i0 + q] : -1;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) filled |= f[q] == id;
+  }
+  return (slot < 0 || filled) ? -1 : slot;
 }
 
 size_t ffn_workspace_bytes(int H, int I, int k, int T, int has_shared);
