@@ -2,9 +2,11 @@
 """Benchmark of the per-layer MoE expert step on one GB300 (or N replicas).
 
 A step is one decode token through every MoE layer of the workload: per
-layer the router (moe_route), the control step with its fill copies
-(moe_cache_step) and the expert FFN + combine (moe_expert_ffn), all through
-the C ABI on inputs already resident in HBM.  `e2e` repeats the measurement
+layer moe_layer_forward (router, control step, fill copies beside the expert
+FFN + combine), through the C ABI on inputs already resident in HBM.  The
+FFN's own duration (roofline) is taken from a separate replay of the same
+steps as moe_route / moe_cache_step / moe_expert_ffn calls with CUDA events
+around each moe_expert_ffn.  `e2e` repeats the measurement
 through moe_layer_forward with the step's hidden states copied in from pinned
 host memory and the layer outputs copied back every step.
 
@@ -357,10 +359,19 @@ def run_gpu(args, w, rank, world, local_rank):
         if ev is not None:
             ev[1].record(torch.cuda.current_stream())
 
+    lws = m.moe_layer_workspace_bytes(spec, T)
+
     def step(s, ev=None):
+        # the timed step: one moe_layer_forward per layer (route, control, fill
+        # beside the FFN, FFN); with events, the same work as separate calls so
+        # that the FFN launches can be bracketed
         sh = torch.cuda.current_stream().cuda_stream
         for l in range(L):
-            layer(xs[s, l], l, sh, None if ev is None else ev[l])
+            if ev is None:
+                m.moe_layer_forward(spec, cache.c, l, xs[s, l], T, wr[l], bias_l(l), shared,
+                                    plan.c, ids, wts, ws, lws, y[l], sh)
+            else:
+                layer(xs[s, l], l, sh, ev[l])
 
     def barrier():
         if world > 1:
@@ -434,7 +445,6 @@ def run_gpu(args, w, rank, world, local_rank):
     # end to end through the public API: pinned host hidden states -> device,
     # the 40 moe_layer_forward calls (one captured graph), layer outputs ->
     # pinned host, every step, no host sync inside the timed region.
-    lws = m.moe_layer_workspace_bytes(spec, T)
     x_host = torch.from_numpy(xs_h[args.warmup + args.steps:].view(np.int16).copy()).pin_memory()
     y_host = torch.empty((args.steps, L, T, H), dtype=torch.float32).pin_memory()
     x_dev = torch.empty((L, T, H), dtype=torch.int16, device=dev)

@@ -20,13 +20,16 @@
 //                 in registers); cp.async.mbarrier.arrive marks a stage full.
 //                 Rows past the group's count are zero-filled, and a tile of at
 //                 most 128 rows skips its second half entirely.
-//       warps 5-12 one B row per thread: int4 codes and the group scale / bias
-//                 prefetched into registers five blocks ahead, dequantised (one
+//       warps 5-12 one B row per thread: the int4 codes arrive by TMA (each
+//                 warp a 3-deep ring of 32-row x 32-byte boxes), the group
+//                 scales / biases 8 groups per 16-byte load; dequantised (one
 //                 LOP3 per nibble pair gives (128+q) as bf16x2, then q = v - 128
 //                 and w = s*q + b by bf16x2 fma) into a 2-deep B ring.
 //       warp 4    one thread waits for both stages, issues the MMAs and frees
 //                 the stages with tcgen05.commit.
-//     Warps 5-12 then read the accumulators (tcgen05.ld) for the epilogue.
+//     Warps 5-12 then read the accumulators (tcgen05.ld) for the epilogue and
+//     stage the bf16 output in shared memory, so that global stores cover whole
+//     row segments.
 //   * Both operands are K-major bf16 in the 128-byte swizzled layout; one
 //     thread issues tcgen05.mma (M=128, N=256, K=16) into two TMEM
 //     accumulators (512 columns) and tcgen05.commit signals an mbarrier when
@@ -168,7 +171,11 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
-__device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
+// silu(g) = g / (1 + e^-g); the fast divide is far inside the bf16 rounding of h
+// (the exponent is clamped so that the divisor stays finite)
+__device__ __forceinline__ float silu(float g) {
+  return __fdividef(g, 1.0f + __expf(fminf(-g, 80.0f)));
+}
 
 __device__ __forceinline__ uint32_t bf2(float lo, float hi) {
   const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
@@ -439,32 +446,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (ok) {
       tc_fence_after();
-      const int q = wid & 3, ch = (wid - kDqWarp0) >> 2;
+      const int q = wid & 3, ch = (wid - kDqWarp0) >> 2;  // TMEM lane quarter, column half
+      // Each warp stages its 32 rows x kRowBytes of output (bf16) in the idle A
+      // ring, 16-byte chunks XOR-swizzled by the row within each 128-byte segment
+      // (conflict-free both ways), then writes whole row segments: a store
+      // instruction covers 4 (or 2) rows x 128 (or 256) contiguous bytes instead
+      // of 32 rows x 16 bytes.
+      constexpr int kRowBytes = MODE == 1 ? kBN / 2 : kBN;  // this warp's bytes of a row
+      constexpr int kLanesPerRow = kRowBytes / 16, kRowsPerStore = 32 / kLanesPerRow;
+      unsigned char* stg = gbase + (wid - kDqWarp0) * 32 * kRowBytes;
+      auto sidx = [](int rr, int c) {
+        return rr * kRowBytes + ((c & ~7) << 4) + (((c & 7) ^ (rr & 7)) << 4);
+      };
 #pragma unroll
       for (int hm = 0; hm < 2; ++hm) {
         if (hm == 1 && !two) break;
-        const int r = hm * 128 + 32 * q + lane;
+        const int r = hm * 128 + 32 * q + lane;  // this lane's accumulator row
         const uint32_t trow = tmem + hm * kBN + ((uint32_t)(32 * q) << 16);
+        int64_t dst_row = 0;
         if (MODE == 1) {
 #pragma unroll
           for (int c = 0; c < 64; c += 32) {
             float gv[32], uv[32];
             tmem_ld32(trow + 64 * ch + c, gv);
             tmem_ld32(trow + kBN / 2 + 64 * ch + c, uv);
-            if (r < rows) {
-              uint16_t* dst = g.h_out + (int64_t)(row0 + r) * I + nt * (kBN / 2) + 64 * ch + c;
 #pragma unroll
-              for (int e = 0; e < 32; e += 8) {
-                float h[8];
+            for (int e = 0; e < 32; e += 8) {
+              float h[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) h[i] = silu(gv[e + i]) * uv[e + i];
-                *reinterpret_cast<uint4*>(dst + e) = make_uint4(
-                    bf2(h[0], h[4]), bf2(h[1], h[5]), bf2(h[2], h[6]), bf2(h[3], h[7]));
-              }
+              for (int i = 0; i < 8; ++i) h[i] = silu(gv[e + i]) * uv[e + i];
+              *reinterpret_cast<uint4*>(stg + sidx(lane, (c + e) >> 3)) = make_uint4(
+                  bf2(h[0], h[4]), bf2(h[1], h[5]), bf2(h[2], h[6]), bf2(h[3], h[7]));
             }
           }
         } else {
-          int64_t dst_row = 0;
           float wgt = 0.0f;
           if (r < rows) {
             const int a = g.perm[row0 + r];
@@ -481,16 +496,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < kBN / 2; c += 32) {
             float v[32];
             tmem_ld32(trow + (kBN / 2) * ch + c, v);
-            if (r < rows) {
-              uint16_t* dst = g.y_out + dst_row * H + nt * kBN + (kBN / 2) * ch + c;
 #pragma unroll
-              for (int e = 0; e < 32; e += 8)
-                *reinterpret_cast<uint4*>(dst + e) = make_uint4(
-                    bf2(wgt * v[e], wgt * v[e + 1]), bf2(wgt * v[e + 2], wgt * v[e + 3]),
-                    bf2(wgt * v[e + 4], wgt * v[e + 5]), bf2(wgt * v[e + 6], wgt * v[e + 7]));
-            }
+            for (int e = 0; e < 32; e += 8)
+              *reinterpret_cast<uint4*>(stg + sidx(lane, (c + e) >> 3)) = make_uint4(
+                  bf2(wgt * v[e], wgt * v[e + 1]), bf2(wgt * v[e + 2], wgt * v[e + 3]),
+                  bf2(wgt * v[e + 4], wgt * v[e + 5]), bf2(wgt * v[e + 6], wgt * v[e + 7]));
           }
         }
+        __syncwarp();
+#pragma unroll 4
+        for (int i = 0; i < 32; i += kRowsPerStore) {
+          const int rr = i + lane / kLanesPerRow, c = lane % kLanesPerRow;
+          const int rt = hm * 128 + 32 * q + rr;  // tile row
+          const int64_t drow = __shfl_sync(0xffffffffu, dst_row, rr);
+          const uint4 v = *reinterpret_cast<const uint4*>(stg + sidx(rr, c));
+          if (rt < rows) {
+            uint16_t* dst = MODE == 1
+                ? g.h_out + (int64_t)(row0 + rt) * I + nt * (kBN / 2) + 64 * ch + 8 * c
+                : g.y_out + drow * H + nt * kBN + (kBN / 2) * ch + 8 * c;
+            *reinterpret_cast<uint4*>(dst) = v;
+          }
+        }
+        __syncwarp();  // the staging tile is refilled for the second half
       }
     }
   }
