@@ -43,6 +43,8 @@
 // frees its TMEM and returns.
 #include <cuda_bf16.h>
 
+#include <cstring>
+
 #include "moe_internal.cuh"
 #include "stream_common.cuh"
 
@@ -50,17 +52,16 @@ namespace moe {
 namespace {
 
 constexpr int kBM = kPrefillTileRows;            // 256 rows: two M=128 accumulators
-constexpr int kBN = 256, kBK = 64;
+constexpr int kBK = 64;
+// output columns of a tile (the N of each MMA): 256 (one CTA per SM) or 128
+// (two co-resident CTAs per SM, so that one's fill and epilogue overlap the
+// other's MMAs)
+constexpr int kTileN = 256;
 // warp roles: 0-3 gather A, 4 issues MMAs (one thread), 5-12 dequantise B and
 // then drain the accumulators
-constexpr int kLoadWarps = 4, kMmaWarp = 4, kDqWarp0 = 5, kDqWarps = 8;
-constexpr int kThreads = (kDqWarp0 + kDqWarps) * 32;
-constexpr int kStagesA = 4;                      // A ring depth
-constexpr int kStagesB = 2;                      // B operand ring depth
+constexpr int kLoadWarps = 4, kMmaWarp = 4, kDqWarp0 = 5;
 constexpr int kHalfBytes = 128 * kBK * 2;        // 16 KB: one 128-row half of A
 constexpr int kABytes = kBM * kBK * 2;           // 32 KB
-constexpr int kBBytes = kBN * kBK * 2;           // 32 KB
-constexpr int kTmemCols = 512;
 // int4 codes reach shared memory by TMA: each dequant warp owns a ring of
 // kCodeStages boxes of its 32 B rows x 32 bytes (one k-block), so the code
 // loads leave the load/store pipe to the A gather and the bf16 stores
@@ -131,15 +132,31 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
 // M = 128 is the largest shape a single CTA may issue).
 constexpr int kMmaM = 128;
 static_assert(kBM == 2 * kMmaM, "the tile is two M=128 halves");
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
-                            ((uint32_t)(kMmaM >> 4) << 24);
+
+// Per tile width BN: dequant warps (one B row per thread), threads, CTAs per
+// SM, ring depths, TMEM columns (two M=128 accumulators of BN columns), the
+// instruction descriptor and the dynamic shared memory.
+template <int BN>
+struct TileCfg {
+  static constexpr int kDqWarps = BN / 32;
+  static constexpr int kThreads = (kDqWarp0 + kDqWarps) * 32;
+  static constexpr int kMinBlocks = BN == 256 ? 1 : 2;
+  static constexpr int kStagesA = BN == 256 ? 4 : 2;  // A ring depth
+  static constexpr int kStagesB = 2;                  // B operand ring depth
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                                     ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kMmaM >> 4) << 24);
+  static constexpr size_t kSmem = 1024 + (size_t)kStagesA * kABytes + (size_t)kStagesB * kBBytes +
+                                  (size_t)kDqWarps * kCodeStages * kCodeBox;
+};
 
 __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t accumulate) {
+                                         uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -192,15 +209,21 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t addr) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(addr) : "memory");
 }
 
-// Code maps of one GEMM: m[0] over the layer's E blobs, m[1] over the shared
-// expert's blob; u32 words [blob][B row][K / 8], boxes of 8 words x 32 rows.
+// Tensor maps of one GEMM: m[0] over the layer's E blobs, m[1] over the shared
+// expert's blob (int4 codes as u32 words [blob][B row][K / 8], boxes of 8 words
+// x 32 rows); mode 2 only, m[2] over h_perm (u32 words [row][I / 2], boxes of
+// 32 words x 256 rows, 128-byte swizzle: the A operand's layout).
 struct GemmMaps {
-  CUtensorMap m[2];
+  CUtensorMap m[3];
 };
 
-template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int MODE, int BN>
+__global__ void __launch_bounds__(TileCfg<BN>::kThreads, TileCfg<BN>::kMinBlocks)
     grouped_gemm_kernel(GemmArgs g, const __grid_constant__ GemmMaps maps) {
+  using C = TileCfg<BN>;
+  constexpr int kDqWarps = C::kDqWarps, kThreads = C::kThreads;
+  constexpr int kStagesA = C::kStagesA, kStagesB = C::kStagesB, kBBytes = C::kBBytes;
+  constexpr int kTmemCols = C::kTmemCols, kBN = BN;
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t full_a[kStagesA], empty_a[kStagesA];
   __shared__ __align__(8) uint64_t full_b[kStagesB], empty_b[kStagesB], acc_full;
@@ -252,7 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (tid == 0) {
     for (int i = 0; i < kStagesA; ++i) {
-      mbar_init(smem_u32(&full_a[i]), 32 * kLoadWarps);  // one cp.async arrive per loader lane
+      // mode 1: one cp.async arrive per loader lane; mode 2: the TMA issuer's expect_tx
+      mbar_init(smem_u32(&full_a[i]), MODE == 1 ? 32 * kLoadWarps : 1);
       mbar_init(smem_u32(&empty_a[i]), 1);  // tcgen05.commit
     }
     for (int i = 0; i < kStagesB; ++i) {
@@ -269,7 +293,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  if (wid < kLoadWarps) {
+  if (MODE == 2 && wid < kLoadWarps) {
+    // ----------------------------------------------- A loader, mode 2: TMA
+    // the tile's h rows are contiguous (row0 ...): one 256-row x 64-column box
+    // per block; rows past the group's count are computed and never stored
+    if (wid == 0 && lane == 0) {
+      const CUtensorMap* amap = &maps.m[2];
+      sc::tma_prefetch_map(amap);
+      int issued = 0;
+      for (int kb = 0; kb < nk; ++kb) {
+        const int st = kb % kStagesA, use = kb / kStagesA;
+        if (use > 0 && !mbar_wait(smem_u32(&empty_a[st]), (use - 1) & 1)) s_fail = 1;
+        if (s_fail) break;
+        sc::bar_expect(smem_u32(&full_a[st]), kABytes);
+        sc::tma_load_3d(a_addr + st * kABytes, amap, kb * (kBK / 2), row0, 0,
+                        smem_u32(&full_a[st]));
+        ++issued;
+      }
+      // after a failed wait: let the copies still in flight land (bounded)
+      if (issued < nk)
+        for (int j = issued > kStagesA ? issued - kStagesA : 0; j < issued; ++j)
+          mbar_wait(smem_u32(&full_a[j % kStagesA]), (j / kStagesA) & 1);
+    }
+  } else if (wid < kLoadWarps) {
     // ---------------------------------------------------------- A loader
     // lane: rows wid*64 + lane/8 + 4j (j < 16), 16-byte chunk lane % 8
     constexpr int kRowsPerLane = kBM / (kLoadWarps * 4);
@@ -318,9 +364,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {
           const uint64_t bd = smem_desc(bb + kk * 32);
-          mma_bf16(tmem, smem_desc(ab + kk * 32), bd, (kb | kk) != 0);
+          mma_bf16(tmem, smem_desc(ab + kk * 32), bd, C::kIdesc, (kb | kk) != 0);
           if (two)
-            mma_bf16(tmem + kBN, smem_desc(ab + kHalfBytes + kk * 32), bd, (kb | kk) != 0);
+            mma_bf16(tmem + kBN, smem_desc(ab + kHalfBytes + kk * 32), bd, C::kIdesc,
+                     (kb | kk) != 0);
         }
         mma_commit(smem_u32(&empty_a[sa]));
         mma_commit(smem_u32(&empty_b[sb]));
@@ -343,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       row = (int64_t)nt * (kBN / 2) + (up ? t - kBN / 2 : t);
       so = up ? off.us : off.gs;
       bo = up ? off.ub : off.gb;
-      my = (up ? I : 0) + nt * (kBN / 2) + 32 * (w & 3);  // up rows follow the gate rows
+      my = (up ? I : 0) + nt * (kBN / 2) + 32 * (w % (kDqWarps / 2));  // up rows follow the gate rows
     } else {
       row = (int64_t)nt * kBN + t;
       so = off.ds;
@@ -384,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     load_sb(0, cur);
     if (span < nk) load_sb(span, nxt);
     const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.0f, 128.0f);
-    int kb = 0;
+    int kb = 0, consumed = 0;
     bool failed = false;
     for (; kb < nk; ++kb) {
       const int sb = kb % kStagesB, use = kb / kStagesB, cs = kb % kCodeStages;
@@ -405,6 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every lane's reads of the slot come before its refill through the async proxy
       fence_async_smem();
       __syncwarp();
+      consumed = kb + 1;
       if (lane == 0 && issued < nk) issue(issued++);
       const int gi = kb % span;  // group within the fetched span
       const uint32_t sw = gi < 2 ? cur.s0 : gi < 4 ? cur.s1 : gi < 6 ? cur.s2 : cur.s3;
@@ -434,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // after a failed wait: let this warp's code copies still in flight land (bounded)
     if (failed && lane == 0)
-      for (int j = kb; j < issued; ++j)
+      for (int j = consumed; j < issued; ++j)
         mbar_wait(smem_u32(&code_full[w][j % kCodeStages]), (j / kCodeStages) & 1);
 
     // ---------------------------------------------------------- epilogue
@@ -452,7 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (conflict-free both ways), then writes whole row segments: a store
       // instruction covers 4 (or 2) rows x 128 (or 256) contiguous bytes instead
       // of 32 rows x 16 bytes.
-      constexpr int kRowBytes = MODE == 1 ? kBN / 2 : kBN;  // this warp's bytes of a row
+      constexpr int kColsW = MODE == 1 ? 64 : 128;  // this warp's output columns (of a row)
+      constexpr int kRowBytes = 2 * kColsW;
       constexpr int kLanesPerRow = kRowBytes / 16, kRowsPerStore = 32 / kLanesPerRow;
       unsigned char* stg = gbase + (wid - kDqWarp0) * 32 * kRowBytes;
       auto sidx = [](int rr, int c) {
@@ -493,9 +542,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
 #pragma unroll
-          for (int c = 0; c < kBN / 2; c += 32) {
+          for (int c = 0; c < kColsW; c += 32) {
             float v[32];
-            tmem_ld32(trow + (kBN / 2) * ch + c, v);
+            tmem_ld32(trow + kColsW * ch + c, v);
 #pragma unroll
             for (int e = 0; e < 32; e += 8)
               *reinterpret_cast<uint4*>(stg + sidx(lane, (c + e) >> 3)) = make_uint4(
@@ -513,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (rt < rows) {
             uint16_t* dst = MODE == 1
                 ? g.h_out + (int64_t)(row0 + rt) * I + nt * (kBN / 2) + 64 * ch + 8 * c
-                : g.y_out + drow * H + nt * kBN + (kBN / 2) * ch + 8 * c;
+                : g.y_out + drow * H + nt * kBN + kColsW * ch + 8 * c;
             *reinterpret_cast<uint4*>(dst) = v;
           }
         }
@@ -534,9 +583,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_grouped_gemm(int mode, const GemmArgs& a, int max_tiles, cudaStream_t st) {
+  using C = TileCfg<kTileN>;
   static bool attr_done[2][64] = {};
-  const size_t smem = 1024 + (size_t)kStagesA * kABytes + (size_t)kStagesB * kBBytes +
-                      (size_t)kDqWarps * kCodeStages * kCodeBox;
+  const size_t smem = C::kSmem;
   int d = 0;
   cudaError_t e = cudaGetDevice(&d);
   if (e != cudaSuccess) return e;
@@ -548,6 +597,15 @@ cudaError_t launch_grouped_gemm(int mode, const GemmArgs& a, int max_tiles, cuda
   const uint64_t rows = mode == 1 ? 2 * (uint64_t)a.I : (uint64_t)a.H;
   const int64_t q0 = mode == 1 ? off.gq : off.dq;
   GemmMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  if (mode == 2) {  // A = h_perm rows as u32 words, 128-byte swizzle
+    const uint64_t R = (uint64_t)a.T * a.k + a.T;
+    const uint64_t dims[3] = {(uint64_t)a.I / 2, R, 1};
+    const uint64_t strides[2] = {(uint64_t)a.I * 2, R * a.I * 2};
+    const uint32_t box[3] = {kBK / 2, kBM, 1};
+    if ((e = encode_tiled_u32(&maps.m[2], a.a_src, 3, dims, strides, box, true)) != cudaSuccess)
+      return e;
+  }
   const uint8_t* bases[2] = {a.experts, a.shared ? a.shared : a.experts};
   const uint64_t nblob[2] = {(uint64_t)a.E, 1};
   for (int i = 0; i < 2; ++i) {
@@ -560,22 +618,22 @@ cudaError_t launch_grouped_gemm(int mode, const GemmArgs& a, int max_tiles, cuda
   }
   if (mode == 1) {
     if (!attr_done[0][d]) {
-      e = cudaFuncSetAttribute(grouped_gemm_kernel<1>,
+      e = cudaFuncSetAttribute(grouped_gemm_kernel<1, kTileN>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
       attr_done[0][d] = true;
     }
-    const dim3 grid(a.I / (kBN / 2), max_tiles);
-    grouped_gemm_kernel<1><<<grid, kThreads, smem, st>>>(a, maps);
+    const dim3 grid(a.I / (kTileN / 2), max_tiles);
+    grouped_gemm_kernel<1, kTileN><<<grid, C::kThreads, smem, st>>>(a, maps);
   } else {
     if (!attr_done[1][d]) {
-      e = cudaFuncSetAttribute(grouped_gemm_kernel<2>,
+      e = cudaFuncSetAttribute(grouped_gemm_kernel<2, kTileN>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
       attr_done[1][d] = true;
     }
-    const dim3 grid(a.H / kBN, max_tiles);
-    grouped_gemm_kernel<2><<<grid, kThreads, smem, st>>>(a, maps);
+    const dim3 grid(a.H / kTileN, max_tiles);
+    grouped_gemm_kernel<2, kTileN><<<grid, C::kThreads, smem, st>>>(a, maps);
   }
   return cudaGetLastError();
 }
