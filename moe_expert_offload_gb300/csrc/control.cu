@@ -41,19 +41,27 @@ __device__ __forceinline__ void insert_key(unsigned long long (&best)[KMAX],
 }
 
 // K rounds of warp-wide minimum over the heads of the per-lane ascending
-// lists; round r's minimum is returned in out_r by every lane (keys unique).
-template <int KMAX>
+// lists; round r's minimum is written to out[r] (keys unique).  A round is two
+// warp reductions of 32-bit halves: the least recency stamp, then the least
+// slot among the lanes holding that stamp.  The winning lane scanned that slot
+// itself: if it is one of its NE early slots it also writes the slot's id from
+// early_id to out_id[r], else -2 (not known).
+template <int KMAX, int NE>
 __device__ __forceinline__ void warp_k_smallest(unsigned long long (&best)[KMAX], int K,
-                                                unsigned long long* out) {
+                                                unsigned long long* out, int32_t* out_id,
+                                                const int32_t (&early_id)[NE > 0 ? NE : 1]) {
   const int lane = threadIdx.x & 31;
   for (int r = 0; r < K; ++r) {
-    unsigned long long m = best[0];
-#pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) {
-      const unsigned long long o = __shfl_xor_sync(0xffffffffu, m, d);
-      m = o < m ? o : m;
-    }
+    const uint32_t hi = (uint32_t)(best[0] >> 32), lo = (uint32_t)best[0];
+    const uint32_t mhi = __reduce_min_sync(0xffffffffu, hi);
+    const uint32_t mlo = __reduce_min_sync(0xffffffffu, hi == mhi ? lo : 0xffffffffu);
+    const unsigned long long m = ((unsigned long long)mhi << 32) | mlo;
     if (m != kNoKey && best[0] == m) {
+      int32_t id = -2;
+#pragma unroll
+      for (int j = 0; j < NE; ++j)
+        if ((int)mlo == (int)threadIdx.x + j * kCtlThreads) id = early_id[j];
+      out_id[r] = id;
 #pragma unroll
       for (int j = 0; j < KMAX - 1; ++j) best[j] = best[j + 1];
       best[KMAX - 1] = kNoKey;
@@ -70,8 +78,10 @@ __global__ void __launch_bounds__(kCtlThreads) cache_step_kernel(CacheArgs a) {
   __shared__ uint8_t sfirst[kMaxRouted];
   __shared__ int swh[kCtlWarps], swm[kCtlWarps];
   __shared__ unsigned long long scand[kCtlWarps * KMAX];
+  __shared__ int32_t scand_id[kCtlWarps * KMAX];
   __shared__ unsigned long long svict[KMAX];
-  __shared__ int s_nu, s_bad;
+  __shared__ int32_t sold[KMAX];
+  __shared__ int s_nu, s_nh, s_nm, s_bad;
   __shared__ uint32_t s_now;
   __shared__ uint32_t shit[kEarlySlots / 32];  // slots hit this step (those < kEarlySlots)
   griddep_launch();
@@ -86,11 +96,16 @@ __global__ void __launch_bounds__(kCtlThreads) cache_step_kernel(CacheArgs a) {
   // become `now`, which the scan excludes).
   constexpr int NE = KMAX <= 16 ? kEarlyTs : 0;  // (the K <= 32 list needs the registers)
   uint32_t early[NE > 0 ? NE : 1];
+  int32_t early_id[NE > 0 ? NE : 1];  // the same slots' ids: a victim's is read from here
 #pragma unroll
   for (int j = 0; j < NE; ++j) {
     const int v = tid + j * kCtlThreads;
     early[j] = v < a.S ? a.ts[v] : 0u;
+    early_id[j] = v < a.S ? a.id_of_slot[v] : -1;
   }
+  // (small steps) the routed ids, also independent of everything above
+  int32_t e_early = 0;
+  if (n <= 32 && wid == 0 && lane < n) e_early = a.ids[lane];
   for (int i = tid; i < kEarlySlots / 32; i += kCtlThreads) shit[i] = 0u;
   if (tid == 0) {
     s_now = a.clock[0] + 1u;
@@ -101,74 +116,126 @@ __global__ void __launch_bounds__(kCtlThreads) cache_step_kernel(CacheArgs a) {
   __syncthreads();
   const uint32_t now = s_now;
 
-  // routed ids -> bank ids l*E + e (INT_MAX marks an id outside [0, E))
-  for (int i = tid; i < n; i += kCtlThreads) {
-    const int32_t e = a.ids[i];
-    if (e < 0 || e >= E) {
-      su[i] = INT_MAX;
-      s_bad = 1;
-    } else {
-      su[i] = a.layer * E + e;
-    }
-  }
-  __syncthreads();
-
-  // dedup: keep first occurrences; an entry's rank among the unique ids is
-  // the number of smaller unique ids.
-  for (int i = tid; i < n; i += kCtlThreads) {
-    const int32_t v = su[i];
-    uint8_t first = v != INT_MAX;
-    for (int j = 0; j < i && first; ++j) first = su[j] != v;
-    sfirst[i] = first;
-  }
-  __syncthreads();
-  for (int i = tid; i < n; i += kCtlThreads) {
-    if (!sfirst[i]) continue;
-    const int32_t v = su[i];
-    int r = 0;
-    for (int j = 0; j < n; ++j) r += (sfirst[j] && su[j] < v);
-    suniq[r] = v;
-    atomicAdd(&s_nu, 1);
-  }
-  __syncthreads();
-  const int n_uniq = s_nu;
-
-  // hit / miss, order-preserving compaction in rounds of kCtlThreads
-  int base_h = 0, base_m = 0;
-  for (int base = 0; base < n_uniq; base += kCtlThreads) {
-    const int r = base + tid;
-    const bool valid = r < n_uniq;
-    const int32_t u = valid ? suniq[r] : 0;
-    const int32_t slot = valid ? a.slot_of_id[u] : -1;
-    const bool hit = valid && slot >= 0, miss = valid && slot < 0;
-    const unsigned hb = __ballot_sync(0xffffffffu, hit), mb = __ballot_sync(0xffffffffu, miss);
-    if (lane == 0) {
-      swh[wid] = __popc(hb);
-      swm[wid] = __popc(mb);
-    }
-    __syncthreads();
-    int oh = base_h, om = base_m, th = 0, tm = 0;
-    for (int w = 0; w < kCtlWarps; ++w) {
-      if (w < wid) {
-        oh += swh[w];
-        om += swm[w];
+  int n_uniq, n_hit, m;
+  if (n <= 32) {
+    // up to 32 routed ids: one warp deduplicates, ranks and classifies them in
+    // registers (one block barrier instead of five)
+    if (wid == 0) {
+      int32_t v = INT_MAX;  // bank id l*E + e; INT_MAX marks an id outside [0, E)
+      if (lane < n) {
+        const int32_t e = e_early;
+        if (e < 0 || e >= E)
+          s_bad = 1;
+        else
+          v = a.layer * E + e;
       }
-      th += swh[w];
-      tm += swm[w];
+      // first occurrences; a unique id's rank is the number of smaller unique ids
+      const unsigned peers = __match_any_sync(0xffffffffu, v);
+      const bool first = v != INT_MAX && (peers & lanemask_lt()) == 0;
+      int rank = 0;
+      for (int jj = 0; jj < n; ++jj) {
+        const int32_t vj = __shfl_sync(0xffffffffu, v, jj);
+        const int fj = __shfl_sync(0xffffffffu, (int)first, jj);
+        rank += (fj && vj < v);
+      }
+      const int nu = __popc(__ballot_sync(0xffffffffu, first));
+      if (first) suniq[rank] = v;
+      __syncwarp();
+      // hit / miss in rank order, order-preserving compaction
+      const bool valid = lane < nu;
+      const int32_t u = valid ? suniq[lane] : 0;
+      const int32_t slot = valid ? a.slot_of_id[u] : -1;
+      const bool hit = valid && slot >= 0, miss = valid && slot < 0;
+      const unsigned hb = __ballot_sync(0xffffffffu, hit), mb = __ballot_sync(0xffffffffu, miss);
+      if (hit) {
+        const int p = __popc(hb & lanemask_lt());
+        a.plan.hit_ids[p] = u;
+        a.plan.hit_slots[p] = slot;
+        a.ts[slot] = now;  // recency moves only when the router selects the expert
+        if (slot < kEarlySlots) atomicOr(&shit[slot >> 5], 1u << (slot & 31));
+      }
+      if (miss) smiss[__popc(mb & lanemask_lt())] = u;
+      if (lane == 0) {
+        s_nu = nu;
+        s_nh = __popc(hb);
+        s_nm = __popc(mb);
+      }
     }
-    if (hit) {
-      const int p = oh + __popc(hb & lanemask_lt());
-      a.plan.hit_ids[p] = u;
-      a.plan.hit_slots[p] = slot;
-      a.ts[slot] = now;  // recency moves only when the router selects the expert
-      if (slot < kEarlySlots) atomicOr(&shit[slot >> 5], 1u << (slot & 31));
-    }
-    if (miss) smiss[om + __popc(mb & lanemask_lt())] = u;
-    base_h += th;
-    base_m += tm;
     __syncthreads();
+    n_uniq = s_nu;
+    n_hit = s_nh;
+    m = s_nm;
+  } else {
+    // routed ids -> bank ids l*E + e (INT_MAX marks an id outside [0, E))
+    for (int i = tid; i < n; i += kCtlThreads) {
+      const int32_t e = a.ids[i];
+      if (e < 0 || e >= E) {
+        su[i] = INT_MAX;
+        s_bad = 1;
+      } else {
+        su[i] = a.layer * E + e;
+      }
+    }
+    __syncthreads();
+
+    // dedup: keep first occurrences; an entry's rank among the unique ids is
+    // the number of smaller unique ids.
+    for (int i = tid; i < n; i += kCtlThreads) {
+      const int32_t v = su[i];
+      uint8_t first = v != INT_MAX;
+      for (int j = 0; j < i && first; ++j) first = su[j] != v;
+      sfirst[i] = first;
+    }
+    __syncthreads();
+    for (int i = tid; i < n; i += kCtlThreads) {
+      if (!sfirst[i]) continue;
+      const int32_t v = su[i];
+      int r = 0;
+      for (int j = 0; j < n; ++j) r += (sfirst[j] && su[j] < v);
+      suniq[r] = v;
+      atomicAdd(&s_nu, 1);
+    }
+    __syncthreads();
+    n_uniq = s_nu;
+
+    // hit / miss, order-preserving compaction in rounds of kCtlThreads
+    int base_h = 0, base_m = 0;
+    for (int base = 0; base < n_uniq; base += kCtlThreads) {
+      const int r = base + tid;
+      const bool valid = r < n_uniq;
+      const int32_t u = valid ? suniq[r] : 0;
+      const int32_t slot = valid ? a.slot_of_id[u] : -1;
+      const bool hit = valid && slot >= 0, miss = valid && slot < 0;
+      const unsigned hb = __ballot_sync(0xffffffffu, hit), mb = __ballot_sync(0xffffffffu, miss);
+      if (lane == 0) {
+        swh[wid] = __popc(hb);
+        swm[wid] = __popc(mb);
+      }
+      __syncthreads();
+      int oh = base_h, om = base_m, th = 0, tm = 0;
+      for (int w = 0; w < kCtlWarps; ++w) {
+        if (w < wid) {
+          oh += swh[w];
+          om += swm[w];
+        }
+        th += swh[w];
+        tm += swm[w];
+      }
+      if (hit) {
+        const int p = oh + __popc(hb & lanemask_lt());
+        a.plan.hit_ids[p] = u;
+        a.plan.hit_slots[p] = slot;
+        a.ts[slot] = now;  // recency moves only when the router selects the expert
+        if (slot < kEarlySlots) atomicOr(&shit[slot >> 5], 1u << (slot & 31));
+      }
+      if (miss) smiss[om + __popc(mb & lanemask_lt())] = u;
+      base_h += th;
+      base_m += tm;
+      __syncthreads();
+    }
+    n_hit = base_h;
+    m = base_m;
   }
-  const int n_hit = base_h, m = base_m;
 
   // q = round half up of m * B_P / B_H; pure fill when B_H <= B_P
   int q;
@@ -196,16 +263,25 @@ __global__ void __launch_bounds__(kCtlThreads) cache_step_kernel(CacheArgs a) {
     const uint32_t t = a.ts[v];
     if (t != now) insert_key<KMAX>(best, ((unsigned long long)t << 32) | (uint32_t)v);
   }
-  warp_k_smallest<KMAX>(best, K, &scand[wid * KMAX]);
+  warp_k_smallest<KMAX, NE>(best, K, &scand[wid * KMAX], &scand_id[wid * KMAX], early_id);
   __syncthreads();
   if (wid == 0) {
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) best[j] = kNoKey;
-    for (int c = lane; c < kCtlWarps * KMAX; c += 32) {
-      const int w = c / KMAX, r = c % KMAX;
-      if (r < K) insert_key<KMAX>(best, scand[w * KMAX + r]);
+    // merge the warps' ascending lists: lane w < kCtlWarps holds the head of
+    // warp w's list; each round takes the least head (keys unique)
+    int pos = 0;
+    for (int r = 0; r < K; ++r) {
+      const unsigned long long h =
+          (lane < kCtlWarps && pos < K) ? scand[lane * KMAX + pos] : kNoKey;
+      const uint32_t hi = (uint32_t)(h >> 32), lo = (uint32_t)h;
+      const uint32_t mhi = __reduce_min_sync(0xffffffffu, hi);
+      const uint32_t mlo = __reduce_min_sync(0xffffffffu, hi == mhi ? lo : 0xffffffffu);
+      const unsigned long long mk = ((unsigned long long)mhi << 32) | mlo;
+      if (mk != kNoKey && h == mk) {
+        sold[r] = scand_id[lane * KMAX + pos];
+        ++pos;
+      }
+      if (lane == 0) svict[r] = mk;
     }
-    warp_k_smallest<KMAX>(best, K, svict);
   }
   __syncthreads();
 
@@ -218,7 +294,8 @@ __global__ void __launch_bounds__(kCtlThreads) cache_step_kernel(CacheArgs a) {
   if (tid < n_fill) {
     const int32_t v = (int32_t)(svict[tid] & 0xffffffffu);
     const int32_t f = smiss[tid];
-    const int32_t old = a.id_of_slot[v];
+    const int32_t known = sold[tid];  // -2: the slot's id was not prefetched
+    const int32_t old = known != -2 ? known : a.id_of_slot[v];
     if (old >= 0) a.slot_of_id[old] = -1;  // an evicted id is never one of F
     a.id_of_slot[v] = f;
     a.slot_of_id[f] = v;
