@@ -102,6 +102,25 @@ int do_route(const moe_spec* spec, const void* x, int32_t T, const void* w_route
   return MOE_OK;
 }
 
+moe::CacheArgs cache_args(const moe_spec* spec, moe_cache* c, int32_t layer, const int32_t* ids,
+                          int32_t T, moe_plan* plan) {
+  moe::CacheArgs a;
+  a.E = spec->num_experts;
+  a.layer = layer;
+  a.n_ids = T * spec->top_k;
+  a.S = c->num_slots;
+  a.K = c->k_victims;
+  a.bp = c->bp_mbps;
+  a.bh = c->bh_mbps;
+  a.ids = ids;
+  a.slot_of_id = c->slot_of_id;
+  a.id_of_slot = c->id_of_slot;
+  a.ts = c->ts;
+  a.clock = c->clock;
+  a.plan = *plan;
+  return a;
+}
+
 int do_cache_step(const moe_spec* spec, moe_cache* c, int32_t layer, const int32_t* ids,
                   int32_t T, moe_plan* plan, int32_t do_fill, cudaStream_t st) {
   moe::CacheArgs a;
@@ -319,11 +338,42 @@ int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, con
   cudaStream_t st = (cudaStream_t)stream;
   float* logits = static_cast<float*>(workspace);
   const size_t lbytes = align256((size_t)T * spec->num_experts * 4);
-  rc = do_route(spec, x, T, w_router, bias, logits, ids, weights, st);
-  if (rc) return rc;
   SideStream* ss = side_stream(st);
-  rc = do_cache_step(spec, cache, layer, ids, T, plan, ss ? 0 : 1, st);
-  if (rc) return rc;
+  if (T <= moe::kSelFusedMaxT && spec->num_experts <= moe::kSelFusedMaxE) {
+    // logits kernel, then the selection inside the control step's CTA
+    if (!x || !w_router || !ids || !weights) return fail(MOE_EINVAL, "moe_layer_forward: NULL argument");
+    if (!aligned(x, 16) || !aligned(w_router, 16))
+      return fail(MOE_EINVAL, "moe_layer_forward: x and w_router must be 16-byte aligned");
+    cudaError_t e = moe::launch_router_logits(static_cast<const uint16_t*>(x),
+                                              static_cast<const uint16_t*>(w_router), T,
+                                              spec->num_experts, spec->hidden, logits, st);
+    if (e != cudaSuccess) return cuda_fail(e, "router logits launch");
+    const moe::CacheArgs a = cache_args(spec, cache, layer, ids, T, plan);
+    moe::SelArgs sa;
+    sa.logits = logits;
+    sa.bias = bias;
+    sa.T = T;
+    sa.k = spec->top_k;
+    sa.router = spec->router;
+    sa.n_groups = spec->n_groups;
+    sa.topk_groups = spec->topk_groups;
+    sa.scale = spec->routed_scale;
+    sa.ids = ids;
+    sa.wts = weights;
+    e = moe::launch_cache_step_sel(a, sa, st);
+    if (e != cudaSuccess) return cuda_fail(e, "control step launch");
+    if (!ss) {
+      const moe::BlobOffsets off = moe::blob_offsets(spec->hidden, spec->inter);
+      e = moe::launch_fill_copy(*plan, cache->k_victims, static_cast<const uint8_t*>(cache->bank),
+                                static_cast<uint8_t*>(cache->slot_pool), off.total, st);
+      if (e != cudaSuccess) return cuda_fail(e, "fill copy launch");
+    }
+  } else {
+    rc = do_route(spec, x, T, w_router, bias, logits, ids, weights, st);
+    if (rc) return rc;
+    rc = do_cache_step(spec, cache, layer, ids, T, plan, ss ? 0 : 1, st);
+    if (rc) return rc;
+  }
   if (ss) {  // fill copy beside the FFN
     cudaError_t e = cudaEventRecord(ss->fork, st);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->s, ss->fork, 0);

@@ -11,6 +11,7 @@
 #include <limits.h>
 
 #include "moe_internal.cuh"
+#include "route_select.cuh"
 
 namespace moe {
 namespace {
@@ -70,8 +71,8 @@ __device__ __forceinline__ void warp_k_smallest(unsigned long long (&best)[KMAX]
   }
 }
 
-template <int KMAX>
-__global__ void __launch_bounds__(kCtlThreads) cache_step_kernel(CacheArgs a) {
+template <int KMAX, bool SEL>
+__global__ void __launch_bounds__(kCtlThreads) cache_step_kernel(CacheArgs a, SelArgs sa) {
   __shared__ int32_t su[kMaxRouted];
   __shared__ int32_t suniq[kMaxRouted];
   __shared__ int32_t smiss[kMaxRouted];
@@ -102,6 +103,23 @@ __global__ void __launch_bounds__(kCtlThreads) cache_step_kernel(CacheArgs a) {
     const int v = tid + j * kCtlThreads;
     early[j] = v < a.S ? a.ts[v] : 0u;
     early_id[j] = v < a.S ? a.id_of_slot[v] : -1;
+  }
+  if constexpr (SEL) {
+    // the router's selection for the step's tokens, one warp per token; the
+    // ids are then read back below like those of a separate select kernel
+    __shared__ float sel_a[kCtlWarps][32 * 8];
+    __shared__ float sel_b[kCtlWarps][rsel::kMaxK], sel_c[kCtlWarps][rsel::kMaxK];
+    __shared__ float sel_sum[kCtlWarps];
+    if (wid < sa.T) {
+      if (sa.router == MOE_ROUTER_SOFTMAX_TOPK)
+        rsel::softmax_token<8>(sa.logits, wid, E, sa.k, sa.ids, sa.wts, sel_b[wid], sel_c[wid],
+                               &sel_sum[wid]);
+      else
+        rsel::sigmoid_group_token<8>(sa.logits, sa.bias, wid, E, sa.n_groups, sa.topk_groups,
+                                     sa.k, sa.scale, sa.ids, sa.wts, sel_a[wid], sel_b[wid],
+                                     &sel_sum[wid]);
+    }
+    __syncthreads();
   }
   // (small steps) the routed ids, also independent of everything above
   int32_t e_early = 0;
@@ -362,9 +380,23 @@ __global__ void cache_reset_kernel(int32_t* slot_of_id, int n_ids, int32_t* id_o
 }  // namespace
 
 cudaError_t launch_cache_step(const CacheArgs& a, cudaStream_t st) {
-  if (a.K <= 8) return launch_pdl(cache_step_kernel<8>, dim3(1), dim3(kCtlThreads), 0, st, a);
-  if (a.K <= 16) return launch_pdl(cache_step_kernel<16>, dim3(1), dim3(kCtlThreads), 0, st, a);
-  return launch_pdl(cache_step_kernel<32>, dim3(1), dim3(kCtlThreads), 0, st, a);
+  const SelArgs none{};
+  if (a.K <= 8)
+    return launch_pdl(cache_step_kernel<8, false>, dim3(1), dim3(kCtlThreads), 0, st, a, none);
+  if (a.K <= 16)
+    return launch_pdl(cache_step_kernel<16, false>, dim3(1), dim3(kCtlThreads), 0, st, a, none);
+  return launch_pdl(cache_step_kernel<32, false>, dim3(1), dim3(kCtlThreads), 0, st, a, none);
+}
+
+cudaError_t launch_cache_step_sel(const CacheArgs& a, const SelArgs& s, cudaStream_t st) {
+  if (s.T < 1 || s.T > kSelFusedMaxT || s.T > kCtlWarps || a.E > kSelFusedMaxE ||
+      s.k > rsel::kMaxK)
+    return cudaErrorInvalidValue;
+  if (a.K <= 8)
+    return launch_pdl(cache_step_kernel<8, true>, dim3(1), dim3(kCtlThreads), 0, st, a, s);
+  if (a.K <= 16)
+    return launch_pdl(cache_step_kernel<16, true>, dim3(1), dim3(kCtlThreads), 0, st, a, s);
+  return launch_pdl(cache_step_kernel<32, true>, dim3(1), dim3(kCtlThreads), 0, st, a, s);
 }
 
 cudaError_t launch_fill_copy(const moe_plan& plan, int K, const uint8_t* bank, uint8_t* pool,

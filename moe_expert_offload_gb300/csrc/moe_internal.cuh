@@ -86,6 +86,19 @@ struct CacheArgs {
   moe_plan plan;
 };
 cudaError_t launch_cache_step(const CacheArgs& a, cudaStream_t st);
+// Router selection done inside the control step's CTA (decode layer step with
+// T <= 16 tokens and E <= 256 experts): one warp per token reads its logits
+// and writes ids / weights before the control step reads them.
+struct SelArgs {
+  const float* logits;
+  const float* bias;
+  int T, k, router, n_groups, topk_groups;
+  float scale;
+  int32_t* ids;
+  float* wts;
+};
+constexpr int kSelFusedMaxT = 16, kSelFusedMaxE = 256;
+cudaError_t launch_cache_step_sel(const CacheArgs& a, const SelArgs& s, cudaStream_t st);
 cudaError_t launch_cache_reset(int32_t* slot_of_id, int n_ids, int32_t* id_of_slot, uint32_t* ts,
                                int S, uint32_t* clock, cudaStream_t st);
 cudaError_t launch_fill_copy(const moe_plan& plan, int K, const uint8_t* bank, uint8_t* pool,
