@@ -106,23 +106,24 @@ __global__ void __launch_bounds__(256) router_logits_tiled_kernel(const uint16_t
     }
     __syncthreads();
     if (s + 1 < ns) fetch(s + 1);
-    uint4 xv[4];
+    // widen once per slice (x) and once per expert row (W), not per product
+    float xf[4][8];
 #pragma unroll
-    for (int a = 0; a < 4; ++a) xv[a] = xs[tw + a][lane];
+    for (int a = 0; a < 4; ++a) {
+      const uint4 v = xs[tw + a][lane];
+      xf[a][0] = bf_lo(v.x); xf[a][1] = bf_hi(v.x); xf[a][2] = bf_lo(v.y); xf[a][3] = bf_hi(v.y);
+      xf[a][4] = bf_lo(v.z); xf[a][5] = bf_hi(v.z); xf[a][6] = bf_lo(v.w); xf[a][7] = bf_hi(v.w);
+    }
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
-      const uint4 wv = ws[ew + b][lane];
+      const uint4 v = ws[ew + b][lane];
+      const float wf[8] = {bf_lo(v.x), bf_hi(v.x), bf_lo(v.y), bf_hi(v.y),
+                           bf_lo(v.z), bf_hi(v.z), bf_lo(v.w), bf_hi(v.w)};
 #pragma unroll
       for (int a = 0; a < 4; ++a) {
         float& r = acc[a * 8 + b];
-        r = __fmaf_rn(bf_lo(xv[a].x), bf_lo(wv.x), r);
-        r = __fmaf_rn(bf_hi(xv[a].x), bf_hi(wv.x), r);
-        r = __fmaf_rn(bf_lo(xv[a].y), bf_lo(wv.y), r);
-        r = __fmaf_rn(bf_hi(xv[a].y), bf_hi(wv.y), r);
-        r = __fmaf_rn(bf_lo(xv[a].z), bf_lo(wv.z), r);
-        r = __fmaf_rn(bf_hi(xv[a].z), bf_hi(wv.z), r);
-        r = __fmaf_rn(bf_lo(xv[a].w), bf_lo(wv.w), r);
-        r = __fmaf_rn(bf_hi(xv[a].w), bf_hi(wv.w), r);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) r = __fmaf_rn(xf[a][e], wf[e], r);
       }
     }
   }
