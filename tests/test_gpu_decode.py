@@ -143,6 +143,7 @@ def _plans_equal(gp, op, K):
     (2, 32, 1, 1, 77300, 77300, 1, 4, 60),       # one slot, pure fill
     (2, 32, 40, 8, 60000, 50000, 8, 8, 80),      # B_H < B_P -> pure fill
     (4, 64, 7, 16, 1, 1000, 8, 8, 80),           # K > S, q mostly 0
+    (2, 64, 40, 20, 52700, 77300, 2, 8, 60),     # K > 16: the long victim lists
 ])
 def test_cache_step_matches_oracle_on_random_traces(oracle, L, E, S, K, bp, bh, T, k, steps):
     rng = np.random.default_rng(S * 31 + K)
@@ -264,6 +265,48 @@ def test_tiny_config_64_decode_steps(oracle):
         if eid >= 0:
             assert np.array_equal(pool[slot], bank_h[eid])
     assert fills > 0
+
+
+@pytest.mark.parametrize("router,T,E", [("softmax", 16, 64), ("softmax", 17, 64),
+                                          ("sigmoid_group", 16, 64), ("sigmoid_group", 17, 64),
+                                          ("softmax", 3, 257)])
+def test_layer_forward_selection_paths(oracle, router, T, E):
+    """moe_layer_forward runs the router selection inside the control step for T <= 16 and
+    E <= 256, with separate kernels otherwise: both give the oracle's ids, weights and plans."""
+    H, I, k, S, K, L = 256, 128, 4, 24, 6, 2
+    kw = dict(router="sigmoid_group", n_groups=8, topk_groups=3, routed_scale=2.5) \
+        if router == "sigmoid_group" else {}
+    spec = m.make_spec(L, H, I, E, k, **kw)
+    bank_h = synth.make_bank(L * E, H, I, 5)
+    bank = dev(bank_h, DEV)
+    cache = m.DeviceCache(spec, S, K, 52700, 77300, bank=bank, device=DEV)
+    plan = m.DevicePlan(T * k, K, device=DEV)
+    wsb = m.moe_layer_workspace_bytes(spec, T)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    wts = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    y = torch.empty((T, H), dtype=torch.float32, device=DEV)
+    ost = oracle.CacheState(L * E, S)
+    for step in range(3):
+        for layer in range(L):
+            rng = np.random.default_rng(1000 * step + layer)
+            xb = synth.bf16_bits(rng.normal(0, 1.5, (T, H)))
+            wb = synth.router_weights(70 + layer, E, H)
+            bias_h = synth.selection_bias(80 + layer, E) if router == "sigmoid_group" else None
+            m.moe_layer_forward(spec, cache.c, layer, dev_bits(xb, DEV), T, dev_bits(wb, DEV),
+                                None if bias_h is None else dev(bias_h, DEV), None, plan.c, ids,
+                                wts, ws, wsb, y)
+            torch.cuda.synchronize()
+            ol = oracle.router_logits(xb, wb)
+            if router == "sigmoid_group":
+                oid, ow = oracle.route_sigmoid_group(ol, bias_h, 8, 3, k, 2.5)
+            else:
+                oid, ow = oracle.route_softmax_topk(ol, k)
+            assert np.array_equal(ids.cpu().numpy(), oid)
+            assert np.array_equal(f32_bits(wts.cpu().numpy()), f32_bits(ow))
+            op = oracle.cache_step(ost, E, layer, oid, K, 52700, 77300)
+            _plans_equal(plan.read(K), op, K)
+    _tables_equal(cache, ost)
 
 
 @pytest.mark.parametrize("H,I,E,k,T,shared", [(2048, 512, 256, 8, 1, True),
