@@ -33,18 +33,29 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const uint16_t* __re
   const uint4* wr = reinterpret_cast<const uint4*>(w + (size_t)e * H);
   const int chunks = H >> 3;
   float acc = 0.0f;
-#pragma unroll 4
-  for (int c = lane; c < chunks; c += 32) {
-    const uint4 xv = __ldg(xr + c);
-    const uint4 wv = __ldg(wr + c);
-    acc = __fmaf_rn(bf_lo(xv.x), bf_lo(wv.x), acc);
-    acc = __fmaf_rn(bf_hi(xv.x), bf_hi(wv.x), acc);
-    acc = __fmaf_rn(bf_lo(xv.y), bf_lo(wv.y), acc);
-    acc = __fmaf_rn(bf_hi(xv.y), bf_hi(wv.y), acc);
-    acc = __fmaf_rn(bf_lo(xv.z), bf_lo(wv.z), acc);
-    acc = __fmaf_rn(bf_hi(xv.z), bf_hi(wv.z), acc);
-    acc = __fmaf_rn(bf_lo(xv.w), bf_lo(wv.w), acc);
-    acc = __fmaf_rn(bf_hi(xv.w), bf_hi(wv.w), acc);
+  // eight chunks' loads in flight at a time, then their fmas in chunk order
+  for (int c0 = lane; c0 < chunks; c0 += 32 * 8) {
+    uint4 xv[8], wv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int c = c0 + 32 * u;
+      if (c < chunks) {
+        xv[u] = __ldg(xr + c);
+        wv[u] = __ldg(wr + c);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (c0 + 32 * u >= chunks) break;
+      acc = __fmaf_rn(bf_lo(xv[u].x), bf_lo(wv[u].x), acc);
+      acc = __fmaf_rn(bf_hi(xv[u].x), bf_hi(wv[u].x), acc);
+      acc = __fmaf_rn(bf_lo(xv[u].y), bf_lo(wv[u].y), acc);
+      acc = __fmaf_rn(bf_hi(xv[u].y), bf_hi(wv[u].y), acc);
+      acc = __fmaf_rn(bf_lo(xv[u].z), bf_lo(wv[u].z), acc);
+      acc = __fmaf_rn(bf_hi(xv[u].z), bf_hi(wv[u].z), acc);
+      acc = __fmaf_rn(bf_lo(xv[u].w), bf_lo(wv[u].w), acc);
+      acc = __fmaf_rn(bf_hi(xv[u].w), bf_hi(wv[u].w), acc);
+    }
   }
 #pragma unroll
   for (int d = 16; d >= 1; d >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, d));
