@@ -118,6 +118,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
   if (blockIdx.x == 0)
     for (int i = tid; i < n_tick; i += blockDim.x) a.tick[i] = 0u;
   const int n_uniq = a.counts[0];
+  // the producer's first unique ids, read alongside the count (rows past the
+  // count exist: the plan holds T*k of them)
+  const int32_t u_first = (wid == kCW && lane < a.T * a.k) ? a.uniq[lane] : 0;
   const int n_exec = n_uniq + a.has_shared;
   if (wid == kCW) {
     if (lane < 3) tma_prefetch_map(&maps.m[lane]);
@@ -125,7 +128,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       // blob pointer (scale copies) and (tensor map, blob index) of entry r
       int mi = 2, bi = 0;
       if (r < n_uniq) {
-        const int32_t id = a.uniq[r];
+        const int32_t id = r == lane ? u_first : a.uniq[r];
         const int32_t slot = ffn_slot(a, id);
         mi = slot >= 0 ? 1 : 0;
         bi = slot >= 0 ? slot : id;
@@ -239,30 +242,45 @@ __global__ void __launch_bounds__(kSThreads, 1)
       // x of those tokens on this warp's groups, in fragment order, + group sums
       const int per_tok = gtot * 4;
       const int n_items = ntok * per_tok;
-      for (int it0 = 0; it0 < n_items; it0 += 32) {
-        const int it = it0 + lane;
-        const bool in = it < n_items;
-        const int n = in ? it / per_tok : 0, rem = it - n * per_tok, gi = rem >> 2, qq = rem & 3;
-        const int g = (gi / GPW) * G + w * GPW + (gi % GPW);
-        uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
-        float sx = 0.0f;
-        if (in) {
-          const uint4* px =
-              reinterpret_cast<const uint4*>(a.x + (int64_t)wtok[w][n] * H + g * 64 + qq * 16);
-          const uint4 v0 = __ldg(px), v1 = __ldg(px + 1);
-          const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      // two items per lane at a time: both loads in flight before either is used
+      for (int it0 = 0; it0 < n_items; it0 += 64) {
+        uint4 v[2][2];
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            sx += __uint_as_float(wv[j] << 16) + __uint_as_float(wv[j] & 0xFFFF0000u);
-          frag_order(wv, o0, o1);
+        for (int h = 0; h < 2; ++h) {
+          const int it = it0 + 32 * h + lane;
+          v[h][0] = v[h][1] = make_uint4(0u, 0u, 0u, 0u);
+          if (it < n_items) {
+            const int n = it / per_tok, rem = it - n * per_tok, gi = rem >> 2, qq = rem & 3;
+            const int g = (gi / GPW) * G + w * GPW + (gi % GPW);
+            const uint4* px =
+                reinterpret_cast<const uint4*>(a.x + (int64_t)wtok[w][n] * H + g * 64 + qq * 16);
+            v[h][0] = __ldg(px);
+            v[h][1] = __ldg(px + 1);
+          }
         }
-        sx += __shfl_xor_sync(0xffffffffu, sx, 1);
-        sx += __shfl_xor_sync(0xffffffffu, sx, 2);
-        if (in) {
-          uint4* d = reinterpret_cast<uint4*>(xw + (size_t)n * geo.xrow + gi * 128 + qq * 32);
-          d[0] = o0;
-          d[1] = o1;
-          if (qq == 0) xsum[gi * kTokS + n] = sx;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int it = it0 + 32 * h + lane;
+          const bool in = it < n_items;
+          const int n = in ? it / per_tok : 0, rem = it - n * per_tok, gi = rem >> 2, qq = rem & 3;
+          uint4 o0 = make_uint4(0u, 0u, 0u, 0u), o1 = o0;
+          float sx = 0.0f;
+          if (in) {
+            const uint32_t wv[8] = {v[h][0].x, v[h][0].y, v[h][0].z, v[h][0].w,
+                                    v[h][1].x, v[h][1].y, v[h][1].z, v[h][1].w};
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              sx += __uint_as_float(wv[j] << 16) + __uint_as_float(wv[j] & 0xFFFF0000u);
+            frag_order(wv, o0, o1);
+          }
+          sx += __shfl_xor_sync(0xffffffffu, sx, 1);
+          sx += __shfl_xor_sync(0xffffffffu, sx, 2);
+          if (in) {
+            uint4* d = reinterpret_cast<uint4*>(xw + (size_t)n * geo.xrow + gi * 128 + qq * 32);
+            d[0] = o0;
+            d[1] = o1;
+            if (qq == 0) xsum[gi * kTokS + n] = sx;
+          }
         }
       }
       __syncwarp();
