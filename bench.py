@@ -79,6 +79,24 @@ def peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+def max_over_ranks(ms, world, device=None):
+    """The slowest rank's time (the job's time) when N replicas run; ms itself for N = 1."""
+    if world <= 1:
+        return ms
+    import torch
+
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_barrier(world):
+    if world > 1:
+        import torch
+
+        torch.distributed.barrier()
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     for f in ("ffn_decode.cu", "ffn_stream.cu", "stream_common.cuh", "moe_internal.cuh"):
@@ -374,8 +392,7 @@ def run_gpu(args, w, rank, world, local_rank):
                 layer(xs[s, l], l, sh, ev[l])
 
     def barrier():
-        if world > 1:
-            torch.distributed.barrier()
+        rank_barrier(world)
 
     m.moe_cache_reset(spec, cache.c, sp)
     for s in range(args.warmup):
@@ -398,11 +415,7 @@ def run_gpu(args, w, rank, world, local_rank):
         t_end.record(stream)
         torch.cuda.synchronize()
     barrier()
-    ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     del graph
 
     # Per-launch FFN duration for the roofline: a second graph of the same
@@ -477,11 +490,7 @@ def run_gpu(args, w, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    ms_e2e = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms_e2e], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1), world, dev)
 
     if rank != 0:
         return
@@ -497,7 +506,9 @@ def run_gpu(args, w, rank, world, local_rank):
             "algorithmic_bytes_per_launch": ffn_bytes, "avg_launch_us": ffn_avg_s * 1e6,
             "peak_kind": peak_kind, "timing": ffn_timing}
     cpu = cpu_baseline(w, xs_h, wr_h, bias_h) if world == 1 and not args.no_cpu else None
-    launches_per_layer = 6  # logits, select, control, fill, gate/up, down
+    # moe_layer_forward: logits, control step (+ selection for T <= 16, E <= 256, else a
+    # separate select kernel), fill copy, gate/up, down
+    launches_per_layer = 5 if (T <= 16 and E <= 256) else 6
     out = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
@@ -603,10 +614,12 @@ def run_prefill(args, w, rank, world, local_rank):
     for s in range(args.warmup):
         step_overlap(s)
     torch.cuda.synchronize()
+    rank_barrier(world)
     with ClockSampler(local_rank) as clk:
         ms, evs = timed(step_overlap, args.steps, True)
+    ms = max_over_ranks(ms, world, dev)
     route_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    ffn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    ffn_ms = max_over_ranks(statistics.mean(e[1].elapsed_time(e[2]) for e in evs), world, dev)
     for s in range(min(args.warmup, 3)):
         step_serial(s)
     ms_serial, _ = timed(step_serial, args.steps, False)
@@ -635,7 +648,9 @@ def run_prefill(args, w, rank, world, local_rank):
     comp_done[1].record(main)
     for s in range(min(args.warmup, 3)):
         e2e_step(s)
+    rank_barrier(world)
     ms_e2e, _ = timed(e2e_step, args.steps, False)
+    ms_e2e = max_over_ranks(ms_e2e, world, dev)
     if rank != 0:
         return
     _, bf16_peak, peak_kind = peaks()
@@ -651,7 +666,7 @@ def run_prefill(args, w, rank, world, local_rank):
     # value: the whole layer step (route + expert FFN with the next layer's copy
     # overlapped); the roofline entry is the expert FFN call alone
     out = {
-        "metric": METRIC, "value": flops / (step_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "metric": METRIC, "value": world * flops / (step_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
         "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
@@ -671,7 +686,7 @@ def run_prefill(args, w, rank, world, local_rank):
         "e2e": {"value": flops * args.steps * world / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "tok_s": tokens / (ms_e2e * 1e-3),
                 "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 4},
-        "gpu_launches": 10 * args.steps,
+        "gpu_launches": 9 * args.steps,  # logits, select, 7 FFN kernels (the copy is a memcpy)
         "clocks": clk.summary(),
     }
     if world == 1 and not args.no_cpu:
@@ -823,6 +838,7 @@ def run_sweep(args, w, rank, world, local_rank):
                 del graphs
             torch.cuda.synchronize()
     row, ms, cache, graphs = head
+    ms = max_over_ranks(ms, world, dev)
 
     # end to end at the headline point: each 64-step chunk of the trace is copied
     # in from pinned host memory and its counts copied back, inside the timed region
@@ -838,14 +854,14 @@ def run_sweep(args, w, rank, world, local_rank):
         st_host[s0 * L:s1 * L].copy_(stats[s0 * L:s1 * L], non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    ms_e2e = e0.elapsed_time(e1)
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1), world, dev)
     if rank != 0:
         return
     hbm, _, peak_kind = peaks()
     t_call = ms * 1e-3 / calls
     scan = row["slots"] * 8 + (k + K) * 16            # ts + id_of_slot scan, plan rows
     out = {
-        "metric": METRIC, "value": calls / (ms * 1e-3), "unit": "layer-steps/s",
+        "metric": METRIC, "value": world * calls / (ms * 1e-3), "unit": "layer-steps/s",
         "n_gpus": world, "steps": n, "warmup": 1, "ms_per_step": ms / n,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
         "data": "synthetic",
@@ -858,7 +874,7 @@ def run_sweep(args, w, rank, world, local_rank):
                      "kernel": "control step (one CTA, latency-bound)", "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": scan, "avg_launch_us": t_call * 1e6},
         "sweep": rows,
-        "e2e": {"value": calls / (ms_e2e * 1e-3), "unit": "layer-steps/s",
+        "e2e": {"value": world * calls / (ms_e2e * 1e-3), "unit": "layer-steps/s",
                 "h2d_bytes_per_step": L * k * 4, "d2h_bytes_per_step": L * 32},
         "gpu_launches": calls,
         "clocks": clk.summary(),
