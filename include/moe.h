@@ -299,6 +299,36 @@ int moe_expert_ffn_noalloc(const moe_spec* spec, const moe_cache* cache, int32_t
                            const float* weights, const void* shared, float* y,
                            moe_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * moe_profile_bandwidths -- measure B_P and B_H on this device
+ * (FreeToken summary "method steps": B_P and B_H are measured on the deployed
+ * machine before q* is used; "weaknesses": they drift, so they should be
+ * re-measured rather than read once from a specification sheet).
+ *   B_P: expert blobs copied from the bank by the library's fill copy (the
+ *        same kernel as the step's fills), into scratch inside `workspace`,
+ *        never into the slot pool.  Rate = blob bytes moved per second.
+ *   B_H: the decode expert FFN (T = 1, the spec's top_k experts 0..k-1 of
+ *        `layer`, no shared expert) executed where the cache tables place
+ *        those experts (slot if resident, else in place from the bank).
+ *        Rate = expert weight bytes executed per second.
+ * Both are returned in MB/s (1 MB = 10^6 bytes), the units of
+ * moe_cache.bp_mbps / bh_mbps, so the result can be stored there directly.
+ *   cache          tables and bank are read, nothing is written (tables,
+ *                  recency stamps, clock and slot pool are left unchanged)
+ *   layer          0 <= layer < num_layers
+ *   workspace      device, >= moe_profile_workspace_bytes(spec), 256-B aligned;
+ *                  its contents are overwritten
+ *   reps           >= 1 timed repetitions of each measurement (after 2 warm-up)
+ *   bp_mbps, bh_mbps  host out-pointers
+ * Unlike the step entry points this call synchronises the stream (it reads
+ * CUDA event timings) and creates and destroys two CUDA events; it must not
+ * be called during stream capture.
+ * ------------------------------------------------------------------------ */
+size_t moe_profile_workspace_bytes(const moe_spec* spec);
+int moe_profile_bandwidths(const moe_spec* spec, const moe_cache* cache, int32_t layer,
+                           void* workspace, size_t workspace_bytes, int32_t reps,
+                           int32_t* bp_mbps, int32_t* bh_mbps, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

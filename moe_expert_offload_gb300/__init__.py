@@ -111,6 +111,11 @@ def lib():
                                                 vp, vp]
         L.moe_expert_ffn_noalloc.restype = C.c_int
         L.moe_expert_ffn_noalloc.argtypes = [sp, cp, i32, pp, vp, i32, vp, vp, vp, vp, vp]
+        L.moe_profile_workspace_bytes.restype = sz
+        L.moe_profile_workspace_bytes.argtypes = [sp]
+        L.moe_profile_bandwidths.restype = C.c_int
+        L.moe_profile_bandwidths.argtypes = [sp, cp, i32, vp, sz, i32, C.POINTER(i32),
+                                             C.POINTER(i32), vp]
         _lib = L
     return _lib
 
@@ -201,6 +206,19 @@ def moe_layer_forward(spec, cache, layer, x, T, w_router, bias, shared, plan, id
 
 def moe_prefill_workspace_bytes(spec, T) -> int:
     return int(lib().moe_prefill_workspace_bytes(C.byref(spec), T))
+
+
+def moe_profile_workspace_bytes(spec) -> int:
+    return int(lib().moe_profile_workspace_bytes(C.byref(spec)))
+
+
+def moe_profile_bandwidths(spec, cache, layer, workspace, workspace_bytes, reps=10, stream=None):
+    """(B_P, B_H) in MB/s measured on the device (synchronises the stream)."""
+    bp, bh = C.c_int32(0), C.c_int32(0)
+    _check(lib().moe_profile_bandwidths(C.byref(spec), C.byref(cache), layer, _ptr(workspace),
+                                        workspace_bytes, reps, C.byref(bp), C.byref(bh),
+                                        _stream(stream)))
+    return bp.value, bh.value
 
 
 def moe_layer_prefetch(spec, bank, layer, dst, stream=None):

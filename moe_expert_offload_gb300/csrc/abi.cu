@@ -396,6 +396,169 @@ int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, con
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
+// On-device B_P / B_H measurement.
+namespace {
+
+constexpr int kProfCopies = 2;  // blobs per timed fill copy
+
+struct ProfLayout {
+  size_t copy, counts_c, ids_c, slots_c, counts_f, uniq, fill_ids, err, ids, wts, x, y, ffn, total;
+};
+
+ProfLayout prof_layout(const moe_spec* s) {
+  ProfLayout L;
+  const size_t se = moe::blob_offsets(s->hidden, s->inter).total;
+  const size_t k = (size_t)s->top_k;
+  size_t o = 0;
+  auto take = [&](size_t b) {
+    const size_t at = o;
+    o += align256(b);
+    return at;
+  };
+  L.copy = take((size_t)kProfCopies * se);
+  L.counts_c = take(8 * 4);
+  L.ids_c = take(kProfCopies * 4);
+  L.slots_c = take(kProfCopies * 4);
+  L.counts_f = take(8 * 4);
+  L.uniq = take(k * 4);
+  L.fill_ids = take(k * 4);
+  L.err = take(4);
+  L.ids = take(k * 4);
+  L.wts = take(k * 4);
+  L.x = take((size_t)s->hidden * 2);
+  L.y = take((size_t)s->hidden * 4);
+  L.ffn = take(moe::ffn_workspace_bytes(s->hidden, s->inter, s->top_k, 1, 0));
+  L.total = o;
+  return L;
+}
+
+// Milliseconds of `reps` launches of fn on st (after two untimed ones).
+template <typename F>
+cudaError_t time_reps(F fn, int reps, cudaStream_t st, float* ms) {
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  cudaError_t e = cudaEventCreate(&e0);
+  if (e == cudaSuccess) e = cudaEventCreate(&e1);
+  for (int i = 0; e == cudaSuccess && i < 2; ++i) e = fn();
+  if (e == cudaSuccess) e = cudaEventRecord(e0, st);
+  for (int i = 0; e == cudaSuccess && i < reps; ++i) e = fn();
+  if (e == cudaSuccess) e = cudaEventRecord(e1, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = cudaEventElapsedTime(ms, e0, e1);
+  if (e0) cudaEventDestroy(e0);
+  if (e1) cudaEventDestroy(e1);
+  return e;
+}
+
+}  // namespace
+
+extern "C" size_t moe_profile_workspace_bytes(const moe_spec* spec) {
+  if (check_spec(spec) != MOE_OK) return 0;
+  return prof_layout(spec).total;
+}
+
+extern "C" int moe_profile_bandwidths(const moe_spec* spec, const moe_cache* cache,
+                                      int32_t layer, void* workspace, size_t workspace_bytes,
+                                      int32_t reps, int32_t* bp_mbps, int32_t* bh_mbps,
+                                      moe_stream_t stream) {
+  int rc = check_spec(spec);
+  if (rc) return rc;
+  rc = check_cache(spec, cache, true);
+  if (rc) return rc;
+  if (layer < 0 || layer >= spec->num_layers) return fail(MOE_EINVAL, "layer out of range");
+  if (reps < 1) return fail(MOE_EINVAL, "reps must be >= 1");
+  if (!bp_mbps || !bh_mbps) return fail(MOE_EINVAL, "moe_profile_bandwidths: NULL output");
+  if (spec->top_k > spec->num_experts) return fail(MOE_EINVAL, "top_k > num_experts");
+  if (!workspace || !aligned(workspace, 256)) return fail(MOE_EINVAL, "workspace must be 256-B aligned");
+  const ProfLayout L = prof_layout(spec);
+  if (workspace_bytes < L.total)
+    return fail(MOE_ECAPACITY, "workspace %zu < %zu bytes", workspace_bytes, L.total);
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+    return fail(MOE_EINVAL, "moe_profile_bandwidths cannot run during stream capture");
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto i32 = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
+  const int E = spec->num_experts, k = spec->top_k;
+  const int64_t se = moe::blob_offsets(spec->hidden, spec->inter).total;
+
+  // fill plan: experts 0, 1 of the layer into scratch blobs 0, 1
+  int32_t hc[8] = {0, 0, 0, 0, kProfCopies, 0, 0, 0};
+  int32_t hid[kProfCopies], hsl[kProfCopies];
+  for (int i = 0; i < kProfCopies; ++i) {
+    hid[i] = layer * E + (i % E);
+    hsl[i] = i;
+  }
+  // FFN plan: experts 0..k-1 of the layer for one token, all executed, none filling
+  int32_t hf[8] = {k, 0, k, 0, 0, k, 0, 0};
+  int32_t huniq[64], hids[64];
+  float hw[64];
+  for (int j = 0; j < k; ++j) {
+    huniq[j] = layer * E + j;
+    hids[j] = j;
+    hw[j] = 1.0f / (float)k;
+  }
+  cudaError_t e = cudaMemcpyAsync(i32(L.counts_c), hc, sizeof(hc), cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(i32(L.ids_c), hid, sizeof(hid), cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(i32(L.slots_c), hsl, sizeof(hsl), cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(i32(L.counts_f), hf, sizeof(hf), cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(i32(L.uniq), huniq, k * 4, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws + L.fill_ids, 0xff, (size_t)k * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws + L.err, 0, 4, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(i32(L.ids), hids, k * 4, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(ws + L.wts, hw, k * 4, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws + L.x, 0, (size_t)spec->hidden * 2, st);
+  // the host arrays above are read before this call returns
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "profile setup");
+
+  moe_plan fp{};
+  fp.counts = i32(L.counts_c);
+  fp.fill_ids = i32(L.ids_c);
+  fp.fill_slots = i32(L.slots_c);
+  const uint8_t* bank = static_cast<const uint8_t*>(cache->bank);
+  float ms_p = 0.0f, ms_h = 0.0f;
+  e = time_reps([&] { return moe::launch_fill_copy(fp, kProfCopies, bank, ws + L.copy, se, st); },
+                reps, st, &ms_p);
+  if (e != cudaSuccess) return cuda_fail(e, "profile fill copy");
+
+  moe::FfnArgs a;
+  a.H = spec->hidden;
+  a.I = spec->inter;
+  a.E = E;
+  a.k = k;
+  a.layer = layer;
+  a.T = 1;
+  a.has_shared = 0;
+  a.blob_bytes = se;
+  a.bank = bank;
+  a.pool = static_cast<const uint8_t*>(cache->slot_pool);
+  a.n_bank = spec->num_layers * E;
+  a.n_pool = cache->num_slots;
+  a.slot_of_id = cache->slot_of_id;
+  a.uniq = i32(L.uniq);
+  a.counts = i32(L.counts_f);
+  a.fill_ids = i32(L.fill_ids);
+  a.err = i32(L.err);
+  a.x = reinterpret_cast<const uint16_t*>(ws + L.x);
+  a.ids = i32(L.ids);
+  a.weights = reinterpret_cast<const float*>(ws + L.wts);
+  a.shared = nullptr;
+  a.y = reinterpret_cast<float*>(ws + L.y);
+  moe::ffn_carve_workspace(a, ws + L.ffn);
+  e = time_reps([&] { return moe::launch_ffn_decode(a, st); }, reps, st, &ms_h);
+  if (e != cudaSuccess) return cuda_fail(e, "profile FFN");
+  int32_t derr = 0;
+  e = cudaMemcpy(&derr, ws + L.err, 4, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "profile FFN status");
+  if (derr) return fail(MOE_ECUDA, "profile FFN flagged device error bits 0x%x", derr);
+  const double bp = (double)kProfCopies * se * reps / (ms_p * 1e-3) / 1e6;
+  const double bh = (double)k * se * reps / (ms_h * 1e-3) / 1e6;
+  *bp_mbps = (int32_t)(bp < 2e9 ? (bp < 1.0 ? 1.0 : bp) : 2e9);
+  *bh_mbps = (int32_t)(bh < 2e9 ? (bh < 1.0 ? 1.0 : bh) : 2e9);
+  return ok();
+}
+
+// ---------------------------------------------------------------------------
 // Prefill entry points.
 namespace {
 

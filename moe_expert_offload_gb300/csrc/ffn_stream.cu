@@ -144,8 +144,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
 
   const int tpe = I / 16;
   const int n_units = n_exec * tpe;
-  const int u_lo = (int)((int64_t)blockIdx.x * n_units / gridDim.x);
-  const int u_hi = (int)((int64_t)(blockIdx.x + 1) * n_units / gridDim.x);
+  // (32-bit: units x CTAs stays far below 2^32 for every shape the stream path takes)
+  const int u_lo = (int)(blockIdx.x * (unsigned)n_units / gridDim.x);
+  const int u_hi = (int)((blockIdx.x + 1) * (unsigned)n_units / gridDim.x);
   const BlobOffsets off = blob_offsets(H, I);
   unsigned char* stages = smem;
   unsigned char* sraw = smem + geo.o_raw;
@@ -555,8 +556,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
 
   const int upe = H / kRowsB;
   const int n_units = n_exec * upe;
-  const int u_lo = (int)((int64_t)blockIdx.x * n_units / gridDim.x);
-  const int u_hi = (int)((int64_t)(blockIdx.x + 1) * n_units / gridDim.x);
+  // (32-bit: units x CTAs stays far below 2^32 for every shape the stream path takes)
+  const int u_lo = (int)(blockIdx.x * (unsigned)n_units / gridDim.x);
+  const int u_hi = (int)((blockIdx.x + 1) * (unsigned)n_units / gridDim.x);
   const BlobOffsets off = blob_offsets(H, I);
   unsigned char* stages = smem;
   unsigned char* sraw = smem + geo.o_raw;

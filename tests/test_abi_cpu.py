@@ -187,3 +187,21 @@ def test_prefill_argument_checks(L):
     assert e.value.code == m.MOE_EINVAL
     assert m.moe_expert_ffn_prefill(s2, None, None, 0, None, None, None, None, None, 0, None,
                                     stream=0) == m.MOE_OK
+
+
+def test_profile_argument_checks(L):
+    s = _spec()
+    need = m.moe_profile_workspace_bytes(s)
+    assert need >= 2 * m.moe_expert_bytes(s)  # two blobs of copy scratch at least
+    with pytest.raises(m.MoeError) as e:  # workspace too small
+        m.moe_profile_bandwidths(s, _cache(), 0, 4096, need - 1, reps=2, stream=0)
+    assert e.value.code == m.MOE_ECAPACITY
+    with pytest.raises(m.MoeError) as e:  # layer out of range
+        m.moe_profile_bandwidths(s, _cache(), 5, 4096, need, reps=2, stream=0)
+    assert e.value.code == m.MOE_EINVAL
+    with pytest.raises(m.MoeError) as e:
+        m.moe_profile_bandwidths(s, _cache(), 0, 4096, need, reps=0, stream=0)
+    assert e.value.code == m.MOE_EINVAL
+    with pytest.raises(m.MoeError) as e:  # misaligned workspace
+        m.moe_profile_bandwidths(s, _cache(), 0, 4100, need, reps=2, stream=0)
+    assert e.value.code == m.MOE_EINVAL

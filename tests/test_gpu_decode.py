@@ -468,3 +468,35 @@ def test_expert_ffn_no_valid_expert_writes_zero(oracle, H, I):
     gp = plan.read(2)
     assert gp["err"] & m.MOE_DERR_BAD_ID and gp["n_uniq"] == 0
     assert torch.count_nonzero(y).item() == 0
+
+
+def test_profile_bandwidths_leaves_cache_and_feeds_q(oracle):
+    """On-device B_P / B_H: positive rates, the cache (tables, stamps, clock, slot pool)
+    untouched, and a control step with the measured values still matches the oracle."""
+    L, H, I, E, k, S, K = 2, 2048, 512, 16, 8, 6, 8
+    spec, bank, bank_h, cache, _ = _layer_rig(L, H, I, E, k, S, K, 52700, 77300, False)
+    plan = m.DevicePlan(k, K, device=DEV)
+    ost = oracle.CacheState(L * E, S)
+    rng = np.random.default_rng(11)
+    for step in range(4):  # populate some slots
+        ids_h = rng.choice(E, size=(1, k), replace=False).astype(np.int32)
+        m.moe_cache_step(spec, cache.c, step % L, dev(ids_h, DEV), 1, plan.c, 1)
+        oracle.cache_step(ost, E, step % L, ids_h, K, 52700, 77300)
+    torch.cuda.synchronize()
+    before = cache.host_tables()
+    pool_before = cache.pool.clone()
+    wsb = m.moe_profile_workspace_bytes(spec)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    bp, bh = m.moe_profile_bandwidths(spec, cache.c, 1, ws, wsb, reps=4)
+    assert 1_000 < bp < 100_000_000 and 1_000 < bh < 100_000_000, (bp, bh)
+    after = cache.host_tables()
+    for x, y in zip(before, after):
+        assert np.array_equal(x, y)
+    assert torch.equal(pool_before, cache.pool)
+    # the measured rates drive q* like configured ones
+    cache.c.bp_mbps, cache.c.bh_mbps = bp, bh
+    ids_h = rng.choice(E, size=(1, k), replace=False).astype(np.int32)
+    m.moe_cache_step(spec, cache.c, 0, dev(ids_h, DEV), 1, plan.c, 0)
+    torch.cuda.synchronize()
+    op = oracle.cache_step(ost, E, 0, ids_h, K, bp, bh)
+    _plans_equal(plan.read(K), op, K)
