@@ -394,6 +394,15 @@ def run_gpu(args, w, rank, world, local_rank):
     def barrier():
         rank_barrier(world)
 
+    # B_P / B_H measured on this device and shape (untimed); with --adaptive-q they
+    # replace the configured rates for the whole run
+    pws_bytes = m.moe_profile_workspace_bytes(spec)
+    pws = torch.empty(pws_bytes, dtype=torch.uint8, device=dev)
+    m.moe_cache_reset(spec, cache.c, sp)
+    bp_meas, bh_meas = m.moe_profile_bandwidths(spec, cache.c, 0, pws, pws_bytes, reps=10)
+    del pws
+    if args.adaptive_q:
+        cache.c.bp_mbps, cache.c.bh_mbps = bp_meas, bh_meas
     m.moe_cache_reset(spec, cache.c, sp)
     for s in range(args.warmup):
         step(s)
@@ -523,6 +532,11 @@ def run_gpu(args, w, rank, world, local_rank):
                 "h2d_bytes_per_step": L * T * H * 2, "d2h_bytes_per_step": L * T * H * 4},
         "gpu_launches": launches_per_layer * L * args.steps,
         "clocks": clk.summary(),
+        "calibration": {"bp_mbps": bp_meas, "bh_mbps": bh_meas,
+                        "configured_mbps": [w["bp"], w["bh"]], "used": "measured" if args.adaptive_q
+                        else "configured",
+                        "how": "moe_profile_bandwidths: the fill copy (B_P) and the decode FFN "
+                               "(B_H) timed on this device, layer 0, untimed"},
         "cache": {"miss_rate": n_miss / max(n_uniq, 1), "fill_per_layer": n_fill / layer_steps,
                   "direct_per_layer": n_direct / layer_steps,
                   "uniq_per_layer": n_uniq / layer_steps},
@@ -915,6 +929,9 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the timed CPU oracle baseline")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (small cases for profiling)")
+    ap.add_argument("--adaptive-q", action="store_true",
+                    help="decode: use B_P / B_H measured on the device instead of the configured "
+                         "rates")
     ap.add_argument("--experts", type=int, default=0,
                     help="override the experts per layer (small cases for profiling; same expert "
                          "shape, slot count scaled in proportion)")
