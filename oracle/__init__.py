@@ -57,8 +57,10 @@ def lib():
         L.or_q_star.restype = i32
         L.or_q_star.argtypes = [i32, i32, i32]
         L.or_cache_step.restype = i32
-        L.or_cache_step.argtypes = [i32, i32, vp, i32, i32, i32, i32, i32,
+        L.or_cache_step.argtypes = [i32, i32, vp, i32, i32, i32, i32, i32, i32, i32,
                                     vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.or_cache_place.restype = i32
+        L.or_cache_place.argtypes = [i32, i32, i32, i32, vp, i32, vp, vp, vp, vp]
         L.or_expert_forward.argtypes = [vp, i32, i32, vp, i32, vp]
         L.or_moe_ffn.argtypes = [vp, i32, i32, i32, vp, i32, vp, vp, i32, vp, i32, vp]
         _lib = L
@@ -162,8 +164,23 @@ class CacheState:
         return c
 
 
-def cache_step(state: CacheState, E: int, layer: int, ids: np.ndarray, K: int, bp: int, bh: int):
-    """Run one control step in place on `state`; return the plan as a dict."""
+SHARED_LRU, LAYER_LRU, STATIC = 0, 1, 2
+
+
+def cache_place(state: CacheState, E: int, L: int, ids, policy: int = SHARED_LRU):
+    """Empty `state`, then preload the bank ids `ids` (l*E + e) into slots."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32).reshape(-1)
+    rc = lib().or_cache_place(E, L, state.id_of_slot.size, policy, _vp(ids), ids.size,
+                              _vp(state.slot_of_id), _vp(state.id_of_slot), _vp(state.ts),
+                              _vp(state.clock))
+    if rc:
+        raise ValueError("cache_place: bad id list for this cache / policy")
+
+
+def cache_step(state: CacheState, E: int, layer: int, ids: np.ndarray, K: int, bp: int, bh: int,
+               policy: int = SHARED_LRU, L: int = 1):
+    """Run one control step in place on `state`; return the plan as a dict.
+    `L` (the number of layers) matters only for the per-layer policy."""
     ids = np.ascontiguousarray(ids, dtype=np.int32).reshape(-1)
     n = ids.size
     S = state.id_of_slot.size
@@ -172,14 +189,14 @@ def cache_step(state: CacheState, E: int, layer: int, ids: np.ndarray, K: int, b
             ("uniq", "hit_ids", "hit_slots", "fill_ids", "fill_slots", "evicted_ids", "direct_ids")}
     victims = np.full(max(K, 1), -1, dtype=np.int32)
     counts = np.zeros(8, dtype=np.int32)
-    rc = lib().or_cache_step(E, layer, _vp(ids), n, S, K, bp, bh,
+    rc = lib().or_cache_step(E, layer, _vp(ids), n, S, K, bp, bh, policy, L,
                              _vp(state.slot_of_id), _vp(state.id_of_slot), _vp(state.ts),
                              _vp(state.clock), _vp(bufs["uniq"]), _vp(bufs["hit_ids"]),
                              _vp(bufs["hit_slots"]), _vp(bufs["fill_ids"]), _vp(bufs["fill_slots"]),
                              _vp(bufs["evicted_ids"]), _vp(bufs["direct_ids"]), _vp(victims),
                              _vp(counts))
     if rc:
-        raise ValueError("cache_step: routed id out of range")
+        raise ValueError("cache_step: routed id out of range or bad policy")
     n_uniq, n_hit, n_miss, q, n_fill, n_direct, n_vict, now = (int(v) for v in counts)
     return {
         "uniq": bufs["uniq"][:n_uniq].copy(),

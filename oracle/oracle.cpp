@@ -327,14 +327,33 @@ int or_q_star(int m, int bp, int bh) {
 //   7. for i < n_fill: slot v = victims[i] drops its old id and takes F[i]
 //      with ts = now.
 // counts = {n_uniq, n_hit, n_miss, q, n_fill, n_direct, n_victims, now}.
-// Returns 0, or -1 on an id outside [0, E).
+//
+// Replacement policy (`policy`), for the miss-rate comparison of FreeToken
+// summary "core method" and reader Figure 4(b), and Edge0 §3.1 "hot" path:
+//   0  shared LRU: one pool for all layers, as above (FreeToken)
+//   1  per-layer LRU: layer l owns the fixed slot range [l*S_l, (l+1)*S_l)
+//      with S_l = floor(S / L); step 5 scans only that range, so each layer
+//      runs its own LRU (Edge0 "hot" path: a fixed per-layer resident set);
+//      the S - L*S_l slots past the last range stay unused
+//   2  static placement: the slots hold what or_cache_place put there and
+//      nothing is ever filled (q = 0, every miss goes to C); the pages'
+//      baselines pin "hot" experts or whole layers at load time
+// Returns 0, or -1 on an id outside [0, E), an unknown policy, or policy 1
+// with S < L.
 int or_cache_step(int E, int layer, const int32_t* ids, int n_ids, int S, int K, int bp, int bh,
-                  int32_t* slot_of_id, int32_t* id_of_slot, uint32_t* ts, uint32_t* clock,
-                  int32_t* uniq, int32_t* hit_ids, int32_t* hit_slots, int32_t* fill_ids,
-                  int32_t* fill_slots, int32_t* evicted_ids, int32_t* direct_ids, int32_t* victims,
-                  int32_t* counts) {
+                  int policy, int L, int32_t* slot_of_id, int32_t* id_of_slot, uint32_t* ts,
+                  uint32_t* clock, int32_t* uniq, int32_t* hit_ids, int32_t* hit_slots,
+                  int32_t* fill_ids, int32_t* fill_slots, int32_t* evicted_ids,
+                  int32_t* direct_ids, int32_t* victims, int32_t* counts) {
   for (int i = 0; i < n_ids; ++i)
     if (ids[i] < 0 || ids[i] >= E) return -1;
+  if (policy < 0 || policy > 2) return -1;
+  if (policy == 1 && (L < 1 || S < L)) return -1;
+  int s_lo = 0, s_hi = S;  // the slots this step may take victims from
+  if (policy == 1) {
+    s_lo = layer * (S / L);
+    s_hi = s_lo + S / L;
+  }
   uint32_t now = *clock + 1;
   *clock = now;
 
@@ -355,10 +374,10 @@ int or_cache_step(int E, int layer, const int32_t* ids, int n_ids, int S, int K,
     }
   }
   int m = (int)M.size();
-  int q = or_q_star(m, bp, bh);
+  int q = policy == 2 ? 0 : or_q_star(m, bp, bh);
 
   std::vector<std::pair<uint32_t, int32_t>> keys;
-  for (int32_t v = 0; v < S; ++v)
+  for (int32_t v = s_lo; v < s_hi; ++v)
     if (ts[v] != now) keys.push_back({ts[v], v});
   std::sort(keys.begin(), keys.end());
   int nv = std::min<int>(K, (int)keys.size());
@@ -392,6 +411,43 @@ int or_cache_step(int E, int layer, const int32_t* ids, int n_ids, int S, int K,
   counts[5] = n_direct;
   counts[6] = nv;
   counts[7] = (int32_t)now;
+  return 0;
+}
+
+// Preload of a chosen set of bank ids (the static placements the pages
+// compare against: KTransformers-style "hot" experts, llama.cpp-style whole
+// layers; also a warm start for the LRU policies).  The tables are emptied,
+// then ids[i] (= l*E + e) goes to
+//   policy 0, 2: slot i
+//   policy 1:    slot l*S_l + (number of ids of layer l before it in the list)
+// with ts = 0 (placed, not yet used) and clock = 0.  Returns 0, or -1 on an
+// id outside [0, L*E), a repeated id, more ids than slots (per layer range
+// for policy 1), an unknown policy, or policy 1 with S < L.
+int or_cache_place(int E, int L, int S, int policy, const int32_t* ids, int n,
+                   int32_t* slot_of_id, int32_t* id_of_slot, uint32_t* ts, uint32_t* clock) {
+  if (policy < 0 || policy > 2 || n < 0 || L < 1 || S < 1) return -1;
+  if (policy == 1 && S < L) return -1;
+  const int n_ids = L * E;
+  std::vector<int32_t> slot(n_ids, -1), owner(S, -1), used(L, 0);
+  for (int i = 0; i < n; ++i) {
+    const int32_t u = ids[i];
+    if (u < 0 || u >= n_ids || slot[u] >= 0) return -1;
+    int v = i;
+    if (policy == 1) {
+      const int l = u / E;
+      if (used[l] >= S / L) return -1;
+      v = l * (S / L) + used[l]++;
+    }
+    if (v >= S) return -1;
+    slot[u] = v;
+    owner[v] = u;
+  }
+  for (int u = 0; u < n_ids; ++u) slot_of_id[u] = slot[u];
+  for (int v = 0; v < S; ++v) {
+    id_of_slot[v] = owner[v];
+    ts[v] = 0;
+  }
+  *clock = 0;
   return 0;
 }
 

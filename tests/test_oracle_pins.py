@@ -412,6 +412,109 @@ def test_control_step_rejects_bad_ids(oracle):
         oracle.cache_step(st, 16, 0, np.array([3, 16]), 2, 1, 2)
 
 
+# ------------------------------------------------ replacement policies (1, 2)
+@pytest.mark.parametrize("seed", range(6))
+def test_layer_lru_equals_independent_lru_per_layer(oracle, seed):
+    """Edge0 §3.1 "hot" path: a fixed per-layer resident set.  Policy 1 over an
+    interleaved multi-layer trace must act as L separate LRU caches of S_l =
+    floor(S / L) slots, each seeing only its own layer's steps, at slot offset
+    l * S_l; the slots past L * S_l are never used."""
+    rng = np.random.default_rng(100 + seed)
+    E, L = 12, 3
+    S = int(rng.integers(L, 14))
+    Sl = S // L
+    K = int(rng.integers(1, 6))
+    bp, bh = [(52700, 77300), (11800, 47500), (77300, 77300)][seed % 3]
+    st = oracle.CacheState(L * E, S)
+    refs = [BruteLRU(Sl) for _ in range(L)]
+    for step in range(150):
+        layer = int(rng.integers(0, L))  # uneven, random layer order
+        ids = rng.integers(0, E, size=(int(rng.integers(1, 4)), 2))
+        plan = oracle.cache_step(st, E, layer, ids, K, bp, bh, policy=oracle.LAYER_LRU, L=L)
+        r = refs[layer].run(E, layer, ids.reshape(-1), K, bp, bh)
+        off = layer * Sl
+        assert list(plan["hit_ids"]) == r["hit"]
+        assert list(plan["fill_ids"]) == r["fill"]
+        assert list(plan["fill_slots"]) == [off + v for v in r["fill_slots"]]
+        assert list(plan["direct_ids"]) == r["direct"]
+        assert list(plan["evicted_ids"]) == r["evicted"]
+        assert [v for v in plan["victims"] if v >= 0] == [off + v for v in r["victims"]]
+        assert plan["q"] == r["q"]
+        for v in np.nonzero(st.id_of_slot >= 0)[0]:
+            assert v < L * Sl and st.id_of_slot[v] // E == v // Sl
+
+
+def test_layer_lru_closed_forms(oracle):
+    """With room for a whole layer (S_l >= E) and pure fill, an LRU misses each
+    id exactly once (compulsory misses only); with S_l = 1 and one new expert
+    per step it misses on every change of expert and hits on every repeat."""
+    E, L, K = 8, 2, 8
+    st = oracle.CacheState(L * E, L * E)
+    rng = np.random.default_rng(7)
+    seen, misses = set(), 0
+    for step in range(200):
+        layer = step % L
+        ids = rng.integers(0, E, size=3)
+        plan = oracle.cache_step(st, E, layer, ids, K, 77300, 77300,
+                                 policy=oracle.LAYER_LRU, L=L)
+        misses += plan["n_miss"]
+        seen |= {layer * E + int(i) for i in ids}
+    assert misses == len(seen)
+    st = oracle.CacheState(L * E, L)
+    seq = [3, 3, 5, 5, 5, 2, 3, 3]
+    got = [oracle.cache_step(st, E, 1, np.array([e]), 1, 77300, 77300, policy=oracle.LAYER_LRU,
+                             L=L)["n_hit"] for e in seq]
+    assert got == [0, 1, 0, 1, 1, 0, 0, 1]
+    assert st.id_of_slot[0] == -1 and st.id_of_slot[1] == E + 3
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_static_policy_is_membership(oracle, seed):
+    """Policy 2 (the pages' static baselines): the placed set never changes,
+    a routed id hits iff it was placed, and every miss goes to C (q = 0)."""
+    rng = np.random.default_rng(200 + seed)
+    E, L, S = 16, 4, 20
+    placed = rng.choice(L * E, size=S - 3, replace=False)
+    st = oracle.CacheState(L * E, S)
+    oracle.cache_place(st, E, L, placed, policy=oracle.STATIC)
+    soi, ios = st.slot_of_id.copy(), st.id_of_slot.copy()
+    pset = set(int(u) for u in placed)
+    for step in range(100):
+        layer = step % L
+        ids = rng.integers(0, E, size=(2, 3))
+        plan = oracle.cache_step(st, E, layer, ids, 4, 52700, 77300, policy=oracle.STATIC, L=L)
+        U = sorted({layer * E + int(i) for i in ids.reshape(-1)})
+        assert list(plan["hit_ids"]) == [u for u in U if u in pset]
+        assert list(plan["direct_ids"]) == [u for u in U if u not in pset]
+        assert plan["q"] == 0 and plan["n_fill"] == 0
+        assert np.array_equal(st.slot_of_id, soi) and np.array_equal(st.id_of_slot, ios)
+
+
+def test_cache_place_layout_and_errors(oracle):
+    E, L, S = 10, 3, 10
+    st = oracle.CacheState(L * E, S)
+    ids = [25, 3, 14, 4, 11]
+    for policy in (oracle.SHARED_LRU, oracle.STATIC):
+        oracle.cache_place(st, E, L, ids, policy=policy)
+        assert list(st.id_of_slot) == ids + [-1] * (S - len(ids))
+        assert [st.slot_of_id[u] for u in ids] == list(range(len(ids)))
+        assert np.sum(st.slot_of_id >= 0) == len(ids)
+        assert not st.ts.any() and st.clock[0] == 0
+    # per-layer: S_l = 3; layer 0 -> slots 0.., layer 1 -> 3.., layer 2 -> 6..; slot 9 unused
+    oracle.cache_place(st, E, L, ids, policy=oracle.LAYER_LRU)
+    assert list(st.id_of_slot) == [3, 4, -1, 14, 11, -1, 25, -1, -1, -1]
+    bad = [[3, 3], [30], [-1], list(range(11)), [0, 1, 2, 5]]  # dup, range, range, > S, > S_l
+    for b in bad:
+        with pytest.raises(ValueError):
+            oracle.cache_place(st, E, L, b, policy=oracle.LAYER_LRU if b == [0, 1, 2, 5]
+                               else oracle.SHARED_LRU)
+    with pytest.raises(ValueError):
+        oracle.cache_step(oracle.CacheState(L * E, 2), E, 0, np.array([1]), 1, 1, 2,
+                          policy=oracle.LAYER_LRU, L=L)  # S < L
+    with pytest.raises(ValueError):
+        oracle.cache_step(st, E, 0, np.array([1]), 1, 1, 2, policy=3, L=L)
+
+
 # ---------------------------------------------------------------------- FFN
 def _uniform_expert(H, I, code, s, b):
     qg = np.full((I, H), code, np.uint8)
