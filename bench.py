@@ -64,10 +64,13 @@ WORKLOADS = {
         desc="Cache stress sweep: 40 layers x 256 experts, top-8, Zipf(1.1) routing traces of "
              "2048 steps per layer with 70% step-to-step overlap fed straight to the control "
              "step (no router, no fill); capacity 5/10/25/50% of pairs x B_P/B_H in "
-             "{52.7/77.3, 11.8/47.5, 77.3/77.3} GB/s, K=8",
+             "{52.7/77.3, 11.8/47.5, 77.3/77.3} GB/s, K=8; replacement policies (shared LRU, "
+             "per-layer LRU, static hot set, static whole layers) replayed on the same traces "
+             "and on phased ones (popular experts redrawn every 256 steps)",
         L=40, H=64, I=64, E=256, k=8, T=1, shared=False, router="softmax", K=8, sweep=True,
         trace_steps=2048, caps=(0.05, 0.10, 0.25, 0.50),
-        ratios=((52700, 77300), (11800, 47500), (77300, 77300)), slots=2560, bp=52700, bh=77300),
+        ratios=((52700, 77300), (11800, 47500), (77300, 77300)), slots=2560, bp=52700, bh=77300,
+        phase_steps=256),
 }
 
 
@@ -869,6 +872,7 @@ def run_sweep(args, w, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    policies = policy_rows(m, spec, w, dev, plans, stats, base)
     if rank != 0:
         return
     hbm, _, peak_kind = peaks()
@@ -888,6 +892,7 @@ def run_sweep(args, w, rank, world, local_rank):
                      "kernel": "control step (one CTA, latency-bound)", "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": scan, "avg_launch_us": t_call * 1e6},
         "sweep": rows,
+        "policies": policies,
         "e2e": {"value": world * calls / (ms_e2e * 1e-3), "unit": "layer-steps/s",
                 "h2d_bytes_per_step": L * k * 4, "d2h_bytes_per_step": L * 32},
         "gpu_launches": calls,
@@ -896,6 +901,56 @@ def run_sweep(args, w, rank, world, local_rank):
     if world == 1 and not args.no_cpu:
         out["cpu_baseline"] = cpu_baseline_sweep(w, tr_h)
     print(json.dumps(out), flush=True)
+
+
+POLICIES = ("shared_lru", "layer_lru", "static_hot", "static_layers")
+
+
+def policy_rows(m, spec, w, dev, plans, stats, base):
+    """Miss rate of each replacement policy at each capacity, replayed on the
+    same traces (stationary Zipf, and the same recipe with the popular experts
+    redrawn every `phase_steps` steps) through moe_cache_step on the device:
+    shared LRU, per-layer LRU (floor(S/L) slots per layer), static hot set
+    (the S most routed pairs of the replayed trace, placed once) and static
+    whole layers.  B_P/B_H 52.7/77.3 GB/s for the LRU policies; the static
+    ones never fill.  Plain stream launches (not timed)."""
+    import torch
+
+    from moe_expert_offload_gb300 import placement, synth
+
+    L, E, k, K, n = w["L"], w["E"], w["k"], w["K"], w["trace_steps"]
+    sp = torch.cuda.current_stream().cuda_stream
+    kinds = {"shared_lru": m.POLICY_SHARED_LRU, "layer_lru": m.POLICY_LAYER_LRU}
+    sets = [("stationary", sweep_traces(w)),
+            (f"phased_{w['phase_steps']}", np.ascontiguousarray(np.stack(
+                [synth.zipf_trace(1000 + l, n, E, k, phase_steps=w["phase_steps"])
+                 for l in range(L)], axis=1)))]
+    out = []
+    for tname, tr_h in sets:
+        tr = torch.from_numpy(tr_h).to(dev)
+        ptr = tr.data_ptr()
+        for cap in w["caps"]:
+            S = int(round(cap * L * E))
+            for pol in POLICIES:
+                cache = m.DeviceCache(spec, S, K, 52700, 77300, bank=None, device=dev,
+                                      with_pool=False, policy=kinds.get(pol, m.POLICY_STATIC))
+                if pol == "static_hot":
+                    m.moe_cache_place(spec, cache.c, placement.hot_placement(tr_h, E, S), sp)
+                elif pol == "static_layers":
+                    m.moe_cache_place(spec, cache.c, placement.layer_placement(L, E, S), sp)
+                else:
+                    m.moe_cache_reset(spec, cache.c, sp)
+                for i in range(n * L):
+                    m.moe_cache_step(spec, cache.c, i % L, ptr + 4 * k * i, 1, plans[i], 0, sp)
+                torch.cuda.synchronize()
+                if int(base.err.cpu()[0]) != 0:
+                    raise RuntimeError("control step flagged an error in the policy replay")
+                st = stats.cpu().numpy().astype(np.int64)
+                out.append({"trace": tname, "capacity": cap, "slots": S, "policy": pol,
+                            "miss_rate": float(st[:, 2].sum() / max(st[:, 0].sum(), 1)),
+                            "mean_F": float(st[:, 4].mean()), "mean_C": float(st[:, 5].mean())})
+                del cache
+    return out
 
 
 def cpu_baseline_sweep(w, tr_h, budget_s=10.0):

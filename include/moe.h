@@ -12,6 +12,10 @@
  *                      method", "method steps", "novelty"; FreeToken reader
  *                      "Semantic-Aware Expert Caching", "Elastic Memory
  *                      Management")
+ *   moe_cache_place    setup: preload a chosen expert set (static placement
+ *                      or warm start); moe_cache.policy picks the shared LRU,
+ *                      a per-layer LRU or static placement (the replacement
+ *                      policies the pages compare)
  *   moe_expert_ffn     int4 affine group-64 SwiGLU experts down(silu(gate(x)) *
  *                      up(x)) over G = H u F (H from the slot pool; F, the
  *                      experts filled in this step, from their bank bytes,
@@ -31,7 +35,9 @@
  *   Streams  Every call is asynchronous on `stream` (a cudaStream_t; NULL is
  *            the legacy default stream).  No call synchronises the host, and
  *            all device-side sizes ("valid counts") live in device memory,
- *            so every call can be captured in a CUDA graph.
+ *            so every call can be captured in a CUDA graph.  The exceptions
+ *            are the setup-time calls moe_cache_place and
+ *            moe_profile_bandwidths, which synchronise `stream`.
  *   Errors   Every int-returning call returns MOE_OK or a negative code.
  *            Arguments are validated on the host before anything is launched;
  *            on failure nothing is launched and moe_last_error() describes the
@@ -93,6 +99,19 @@ typedef struct moe_spec {
   int32_t shared_inter; /* its intermediate size (must equal inter) */
 } moe_spec;
 
+/* Replacement policy of a slot cache (moe_cache.policy).  FreeToken's own
+ * policy is the shared LRU (summary "core method"); the other two are the
+ * placements its miss-rate comparison replays on the same routing traces
+ * (summary "Key results"; reader Figure 4(b)) and Edge0's per-layer "hot"
+ * resident set (Edge0 §3.1 "executor paths").
+ *   MOE_POLICY_SHARED_LRU  one LRU over all S slots, all layers
+ *   MOE_POLICY_LAYER_LRU   layer l owns slots [l*S_l, (l+1)*S_l) with
+ *                          S_l = floor(S / L) and runs its own LRU there;
+ *                          the S - L*S_l slots past the last range are unused
+ *   MOE_POLICY_STATIC      the slots hold what moe_cache_place put there; a
+ *                          step never fills (q = 0: every miss goes to C) */
+enum { MOE_POLICY_SHARED_LRU = 0, MOE_POLICY_LAYER_LRU = 1, MOE_POLICY_STATIC = 2 };
+
 /* The shared expert slot cache (FreeToken summary "core method": one pool
  * for all MoE layers, one slot per (layer, expert) pair).  The struct itself
  * lives on the host; the tables live on the device. */
@@ -107,6 +126,7 @@ typedef struct moe_cache {
   uint32_t* clock;     /* device [1]: step counter, advanced once per cache step */
   void* slot_pool;     /* device [S * S_e] bytes, 16-byte aligned */
   const void* bank;    /* device [L * E * S_e] bytes, 16-byte aligned */
+  int32_t policy;      /* MOE_POLICY_*; MOE_POLICY_LAYER_LRU needs S >= L */
 } moe_cache;
 
 /* Fixed-shape step buffers with device-side valid counts (FreeToken summary
@@ -168,6 +188,23 @@ int moe_route(const moe_spec* spec, const void* x, int32_t T, const void* w_rout
 int moe_cache_reset(const moe_spec* spec, moe_cache* cache, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * moe_cache_place -- empty the cache, then preload a chosen set of experts:
+ * the static placements of the pages' baselines (hot experts pinned at load
+ * time; whole layers assigned to the GPU), or a warm start for an LRU.
+ *   ids      HOST int32 [n]: bank ids l*E + e, distinct, in [0, L*E)
+ *   n        0 <= n; n <= S (policy LAYER_LRU: ids of one layer <= S_l)
+ * ids[i] goes to slot i (SHARED_LRU, STATIC) or, for LAYER_LRU, to slot
+ * l*S_l + (number of ids of layer l before it in the list); every other slot
+ * is emptied; ts = 0 everywhere (placed, not yet used); clock = 0.  When the
+ * cache has a slot pool and bank, each placed blob is copied bank -> slot.
+ * The list is checked on the host before anything is written (MOE_EINVAL
+ * leaves the cache untouched).  Synchronises `stream` before it returns
+ * (the tables are staged from host memory); not capturable.
+ * ------------------------------------------------------------------------ */
+int moe_cache_place(const moe_spec* spec, moe_cache* cache, const int32_t* ids, int32_t n,
+                    moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * moe_cache_step -- one decode control step for layer `layer` (one CTA),
  * then (do_fill != 0) the fill copies bank[F_i] -> slot_pool[victim_i].
  *   ids      device int32 [T][k]: routed expert indices of this layer
@@ -180,6 +217,8 @@ int moe_cache_reset(const moe_spec* spec, moe_cache* cache, moe_stream_t stream)
  *   of m*B_P/B_H); victims = the K smallest (ts, slot) over slots with
  *   ts != now, in one pass; n_fill = min(q, K, #victims); F = M[:n_fill] into
  *   victims[:n_fill] (old ids evicted, ts = now); C = M[n_fill:] (not cached).
+ * Policy: LAYER_LRU takes victims from layer's own slot range only; STATIC
+ *   sets q = 0 (victims are still listed, nothing is filled).
  * Requires T*k <= 1024 and T*k <= plan->capacity (else MOE_ECAPACITY).
  * With do_fill == 0 only the tables change (trace replay).
  * ------------------------------------------------------------------------ */

@@ -55,7 +55,11 @@ class MoeCache(C.Structure):
     _fields_ = [("num_slots", C.c_int32), ("k_victims", C.c_int32), ("bp_mbps", C.c_int32),
                 ("bh_mbps", C.c_int32), ("slot_of_id", C.c_void_p), ("id_of_slot", C.c_void_p),
                 ("ts", C.c_void_p), ("clock", C.c_void_p), ("slot_pool", C.c_void_p),
-                ("bank", C.c_void_p)]
+                ("bank", C.c_void_p), ("policy", C.c_int32)]
+
+
+# moe_cache.policy values (include/moe.h)
+POLICY_SHARED_LRU, POLICY_LAYER_LRU, POLICY_STATIC = 0, 1, 2
 
 
 class MoePlan(C.Structure):
@@ -89,6 +93,8 @@ def lib():
         L.moe_route.argtypes = [sp, vp, i32, vp, vp, vp, vp, vp, vp]
         L.moe_cache_reset.restype = C.c_int
         L.moe_cache_reset.argtypes = [sp, cp, vp]
+        L.moe_cache_place.restype = C.c_int
+        L.moe_cache_place.argtypes = [sp, cp, vp, i32, vp]
         L.moe_cache_step.restype = C.c_int
         L.moe_cache_step.argtypes = [sp, cp, i32, vp, i32, pp, i32, vp]
         L.moe_ffn_workspace_bytes.restype = sz
@@ -164,6 +170,16 @@ def moe_route(spec, x, T, w_router, bias, logits, ids, weights, stream=None):
 
 def moe_cache_reset(spec, cache, stream=None):
     return _check(lib().moe_cache_reset(C.byref(spec), C.byref(cache), _stream(stream)))
+
+
+def moe_cache_place(spec, cache, ids, stream=None):
+    """Preload the bank ids `ids` (host sequence of l*E + e) into the cache."""
+    import numpy as np
+
+    a = np.ascontiguousarray(np.asarray(ids, dtype=np.int32).reshape(-1))
+    return _check(lib().moe_cache_place(C.byref(spec), C.byref(cache),
+                                        a.ctypes.data if a.size else None, int(a.size),
+                                        _stream(stream)))
 
 
 def moe_cache_step(spec, cache, layer, ids, T, plan, do_fill=1, stream=None):
@@ -256,7 +272,7 @@ class DeviceCache:
     """Slot tables and slot pool in device memory (torch tensors) + the C struct."""
 
     def __init__(self, spec: MoeSpec, num_slots, k_victims, bp_mbps, bh_mbps, bank, device="cuda",
-                 with_pool=True):
+                 with_pool=True, policy=POLICY_SHARED_LRU):
         import torch
 
         n_ids = spec.num_layers * spec.num_experts
@@ -270,7 +286,7 @@ class DeviceCache:
         self.bank = bank
         self.c = MoeCache(num_slots, k_victims, bp_mbps, bh_mbps, _ptr(self.slot_of_id),
                           _ptr(self.id_of_slot), _ptr(self.ts), _ptr(self.clock),
-                          _ptr(self.pool), _ptr(bank))
+                          _ptr(self.pool), _ptr(bank), policy)
 
     def host_tables(self):
         import numpy as np

@@ -5,6 +5,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <vector>
+
 #include "moe_internal.cuh"
 
 namespace {
@@ -68,12 +70,16 @@ int check_cache(const moe_spec* s, const moe_cache* c, bool need_data) {
   if (c->bp_mbps <= 0 || c->bh_mbps <= 0) return fail(MOE_EINVAL, "bandwidths must be > 0");
   if (!c->slot_of_id || !c->id_of_slot || !c->ts || !c->clock)
     return fail(MOE_EINVAL, "cache table pointer is NULL");
+  if (c->policy < MOE_POLICY_SHARED_LRU || c->policy > MOE_POLICY_STATIC)
+    return fail(MOE_EINVAL, "unknown cache policy %d", c->policy);
+  if (c->policy == MOE_POLICY_LAYER_LRU && c->num_slots < s->num_layers)
+    return fail(MOE_EINVAL, "the per-layer LRU needs num_slots >= num_layers (%d < %d)",
+                c->num_slots, s->num_layers);
   if (need_data) {
     if (!c->slot_pool || !c->bank) return fail(MOE_EINVAL, "slot_pool / bank is NULL");
     if (!aligned(c->slot_pool, 16) || !aligned(c->bank, 16))
       return fail(MOE_EINVAL, "slot_pool / bank must be 16-byte aligned");
   }
-  (void)s;
   return MOE_OK;
 }
 
@@ -108,7 +114,11 @@ moe::CacheArgs cache_args(const moe_spec* spec, moe_cache* c, int32_t layer, con
   a.E = spec->num_experts;
   a.layer = layer;
   a.n_ids = T * spec->top_k;
-  a.S = c->num_slots;
+  // per-layer LRU: layer's own range of floor(S / L) slots; else all S slots
+  const bool per_layer = c->policy == MOE_POLICY_LAYER_LRU;
+  a.S = per_layer ? c->num_slots / spec->num_layers : c->num_slots;
+  a.S0 = per_layer ? layer * a.S : 0;
+  a.no_fill = c->policy == MOE_POLICY_STATIC;
   a.K = c->k_victims;
   a.bp = c->bp_mbps;
   a.bh = c->bh_mbps;
@@ -123,20 +133,7 @@ moe::CacheArgs cache_args(const moe_spec* spec, moe_cache* c, int32_t layer, con
 
 int do_cache_step(const moe_spec* spec, moe_cache* c, int32_t layer, const int32_t* ids,
                   int32_t T, moe_plan* plan, int32_t do_fill, cudaStream_t st) {
-  moe::CacheArgs a;
-  a.E = spec->num_experts;
-  a.layer = layer;
-  a.n_ids = T * spec->top_k;
-  a.S = c->num_slots;
-  a.K = c->k_victims;
-  a.bp = c->bp_mbps;
-  a.bh = c->bh_mbps;
-  a.ids = ids;
-  a.slot_of_id = c->slot_of_id;
-  a.id_of_slot = c->id_of_slot;
-  a.ts = c->ts;
-  a.clock = c->clock;
-  a.plan = *plan;
+  const moe::CacheArgs a = cache_args(spec, c, layer, ids, T, plan);
   cudaError_t e = moe::launch_cache_step(a, st);
   if (e != cudaSuccess) return cuda_fail(e, "cache step launch");
   if (do_fill) {
@@ -268,6 +265,55 @@ int moe_cache_reset(const moe_spec* spec, moe_cache* cache, moe_stream_t stream)
                                           cache->id_of_slot, cache->ts, cache->num_slots,
                                           cache->clock, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "cache reset launch");
+  return ok();
+}
+
+int moe_cache_place(const moe_spec* spec, moe_cache* cache, const int32_t* ids, int32_t n,
+                    moe_stream_t stream) {
+  int rc = check_spec(spec);
+  if (rc) return rc;
+  rc = check_cache(spec, cache, false);
+  if (rc) return rc;
+  if (n < 0 || (n > 0 && !ids)) return fail(MOE_EINVAL, "moe_cache_place: bad id list");
+  const int L = spec->num_layers, E = spec->num_experts, S = cache->num_slots;
+  const int64_t n_ids = (int64_t)L * E;
+  const bool per_layer = cache->policy == MOE_POLICY_LAYER_LRU;
+  const int range = per_layer ? S / L : S;  // slots one layer (or all of them) may use
+  std::vector<int32_t> slot_of_id((size_t)n_ids, -1), id_of_slot((size_t)S, -1);
+  std::vector<int32_t> used(per_layer ? L : 1, 0);
+  // the whole list is checked before anything on the device is written
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t u = ids[i];
+    if (u < 0 || u >= n_ids)
+      return fail(MOE_EINVAL, "moe_cache_place: id %d outside [0, L*E)", u);
+    if (slot_of_id[(size_t)u] >= 0) return fail(MOE_EINVAL, "moe_cache_place: id %d repeated", u);
+    const int l = per_layer ? u / E : 0;
+    if (used[l] >= range)
+      return fail(MOE_EINVAL, "moe_cache_place: more ids than the %d slots %s", range,
+                  per_layer ? "of one layer" : "of the cache");
+    const int32_t v = l * range + used[l]++;
+    slot_of_id[(size_t)u] = v;
+    id_of_slot[(size_t)v] = u;
+  }
+  const cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(cache->slot_of_id, slot_of_id.data(),
+                                  (size_t)n_ids * sizeof(int32_t), cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(cache->id_of_slot, id_of_slot.data(), (size_t)S * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(cache->ts, 0, (size_t)S * sizeof(uint32_t), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(cache->clock, 0, sizeof(uint32_t), st);
+  if (cache->slot_pool && cache->bank) {
+    const int64_t blob = moe::blob_offsets(spec->hidden, spec->inter).total;
+    for (int32_t i = 0; i < n && e == cudaSuccess; ++i) {
+      const int32_t u = ids[i];
+      e = cudaMemcpyAsync(static_cast<uint8_t*>(cache->slot_pool) + slot_of_id[(size_t)u] * blob,
+                          static_cast<const uint8_t*>(cache->bank) + (int64_t)u * blob,
+                          (size_t)blob, cudaMemcpyDeviceToDevice, st);
+    }
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);  // the host tables die on return
+  if (e != cudaSuccess) return cuda_fail(e, "moe_cache_place");
   return ok();
 }
 

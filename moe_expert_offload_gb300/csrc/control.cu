@@ -50,7 +50,8 @@ __device__ __forceinline__ void insert_key(unsigned long long (&best)[KMAX],
 template <int KMAX, int NE>
 __device__ __forceinline__ void warp_k_smallest(unsigned long long (&best)[KMAX], int K,
                                                 unsigned long long* out, int32_t* out_id,
-                                                const int32_t (&early_id)[NE > 0 ? NE : 1]) {
+                                                const int32_t (&early_id)[NE > 0 ? NE : 1],
+                                                int s0) {
   const int lane = threadIdx.x & 31;
   for (int r = 0; r < K; ++r) {
     const uint32_t hi = (uint32_t)(best[0] >> 32), lo = (uint32_t)best[0];
@@ -61,7 +62,7 @@ __device__ __forceinline__ void warp_k_smallest(unsigned long long (&best)[KMAX]
       int32_t id = -2;
 #pragma unroll
       for (int j = 0; j < NE; ++j)
-        if ((int)mlo == (int)threadIdx.x + j * kCtlThreads) id = early_id[j];
+        if ((int)mlo == s0 + (int)threadIdx.x + j * kCtlThreads) id = early_id[j];
       out_id[r] = id;
 #pragma unroll
       for (int j = 0; j < KMAX - 1; ++j) best[j] = best[j + 1];
@@ -101,8 +102,8 @@ __global__ void __launch_bounds__(kCtlThreads) cache_step_kernel(CacheArgs a, Se
 #pragma unroll
   for (int j = 0; j < NE; ++j) {
     const int v = tid + j * kCtlThreads;
-    early[j] = v < a.S ? a.ts[v] : 0u;
-    early_id[j] = v < a.S ? a.id_of_slot[v] : -1;
+    early[j] = v < a.S ? a.ts[a.S0 + v] : 0u;
+    early_id[j] = v < a.S ? a.id_of_slot[a.S0 + v] : -1;
   }
   if constexpr (SEL) {
     // the router's selection for the step's tokens, one warp per token; the
@@ -170,7 +171,8 @@ __global__ void __launch_bounds__(kCtlThreads) cache_step_kernel(CacheArgs a, Se
         a.plan.hit_ids[p] = u;
         a.plan.hit_slots[p] = slot;
         a.ts[slot] = now;  // recency moves only when the router selects the expert
-        if (slot < kEarlySlots) atomicOr(&shit[slot >> 5], 1u << (slot & 31));
+        const unsigned r = (unsigned)(slot - a.S0);  // the slot's place in the scanned range
+        if (r < (unsigned)kEarlySlots) atomicOr(&shit[r >> 5], 1u << (r & 31));
       }
       if (miss) smiss[__popc(mb & lanemask_lt())] = u;
       if (lane == 0) {
@@ -244,7 +246,8 @@ __global__ void __launch_bounds__(kCtlThreads) cache_step_kernel(CacheArgs a, Se
         a.plan.hit_ids[p] = u;
         a.plan.hit_slots[p] = slot;
         a.ts[slot] = now;  // recency moves only when the router selects the expert
-        if (slot < kEarlySlots) atomicOr(&shit[slot >> 5], 1u << (slot & 31));
+        const unsigned r = (unsigned)(slot - a.S0);  // the slot's place in the scanned range
+        if (r < (unsigned)kEarlySlots) atomicOr(&shit[r >> 5], 1u << (r & 31));
       }
       if (miss) smiss[om + __popc(mb & lanemask_lt())] = u;
       base_h += th;
@@ -257,7 +260,7 @@ __global__ void __launch_bounds__(kCtlThreads) cache_step_kernel(CacheArgs a, Se
 
   // q = round half up of m * B_P / B_H; pure fill when B_H <= B_P
   int q;
-  if (m <= 0) {
+  if (m <= 0 || a.no_fill) {
     q = 0;
   } else if (a.bh <= a.bp) {
     q = m;
@@ -275,13 +278,14 @@ __global__ void __launch_bounds__(kCtlThreads) cache_step_kernel(CacheArgs a, Se
   for (int j = 0; j < NE; ++j) {
     const int v = tid + j * kCtlThreads;
     if (v < a.S && !(shit[v >> 5] >> (v & 31) & 1u))
-      insert_key<KMAX>(best, ((unsigned long long)early[j] << 32) | (uint32_t)v);
+      insert_key<KMAX>(best, ((unsigned long long)early[j] << 32) | (uint32_t)(a.S0 + v));
   }
   for (int v = tid + NE * kCtlThreads; v < a.S; v += kCtlThreads) {  // read after the hit updates
-    const uint32_t t = a.ts[v];
-    if (t != now) insert_key<KMAX>(best, ((unsigned long long)t << 32) | (uint32_t)v);
+    const uint32_t t = a.ts[a.S0 + v];
+    if (t != now) insert_key<KMAX>(best, ((unsigned long long)t << 32) | (uint32_t)(a.S0 + v));
   }
-  warp_k_smallest<KMAX, NE>(best, K, &scand[wid * KMAX], &scand_id[wid * KMAX], early_id);
+  warp_k_smallest<KMAX, NE>(best, K, &scand[wid * KMAX], &scand_id[wid * KMAX], early_id,
+                              a.S0);
   __syncthreads();
   if (wid == 0) {
     // merge the warps' ascending lists: lane w < kCtlWarps holds the head of

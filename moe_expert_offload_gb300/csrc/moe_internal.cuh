@@ -78,8 +78,11 @@ cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* w, int T, in
 cudaError_t launch_router_select(const moe_spec& sp, const float* logits, const float* bias,
                                  int T, int32_t* ids, float* weights, cudaStream_t st);
 
+// The victim scan covers slots [S0, S0 + S): all S slots of the pool for the
+// shared LRU and static placement, layer's own range for the per-layer LRU.
+// no_fill (static placement) makes q = 0.
 struct CacheArgs {
-  int E, layer, n_ids, S, K, bp, bh;
+  int E, layer, n_ids, S0, S, K, bp, bh, no_fill;
   const int32_t* ids;
   int32_t *slot_of_id, *id_of_slot;
   uint32_t *ts, *clock;

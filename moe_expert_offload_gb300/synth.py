@@ -198,22 +198,29 @@ def prefill_hidden(seed: int, T: int, H: int, w_router_bits: np.ndarray, boost: 
 
 
 def zipf_trace(seed: int, steps: int, E: int, k: int, alpha: float = 1.1,
-               overlap: float = 0.7) -> np.ndarray:
+               overlap: float = 0.7, phase_steps: int | None = None) -> np.ndarray:
     """Synthetic routing trace int32 [steps][k] of distinct expert ids.
 
     Expert popularity is Zipf(alpha) over a random permutation of the experts.
     Step t keeps each of step t-1's experts with probability `overlap`, then
     tops up to k distinct experts with popularity-weighted draws without
-    replacement.
+    replacement.  With `phase_steps`, a new permutation is drawn every
+    `phase_steps` steps (a change of task or workload phase: the popular
+    experts change, the popularity curve does not).
     """
     rng = np.random.default_rng(seed)
-    perm = rng.permutation(E)
     p_rank = 1.0 / np.arange(1, E + 1) ** alpha
     pop = np.empty(E)
-    pop[perm] = p_rank / p_rank.sum()
+
+    def draw_popularity():
+        pop[rng.permutation(E)] = p_rank / p_rank.sum()
+
+    draw_popularity()
     out = np.empty((steps, k), dtype=np.int32)
     prev: list[int] = []
     for t in range(steps):
+        if phase_steps and t and t % phase_steps == 0:
+            draw_popularity()
         keep = [e for e in prev if rng.random() < overlap]
         chosen = list(keep)
         avail = np.ones(E, dtype=bool)

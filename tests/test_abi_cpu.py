@@ -106,7 +106,8 @@ def _plan(cap=2):
     (dict(num_slots=0), m.MOE_EINVAL), (dict(k_victims=0), m.MOE_EINVAL),
     (dict(k_victims=33), m.MOE_EINVAL), (dict(bp_mbps=0), m.MOE_EINVAL),
     (dict(ts=None), m.MOE_EINVAL), (dict(bank=None), m.MOE_EINVAL),
-    (dict(slot_pool=4100), m.MOE_EINVAL),
+    (dict(slot_pool=4100), m.MOE_EINVAL), (dict(policy=3), m.MOE_EINVAL),
+    (dict(policy=-1), m.MOE_EINVAL), (dict(policy=m.POLICY_LAYER_LRU, num_slots=1), m.MOE_EINVAL),
 ])
 def test_cache_step_rejects_bad_cache(L, kw, code):
     with pytest.raises(m.MoeError) as e:
@@ -130,6 +131,25 @@ def test_cache_step_rejects_bad_layer_and_capacity(L):
         m.moe_cache_step(_spec(), _cache(), 0, 64, 1, p, 1, stream=0)
     assert e.value.code == m.MOE_EINVAL
     assert m.moe_cache_step(_spec(), _cache(), 0, 64, 0, _plan(), 1, stream=0) == m.MOE_OK
+
+
+def test_cache_place_argument_checks(L):
+    # every rejection happens on the host before any device write
+    sp = _spec()
+    E, nl = sp.num_experts, sp.num_layers
+    bad = [([3, 3], m.POLICY_SHARED_LRU), ([nl * E], m.POLICY_SHARED_LRU),
+           ([-1], m.POLICY_STATIC), (list(range(9)), m.POLICY_SHARED_LRU),
+           ([0, 1, 2, 3, 4], m.POLICY_LAYER_LRU)]  # dup, range, range, > S, > S_l = 4
+    for ids, pol in bad:
+        with pytest.raises(m.MoeError) as e:
+            m.moe_cache_place(sp, _cache(policy=pol), ids, stream=0)
+        assert e.value.code == m.MOE_EINVAL, (ids, pol)
+    with pytest.raises(m.MoeError) as e:
+        m.moe_cache_place(sp, _cache(policy=5), [1], stream=0)
+    assert e.value.code == m.MOE_EINVAL
+    with pytest.raises(m.MoeError) as e:
+        m._check(L.moe_cache_place(C.byref(sp), C.byref(_cache()), None, 2, None))
+    assert e.value.code == m.MOE_EINVAL
 
 
 def test_ffn_argument_checks(L):
@@ -205,3 +225,29 @@ def test_profile_argument_checks(L):
     with pytest.raises(m.MoeError) as e:  # misaligned workspace
         m.moe_profile_bandwidths(s, _cache(), 0, 4100, need, reps=2, stream=0)
     assert e.value.code == m.MOE_EINVAL
+
+
+def test_hot_placement_is_best_fixed_set():
+    """hot_placement against brute force: on tiny traces no other set of S ids
+    collects more static hits, and its order is count-descending, id-ascending."""
+    import itertools
+
+    import numpy as np
+
+    from moe_expert_offload_gb300 import placement
+
+    rng = np.random.default_rng(3)
+    L, E, k = 2, 5, 2
+    tr = np.stack([[rng.choice(E, size=k, replace=False) for _ in range(L)]
+                   for _ in range(30)]).astype(np.int32)
+    hits = lambda P: sum(int(l * E + e in P) for t in range(30) for l in range(L)
+                         for e in set(tr[t, l].tolist()))
+    for S in (1, 3, 6):
+        got = placement.hot_placement(tr, E, S)
+        best = max(hits(set(c)) for c in itertools.combinations(range(L * E), S))
+        assert len(got) == S and hits(set(got.tolist())) == best
+        cnt = [sum(int(u % E in tr[t, u // E]) for t in range(30)) for u in got]
+        assert all((cnt[i], -got[i]) >= (cnt[i + 1], -got[i + 1]) for i in range(S - 1))
+    assert list(placement.layer_placement(3, 4, 9)) == list(range(8))
+    assert list(placement.layer_placement(3, 4, 100)) == list(range(12))
+    assert placement.layer_placement(3, 4, 3).size == 0

@@ -216,6 +216,98 @@ def test_cache_step_flags_bad_ids(oracle):
     _plans_equal(gp, op, K)
 
 
+# ------------------------------------------------------- replacement policies
+def _placement(rng, policy, L, E, S):
+    """A random warm-start / static set in shuffled order (at most S_l per layer)."""
+    if policy == m.POLICY_LAYER_LRU:
+        Sl = S // L
+        ids = [l * E + int(e) for l in range(L)
+               for e in rng.choice(E, size=int(rng.integers(0, min(Sl, E) + 1)), replace=False)]
+    else:
+        ids = [int(u) for u in rng.choice(L * E, size=min(S, L * E) - 1, replace=False)]
+    rng.shuffle(ids)
+    return np.array(ids, np.int32)
+
+
+@pytest.mark.parametrize("policy,L,E,S,K,T,k,steps", [
+    (m.POLICY_LAYER_LRU, 3, 16, 14, 3, 2, 2, 40),       # S_l = 4; slots 12, 13 unused
+    (m.POLICY_LAYER_LRU, 40, 256, 5120, 8, 1, 8, 3),    # ranges past the early-loaded slots
+    (m.POLICY_LAYER_LRU, 2, 64, 90, 20, 2, 8, 30),      # K > 16: the long victim lists
+    (m.POLICY_LAYER_LRU, 4, 16, 4, 1, 1, 2, 20),        # one slot per layer
+    (m.POLICY_STATIC, 3, 16, 20, 4, 2, 3, 30),
+    (m.POLICY_STATIC, 40, 256, 2560, 8, 1, 8, 3),
+])
+def test_cache_policies_match_oracle(oracle, policy, L, E, S, K, T, k, steps):
+    """Per-layer LRU and static placement: plans and tables equal the oracle's after a
+    placement and over random multi-layer traces (layers in random order)."""
+    rng = np.random.default_rng(S + 7 * K + policy)
+    spec = m.make_spec(L, 64, 64, E, k)
+    cache = m.DeviceCache(spec, S, K, 52700, 77300, bank=None, device=DEV, with_pool=False,
+                          policy=policy)
+    plan = m.DevicePlan(T * k, K, device=DEV)
+    ost = oracle.CacheState(L * E, S)
+    placed = _placement(rng, policy, L, E, S)
+    m.moe_cache_place(spec, cache.c, placed)
+    oracle.cache_place(ost, E, L, placed, policy=policy)
+    _tables_equal(cache, ost)
+    for it in range(steps * L):
+        layer = int(rng.integers(L))
+        ids_h = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+        m.moe_cache_step(spec, cache.c, layer, dev(ids_h, DEV), T, plan.c, do_fill=0)
+        torch.cuda.synchronize()
+        op = oracle.cache_step(ost, E, layer, ids_h, K, 52700, 77300, policy=policy, L=L)
+        _plans_equal(plan.read(K), op, K)
+        if it % 16 == 0:
+            _tables_equal(cache, ost)
+    _tables_equal(cache, ost)
+
+
+@pytest.mark.parametrize("policy", [m.POLICY_LAYER_LRU, m.POLICY_STATIC])
+def test_layer_forward_under_policies(oracle, policy):
+    """Whole decode layer step under each policy: routing, plans and FFN output equal the
+    oracle's, and every resident slot holds its expert's bank blob (placement copies and
+    per-layer fills)."""
+    L, H, I, E, k, S, K, T = 2, 256, 128, 16, 2, 7, 2, 2   # per-layer: S_l = 3, slot 6 unused
+    spec, bank, bank_h, cache, _ = _layer_rig(L, H, I, E, k, S, K, 52700, 77300, False, seed=9)
+    cache.c.policy = policy
+    rng = np.random.default_rng(policy)
+    placed = _placement(rng, policy, L, E, S)
+    m.moe_cache_place(spec, cache.c, placed)
+    ost = oracle.CacheState(L * E, S)
+    oracle.cache_place(ost, E, L, placed, policy=policy)
+    pool = cache.pool.cpu().numpy()
+    for slot, eid in enumerate(ost.id_of_slot):
+        if eid >= 0:
+            assert np.array_equal(pool[slot], bank_h[eid])
+    plan = m.DevicePlan(T * k, K, device=DEV)
+    wsb = m.moe_layer_workspace_bytes(spec, T)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    wts = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    y = torch.empty((T, H), dtype=torch.float32, device=DEV)
+    hits = 0
+    for step in range(12):
+        layer = step % L
+        wr_h = synth.router_weights(30 + layer, E, H)
+        xb = synth.bf16_bits(rng.normal(0, 1.5, (T, H)))
+        m.moe_layer_forward(spec, cache.c, layer, dev_bits(xb, DEV), T, dev_bits(wr_h, DEV), None,
+                            None, plan.c, ids, wts, ws, wsb, y)
+        torch.cuda.synchronize()
+        oid, ow = oracle.route_softmax_topk(oracle.router_logits(xb, wr_h), k)
+        assert np.array_equal(ids.cpu().numpy(), oid)
+        op = oracle.cache_step(ost, E, layer, oid, K, 52700, 77300, policy=policy, L=L)
+        _plans_equal(plan.read(K), op, K)
+        hits += op["n_hit"]
+        ref = oracle.moe_ffn(list(bank_h[layer * E:(layer + 1) * E]), H, I, xb, oid, ow)
+        assert_ffn_close(y.cpu().numpy(), ref, f"policy {policy} step {step}")
+    _tables_equal(cache, ost)
+    pool = cache.pool.cpu().numpy()
+    for slot, eid in enumerate(ost.id_of_slot):
+        if eid >= 0:
+            assert np.array_equal(pool[slot], bank_h[eid])
+    assert hits > 0
+
+
 # ------------------------------------------------------- fill + expert FFN
 def _layer_rig(L, H, I, E, k, S, K, bp, bh, has_shared, seed=0, big=False):
     spec = m.make_spec(L, H, I, E, k, has_shared=has_shared)
