@@ -50,8 +50,7 @@ __device__ __forceinline__ void insert_key(unsigned long long (&best)[KMAX],
 template <int KMAX, int NE>
 __device__ __forceinline__ void warp_k_smallest(unsigned long long (&best)[KMAX], int K,
                                                 unsigned long long* out, int32_t* out_id,
-                                                const int32_t (&early_id)[NE > 0 ? NE : 1],
-                                                int s0) {
+                                                const int32_t (&early_id)[NE > 0 ? NE : 1]) {
   const int lane = threadIdx.x & 31;
   for (int r = 0; r < K; ++r) {
     const uint32_t hi = (uint32_t)(best[0] >> 32), lo = (uint32_t)best[0];
@@ -62,7 +61,7 @@ __device__ __forceinline__ void warp_k_smallest(unsigned long long (&best)[KMAX]
       int32_t id = -2;
 #pragma unroll
       for (int j = 0; j < NE; ++j)
-        if ((int)mlo == s0 + (int)threadIdx.x + j * kCtlThreads) id = early_id[j];
+        if ((int)mlo == (int)threadIdx.x + j * kCtlThreads) id = early_id[j];
       out_id[r] = id;
 #pragma unroll
       for (int j = 0; j < KMAX - 1; ++j) best[j] = best[j + 1];
@@ -97,6 +96,8 @@ __global__ void __launch_bounds__(kCtlThreads) cache_step_kernel(CacheArgs a, Se
   // the slots hit this step are left out through a bitmap (their stamps
   // become `now`, which the scan excludes).
   constexpr int NE = KMAX <= 16 ? kEarlyTs : 0;  // (the K <= 32 list needs the registers)
+  // keys hold the slot's place v in the scanned range [S0, S0 + S); the
+  // victims written out are S0 + v (the order of (ts, v) and (ts, slot) agree)
   uint32_t early[NE > 0 ? NE : 1];
   int32_t early_id[NE > 0 ? NE : 1];  // the same slots' ids: a victim's is read from here
 #pragma unroll
@@ -278,14 +279,14 @@ __global__ void __launch_bounds__(kCtlThreads) cache_step_kernel(CacheArgs a, Se
   for (int j = 0; j < NE; ++j) {
     const int v = tid + j * kCtlThreads;
     if (v < a.S && !(shit[v >> 5] >> (v & 31) & 1u))
-      insert_key<KMAX>(best, ((unsigned long long)early[j] << 32) | (uint32_t)(a.S0 + v));
+      insert_key<KMAX>(best, ((unsigned long long)early[j] << 32) | (uint32_t)v);
   }
+  const uint32_t* ts_r = a.ts + a.S0;
   for (int v = tid + NE * kCtlThreads; v < a.S; v += kCtlThreads) {  // read after the hit updates
-    const uint32_t t = a.ts[a.S0 + v];
-    if (t != now) insert_key<KMAX>(best, ((unsigned long long)t << 32) | (uint32_t)(a.S0 + v));
+    const uint32_t t = ts_r[v];
+    if (t != now) insert_key<KMAX>(best, ((unsigned long long)t << 32) | (uint32_t)v);
   }
-  warp_k_smallest<KMAX, NE>(best, K, &scand[wid * KMAX], &scand_id[wid * KMAX], early_id,
-                              a.S0);
+  warp_k_smallest<KMAX, NE>(best, K, &scand[wid * KMAX], &scand_id[wid * KMAX], early_id);
   __syncthreads();
   if (wid == 0) {
     // merge the warps' ascending lists: lane w < kCtlWarps holds the head of
@@ -312,9 +313,9 @@ __global__ void __launch_bounds__(kCtlThreads) cache_step_kernel(CacheArgs a, Se
   const int n_fill = min(q, nv);
 
   for (int i = tid; i < K; i += kCtlThreads)
-    a.plan.victims[i] = (i < nv) ? (int32_t)(svict[i] & 0xffffffffu) : -1;
+    a.plan.victims[i] = (i < nv) ? a.S0 + (int32_t)(svict[i] & 0xffffffffu) : -1;
   if (tid < n_fill) {
-    const int32_t v = (int32_t)(svict[tid] & 0xffffffffu);
+    const int32_t v = a.S0 + (int32_t)(svict[tid] & 0xffffffffu);
     const int32_t f = smiss[tid];
     const int32_t known = sold[tid];  // -2: the slot's id was not prefetched
     const int32_t old = known != -2 ? known : a.id_of_slot[v];
