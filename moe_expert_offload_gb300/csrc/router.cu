@@ -63,95 +63,112 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const uint16_t* __re
 }
 
 // Tiled logits for many tokens, same order as router_logits_kernel: CTA =
-// 16 tokens x 16 experts, 8 warps of 4 tokens x 8 experts.  H goes through
-// shared memory in 256-column slices; in slice s lane j owns chunk 32 s + j,
-// so each lane still accumulates chunks j, j+32, ... in ascending order with
-// fma from 0.  The 32 sums of a lane are then combined by a reduce-scatter
-// over the same xor partners 16, 8, 4, 2, 1 (each add pairs the same two
-// lane partials as the butterfly, and fp addition is commutative, so every
-// logit is bit-identical); lane j ends with pair j.  Needs H % 256 == 0.
-constexpr int kTileTok = 16, kTileExp = 16;
+// 32 tokens x 16 experts, 8 warps of 8 tokens x 8 experts.  H goes through
+// shared memory in 256-column slices (cp.async into a ring of kTileStages
+// slices, kTileStages - 1 of them in flight while one is used); in
+// slice s lane j owns chunk 32 s + j, so each lane still accumulates chunks
+// j, j+32, ... in ascending order with fma from 0.  A lane holds its chunk of
+// the warp's 8 expert rows widened to fp32 and streams the 8 token rows
+// through them: 64 partial sums per lane.  These are combined by a
+// reduce-scatter over the same xor partners 16, 8, 4, 2, 1 (each add pairs
+// the same two lane partials as the butterfly, and fp addition is
+// commutative, so every logit is bit-identical), separately for pairs 0..31
+// and 32..63; lane j ends with pairs j and 32 + j.  Needs H % 256 == 0.
+constexpr int kTileTok = 32, kTileExp = 16, kTileMinT = 16, kTileStages = 4;
+constexpr int kTileRows = kTileTok + kTileExp;                          // rows per slice
+constexpr size_t kTileSmem = (size_t)kTileStages * kTileRows * 32 * 16;  // 96 KB
 
-__global__ void __launch_bounds__(256) router_logits_tiled_kernel(const uint16_t* __restrict__ x,
-                                                                  const uint16_t* __restrict__ w,
-                                                                  int T, int E, int H,
-                                                                  float* __restrict__ logits) {
-  __shared__ __align__(16) uint4 xs[kTileTok][32];  // 16 rows x 256 bf16
+__device__ __forceinline__ void cp16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(256, 1) router_logits_tiled_kernel(const uint16_t* __restrict__ x,
+                                                                     const uint16_t* __restrict__ w,
+                                                                     int T, int E, int H,
+                                                                     float* __restrict__ logits) {
+  // ring of slices: 32 token rows then 16 expert rows of 256 bf16 (32 x 16 B) each
+  extern __shared__ __align__(16) uint4 ring[];  // [kTileStages][kTileRows][32]
   griddep_launch();
   griddep_wait();
-  __shared__ __align__(16) uint4 ws[kTileExp][32];
   const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
   const int t0 = blockIdx.x * kTileTok, e0 = blockIdx.y * kTileExp;
-  const int tw = (wid >> 1) * 4, ew = (wid & 1) * 8;
-  float acc[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
-  // staging: 32 rows (16 x, 16 W) x 32 chunks = 1024 uint4, 4 per thread
-  uint4 nx[4];
-  auto fetch = [&](int s) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int i = tid + 256 * j, row = i >> 5, c = i & 31;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (row < kTileTok) {
-        if (t0 + row < T)
-          v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + row) * H + s * 256) + c);
-      } else if (e0 + row - kTileTok < E) {
-        v = __ldg(reinterpret_cast<const uint4*>(w + (size_t)(e0 + row - kTileTok) * H +
-                                                 s * 256) + c);
-      }
-      nx[j] = v;
-    }
-  };
+  const int tw = (wid >> 1) * 8, ew = (wid & 1) * 8;
   const int ns = H / 256;
-  fetch(0);
+  // slice s into ring slot s % kTileStages: 48 rows x 32 chunks = 1536 16-byte
+  // copies, 6 per thread; rows past T or E are zero-filled (source size 0,
+  // address kept in bounds).  A group is committed even when s >= ns, so the
+  // wait below always counts kTileStages - 1 groups.
+  auto issue = [&](int s) {
+    if (s < ns) {
+      uint4* slot = ring + (size_t)(s % kTileStages) * kTileRows * 32;
+#pragma unroll
+      for (int j = 0; j < 6; ++j) {
+        const int i = tid + 256 * j, row = i >> 5, c = i & 31;
+        const bool ok = row < kTileTok ? t0 + row < T : e0 + row - kTileTok < E;
+        const size_t grow = row < kTileTok ? (size_t)(t0 + row) : (size_t)(e0 + row - kTileTok);
+        const uint16_t* base = row < kTileTok ? x : w;
+        const uint16_t* src = base + (ok ? grow * H + (size_t)s * 256 + c * 8 : 0);
+        cp16((uint32_t)__cvta_generic_to_shared(slot + row * 32 + c), src, ok);
+      }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  float acc[64];
+#pragma unroll
+  for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+#pragma unroll
+  for (int s = 0; s < kTileStages - 1; ++s) issue(s);
   for (int s = 0; s < ns; ++s) {
+    issue(s + kTileStages - 1);  // into the slot freed at the end of slice s - 1
+    asm volatile("cp.async.wait_group %0;" ::"n"(kTileStages - 1) : "memory");
     __syncthreads();
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int i = tid + 256 * j, row = i >> 5, c = i & 31;
-      if (row < kTileTok)
-        xs[row][c] = nx[j];
-      else
-        ws[row - kTileTok][c] = nx[j];
-    }
-    __syncthreads();
-    if (s + 1 < ns) fetch(s + 1);
-    // widen once per slice (x) and once per expert row (W), not per product
-    float xf[4][8];
-#pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      const uint4 v = xs[tw + a][lane];
-      xf[a][0] = bf_lo(v.x); xf[a][1] = bf_hi(v.x); xf[a][2] = bf_lo(v.y); xf[a][3] = bf_hi(v.y);
-      xf[a][4] = bf_lo(v.z); xf[a][5] = bf_hi(v.z); xf[a][6] = bf_lo(v.w); xf[a][7] = bf_hi(v.w);
-    }
+    const uint4* xs = ring + (size_t)(s % kTileStages) * kTileRows * 32;
+    const uint4* ws = xs + kTileTok * 32;
+    float wf[8][8];
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
-      const uint4 v = ws[ew + b][lane];
-      const float wf[8] = {bf_lo(v.x), bf_hi(v.x), bf_lo(v.y), bf_hi(v.y),
+      const uint4 v = ws[(ew + b) * 32 + lane];
+      wf[b][0] = bf_lo(v.x); wf[b][1] = bf_hi(v.x); wf[b][2] = bf_lo(v.y); wf[b][3] = bf_hi(v.y);
+      wf[b][4] = bf_lo(v.z); wf[b][5] = bf_hi(v.z); wf[b][6] = bf_lo(v.w); wf[b][7] = bf_hi(v.w);
+    }
+#pragma unroll
+    for (int a = 0; a < 8; ++a) {
+      const uint4 v = xs[(tw + a) * 32 + lane];
+      const float xf[8] = {bf_lo(v.x), bf_hi(v.x), bf_lo(v.y), bf_hi(v.y),
                            bf_lo(v.z), bf_hi(v.z), bf_lo(v.w), bf_hi(v.w)};
 #pragma unroll
-      for (int a = 0; a < 4; ++a) {
+      for (int b = 0; b < 8; ++b) {
         float& r = acc[a * 8 + b];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) r = __fmaf_rn(xf[a][e], wf[e], r);
+        for (int e = 0; e < 8; ++e) r = __fmaf_rn(xf[e], wf[b][e], r);
+      }
+    }
+    __syncthreads();  // slot s % kTileStages is refilled by the issue of slice s + kTileStages
+  }
+  // reduce-scatter of each half: after the step of width d the lane keeps the
+  // half of its values selected by (lane & d); lane j ends with pair h*32 + j
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float* v = acc + 32 * h;
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) {
+#pragma unroll
+      for (int i = 0; i < d; ++i) {
+        const bool upper = lane & d;
+        const float send = upper ? v[i] : v[i + d];
+        const float keep = upper ? v[i + d] : v[i];
+        v[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, d));
       }
     }
   }
-  // reduce-scatter: after the step of width d the lane keeps the half of its
-  // values selected by (lane & d); finally lane j holds pair j = a*8 + b
 #pragma unroll
-  for (int d = 16; d >= 1; d >>= 1) {
-#pragma unroll
-    for (int i = 0; i < d; ++i) {
-      const bool upper = lane & d;
-      const float send = upper ? acc[i] : acc[i + d];
-      const float keep = upper ? acc[i + d] : acc[i];
-      acc[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, d));
-    }
+  for (int h = 0; h < 2; ++h) {
+    const int pr = 32 * h + lane;  // pair a * 8 + b
+    const int t = t0 + tw + (pr >> 3), e = e0 + ew + (pr & 7);
+    if (t < T && e < E) logits[(size_t)t * E + e] = acc[32 * h];
   }
-  const int t = t0 + tw + (lane >> 3), e = e0 + ew + (lane & 7);
-  if (t < T && e < E) logits[(size_t)t * E + e] = acc[0];
 }
 
 constexpr int kSelWarps = 4;
@@ -206,9 +223,20 @@ cudaError_t launch_select(const moe_spec& sp, const float* logits, const float* 
 
 cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* w, int T, int E, int H,
                                  float* logits, cudaStream_t st) {
-  if (H % 256 == 0 && T >= kTileTok) {
+  if (H % 256 == 0 && T >= kTileMinT) {
     const dim3 grid((T + kTileTok - 1) / kTileTok, (E + kTileExp - 1) / kTileExp);
-    return launch_pdl(router_logits_tiled_kernel, grid, dim3(256), 0, st, x, w, T, E, H, logits);
+    static bool attr_set[64];
+    int d = 0;
+    cudaError_t e = cudaGetDevice(&d);
+    if (e != cudaSuccess) return e;
+    if (d >= 0 && d < 64 && !attr_set[d]) {
+      e = cudaFuncSetAttribute(router_logits_tiled_kernel,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTileSmem);
+      if (e != cudaSuccess) return e;
+      attr_set[d] = true;
+    }
+    return launch_pdl(router_logits_tiled_kernel, grid, dim3(256), kTileSmem, st, x, w, T, E, H,
+                      logits);
   }
   const long warps = (long)T * E;
   const int grid = (int)((warps + 3) / 4);
