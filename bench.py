@@ -519,8 +519,9 @@ def run_gpu(args, w, rank, world, local_rank):
             "peak_kind": peak_kind, "timing": ffn_timing}
     cpu = cpu_baseline(w, xs_h, wr_h, bias_h) if world == 1 and not args.no_cpu else None
     # moe_layer_forward: logits, control step (+ selection for T <= 16, E <= 256, else a
-    # separate select kernel), fill copy, gate/up, down
-    launches_per_layer = 5 if (T <= 16 and E <= 256) else 6
+    # separate select kernel), gate/up, down (+ a fill copy kernel for shapes whose FFN
+    # does not carry the fill); the library reports the count for the shape
+    launches_per_layer = m.moe_layer_kernel_count(spec, T)
     out = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,

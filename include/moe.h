@@ -255,16 +255,25 @@ size_t moe_layer_workspace_bytes(const moe_spec* spec, int32_t T);
  * moe_expert_ffn for one decode layer, no host sync.
  *   ids, weights  device out [T][k] (the routing decision, kept for the caller)
  *   workspace     >= moe_layer_workspace_bytes(spec, T)
- * The fill copies run beside the FFN (which reads the experts being filled
- * from the bank, byte-identical to their new slots) on a stream owned by the
- * library; `stream` waits for them before any later work, so everything the
- * call enqueues is complete, in order, from the caller's stream's view (also
- * when the stream is being captured into a graph).
+ * The fill copies (bank -> slot of every F expert): when the decode FFN's
+ * streaming kernels serve the shape (hidden % 512 == 0, inter % 256 == 0,
+ * T <= 8, T*k + shared <= 128, and their shared-memory plan fits), those
+ * kernels write each F expert's bytes into its slot as they read them from
+ * the bank (FreeToken summary "method steps": the miss path fills the slot),
+ * so no separate copy runs.  Otherwise a copy kernel runs beside the FFN on
+ * a stream owned by the library and `stream` waits for it before any later
+ * work.  Either way everything the call enqueues is complete, in order, from
+ * the caller's stream's view (also when the stream is being captured into a
+ * graph), and the slot contents are the same.
  * ------------------------------------------------------------------------ */
 int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, const void* x,
                       int32_t T, const void* w_router, const float* bias, const void* shared,
                       moe_plan* plan, int32_t* ids, float* weights, void* workspace,
                       size_t workspace_bytes, float* y, moe_stream_t stream);
+
+/* Kernels one moe_layer_forward call launches for T tokens (for graph sizing
+ * and launch accounting); 0 for an invalid spec or T outside 1..64. */
+int32_t moe_layer_kernel_count(const moe_spec* spec, int32_t T);
 
 /* ------------------------------------------------------------------------
  * Prefill (FreeToken summary "method steps": the GPU computes layer l from

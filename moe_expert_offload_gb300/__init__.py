@@ -93,6 +93,8 @@ def lib():
         L.moe_route.argtypes = [sp, vp, i32, vp, vp, vp, vp, vp, vp]
         L.moe_cache_reset.restype = C.c_int
         L.moe_cache_reset.argtypes = [sp, cp, vp]
+        L.moe_layer_kernel_count.restype = i32
+        L.moe_layer_kernel_count.argtypes = [sp, i32]
         L.moe_cache_place.restype = C.c_int
         L.moe_cache_place.argtypes = [sp, cp, vp, i32, vp]
         L.moe_cache_step.restype = C.c_int
@@ -170,6 +172,10 @@ def moe_route(spec, x, T, w_router, bias, logits, ids, weights, stream=None):
 
 def moe_cache_reset(spec, cache, stream=None):
     return _check(lib().moe_cache_reset(C.byref(spec), C.byref(cache), _stream(stream)))
+
+
+def moe_layer_kernel_count(spec, T) -> int:
+    return int(lib().moe_layer_kernel_count(C.byref(spec), T))
 
 
 def moe_cache_place(spec, cache, ids, stream=None):

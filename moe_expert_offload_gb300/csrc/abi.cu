@@ -188,9 +188,11 @@ int check_step_args(const moe_spec* spec, int32_t layer, int32_t T) {
   return MOE_OK;
 }
 
+// fuse_fill: the streaming FFN kernels also write F's blobs into their slots
+// (the caller launches no fill copy); only when ffn_fill_fusable holds.
 int do_ffn(const moe_spec* spec, const moe_cache* c, int32_t layer, const moe_plan* plan,
            const void* x, int32_t T, const int32_t* ids, const float* weights, const void* shared,
-           void* ws, size_t ws_bytes, float* y, cudaStream_t st) {
+           void* ws, size_t ws_bytes, float* y, cudaStream_t st, bool fuse_fill = false) {
   if (T > moe::kMaxDecodeT) return fail(MOE_EUNSUPPORTED, "decode FFN supports T <= %d",
                                         moe::kMaxDecodeT);
   if (!x || !ids || !weights || !y || !ws) return fail(MOE_EINVAL, "moe_expert_ffn: NULL argument");
@@ -217,6 +219,9 @@ int do_ffn(const moe_spec* spec, const moe_cache* c, int32_t layer, const moe_pl
   a.uniq = plan->uniq;
   a.counts = plan->counts;
   a.fill_ids = plan->fill_ids;
+  a.fill_slots = plan->fill_slots;
+  a.fill_fused = fuse_fill ? 1 : 0;
+  a.pool_w = static_cast<uint8_t*>(c->slot_pool);
   a.err = plan->err;
   a.x = static_cast<const uint16_t*>(x);
   a.ids = ids;
@@ -362,6 +367,15 @@ size_t moe_layer_workspace_bytes(const moe_spec* spec, int32_t T) {
          moe::ffn_workspace_bytes(spec->hidden, spec->inter, spec->top_k, T, spec->has_shared);
 }
 
+int32_t moe_layer_kernel_count(const moe_spec* spec, int32_t T) {
+  if (check_spec(spec) != MOE_OK || T < 1 || T > moe::kMaxDecodeT) return 0;
+  const bool fused_sel = T <= moe::kSelFusedMaxT && spec->num_experts <= moe::kSelFusedMaxE;
+  const bool fused_fill =
+      moe::ffn_fill_fusable(spec->hidden, spec->inter, spec->top_k, T, spec->has_shared);
+  // logits, [select], control step, [fill copy], gate/up, down
+  return 1 + (fused_sel ? 0 : 1) + 1 + (fused_fill ? 0 : 1) + 2;
+}
+
 int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, const void* x,
                       int32_t T, const void* w_router, const float* bias, const void* shared,
                       moe_plan* plan, int32_t* ids, float* weights, void* workspace,
@@ -384,7 +398,12 @@ int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, con
   cudaStream_t st = (cudaStream_t)stream;
   float* logits = static_cast<float*>(workspace);
   const size_t lbytes = align256((size_t)T * spec->num_experts * 4);
-  SideStream* ss = side_stream(st);
+  // fill copy: written by the streaming FFN kernels as they read F from the
+  // bank when both run for this shape (FreeToken "method steps": the miss
+  // path copies the expert into its slot), else a copy kernel beside the FFN
+  const bool fused_fill = moe::ffn_fill_fusable(spec->hidden, spec->inter, spec->top_k, T,
+                                                spec->has_shared);
+  SideStream* ss = fused_fill ? nullptr : side_stream(st);
   if (T <= moe::kSelFusedMaxT && spec->num_experts <= moe::kSelFusedMaxE) {
     // logits kernel, then the selection inside the control step's CTA
     if (!x || !w_router || !ids || !weights) return fail(MOE_EINVAL, "moe_layer_forward: NULL argument");
@@ -408,7 +427,7 @@ int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, con
     sa.wts = weights;
     e = moe::launch_cache_step_sel(a, sa, st);
     if (e != cudaSuccess) return cuda_fail(e, "control step launch");
-    if (!ss) {
+    if (!ss && !fused_fill) {
       const moe::BlobOffsets off = moe::blob_offsets(spec->hidden, spec->inter);
       e = moe::launch_fill_copy(*plan, cache->k_victims, static_cast<const uint8_t*>(cache->bank),
                                 static_cast<uint8_t*>(cache->slot_pool), off.total, st);
@@ -417,7 +436,7 @@ int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, con
   } else {
     rc = do_route(spec, x, T, w_router, bias, logits, ids, weights, st);
     if (rc) return rc;
-    rc = do_cache_step(spec, cache, layer, ids, T, plan, ss ? 0 : 1, st);
+    rc = do_cache_step(spec, cache, layer, ids, T, plan, (ss || fused_fill) ? 0 : 1, st);
     if (rc) return rc;
   }
   if (ss) {  // fill copy beside the FFN
@@ -431,7 +450,8 @@ int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, con
     if (e != cudaSuccess) return cuda_fail(e, "fill copy launch");
   }
   rc = do_ffn(spec, cache, layer, plan, x, T, ids, weights, shared,
-              static_cast<uint8_t*>(workspace) + lbytes, workspace_bytes - lbytes, y, st);
+              static_cast<uint8_t*>(workspace) + lbytes, workspace_bytes - lbytes, y, st,
+              fused_fill);
   if (ss) {
     const cudaError_t e = cudaStreamWaitEvent(st, ss->join, 0);
     if (e != cudaSuccess && !rc) return cuda_fail(e, "fill join");

@@ -594,6 +594,12 @@ void ffn_carve_workspace(FfnArgs& a, void* ws) {
   a.max_entries = (int)max_entries;
 }
 
+bool ffn_fill_fusable(int H, int I, int k, int T, int has_shared) {
+  const long max_entries = (long)T * k + has_shared;  // as ffn_carve_workspace
+  return max_entries <= 128 && ffn_stream_smem(H, T) != SIZE_MAX &&
+         ffn_down_stream_smem(H, I, T) != SIZE_MAX;
+}
+
 cudaError_t launch_ffn_decode(const FfnArgs& a, cudaStream_t st) {
   static size_t done_a1[64], done_a2[64], done_b1[64], done_b2[64];
   const int nblk = (a.H + kRowsBlkB - 1) / kRowsBlkB;

@@ -15,7 +15,11 @@
 //    warps meet only at the stage mbarriers;
 //  * the warps' partial sums go to a two-deep ring in shared memory and one
 //    designated warp per unit (rotating) adds them in warp order and writes
-//    h = silu(g) * u: the sum order is fixed, the result deterministic.
+//    h = silu(g) * u: the sum order is fixed, the result deterministic;
+//  * when the call carries the step's fill copy, a writer warp follows the
+//    same stages and, for an expert being filled (read from the bank), stores
+//    each landed tile and scale block into the expert's new slot before the
+//    stage goes back to the producer (one more arrival on the empty barriers).
 // Every wait is bounded; on a time-out the kernel sets MOE_DERR_WAIT in the
 // plan's error word, the producer still waits (bounded) for the copies it
 // issued, and every warp returns.
@@ -26,7 +30,8 @@ namespace {
 using namespace sc;
 
 constexpr int kCW = 8;                     // consumer warps
-constexpr int kSThreads = (kCW + 1) * 32;  // + producer warp (warp kCW)
+constexpr int kFillW = kCW + 1;            // fill writer warp (after the producer, warp kCW)
+constexpr int kSThreads = (kCW + 2) * 32;
 constexpr int kTokS = 8;                   // tokens per MMA N tile (one per column)
 constexpr int kRing = 2;                   // partial-sum ring depth
 constexpr int kMaxStages = 8;
@@ -91,6 +96,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   __shared__ __align__(8) uint64_t rfull[kRing], rfree[kRing];
   __shared__ const uint8_t* sblob[kStreamMaxEntries];
   __shared__ int smap[kStreamMaxEntries], sbi[kStreamMaxEntries];
+  __shared__ int sfs[kStreamMaxEntries];  // slot an F entry's blob is written to, else -1
   __shared__ int wtok[kCW][kTokS];
   __shared__ int s_fail;
   const int H = a.H, I = a.I, ng = H / kGroup;
@@ -101,12 +107,13 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
+    const int nrel = kCW + (a.fill_fused ? 1 : 0);  // warps that release a stage
     for (int i = 0; i < nst; ++i) {
       bar_init(su32(&full[i]), 1);
-      bar_init(su32(&empty[i]), kCW);
+      bar_init(su32(&empty[i]), nrel);
     }
     bar_init(su32(&sfull), 1);
-    bar_init(su32(&sempty), kCW);
+    bar_init(su32(&sempty), nrel);
     for (int i = 0; i < kRing; ++i) {
       bar_init(su32(&rfull[i]), kCW);
       bar_init(su32(&rfree[i]), 1);
@@ -136,6 +143,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       smap[r] = mi;
       sbi[r] = bi;
       sblob[r] = (mi == 2 ? a.shared : mi == 1 ? a.pool : a.bank) + (int64_t)bi * a.blob_bytes;
+      sfs[r] = a.fill_fused && r < n_uniq ? fill_slot(a, r == lane ? u_first : a.uniq[r]) : -1;
     }
   }
   __syncthreads();
@@ -199,6 +207,48 @@ __global__ void __launch_bounds__(kSThreads, 1)
       if (uses > 0 && !bar_wait(su32(&full[lane]), (uses - 1) & 1)) ok = false;
     }
     if (lane == 31 && nu > 0 && !bar_wait(su32(&sfull), (nu - 1) & 1)) ok = false;
+    if (!__all_sync(0xffffffffu, ok)) s_fail = 1;
+    if (lane == 0 && s_fail && a.err) atomicOr(a.err, MOE_DERR_WAIT);
+    return;
+  }
+  if (wid == kFillW) {
+    // ---------------------------------------------------- fill writer
+    if (!a.fill_fused) return;
+    int s = 0, rnd = 0;
+    bool ok = true;
+    for (int u = u_lo; ok && u < u_hi; ++u) {
+      const int i = u - u_lo, row0 = (u % tpe) * 16, fs = sfs[u / tpe];
+      ok = warp_wait(su32(&sfull), i & 1);
+      if (!ok) break;
+      if (fs >= 0 && lane < 4) {  // the unit's gate / up scale and bias rows
+        const int64_t so = lane == 0 ? off.gs : lane == 1 ? off.gb : lane == 2 ? off.us : off.ub;
+        fence_proxy_async_smem();
+        bulk_s2g(a.pool_w + (int64_t)fs * a.blob_bytes + so + (int64_t)row0 * ng * 2,
+                 su32(sraw + lane * sblk), sblk);
+        bulk_commit();
+        bulk_read_done();
+      }
+      __syncwarp();
+      if (lane == 0) bar_arrive(su32(&sempty));
+      for (int kc = 0; kc < nch; ++kc) {
+        ok = warp_wait(su32(&full[s]), rnd & 1);
+        if (!ok) break;
+        if (fs >= 0 && lane < geo.nsub) {  // the stage's sub-tiles, same boxes as the loads
+          fence_proxy_async_smem();
+          tma_store_4d(&maps.m[1], kc * (geo.KC / 8) + 32 * lane, row0, 0, fs,
+                       su32(stages + s * geo.stage + lane * 4096));
+          bulk_commit();
+          bulk_read_done();
+        }
+        __syncwarp();
+        if (lane == 0) bar_arrive(su32(&empty[s]));
+        if (++s == nst) {
+          s = 0;
+          ++rnd;
+        }
+      }
+    }
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // the slot writes are done
     if (!__all_sync(0xffffffffu, ok)) s_fail = 1;
     if (lane == 0 && s_fail && a.err) atomicOr(a.err, MOE_DERR_WAIT);
     return;
@@ -510,6 +560,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages], sfull, sempty;
   __shared__ const uint8_t* sblob[kStreamMaxEntries];
   __shared__ int smap[kStreamMaxEntries], sbi[kStreamMaxEntries];
+  __shared__ int sfs[kStreamMaxEntries];  // slot an F entry's blob is written to, else -1
   __shared__ int utok[kTokS], s_ntok;
   // routing slots j (and weights) of each staged token that name the entry
   __shared__ int mj[kTokS][kMaxMatch], mcnt[kTokS];
@@ -520,12 +571,13 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
+    const int nrel = kCW + (a.fill_fused ? 1 : 0);  // warps that release a stage
     for (int i = 0; i < nst; ++i) {
       bar_init(su32(&full[i]), 1);
-      bar_init(su32(&empty[i]), kCW);
+      bar_init(su32(&empty[i]), nrel);
     }
     bar_init(su32(&sfull), 1);
-    bar_init(su32(&sempty), kCW);
+    bar_init(su32(&sempty), nrel);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   // the routing plan is complete before the gate/up kernel starts; only h
@@ -550,6 +602,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       smap[r] = mi;
       sbi[r] = bi;
       sblob[r] = (mi == 2 ? a.shared : mi == 1 ? a.pool : a.bank) + (int64_t)bi * a.blob_bytes;
+      sfs[r] = a.fill_fused && r < n_uniq ? fill_slot(a, a.uniq[r]) : -1;
     }
   }
   __syncthreads();
@@ -604,6 +657,46 @@ __global__ void __launch_bounds__(kSThreads, 1)
       if (uses > 0 && !bar_wait(su32(&full[lane]), (uses - 1) & 1)) ok = false;
     }
     if (lane == 31 && nu > 0 && !bar_wait(su32(&sfull), (nu - 1) & 1)) ok = false;
+    if (!__all_sync(0xffffffffu, ok) && lane == 0 && a.err) atomicOr(a.err, MOE_DERR_WAIT);
+    return;
+  }
+  if (wid == kFillW) {
+    // ---------------------------------------------------- fill writer
+    if (!a.fill_fused) return;
+    int s = 0, rnd = 0;
+    bool ok = true;
+    for (int u = u_lo; ok && u < u_hi; ++u) {
+      const int i = u - u_lo, o0 = (u % upe) * kRowsB, fs = sfs[u / upe];
+      ok = warp_wait(su32(&sfull), i & 1);
+      if (!ok) break;
+      if (fs >= 0 && lane < 2) {  // the unit's down scale and bias rows
+        fence_proxy_async_smem();
+        bulk_s2g(a.pool_w + (int64_t)fs * a.blob_bytes + (lane ? off.db : off.ds) +
+                     (int64_t)o0 * ngi * 2,
+                 su32(sraw + lane * rblk), rblk);
+        bulk_commit();
+        bulk_read_done();
+      }
+      __syncwarp();
+      if (lane == 0) bar_arrive(su32(&sempty));
+      for (int kc = 0; kc < nch; ++kc) {
+        ok = warp_wait(su32(&full[s]), rnd & 1);
+        if (!ok) break;
+        if (fs >= 0 && lane == 0) {  // the stage: one 128-row box, as loaded
+          fence_proxy_async_smem();
+          tma_store_3d(&maps.m[1], kc * 32, o0, fs, su32(stages + s * kStageB));
+          bulk_commit();
+          bulk_read_done();
+        }
+        __syncwarp();
+        if (lane == 0) bar_arrive(su32(&empty[s]));
+        if (++s == nst) {
+          s = 0;
+          ++rnd;
+        }
+      }
+    }
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // the slot writes are done
     if (!__all_sync(0xffffffffu, ok) && lane == 0 && a.err) atomicOr(a.err, MOE_DERR_WAIT);
     return;
   }

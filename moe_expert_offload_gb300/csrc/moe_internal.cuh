@@ -116,6 +116,12 @@ struct FfnArgs {
   const int32_t* uniq;
   const int32_t* counts;
   const int32_t* fill_ids;  // F of this step (counts[4] entries)
+  const int32_t* fill_slots;  // and their slots
+  // 1: the streaming kernels also write each F expert's blob into its slot as
+  // they read it from the bank (the step's fill copy, fused); set only when
+  // both streaming kernels run (ffn_fill_fusable)
+  int fill_fused;
+  uint8_t* pool_w;  // the slot pool, written when fill_fused
   int32_t* err;
   const uint16_t* x;
   const int32_t* ids;
@@ -129,6 +135,14 @@ struct FfnArgs {
   int n_bank;       // blobs in the bank (num_layers * E)
   int n_pool;       // slots in the pool
 };
+// The slot an expert filled in this step goes to, or -1 (id not in F).
+__device__ __forceinline__ int32_t fill_slot(const FfnArgs& a, int32_t id) {
+  const int nf = a.counts[4];
+  int32_t v = -1;
+  for (int i = 0; i < nf; ++i)
+    if (a.fill_ids[i] == id) v = a.fill_slots[i];
+  return v;
+}
 // Where the FFN reads a routed id's weights: its slot when it was cached
 // before this step (H), else in place from the bank (C, and F: an expert being
 // filled in this step is read from the bank, byte-identical to its new slot,
@@ -152,6 +166,9 @@ __device__ __forceinline__ int32_t ffn_slot(const FfnArgs& a, int32_t id) {
 size_t ffn_workspace_bytes(int H, int I, int k, int T, int has_shared);
 void ffn_carve_workspace(FfnArgs& a, void* ws);
 cudaError_t launch_ffn_decode(const FfnArgs& a, cudaStream_t st);
+// Both streaming decode kernels run for this shape, so they can carry the
+// step's fill copy (FfnArgs::fill_fused).
+bool ffn_fill_fusable(int H, int I, int k, int T, int has_shared);
 // streaming gate/up phase (T <= 8, H % 256 == 0): persistent CTAs fed by
 // cp.async.bulk stages
 cudaError_t launch_ffn_gate_up_stream(const FfnArgs& a, int n_tick, cudaStream_t st);

@@ -251,3 +251,15 @@ def test_hot_placement_is_best_fixed_set():
     assert list(placement.layer_placement(3, 4, 9)) == list(range(8))
     assert list(placement.layer_placement(3, 4, 100)) == list(range(12))
     assert placement.layer_placement(3, 4, 3).size == 0
+
+
+def test_layer_kernel_count(L):
+    """Host-side launch accounting of moe_layer_forward (no device work)."""
+    assert m.moe_layer_kernel_count(m.make_spec(1, 2048, 512, 256, 8), 1) == 4  # FFN carries fill
+    assert m.moe_layer_kernel_count(m.make_spec(1, 7168, 2048, 256, 8), 8) == 4
+    # H = 256 is below the streaming kernels' 512-column tiles: a fill copy kernel runs
+    assert m.moe_layer_kernel_count(m.make_spec(1, 256, 128, 16, 2), 1) == 5
+    assert m.moe_layer_kernel_count(m.make_spec(1, 256, 128, 300, 2), 1) == 6  # + select
+    assert m.moe_layer_kernel_count(m.make_spec(1, 2048, 512, 256, 8), 9) == 5  # T > 8
+    assert m.moe_layer_kernel_count(m.make_spec(1, 2048, 512, 256, 8), 0) == 0
+    assert m.moe_layer_kernel_count(m.make_spec(1, 2048, 512, 256, 8), 65) == 0

@@ -308,6 +308,51 @@ def test_layer_forward_under_policies(oracle, policy):
     assert hits > 0
 
 
+# --------------------------------------------- fill carried by the decode FFN
+@pytest.mark.parametrize("H,I,E,k,T,shared,S,K", [(1024, 256, 16, 4, 1, True, 6, 3),
+                                                  (1024, 256, 16, 4, 3, False, 5, 4),
+                                                  (2048, 512, 24, 8, 8, True, 20, 8),
+                                                  (512, 256, 12, 3, 2, True, 4, 2)])
+def test_layer_forward_fused_fill(oracle, H, I, E, k, T, shared, S, K):
+    """Shapes the streaming FFN serves: the fill copy is written by the FFN kernels as they
+    read F from the bank (no copy kernel).  Plans, outputs and every resident slot's bytes
+    equal the oracle's and the bank's over steps with fills and evictions."""
+    L = 2
+    spec, bank, bank_h, cache, sh = _layer_rig(L, H, I, E, k, S, K, 52700, 77300, shared,
+                                               seed=H + T)
+    assert m.moe_layer_kernel_count(spec, T) == 4  # logits, control, gate/up, down
+    plan = m.DevicePlan(T * k, K, device=DEV)
+    wsb = m.moe_layer_workspace_bytes(spec, T)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    wts = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    y = torch.empty((T, H), dtype=torch.float32, device=DEV)
+    ost = oracle.CacheState(L * E, S)
+    rng = np.random.default_rng(T * 7 + S)
+    fills = 0
+    for step in range(10):
+        layer = step % L
+        wr_h = synth.router_weights(50 + layer, E, H)
+        xb = synth.bf16_bits(rng.normal(0, 1.5, (T, H)))
+        m.moe_layer_forward(spec, cache.c, layer, dev_bits(xb, DEV), T, dev_bits(wr_h, DEV), None,
+                            sh, plan.c, ids, wts, ws, wsb, y)
+        torch.cuda.synchronize()
+        oid, ow = oracle.route_softmax_topk(oracle.router_logits(xb, wr_h), k)
+        assert np.array_equal(ids.cpu().numpy(), oid)
+        op = oracle.cache_step(ost, E, layer, oid, K, 52700, 77300)
+        _plans_equal(plan.read(K), op, K)
+        fills += op["n_fill"]
+        ref = oracle.moe_ffn(list(bank_h[layer * E:(layer + 1) * E]), H, I, xb, oid, ow,
+                             bank_h[L * E] if shared else None, I)
+        assert_ffn_close(y.cpu().numpy(), ref, f"step {step}")
+        pool = cache.pool.cpu().numpy()
+        for slot, eid in enumerate(ost.id_of_slot):
+            if eid >= 0:
+                assert np.array_equal(pool[slot], bank_h[eid]), f"step {step} slot {slot}"
+    assert fills > 0
+    assert int(plan.err[0].item()) == 0
+
+
 # ------------------------------------------------------- fill + expert FFN
 def _layer_rig(L, H, I, E, k, S, K, bp, bh, has_shared, seed=0, big=False):
     spec = m.make_spec(L, H, I, E, k, has_shared=has_shared)
