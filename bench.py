@@ -383,9 +383,9 @@ def run_gpu(args, w, rank, world, local_rank):
     lws = m.moe_layer_workspace_bytes(spec, T)
 
     def step(s, ev=None):
-        # the timed step: one moe_layer_forward per layer (route, control, fill
-        # beside the FFN, FFN); with events, the same work as separate calls so
-        # that the FFN launches can be bracketed
+        # the timed step: one moe_layer_forward per layer (route, control, FFN
+        # carrying the fill copy); with events, the same work as separate calls
+        # (FFN, fill copy kernel) so that the FFN launches can be bracketed
         sh = torch.cuda.current_stream().cuda_stream
         for l in range(L):
             if ev is None:
