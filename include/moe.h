@@ -271,6 +271,16 @@ int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, con
                       moe_plan* plan, int32_t* ids, float* weights, void* workspace,
                       size_t workspace_bytes, float* y, moe_stream_t stream);
 
+/* Test hook for failure detection without a GPU fault.  With on != 0 the
+ * next decode FFN call of this process (moe_expert_ffn or moe_layer_forward,
+ * on a shape the streaming kernels serve) issues no weight copies in its
+ * gate/up kernel: that kernel's warps find their stages never filled, give
+ * up after their bounded wait (one second of device time each), set
+ * MOE_DERR_WAIT in plan->err and return; y of that call is undefined.  The
+ * flag is cleared by that call (or by on == 0); the device context stays
+ * usable and the next call runs normally.  Returns MOE_OK. */
+int moe_debug_inject_ffn_stall(int32_t on);
+
 /* Kernels one moe_layer_forward call launches for T tokens (for graph sizing
  * and launch accounting); 0 for an invalid spec or T outside 1..64. */
 int32_t moe_layer_kernel_count(const moe_spec* spec, int32_t T);

@@ -93,6 +93,8 @@ def lib():
         L.moe_route.argtypes = [sp, vp, i32, vp, vp, vp, vp, vp, vp]
         L.moe_cache_reset.restype = C.c_int
         L.moe_cache_reset.argtypes = [sp, cp, vp]
+        L.moe_debug_inject_ffn_stall.restype = C.c_int
+        L.moe_debug_inject_ffn_stall.argtypes = [i32]
         L.moe_layer_kernel_count.restype = i32
         L.moe_layer_kernel_count.argtypes = [sp, i32]
         L.moe_cache_place.restype = C.c_int
@@ -172,6 +174,12 @@ def moe_route(spec, x, T, w_router, bias, logits, ids, weights, stream=None):
 
 def moe_cache_reset(spec, cache, stream=None):
     return _check(lib().moe_cache_reset(C.byref(spec), C.byref(cache), _stream(stream)))
+
+
+def moe_debug_inject_ffn_stall(on=True):
+    """Test hook: the next decode FFN call's gate/up kernel issues no copies, so its
+    bounded waits run out and plan.err gets MOE_DERR_WAIT (include/moe.h)."""
+    return _check(lib().moe_debug_inject_ffn_stall(1 if on else 0))
 
 
 def moe_layer_kernel_count(spec, T) -> int:

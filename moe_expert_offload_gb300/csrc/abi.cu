@@ -5,6 +5,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <vector>
 
 #include "moe_internal.cuh"
@@ -188,6 +189,9 @@ int check_step_args(const moe_spec* spec, int32_t layer, int32_t T) {
   return MOE_OK;
 }
 
+// moe_debug_inject_ffn_stall: consumed by the next do_ffn
+std::atomic<int> g_inject_stall{0};
+
 // fuse_fill: the streaming FFN kernels also write F's blobs into their slots
 // (the caller launches no fill copy); only when ffn_fill_fusable holds.
 int do_ffn(const moe_spec* spec, const moe_cache* c, int32_t layer, const moe_plan* plan,
@@ -222,6 +226,7 @@ int do_ffn(const moe_spec* spec, const moe_cache* c, int32_t layer, const moe_pl
   a.fill_slots = plan->fill_slots;
   a.fill_fused = fuse_fill ? 1 : 0;
   a.pool_w = static_cast<uint8_t*>(c->slot_pool);
+  a.inject_stall = g_inject_stall.exchange(0);
   a.err = plan->err;
   a.x = static_cast<const uint16_t*>(x);
   a.ids = ids;
@@ -365,6 +370,11 @@ size_t moe_layer_workspace_bytes(const moe_spec* spec, int32_t T) {
   if (check_spec(spec) != MOE_OK || T < 1) return 0;
   return align256((size_t)T * spec->num_experts * 4) +
          moe::ffn_workspace_bytes(spec->hidden, spec->inter, spec->top_k, T, spec->has_shared);
+}
+
+int moe_debug_inject_ffn_stall(int32_t on) {
+  g_inject_stall.store(on ? 1 : 0);
+  return MOE_OK;
 }
 
 int32_t moe_layer_kernel_count(const moe_spec* spec, int32_t T) {
@@ -654,7 +664,7 @@ int do_prefill(const moe_spec* spec, const void* experts, const void* x, int32_t
   const size_t need = moe::prefill_workspace_bytes(spec->hidden, spec->inter, spec->num_experts,
                                                    spec->top_k, T);
   if (ws_bytes < need) return fail(MOE_ECAPACITY, "workspace %zu < %zu bytes", ws_bytes, need);
-  moe::PrefillBufs b;
+  moe::PrefillBufs b{};
   moe::prefill_carve(b, ws, spec->hidden, spec->inter, spec->num_experts, spec->top_k, T);
   moe::GemmArgs a = {};
   a.H = spec->hidden;

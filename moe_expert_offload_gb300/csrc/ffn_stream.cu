@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
 
   if (wid == kCW) {
     // -------------------------------------------------------- producer
+    if (a.inject_stall) return;  // test hook: the other warps' waits run out
     int s = 0, rnd = 0, nq = 0, nu = 0;
     bool ok = true;
     for (int u = u_lo; ok && u < u_hi; ++u) {

@@ -68,7 +68,6 @@ constexpr int kABytes = kBM * kBK * 2;           // 32 KB
 // loads leave the load/store pipe to the A gather and the bf16 stores
 constexpr int kCodeStages = 3;
 constexpr int kCodeBox = 32 * 32;
-constexpr uint32_t kWaitIters = 1u << 20;
 
 // ------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -94,19 +93,10 @@ __device__ __forceinline__ void mbar_init(uint32_t addr, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(addr), "r"(count) : "memory");
 }
 
-// Bounded wait for the completion of the phase with parity `parity`.
+// Bounded wait (one second of global time) for the completion of the phase
+// with parity `parity`.
 __device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitIters; ++i) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(addr), "r"(parity)
-        : "memory");
-    if (done) return true;
-  }
-  return false;
+  return sc::bar_wait(addr, parity);
 }
 
 __device__ __forceinline__ void tc_fence_before() {

@@ -82,23 +82,23 @@ cudaError_t launch_router_select(const moe_spec& sp, const float* logits, const 
 // shared LRU and static placement, layer's own range for the per-layer LRU.
 // no_fill (static placement) makes q = 0.
 struct CacheArgs {
-  int E, layer, n_ids, S0, S, K, bp, bh, no_fill;
-  const int32_t* ids;
-  int32_t *slot_of_id, *id_of_slot;
-  uint32_t *ts, *clock;
-  moe_plan plan;
+  int E = 0, layer = 0, n_ids = 0, S0 = 0, S = 0, K = 0, bp = 0, bh = 0, no_fill = 0;
+  const int32_t* ids = nullptr;
+  int32_t *slot_of_id = nullptr, *id_of_slot = nullptr;
+  uint32_t *ts = nullptr, *clock = nullptr;
+  moe_plan plan{};
 };
 cudaError_t launch_cache_step(const CacheArgs& a, cudaStream_t st);
 // Router selection done inside the control step's CTA (decode layer step with
 // T <= 16 tokens and E <= 256 experts): one warp per token reads its logits
 // and writes ids / weights before the control step reads them.
 struct SelArgs {
-  const float* logits;
-  const float* bias;
-  int T, k, router, n_groups, topk_groups;
-  float scale;
-  int32_t* ids;
-  float* wts;
+  const float* logits = nullptr;
+  const float* bias = nullptr;
+  int T = 0, k = 0, router = 0, n_groups = 0, topk_groups = 0;
+  float scale = 0.0f;
+  int32_t* ids = nullptr;
+  float* wts = nullptr;
 };
 constexpr int kSelFusedMaxT = 16, kSelFusedMaxE = 256;
 cudaError_t launch_cache_step_sel(const CacheArgs& a, const SelArgs& s, cudaStream_t st);
@@ -108,32 +108,35 @@ cudaError_t launch_fill_copy(const moe_plan& plan, int K, const uint8_t* bank, u
                              int64_t blob_bytes, cudaStream_t st);
 
 struct FfnArgs {
-  int H, I, E, k, layer, T, has_shared;
-  int64_t blob_bytes;
-  const uint8_t* bank;
-  const uint8_t* pool;
-  const int32_t* slot_of_id;
-  const int32_t* uniq;
-  const int32_t* counts;
-  const int32_t* fill_ids;  // F of this step (counts[4] entries)
-  const int32_t* fill_slots;  // and their slots
+  // every member has a zero default, so a caller that fills in only some
+  // fields never hands a kernel an indeterminate flag or pointer
+  int H = 0, I = 0, E = 0, k = 0, layer = 0, T = 0, has_shared = 0;
+  int64_t blob_bytes = 0;
+  const uint8_t* bank = nullptr;
+  const uint8_t* pool = nullptr;
+  const int32_t* slot_of_id = nullptr;
+  const int32_t* uniq = nullptr;
+  const int32_t* counts = nullptr;
+  const int32_t* fill_ids = nullptr;    // F of this step (counts[4] entries)
+  const int32_t* fill_slots = nullptr;  // and their slots
   // 1: the streaming kernels also write each F expert's blob into its slot as
   // they read it from the bank (the step's fill copy, fused); set only when
   // both streaming kernels run (ffn_fill_fusable)
-  int fill_fused;
-  uint8_t* pool_w;  // the slot pool, written when fill_fused
-  int32_t* err;
-  const uint16_t* x;
-  const int32_t* ids;
-  const float* weights;
-  const uint8_t* shared;
-  float* h;         // [max_entries][T][I]
-  float* partial;   // [T][k + has_shared][H]
-  uint32_t* tick;   // [ceil(H / 16)] arrival counters, one per 16-row tile of y
-  float* y;         // [T][H]
-  int max_entries;
-  int n_bank;       // blobs in the bank (num_layers * E)
-  int n_pool;       // slots in the pool
+  int fill_fused = 0;
+  uint8_t* pool_w = nullptr;  // the slot pool, written when fill_fused
+  int inject_stall = 0;       // test hook: the gate/up producer issues no copies
+  int32_t* err = nullptr;
+  const uint16_t* x = nullptr;
+  const int32_t* ids = nullptr;
+  const float* weights = nullptr;
+  const uint8_t* shared = nullptr;
+  float* h = nullptr;         // [max_entries][T][I]
+  float* partial = nullptr;   // [T][k + has_shared][H]
+  uint32_t* tick = nullptr;   // [ceil(H / 16)] arrival counters, one per 16-row tile of y
+  float* y = nullptr;         // [T][H]
+  int max_entries = 0;
+  int n_bank = 0;             // blobs in the bank (num_layers * E)
+  int n_pool = 0;             // slots in the pool
 };
 // The slot an expert filled in this step goes to, or -1 (id not in F).
 __device__ __forceinline__ int32_t fill_slot(const FfnArgs& a, int32_t id) {

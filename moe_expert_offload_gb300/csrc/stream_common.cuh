@@ -11,7 +11,13 @@
 namespace moe {
 namespace sc {
 
-constexpr uint32_t kSpin = 1u << 20;  // try_wait rounds before a wait gives up
+// A wait gives up after kWaitNs of global time (one second), so a failure
+// (a copy that never lands, a stage never released) ends the kernel with an
+// error word instead of a hang.  One try_wait round may suspend the thread
+// for a system-dependent time, so the bound is kept in time; kSpin rounds is
+// a second cap in case the timer did not advance.
+constexpr uint64_t kWaitNs = 1000000000ull;
+constexpr uint32_t kSpin = 1u << 26;
 
 __device__ __forceinline__ uint32_t su32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -21,16 +27,30 @@ __device__ __forceinline__ void bar_init(uint32_t a, uint32_t n) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(n) : "memory");
 }
 
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool try_wait_parity(uint32_t a, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(a), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Bounded wait for the completion of the phase with parity `parity`.
 __device__ __forceinline__ bool bar_wait(uint32_t a, uint32_t parity) {
+  if (try_wait_parity(a, parity)) return true;
+  const uint64_t t0 = global_ns();
   for (uint32_t i = 0; i < kSpin; ++i) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(a), "r"(parity)
-        : "memory");
-    if (done) return true;
+    if (try_wait_parity(a, parity)) return true;
+    if (global_ns() - t0 > kWaitNs) return false;
   }
   return false;
 }

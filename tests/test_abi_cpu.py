@@ -263,3 +263,9 @@ def test_layer_kernel_count(L):
     assert m.moe_layer_kernel_count(m.make_spec(1, 2048, 512, 256, 8), 9) == 5  # T > 8
     assert m.moe_layer_kernel_count(m.make_spec(1, 2048, 512, 256, 8), 0) == 0
     assert m.moe_layer_kernel_count(m.make_spec(1, 2048, 512, 256, 8), 65) == 0
+
+
+def test_inject_hook_sets_and_clears(L):
+    # host-side only: the flag is armed and cleared without any device work
+    assert m.moe_debug_inject_ffn_stall(True) == m.MOE_OK
+    assert m.moe_debug_inject_ffn_stall(False) == m.MOE_OK

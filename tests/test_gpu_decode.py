@@ -4,6 +4,8 @@ Routing (logits, ids, weights), the control step (sets, victims, tables) and
 the slot-pool contents must match bit for bit; expert-FFN outputs must be
 within the Edge0 tolerance (relative L2 <= 1e-2, |err| <= 2e-2 * max|y|).
 """
+import time
+
 import numpy as np
 import pytest
 
@@ -351,6 +353,39 @@ def test_layer_forward_fused_fill(oracle, H, I, E, k, T, shared, S, K):
                 assert np.array_equal(pool[slot], bank_h[eid]), f"step {step} slot {slot}"
     assert fills > 0
     assert int(plan.err[0].item()) == 0
+
+
+# ------------------------------------------------ failure detection (no fault)
+def test_ffn_wait_timeout_sets_error_and_context_survives(oracle):
+    """The injected stall leaves the gate/up stages unfilled: the kernel's bounded waits
+    (one second of device time) run out, plan.err gets MOE_DERR_WAIT and the call returns;
+    the next call on the same context is correct."""
+    H, I, E, k, T, S, K = 1024, 256, 16, 4, 1, 6, 3
+    spec, bank, bank_h, cache, sh = _layer_rig(1, H, I, E, k, S, K, 52700, 77300, True, seed=5)
+    plan = m.DevicePlan(T * k, K, device=DEV)
+    fws = m.moe_ffn_workspace_bytes(spec, T)
+    ws = torch.empty(fws, dtype=torch.uint8, device=DEV)
+    ids_h = np.array([[1, 5, 9, 12]], np.int32)
+    wts_h = np.array([[0.4, 0.3, 0.2, 0.1]], np.float32)
+    ids, wts = dev(ids_h, DEV), dev(wts_h, DEV)
+    xb = synth.bf16_bits(np.random.default_rng(0).normal(0, 1, (T, H)))
+    x = dev_bits(xb, DEV)
+    y = torch.empty((T, H), dtype=torch.float32, device=DEV)
+    m.moe_cache_step(spec, cache.c, 0, ids, T, plan.c, do_fill=1)
+    torch.cuda.synchronize()
+    m.moe_debug_inject_ffn_stall(True)
+    t0 = time.perf_counter()
+    m.moe_expert_ffn(spec, cache.c, 0, plan.c, x, T, ids, wts, sh, ws, fws, y)
+    torch.cuda.synchronize()
+    took = time.perf_counter() - t0
+    assert plan.read(K)["err"] & m.MOE_DERR_WAIT
+    assert 0.5 < took < 30.0, took
+    plan.err.zero_()
+    m.moe_expert_ffn(spec, cache.c, 0, plan.c, x, T, ids, wts, sh, ws, fws, y)
+    torch.cuda.synchronize()
+    assert int(plan.err[0].item()) == 0
+    ref = oracle.moe_ffn(list(bank_h[:E]), H, I, xb, ids_h, wts_h, bank_h[E], I)
+    assert_ffn_close(y.cpu().numpy(), ref, "after the stall")
 
 
 # ------------------------------------------------------- fill + expert FFN
