@@ -93,8 +93,8 @@ __device__ __forceinline__ void mbar_init(uint32_t addr, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(addr), "r"(count) : "memory");
 }
 
-// Bounded wait (one second of global time) for the completion of the phase
-// with parity `parity`.
+// Bounded wait (about one second) for the completion of the phase with
+// parity `parity`.
 __device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity) {
   return sc::bar_wait(addr, parity);
 }

@@ -11,12 +11,16 @@
 namespace moe {
 namespace sc {
 
-// A wait gives up after kWaitNs of global time (one second), so a failure
-// (a copy that never lands, a stage never released) ends the kernel with an
-// error word instead of a hang.  One try_wait round may suspend the thread
-// for a system-dependent time, so the bound is kept in time; kSpin rounds is
-// a second cap in case the timer did not advance.
-constexpr uint64_t kWaitNs = 1000000000ull;
+// A wait gives up after 1024 try_wait rounds plus kWaitCycles SM clock
+// cycles (2^31: about one second at the 2.07 GHz maximum clock, longer at
+// lower clocks), so a failure (a copy that never lands, a stage never
+// released) ends the kernel with an error word instead of a hang.  One round
+// may suspend the thread for a system-dependent time, so the bound is kept in
+// cycles; kSpin rounds is a second cap.  The counter is read only once a wait
+// has run 1024 rounds: the waits of the streaming kernels sit in their inner
+// loops, where any extra work at the wait site (an early counter read, a
+// second copy of the try_wait) measurably slowed them.
+constexpr long long kWaitCycles = 1ll << 31;
 constexpr uint32_t kSpin = 1u << 26;
 
 __device__ __forceinline__ uint32_t su32(const void* p) {
@@ -27,30 +31,23 @@ __device__ __forceinline__ void bar_init(uint32_t a, uint32_t n) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(n) : "memory");
 }
 
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ bool try_wait_parity(uint32_t a, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(done)
-      : "r"(a), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
 // Bounded wait for the completion of the phase with parity `parity`.
 __device__ __forceinline__ bool bar_wait(uint32_t a, uint32_t parity) {
-  if (try_wait_parity(a, parity)) return true;
-  const uint64_t t0 = global_ns();
+  long long t0 = 0;  // taken after the first 1024 rounds
   for (uint32_t i = 0; i < kSpin; ++i) {
-    if (try_wait_parity(a, parity)) return true;
-    if (global_ns() - t0 > kWaitNs) return false;
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((i & 1023u) == 1023u) {
+      const long long t = clock64();
+      if (t0 == 0) t0 = t;
+      else if (t - t0 > kWaitCycles) return false;
+    }
   }
   return false;
 }
