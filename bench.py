@@ -2,8 +2,8 @@
 """Benchmark of the per-layer MoE expert step on one GB300 (or N replicas).
 
 A step is one decode token through every MoE layer of the workload: per
-layer moe_layer_forward (router, control step, fill copies beside the expert
-FFN + combine), through the C ABI on inputs already resident in HBM.  The
+layer moe_layer_forward (router, control step, expert FFN + combine carrying
+the fill copies), through the C ABI on inputs already resident in HBM.  The
 FFN's own duration (roofline) is taken from a separate replay of the same
 steps as moe_route / moe_cache_step / moe_expert_ffn calls with CUDA events
 around each moe_expert_ffn.  `e2e` repeats the measurement

@@ -27,6 +27,9 @@
 //   * sigmoid-group tie rules and normalise-then-scale order
 //   * q rounding half-up, F = lowest-id misses, q capped by K
 //   * clock advanced once per control call; victims exclude slots hit now
+//   * replacement policies compared with the shared LRU: per-layer LRU on an
+//     equal split of the slots (floor(S / L) each, the rest unused); static
+//     placement fills nothing (q = 0); a placed slot starts with ts 0
 //   * shared expert added with weight 1
 //
 // Parity status: every function below is pinned by the not-gpu tests
