@@ -490,6 +490,25 @@ def test_static_policy_is_membership(oracle, seed):
         assert np.array_equal(st.slot_of_id, soi) and np.array_equal(st.id_of_slot, ios)
 
 
+def test_placed_slots_are_first_victims_until_used(oracle):
+    """A placed slot has ts 0 (placed, not yet used): under the shared LRU the placed but
+    unrouted slots are taken first, in slot order, before any slot routed since; a placed
+    id that is routed is a hit and leaves the victim list."""
+    E, L, S, K = 8, 2, 6, 6
+    st = oracle.CacheState(L * E, S)
+    placed = [9, 2, 14, 5]  # slots 0..3; slots 4, 5 empty (ts 0 too)
+    oracle.cache_place(st, E, L, placed)
+    plan = oracle.cache_step(st, E, 0, np.array([2, 7]), K, 77300, 77300)  # 2 hits, 7 misses
+    assert list(plan["hit_ids"]) == [2] and list(plan["hit_slots"]) == [1]
+    assert [v for v in plan["victims"] if v >= 0] == [0, 2, 3, 4, 5]
+    assert list(plan["fill_slots"]) == [0] and list(plan["evicted_ids"]) == [9]
+    plan = oracle.cache_step(st, E, 1, np.array([0, 1, 2]), K, 77300, 77300)  # ids 8, 9, 10
+    # slots 2, 3, 4, 5 still have ts 0; slots 0 (id 7) and 1 (id 2) were used at steps 1
+    assert [v for v in plan["victims"] if v >= 0] == [2, 3, 4, 5, 0, 1]
+    assert list(plan["fill_slots"]) == [2, 3, 4]
+    assert list(plan["evicted_ids"]) == [14, 5, -1]
+
+
 def test_cache_place_layout_and_errors(oracle):
     E, L, S = 10, 3, 10
     st = oracle.CacheState(L * E, S)
