@@ -134,16 +134,17 @@ __global__ void __launch_bounds__(kSThreads, 1)
     for (int r = lane; r < n_exec; r += 32) {
       // blob pointer (scale copies) and (tensor map, blob index) of entry r
       int mi = 2, bi = 0;
+      int32_t fs = -1;
       if (r < n_uniq) {
         const int32_t id = r == lane ? u_first : a.uniq[r];
-        const int32_t slot = ffn_slot(a, id);
+        const int32_t slot = ffn_slot(a, id, &fs);
         mi = slot >= 0 ? 1 : 0;
         bi = slot >= 0 ? slot : id;
       }
       smap[r] = mi;
       sbi[r] = bi;
       sblob[r] = (mi == 2 ? a.shared : mi == 1 ? a.pool : a.bank) + (int64_t)bi * a.blob_bytes;
-      sfs[r] = a.fill_fused && r < n_uniq ? fill_slot(a, r == lane ? u_first : a.uniq[r]) : -1;
+      sfs[r] = fs;
     }
   }
   __syncthreads();
@@ -594,16 +595,17 @@ __global__ void __launch_bounds__(kSThreads, 1)
     if (lane < 3) tma_prefetch_map(&maps.m[lane]);
     for (int r = lane; r < n_exec; r += 32) {
       int mi = 2, bi = 0;
+      int32_t fs = -1;
       if (r < n_uniq) {
         const int32_t id = a.uniq[r];
-        const int32_t slot = ffn_slot(a, id);
+        const int32_t slot = ffn_slot(a, id, &fs);
         mi = slot >= 0 ? 1 : 0;
         bi = slot >= 0 ? slot : id;
       }
       smap[r] = mi;
       sbi[r] = bi;
       sblob[r] = (mi == 2 ? a.shared : mi == 1 ? a.pool : a.bank) + (int64_t)bi * a.blob_bytes;
-      sfs[r] = a.fill_fused && r < n_uniq ? fill_slot(a, a.uniq[r]) : -1;
+      sfs[r] = fs;
     }
   }
   __syncthreads();

@@ -138,31 +138,37 @@ struct FfnArgs {
   int n_bank = 0;             // blobs in the bank (num_layers * E)
   int n_pool = 0;             // slots in the pool
 };
-// The slot an expert filled in this step goes to, or -1 (id not in F).
-__device__ __forceinline__ int32_t fill_slot(const FfnArgs& a, int32_t id) {
-  const int nf = a.counts[4];
-  int32_t v = -1;
-  for (int i = 0; i < nf; ++i)
-    if (a.fill_ids[i] == id) v = a.fill_slots[i];
-  return v;
-}
 // Where the FFN reads a routed id's weights: its slot when it was cached
 // before this step (H), else in place from the bank (C, and F: an expert being
 // filled in this step is read from the bank, byte-identical to its new slot,
-// so the FFN need not wait for the fill copy).  Returns the slot or -1.
-// The slot, the fill count and the first fill ids are loaded together (no load
-// waits for another's result) since this sits on the FFN's start-up path.
-__device__ __forceinline__ int32_t ffn_slot(const FfnArgs& a, int32_t id) {
+// so the FFN need not wait for the fill copy).  Returns the slot or -1; with
+// fs, also the slot an F expert goes to (-1 for H and C; only when the call
+// carries the fill, the one case fill_slots is set).
+// The slot, the fill count and the first fill ids (and slots) are loaded
+// together, no load waiting for another's result beyond the fill count, since
+// this sits on the FFN's start-up path.
+__device__ __forceinline__ int32_t ffn_slot(const FfnArgs& a, int32_t id,
+                                            int32_t* fs = nullptr) {
   const int32_t slot = a.slot_of_id[id];
   const int nf = a.counts[4];
+  const bool want = fs != nullptr && a.fill_fused;
   bool filled = false;
+  int32_t fv = -1;
   for (int i0 = 0; i0 < nf; i0 += 8) {
-    int32_t f[8];
+    int32_t f[8], v[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) f[q] = i0 + q < nf ? a.fill_ids[i0 + q] : -1;
+    for (int q = 0; q < 8; ++q) {
+      f[q] = i0 + q < nf ? a.fill_ids[i0 + q] : -1;
+      v[q] = want && i0 + q < nf ? a.fill_slots[i0 + q] : -1;
+    }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) filled |= f[q] == id;
+    for (int q = 0; q < 8; ++q)
+      if (f[q] == id) {
+        filled = true;
+        fv = v[q];
+      }
   }
+  if (fs) *fs = want ? fv : -1;
   return (slot < 0 || filled) ? -1 : slot;
 }
 
