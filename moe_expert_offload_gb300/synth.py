@@ -154,6 +154,58 @@ def make_bank_torch(n_experts: int, H: int, I: int, seed: int, device):
 
 
 # ---------------------------------------------------------- routing inputs
+# ----------------------------------------------------------- FP4 experts
+FP4_BLOCK = {0: 32, 1: 16}  # MXFP4: 32 elements per E8M0 scale; NVFP4: 16 per E4M3 scale
+
+
+def fp4_blob_sections(H: int, I: int, fmt: int):
+    """Byte offsets of an FP4 expert blob: codes Wg, Wu, Wd (as int4), one scale
+    byte per block of each matrix, then (NVFP4) three fp32 matrix scales."""
+    if H % GROUP or I % GROUP or fmt not in FP4_BLOCK:
+        raise ValueError("hidden and intermediate sizes must be multiples of 64")
+    B = FP4_BLOCK[fmt]
+    sizes = {"gq": I * H // 2, "uq": I * H // 2, "dq": H * I // 2,
+             "gs": I * H // B, "us": I * H // B, "ds": H * I // B, "mat": 12 if fmt == 1 else 0}
+    off, o = {}, 0
+    for name in ("gq", "uq", "dq", "gs", "us", "ds", "mat"):
+        off[name] = o
+        o += sizes[name]
+    return off, sizes, (o + 255) // 256 * 256
+
+
+def pack_fp4_blob(H, I, fmt, qg, qu, qd, sg, su, sd, mat=(1.0, 1.0, 1.0)) -> np.ndarray:
+    """Assemble one FP4 expert blob from E2M1 codes (0..15) [rows][cols] and
+    scale bytes [rows][cols / block] (E8M0 for MXFP4, E4M3 for NVFP4)."""
+    off, sizes, total = fp4_blob_sections(H, I, fmt)
+    blob = np.zeros(total, dtype=np.uint8)
+    parts = {"gq": pack_codes(qg), "uq": pack_codes(qu), "dq": pack_codes(qd),
+             "gs": np.asarray(sg, np.uint8), "us": np.asarray(su, np.uint8),
+             "ds": np.asarray(sd, np.uint8)}
+    if fmt == 1:
+        parts["mat"] = np.asarray(mat, dtype="<f4").view(np.uint8)
+    for name, arr in parts.items():
+        flat = np.ascontiguousarray(arr).reshape(-1).view(np.uint8)
+        assert flat.size == sizes[name], name
+        blob[off[name]:off[name] + sizes[name]] = flat
+    return blob
+
+
+def make_fp4_expert(rng, H: int, I: int, fmt: int) -> np.ndarray:
+    """Random FP4 expert: codes uniform over all 16, block scales around 2^-6
+    (E8M0 bytes 118..124; E4M3 bytes with exponent field 1..5, no NaN), matrix
+    scales U[0.5, 2) for NVFP4."""
+    B = FP4_BLOCK[fmt]
+    q = [rng.integers(0, 16, size=shape, dtype=np.uint8) for shape in ((I, H), (I, H), (H, I))]
+    if fmt == 0:
+        sc = [rng.integers(118, 125, size=(r, c // B), dtype=np.uint8)
+              for r, c in ((I, H), (I, H), (H, I))]
+    else:
+        sc = [((rng.integers(1, 6, size=(r, c // B)) << 3) | rng.integers(0, 8, size=(r, c // B)))
+              .astype(np.uint8) for r, c in ((I, H), (I, H), (H, I))]
+    mat = tuple(float(v) for v in rng.uniform(0.5, 2.0, size=3)) if fmt == 1 else (1.0, 1.0, 1.0)
+    return pack_fp4_blob(H, I, fmt, *q, *sc, mat=mat)
+
+
 def router_weights(seed: int, E: int, H: int, std: float = 0.02) -> np.ndarray:
     """bf16 bits [E][H], N(0, std)."""
     rng = np.random.default_rng(seed)

@@ -62,6 +62,16 @@ def lib():
         L.or_cache_place.restype = i32
         L.or_cache_place.argtypes = [i32, i32, i32, i32, vp, i32, vp, vp, vp, vp]
         L.or_expert_forward.argtypes = [vp, i32, i32, vp, i32, vp]
+        f64 = C.c_double
+        for name in ("or_e2m1", "or_e4m3", "or_e8m0"):
+            getattr(L, name).restype = f64
+            getattr(L, name).argtypes = [i32]
+        L.or_fp4_blob_offsets.restype = i32
+        L.or_fp4_blob_offsets.argtypes = [i32, i32, i32, vp]
+        L.or_fp4_blob_matrix.restype = i32
+        L.or_fp4_blob_matrix.argtypes = [vp, i32, i32, i32, i32, vp]
+        L.or_fp4_expert_forward.restype = i32
+        L.or_fp4_expert_forward.argtypes = [vp, i32, i32, i32, vp, i32, vp]
         L.or_moe_ffn.argtypes = [vp, i32, i32, i32, vp, i32, vp, vp, i32, vp, i32, vp]
         _lib = L
     return _lib
@@ -237,4 +247,46 @@ def moe_ffn(blobs, H: int, I: int, x_bits: np.ndarray, ids: np.ndarray, wts: np.
     y = np.empty((T, H), dtype=np.float64)
     lib().or_moe_ffn(C.cast(ptrs, C.c_void_p), E, H, I, _vp(x), T, _vp(ids), _vp(wts), k,
                      _vp(sb), shared_I, _vp(y))
+    return y
+
+
+# ------------------------------------------------------ FP4 expert formats
+MXFP4, NVFP4 = 0, 1
+
+
+def e2m1(code: int) -> float:
+    return float(lib().or_e2m1(int(code)))
+
+
+def e4m3(byte: int) -> float:
+    return float(lib().or_e4m3(int(byte)))
+
+
+def e8m0(byte: int) -> float:
+    return float(lib().or_e8m0(int(byte)))
+
+
+def fp4_blob_offsets(H: int, I: int, fmt: int) -> dict:
+    off = np.zeros(8, dtype=np.int64)
+    if lib().or_fp4_blob_offsets(H, I, fmt, _vp(off)):
+        raise ValueError("fp4_blob_offsets: bad format or shape")
+    keys = ("gq", "uq", "dq", "gs", "us", "ds", "mat", "total")
+    return {k: int(v) for k, v in zip(keys, off)}
+
+
+def fp4_blob_matrix(blob: np.ndarray, H: int, I: int, which: int, fmt: int) -> np.ndarray:
+    blob = np.ascontiguousarray(blob, dtype=np.uint8)
+    rows, cols = (H, I) if which == 2 else (I, H)
+    out = np.empty((rows, cols), dtype=np.float64)
+    if lib().or_fp4_blob_matrix(_vp(blob), H, I, which, fmt, _vp(out)):
+        raise ValueError("fp4_blob_matrix: bad arguments")
+    return out
+
+
+def fp4_expert_forward(blob: np.ndarray, H: int, I: int, fmt: int, x_bits: np.ndarray) -> np.ndarray:
+    blob = np.ascontiguousarray(blob, dtype=np.uint8)
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16).reshape(-1, H)
+    y = np.empty(x_bits.shape, dtype=np.float64)
+    if lib().or_fp4_expert_forward(_vp(blob), H, I, fmt, _vp(x_bits), x_bits.shape[0], _vp(y)):
+        raise ValueError("fp4_expert_forward: bad arguments")
     return y

@@ -547,4 +547,110 @@ void or_moe_ffn(const uint8_t* const* blobs, int E, int H, int I, const uint16_t
   }
 }
 
+
+// ------------------------------------------------------ FP4 expert formats
+// The pages' deployed models keep their experts in NVFP4 (Qwen3.6 on the
+// laptop, GLM-5.2) or MXFP4 (DeepSeek-V4-Flash) (FreeToken summary "Key
+// results" table).  Both store FP4 E2M1 elements -- 1 sign, 2 exponent and 1
+// mantissa bit, exponent bias 1, no infinity or NaN -- with one scale per
+// block of consecutive elements of a row:
+//   MXFP4  blocks of 32; scale E8M0 = 2^(e - 127), e = 255 is NaN
+//   NVFP4  blocks of 16; scale FP8 E4M3 (bias 7, no infinity, S.1111.111 is
+//          NaN), times one fp32 scale per matrix
+// (the OCP Microscaling Formats specification for E2M1, E8M0 and E4M3;
+// NVFP4 is NVIDIA's 16-element variant with E4M3 block scales).
+// Expert blob (a reading: the pages give no layout): Wg codes [I][H/2], Wu
+// codes [I][H/2], Wd codes [H][I/2] (low nibble = even column, as for int4),
+// then one scale byte per block: Wg [I][H/B], Wu [I][H/B], Wd [H][I/B]; for
+// NVFP4 then the fp32 matrix scales of Wg, Wu, Wd; the total rounded up to
+// 256 bytes.  fmt: 0 = MXFP4 (B = 32), 1 = NVFP4 (B = 16).
+
+double or_e2m1(int code) {
+  const int sgn = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+  const double mag = e == 0 ? 0.5 * m : std::ldexp(1.0 + 0.5 * m, e - 1);
+  return sgn ? -mag : mag;
+}
+
+double or_e4m3(int byte) {
+  const int sgn = (byte >> 7) & 1, e = (byte >> 3) & 15, m = byte & 7;
+  if (e == 15 && m == 7) return std::nan("");
+  const double mag = e == 0 ? std::ldexp(m / 8.0, -6) : std::ldexp(1.0 + m / 8.0, e - 7);
+  return sgn ? -mag : mag;
+}
+
+double or_e8m0(int byte) { return byte == 255 ? std::nan("") : std::ldexp(1.0, byte - 127); }
+
+// off[8]: gate codes, up codes, down codes, gate scales, up scales, down
+// scales, matrix scales (NVFP4), total bytes.  Returns 0, or -1 on a bad
+// format or shape (H, I multiples of 64).
+int or_fp4_blob_offsets(int H, int I, int fmt, int64_t* off) {
+  if ((fmt != 0 && fmt != 1) || H <= 0 || I <= 0 || H % 64 || I % 64) return -1;
+  const int64_t B = fmt == 1 ? 16 : 32, hi = (int64_t)H * I;
+  off[0] = 0;
+  off[1] = hi / 2;
+  off[2] = hi;
+  off[3] = hi / 2 * 3;
+  off[4] = off[3] + hi / B;
+  off[5] = off[4] + hi / B;
+  off[6] = off[5] + hi / B;
+  const int64_t end = off[6] + (fmt == 1 ? 12 : 0);
+  off[7] = (end + 255) / 256 * 256;
+  return 0;
+}
+
+// Dequantised matrix `which` (0 gate [I][H], 1 up [I][H], 2 down [H][I]) in
+// float64: w[r][c] = e2m1(code) * block scale (* the matrix scale, NVFP4).
+int or_fp4_blob_matrix(const uint8_t* blob, int H, int I, int which, int fmt, double* out) {
+  int64_t off[8];
+  if (or_fp4_blob_offsets(H, I, fmt, off) || which < 0 || which > 2) return -1;
+  const int rows = which == 2 ? H : I, cols = which == 2 ? I : H;
+  const int B = fmt == 1 ? 16 : 32;
+  const uint8_t* q = blob + off[which];
+  const uint8_t* sc = blob + off[3 + which];
+  double mat = 1.0;
+  if (fmt == 1) {
+    float f;
+    std::memcpy(&f, blob + off[6] + 4 * which, 4);
+    mat = f;
+  }
+  for (int r = 0; r < rows; ++r)
+    for (int c = 0; c < cols; ++c) {
+      const uint8_t byte = q[(int64_t)r * (cols / 2) + c / 2];
+      const int code = (c & 1) ? (byte >> 4) : (byte & 15);
+      const int sb = sc[(int64_t)r * (cols / B) + c / B];
+      const double scale = fmt == 1 ? or_e4m3(sb) * mat : or_e8m0(sb);
+      out[(int64_t)r * cols + c] = or_e2m1(code) * scale;
+    }
+  return 0;
+}
+
+// One FP4 expert on T tokens in float64, the same math as or_expert_forward:
+// g = Wg x, u = Wu x, h = silu(g) * u, y = Wd h, x widened from bf16.
+int or_fp4_expert_forward(const uint8_t* blob, int H, int I, int fmt, const uint16_t* x, int T,
+                          double* y) {
+  std::vector<double> wg((size_t)I * H), wu((size_t)I * H), wd((size_t)H * I);
+  if (or_fp4_blob_matrix(blob, H, I, 0, fmt, wg.data()) ||
+      or_fp4_blob_matrix(blob, H, I, 1, fmt, wu.data()) ||
+      or_fp4_blob_matrix(blob, H, I, 2, fmt, wd.data()))
+    return -1;
+  std::vector<double> xv(H), h(I);
+  for (int t = 0; t < T; ++t) {
+    for (int c = 0; c < H; ++c) xv[c] = bf16_to_float(x[(int64_t)t * H + c]);
+    for (int i = 0; i < I; ++i) {
+      double g = 0.0, u = 0.0;
+      for (int c = 0; c < H; ++c) {
+        g += wg[(size_t)i * H + c] * xv[c];
+        u += wu[(size_t)i * H + c] * xv[c];
+      }
+      h[i] = g / (1.0 + std::exp(-g)) * u;
+    }
+    for (int o = 0; o < H; ++o) {
+      double acc = 0.0;
+      for (int i = 0; i < I; ++i) acc += wd[(size_t)o * I + i] * h[i];
+      y[(int64_t)t * H + o] = acc;
+    }
+  }
+  return 0;
+}
+
 }  // extern "C"
