@@ -544,6 +544,13 @@ def test_full_size_qwen_shape_decode(oracle):
                 assert_ffn_close(y.cpu().numpy(), ref, f"step {step} layer {layer}")
     torch.cuda.synchronize()
     _tables_equal(cache, ost)
+    # every resident slot holds its expert's blob, written by the FFN kernels that
+    # carried the fill (compared on the device)
+    assert m.moe_layer_kernel_count(spec, T) == 4
+    resident = [(v, int(e)) for v, e in enumerate(ost.id_of_slot) if e >= 0]
+    assert resident
+    for v, e in resident:
+        assert torch.equal(cache.pool[v], bank[e]), f"slot {v} (id {e})"
     del bank, cache
     torch.cuda.empty_cache()
 
