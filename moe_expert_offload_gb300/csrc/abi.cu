@@ -133,8 +133,11 @@ moe::CacheArgs cache_args(const moe_spec* spec, moe_cache* c, int32_t layer, con
 }
 
 int do_cache_step(const moe_spec* spec, moe_cache* c, int32_t layer, const int32_t* ids,
-                  int32_t T, moe_plan* plan, int32_t do_fill, cudaStream_t st) {
-  const moe::CacheArgs a = cache_args(spec, c, layer, ids, T, plan);
+                  int32_t T, moe_plan* plan, int32_t do_fill, cudaStream_t st,
+                  uint32_t* zero_words = nullptr, int n_zero = 0) {
+  moe::CacheArgs a = cache_args(spec, c, layer, ids, T, plan);
+  a.zero_words = zero_words;
+  a.n_zero = n_zero;
   cudaError_t e = moe::launch_cache_step(a, st);
   if (e != cudaSuccess) return cuda_fail(e, "cache step launch");
   if (do_fill) {
@@ -194,9 +197,12 @@ std::atomic<int> g_inject_stall{0};
 
 // fuse_fill: the streaming FFN kernels also write F's blobs into their slots
 // (the caller launches no fill copy); only when ffn_fill_fusable holds.
+// ctr_zeroed: the control step launched just before cleared the FFN's counter
+// words (moe_layer_forward); otherwise the FFN launch clears them itself.
 int do_ffn(const moe_spec* spec, const moe_cache* c, int32_t layer, const moe_plan* plan,
            const void* x, int32_t T, const int32_t* ids, const float* weights, const void* shared,
-           void* ws, size_t ws_bytes, float* y, cudaStream_t st, bool fuse_fill = false) {
+           void* ws, size_t ws_bytes, float* y, cudaStream_t st, bool fuse_fill = false,
+           bool ctr_zeroed = false) {
   if (T > moe::kMaxDecodeT) return fail(MOE_EUNSUPPORTED, "decode FFN supports T <= %d",
                                         moe::kMaxDecodeT);
   if (!x || !ids || !weights || !y || !ws) return fail(MOE_EINVAL, "moe_expert_ffn: NULL argument");
@@ -226,6 +232,9 @@ int do_ffn(const moe_spec* spec, const moe_cache* c, int32_t layer, const moe_pl
   a.fill_slots = plan->fill_slots;
   a.fill_fused = fuse_fill ? 1 : 0;
   a.pool_w = static_cast<uint8_t*>(c->slot_pool);
+  a.tab_slot_of_id = c->slot_of_id;
+  a.tab_id_of_slot = c->id_of_slot;
+  a.tab_ts = c->ts;
   a.inject_stall = g_inject_stall.exchange(0);
   a.err = plan->err;
   a.x = static_cast<const uint16_t*>(x);
@@ -234,7 +243,7 @@ int do_ffn(const moe_spec* spec, const moe_cache* c, int32_t layer, const moe_pl
   a.shared = static_cast<const uint8_t*>(shared);
   a.y = y;
   moe::ffn_carve_workspace(a, ws);
-  cudaError_t e = moe::launch_ffn_decode(a, st);
+  cudaError_t e = moe::launch_ffn_decode(a, st, ctr_zeroed);
   if (e != cudaSuccess) return cuda_fail(e, "decode FFN launch");
   return MOE_OK;
 }
@@ -382,8 +391,11 @@ int32_t moe_layer_kernel_count(const moe_spec* spec, int32_t T) {
   const bool fused_sel = T <= moe::kSelFusedMaxT && spec->num_experts <= moe::kSelFusedMaxE;
   const bool fused_fill =
       moe::ffn_fill_fusable(spec->hidden, spec->inter, spec->top_k, T, spec->has_shared);
-  // logits, [select], control step, [fill copy], gate/up, down
-  return 1 + (fused_sel ? 0 : 1) + 1 + (fused_fill ? 0 : 1) + 2;
+  const bool coop =
+      moe::ffn_coop_supported(spec->hidden, spec->inter, spec->top_k, T, spec->has_shared);
+  // logits, [select], control step, [fill copy], FFN (one cooperative kernel, or
+  // gate/up and down)
+  return 1 + (fused_sel ? 0 : 1) + 1 + (fused_fill ? 0 : 1) + (coop ? 1 : 2);
 }
 
 int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, const void* x,
@@ -414,6 +426,16 @@ int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, con
   const bool fused_fill = moe::ffn_fill_fusable(spec->hidden, spec->inter, spec->top_k, T,
                                                 spec->has_shared);
   SideStream* ss = fused_fill ? nullptr : side_stream(st);
+  // the cooperative FFN's counter words, cleared by the control step
+  const bool coop = moe::ffn_coop_supported(spec->hidden, spec->inter, spec->top_k, T,
+                                            spec->has_shared);
+  moe::FfnArgs carve;
+  carve.H = spec->hidden;
+  carve.I = spec->inter;
+  carve.k = spec->top_k;
+  carve.T = T;
+  carve.has_shared = spec->has_shared;
+  moe::ffn_carve_workspace(carve, static_cast<uint8_t*>(workspace) + lbytes);
   if (T <= moe::kSelFusedMaxT && spec->num_experts <= moe::kSelFusedMaxE) {
     // logits kernel, then the selection inside the control step's CTA
     if (!x || !w_router || !ids || !weights) return fail(MOE_EINVAL, "moe_layer_forward: NULL argument");
@@ -423,7 +445,11 @@ int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, con
                                               static_cast<const uint16_t*>(w_router), T,
                                               spec->num_experts, spec->hidden, logits, st);
     if (e != cudaSuccess) return cuda_fail(e, "router logits launch");
-    const moe::CacheArgs a = cache_args(spec, cache, layer, ids, T, plan);
+    moe::CacheArgs a = cache_args(spec, cache, layer, ids, T, plan);
+    if (coop) {
+      a.zero_words = carve.ctr;
+      a.n_zero = carve.n_ctr;
+    }
     moe::SelArgs sa;
     sa.logits = logits;
     sa.bias = bias;
@@ -446,7 +472,8 @@ int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, con
   } else {
     rc = do_route(spec, x, T, w_router, bias, logits, ids, weights, st);
     if (rc) return rc;
-    rc = do_cache_step(spec, cache, layer, ids, T, plan, (ss || fused_fill) ? 0 : 1, st);
+    rc = do_cache_step(spec, cache, layer, ids, T, plan, (ss || fused_fill) ? 0 : 1, st,
+                       coop ? carve.ctr : nullptr, coop ? carve.n_ctr : 0);
     if (rc) return rc;
   }
   if (ss) {  // fill copy beside the FFN
@@ -461,7 +488,7 @@ int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, con
   }
   rc = do_ffn(spec, cache, layer, plan, x, T, ids, weights, shared,
               static_cast<uint8_t*>(workspace) + lbytes, workspace_bytes - lbytes, y, st,
-              fused_fill);
+              fused_fill, coop);
   if (ss) {
     const cudaError_t e = cudaStreamWaitEvent(st, ss->join, 0);
     if (e != cudaSuccess && !rc) return cuda_fail(e, "fill join");

@@ -89,6 +89,9 @@ __global__ void __launch_bounds__(kCtlThreads) cache_step_kernel(CacheArgs a, Se
   griddep_wait();  // routed ids from the previous kernel
 
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  // the counters of the decode FFN that follows (its kernel reads them only
+  // after this grid has completed)
+  for (int i = tid; i < a.n_zero; i += kCtlThreads) a.zero_words[i] = 0u;
   const int n = a.n_ids, E = a.E;
 
   // The victim scan does not depend on the routed ids: the recency stamps of

@@ -578,8 +578,8 @@ cudaError_t raise_smem(Kern kernel, size_t bytes, size_t (&done)[64]) {
 size_t ffn_workspace_bytes(int H, int I, int k, int T, int has_shared) {
   auto al = [](size_t b) { return (b + 255) / 256 * 256; };
   const size_t max_entries = (size_t)T * k + has_shared;
-  const size_t ntick = (H + 15) / 16;  // one arrival counter per 16-row tile of H
-  return al(max_entries * T * I * 4) + al((size_t)T * (k + has_shared) * H * 4) + al(ntick * 4);
+  const size_t nctr = (size_t)ffn_ctr_words(H, (int)max_entries);
+  return al(max_entries * T * I * 4) + al((size_t)T * (k + has_shared) * H * 4) + al(nctr * 4);
 }
 
 void ffn_carve_workspace(FfnArgs& a, void* ws) {
@@ -592,15 +592,26 @@ void ffn_carve_workspace(FfnArgs& a, void* ws) {
   p += al((size_t)a.T * (a.k + a.has_shared) * a.H * 4);
   a.tick = reinterpret_cast<uint32_t*>(p);
   a.max_entries = (int)max_entries;
+  a.ctr = a.tick;
+  a.n_ctr = ffn_ctr_words(a.H, a.max_entries);
 }
 
 bool ffn_fill_fusable(int H, int I, int k, int T, int has_shared) {
   const long max_entries = (long)T * k + has_shared;  // as ffn_carve_workspace
+  if (ffn_coop_supported(H, I, k, T, has_shared)) return true;
   return max_entries <= 128 && ffn_stream_smem(H, T) != SIZE_MAX &&
          ffn_down_stream_smem(H, I, T) != SIZE_MAX;
 }
 
-cudaError_t launch_ffn_decode(const FfnArgs& a, cudaStream_t st) {
+cudaError_t launch_ffn_decode(const FfnArgs& a, cudaStream_t st, bool ctr_zeroed) {
+  if (ffn_coop_supported(a.H, a.I, a.k, a.T, a.has_shared)) {
+    // the cooperative kernel needs its counters at zero
+    if (!ctr_zeroed) {
+      const cudaError_t e = cudaMemsetAsync(a.ctr, 0, (size_t)a.n_ctr * 4, st);
+      if (e != cudaSuccess) return e;
+    }
+    return launch_ffn_coop(a, st);
+  }
   static size_t done_a1[64], done_a2[64], done_b1[64], done_b2[64];
   const int nblk = (a.H + kRowsBlkB - 1) / kRowsBlkB;
   const int grid_a = a.max_entries * (a.I / 16);

@@ -83,6 +83,9 @@ cudaError_t launch_router_select(const moe_spec& sp, const float* logits, const 
 // no_fill (static placement) makes q = 0.
 struct CacheArgs {
   int E = 0, layer = 0, n_ids = 0, S0 = 0, S = 0, K = 0, bp = 0, bh = 0, no_fill = 0;
+  // words the step clears for the decode FFN that follows it (its counters)
+  uint32_t* zero_words = nullptr;
+  int n_zero = 0;
   const int32_t* ids = nullptr;
   int32_t *slot_of_id = nullptr, *id_of_slot = nullptr;
   uint32_t *ts = nullptr, *clock = nullptr;
@@ -137,6 +140,15 @@ struct FfnArgs {
   int max_entries = 0;
   int n_bank = 0;             // blobs in the bank (num_layers * E)
   int n_pool = 0;             // slots in the pool
+  // cooperative decode kernel (ffn_coop.cu): counter words [n_ctr] that must
+  // be zero when the kernel starts (cleared by the control step or by a
+  // memset ahead of the launch), and the cache tables it restores when a
+  // bounded wait gave up while the call carried the step's fills
+  uint32_t* ctr = nullptr;
+  int n_ctr = 0;
+  int32_t* tab_slot_of_id = nullptr;
+  int32_t* tab_id_of_slot = nullptr;
+  uint32_t* tab_ts = nullptr;
 };
 // Where the FFN reads a routed id's weights: its slot when it was cached
 // before this step (H), else in place from the bank (C, and F: an expert being
@@ -174,7 +186,23 @@ __device__ __forceinline__ int32_t ffn_slot(const FfnArgs& a, int32_t id,
 
 size_t ffn_workspace_bytes(int H, int I, int k, int T, int has_shared);
 void ffn_carve_workspace(FfnArgs& a, void* ws);
-cudaError_t launch_ffn_decode(const FfnArgs& a, cudaStream_t st);
+// Counter words at the end of the decode FFN workspace (ffn_carve_workspace
+// points FfnArgs::ctr / n_ctr at them): the arrival counters of the 16-row
+// output tiles, plus the cooperative kernel's per-entry readiness counters
+// and its completion and failure words and per (entry, token) maxima of h.
+inline int ffn_ctr_words(int H, int max_entries) {
+  return (H + 15) / 16 + 9 * max_entries + 4;
+}
+// ctr_zeroed: the counter words are known to be zero (cleared by the control
+// step just before); otherwise a memset clears them ahead of a kernel that
+// needs them.
+cudaError_t launch_ffn_decode(const FfnArgs& a, cudaStream_t st, bool ctr_zeroed = false);
+// The cooperative decode kernel serves this shape: H % 1024 == 0,
+// I % 512 == 0, 1 <= T <= 8, T * k <= 512, T * k + shared <= 128, and its
+// shared-memory plan fits.  Its counters (FfnArgs::ctr) must be zero at
+// launch.
+bool ffn_coop_supported(int H, int I, int k, int T, int has_shared);
+cudaError_t launch_ffn_coop(const FfnArgs& a, cudaStream_t st);
 // Both streaming decode kernels run for this shape, so they can carry the
 // step's fill copy (FfnArgs::fill_fused).
 bool ffn_fill_fusable(int H, int I, int k, int T, int has_shared);

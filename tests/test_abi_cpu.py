@@ -255,8 +255,11 @@ def test_hot_placement_is_best_fixed_set():
 
 def test_layer_kernel_count(L):
     """Host-side launch accounting of moe_layer_forward (no device work)."""
-    assert m.moe_layer_kernel_count(m.make_spec(1, 2048, 512, 256, 8), 1) == 4  # FFN carries fill
-    assert m.moe_layer_kernel_count(m.make_spec(1, 7168, 2048, 256, 8), 8) == 4
+    # logits, control step with the selection, one cooperative FFN kernel carrying the fill
+    assert m.moe_layer_kernel_count(m.make_spec(1, 2048, 512, 256, 8), 1) == 3
+    assert m.moe_layer_kernel_count(m.make_spec(1, 7168, 2048, 256, 8), 8) == 3
+    # I % 512 != 0: the two streaming kernels (gate/up, down) carry the fill
+    assert m.moe_layer_kernel_count(m.make_spec(1, 2048, 256, 256, 8), 1) == 4
     # H = 256 is below the streaming kernels' 512-column tiles: a fill copy kernel runs
     assert m.moe_layer_kernel_count(m.make_spec(1, 256, 128, 16, 2), 1) == 5
     assert m.moe_layer_kernel_count(m.make_spec(1, 256, 128, 300, 2), 1) == 6  # + select

@@ -311,18 +311,32 @@ def test_layer_forward_under_policies(oracle, policy):
 
 
 # --------------------------------------------- fill carried by the decode FFN
+def _ffn_kernels(H, I, T):
+    """FFN launches of a decode layer step: one cooperative kernel where it serves the shape
+    (H % 1024 == 0, I % 512 == 0, T <= 8), else the streaming gate/up and down kernels."""
+    return 1 if (H % 1024 == 0 and I % 512 == 0 and T <= 8) else 2
+
+
 @pytest.mark.parametrize("H,I,E,k,T,shared,S,K", [(1024, 256, 16, 4, 1, True, 6, 3),
                                                   (1024, 256, 16, 4, 3, False, 5, 4),
                                                   (2048, 512, 24, 8, 8, True, 20, 8),
-                                                  (512, 256, 12, 3, 2, True, 4, 2)])
+                                                  (512, 256, 12, 3, 2, True, 4, 2),
+                                                  (1024, 512, 16, 4, 1, True, 6, 3),
+                                                  (1024, 512, 16, 4, 3, False, 5, 4),
+                                                  (2048, 1024, 12, 4, 8, True, 10, 4),
+                                                  (3072, 512, 20, 6, 5, True, 8, 6)])
 def test_layer_forward_fused_fill(oracle, H, I, E, k, T, shared, S, K):
-    """Shapes the streaming FFN serves: the fill copy is written by the FFN kernels as they
-    read F from the bank (no copy kernel).  Plans, outputs and every resident slot's bytes
-    equal the oracle's and the bank's over steps with fills and evictions."""
+    """Shapes the FFN kernels serve with the fill carried: the fill copy is written by the
+    FFN kernels as they read F from the bank (no copy kernel).  Plans, outputs and every
+    resident slot's bytes equal the oracle's and the bank's over steps with fills and
+    evictions.  The shapes cover both FFN paths (cooperative kernel: H % 1024 == 0 and
+    I % 512 == 0), both down-tile geometries of the cooperative kernel (I % 1024 == 0 or
+    not) and gate/up tiles of one, two and three stages."""
     L = 2
     spec, bank, bank_h, cache, sh = _layer_rig(L, H, I, E, k, S, K, 52700, 77300, shared,
                                                seed=H + T)
-    assert m.moe_layer_kernel_count(spec, T) == 4  # logits, control, gate/up, down
+    # logits, control step with the selection, FFN
+    assert m.moe_layer_kernel_count(spec, T) == 2 + _ffn_kernels(H, I, T)
     plan = m.DevicePlan(T * k, K, device=DEV)
     wsb = m.moe_layer_workspace_bytes(spec, T)
     ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
@@ -386,6 +400,63 @@ def test_ffn_wait_timeout_sets_error_and_context_survives(oracle):
     assert int(plan.err[0].item()) == 0
     ref = oracle.moe_ffn(list(bank_h[:E]), H, I, xb, ids_h, wts_h, bank_h[E], I)
     assert_ffn_close(y.cpu().numpy(), ref, "after the stall")
+
+
+def test_wait_timeout_in_layer_step_unmaps_fills(oracle):
+    """A decode layer step whose FFN carries the fill and whose bounded waits run out
+    (injected stall): plan.err gets MOE_DERR_WAIT, and the experts the step filled are
+    unmapped again (their slots may hold a partial copy): slot_of_id = -1, the slot empty,
+    ts 0.  With the same edit applied to the oracle's tables, the following steps match the
+    oracle bit for bit (plans, tables) and within tolerance (outputs), and every resident
+    slot holds its bank blob."""
+    H, I, E, k, T, S, K, L = 1024, 512, 16, 4, 1, 6, 3, 1
+    spec, bank, bank_h, cache, sh = _layer_rig(L, H, I, E, k, S, K, 52700, 77300, True, seed=9)
+    assert m.moe_layer_kernel_count(spec, T) == 3  # the cooperative FFN carries the fill
+    plan = m.DevicePlan(T * k, K, device=DEV)
+    wsb = m.moe_layer_workspace_bytes(spec, T)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    wts = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    y = torch.empty((T, H), dtype=torch.float32, device=DEV)
+    wr_h = synth.router_weights(21, E, H)
+    wr = dev_bits(wr_h, DEV)
+    ost = oracle.CacheState(L * E, S)
+    rng = np.random.default_rng(4)
+    stalled_fills = 0
+    for step in range(8):
+        xb = synth.bf16_bits(rng.normal(0, 1.5, (T, H)))
+        stall = step == 3
+        if stall:
+            m.moe_debug_inject_ffn_stall(True)
+        t0 = time.perf_counter()
+        m.moe_layer_forward(spec, cache.c, 0, dev_bits(xb, DEV), T, wr, None, sh, plan.c, ids,
+                            wts, ws, wsb, y)
+        torch.cuda.synchronize()
+        took = time.perf_counter() - t0
+        oid, ow = oracle.route_softmax_topk(oracle.router_logits(xb, wr_h), k)
+        assert np.array_equal(ids.cpu().numpy(), oid)
+        op = oracle.cache_step(ost, E, 0, oid, K, 52700, 77300)
+        gp = plan.read(K)
+        _plans_equal(gp, op, K)
+        if stall:
+            assert gp["err"] & m.MOE_DERR_WAIT
+            assert 0.5 < took < 30.0, took
+            stalled_fills = op["n_fill"]
+            for f, v in zip(op["fill_ids"][:op["n_fill"]], op["fill_slots"][:op["n_fill"]]):
+                ost.slot_of_id[f] = -1
+                ost.id_of_slot[v] = -1
+                ost.ts[v] = 0
+            plan.err.zero_()
+        else:
+            assert gp["err"] == 0
+            ref = oracle.moe_ffn(list(bank_h[:E]), H, I, xb, oid, ow, bank_h[E], I)
+            assert_ffn_close(y.cpu().numpy(), ref, f"step {step}")
+        _tables_equal(cache, ost)
+        pool = cache.pool.cpu().numpy()
+        for slot, eid in enumerate(ost.id_of_slot):
+            if eid >= 0:
+                assert np.array_equal(pool[slot], bank_h[eid]), f"step {step} slot {slot}"
+    assert stalled_fills > 0, "the stalled step filled nothing: pick another seed"
 
 
 # ------------------------------------------------------- fill + expert FFN
@@ -513,7 +584,8 @@ def test_expert_ffn_direct_and_cached(oracle, H, I, E, k, T, shared):
 
 def test_full_size_qwen_shape_decode(oracle):
     """40 layers x 256 experts (18.1 GB bank), 2560 slots, shared expert, T=1:
-    several decode steps over all layers, sampled layers checked against the oracle."""
+    four decode steps over all layers; layers 0, 17 and 39 checked against the oracle on
+    every step, all 40 layers on the last step."""
     L, H, I, E, k, S, K, T = 40, 2048, 512, 256, 8, 2560, 8, 1
     spec, bank, _, cache, sh = _layer_rig(L, H, I, E, k, S, K, 52700, 77300, True, big=True)
     wr_h = [synth.router_weights(100 + l, E, H) for l in range(L)]
@@ -534,7 +606,7 @@ def test_full_size_qwen_shape_decode(oracle):
                                 plan.c, ids, wts, ws, wsb, y)
             oid, ow = oracle.route_softmax_topk(oracle.router_logits(xb, wr_h[layer]), k)
             op = oracle.cache_step(ost, E, layer, oid, K, 52700, 77300)
-            if layer in (0, 17, 39):
+            if layer in (0, 17, 39) or step == 3:  # every layer on the last step
                 torch.cuda.synchronize()
                 assert np.array_equal(ids.cpu().numpy(), oid)
                 _plans_equal(plan.read(K), op, K)
@@ -544,9 +616,9 @@ def test_full_size_qwen_shape_decode(oracle):
                 assert_ffn_close(y.cpu().numpy(), ref, f"step {step} layer {layer}")
     torch.cuda.synchronize()
     _tables_equal(cache, ost)
-    # every resident slot holds its expert's blob, written by the FFN kernels that
+    # every resident slot holds its expert's blob, written by the FFN kernel that
     # carried the fill (compared on the device)
-    assert m.moe_layer_kernel_count(spec, T) == 4
+    assert m.moe_layer_kernel_count(spec, T) == 2 + _ffn_kernels(H, I, T)
     resident = [(v, int(e)) for v, e in enumerate(ost.id_of_slot) if e >= 0]
     assert resident
     for v, e in resident:
@@ -597,9 +669,9 @@ def test_full_size_deepseek_shape_decode(oracle, T):
                 assert_ffn_close(y.cpu().numpy()[toks], ref, f"layer {layer}")
     torch.cuda.synchronize()
     _tables_equal(cache, ost)
-    # every resident slot holds its expert's blob, written by the FFN kernels that
+    # every resident slot holds its expert's blob, written by the FFN kernel that
     # carried the fill (compared on the device: 24.8 MB per slot)
-    assert m.moe_layer_kernel_count(spec, T) == 4
+    assert m.moe_layer_kernel_count(spec, T) == 2 + _ffn_kernels(H, I, T)
     resident = [(v, int(e)) for v, e in enumerate(ost.id_of_slot) if e >= 0]
     assert resident
     for v, e in resident:
@@ -635,7 +707,7 @@ def test_expert_ffn_repeated_ids(oracle, H, I, T):
         assert_ffn_close(y.cpu().numpy(), ref, f"step {step}")
 
 
-@pytest.mark.parametrize("H,I", [(1024, 256), (256, 128)])
+@pytest.mark.parametrize("H,I", [(1024, 256), (256, 128), (1024, 512)])
 def test_expert_ffn_no_valid_expert_writes_zero(oracle, H, I):
     """Every routed id out of range and no shared expert: the control step flags
     the ids, nothing executes, and y is all zeros (stale contents are replaced)."""
