@@ -74,6 +74,34 @@ WORKLOADS = {
 }
 
 
+def run_config(args, w, world):
+    """The `config` object of a bench line; the same for the GPU arm and the
+    reference arm of a workload."""
+    par = f"replicas x{world}" if world > 1 else "single GPU"
+    if w.get("prefill"):
+        return {"workload": args.workload, "desc": w["desc"], "tokens": w["T"], "layers": w["L"],
+                "parallelism": par,
+                "l2": "inputs larger than L2: 453 MB of int4 experts per layer + 32 MB x"}
+    if w.get("sweep"):
+        return {"workload": args.workload, "desc": w["desc"], "layers": w["L"],
+                "headline_point": "capacity 25%, B_P/B_H 52.7/77.3", "parallelism": par,
+                "l2": "integer tables (<1 MB) stay in L2; this is a latency measurement"}
+    se = 27 * w["H"] * w["I"] // 16  # int4 blob bytes (codes + bf16 scales / biases)
+    per_layer = min(w["T"] * w["k"], w["E"]) + (1 if w["shared"] else 0)
+    return {"workload": args.workload, "desc": w["desc"], "layers": w["L"], "batch": w["T"],
+            "parallelism": par,
+            "l2": f"inputs larger than L2: up to {per_layer * se * w['L'] / 1e6:.0f} MB of expert "
+                  "weights touched per step vs 129 MB L2"}
+
+
+def host_cores():
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -202,8 +230,9 @@ def spec_of(w):
 
 # --------------------------------------------------------------- CPU oracle
 class OracleRunner:
-    """Times the CPU oracle (single thread) on the same workload.  Expert blobs
-    are generated on the host on first use (untimed); only oracle calls count."""
+    """Times the CPU oracle on the same workload (its row loops on
+    oracle.set_threads() host threads).  Expert blobs are generated on the host
+    on first use (untimed); only oracle calls count."""
 
     def __init__(self, w, xs, wr, bias):
         import oracle
@@ -249,23 +278,41 @@ class OracleRunner:
         self.tokens += w["T"]
 
 
-def cpu_baseline(w, xs, wr, bias, budget_s=12.0, max_steps=64):
-    r = OracleRunner(w, xs, wr, bias)
-    s = 0
-    while s < min(max_steps, xs.shape[0]) and (r.spent < budget_s or s == 0):
-        r.step(s)
-        s += 1
-    return {"value": r.tokens / r.spent, "unit": "tok/s", "cores": 1, "kind": "oracle",
-            "sample": f"{s} decode steps x {w['L']} layers x batch {w['T']} (route, control, "
-                      f"float64 FFN) in {r.spent:.1f} s of oracle time, single thread"}
+def cpu_baseline(w, xs, wr, bias, budget_s=8.0, max_steps=64):
+    """The oracle on a bounded sample of the workload, twice: on one thread (the
+    oracle as it stands) and with its row loops on every host core (the same
+    arithmetic and results)."""
+    import oracle
+
+    oracle.build()
+    ncores = host_cores()
+
+    def run(threads):
+        used = oracle.set_threads(threads)
+        r = OracleRunner(w, xs, wr, bias)
+        s = 0
+        while s < min(max_steps, xs.shape[0]) and (r.spent < budget_s or s == 0):
+            r.step(s)
+            s += 1
+        oracle.set_threads(1)
+        return r.tokens / r.spent, used, (f"{s} decode steps x {w['L']} layers x batch {w['T']} "
+                                          f"(route, control, float64 FFN) in {r.spent:.1f} s of "
+                                          f"oracle time, {used} thread(s)")
+
+    v1, _, s1 = run(1)
+    vn, used, sn = run(ncores)
+    return {"value": v1, "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": s1,
+            "host_cores": ncores,
+            "all_cores": {"value": vn, "unit": "tok/s", "cores": used,
+                          "kind": "oracle, row loops on every host core", "sample": sn}}
 
 
-def reference_line(args, w, world, val, unit, spent, sample, dtype):
+def reference_line(args, w, world, val, unit, spent, sample, dtype, cores=1):
     return {"impl": "reference", "metric": METRIC, "value": val, "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * spent / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
-            "data": "synthetic", "config": {"workload": args.workload, "desc": w["desc"]},
-            "cpu_baseline": {"value": val, "unit": unit, "cores": 1, "kind": "oracle",
+            "data": "synthetic", "config": run_config(args, w, world),
+            "cpu_baseline": {"value": val, "unit": unit, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -273,7 +320,11 @@ def reference_line(args, w, world, val, unit, spent, sample, dtype):
 def run_reference_prefill(args, w, world):
     """Each step is one token of the prefill layer through the oracle (route +
     float64 FFN, the token's experts dequantised per call): a bounded sample."""
+    import oracle
+
     x_h, wr_h = prefill_inputs(w)
+    oracle.build()
+    used = oracle.set_threads(host_cores())
     r = PrefillOracle(w, x_h, wr_h)
     for t in range(args.warmup):
         r.token(t)
@@ -281,10 +332,10 @@ def run_reference_prefill(args, w, world):
     for t in range(args.warmup, args.warmup + args.steps):
         r.token(t % w["T"])
     val = r.flops_per_token * r.n / r.spent / 1e12
-    sample = (f"{r.n} tokens of the {w['T']}-token prefill layer (route + float64 FFN), "
-              f"single thread, {r.spent:.1f} s of oracle time")
-    print(json.dumps(reference_line(args, w, world, val, "TFLOP/s", r.spent, sample, "f64")),
-          flush=True)
+    sample = (f"{r.n} tokens of the {w['T']}-token prefill layer (route + float64 FFN, row loops "
+              f"on {used} host thread(s)), {r.spent:.1f} s of oracle time")
+    print(json.dumps(reference_line(args, w, world, val, "TFLOP/s", r.spent, sample, "f64",
+                                    cores=used)), flush=True)
 
 
 def run_reference_sweep(args, w, world):
@@ -320,8 +371,12 @@ def run_reference(args, w, rank, world):
         return run_reference_prefill(args, w, world)
     if w.get("sweep"):
         return run_reference_sweep(args, w, world)
+    import oracle
+
     n = args.warmup + args.steps
     xs, wr, bias = make_inputs(w, n)
+    oracle.build()
+    used = oracle.set_threads(host_cores())
     r = OracleRunner(w, xs, wr, bias)
     for s in range(args.warmup):
         r.step(s)
@@ -330,9 +385,9 @@ def run_reference(args, w, rank, world):
         r.step(s)
     val = r.tokens / r.spent
     sample = (f"{args.steps} decode steps x {w['L']} layers x batch {w['T']} (route, control, "
-              f"float64 FFN), single thread, {r.spent:.1f} s of oracle time")
-    print(json.dumps(reference_line(args, w, world, val, "tok/s", r.spent, sample, "f64")),
-          flush=True)
+              f"float64 FFN, row loops on {used} host thread(s)), {r.spent:.1f} s of oracle time")
+    print(json.dumps(reference_line(args, w, world, val, "tok/s", r.spent, sample, "f64",
+                                    cores=used)), flush=True)
 
 
 # ----------------------------------------------------------------- GPU arm
@@ -421,11 +476,19 @@ def run_gpu(args, w, rank, world, local_rank):
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     barrier()
+    # The timed region is the one replay of the K steps.  The clock sampler runs
+    # from before it until the GPU has been kept busy for >= 1 s by untimed
+    # replays of the same graph after it, so that the clock record reflects the
+    # sustained state of this load (a K-step region alone can be a few ms).
     with ClockSampler(local_rank) as clk:
         t_start.record(stream)
         graph.replay()
         t_end.record(stream)
         torch.cuda.synchronize()
+        soak_t0 = time.perf_counter()
+        while time.perf_counter() - soak_t0 < 1.0:
+            graph.replay()
+            torch.cuda.synchronize()
     barrier()
     ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     del graph
@@ -467,10 +530,12 @@ def run_gpu(args, w, rank, world, local_rank):
             n_direct += int(c[5])
     layer_steps = stat_steps * L
 
-    # end to end through the public API: pinned host hidden states -> device,
-    # the 40 moe_layer_forward calls (one captured graph), layer outputs ->
-    # pinned host, every step, no host sync inside the timed region.
-    x_host = torch.from_numpy(xs_h[args.warmup + args.steps:].view(np.int16).copy()).pin_memory()
+    # end to end through the public API, on the timed steps' own inputs and from
+    # the same cache state (reset, then the warm-up steps): pinned host hidden
+    # states -> device, the layers' moe_layer_forward calls (one captured graph),
+    # layer outputs -> pinned host, every step, no host sync in the timed region.
+    x_host = torch.from_numpy(
+        xs_h[args.warmup:args.warmup + args.steps].view(np.int16).copy()).pin_memory()
     y_host = torch.empty((args.steps, L, T, H), dtype=torch.float32).pin_memory()
     x_dev = torch.empty((L, T, H), dtype=torch.int16, device=dev)
 
@@ -491,8 +556,9 @@ def run_gpu(args, w, rank, world, local_rank):
         g1.replay()
         y_host[s].copy_(y, non_blocking=True)
 
-    for s in range(min(args.warmup, args.steps)):
-        e2e_step(s)
+    m.moe_cache_reset(spec, cache.c, sp)
+    for s in range(args.warmup):
+        step(s)
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -514,7 +580,8 @@ def run_gpu(args, w, rank, world, local_rank):
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
             "frac": achieved / hbm,
             "traffic": ncu_traffic(args.workload, n_uniq / layer_steps + (1 if w["shared"] else 0)),
-            "kernel": "decode expert FFN (gate/up + down launches of moe_expert_ffn)",
+            "kernel": "decode expert FFN (moe_expert_ffn: counter memset + one cooperative "
+                      "gate/up + down kernel)",
             "algorithmic_bytes_per_launch": ffn_bytes, "avg_launch_us": ffn_avg_s * 1e6,
             "peak_kind": peak_kind, "timing": ffn_timing}
     cpu = cpu_baseline(w, xs_h, wr_h, bias_h) if world == 1 and not args.no_cpu else None
@@ -522,15 +589,15 @@ def run_gpu(args, w, rank, world, local_rank):
     # separate select kernel), gate/up, down (+ a fill copy kernel for shapes whose FFN
     # does not carry the fill); the library reports the count for the shape
     launches_per_layer = m.moe_layer_kernel_count(spec, T)
+    # the FFN carries the fill when no copy kernel is counted: logits, control, FFN
+    # (+ a separate selection kernel past 16 tokens or 256 experts)
+    fused = launches_per_layer == 3 + (0 if T <= 16 and E <= 256 else 1)
     out = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": args.workload, "desc": w["desc"], "layers": L, "batch": T,
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": f"inputs larger than L2: ~{(n_uniq / layer_steps + w['shared']) * se * L / 1e6:.0f} MB "
-                         "of expert weights touched per step vs 129 MB L2"},
+        "config": run_config(args, w, world),
         "roofline": roof,
         "e2e": {"value": tokens / (ms_e2e * 1e-3), "unit": "tok/s",
                 "h2d_bytes_per_step": L * T * H * 2, "d2h_bytes_per_step": L * T * H * 4},
@@ -545,7 +612,10 @@ def run_gpu(args, w, rank, world, local_rank):
                   "direct_per_layer": n_direct / layer_steps,
                   "uniq_per_layer": n_uniq / layer_steps},
         "ffn_gbs": achieved,
-        "step_gbs": (ffn_bytes + 2 * se * n_fill / layer_steps) * L / (ms * 1e-3 / args.steps) / 1e9,
+        # a fill carried by the FFN writes the slot (S_e) and reads nothing extra; a
+        # fill copy kernel reads and writes (2 S_e)
+        "step_gbs": (ffn_bytes + (1 if fused else 2) * se * n_fill / layer_steps) * L /
+                    (ms * 1e-3 / args.steps) / 1e9,
     }
     if cpu:
         out["cpu_baseline"] = cpu
@@ -635,6 +705,15 @@ def run_prefill(args, w, rank, world, local_rank):
     rank_barrier(world)
     with ClockSampler(local_rank) as clk:
         ms, evs = timed(step_overlap, args.steps, True)
+        # untimed steps after the timed ones keep the GPU busy for >= 1 s, so that
+        # the clock record reflects the sustained state of this load
+        soak_t0, s = time.perf_counter(), args.steps
+        while time.perf_counter() - soak_t0 < 1.0:
+            step_overlap(s)
+            s += 1
+            if s % 8 == 0:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
     ms = max_over_ranks(ms, world, dev)
     route_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     ffn_ms = max_over_ranks(statistics.mean(e[1].elapsed_time(e[2]) for e in evs), world, dev)
@@ -689,8 +768,7 @@ def run_prefill(args, w, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": args.workload, "desc": w["desc"], "tokens": T, "layers": L,
-                   "l2": "inputs larger than L2: 453 MB of int4 experts per layer + 32 MB x"},
+        "config": run_config(args, w, world),
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": tflops / peak, "traffic": None,
                      "kernel": "prefill expert FFN (moe_expert_ffn_prefill: permute, 2 grouped "
@@ -754,18 +832,33 @@ class PrefillOracle:
         self.n += 1
 
 
-def cpu_baseline_prefill(w, x_h, wr_h, budget_s=12.0):
-    """The oracle (single thread) on a bounded sample of the prefill layer: successive
-    tokens until the budget is spent; reported as TFLOP/s."""
-    r = PrefillOracle(w, x_h, wr_h)
-    t = 0
-    while r.spent < budget_s and t < w["T"]:
-        r.token(t)
-        t += 1
-    return {"value": r.flops_per_token * r.n / r.spent / 1e12, "unit": "TFLOP/s", "cores": 1,
-            "kind": "oracle",
-            "sample": f"{r.n} prefill tokens (route + float64 FFN, experts dequantised per call) "
-                      f"in {r.spent:.1f} s, single thread"}
+def cpu_baseline_prefill(w, x_h, wr_h, budget_s=8.0):
+    """The oracle on a bounded sample of the prefill layer (successive tokens until
+    the budget is spent; TFLOP/s), on one thread and with its row loops on every
+    host core (the same arithmetic and results)."""
+    import oracle
+
+    oracle.build()
+    ncores = host_cores()
+
+    def run(threads):
+        used = oracle.set_threads(threads)
+        r = PrefillOracle(w, x_h, wr_h)
+        t = 0
+        while r.spent < budget_s and t < w["T"]:
+            r.token(t)
+            t += 1
+        oracle.set_threads(1)
+        return (r.flops_per_token * r.n / r.spent / 1e12, used,
+                f"{r.n} prefill tokens (route + float64 FFN, experts dequantised per call) in "
+                f"{r.spent:.1f} s, {used} thread(s)")
+
+    v1, _, s1 = run(1)
+    vn, used, sn = run(ncores)
+    return {"value": v1, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": s1,
+            "host_cores": ncores,
+            "all_cores": {"value": vn, "unit": "TFLOP/s", "cores": used,
+                          "kind": "oracle, row loops on every host core", "sample": sn}}
 
 
 # ------------------------------------------------------------- cache sweep
@@ -884,10 +977,7 @@ def run_sweep(args, w, rank, world, local_rank):
         "n_gpus": world, "steps": n, "warmup": 1, "ms_per_step": ms / n,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
         "data": "synthetic",
-        "config": {"workload": args.workload, "desc": w["desc"], "layers": L,
-                   "headline_point": "capacity 25%, B_P/B_H 52.7/77.3",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "integer tables (<1 MB) stay in L2; this is a latency measurement"},
+        "config": run_config(args, w, world),
         "roofline": {"bound": "hbm", "achieved": scan / t_call / 1e9, "peak": hbm, "unit": "GB/s",
                      "frac": scan / t_call / 1e9 / hbm, "traffic": None,
                      "kernel": "control step (one CTA, latency-bound)", "peak_kind": peak_kind,
@@ -972,7 +1062,9 @@ def cpu_baseline_sweep(w, tr_h, budget_s=10.0):
         s += 1
     return {"value": calls / spent, "unit": "layer-steps/s", "cores": 1, "kind": "oracle",
             "sample": f"{s} trace steps x {L} layers at capacity 25%, B_P/B_H 52.7/77.3 in "
-                      f"{spent:.1f} s, single thread"}
+                      f"{spent:.1f} s, single thread (each control step depends on the last: "
+                      "no multi-core variant)",
+            "host_cores": host_cores()}
 
 
 def main():

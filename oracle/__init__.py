@@ -20,11 +20,16 @@ _lib = None
 
 
 def build(force: bool = False) -> str:
-    """Compile liboracle.so next to its source (plain g++, no fast-math)."""
+    """Compile liboracle.so next to its source (plain g++, no fast-math; with
+    OpenMP for the optional multi-threaded row loops when the compiler has it)."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(["g++", "-std=c++17", "-O2", "-ffp-contract=off", "-fPIC",
-                               "-shared", "-o", tmp, _SRC])
+        base = ["g++", "-std=c++17", "-O2", "-ffp-contract=off", "-fPIC", "-shared"]
+        try:
+            subprocess.check_call(base + ["-fopenmp", "-o", tmp, _SRC],
+                                  stderr=subprocess.DEVNULL)
+        except subprocess.CalledProcessError:
+            subprocess.check_call(base + ["-o", tmp, _SRC])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -73,6 +78,8 @@ def lib():
         L.or_fp4_expert_forward.restype = i32
         L.or_fp4_expert_forward.argtypes = [vp, i32, i32, i32, vp, i32, vp]
         L.or_moe_ffn.argtypes = [vp, i32, i32, i32, vp, i32, vp, vp, i32, vp, i32, vp]
+        L.or_set_threads.restype = i32
+        L.or_set_threads.argtypes = [i32]
         _lib = L
     return _lib
 
@@ -290,3 +297,9 @@ def fp4_expert_forward(blob: np.ndarray, H: int, I: int, fmt: int, x_bits: np.nd
     if lib().or_fp4_expert_forward(_vp(blob), H, I, fmt, _vp(x_bits), x_bits.shape[0], _vp(y)):
         raise ValueError("fp4_expert_forward: bad arguments")
     return y
+
+
+def set_threads(n: int) -> int:
+    """Host threads for the oracle's row loops (dequantisation, float64 expert);
+    returns the count in effect (1 without OpenMP).  Results do not depend on it."""
+    return int(lib().or_set_threads(int(n)))

@@ -35,7 +35,13 @@
 // Parity status: every function below is pinned by the not-gpu tests
 // (worked examples from the pages, closed forms, brute force, float64).
 //
-// Build: g++ -std=c++17 -O2 -ffp-contract=off -fPIC -shared (no -ffast-math).
+// Threads: or_set_threads(n) lets the row loops of the dequantisation and of
+// the float64 expert run on n host threads (OpenMP when built with -fopenmp).
+// Each output row is computed by one thread in the same order as with one
+// thread, so the results are identical bit for bit; the default is one thread.
+//
+// Build: g++ -std=c++17 -O2 -ffp-contract=off -fPIC -shared [-fopenmp]
+// (no -ffast-math).
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
@@ -45,6 +51,7 @@
 namespace {
 
 const int kGroup = 64;
+int g_threads = 1;  // host threads for the row loops (or_set_threads)
 
 float bf16_to_float(uint16_t b) {
   uint32_t u = (uint32_t)b << 16;
@@ -106,6 +113,18 @@ float weight_at(const uint8_t* codes, const uint16_t* s, const uint16_t* b, int6
 
 extern "C" {
 
+// Host threads for the row loops (n >= 1); returns the count now in effect
+// (1 when the library was built without OpenMP).
+int or_set_threads(int n) {
+#ifdef _OPENMP
+  g_threads = n < 1 ? 1 : n;
+#else
+  (void)n;
+  g_threads = 1;
+#endif
+  return g_threads;
+}
+
 // ------------------------------------------------------------------ layout
 int64_t or_expert_bytes(int H, int I) {
   if (H <= 0 || I <= 0 || H % kGroup || I % kGroup) return -1;
@@ -124,6 +143,7 @@ void or_blob_offsets(int H, int I, int64_t* off) {
 // and a bias per group.  out[r][c] = s[r][c/64] * q[r][c] + b[r][c/64].
 void or_dequant(const uint8_t* codes, const uint16_t* s, const uint16_t* b, int rows, int cols,
                 float* out) {
+#pragma omp parallel for schedule(static) num_threads(g_threads) if (g_threads > 1)
   for (int64_t r = 0; r < rows; ++r)
     for (int64_t c = 0; c < cols; ++c) out[r * cols + c] = weight_at(codes, s, b, cols, r, c);
 }
@@ -482,6 +502,7 @@ void dense_forward(const DenseExpert& d, const uint16_t* x, double* y) {
   const int H = d.H, I = d.I;
   std::vector<double> xv(H), h(I);
   for (int c = 0; c < H; ++c) xv[c] = bf16_to_float(x[c]);
+#pragma omp parallel for schedule(static) num_threads(g_threads) if (g_threads > 1)
   for (int i = 0; i < I; ++i) {
     double g = 0.0, u = 0.0;
     for (int c = 0; c < H; ++c) {
@@ -491,6 +512,7 @@ void dense_forward(const DenseExpert& d, const uint16_t* x, double* y) {
     double silu = g / (1.0 + std::exp(-g));
     h[i] = silu * u;
   }
+#pragma omp parallel for schedule(static) num_threads(g_threads) if (g_threads > 1)
   for (int o = 0; o < H; ++o) {
     double acc = 0.0;
     for (int i = 0; i < I; ++i) acc += (double)d.wd[(size_t)o * I + i] * h[i];

@@ -603,3 +603,28 @@ def test_moe_ffn_is_weighted_sum_plus_shared(oracle):
     # shared expert alone: zero routing weights
     y0 = oracle.moe_ffn(bank[:E], H, I, xb, ids, np.zeros_like(w), shared_blob=bank[E], shared_I=I)
     assert np.allclose(y0, oracle.expert_forward(bank[E], H, I, xb), rtol=1e-12, atol=1e-12)
+
+
+def test_threaded_row_loops_give_identical_bits(oracle):
+    """The timed all-cores baseline runs the oracle's row loops on several host
+    threads; every output row is still one thread's sum in the same order, so the
+    dequantised matrices and the float64 outputs equal the one-thread results."""
+    H, I, E = 256, 128, 6
+    bank = synth.make_bank(E + 1, H, I, seed=21)
+    rng = np.random.default_rng(9)
+    xb = synth.bf16_bits(rng.normal(0, 1, (2, H)))
+    ids = np.array([[4, 1, 0], [2, 2, 5]], np.int32)
+    w = np.array([[0.5, 0.3, 0.2], [0.6, 0.1, 0.3]], np.float32)
+    try:
+        oracle.set_threads(1)
+        y1 = oracle.moe_ffn(bank[:E], H, I, xb, ids, w, shared_blob=bank[E], shared_I=I)
+        d1 = [oracle.blob_matrix(bank[3], H, I, m) for m in range(3)]
+        n = oracle.set_threads(4)
+        yn = oracle.moe_ffn(bank[:E], H, I, xb, ids, w, shared_blob=bank[E], shared_I=I)
+        dn = [oracle.blob_matrix(bank[3], H, I, m) for m in range(3)]
+    finally:
+        oracle.set_threads(1)
+    assert n in (1, 4)
+    assert np.array_equal(y1.view(np.uint64), yn.view(np.uint64))
+    for a, b in zip(d1, dn):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
