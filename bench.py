@@ -130,7 +130,8 @@ def rank_barrier(world):
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("ffn_decode.cu", "ffn_stream.cu", "stream_common.cuh", "moe_internal.cuh"):
+    for f in ("ffn_coop.cu", "control_common.cuh", "route_select.cuh", "stream_common.cuh",
+              "moe_internal.cuh"):
         h.update(open(os.path.join(ROOT, "moe_expert_offload_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -436,16 +437,23 @@ def run_gpu(args, w, rank, world, local_rank):
             ev[1].record(torch.cuda.current_stream())
 
     lws = m.moe_layer_workspace_bytes(spec, T)
+    # the whole layer step is one cooperative kernel for this shape (the cache has sync words)
+    one_kernel = m.moe_layer_kernel_count(spec, cache.c, T) == 1
 
     def step(s, ev=None):
         # the timed step: one moe_layer_forward per layer (route, control, FFN
-        # carrying the fill copy); with events, the same work as separate calls
-        # (FFN, fill copy kernel) so that the FFN launches can be bracketed
+        # carrying the fill copy).  With events: around each layer call when the
+        # step is one kernel, else the same work as separate calls so that the
+        # FFN launches can be bracketed
         sh = torch.cuda.current_stream().cuda_stream
         for l in range(L):
-            if ev is None:
+            if ev is None or one_kernel:
+                if ev is not None:
+                    ev[l][0].record(torch.cuda.current_stream())
                 m.moe_layer_forward(spec, cache.c, l, xs[s, l], T, wr[l], bias_l(l), shared,
                                     plan.c, ids, wts, ws, lws, y[l], sh)
+                if ev is not None:
+                    ev[l][1].record(torch.cuda.current_stream())
             else:
                 layer(xs[s, l], l, sh, ev[l])
 
@@ -493,8 +501,9 @@ def run_gpu(args, w, rank, world, local_rank):
     ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     del graph
 
-    # Per-launch FFN duration for the roofline: a second graph of the same
-    # steps with timing events around every FFN launch (event nodes sit
+    # Per-launch duration of the dominant kernel for the roofline (the layer
+    # kernel, or the FFN kernel of the multi-kernel form): a second graph of the
+    # same steps with timing events around every such launch (event nodes sit
     # between kernels, so this graph is replayed outside the timed region).
     ev_steps = min(args.steps, 16)
     try:
@@ -509,8 +518,8 @@ def run_gpu(args, w, rank, world, local_rank):
         torch.cuda.synchronize()
         ffn_ms = [evs[s][l][0].elapsed_time(evs[s][l][1]) for s in range(ev_steps)
                   for l in range(L)]
-        ffn_timing = (f"CUDA events around every FFN launch, {ev_steps} steps replayed as a graph "
-                      "outside the timed region")
+        ffn_timing = (f"CUDA events around every {'layer' if one_kernel else 'FFN'} launch, "
+                      f"{ev_steps} steps replayed as a graph outside the timed region")
         del g_ev
     except TypeError:
         ffn_ms = []
@@ -522,7 +531,8 @@ def run_gpu(args, w, rank, world, local_rank):
     stat_steps = min(args.steps, 16)
     for s in range(stat_steps):
         for l in range(L):
-            layer(xs[args.warmup + args.steps + s, l], l, sp)
+            m.moe_layer_forward(spec, cache.c, l, xs[args.warmup + args.steps + s, l], T, wr[l],
+                                bias_l(l), shared, plan.c, ids, wts, ws, lws, y[l], sp)
             c = plan.counts.cpu().numpy()
             n_uniq += int(c[0])
             n_miss += int(c[2])
@@ -574,24 +584,30 @@ def run_gpu(args, w, rank, world, local_rank):
         return
     hbm, _, peak_kind = peaks()
     ffn_bytes = (n_uniq / layer_steps + (1 if w["shared"] else 0)) * se  # per FFN launch
+    if one_kernel:
+        # the layer kernel also reads the router weights and writes the fills
+        ffn_bytes += E * H * 2 + (n_fill / layer_steps) * se
     achieved = ffn_bytes / ffn_avg_s / 1e9
     tokens = args.steps * T * world
     value = tokens / (ms * 1e-3)
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
             "frac": achieved / hbm,
             "traffic": ncu_traffic(args.workload, n_uniq / layer_steps + (1 if w["shared"] else 0)),
-            "kernel": "decode expert FFN (moe_expert_ffn: counter memset + one cooperative "
-                      "gate/up + down kernel)",
+            "kernel": ("decode layer step (moe_layer_forward as one cooperative kernel: router "
+                       "logits, selection, control step, gate/up + down carrying the fill)"
+                       if one_kernel else
+                       "decode expert FFN (moe_expert_ffn: counter memset + one cooperative "
+                       "gate/up + down kernel)"),
             "algorithmic_bytes_per_launch": ffn_bytes, "avg_launch_us": ffn_avg_s * 1e6,
             "peak_kind": peak_kind, "timing": ffn_timing}
     cpu = cpu_baseline(w, xs_h, wr_h, bias_h) if world == 1 and not args.no_cpu else None
     # moe_layer_forward: logits, control step (+ selection for T <= 16, E <= 256, else a
     # separate select kernel), gate/up, down (+ a fill copy kernel for shapes whose FFN
     # does not carry the fill); the library reports the count for the shape
-    launches_per_layer = m.moe_layer_kernel_count(spec, T)
-    # the FFN carries the fill when no copy kernel is counted: logits, control, FFN
-    # (+ a separate selection kernel past 16 tokens or 256 experts)
-    fused = launches_per_layer == 3 + (0 if T <= 16 and E <= 256 else 1)
+    launches_per_layer = m.moe_layer_kernel_count(spec, cache.c, T)
+    # the FFN carries the fill when no copy kernel is counted: one kernel, or logits,
+    # control, FFN (+ a separate selection kernel past 16 tokens or 256 experts)
+    fused = launches_per_layer in (1, 3 + (0 if T <= 16 and E <= 256 else 1))
     out = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,

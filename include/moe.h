@@ -127,7 +127,15 @@ typedef struct moe_cache {
   void* slot_pool;     /* device [S * S_e] bytes, 16-byte aligned */
   const void* bank;    /* device [L * E * S_e] bytes, 16-byte aligned */
   int32_t policy;      /* MOE_POLICY_*; MOE_POLICY_LAYER_LRU needs S >= L */
+  uint32_t* sync;      /* device [MOE_CACHE_SYNC_WORDS] or NULL: words the one-kernel decode
+                          layer step (moe_layer_forward) uses to coordinate its CTAs.  They
+                          must be zero before the first step: moe_cache_reset and
+                          moe_cache_place clear them, and every step leaves them zero.  With
+                          NULL, moe_layer_forward runs its multi-kernel form. */
 } moe_cache;
+
+/* Words behind moe_cache.sync (16 KB; 4-byte aligned). */
+#define MOE_CACHE_SYNC_WORDS 4096
 
 /* Fixed-shape step buffers with device-side valid counts (FreeToken summary
  * "novelty": routing-dependent control kept as data).  All device pointers,
@@ -281,9 +289,10 @@ int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, con
  * usable and the next call runs normally.  Returns MOE_OK. */
 int moe_debug_inject_ffn_stall(int32_t on);
 
-/* Kernels one moe_layer_forward call launches for T tokens (for graph sizing
- * and launch accounting); 0 for an invalid spec or T outside 1..64. */
-int32_t moe_layer_kernel_count(const moe_spec* spec, int32_t T);
+/* Kernels one moe_layer_forward call on `cache` launches for T tokens (for
+ * graph sizing and launch accounting); 0 for an invalid spec, a NULL cache or
+ * T outside 1..64. */
+int32_t moe_layer_kernel_count(const moe_spec* spec, const moe_cache* cache, int32_t T);
 
 /* ------------------------------------------------------------------------
  * Prefill (FreeToken summary "method steps": the GPU computes layer l from

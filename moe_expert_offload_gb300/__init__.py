@@ -55,7 +55,11 @@ class MoeCache(C.Structure):
     _fields_ = [("num_slots", C.c_int32), ("k_victims", C.c_int32), ("bp_mbps", C.c_int32),
                 ("bh_mbps", C.c_int32), ("slot_of_id", C.c_void_p), ("id_of_slot", C.c_void_p),
                 ("ts", C.c_void_p), ("clock", C.c_void_p), ("slot_pool", C.c_void_p),
-                ("bank", C.c_void_p), ("policy", C.c_int32)]
+                ("bank", C.c_void_p), ("policy", C.c_int32), ("sync", C.c_void_p)]
+
+
+# words behind moe_cache.sync (include/moe.h)
+CACHE_SYNC_WORDS = 4096
 
 
 # moe_cache.policy values (include/moe.h)
@@ -96,7 +100,7 @@ def lib():
         L.moe_debug_inject_ffn_stall.restype = C.c_int
         L.moe_debug_inject_ffn_stall.argtypes = [i32]
         L.moe_layer_kernel_count.restype = i32
-        L.moe_layer_kernel_count.argtypes = [sp, i32]
+        L.moe_layer_kernel_count.argtypes = [sp, cp, i32]
         L.moe_cache_place.restype = C.c_int
         L.moe_cache_place.argtypes = [sp, cp, vp, i32, vp]
         L.moe_cache_step.restype = C.c_int
@@ -182,8 +186,8 @@ def moe_debug_inject_ffn_stall(on=True):
     return _check(lib().moe_debug_inject_ffn_stall(1 if on else 0))
 
 
-def moe_layer_kernel_count(spec, T) -> int:
-    return int(lib().moe_layer_kernel_count(C.byref(spec), T))
+def moe_layer_kernel_count(spec, cache, T) -> int:
+    return int(lib().moe_layer_kernel_count(C.byref(spec), C.byref(cache), T))
 
 
 def moe_cache_place(spec, cache, ids, stream=None):
@@ -286,7 +290,7 @@ class DeviceCache:
     """Slot tables and slot pool in device memory (torch tensors) + the C struct."""
 
     def __init__(self, spec: MoeSpec, num_slots, k_victims, bp_mbps, bh_mbps, bank, device="cuda",
-                 with_pool=True, policy=POLICY_SHARED_LRU):
+                 with_pool=True, policy=POLICY_SHARED_LRU, sync=True):
         import torch
 
         n_ids = spec.num_layers * spec.num_experts
@@ -298,9 +302,12 @@ class DeviceCache:
         self.pool = (torch.empty((num_slots, se), dtype=torch.uint8, device=device)
                      if with_pool else None)
         self.bank = bank
+        # sync words of the one-kernel decode layer step (None: the multi-kernel form)
+        self.sync = (torch.zeros(CACHE_SYNC_WORDS, dtype=torch.int32, device=device)
+                     if sync else None)
         self.c = MoeCache(num_slots, k_victims, bp_mbps, bh_mbps, _ptr(self.slot_of_id),
                           _ptr(self.id_of_slot), _ptr(self.ts), _ptr(self.clock),
-                          _ptr(self.pool), _ptr(bank), policy)
+                          _ptr(self.pool), _ptr(bank), policy, _ptr(self.sync))
 
     def host_tables(self):
         import numpy as np

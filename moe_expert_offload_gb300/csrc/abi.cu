@@ -132,6 +132,15 @@ moe::CacheArgs cache_args(const moe_spec* spec, moe_cache* c, int32_t layer, con
   return a;
 }
 
+// The whole decode layer step as one cooperative kernel (ffn_coop.cu): the
+// cache carries sync words and the shape is one it serves.
+bool layer_one_kernel(const moe_spec* spec, const moe_cache* c, int32_t T) {
+  return c->sync != nullptr &&
+         moe::layer_fused_supported(spec->hidden, spec->inter, spec->num_experts, spec->top_k, T,
+                                    spec->has_shared, c->k_victims, spec->router,
+                                    spec->n_groups);
+}
+
 int do_cache_step(const moe_spec* spec, moe_cache* c, int32_t layer, const int32_t* ids,
                   int32_t T, moe_plan* plan, int32_t do_fill, cudaStream_t st,
                   uint32_t* zero_words = nullptr, int n_zero = 0) {
@@ -199,19 +208,10 @@ std::atomic<int> g_inject_stall{0};
 // (the caller launches no fill copy); only when ffn_fill_fusable holds.
 // ctr_zeroed: the control step launched just before cleared the FFN's counter
 // words (moe_layer_forward); otherwise the FFN launch clears them itself.
-int do_ffn(const moe_spec* spec, const moe_cache* c, int32_t layer, const moe_plan* plan,
-           const void* x, int32_t T, const int32_t* ids, const float* weights, const void* shared,
-           void* ws, size_t ws_bytes, float* y, cudaStream_t st, bool fuse_fill = false,
-           bool ctr_zeroed = false) {
-  if (T > moe::kMaxDecodeT) return fail(MOE_EUNSUPPORTED, "decode FFN supports T <= %d",
-                                        moe::kMaxDecodeT);
-  if (!x || !ids || !weights || !y || !ws) return fail(MOE_EINVAL, "moe_expert_ffn: NULL argument");
-  if (spec->has_shared && !shared) return fail(MOE_EINVAL, "spec has a shared expert: pass its blob");
-  if (!aligned(x, 16) || !aligned(ws, 256) || (shared && !aligned(shared, 16)))
-    return fail(MOE_EINVAL, "x (16 B), shared (16 B) and workspace (256 B) alignment");
-  const size_t need = moe::ffn_workspace_bytes(spec->hidden, spec->inter, spec->top_k, T,
-                                               spec->has_shared);
-  if (ws_bytes < need) return fail(MOE_ECAPACITY, "workspace %zu < %zu bytes", ws_bytes, need);
+moe::FfnArgs ffn_args(const moe_spec* spec, const moe_cache* c, int32_t layer,
+                      const moe_plan* plan, const void* x, int32_t T, const int32_t* ids,
+                      const float* weights, const void* shared, void* ws, float* y,
+                      bool fuse_fill) {
   moe::FfnArgs a;
   a.H = spec->hidden;
   a.I = spec->inter;
@@ -243,6 +243,23 @@ int do_ffn(const moe_spec* spec, const moe_cache* c, int32_t layer, const moe_pl
   a.shared = static_cast<const uint8_t*>(shared);
   a.y = y;
   moe::ffn_carve_workspace(a, ws);
+  return a;
+}
+
+int do_ffn(const moe_spec* spec, const moe_cache* c, int32_t layer, const moe_plan* plan,
+           const void* x, int32_t T, const int32_t* ids, const float* weights, const void* shared,
+           void* ws, size_t ws_bytes, float* y, cudaStream_t st, bool fuse_fill = false,
+           bool ctr_zeroed = false) {
+  if (T > moe::kMaxDecodeT) return fail(MOE_EUNSUPPORTED, "decode FFN supports T <= %d",
+                                        moe::kMaxDecodeT);
+  if (!x || !ids || !weights || !y || !ws) return fail(MOE_EINVAL, "moe_expert_ffn: NULL argument");
+  if (spec->has_shared && !shared) return fail(MOE_EINVAL, "spec has a shared expert: pass its blob");
+  if (!aligned(x, 16) || !aligned(ws, 256) || (shared && !aligned(shared, 16)))
+    return fail(MOE_EINVAL, "x (16 B), shared (16 B) and workspace (256 B) alignment");
+  const size_t need = moe::ffn_workspace_bytes(spec->hidden, spec->inter, spec->top_k, T,
+                                               spec->has_shared);
+  if (ws_bytes < need) return fail(MOE_ECAPACITY, "workspace %zu < %zu bytes", ws_bytes, need);
+  moe::FfnArgs a = ffn_args(spec, c, layer, plan, x, T, ids, weights, shared, ws, y, fuse_fill);
   cudaError_t e = moe::launch_ffn_decode(a, st, ctr_zeroed);
   if (e != cudaSuccess) return cuda_fail(e, "decode FFN launch");
   return MOE_OK;
@@ -282,7 +299,7 @@ int moe_cache_reset(const moe_spec* spec, moe_cache* cache, moe_stream_t stream)
   cudaError_t e = moe::launch_cache_reset(cache->slot_of_id,
                                           spec->num_layers * spec->num_experts,
                                           cache->id_of_slot, cache->ts, cache->num_slots,
-                                          cache->clock, (cudaStream_t)stream);
+                                          cache->clock, cache->sync, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "cache reset launch");
   return ok();
 }
@@ -322,6 +339,8 @@ int moe_cache_place(const moe_spec* spec, moe_cache* cache, const int32_t* ids, 
                         cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(cache->ts, 0, (size_t)S * sizeof(uint32_t), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(cache->clock, 0, sizeof(uint32_t), st);
+  if (e == cudaSuccess && cache->sync)
+    e = cudaMemsetAsync(cache->sync, 0, MOE_CACHE_SYNC_WORDS * sizeof(uint32_t), st);
   if (cache->slot_pool && cache->bank) {
     const int64_t blob = moe::blob_offsets(spec->hidden, spec->inter).total;
     for (int32_t i = 0; i < n && e == cudaSuccess; ++i) {
@@ -386,8 +405,9 @@ int moe_debug_inject_ffn_stall(int32_t on) {
   return MOE_OK;
 }
 
-int32_t moe_layer_kernel_count(const moe_spec* spec, int32_t T) {
-  if (check_spec(spec) != MOE_OK || T < 1 || T > moe::kMaxDecodeT) return 0;
+int32_t moe_layer_kernel_count(const moe_spec* spec, const moe_cache* cache, int32_t T) {
+  if (check_spec(spec) != MOE_OK || !cache || T < 1 || T > moe::kMaxDecodeT) return 0;
+  if (layer_one_kernel(spec, cache, T)) return 1;
   const bool fused_sel = T <= moe::kSelFusedMaxT && spec->num_experts <= moe::kSelFusedMaxE;
   const bool fused_fill =
       moe::ffn_fill_fusable(spec->hidden, spec->inter, spec->top_k, T, spec->has_shared);
@@ -420,6 +440,32 @@ int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, con
   cudaStream_t st = (cudaStream_t)stream;
   float* logits = static_cast<float*>(workspace);
   const size_t lbytes = align256((size_t)T * spec->num_experts * 4);
+  if (layer_one_kernel(spec, cache, T)) {
+    if (!x || !w_router || !ids || !weights || !y)
+      return fail(MOE_EINVAL, "moe_layer_forward: NULL argument");
+    if (spec->has_shared && !shared) return fail(MOE_EINVAL, "spec has a shared expert: pass its blob");
+    if (!aligned(x, 16) || !aligned(w_router, 16) || (shared && !aligned(shared, 16)))
+      return fail(MOE_EINVAL, "moe_layer_forward: x, w_router and shared must be 16-byte aligned");
+    moe::FfnArgs a = ffn_args(spec, cache, layer, plan, x, T, ids, weights, shared,
+                              static_cast<uint8_t*>(workspace) + lbytes, y, true);
+    a.ctr = cache->sync + moe::kSyncCtr;
+    a.n_ctr = MOE_CACHE_SYNC_WORDS - moe::kSyncCtr;
+    moe::LayerFuse lf;
+    lf.w_router = static_cast<const uint16_t*>(w_router);
+    lf.sel_bias = bias;
+    lf.logits = logits;
+    lf.router = spec->router;
+    lf.n_groups = spec->n_groups;
+    lf.topk_groups = spec->topk_groups;
+    lf.scale = spec->routed_scale;
+    lf.ids_out = ids;
+    lf.wts_out = weights;
+    lf.sync = cache->sync;
+    lf.c = cache_args(spec, cache, layer, ids, T, plan);
+    const cudaError_t e = moe::launch_layer_fused(a, lf, st);
+    if (e != cudaSuccess) return cuda_fail(e, "decode layer kernel launch");
+    return ok();
+  }
   // fill copy: written by the streaming FFN kernels as they read F from the
   // bank when both run for this shape (FreeToken "method steps": the miss
   // path copies the expert into its slot), else a copy kernel beside the FFN

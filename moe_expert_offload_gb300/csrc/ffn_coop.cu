@@ -47,7 +47,9 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "control_common.cuh"
 #include "moe_internal.cuh"
+#include "route_select.cuh"
 #include "stream_common.cuh"
 
 namespace moe {
@@ -260,8 +262,80 @@ __device__ bool wait_count(const uint32_t* p, uint32_t target) {
   return false;
 }
 
+__device__ __forceinline__ void red_release_gpu_add(uint32_t* p) { red_release_add(p, 1u); }
+
+struct ConsSync {
+  __device__ void operator()() const { cons_sync(); }
+};
+
+// One-kernel layer step: CTA 0's consumer warps run the selection and the
+// control step in the ring's shared memory (CTA 0 streams no weights).
+constexpr int kCtlK = 8;  // victims per step (KMAX of the victim lists)
+using CtlSh = ctl::CtlShared<kCtlK, kConsThreads>;
+struct SelScratch {
+  float a[kMaxTok][32 * 8];
+  float b[kMaxTok][rsel::kMaxK], c[kMaxTok][rsel::kMaxK];
+  float sum[kMaxTok];
+};
+static_assert(sizeof(CtlSh) + sizeof(SelScratch) <= 3 * (size_t)kSlotBytes,
+              "control step scratch must fit in the smallest ring");
+
+// CTA 0 of the one-kernel layer step, consumer threads (tid < 512): once
+// every CTA's logits are stored, the router selection (one warp per token),
+// then the classification of the routed ids, whose entries (ranked unique
+// ids and their slots before the step) are published for the FFN CTAs at
+// once; then the victim scan and the slot-table update, whose fill set is
+// published second (FreeToken summary "method steps").
+__device__ void layer_control(const FfnArgs& a, const LayerFuse& lf, CtlSh& cs, SelScratch& ss,
+                              const uint32_t (&early)[CtlSh::NE], const int32_t (&early_id)[CtlSh::NE],
+                              int& s_fail) {
+  const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
+  const int T = a.T, k = a.k, E = a.E, n = T * k;
+  uint32_t* sync = lf.sync;
+  for (int i = tid; i < (int)(sizeof(cs.shit) / 4); i += kConsThreads) cs.shit[i] = 0u;
+  if (tid == 0) {
+    cs.bad = 0;
+    cs.nu = 0;
+    cs.nh = 0;
+    cs.nm = 0;
+    if (!wait_count(sync + kSyncLogits, gridDim.x)) s_fail = 1;  // every CTA's logits
+  }
+  cons_sync();
+  const bool ok = s_fail == 0;
+  if (ok && wid < T) {
+    if (lf.router == MOE_ROUTER_SOFTMAX_TOPK)
+      rsel::softmax_token<8>(lf.logits, wid, E, k, lf.ids_out, lf.wts_out, ss.b[wid], ss.c[wid],
+                             &ss.sum[wid]);
+    else
+      rsel::sigmoid_group_token<8>(lf.logits, lf.sel_bias, wid, E, lf.n_groups, lf.topk_groups, k,
+                                   lf.scale, lf.ids_out, lf.wts_out, ss.a[wid], ss.b[wid],
+                                   &ss.sum[wid]);
+  }
+  cons_sync();
+  const uint32_t now = cs.now;
+  if (ok && wid == 0) {
+    const int32_t e = lane < n ? lf.ids_out[lane] : 0;
+    ctl::ctl_classify_warp<kCtlK, kConsThreads>(lf.c, cs, n, e, now);
+  }
+  cons_sync();
+  const int nu = cs.nu;
+  // the entries, for the FFN CTAs: ranked unique ids and their slots before the step
+  if (tid < nu) {
+    sync[kSyncUniq + tid] = (uint32_t)cs.suniq[tid];
+    sync[kSyncSlot + tid] = (uint32_t)cs.sslot[tid];
+  }
+  if (tid == 0) sync[kSyncNu] = (uint32_t)nu;
+  cons_sync();
+  if (tid == 0) red_release_gpu_add(sync + kSyncPlan);  // release: ids, weights, entries
+  ctl::ctl_evict<kCtlK, kConsThreads>(lf.c, cs, now, nu, cs.nh, cs.nm, early, early_id,
+                                      ConsSync{});
+  cons_sync();
+  if (tid == 0) red_release_gpu_add(sync + kSyncFill);  // release: the plan and the tables
+}
+
+template <bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
-    ffn_coop_kernel(FfnArgs a, CoopGeom geo, const __grid_constant__ CoopMaps maps) {
+    ffn_coop_kernel(FfnArgs a, CoopGeom geo, const __grid_constant__ CoopMaps maps, LayerFuse lf) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t full[kMaxSt], empty[kMaxSt], rfull[2], rfree[2];
   __shared__ int s_map[kMaxEnt], s_bi[kMaxEnt], s_fs[kMaxEnt], s_uid[kMaxEnt];
@@ -314,36 +388,155 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (tid < kMaxTok) s_vmax[tid] = 0u;
   if (tid < 8) s_zero[tid] = 0u;
-  griddep_wait();  // the plan (and the cleared counters) of the previous kernels
-  const int n_uniq = a.counts[0];
-  const int n_exec = n_uniq + a.has_shared;
-  const int n_ids = T * k;
-  for (int i = tid; i < n_ids; i += kThreads) {
-    s_ids[i] = a.ids[i];
-    s_wts[i] = a.weights[i];
-  }
-  if (tid < n_exec) {
-    // where entry r's weights are read and the slot an F entry is written to
-    const int r = tid;
-    int mi = 2, bi = 0, uid = -1;
-    int32_t fs = -1;
-    if (r < n_uniq) {
-      uid = a.uniq[r];
-      const int32_t slot = ffn_slot(a, uid, &fs);
-      mi = slot >= 0 ? 1 : 0;
-      bi = slot >= 0 ? slot : uid;
+  // x as fp16 B fragments of this CTA (scaled by a power of two per token),
+  // the per-group sums O and X of the scaled, rounded values, and y = 0 on
+  // this CTA's slice of the NY CTAs that run tiles (consumer threads)
+  auto prep_x = [&](unsigned yb, unsigned NY) {
+    const int ctid = tid;
+    for (int t = 0; t < T; ++t) {
+      uint32_t m = 0u;
+      const uint4* xp = reinterpret_cast<const uint4*>(a.x + (int64_t)t * H);
+      for (int i = ctid; i < H / 8; i += kConsThreads) {
+        const uint4 v = __ldg(xp + i);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          m = max(m, (w4[q] << 16) & 0x7FFFFFFFu);
+          m = max(m, w4[q] & 0x7FFF0000u);
+        }
+      }
+      m = __reduce_max_sync(0xffffffffu, m);
+      if (lane == 0) atomicMax(&s_vmax[t], m);
     }
-    s_map[r] = mi;
-    s_bi[r] = bi;
-    s_fs[r] = fs;
-    s_uid[r] = uid;
+    cons_sync();
+    if (ctid < T) s_px[ctid] = 1.0f / inv_pow2_above(__uint_as_float(s_vmax[ctid]));
+    const int ng = H / 64, n_items = T * ng * 4;
+    for (int b0 = 0; b0 < n_items; b0 += kConsThreads) {
+      const int it = b0 + ctid;
+      const bool in = it < n_items;
+      const int t = in ? it / (ng * 4) : 0, rem = it - t * ng * 4, G = rem >> 2, q4 = rem & 3;
+      float v[16];
+      float o = 0.0f, xs = 0.0f;
+      if (in) {
+        const float sc = inv_pow2_above(__uint_as_float(s_vmax[t]));
+        const uint4* px = reinterpret_cast<const uint4*>(a.x + (int64_t)t * H + G * 64 + q4 * 16);
+        const uint4 p0 = __ldg(px), p1 = __ldg(px + 1);
+        const uint32_t wv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          v[2 * i] = __uint_as_float(wv[i] << 16) * sc;
+          v[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u) * sc;
+        }
+        frag_item(v, frag + (size_t)t * geo.frow + G * 128 + q4 * 32, o, xs);
+      }
+      o += __shfl_xor_sync(0xffffffffu, o, 1);
+      o += __shfl_xor_sync(0xffffffffu, o, 2);
+      xs += __shfl_xor_sync(0xffffffffu, xs, 1);
+      xs += __shfl_xor_sync(0xffffffffu, xs, 2);
+      if (in && q4 == 0) ox[G * kMaxTok + t] = make_float2(o, xs);
+    }
+    // y starts at zero (ordered before the down tiles' adds by the grid-wide
+    // gate/up count)
+    const unsigned ny = (unsigned)T * H;
+    for (unsigned i = yb * ny / NY + ctid; i < (yb + 1) * ny / NY; i += kConsThreads) a.y[i] = 0.0f;
+    cons_sync();
+  };
+
+  const unsigned Gall = gridDim.x;
+  // CTAs that run tiles: all of them, or all but CTA 0 in the one-kernel layer step
+  const unsigned G = FUSED ? Gall - 1 : Gall, b = FUSED ? blockIdx.x - 1 : blockIdx.x;
+  const bool ctl_cta = FUSED && blockIdx.x == 0;
+  int n_uniq = 0, n_exec = 0;
+  const int n_ids = T * k;
+  if constexpr (FUSED) {
+    // ------------------------------------------- one-kernel layer step
+    uint32_t* sync = lf.sync;
+    uint32_t early[CtlSh::NE];
+    int32_t early_id[CtlSh::NE];
+    CtlSh& cs = *reinterpret_cast<CtlSh*>(ring);
+    SelScratch& ss = *reinterpret_cast<SelScratch*>(ring + sizeof(CtlSh));
+    griddep_wait();  // x, the cache tables and the pool of the previous kernels
+    if (wid < kCW) {
+      if (ctl_cta) {
+        // the victim scan's first stamps, and the step's clock
+        ctl::ctl_early_loads<CtlSh::NE, kConsThreads>(lf.c, early, early_id);
+        if (tid == 0) {
+          cs.now = lf.c.clock[0] + 1u;
+          lf.c.clock[0] = cs.now;
+        }
+      }
+      // router logits (the fixed order of every router path): pair p = (t, e)
+      // on CTA p % Gall, warp p / Gall
+      const int E = a.E, np = T * E;
+      for (int p = (int)blockIdx.x + (int)Gall * wid; p < np; p += (int)Gall * kCW) {
+        const int t = p / E, e = p - t * E;
+        const float v =
+            rsel::router_dot_warp(a.x + (size_t)t * H, lf.w_router + (size_t)e * H, H);
+        if (lane == 0) lf.logits[p] = v;
+      }
+      cons_sync();
+      if (tid == 0) red_release_gpu_add(sync + kSyncLogits);
+      if (ctl_cta) {
+        layer_control(a, lf, cs, ss, early, early_id, s_fail);
+      } else {
+        prep_x(b, G);
+        if (tid == 0 && !wait_count(sync + kSyncPlan, 1u)) s_fail = 1;
+      }
+    }
+    __syncthreads();
+    if (!ctl_cta && !s_fail) {
+      // the published entries, ids and weights
+      n_uniq = (int)__ldcg(sync + kSyncNu);
+      n_exec = n_uniq + a.has_shared;
+      for (int i = tid; i < n_ids; i += kThreads) {
+        s_ids[i] = __ldcg(a.ids + i);
+        s_wts[i] = __ldcg(a.weights + i);
+      }
+      if (tid < n_exec) {
+        const int r = tid;
+        int mi = 2, bi = 0, uid = -1;
+        if (r < n_uniq) {
+          uid = (int)__ldcg(sync + kSyncUniq + r);
+          const int32_t slot = (int32_t)__ldcg(sync + kSyncSlot + r);
+          mi = slot >= 0 ? 1 : 0;
+          bi = slot >= 0 ? slot : uid;
+        }
+        s_map[r] = mi;
+        s_bi[r] = bi;
+        s_fs[r] = -1;  // an F entry's slot: learnt by the fill writer
+        s_uid[r] = uid;
+      }
+    }
+  } else {
+    griddep_wait();  // the plan (and the cleared counters) of the previous kernels
+    n_uniq = a.counts[0];
+    n_exec = n_uniq + a.has_shared;
+    for (int i = tid; i < n_ids; i += kThreads) {
+      s_ids[i] = a.ids[i];
+      s_wts[i] = a.weights[i];
+    }
+    if (tid < n_exec) {
+      // where entry r's weights are read and the slot an F entry is written to
+      const int r = tid;
+      int mi = 2, bi = 0, uid = -1;
+      int32_t fs = -1;
+      if (r < n_uniq) {
+        uid = a.uniq[r];
+        const int32_t slot = ffn_slot(a, uid, &fs);
+        mi = slot >= 0 ? 1 : 0;
+        bi = slot >= 0 ? slot : uid;
+      }
+      s_map[r] = mi;
+      s_bi[r] = bi;
+      s_fs[r] = fs;
+      s_uid[r] = uid;
+    }
   }
   __syncthreads();
 
   const int tpe_gu = I / 16, tpe_dn = H / geo.RD;
-  const int n_gu = n_exec * tpe_gu, n_dn = n_exec * tpe_dn;
+  const int n_gu = ctl_cta ? 0 : n_exec * tpe_gu, n_dn = ctl_cta ? 0 : n_exec * tpe_dn;
   // balanced contiguous ranges (32-bit: tiles x CTAs stays below 2^32)
-  const unsigned G = gridDim.x, b = blockIdx.x;
   const int gu_lo = (int)(b * (unsigned)n_gu / G), gu_hi = (int)((b + 1) * (unsigned)n_gu / G);
   const int dn_lo = (int)(b * (unsigned)n_dn / G), dn_hi = (int)((b + 1) * (unsigned)n_dn / G);
   const int nks = geo.nks, nkd = geo.nkd, RD = geo.RD, KSD = geo.KSD;
@@ -413,8 +606,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       bool ok = true;
+      // (one-kernel step) the F entries' slots are learnt at the first entry
+      // read from the bank, once the control step has published its fills
+      bool known = !FUSED;
+      auto fill_slot = [&](int r) -> int {
+        if (!known && r < n_uniq && s_map[r] == 0) {
+          bool got = true;
+          if (lane == 0) got = wait_count(lf.sync + kSyncFill, 1u);
+          got = __shfl_sync(0xffffffffu, (int)got, 0) != 0;
+          asm volatile("fence.acq_rel.gpu;" ::: "memory");
+          if (got) {
+            const int nf = __ldcg(a.counts + 4);
+            for (int e = lane; e < n_uniq; e += 32) {
+              int32_t fs = -1;
+              if (s_map[e] == 0)
+                for (int i = 0; i < nf; ++i)
+                  if (__ldcg(a.fill_ids + i) == s_uid[e]) fs = __ldcg(a.fill_slots + i);
+              s_fs[e] = fs;
+            }
+          } else {
+            ok = false;
+          }
+          __syncwarp();
+          known = true;
+        }
+        return s_fs[r];
+      };
       for (int tile = gu_lo; ok && tile < gu_hi; ++tile) {
-        const int r = tile / tpe_gu, row0 = (tile % tpe_gu) * 16, fs = s_fs[r];
+        const int r = tile / tpe_gu, row0 = (tile % tpe_gu) * 16, fs = fill_slot(r);
         for (int ks = 0; ks < nks; ++ks, advance()) {
           if (!(ok = warp_wait(su32(&full[s]), ph))) break;
           if (fs >= 0 && lane <= 4) {
@@ -432,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       for (int tile = dn_lo; ok && tile < dn_hi; ++tile) {
-        const int r = tile / tpe_dn, row0 = (tile % tpe_dn) * RD, fs = s_fs[r];
+        const int r = tile / tpe_dn, row0 = (tile % tpe_dn) * RD, fs = fill_slot(r);
         for (int kd = 0; kd < nkd; ++kd, advance()) {
           if (!(ok = warp_wait(su32(&full[s]), ph))) break;
           if (fs >= 0 && lane <= geo.nbd) {
@@ -456,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ----------------------------------------------------------- consumers
     const int w = wid, g = lane >> 2, t4 = lane & 3, ctid = tid;
-    // tokens routed to each entry (ascending), and max |x| per token
+    // tokens routed to each entry (ascending)
     if (ctid < n_exec) {
       const int r = ctid, uid = s_uid[r];
       int nt = 0;
@@ -467,60 +686,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       s_ntok[r] = nt;
     }
-    for (int t = 0; t < T; ++t) {
-      uint32_t m = 0u;
-      const uint4* xp = reinterpret_cast<const uint4*>(a.x + (int64_t)t * H);
-      for (int i = ctid; i < H / 8; i += kConsThreads) {
-        const uint4 v = __ldg(xp + i);
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          m = max(m, (w4[q] << 16) & 0x7FFFFFFFu);
-          m = max(m, w4[q] & 0x7FFF0000u);
-        }
-      }
-      m = __reduce_max_sync(0xffffffffu, m);
-      if (lane == 0) atomicMax(&s_vmax[t], m);
-    }
-    cons_sync();
-    // x as fp16 B fragments, scaled by a power of two per token, and the
-    // per-group sums O and X (of the scaled, rounded values)
-    {
-      if (ctid < T) s_px[ctid] = 1.0f / inv_pow2_above(__uint_as_float(s_vmax[ctid]));
-      const int ng = H / 64, n_items = T * ng * 4;
-      for (int b0 = 0; b0 < n_items; b0 += kConsThreads) {
-        const int it = b0 + ctid;
-        const bool in = it < n_items;
-        const int t = in ? it / (ng * 4) : 0, rem = it - t * ng * 4, G = rem >> 2, q4 = rem & 3;
-        float v[16];
-        float o = 0.0f, xs = 0.0f;
-        if (in) {
-          const float sc = inv_pow2_above(__uint_as_float(s_vmax[t]));
-          const uint4* px = reinterpret_cast<const uint4*>(a.x + (int64_t)t * H + G * 64 + q4 * 16);
-          const uint4 p0 = __ldg(px), p1 = __ldg(px + 1);
-          const uint32_t wv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            v[2 * i] = __uint_as_float(wv[i] << 16) * sc;
-            v[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u) * sc;
-          }
-          frag_item(v, frag + (size_t)t * geo.frow + G * 128 + q4 * 32, o, xs);
-        }
-        o += __shfl_xor_sync(0xffffffffu, o, 1);
-        o += __shfl_xor_sync(0xffffffffu, o, 2);
-        xs += __shfl_xor_sync(0xffffffffu, xs, 1);
-        xs += __shfl_xor_sync(0xffffffffu, xs, 2);
-        if (in && q4 == 0) ox[G * kMaxTok + t] = make_float2(o, xs);
-      }
-    }
-    cons_sync();
-
-    // y starts at zero: this CTA's slice (ordered before the down tiles' adds by
-    // the grid-wide gate/up count)
-    {
-      const unsigned ny = (unsigned)T * H;
-      for (unsigned i = b * ny / G + ctid; i < (b + 1) * ny / G; i += kConsThreads) a.y[i] = 0.0f;
-    }
+    if constexpr (!FUSED)
+      prep_x(b, G);  // (ends with a consumer barrier)
+    else
+      cons_sync();
     bool ok = true;
     int n = 0, lt = 0;  // stages consumed; gate/up tiles finished (partial buffer ring)
     const unsigned char* zblk = reinterpret_cast<const unsigned char*>(s_zero);
@@ -679,7 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         cons_sync();
         if (ctid == 0) {
           // every CTA's h rows (all entries) before the first down tile
-          if (cur < 0 && ok && !wait_count(gu_cnt, G)) s_fail = 1;
+          if (cur < 0 && ok && !wait_count(gu_cnt, Gall)) s_fail = 1;
           const int uid = s_uid[r];
           for (int nn = 0; nn < ntok; ++nn) {
             const float inv = inv_pow2_above(__uint_as_float(__ldcg(hmax + r * kMaxTok + nn)));
@@ -804,6 +973,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   __syncthreads();
+  __shared__ int s_last;
   if (tid == 0) {
     const bool f = s_fail != 0;
     if (f) {
@@ -811,14 +981,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       atomicExch(failw, 1u);
     }
     __threadfence();
-    if (atomicAdd(done, 1u) == gridDim.x - 1) {
+    s_last = atomicAdd(done, 1u) == gridDim.x - 1;
+    if (s_last) {
       // last CTA: when any CTA gave up while this call carried the step's
       // fills, an F slot may hold a partial copy -- unmap every F entry
       __threadfence();
       if (a.fill_fused && atomicAdd(failw, 0u) != 0u) {
-        const int nf = a.counts[4];
+        const int nf = __ldcg(a.counts + 4);
         for (int i = 0; i < nf; ++i) {
-          const int32_t f = a.fill_ids[i], v = a.fill_slots[i];
+          const int32_t f = __ldcg(a.fill_ids + i), v = __ldcg(a.fill_slots + i);
           a.tab_slot_of_id[f] = -1;
           a.tab_id_of_slot[v] = -1;
           a.tab_ts[v] = 0u;
@@ -826,15 +997,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+  if constexpr (FUSED) {
+    // last CTA: every other CTA is past its last use of the sync words, which
+    // are left zero for the next step
+    __syncthreads();
+    if (s_last)
+      for (int i = tid; i < kSyncCtr + 4 + 8 * kMaxEnt; i += kThreads) lf.sync[i] = 0u;
+  }
   griddep_launch();
 }
 
+static_assert(kSyncCtr + 4 + 8 * kMaxEnt <= MOE_CACHE_SYNC_WORDS, "sync words");
+
+template <bool FUSED>
 bool coop_attr_set(size_t smem) {
   static size_t done[64];
   int d = 0;
   if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) return false;
   if (done[d] >= smem) return true;
-  if (cudaFuncSetAttribute(ffn_coop_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(ffn_coop_kernel<FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
     return false;
   done[d] = smem;
@@ -849,7 +1030,10 @@ bool ffn_coop_supported(int H, int I, int k, int T, int has_shared) {
   return coop_geom(H, I, T).nst > 0;
 }
 
-cudaError_t launch_ffn_coop(const FfnArgs& a, cudaStream_t st) {
+namespace {
+
+template <bool FUSED>
+cudaError_t launch_coop(const FfnArgs& a, const LayerFuse& lf, cudaStream_t st) {
   static int sms[64];
   if (!ffn_coop_supported(a.H, a.I, a.k, a.T, a.has_shared) || a.max_entries > kMaxEnt ||
       a.n_ctr < ffn_ctr_words(a.H, a.max_entries))
@@ -904,7 +1088,7 @@ cudaError_t launch_ffn_coop(const FfnArgs& a, cudaStream_t st) {
         return e;
     }
   }
-  if (!coop_attr_set(geo.smem)) return cudaErrorInvalidValue;
+  if (!coop_attr_set<FUSED>(geo.smem)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -917,15 +1101,39 @@ cudaError_t launch_ffn_coop(const FfnArgs& a, cudaStream_t st) {
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, ffn_coop_kernel, a, geo, maps);
+  e = cudaLaunchKernelEx(&cfg, ffn_coop_kernel<FUSED>, a, geo, maps, lf);
   if (e == cudaErrorInvalidValue || e == cudaErrorNotSupported) {
     // a runtime that does not take both attributes together: launch it
     // cooperatively, after the previous kernel has completed
     (void)cudaGetLastError();
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, ffn_coop_kernel, a, geo, maps);
+    e = cudaLaunchKernelEx(&cfg, ffn_coop_kernel<FUSED>, a, geo, maps, lf);
   }
   return e;
+}
+
+}  // namespace
+
+cudaError_t launch_ffn_coop(const FfnArgs& a, cudaStream_t st) {
+  return launch_coop<false>(a, LayerFuse{}, st);
+}
+
+bool layer_fused_supported(int H, int I, int E, int k, int T, int has_shared, int K, int router,
+                           int n_groups) {
+  if (!ffn_coop_supported(H, I, k, T, has_shared)) return false;
+  if (T * k > 32 || K < 1 || K > kCtlK || E < 1 || E > 256 || k > rsel::kMaxK) return false;
+  if (router != MOE_ROUTER_SOFTMAX_TOPK && (n_groups < 1 || n_groups > 32)) return false;
+  return true;
+}
+
+cudaError_t launch_layer_fused(const FfnArgs& a, const LayerFuse& lf, cudaStream_t st) {
+  if (!layer_fused_supported(a.H, a.I, a.E, a.k, a.T, a.has_shared, lf.c.K, lf.router,
+                             lf.n_groups) ||
+      !lf.sync || !lf.logits || !lf.w_router || !lf.ids_out || !lf.wts_out || !a.fill_fused ||
+      a.ids != lf.ids_out || a.weights != lf.wts_out || lf.c.ids != lf.ids_out ||
+      a.ctr != lf.sync + kSyncCtr)
+    return cudaErrorInvalidValue;
+  return launch_coop<true>(a, lf, st);
 }
 
 }  // namespace moe

@@ -104,9 +104,29 @@ struct SelArgs {
   float* wts = nullptr;
 };
 constexpr int kSelFusedMaxT = 16, kSelFusedMaxE = 256;
+
+// One-kernel decode layer step (ffn_coop.cu): the router logits, the
+// selection and the control step run inside the cooperative decode FFN
+// kernel.  Layout of the cache's sync words (moe_cache.sync, zero between
+// steps): the logits count, the two publication flags (entries, fills), the
+// published entries (count, ranked unique ids, their slots before the step),
+// then the FFN's counter block (FfnArgs::ctr).
+constexpr int kSyncLogits = 0, kSyncPlan = 1, kSyncFill = 2, kSyncNu = 3, kSyncUniq = 4,
+              kSyncSlot = 36, kSyncCtr = 68;
+struct LayerFuse {
+  const uint16_t* w_router = nullptr;  // [E][H] bf16
+  const float* sel_bias = nullptr;     // [E] or null (sigmoid-group selection)
+  float* logits = nullptr;             // [T][E] scratch
+  int router = 0, n_groups = 0, topk_groups = 0;
+  float scale = 0.0f;
+  int32_t* ids_out = nullptr;          // [T][k] routed ids (written, then read by every CTA)
+  float* wts_out = nullptr;            // [T][k] routing weights
+  uint32_t* sync = nullptr;            // the cache's sync words
+  CacheArgs c;                         // the control step (c.ids == ids_out)
+};
 cudaError_t launch_cache_step_sel(const CacheArgs& a, const SelArgs& s, cudaStream_t st);
 cudaError_t launch_cache_reset(int32_t* slot_of_id, int n_ids, int32_t* id_of_slot, uint32_t* ts,
-                               int S, uint32_t* clock, cudaStream_t st);
+                               int S, uint32_t* clock, uint32_t* sync, cudaStream_t st);
 cudaError_t launch_fill_copy(const moe_plan& plan, int K, const uint8_t* bank, uint8_t* pool,
                              int64_t blob_bytes, cudaStream_t st);
 
@@ -203,6 +223,11 @@ cudaError_t launch_ffn_decode(const FfnArgs& a, cudaStream_t st, bool ctr_zeroed
 // launch.
 bool ffn_coop_supported(int H, int I, int k, int T, int has_shared);
 cudaError_t launch_ffn_coop(const FfnArgs& a, cudaStream_t st);
+// The one-kernel step serves this shape: the cooperative FFN's, T k <= 32
+// routed ids, K <= 8 victims, E <= 256 experts, k <= 64.
+bool layer_fused_supported(int H, int I, int E, int k, int T, int has_shared, int K, int router,
+                           int n_groups);
+cudaError_t launch_layer_fused(const FfnArgs& a, const LayerFuse& lf, cudaStream_t st);
 // Both streaming decode kernels run for this shape, so they can carry the
 // step's fill copy (FfnArgs::fill_fused).
 bool ffn_fill_fusable(int H, int I, int k, int T, int has_shared);

@@ -1,7 +1,9 @@
-// Router selection shared by the select kernels and the fused decode control
-// step (Edge0 §2 "MoE routing"): the library's exp and sigmoid, the top-k
-// order, and the per-token softmax-top-k and sigmoid-group selections, each
-// run by one warp.  Every floating-point step is an explicitly rounded IEEE
+// Router scoring and selection shared by the router kernels, the fused decode
+// control step and the fused decode layer kernel (Edge0 §2 "MoE routing"):
+// one logit per warp in a fixed order, the library's exp and sigmoid, the
+// top-k order, and the per-token softmax-top-k and sigmoid-group selections,
+// each run by one warp.  Logits are read through L2 (they may have been
+// written by other CTAs of the same grid).  Every floating-point step is an explicitly rounded IEEE
 // operation, so a plain CPU program reproduces the decisions bit for bit.
 #pragma once
 #include <float.h>
@@ -12,6 +14,50 @@ namespace moe {
 namespace rsel {
 
 constexpr int kMaxK = 64;
+
+__device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// One router logit x . w (bf16 rows of H, 16-byte aligned) by one warp, in
+// the fixed order every router path uses: lane j accumulates the 8-element
+// chunks c = j, j+32, ... in ascending order with fma from 0, then the lane
+// sums go through an xor butterfly 16, 8, 4, 2, 1.  Every lane returns the
+// logit.
+__device__ __forceinline__ float router_dot_warp(const uint16_t* __restrict__ x,
+                                                 const uint16_t* __restrict__ w, int H) {
+  const int lane = threadIdx.x & 31;
+  const uint4* xr = reinterpret_cast<const uint4*>(x);
+  const uint4* wr = reinterpret_cast<const uint4*>(w);
+  const int chunks = H >> 3;
+  float acc = 0.0f;
+  // eight chunks' loads in flight at a time, then their fmas in chunk order
+  for (int c0 = lane; c0 < chunks; c0 += 32 * 8) {
+    uint4 xv[8], wv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int c = c0 + 32 * u;
+      if (c < chunks) {
+        xv[u] = __ldg(xr + c);
+        wv[u] = __ldg(wr + c);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (c0 + 32 * u >= chunks) break;
+      acc = __fmaf_rn(bf_lo(xv[u].x), bf_lo(wv[u].x), acc);
+      acc = __fmaf_rn(bf_hi(xv[u].x), bf_hi(wv[u].x), acc);
+      acc = __fmaf_rn(bf_lo(xv[u].y), bf_lo(wv[u].y), acc);
+      acc = __fmaf_rn(bf_hi(xv[u].y), bf_hi(wv[u].y), acc);
+      acc = __fmaf_rn(bf_lo(xv[u].z), bf_lo(wv[u].z), acc);
+      acc = __fmaf_rn(bf_hi(xv[u].z), bf_hi(wv[u].z), acc);
+      acc = __fmaf_rn(bf_lo(xv[u].w), bf_lo(wv[u].w), acc);
+      acc = __fmaf_rn(bf_hi(xv[u].w), bf_hi(wv[u].w), acc);
+    }
+  }
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, d));
+  return acc;
+}
 
 // exp(x) in fp32: Cody-Waite reduction x = n ln2 + r (ln2 = 0x1.62e4p-1 +
 // 0x1.7f7d1cp-20, the high part short enough that n * hi is exact), the
@@ -71,7 +117,7 @@ __device__ __forceinline__ void softmax_token(const float* __restrict__ logits, 
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = lane + 32 * i;
-    v[i] = (e < E) ? logits[(size_t)t * E + e] : -FLT_MAX;
+    v[i] = (e < E) ? __ldcg(logits + (size_t)t * E + e) : -FLT_MAX;
     if (e >= E) taken |= 1u << i;
   }
   for (int r = 0; r < k; ++r) {
@@ -123,7 +169,7 @@ __device__ __forceinline__ void sigmoid_group_token(const float* __restrict__ lo
   for (int i = 0; i < EPL; ++i) {
     const int e = lane + 32 * i;
     if (e < E) {
-      s[i] = moe_sigmoid(logits[(size_t)t * E + e]);
+      s[i] = moe_sigmoid(__ldcg(logits + (size_t)t * E + e));
       sel[i] = __fadd_rn(s[i], bias ? bias[e] : 0.0f);
       ssel[e] = sel[i];
     } else {

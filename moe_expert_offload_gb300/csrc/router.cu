@@ -13,12 +13,10 @@
 namespace moe {
 namespace {
 
-__device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+using rsel::bf_hi;
+using rsel::bf_lo;
 
-// One warp per (token, expert).  Lane j accumulates 8-element chunks
-// c = j, j+32, ... in order with fma from 0; the lane sums then go through an
-// xor butterfly 16, 8, 4, 2, 1.  x rows and W rows are 16-byte aligned.
+// One warp per (token, expert): rsel::router_dot_warp.
 __global__ void __launch_bounds__(128) router_logits_kernel(const uint16_t* __restrict__ x,
                                                             const uint16_t* __restrict__ w, int T,
                                                             int E, int H,
@@ -29,36 +27,7 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const uint16_t* __re
   const int lane = threadIdx.x & 31;
   if (warp >= T * E) return;
   const int t = warp / E, e = warp - t * E;
-  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
-  const uint4* wr = reinterpret_cast<const uint4*>(w + (size_t)e * H);
-  const int chunks = H >> 3;
-  float acc = 0.0f;
-  // eight chunks' loads in flight at a time, then their fmas in chunk order
-  for (int c0 = lane; c0 < chunks; c0 += 32 * 8) {
-    uint4 xv[8], wv[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int c = c0 + 32 * u;
-      if (c < chunks) {
-        xv[u] = __ldg(xr + c);
-        wv[u] = __ldg(wr + c);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      if (c0 + 32 * u >= chunks) break;
-      acc = __fmaf_rn(bf_lo(xv[u].x), bf_lo(wv[u].x), acc);
-      acc = __fmaf_rn(bf_hi(xv[u].x), bf_hi(wv[u].x), acc);
-      acc = __fmaf_rn(bf_lo(xv[u].y), bf_lo(wv[u].y), acc);
-      acc = __fmaf_rn(bf_hi(xv[u].y), bf_hi(wv[u].y), acc);
-      acc = __fmaf_rn(bf_lo(xv[u].z), bf_lo(wv[u].z), acc);
-      acc = __fmaf_rn(bf_hi(xv[u].z), bf_hi(wv[u].z), acc);
-      acc = __fmaf_rn(bf_lo(xv[u].w), bf_lo(wv[u].w), acc);
-      acc = __fmaf_rn(bf_hi(xv[u].w), bf_hi(wv[u].w), acc);
-    }
-  }
-#pragma unroll
-  for (int d = 16; d >= 1; d >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, d));
+  const float acc = rsel::router_dot_warp(x + (size_t)t * H, w + (size_t)e * H, H);
   if (lane == 0) logits[(size_t)t * E + e] = acc;
 }
 

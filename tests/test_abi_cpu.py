@@ -255,17 +255,25 @@ def test_hot_placement_is_best_fixed_set():
 
 def test_layer_kernel_count(L):
     """Host-side launch accounting of moe_layer_forward (no device work)."""
+    c, cs = _cache(sync=None), _cache(sync=1 << 20)  # without / with sync words (K = 4)
+    kc = m.moe_layer_kernel_count
+    # sync words and T k <= 32, K <= 8, E <= 256: the whole step is one cooperative kernel
+    assert kc(m.make_spec(1, 2048, 512, 256, 8), cs, 1) == 1
+    assert kc(m.make_spec(1, 7168, 2048, 256, 8, router="sigmoid_group", n_groups=8,
+                          topk_groups=4), cs, 4) == 1
+    assert kc(m.make_spec(1, 2048, 512, 256, 8), cs, 8) == 3  # T k = 64 > 32
+    assert kc(m.make_spec(1, 2048, 512, 256, 8), _cache(sync=1 << 20, k_victims=16), 1) == 3
     # logits, control step with the selection, one cooperative FFN kernel carrying the fill
-    assert m.moe_layer_kernel_count(m.make_spec(1, 2048, 512, 256, 8), 1) == 3
-    assert m.moe_layer_kernel_count(m.make_spec(1, 7168, 2048, 256, 8), 8) == 3
+    assert kc(m.make_spec(1, 2048, 512, 256, 8), c, 1) == 3
+    assert kc(m.make_spec(1, 7168, 2048, 256, 8), c, 8) == 3
     # I % 512 != 0: the two streaming kernels (gate/up, down) carry the fill
-    assert m.moe_layer_kernel_count(m.make_spec(1, 2048, 256, 256, 8), 1) == 4
+    assert kc(m.make_spec(1, 2048, 256, 256, 8), cs, 1) == 4
     # H = 256 is below the streaming kernels' 512-column tiles: a fill copy kernel runs
-    assert m.moe_layer_kernel_count(m.make_spec(1, 256, 128, 16, 2), 1) == 5
-    assert m.moe_layer_kernel_count(m.make_spec(1, 256, 128, 300, 2), 1) == 6  # + select
-    assert m.moe_layer_kernel_count(m.make_spec(1, 2048, 512, 256, 8), 9) == 5  # T > 8
-    assert m.moe_layer_kernel_count(m.make_spec(1, 2048, 512, 256, 8), 0) == 0
-    assert m.moe_layer_kernel_count(m.make_spec(1, 2048, 512, 256, 8), 65) == 0
+    assert kc(m.make_spec(1, 256, 128, 16, 2), cs, 1) == 5
+    assert kc(m.make_spec(1, 256, 128, 300, 2), cs, 1) == 6  # + select
+    assert kc(m.make_spec(1, 2048, 512, 256, 8), cs, 9) == 5  # T > 8
+    assert kc(m.make_spec(1, 2048, 512, 256, 8), cs, 0) == 0
+    assert kc(m.make_spec(1, 2048, 512, 256, 8), cs, 65) == 0
 
 
 def test_inject_hook_sets_and_clears(L):

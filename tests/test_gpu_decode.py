@@ -317,6 +317,16 @@ def _ffn_kernels(H, I, T):
     return 1 if (H % 1024 == 0 and I % 512 == 0 and T <= 8) else 2
 
 
+def _layer_kernels(H, I, E, k, T, K, sync):
+    """Launches of a decode layer step whose selection runs in the control step and whose
+    fill the FFN carries: the whole step as one cooperative kernel when the cache has sync
+    words and T k <= 32, K <= 8, E <= 256 on a cooperative-FFN shape; else logits, control
+    step and the FFN kernels."""
+    if sync and _ffn_kernels(H, I, T) == 1 and T * k <= 32 and K <= 8 and E <= 256:
+        return 1
+    return 2 + _ffn_kernels(H, I, T)
+
+
 @pytest.mark.parametrize("H,I,E,k,T,shared,S,K", [(1024, 256, 16, 4, 1, True, 6, 3),
                                                   (1024, 256, 16, 4, 3, False, 5, 4),
                                                   (2048, 512, 24, 8, 8, True, 20, 8),
@@ -325,18 +335,20 @@ def _ffn_kernels(H, I, T):
                                                   (1024, 512, 16, 4, 3, False, 5, 4),
                                                   (2048, 1024, 12, 4, 8, True, 10, 4),
                                                   (3072, 512, 20, 6, 5, True, 8, 6)])
-def test_layer_forward_fused_fill(oracle, H, I, E, k, T, shared, S, K):
+@pytest.mark.parametrize("sync", [True, False])
+def test_layer_forward_fused_fill(oracle, H, I, E, k, T, shared, S, K, sync):
     """Shapes the FFN kernels serve with the fill carried: the fill copy is written by the
     FFN kernels as they read F from the bank (no copy kernel).  Plans, outputs and every
     resident slot's bytes equal the oracle's and the bank's over steps with fills and
     evictions.  The shapes cover both FFN paths (cooperative kernel: H % 1024 == 0 and
     I % 512 == 0), both down-tile geometries of the cooperative kernel (I % 1024 == 0 or
-    not) and gate/up tiles of one, two and three stages."""
+    not) and gate/up tiles of one, two and three stages.  With the cache's sync words
+    (sync) the shapes with T k <= 32 run as one cooperative kernel (router logits,
+    selection, control step and FFN); without them as logits, control step and FFN."""
     L = 2
     spec, bank, bank_h, cache, sh = _layer_rig(L, H, I, E, k, S, K, 52700, 77300, shared,
-                                               seed=H + T)
-    # logits, control step with the selection, FFN
-    assert m.moe_layer_kernel_count(spec, T) == 2 + _ffn_kernels(H, I, T)
+                                               seed=H + T, sync=sync)
+    assert m.moe_layer_kernel_count(spec, cache.c, T) == _layer_kernels(H, I, E, k, T, K, sync)
     plan = m.DevicePlan(T * k, K, device=DEV)
     wsb = m.moe_layer_workspace_bytes(spec, T)
     ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
@@ -367,6 +379,8 @@ def test_layer_forward_fused_fill(oracle, H, I, E, k, T, shared, S, K):
                 assert np.array_equal(pool[slot], bank_h[eid]), f"step {step} slot {slot}"
     assert fills > 0
     assert int(plan.err[0].item()) == 0
+    if sync:
+        assert not cache.sync.any().item()  # every step leaves the sync words zero
 
 
 # ------------------------------------------------ failure detection (no fault)
@@ -402,7 +416,8 @@ def test_ffn_wait_timeout_sets_error_and_context_survives(oracle):
     assert_ffn_close(y.cpu().numpy(), ref, "after the stall")
 
 
-def test_wait_timeout_in_layer_step_unmaps_fills(oracle):
+@pytest.mark.parametrize("sync", [True, False])
+def test_wait_timeout_in_layer_step_unmaps_fills(oracle, sync):
     """A decode layer step whose FFN carries the fill and whose bounded waits run out
     (injected stall): plan.err gets MOE_DERR_WAIT, and the experts the step filled are
     unmapped again (their slots may hold a partial copy): slot_of_id = -1, the slot empty,
@@ -410,8 +425,10 @@ def test_wait_timeout_in_layer_step_unmaps_fills(oracle):
     oracle bit for bit (plans, tables) and within tolerance (outputs), and every resident
     slot holds its bank blob."""
     H, I, E, k, T, S, K, L = 1024, 512, 16, 4, 1, 6, 3, 1
-    spec, bank, bank_h, cache, sh = _layer_rig(L, H, I, E, k, S, K, 52700, 77300, True, seed=9)
-    assert m.moe_layer_kernel_count(spec, T) == 3  # the cooperative FFN carries the fill
+    spec, bank, bank_h, cache, sh = _layer_rig(L, H, I, E, k, S, K, 52700, 77300, True, seed=9,
+                                               sync=sync)
+    # one kernel for the whole step, or logits, control step and the cooperative FFN
+    assert m.moe_layer_kernel_count(spec, cache.c, T) == (1 if sync else 3)
     plan = m.DevicePlan(T * k, K, device=DEV)
     wsb = m.moe_layer_workspace_bytes(spec, T)
     ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
@@ -460,7 +477,7 @@ def test_wait_timeout_in_layer_step_unmaps_fills(oracle):
 
 
 # ------------------------------------------------------- fill + expert FFN
-def _layer_rig(L, H, I, E, k, S, K, bp, bh, has_shared, seed=0, big=False):
+def _layer_rig(L, H, I, E, k, S, K, bp, bh, has_shared, seed=0, big=False, sync=True):
     spec = m.make_spec(L, H, I, E, k, has_shared=has_shared)
     if big:
         bank = synth.make_bank_torch(L * E + 1, H, I, seed, DEV)
@@ -468,7 +485,7 @@ def _layer_rig(L, H, I, E, k, S, K, bp, bh, has_shared, seed=0, big=False):
     else:
         bank_h = synth.make_bank(L * E + 1, H, I, seed)
         bank = dev(bank_h, DEV)
-    cache = m.DeviceCache(spec, S, K, bp, bh, bank=bank[:L * E], device=DEV)
+    cache = m.DeviceCache(spec, S, K, bp, bh, bank=bank[:L * E], device=DEV, sync=sync)
     shared = bank[L * E] if has_shared else None
     return spec, bank, bank_h, cache, shared
 
@@ -618,7 +635,7 @@ def test_full_size_qwen_shape_decode(oracle):
     _tables_equal(cache, ost)
     # every resident slot holds its expert's blob, written by the FFN kernel that
     # carried the fill (compared on the device)
-    assert m.moe_layer_kernel_count(spec, T) == 2 + _ffn_kernels(H, I, T)
+    assert m.moe_layer_kernel_count(spec, cache.c, T) == _layer_kernels(H, I, E, k, T, K, True)
     resident = [(v, int(e)) for v, e in enumerate(ost.id_of_slot) if e >= 0]
     assert resident
     for v, e in resident:
@@ -671,7 +688,7 @@ def test_full_size_deepseek_shape_decode(oracle, T):
     _tables_equal(cache, ost)
     # every resident slot holds its expert's blob, written by the FFN kernel that
     # carried the fill (compared on the device: 24.8 MB per slot)
-    assert m.moe_layer_kernel_count(spec, T) == 2 + _ffn_kernels(H, I, T)
+    assert m.moe_layer_kernel_count(spec, cache.c, T) == _layer_kernels(H, I, E, k, T, K, True)
     resident = [(v, int(e)) for v, e in enumerate(ost.id_of_slot) if e >= 0]
     assert resident
     for v, e in resident:
