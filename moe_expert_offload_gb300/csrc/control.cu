@@ -74,7 +74,9 @@ __global__ void __launch_bounds__(kCtlThreads) cache_step_kernel(CacheArgs a, Se
   if (n <= 32) {
     // up to 32 routed ids: one warp deduplicates, ranks and classifies them in
     // registers (one block barrier instead of five)
-    if (wid == 0) ctl_classify_warp<KMAX, kCtlThreads>(a, s, n, e_early, now);
+    if (wid == 0)
+      ctl_classify_warp<true, KMAX, kCtlThreads>(a, s, n, e_early, now,
+                                                 [&](int32_t u) { return a.slot_of_id[u]; });
     __syncthreads();
     n_uniq = s.nu;
     n_hit = s.nh;

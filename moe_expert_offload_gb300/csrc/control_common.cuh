@@ -108,15 +108,16 @@ __device__ __forceinline__ void ctl_early_loads(const CacheArgs& a, uint32_t (&e
   }
 }
 
-// Up to 32 routed ids (n <= 32, lane < n holds its expert id e): warp 0
+// Up to 32 routed ids (n <= 32, lane < n holds its expert id e): one warp
 // deduplicates, ranks and classifies them in registers.  Unique bank ids
-// l*E + e go to s.suniq in ascending order (with their slots before the step
-// in s.sslot), hits to the plan in rank order with ts[slot] = now, misses to
-// s.smiss in rank order; counts to s.nu, s.nh, s.nm; an id outside [0, E)
-// sets s.bad and is skipped.  Warp 0 only; the caller syncs after it.
-template <int KMAX, int NTH>
+// l*E + e go to s.suniq in ascending order (with their slots before the step,
+// slot_of(u), in s.sslot); counts to s.nu, s.nh, s.nm; an id outside [0, E)
+// sets s.bad and is skipped.  With TABLES, also the hits to the plan in rank
+// order with ts[slot] = now and the misses to s.smiss in rank order.  The
+// caller syncs after it.
+template <bool TABLES, int KMAX, int NTH, class SlotOf>
 __device__ __forceinline__ void ctl_classify_warp(const CacheArgs& a, CtlShared<KMAX, NTH>& s,
-                                                  int n, int32_t e, uint32_t now) {
+                                                  int n, int32_t e, uint32_t now, SlotOf slot_of) {
   constexpr int kEarlySlots = CtlShared<KMAX, NTH>::kEarlySlots;
   const int lane = threadIdx.x & 31;
   int32_t v = INT_MAX;  // bank id l*E + e; INT_MAX marks an id outside [0, E)
@@ -141,11 +142,11 @@ __device__ __forceinline__ void ctl_classify_warp(const CacheArgs& a, CtlShared<
   // hit / miss in rank order, order-preserving compaction
   const bool valid = lane < nu;
   const int32_t u = valid ? s.suniq[lane] : 0;
-  const int32_t slot = valid ? a.slot_of_id[u] : -1;
+  const int32_t slot = valid ? slot_of(u) : -1;
   const bool hit = valid && slot >= 0, miss = valid && slot < 0;
   const unsigned hb = __ballot_sync(0xffffffffu, hit), mb = __ballot_sync(0xffffffffu, miss);
   if (valid) s.sslot[lane] = slot;
-  if (hit) {
+  if (TABLES && hit) {
     const int p = __popc(hb & lanemask_lt());
     a.plan.hit_ids[p] = u;
     a.plan.hit_slots[p] = slot;
@@ -153,7 +154,7 @@ __device__ __forceinline__ void ctl_classify_warp(const CacheArgs& a, CtlShared<
     const unsigned r = (unsigned)(slot - a.S0);  // the slot's place in the scanned range
     if (r < (unsigned)kEarlySlots) atomicOr(&s.shit[r >> 5], 1u << (r & 31));
   }
-  if (miss) s.smiss[__popc(mb & lanemask_lt())] = u;
+  if (TABLES && miss) s.smiss[__popc(mb & lanemask_lt())] = u;
   if (lane == 0) {
     s.nu = nu;
     s.nh = __popc(hb);

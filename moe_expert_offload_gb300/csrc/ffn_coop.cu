@@ -276,61 +276,65 @@ struct SelScratch {
   float a[kMaxTok][32 * 8];
   float b[kMaxTok][rsel::kMaxK], c[kMaxTok][rsel::kMaxK];
   float sum[kMaxTok];
+  int32_t slot[256];  // slot_of_id of the layer's E experts before the step
 };
 static_assert(sizeof(CtlSh) + sizeof(SelScratch) <= 3 * (size_t)kSlotBytes,
               "control step scratch must fit in the smallest ring");
 
-// CTA 0 of the one-kernel layer step, consumer threads (tid < 512): once
-// every CTA's logits are stored, the router selection (one warp per token),
-// then the classification of the routed ids, whose entries (ranked unique
-// ids and their slots before the step) are published for the FFN CTAs at
-// once; then the victim scan and the slot-table update, whose fill set is
-// published second (FreeToken summary "method steps").
-__device__ void layer_control(const FfnArgs& a, const LayerFuse& lf, CtlSh& cs, SelScratch& ss,
-                              const uint32_t (&early)[CtlSh::NE], const int32_t (&early_id)[CtlSh::NE],
-                              int& s_fail) {
+// Every CTA of the one-kernel layer step, consumer threads (tid < 512), once
+// every CTA's logits are stored: the router selection (one warp per token,
+// into s_ids / s_wts), then the dedup, ranks and hit / miss of the routed ids
+// against the slot table read before the logits count (FreeToken summary
+// "method steps").  Every CTA takes the same decisions from the same data, so
+// no CTA waits for another's plan; CTA 0 (ctl) also writes the routing
+// outputs, moves the hits' recency stamps and keeps the misses for the
+// victim scan.  Returns false when the logits never all arrived.
+template <bool CTL>
+__device__ bool layer_route_classify(const FfnArgs& a, const LayerFuse& lf, CtlSh& cs,
+                                     SelScratch& ss, int32_t* s_ids, float* s_wts) {
   const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
   const int T = a.T, k = a.k, E = a.E, n = T * k;
-  uint32_t* sync = lf.sync;
-  for (int i = tid; i < (int)(sizeof(cs.shit) / 4); i += kConsThreads) cs.shit[i] = 0u;
   if (tid == 0) {
     cs.bad = 0;
     cs.nu = 0;
     cs.nh = 0;
     cs.nm = 0;
-    if (!wait_count(sync + kSyncLogits, gridDim.x)) s_fail = 1;  // every CTA's logits
+    cs.nu = wait_count(lf.sync + kSyncLogits, gridDim.x) ? 0 : -1;  // every CTA's logits
   }
   cons_sync();
-  const bool ok = s_fail == 0;
-  if (ok && wid < T) {
+  if (cs.nu < 0) return false;
+  if (wid < T) {
     if (lf.router == MOE_ROUTER_SOFTMAX_TOPK)
-      rsel::softmax_token<8>(lf.logits, wid, E, k, lf.ids_out, lf.wts_out, ss.b[wid], ss.c[wid],
+      rsel::softmax_token<8>(lf.logits, wid, E, k, s_ids, s_wts, ss.b[wid], ss.c[wid],
                              &ss.sum[wid]);
     else
       rsel::sigmoid_group_token<8>(lf.logits, lf.sel_bias, wid, E, lf.n_groups, lf.topk_groups, k,
-                                   lf.scale, lf.ids_out, lf.wts_out, ss.a[wid], ss.b[wid],
-                                   &ss.sum[wid]);
+                                   lf.scale, s_ids, s_wts, ss.a[wid], ss.b[wid], &ss.sum[wid]);
   }
   cons_sync();
-  const uint32_t now = cs.now;
-  if (ok && wid == 0) {
-    const int32_t e = lane < n ? lf.ids_out[lane] : 0;
-    ctl::ctl_classify_warp<kCtlK, kConsThreads>(lf.c, cs, n, e, now);
+  if (wid == 0) {
+    const int32_t e = lane < n ? s_ids[lane] : 0;
+    const int base = a.layer * E;
+    ctl::ctl_classify_warp<CTL, kCtlK, kConsThreads>(
+        lf.c, cs, n, e, cs.now, [&](int32_t u) { return ss.slot[u - base]; });
+  } else if (CTL && wid == 1 && lane < n) {
+    lf.ids_out[lane] = s_ids[lane];
+    lf.wts_out[lane] = s_wts[lane];
   }
   cons_sync();
-  const int nu = cs.nu;
-  // the entries, for the FFN CTAs: ranked unique ids and their slots before the step
-  if (tid < nu) {
-    sync[kSyncUniq + tid] = (uint32_t)cs.suniq[tid];
-    sync[kSyncSlot + tid] = (uint32_t)cs.sslot[tid];
-  }
-  if (tid == 0) sync[kSyncNu] = (uint32_t)nu;
-  cons_sync();
-  if (tid == 0) red_release_gpu_add(sync + kSyncPlan);  // release: ids, weights, entries
-  ctl::ctl_evict<kCtlK, kConsThreads>(lf.c, cs, now, nu, cs.nh, cs.nm, early, early_id,
+  return true;
+}
+
+// CTA 0 of the one-kernel layer step, after the classification: the victim
+// scan and the slot-table update (every CTA has read the slot table before
+// the logits count), then the fill set is published for the fill writers.
+__device__ void layer_evict(const LayerFuse& lf, CtlSh& cs,
+                            const uint32_t (&early)[CtlSh::NE],
+                            const int32_t (&early_id)[CtlSh::NE]) {
+  ctl::ctl_evict<kCtlK, kConsThreads>(lf.c, cs, cs.now, cs.nu, cs.nh, cs.nm, early, early_id,
                                       ConsSync{});
   cons_sync();
-  if (tid == 0) red_release_gpu_add(sync + kSyncFill);  // release: the plan and the tables
+  if (threadIdx.x == 0) red_release_gpu_add(lf.sync + kSyncFill);  // the plan and the tables
 }
 
 template <bool FUSED>
@@ -457,17 +461,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     SelScratch& ss = *reinterpret_cast<SelScratch*>(ring + sizeof(CtlSh));
     griddep_wait();  // x, the cache tables and the pool of the previous kernels
     if (wid < kCW) {
+      const int E = a.E, np = T * E;
       if (ctl_cta) {
         // the victim scan's first stamps, and the step's clock
         ctl::ctl_early_loads<CtlSh::NE, kConsThreads>(lf.c, early, early_id);
+        for (int i = tid; i < (int)(sizeof(cs.shit) / 4); i += kConsThreads) cs.shit[i] = 0u;
         if (tid == 0) {
           cs.now = lf.c.clock[0] + 1u;
           lf.c.clock[0] = cs.now;
         }
       }
+      // the layer's slot table before the step (read before the logits count:
+      // CTA 0 changes it only after every CTA has arrived there)
+      for (int i = tid; i < E; i += kConsThreads) ss.slot[i] = lf.c.slot_of_id[a.layer * E + i];
       // router logits (the fixed order of every router path): pair p = (t, e)
       // on CTA p % Gall, warp p / Gall
-      const int E = a.E, np = T * E;
       for (int p = (int)blockIdx.x + (int)Gall * wid; p < np; p += (int)Gall * kCW) {
         const int t = p / E, e = p - t * E;
         const float v =
@@ -476,36 +484,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       cons_sync();
       if (tid == 0) red_release_gpu_add(sync + kSyncLogits);
-      if (ctl_cta) {
-        layer_control(a, lf, cs, ss, early, early_id, s_fail);
+      if (!ctl_cta) prep_x(b, G);
+      const bool routed = ctl_cta ? layer_route_classify<true>(a, lf, cs, ss, s_ids, s_wts)
+                                  : layer_route_classify<false>(a, lf, cs, ss, s_ids, s_wts);
+      if (!routed) {
+        if (tid == 0) s_fail = 1;
+      } else if (!ctl_cta) {
+        // the entries: ranked unique ids, read from their slot (hit) or the bank
+        n_uniq = cs.nu;
+        n_exec = n_uniq + a.has_shared;
+        if (tid < n_exec) {
+          const int r = tid;
+          int mi = 2, bi = 0, uid = -1;
+          if (r < n_uniq) {
+            uid = cs.suniq[r];
+            const int32_t slot = cs.sslot[r];
+            mi = slot >= 0 ? 1 : 0;
+            bi = slot >= 0 ? slot : uid;
+          }
+          s_map[r] = mi;
+          s_bi[r] = bi;
+          s_fs[r] = -1;  // an F entry's slot: learnt by the fill writer
+          s_uid[r] = uid;
+        }
       } else {
-        prep_x(b, G);
-        if (tid == 0 && !wait_count(sync + kSyncPlan, 1u)) s_fail = 1;
+        layer_evict(lf, cs, early, early_id);
       }
     }
     __syncthreads();
     if (!ctl_cta && !s_fail) {
-      // the published entries, ids and weights
-      n_uniq = (int)__ldcg(sync + kSyncNu);
+      n_uniq = cs.nu;
       n_exec = n_uniq + a.has_shared;
-      for (int i = tid; i < n_ids; i += kThreads) {
-        s_ids[i] = __ldcg(a.ids + i);
-        s_wts[i] = __ldcg(a.weights + i);
-      }
-      if (tid < n_exec) {
-        const int r = tid;
-        int mi = 2, bi = 0, uid = -1;
-        if (r < n_uniq) {
-          uid = (int)__ldcg(sync + kSyncUniq + r);
-          const int32_t slot = (int32_t)__ldcg(sync + kSyncSlot + r);
-          mi = slot >= 0 ? 1 : 0;
-          bi = slot >= 0 ? slot : uid;
-        }
-        s_map[r] = mi;
-        s_bi[r] = bi;
-        s_fs[r] = -1;  // an F entry's slot: learnt by the fill writer
-        s_uid[r] = uid;
-      }
     }
   } else {
     griddep_wait();  // the plan (and the cleared counters) of the previous kernels
@@ -546,6 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     int n = 0, s = 0, rnd = 0;  // stages issued; ring slot and round of stage n
     bool ok = !a.inject_stall;  // test hook: no copies, every wait runs out
+    const uint64_t pol = l2_evict_first();  // weights are read once per call
     auto slot_ready = [&]() {
       bool r = true;
       if (lane == 0) {
@@ -567,10 +577,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = slot_ready())) break;
         const uint32_t dst = su32(ring + (size_t)s * kSlotBytes);
         if (lane < 4)
-          tma_load_4d(dst + lane * 4096, &maps.gu_code[m], ks * 128 + 32 * lane, row0, 0, bi,
-                      su32(&full[s]));
+          tma_load_4d_ef(dst + lane * 4096, &maps.gu_code[m], ks * 128 + 32 * lane, row0, 0, bi,
+                         su32(&full[s]), pol);
         else if (lane == 4)
-          tma_load_4d(dst + kCodeBytes, &maps.gu_scale[m], ks * 8, row0, 0, bi, su32(&full[s]));
+          tma_load_4d_ef(dst + kCodeBytes, &maps.gu_scale[m], ks * 8, row0, 0, bi,
+                         su32(&full[s]), pol);
         advance();
       }
     }
@@ -580,11 +591,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = slot_ready())) break;
         const uint32_t dst = su32(ring + (size_t)s * kSlotBytes);
         if (lane < geo.nbd)
-          tma_load_3d(dst + lane * RD * 128, &maps.dn_code[m], kd * (KSD / 8) + 32 * lane, row0,
-                      bi, su32(&full[s]));
+          tma_load_3d_ef(dst + lane * RD * 128, &maps.dn_code[m], kd * (KSD / 8) + 32 * lane,
+                         row0, bi, su32(&full[s]), pol);
         else if (lane == geo.nbd)
-          tma_load_4d(dst + kCodeBytes, &maps.dn_scale[m], kd * (KSD / 128), row0, 0, bi,
-                      su32(&full[s]));
+          tma_load_4d_ef(dst + kCodeBytes, &maps.dn_scale[m], kd * (KSD / 128), row0, 0, bi,
+                         su32(&full[s]), pol);
         advance();
       }
     }
@@ -606,6 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       bool ok = true;
+      const uint64_t pol = l2_evict_first();  // the slot is not read again in this call
       // (one-kernel step) the F entries' slots are learnt at the first entry
       // read from the bank, once the control step has published its fills
       bool known = !FUSED;
@@ -640,9 +652,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t src = su32(ring + (size_t)s * kSlotBytes);
             fence_proxy_async_smem();
             if (lane < 4)
-              tma_store_4d(&maps.gu_code[1], ks * 128 + 32 * lane, row0, 0, fs, src + lane * 4096);
+              tma_store_4d_ef(&maps.gu_code[1], ks * 128 + 32 * lane, row0, 0, fs,
+                              src + lane * 4096, pol);
             else
-              tma_store_4d(&maps.gu_scale[1], ks * 8, row0, 0, fs, src + kCodeBytes);
+              tma_store_4d_ef(&maps.gu_scale[1], ks * 8, row0, 0, fs, src + kCodeBytes, pol);
             bulk_commit();
             bulk_read_done();
           }
@@ -658,10 +671,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t src = su32(ring + (size_t)s * kSlotBytes);
             fence_proxy_async_smem();
             if (lane < geo.nbd)
-              tma_store_3d(&maps.dn_code[1], kd * (KSD / 8) + 32 * lane, row0, fs,
-                           src + lane * RD * 128);
+              tma_store_3d_ef(&maps.dn_code[1], kd * (KSD / 8) + 32 * lane, row0, fs,
+                              src + lane * RD * 128, pol);
             else
-              tma_store_4d(&maps.dn_scale[1], kd * (KSD / 128), row0, 0, fs, src + kCodeBytes);
+              tma_store_4d_ef(&maps.dn_scale[1], kd * (KSD / 128), row0, 0, fs,
+                              src + kCodeBytes, pol);
             bulk_commit();
             bulk_read_done();
           }

@@ -108,11 +108,9 @@ constexpr int kSelFusedMaxT = 16, kSelFusedMaxE = 256;
 // One-kernel decode layer step (ffn_coop.cu): the router logits, the
 // selection and the control step run inside the cooperative decode FFN
 // kernel.  Layout of the cache's sync words (moe_cache.sync, zero between
-// steps): the logits count, the two publication flags (entries, fills), the
-// published entries (count, ranked unique ids, their slots before the step),
-// then the FFN's counter block (FfnArgs::ctr).
-constexpr int kSyncLogits = 0, kSyncPlan = 1, kSyncFill = 2, kSyncNu = 3, kSyncUniq = 4,
-              kSyncSlot = 36, kSyncCtr = 68;
+// steps): the logits count, the fill publication flag, then the FFN's counter
+// block (FfnArgs::ctr).
+constexpr int kSyncLogits = 0, kSyncFill = 1, kSyncCtr = 4;
 struct LayerFuse {
   const uint16_t* w_router = nullptr;  // [E][H] bf16
   const float* sel_bias = nullptr;     // [E] or null (sigmoid-group selection)

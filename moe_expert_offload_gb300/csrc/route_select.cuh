@@ -104,141 +104,257 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
   }
 }
 
-// Softmax-top-k of token t, one warp; lane j holds experts j + 32 i.  Scratch
-// in shared memory: sv, sex [kMaxK], ssum [1].
+// Unsigned key with the order of the fp32 values (larger value <=> larger
+// key; -0 and +0 share a key, so equal values tie); a NaN gets key 1, below
+// every number.  Key 0 marks an entry that is out of the race.  Branch-free,
+// so that the loads feeding it stay in flight together.
+__device__ __forceinline__ uint32_t ord_key(float v) {
+  const uint32_t u = __float_as_uint(__fadd_rn(v, 0.0f));  // -0 -> +0
+  const uint32_t k = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (v != v) ? 1u : k;
+}
+
+// Compare-exchange of (key, slot) pairs into descending order of `better`:
+// larger key first, the lower slot first among equal keys.
+__device__ __forceinline__ void cex_desc(uint32_t& ka, uint32_t& ia, uint32_t& kb, uint32_t& ib) {
+  const bool sw = kb > ka || (kb == ka && ib < ia);
+  const uint32_t k0 = sw ? kb : ka, i0 = sw ? ib : ia, k1 = sw ? ka : kb, i1 = sw ? ia : ib;
+  ka = k0;
+  ia = i0;
+  kb = k1;
+  ib = i1;
+}
+
+// The lane's N (a power of two) candidates sorted into descending order by
+// Batcher's odd-even merge sort (a fixed network: every index is a constant).
+template <int N>
+__device__ __forceinline__ void lane_sort_desc(uint32_t (&key)[N], uint32_t (&slot)[N]) {
+#pragma unroll
+  for (int p = 1; p < N; p <<= 1)
+#pragma unroll
+    for (int q = p; q >= 1; q >>= 1)
+#pragma unroll
+      for (int j = q % p; j + q < N; j += 2 * q)
+#pragma unroll
+        for (int i = 0; i < q; ++i)
+          if (i + j + q < N && (i + j) / (2 * p) == (i + j + q) / (2 * p))
+            cex_desc(key[i + j], slot[i + j], key[i + j + q], slot[i + j + q]);
+}
+
+// The warp's k best candidates in the order of `better`: lane j holds
+// candidates e = j + 32 slot, sorted per lane (key 0: out).  Each round the
+// warp takes the largest head key, the lowest index among the lanes holding
+// it, and that lane pops its head.  Rank r's index goes to lane r % 32
+// (rid[r / 32]); with no candidate left, 0x7fffffff.
+template <int N>
+__device__ __forceinline__ void warp_topk(uint32_t (&key)[N], uint32_t (&slot)[N], int k,
+                                          int (&rid)[2]) {
+  const int lane = threadIdx.x & 31;
+  rid[0] = rid[1] = 0x7fffffff;
+  for (int r = 0; r < k; ++r) {
+    const uint32_t M = __reduce_max_sync(0xffffffffu, key[0]);
+    const uint32_t mine = (M != 0u && key[0] == M) ? (uint32_t)(lane + 32 * slot[0]) : 0xffffffffu;
+    const uint32_t emin = __reduce_min_sync(0xffffffffu, mine);
+    if (mine == emin) {
+#pragma unroll
+      for (int i = 0; i < N - 1; ++i) {
+        key[i] = key[i + 1];
+        slot[i] = slot[i + 1];
+      }
+      key[N - 1] = 0u;
+    }
+    const int id = M != 0u ? (int)emin : 0x7fffffff;
+    if (r == lane) rid[0] = id;
+    if (r == lane + 32) rid[1] = id;
+  }
+}
+
+// v[id / 32] of lane id % 32, for the id each lane asks for (0 for 0x7fffffff).
+template <int N>
+__device__ __forceinline__ float warp_fetch(const float (&v)[N], int id) {
+  float r = 0.0f;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const float x = __shfl_sync(0xffffffffu, v[i], id & 31);
+    if ((id >> 5) == i) r = x;
+  }
+  return r;
+}
+
+// Softmax-top-k of token t, one warp; lane j holds experts j + 32 i.  The k
+// winners in the order of `better` (larger logit first, lower index among
+// equal logits); weights exp(l_r - l_0) / S with S the fixed-order sum
+// r = 0, 1, ..., k-1 from 0 (k <= kMaxK).  The trailing scratch pointers are
+// unused (kept for the callers' layout).
 template <int EPL>
 __device__ __forceinline__ void softmax_token(const float* __restrict__ logits, int t, int E,
                                               int k, int32_t* __restrict__ ids,
-                                              float* __restrict__ wts, float* sv, float* sex,
-                                              float* ssum) {
+                                              float* __restrict__ wts, float*, float*, float*) {
   const int lane = threadIdx.x & 31;
   float v[EPL];
-  uint32_t taken = 0;
+  uint32_t key[EPL], slot[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i)
+    v[i] = (lane + 32 * i < E) ? __ldcg(logits + (size_t)t * E + lane + 32 * i) : 0.0f;
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
-    const int e = lane + 32 * i;
-    v[i] = (e < E) ? __ldcg(logits + (size_t)t * E + e) : -FLT_MAX;
-    if (e >= E) taken |= 1u << i;
+    key[i] = (lane + 32 * i < E) ? ord_key(v[i]) : 0u;
+    slot[i] = (uint32_t)i;
   }
-  for (int r = 0; r < k; ++r) {
-    float bv = -FLT_MAX;
-    int bi = 0x7fffffff;
+  lane_sort_desc<EPL>(key, slot);
+  int rid[2];
+  warp_topk<EPL>(key, slot, k, rid);
+  const float top = warp_fetch<EPL>(v, __shfl_sync(0xffffffffu, rid[0], 0));
+  float ex[2] = {0.0f, 0.0f};
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int e = lane + 32 * i;
-      if (!(taken >> i & 1u) && better(v[i], e, bv, bi)) {
-        bv = v[i];
-        bi = e;
-      }
-    }
-    warp_argmax(bv, bi);
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (lane == 0) {
-      sv[r] = bv;
-      ids[(size_t)t * k + r] = bi;
+  for (int h = 0; h < 2; ++h) {
+    const float lv = warp_fetch<EPL>(v, rid[h]);
+    if (lane + 32 * h < k) ex[h] = moe_exp(__fsub_rn(lv, top));
+  }
+  float S = 0.0f;
+  for (int r = 0; r < k; ++r)
+    S = __fadd_rn(S, __shfl_sync(0xffffffffu, r < 32 ? ex[0] : ex[1], r & 31));
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int r = lane + 32 * h;
+    if (r < k) {
+      ids[(size_t)t * k + r] = rid[h];
+      wts[(size_t)t * k + r] = __fdiv_rn(ex[h], S);
     }
   }
-  __syncwarp();
-  if (lane == 0) {
-    const float top = sv[0];
-    float S = 0.0f;
-    for (int r = 0; r < k; ++r) {
-      const float ex = moe_exp(__fsub_rn(sv[r], top));
-      sex[r] = ex;
-      S = __fadd_rn(S, ex);
-    }
-    ssum[0] = S;
-  }
-  __syncwarp();
-  for (int r = lane; r < k; r += 32) wts[(size_t)t * k + r] = __fdiv_rn(sex[r], ssum[0]);
 }
 
-// Sigmoid-group selection of token t, one warp (n_groups <= 32, E <= 32 * EPL).
-// Scratch in shared memory: ssel [32 * EPL], ss [kMaxK], ssum [1].
+// Sigmoid-group selection of token t, one warp (n_groups <= 32, E <= 32 * EPL):
+// s = sigmoid(logit), selection score s + bias; group score = the sum of the
+// two largest selection scores of the group; the topk_groups best groups
+// (order of `better`) are kept and the k best selection scores among their
+// experts win; weights s_r / S * scale, S the fixed-order sum of the winners'
+// s.  Scratch in shared memory (groups narrower than 32 experts only): ssel
+// [32 * EPL]; the other scratch pointers are unused.
 template <int EPL>
 __device__ __forceinline__ void sigmoid_group_token(const float* __restrict__ logits,
                                                     const float* __restrict__ bias, int t, int E,
                                                     int n_groups, int topk_groups, int k,
                                                     float scale, int32_t* __restrict__ ids,
-                                                    float* __restrict__ wts, float* ssel,
-                                                    float* ss, float* ssum) {
+                                                    float* __restrict__ wts, float* ssel, float*,
+                                                    float*) {
   const int lane = threadIdx.x & 31;
   const int gsz = E / n_groups;
-  float s[EPL], sel[EPL];
+  float s[EPL], sel[EPL], bv[EPL];
+  uint32_t key[EPL], slot[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
-    const int e = lane + 32 * i;
-    if (e < E) {
-      s[i] = moe_sigmoid(__ldcg(logits + (size_t)t * E + e));
-      sel[i] = __fadd_rn(s[i], bias ? bias[e] : 0.0f);
-      ssel[e] = sel[i];
-    } else {
-      s[i] = 0.0f;
-      sel[i] = -FLT_MAX;
-    }
+    const bool in = lane + 32 * i < E;
+    s[i] = in ? __ldcg(logits + (size_t)t * E + lane + 32 * i) : 0.0f;
+    bv[i] = (in && bias) ? bias[lane + 32 * i] : 0.0f;
   }
-  __syncwarp();
-  // group score: sum of the two largest selection scores of the group
-  float gscore = -FLT_MAX;
-  if (lane < n_groups) {
-    float t1 = -FLT_MAX, t2 = -FLT_MAX;
-    for (int e = lane * gsz; e < (lane + 1) * gsz; ++e) {
-      const float z = ssel[e];
-      if (z > t1) {
-        t2 = t1;
-        t1 = z;
-      } else if (z > t2) {
-        t2 = z;
-      }
-    }
-    gscore = __fadd_rn(t1, t2);
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const bool in = lane + 32 * i < E;
+    s[i] = in ? moe_sigmoid(s[i]) : 0.0f;
+    sel[i] = in ? __fadd_rn(s[i], bv[i]) : -FLT_MAX;
   }
+  // group score: sum of the two largest selection scores of the group; t1 >= t2
+  // (t2 == t1 when the largest appears twice)
   uint32_t kept = 0;  // bit g: group g kept
-  uint32_t gtaken = (lane < n_groups) ? 0u : 1u;
-  for (int r = 0; r < topk_groups; ++r) {
-    float bv = gtaken ? -FLT_MAX : gscore;
-    int bi = gtaken ? 0x7fffffff : lane;
-    warp_argmax(bv, bi);
-    if (bi == lane) gtaken = 1;
-    kept |= 1u << bi;
+  if (gsz % 32 == 0) {
+    // group g = register rows i in [g gsz/32, (g+1) gsz/32) of every lane: the
+    // lane's two largest, then the warp's two largest (all lanes get every score)
+    const int rows = gsz >> 5;
+    float gs[EPL];  // n_groups <= EPL here
+#pragma unroll
+    for (int g = 0; g < EPL; ++g) {
+      gs[g] = -FLT_MAX;
+      if (g < n_groups) {
+        float t1 = -FLT_MAX, t2 = -FLT_MAX;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i)
+          if (i >= g * rows && i < (g + 1) * rows) {
+            const float z = sel[i];
+            if (z > t1) {
+              t2 = t1;
+              t1 = z;
+            } else if (z > t2) {
+              t2 = z;
+            }
+          }
+        const uint32_t k1 = ord_key(t1), k2 = ord_key(t2);
+        const uint32_t m1 = __reduce_max_sync(0xffffffffu, k1);
+        const unsigned at = __ballot_sync(0xffffffffu, k1 == m1);
+        // second largest: m1 again when two lanes hold it, else the larger of the
+        // other lanes' first and the holder's second
+        const uint32_t c2 = k1 == m1 ? k2 : k1;
+        const uint32_t m2 = __popc(at) > 1 ? m1 : __reduce_max_sync(0xffffffffu, c2);
+        const float v1 = __shfl_sync(0xffffffffu, t1, __ffs(at) - 1);
+        const unsigned at2 = __ballot_sync(0xffffffffu, c2 == m2);
+        const float v2c = __shfl_sync(0xffffffffu, k1 == m1 ? t2 : t1, __ffs(at2) - 1);
+        gs[g] = __fadd_rn(v1, __popc(at) > 1 ? v1 : v2c);
+      }
+    }
+    // the topk_groups best groups, computed alike by every lane
+    for (int r = 0; r < topk_groups; ++r) {
+      float bvg = -FLT_MAX;
+      int bg = 0x7fffffff;
+#pragma unroll
+      for (int g = 0; g < EPL; ++g)
+        if (g < n_groups && !(kept >> g & 1u) && better(gs[g], g, bvg, bg)) {
+          bvg = gs[g];
+          bg = g;
+        }
+      kept |= 1u << bg;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (lane + 32 * i < E) ssel[lane + 32 * i] = sel[i];
+    __syncwarp();
+    float gscore = -FLT_MAX;
+    if (lane < n_groups) {
+      float t1 = -FLT_MAX, t2 = -FLT_MAX;
+      for (int e = lane * gsz; e < (lane + 1) * gsz; ++e) {
+        const float z = ssel[e];
+        if (z > t1) {
+          t2 = t1;
+          t1 = z;
+        } else if (z > t2) {
+          t2 = z;
+        }
+      }
+      gscore = __fadd_rn(t1, t2);
+    }
+    uint32_t gtaken = (lane < n_groups) ? 0u : 1u;
+    for (int r = 0; r < topk_groups; ++r) {
+      float bvg = gtaken ? -FLT_MAX : gscore;
+      int bi = gtaken ? 0x7fffffff : lane;
+      warp_argmax(bvg, bi);
+      if (bi == lane) gtaken = 1;
+      kept |= 1u << bi;
+    }
+    __syncwarp();
   }
-  uint32_t taken = 0;
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = lane + 32 * i;
-    if (e >= E || !((kept >> (e / gsz)) & 1u)) taken |= 1u << i;
+    key[i] = (e < E && ((kept >> (e / gsz)) & 1u)) ? ord_key(sel[i]) : 0u;
+    slot[i] = (uint32_t)i;
   }
-  for (int r = 0; r < k; ++r) {
-    float bv = -FLT_MAX;
-    int bi = 0x7fffffff;
-    float bs = 0.0f;
+  lane_sort_desc<EPL>(key, slot);
+  int rid[2];
+  warp_topk<EPL>(key, slot, k, rid);
+  float rs[2];
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int e = lane + 32 * i;
-      if (!(taken >> i & 1u) && better(sel[i], e, bv, bi)) {
-        bv = sel[i];
-        bi = e;
-        bs = s[i];
-      }
-    }
-    const int mine = bi;
-    warp_argmax(bv, bi);
-    const bool win = (bi == mine) && ((bi & 31) == lane);
-    if (win) {
-      taken |= 1u << (bi >> 5);
-      ss[r] = bs;
-      ids[(size_t)t * k + r] = bi;
+  for (int h = 0; h < 2; ++h) rs[h] = warp_fetch<EPL>(s, rid[h]);
+  float S = 0.0f;
+  for (int r = 0; r < k; ++r)
+    S = __fadd_rn(S, __shfl_sync(0xffffffffu, r < 32 ? rs[0] : rs[1], r & 31));
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int r = lane + 32 * h;
+    if (r < k) {
+      ids[(size_t)t * k + r] = rid[h];
+      wts[(size_t)t * k + r] = __fmul_rn(__fdiv_rn(rs[h], S), scale);
     }
   }
-  __syncwarp();
-  if (lane == 0) {
-    float S = 0.0f;
-    for (int r = 0; r < k; ++r) S = __fadd_rn(S, ss[r]);
-    ssum[0] = S;
-  }
-  __syncwarp();
-  for (int r = lane; r < k; r += 32)
-    wts[(size_t)t * k + r] = __fmul_rn(__fdiv_rn(ss[r], ssum[0]), scale);
 }
 
 }  // namespace rsel

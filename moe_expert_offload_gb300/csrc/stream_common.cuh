@@ -167,6 +167,51 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// L2 policy for data read or written once per call (streamed weights): first
+// in line for eviction, so that it does not push out what stays hot across
+// calls (kernel code, cache tables, router weights).
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void tma_load_4d_ef(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                               int z, int w, uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar), "l"(pol)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_ef(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                               int z, uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(pol)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_store_4d_ef(const CUtensorMap* map, int x, int y, int z,
+                                                int w, uint32_t src, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group.L2::cache_hint"
+      " [%0, {%1, %2, %3, %4}], [%5], %6;" ::"l"(map),
+      "r"(x), "r"(y), "r"(z), "r"(w), "r"(src), "l"(pol)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_store_3d_ef(const CUtensorMap* map, int x, int y, int z,
+                                                uint32_t src, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint"
+      " [%0, {%1, %2, %3}], [%4], %5;" ::"l"(map),
+      "r"(x), "r"(y), "r"(z), "r"(src), "l"(pol)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, int x, int y, int z, int w,
                                              uint32_t src) {
   asm volatile(
