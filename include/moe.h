@@ -78,6 +78,22 @@ enum {
 
 enum { MOE_ROUTER_SOFTMAX_TOPK = 0, MOE_ROUTER_SIGMOID_GROUP = 1 };
 
+/* Expert weight formats (moe_spec.format).  The pages' deployed models keep
+ * their experts in NVFP4 (Qwen3.6, GLM-5.2) or MXFP4 (DeepSeek-V4-Flash)
+ * (FreeToken summary "Key results" table); Edge0 §2 "Quantisation" uses int4
+ * affine.  FP4 elements are E2M1 (1 sign, 2 exponent, 1 mantissa bit, bias 1)
+ * with one scale per block of a row: MXFP4 blocks of 32 with an E8M0 scale
+ * 2^(e - 127); NVFP4 blocks of 16 with an FP8 E4M3 scale times one fp32 scale
+ * per matrix.  FP4 blob layout (moe_expert_bytes):
+ *   Wg codes [I][H/2] | Wu codes [I][H/2] | Wd codes [H][I/2]   (low nibble =
+ *   even column) | Wg scales [I][H/B] | Wu scales [I][H/B] | Wd scales [H][I/B]
+ *   (one byte per block) | NVFP4: fp32 matrix scales of Wg, Wu, Wd
+ * rounded up to 256 bytes.  FP4 experts run in the decode FFN where its
+ * one-kernel form serves the shape (hidden % 1024 == 0, inter % 512 == 0,
+ * T <= 8); MXFP4 block scales must lie in 2^-32 .. 2^7 (E8M0 bytes 95..134:
+ * smaller ones contribute 0, larger ones overflow).  Prefill: int4 only. */
+enum { MOE_FORMAT_INT4 = 0, MOE_FORMAT_MXFP4 = 1, MOE_FORMAT_NVFP4 = 2 };
+
 /* Device-side error bits written to plan->err[0] (OR-ed, never cleared by the
  * library; the caller may zero it). */
 enum { MOE_DERR_BAD_ID = 1, MOE_DERR_WAIT = 2 };
@@ -94,9 +110,10 @@ typedef struct moe_spec {
   int32_t n_groups;     /* sigmoid-group: expert groups (E % n_groups == 0) */
   int32_t topk_groups;  /* sigmoid-group: groups kept per token */
   float routed_scale;   /* sigmoid-group: factor applied after renormalising */
-  int32_t group_size;   /* quantisation group, must be 64 */
+  int32_t group_size;   /* int4 quantisation group, must be 64 (FP4 formats fix their own) */
   int32_t has_shared;   /* 1: an always-on shared expert, added with weight 1 */
   int32_t shared_inter; /* its intermediate size (must equal inter) */
+  int32_t format;       /* MOE_FORMAT_*: expert weight format (0: int4 affine) */
 } moe_spec;
 
 /* Replacement policy of a slot cache (moe_cache.policy).  FreeToken's own

@@ -48,7 +48,11 @@ class MoeSpec(C.Structure):
                 ("num_experts", C.c_int32), ("top_k", C.c_int32), ("router", C.c_int32),
                 ("n_groups", C.c_int32), ("topk_groups", C.c_int32), ("routed_scale", C.c_float),
                 ("group_size", C.c_int32), ("has_shared", C.c_int32),
-                ("shared_inter", C.c_int32)]
+                ("shared_inter", C.c_int32), ("format", C.c_int32)]
+
+
+# moe_spec.format values (include/moe.h)
+FORMAT_INT4, FORMAT_MXFP4, FORMAT_NVFP4 = 0, 1, 2
 
 
 class MoeCache(C.Structure):
@@ -279,11 +283,12 @@ def moe_layer_forward_prefill(spec, layer_experts, x, T, w_router, bias, shared,
 
 # ------------------------------------------------- device memory (plumbing)
 def make_spec(num_layers, hidden, inter, num_experts, top_k, router="softmax", n_groups=1,
-              topk_groups=1, routed_scale=1.0, has_shared=False, shared_inter=None) -> MoeSpec:
+              topk_groups=1, routed_scale=1.0, has_shared=False, shared_inter=None,
+              fmt=FORMAT_INT4) -> MoeSpec:
     return MoeSpec(num_layers, hidden, inter, num_experts, top_k,
                    MOE_ROUTER_SIGMOID_GROUP if router == "sigmoid_group" else
                    MOE_ROUTER_SOFTMAX_TOPK, n_groups, topk_groups, routed_scale, 64,
-                   1 if has_shared else 0, shared_inter if shared_inter else inter)
+                   1 if has_shared else 0, shared_inter if shared_inter else inter, fmt)
 
 
 class DeviceCache:

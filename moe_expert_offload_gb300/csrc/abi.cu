@@ -42,7 +42,11 @@ int check_spec(const moe_spec* s) {
     return fail(MOE_EINVAL, "num_experts must be in 1..%d", moe::kMaxExperts);
   if (s->top_k < 1 || s->top_k > s->num_experts || s->top_k > 64)
     return fail(MOE_EINVAL, "top_k must be in 1..min(num_experts, 64)");
-  if (s->group_size != moe::kGroup) return fail(MOE_EUNSUPPORTED, "group_size must be 64");
+  if (s->format != MOE_FORMAT_INT4 && s->format != MOE_FORMAT_MXFP4 &&
+      s->format != MOE_FORMAT_NVFP4)
+    return fail(MOE_EINVAL, "unknown expert format %d", s->format);
+  if (s->format == MOE_FORMAT_INT4 && s->group_size != moe::kGroup)
+    return fail(MOE_EUNSUPPORTED, "group_size must be 64");
   if ((int64_t)s->num_layers * s->num_experts > (int64_t)1 << 30)
     return fail(MOE_EINVAL, "num_layers * num_experts too large");
   if (s->router == MOE_ROUTER_SIGMOID_GROUP) {
@@ -150,9 +154,9 @@ int do_cache_step(const moe_spec* spec, moe_cache* c, int32_t layer, const int32
   cudaError_t e = moe::launch_cache_step(a, st);
   if (e != cudaSuccess) return cuda_fail(e, "cache step launch");
   if (do_fill) {
-    const moe::BlobOffsets off = moe::blob_offsets(spec->hidden, spec->inter);
     e = moe::launch_fill_copy(*plan, c->k_victims, static_cast<const uint8_t*>(c->bank),
-                              static_cast<uint8_t*>(c->slot_pool), off.total, st);
+                              static_cast<uint8_t*>(c->slot_pool),
+                              moe::expert_blob_bytes(spec->hidden, spec->inter, spec->format), st);
     if (e != cudaSuccess) return cuda_fail(e, "fill copy launch");
   }
   return MOE_OK;
@@ -220,7 +224,8 @@ moe::FfnArgs ffn_args(const moe_spec* spec, const moe_cache* c, int32_t layer,
   a.layer = layer;
   a.T = T;
   a.has_shared = spec->has_shared;
-  a.blob_bytes = moe::blob_offsets(a.H, a.I).total;
+  a.format = spec->format;
+  a.blob_bytes = moe::expert_blob_bytes(a.H, a.I, a.format);
   a.bank = static_cast<const uint8_t*>(c->bank);
   a.pool = static_cast<const uint8_t*>(c->slot_pool);
   a.n_bank = spec->num_layers * spec->num_experts;
@@ -259,6 +264,10 @@ int do_ffn(const moe_spec* spec, const moe_cache* c, int32_t layer, const moe_pl
   const size_t need = moe::ffn_workspace_bytes(spec->hidden, spec->inter, spec->top_k, T,
                                                spec->has_shared);
   if (ws_bytes < need) return fail(MOE_ECAPACITY, "workspace %zu < %zu bytes", ws_bytes, need);
+  if (spec->format != MOE_FORMAT_INT4 &&
+      !moe::ffn_coop_supported(spec->hidden, spec->inter, spec->top_k, T, spec->has_shared))
+    return fail(MOE_EUNSUPPORTED,
+                "FP4 experts need hidden %% 1024 == 0, inter %% 512 == 0 and T <= 8");
   moe::FfnArgs a = ffn_args(spec, c, layer, plan, x, T, ids, weights, shared, ws, y, fuse_fill);
   cudaError_t e = moe::launch_ffn_decode(a, st, ctr_zeroed);
   if (e != cudaSuccess) return cuda_fail(e, "decode FFN launch");
@@ -277,7 +286,7 @@ const char* moe_version(void) { return "moe-gb300 0.1 (sm_103a)"; }
 
 size_t moe_expert_bytes(const moe_spec* spec) {
   if (check_spec(spec) != MOE_OK) return 0;
-  return (size_t)moe::blob_offsets(spec->hidden, spec->inter).total;
+  return (size_t)moe::expert_blob_bytes(spec->hidden, spec->inter, spec->format);
 }
 
 int moe_route(const moe_spec* spec, const void* x, int32_t T, const void* w_router,
@@ -342,7 +351,7 @@ int moe_cache_place(const moe_spec* spec, moe_cache* cache, const int32_t* ids, 
   if (e == cudaSuccess && cache->sync)
     e = cudaMemsetAsync(cache->sync, 0, MOE_CACHE_SYNC_WORDS * sizeof(uint32_t), st);
   if (cache->slot_pool && cache->bank) {
-    const int64_t blob = moe::blob_offsets(spec->hidden, spec->inter).total;
+    const int64_t blob = moe::expert_blob_bytes(spec->hidden, spec->inter, spec->format);
     for (int32_t i = 0; i < n && e == cudaSuccess; ++i) {
       const int32_t u = ids[i];
       e = cudaMemcpyAsync(static_cast<uint8_t*>(cache->slot_pool) + slot_of_id[(size_t)u] * blob,
@@ -510,9 +519,10 @@ int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, con
     e = moe::launch_cache_step_sel(a, sa, st);
     if (e != cudaSuccess) return cuda_fail(e, "control step launch");
     if (!ss && !fused_fill) {
-      const moe::BlobOffsets off = moe::blob_offsets(spec->hidden, spec->inter);
       e = moe::launch_fill_copy(*plan, cache->k_victims, static_cast<const uint8_t*>(cache->bank),
-                                static_cast<uint8_t*>(cache->slot_pool), off.total, st);
+                                static_cast<uint8_t*>(cache->slot_pool),
+                                moe::expert_blob_bytes(spec->hidden, spec->inter, spec->format),
+                                st);
       if (e != cudaSuccess) return cuda_fail(e, "fill copy launch");
     }
   } else {
@@ -526,9 +536,10 @@ int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, con
     cudaError_t e = cudaEventRecord(ss->fork, st);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->s, ss->fork, 0);
     if (e != cudaSuccess) return cuda_fail(e, "fill fork");
-    const moe::BlobOffsets off = moe::blob_offsets(spec->hidden, spec->inter);
     e = moe::launch_fill_copy(*plan, cache->k_victims, static_cast<const uint8_t*>(cache->bank),
-                              static_cast<uint8_t*>(cache->slot_pool), off.total, ss->s);
+                              static_cast<uint8_t*>(cache->slot_pool),
+                              moe::expert_blob_bytes(spec->hidden, spec->inter, spec->format),
+                              ss->s);
     if (e == cudaSuccess) e = cudaEventRecord(ss->join, ss->s);
     if (e != cudaSuccess) return cuda_fail(e, "fill copy launch");
   }
@@ -556,7 +567,7 @@ struct ProfLayout {
 
 ProfLayout prof_layout(const moe_spec* s) {
   ProfLayout L;
-  const size_t se = moe::blob_offsets(s->hidden, s->inter).total;
+  const size_t se = moe::expert_blob_bytes(s->hidden, s->inter, s->format);
   const size_t k = (size_t)s->top_k;
   size_t o = 0;
   auto take = [&](size_t b) {
@@ -628,7 +639,7 @@ extern "C" int moe_profile_bandwidths(const moe_spec* spec, const moe_cache* cac
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   auto i32 = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
   const int E = spec->num_experts, k = spec->top_k;
-  const int64_t se = moe::blob_offsets(spec->hidden, spec->inter).total;
+  const int64_t se = moe::expert_blob_bytes(spec->hidden, spec->inter, spec->format);
 
   // fill plan: experts 0, 1 of the layer into scratch blobs 0, 1
   int32_t hc[8] = {0, 0, 0, 0, kProfCopies, 0, 0, 0};
@@ -678,6 +689,7 @@ extern "C" int moe_profile_bandwidths(const moe_spec* spec, const moe_cache* cac
   a.layer = layer;
   a.T = 1;
   a.has_shared = 0;
+  a.format = spec->format;
   a.blob_bytes = se;
   a.bank = bank;
   a.pool = static_cast<const uint8_t*>(cache->slot_pool);
@@ -716,6 +728,7 @@ int check_prefill(const moe_spec* s, int32_t T) {
   if (s->hidden % 256 || s->inter % 128)
     return fail(MOE_EUNSUPPORTED, "prefill needs hidden %% 256 == 0 and inter %% 128 == 0");
   if (s->num_experts > 1023) return fail(MOE_EUNSUPPORTED, "prefill supports num_experts <= 1023");
+  if (s->format != MOE_FORMAT_INT4) return fail(MOE_EUNSUPPORTED, "prefill supports int4 experts");
   if ((int64_t)T * (s->top_k + 1) > ((int64_t)1 << 30)) return fail(MOE_EINVAL, "T too large");
   return MOE_OK;
 }
@@ -769,7 +782,7 @@ extern "C" int moe_layer_prefetch(const moe_spec* spec, const void* bank, int32_
   if (rc) return rc;
   if (layer < 0 || layer >= spec->num_layers) return fail(MOE_EINVAL, "layer out of range");
   if (!bank || !dst) return fail(MOE_EINVAL, "moe_layer_prefetch: NULL argument");
-  const size_t se = (size_t)moe::blob_offsets(spec->hidden, spec->inter).total;
+  const size_t se = (size_t)moe::expert_blob_bytes(spec->hidden, spec->inter, spec->format);
   const size_t bytes = se * spec->num_experts;
   const uint8_t* src = static_cast<const uint8_t*>(bank) + (size_t)layer * bytes;
   cudaError_t e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, (cudaStream_t)stream);

@@ -188,6 +188,86 @@ __device__ __forceinline__ void group2(float (&d0)[4], float (&d1)[4], uint2 l0,
   mma_cvt<false>(d1, l1.y >> 8, h1.y >> 8, b[6], b[7], c);
 }
 
+// ------------------------------------------------------------ FP4 operands
+// An FP4 weight is e2m1(code) * block scale.  Both factors are exact in fp16
+// and so is their product for an NVFP4 block (|e2m1| <= 6, E4M3 in
+// [2^-9, 448]); an MXFP4 block's E8M0 power of two enters as 2^(e - 127 + 8)
+// (the 2^-8 is applied back in fp32), exact for E8M0 bytes 95..134.  The
+// product goes into the MMA's A operand, so the fp32 accumulator sums
+// dequantised weights times x with no per-block correction; the NVFP4 matrix
+// scale is applied in fp32 after the sum.
+constexpr int kMxBias = 8;
+
+// fp16x2 {s, s} of one block scale byte.
+template <int FMT>
+__device__ __forceinline__ uint32_t fp4_scale2(uint32_t byte) {
+  uint32_t r;
+  if constexpr (FMT == MOE_FORMAT_NVFP4) {
+    const uint16_t pair = (uint16_t)(byte | (byte << 8));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(pair));
+  } else {
+    const int e = (int)byte - 127 + kMxBias;  // 2^e in fp16
+    uint32_t h;
+    if (byte == 255u) h = 0x7E00u;           // NaN
+    else if (e > 15) h = 0x7C00u;            // beyond fp16: inf
+    else if (e >= -14) h = (uint32_t)(e + 15) << 10;
+    else if (e >= -24) h = 1u << (e + 24);   // fp16 subnormal, still exact
+    else h = 0u;
+    r = h | (h << 16);
+  }
+  return r;
+}
+
+// D += A B (m16n8k16, fp16 in, fp32 accumulate) with A from E2M1 codes:
+// word wl of row g and wh of row g + 8 (8 codes each, columns 8j .. 8j + 7 of
+// the lane's 16), bytes 2 HB (columns +4HB, +4HB+1: k slots 2t, 2t+1) and
+// 2 HB + 1 (+4HB+2, +4HB+3: k slots 2t+8, 2t+9), each times its row's block
+// scale (sl, sh).
+template <int HB>
+__device__ __forceinline__ void mma_fp4(float (&d)[4], uint32_t wl, uint32_t wh, uint32_t sl,
+                                        uint32_t sh, uint32_t b0, uint32_t b1) {
+  if (HB == 0) {
+    asm("{\n .reg .b8 l0, l1, l2, l3, h0, h1, h2, h3;\n .reg .b32 a0, a1, a2, a3;\n"
+        " mov.b32 {l0, l1, l2, l3}, %4;\n mov.b32 {h0, h1, h2, h3}, %5;\n"
+        " cvt.rn.f16x2.e2m1x2 a0, l0;\n cvt.rn.f16x2.e2m1x2 a1, h0;\n"
+        " cvt.rn.f16x2.e2m1x2 a2, l1;\n cvt.rn.f16x2.e2m1x2 a3, h1;\n"
+        " mul.rn.f16x2 a0, a0, %6;\n mul.rn.f16x2 a1, a1, %7;\n"
+        " mul.rn.f16x2 a2, a2, %6;\n mul.rn.f16x2 a3, a3, %7;\n"
+        " mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {a0,a1,a2,a3},"
+        " {%8,%9}, {%0,%1,%2,%3};\n}"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(wl), "r"(wh), "r"(sl), "r"(sh), "r"(b0), "r"(b1));
+  } else {
+    asm("{\n .reg .b8 l0, l1, l2, l3, h0, h1, h2, h3;\n .reg .b32 a0, a1, a2, a3;\n"
+        " mov.b32 {l0, l1, l2, l3}, %4;\n mov.b32 {h0, h1, h2, h3}, %5;\n"
+        " cvt.rn.f16x2.e2m1x2 a0, l2;\n cvt.rn.f16x2.e2m1x2 a1, h2;\n"
+        " cvt.rn.f16x2.e2m1x2 a2, l3;\n cvt.rn.f16x2.e2m1x2 a3, h3;\n"
+        " mul.rn.f16x2 a0, a0, %6;\n mul.rn.f16x2 a1, a1, %7;\n"
+        " mul.rn.f16x2 a2, a2, %6;\n mul.rn.f16x2 a3, a3, %7;\n"
+        " mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {a0,a1,a2,a3},"
+        " {%8,%9}, {%0,%1,%2,%3};\n}"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(wl), "r"(wh), "r"(sl), "r"(sh), "r"(b0), "r"(b1));
+  }
+}
+
+// Two 16-row x 64-column FP4 group tiles against one set of B registers, added
+// into d0, d1: (l0, h0) are the lane's codes of rows g and g + 8 of tile 0
+// (16 columns, 8 bytes each) with scales (s0l, s0h), likewise tile 1; b holds
+// the 16 x values of the lane's columns in order (MMA m: b[2m], b[2m + 1]).
+__device__ __forceinline__ void group2_fp4(float (&d0)[4], float (&d1)[4], uint2 l0, uint2 h0,
+                                           uint2 l1, uint2 h1, uint32_t s0l, uint32_t s0h,
+                                           uint32_t s1l, uint32_t s1h, const uint32_t (&b)[8]) {
+  mma_fp4<0>(d0, l0.x, h0.x, s0l, s0h, b[0], b[1]);
+  mma_fp4<0>(d1, l1.x, h1.x, s1l, s1h, b[0], b[1]);
+  mma_fp4<1>(d0, l0.x, h0.x, s0l, s0h, b[2], b[3]);
+  mma_fp4<1>(d1, l1.x, h1.x, s1l, s1h, b[2], b[3]);
+  mma_fp4<0>(d0, l0.y, h0.y, s0l, s0h, b[4], b[5]);
+  mma_fp4<0>(d1, l1.y, h1.y, s1l, s1h, b[4], b[5]);
+  mma_fp4<1>(d0, l0.y, h0.y, s0l, s0h, b[6], b[7]);
+  mma_fp4<1>(d1, l1.y, h1.y, s1l, s1h, b[6], b[7]);
+}
+
 __device__ __forceinline__ uint32_t h2u(float lo, float hi) {
   const __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
@@ -228,6 +308,16 @@ __device__ __forceinline__ void frag_item(const float (&v)[16], unsigned char* d
     o += ((i & 1) ? 64.0f : 1024.0f) * q;
     x += q;
   }
+}
+
+// B fragment item of the FP4 path: 16 columns of one token row, already
+// scaled, rounded to fp16 and stored in column order.
+__device__ __forceinline__ void frag_plain(const float (&v)[16], unsigned char* dst) {
+  uint32_t r[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) r[j] = h2u(v[2 * j], v[2 * j + 1]);
+  reinterpret_cast<uint4*>(dst)[0] = make_uint4(r[0], r[1], r[2], r[3]);
+  reinterpret_cast<uint4*>(dst)[1] = make_uint4(r[4], r[5], r[6], r[7]);
 }
 
 __device__ __forceinline__ void cons_sync() {
@@ -337,9 +427,15 @@ __device__ void layer_evict(const LayerFuse& lf, CtlSh& cs,
   if (threadIdx.x == 0) red_release_gpu_add(lf.sync + kSyncFill);  // the plan and the tables
 }
 
-template <bool FUSED>
+template <bool FUSED, int FMT>
 __global__ void __launch_bounds__(kThreads, 1)
     ffn_coop_kernel(FfnArgs a, CoopGeom geo, const __grid_constant__ CoopMaps maps, LayerFuse lf) {
+  // bytes of scales per stage; FP4: elements per block scale
+  constexpr int kSB = FMT == MOE_FORMAT_MXFP4 ? 1024 : 2048;
+  constexpr int kBlk = FMT == MOE_FORMAT_NVFP4 ? 16 : 32;
+  // FP4: per entry, the fp32 factors applied after the sums of gate, up and
+  // down (the NVFP4 matrix scales; 2^-8 for MXFP4's shifted block scales)
+  __shared__ float s_fac[FMT != MOE_FORMAT_INT4 ? kMaxEnt : 1][3];
   extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t full[kMaxSt], empty[kMaxSt], rfull[2], rfree[2];
   __shared__ int s_map[kMaxEnt], s_bi[kMaxEnt], s_fs[kMaxEnt], s_uid[kMaxEnt];
@@ -431,7 +527,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           v[2 * i] = __uint_as_float(wv[i] << 16) * sc;
           v[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u) * sc;
         }
-        frag_item(v, frag + (size_t)t * geo.frow + G * 128 + q4 * 32, o, xs);
+        if constexpr (FMT == MOE_FORMAT_INT4)
+          frag_item(v, frag + (size_t)t * geo.frow + G * 128 + q4 * 32, o, xs);
+        else
+          frag_plain(v, frag + (size_t)t * geo.frow + G * 128 + q4 * 32);
       }
       o += __shfl_xor_sync(0xffffffffu, o, 1);
       o += __shfl_xor_sync(0xffffffffu, o, 2);
@@ -444,6 +543,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const unsigned ny = (unsigned)T * H;
     for (unsigned i = yb * ny / NY + ctid; i < (yb + 1) * ny / NY; i += kConsThreads) a.y[i] = 0.0f;
     cons_sync();
+  };
+
+  // FP4: entry r's fp32 factors (map m, blob index bi)
+  auto set_factors = [&](int r, int m, int bi) {
+    if constexpr (FMT == MOE_FORMAT_NVFP4) {
+      const uint8_t* base = m == 0 ? a.bank : m == 1 ? a.pool : a.shared;
+      const float* mat = reinterpret_cast<const float*>(
+          base + (int64_t)bi * a.blob_bytes + fp4_offsets(H, I, FMT).mat);
+      s_fac[r][0] = __ldg(mat);
+      s_fac[r][1] = __ldg(mat + 1);
+      s_fac[r][2] = __ldg(mat + 2);
+    } else if constexpr (FMT == MOE_FORMAT_MXFP4) {
+      s_fac[r][0] = s_fac[r][1] = s_fac[r][2] = 1.0f / (float)(1 << kMxBias);
+    }
   };
 
   const unsigned Gall = gridDim.x;
@@ -506,6 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           s_bi[r] = bi;
           s_fs[r] = -1;  // an F entry's slot: learnt by the fill writer
           s_uid[r] = uid;
+          set_factors(r, mi, bi);
         }
       } else {
         layer_evict(lf, cs, early, early_id);
@@ -539,6 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       s_bi[r] = bi;
       s_fs[r] = fs;
       s_uid[r] = uid;
+      set_factors(r, mi, bi);
     }
   }
   __syncthreads();
@@ -560,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool r = true;
       if (lane == 0) {
         r = rnd == 0 || bar_wait(su32(&empty[s]), (rnd - 1) & 1);
-        if (r) bar_expect(su32(&full[s]), kSlotBytes);
+        if (r) bar_expect(su32(&full[s]), kCodeBytes + kSB);
       }
       return __shfl_sync(0xffffffffu, r, 0) != 0;
     };
@@ -580,7 +695,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d_ef(dst + lane * 4096, &maps.gu_code[m], ks * 128 + 32 * lane, row0, 0, bi,
                          su32(&full[s]), pol);
         else if (lane == 4)
-          tma_load_4d_ef(dst + kCodeBytes, &maps.gu_scale[m], ks * 8, row0, 0, bi,
+          tma_load_4d_ef(dst + kCodeBytes, &maps.gu_scale[m],
+                         FMT == MOE_FORMAT_INT4 ? ks * 8 : ks * (kGuCols / kBlk / 4), row0, 0, bi,
                          su32(&full[s]), pol);
         advance();
       }
@@ -593,9 +709,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane < geo.nbd)
           tma_load_3d_ef(dst + lane * RD * 128, &maps.dn_code[m], kd * (KSD / 8) + 32 * lane,
                          row0, bi, su32(&full[s]), pol);
-        else if (lane == geo.nbd)
-          tma_load_4d_ef(dst + kCodeBytes, &maps.dn_scale[m], kd * (KSD / 128), row0, 0, bi,
-                         su32(&full[s]), pol);
+        else if (lane == geo.nbd) {
+          if constexpr (FMT == MOE_FORMAT_INT4)
+            tma_load_4d_ef(dst + kCodeBytes, &maps.dn_scale[m], kd * (KSD / 128), row0, 0, bi,
+                           su32(&full[s]), pol);
+          else
+            tma_load_3d_ef(dst + kCodeBytes, &maps.dn_scale[m], kd * (KSD / kBlk / 4), row0, bi,
+                           su32(&full[s]), pol);
+        }
         advance();
       }
     }
@@ -644,8 +765,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return s_fs[r];
       };
+      // bytes of the blob past its tiled sections (FP4: the matrix scales, and
+      // the padding to 256 bytes), copied by the CTA with the entry's first tile
+      const int64_t tail_off = FMT == MOE_FORMAT_INT4
+                                   ? blob_offsets(H, I).db + (int64_t)H * (I / kGroup) * 2
+                                   : fp4_offsets(H, I, FMT).mat;
+      const int tail16 = (int)((a.blob_bytes - tail_off) / 16);
       for (int tile = gu_lo; ok && tile < gu_hi; ++tile) {
         const int r = tile / tpe_gu, row0 = (tile % tpe_gu) * 16, fs = fill_slot(r);
+        if (fs >= 0 && row0 == 0 && tail16 > 0) {
+          const uint4* src =
+              reinterpret_cast<const uint4*>(a.bank + (int64_t)s_bi[r] * a.blob_bytes + tail_off);
+          uint4* dst = reinterpret_cast<uint4*>(a.pool_w + (int64_t)fs * a.blob_bytes + tail_off);
+          for (int i = lane; i < tail16; i += 32) dst[i] = __ldg(src + i);
+        }
         for (int ks = 0; ks < nks; ++ks, advance()) {
           if (!(ok = warp_wait(su32(&full[s]), ph))) break;
           if (fs >= 0 && lane <= 4) {
@@ -655,7 +788,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_store_4d_ef(&maps.gu_code[1], ks * 128 + 32 * lane, row0, 0, fs,
                               src + lane * 4096, pol);
             else
-              tma_store_4d_ef(&maps.gu_scale[1], ks * 8, row0, 0, fs, src + kCodeBytes, pol);
+              tma_store_4d_ef(&maps.gu_scale[1],
+                              FMT == MOE_FORMAT_INT4 ? ks * 8 : ks * (kGuCols / kBlk / 4), row0, 0,
+                              fs, src + kCodeBytes, pol);
             bulk_commit();
             bulk_read_done();
           }
@@ -673,8 +808,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane < geo.nbd)
               tma_store_3d_ef(&maps.dn_code[1], kd * (KSD / 8) + 32 * lane, row0, fs,
                               src + lane * RD * 128, pol);
-            else
+            else if constexpr (FMT == MOE_FORMAT_INT4)
               tma_store_4d_ef(&maps.dn_scale[1], kd * (KSD / 128), row0, 0, fs,
+                              src + kCodeBytes, pol);
+            else
+              tma_store_3d_ef(&maps.dn_scale[1], kd * (KSD / kBlk / 4), row0, fs,
                               src + kCodeBytes, pol);
             bulk_commit();
             bulk_read_done();
@@ -737,6 +875,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int coff_gu =
         (w >> 2) * 4096 + (((((w & 3) << 1) | (t4 >> 1)) ^ g) << 4) + (t4 & 1) * 8 + g * 128;
     const int soff_gu = kCodeBytes + (g * 16 + w) * 2;
+    // FP4: the lane's block scale byte of row g in a stage ([gate, up][16 rows]
+    // [1024 / block bytes]); row g + 8 at +8 rows, up at +16 rows
+    constexpr int kRowB = kGuCols / kBlk;
+    const int fsoff_gu =
+        kCodeBytes + g * kRowB + (FMT == MOE_FORMAT_NVFP4 ? 4 * w + t4 : 2 * w + (t4 >> 1));
     const unsigned char* st = ring;  // the ring slot of stage n
     int sidx = 0;
     uint32_t ph = 0;
@@ -773,15 +916,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         // to the producer at once: its refill overlaps this warp's math
         uint2 gl, gh, ul, uh;
         uint16_t sv[8];
+        uint32_t fsc[4];  // FP4: scale bytes of gate rows g, g + 8, up rows g, g + 8
         if (ok) {
           const unsigned char* cb = st + coff_gu;
           gl = *reinterpret_cast<const uint2*>(cb);
           gh = *reinterpret_cast<const uint2*>(cb + 1024);
           ul = *reinterpret_cast<const uint2*>(cb + 2048);
           uh = *reinterpret_cast<const uint2*>(cb + 3072);
-          const unsigned char* sc = st + soff_gu;
+          if constexpr (FMT == MOE_FORMAT_INT4) {
+            const unsigned char* sc = st + soff_gu;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) sv[e] = *reinterpret_cast<const uint16_t*>(sc + 256 * e);
+            for (int e = 0; e < 8; ++e) sv[e] = *reinterpret_cast<const uint16_t*>(sc + 256 * e);
+          } else {
+            const unsigned char* sc = st + fsoff_gu;
+            fsc[0] = sc[0];
+            fsc[1] = sc[8 * kRowB];
+            fsc[2] = sc[16 * kRowB];
+            fsc[3] = sc[24 * kRowB];
+          }
         }
         __syncwarp();
         if (lane == 0) bar_arrive(su32(&empty[sidx]));
@@ -790,20 +942,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint4 v0 = reinterpret_cast<const uint4*>(pb)[0];
           const uint4 v1 = reinterpret_cast<const uint4*>(pb)[1];
           const uint32_t b[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-          const float2 q0 = *pq0, q1 = *pq1;
-          // sv: gs, gb, us, ub of rows g and g + 8 ([array][row] order, rows 8 apart)
-          const float sg0 = bf(sv[0]), sg1 = bf(sv[1]), bg0 = bf(sv[2]), bg1 = bf(sv[3]);
-          const float su0 = bf(sv[4]), su1 = bf(sv[5]), bu0 = bf(sv[6]), bu1 = bf(sv[7]);
-          float dg[4], du[4];
-          group2(dg, du, gl, gh, ul, uh, b, cv);
-          ag[0] = fmaf(sg0, dg[0] - q0.x, fmaf(bg0, q0.y, ag[0]));
-          ag[1] = fmaf(sg0, dg[1] - q1.x, fmaf(bg0, q1.y, ag[1]));
-          ag[2] = fmaf(sg1, dg[2] - q0.x, fmaf(bg1, q0.y, ag[2]));
-          ag[3] = fmaf(sg1, dg[3] - q1.x, fmaf(bg1, q1.y, ag[3]));
-          au[0] = fmaf(su0, du[0] - q0.x, fmaf(bu0, q0.y, au[0]));
-          au[1] = fmaf(su0, du[1] - q1.x, fmaf(bu0, q1.y, au[1]));
-          au[2] = fmaf(su1, du[2] - q0.x, fmaf(bu1, q0.y, au[2]));
-          au[3] = fmaf(su1, du[3] - q1.x, fmaf(bu1, q1.y, au[3]));
+          if constexpr (FMT == MOE_FORMAT_INT4) {
+            const float2 q0 = *pq0, q1 = *pq1;
+            // sv: gs, gb, us, ub of rows g and g + 8 ([array][row] order, rows 8 apart)
+            const float sg0 = bf(sv[0]), sg1 = bf(sv[1]), bg0 = bf(sv[2]), bg1 = bf(sv[3]);
+            const float su0 = bf(sv[4]), su1 = bf(sv[5]), bu0 = bf(sv[6]), bu1 = bf(sv[7]);
+            float dg[4], du[4];
+            group2(dg, du, gl, gh, ul, uh, b, cv);
+            ag[0] = fmaf(sg0, dg[0] - q0.x, fmaf(bg0, q0.y, ag[0]));
+            ag[1] = fmaf(sg0, dg[1] - q1.x, fmaf(bg0, q1.y, ag[1]));
+            ag[2] = fmaf(sg1, dg[2] - q0.x, fmaf(bg1, q0.y, ag[2]));
+            ag[3] = fmaf(sg1, dg[3] - q1.x, fmaf(bg1, q1.y, ag[3]));
+            au[0] = fmaf(su0, du[0] - q0.x, fmaf(bu0, q0.y, au[0]));
+            au[1] = fmaf(su0, du[1] - q1.x, fmaf(bu0, q1.y, au[1]));
+            au[2] = fmaf(su1, du[2] - q0.x, fmaf(bu1, q0.y, au[2]));
+            au[3] = fmaf(su1, du[3] - q1.x, fmaf(bu1, q1.y, au[3]));
+          } else {
+            group2_fp4(ag, au, gl, gh, ul, uh, fp4_scale2<FMT>(fsc[0]), fp4_scale2<FMT>(fsc[1]),
+                       fp4_scale2<FMT>(fsc[2]), fp4_scale2<FMT>(fsc[3]), b);
+          }
         }
         pb += sb;
         pq0 += sq0;
@@ -826,8 +983,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               us += rb[((size_t)ww * 32 + 16 + lane) * T + nn];
             }
             const float P = s_px[s_tok[r][nn]];
-            gs *= P;
-            us *= P;
+            if constexpr (FMT == MOE_FORMAT_INT4) {
+              gs *= P;
+              us *= P;
+            } else {
+              gs *= P * s_fac[r][0];
+              us *= P * s_fac[r][1];
+            }
             v = __fdividef(gs, 1.0f + __expf(fminf(-gs, 80.0f))) * us;
             a.h[((int64_t)r * T + nn) * I + row0 + lane] = v;
           }
@@ -851,6 +1013,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int coff_dn = (gi >> 2) * (RD * 128) + (((((gi & 3) << 1) | (t4 >> 1)) ^ g) << 4) +
                         (t4 & 1) * 8 + (32 * p + g) * 128;
     const int soff_dn = kCodeBytes + ((32 * p + g) * ngs + gi) * 2;
+    // FP4: the lane's block scale byte of row 32 p + g ([RD rows][KSD / block
+    // bytes]); rows + 8, + 16, + 24 follow at 8 row strides
+    const int kRowD = KSD / kBlk;
+    const int fsoff_dn = kCodeBytes + (32 * p + g) * kRowD +
+                         (FMT == MOE_FORMAT_NVFP4 ? 4 * gi + t4 : 2 * gi + (t4 >> 1));
     const int sbo = RD * ngs * 2;
     cur = -1;
     for (int tile = dn_lo; tile < dn_hi; ++tile) {
@@ -877,6 +1044,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int j = 0; j < k; ++j)
                 if (base + s_ids[t * k + j] == uid) wsum += s_wts[t * k + j];
             }
+            if constexpr (FMT != MOE_FORMAT_INT4) wsum *= s_fac[r][2];
             s_wp[nn] = wsum / inv;
           }
         }
@@ -903,7 +1071,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               v[4 * e + 2] = f.z * sc;
               v[4 * e + 3] = f.w * sc;
             }
-            frag_item(v, frag + (size_t)nn * geo.frow + G * 128 + q4 * 32, o, xs);
+            if constexpr (FMT == MOE_FORMAT_INT4)
+              frag_item(v, frag + (size_t)nn * geo.frow + G * 128 + q4 * 32, o, xs);
+            else
+              frag_plain(v, frag + (size_t)nn * geo.frow + G * 128 + q4 * 32);
           }
           o += __shfl_xor_sync(0xffffffffu, o, 1);
           o += __shfl_xor_sync(0xffffffffu, o, 2);
@@ -929,17 +1100,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         // codes and scales into registers, then the slot goes back at once
         uint2 l0, h0, l1, h1;
         uint16_t sv[8];
+        uint32_t fsc[4];  // FP4: scale bytes of rows g, g + 8, g + 16, g + 24 (of 32 p ..)
         if (ok) {
           const unsigned char* cb = st + coff_dn;
           l0 = *reinterpret_cast<const uint2*>(cb);
           h0 = *reinterpret_cast<const uint2*>(cb + 1024);
           l1 = *reinterpret_cast<const uint2*>(cb + 2048);
           h1 = *reinterpret_cast<const uint2*>(cb + 3072);
-          const unsigned char* sc = st + soff_dn;
+          if constexpr (FMT == MOE_FORMAT_INT4) {
+            const unsigned char* sc = st + soff_dn;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            sv[e] = *reinterpret_cast<const uint16_t*>(sc + 16 * ngs * e);
-            sv[4 + e] = *reinterpret_cast<const uint16_t*>(sc + sbo + 16 * ngs * e);
+            for (int e = 0; e < 4; ++e) {
+              sv[e] = *reinterpret_cast<const uint16_t*>(sc + 16 * ngs * e);
+              sv[4 + e] = *reinterpret_cast<const uint16_t*>(sc + sbo + 16 * ngs * e);
+            }
+          } else {
+            const unsigned char* sc = st + fsoff_dn;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) fsc[e] = sc[8 * e * kRowD];
           }
         }
         __syncwarp();
@@ -949,20 +1127,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint4 v0 = reinterpret_cast<const uint4*>(pb)[0];
           const uint4 v1 = reinterpret_cast<const uint4*>(pb)[1];
           const uint32_t b[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-          const float2 q0 = *pq0, q1 = *pq1;
-          // sv: ds of rows g, g + 8, g + 16, g + 24 (of the warp's 32), then db
-          const float s00 = bf(sv[0]), s01 = bf(sv[1]), s10 = bf(sv[2]), s11 = bf(sv[3]);
-          const float b00 = bf(sv[4]), b01 = bf(sv[5]), b10 = bf(sv[6]), b11 = bf(sv[7]);
-          float d0[4], d1[4];
-          group2(d0, d1, l0, h0, l1, h1, b, cv);
-          a0[0] = fmaf(s00, d0[0] - q0.x, fmaf(b00, q0.y, a0[0]));
-          a0[1] = fmaf(s00, d0[1] - q1.x, fmaf(b00, q1.y, a0[1]));
-          a0[2] = fmaf(s01, d0[2] - q0.x, fmaf(b01, q0.y, a0[2]));
-          a0[3] = fmaf(s01, d0[3] - q1.x, fmaf(b01, q1.y, a0[3]));
-          a1[0] = fmaf(s10, d1[0] - q0.x, fmaf(b10, q0.y, a1[0]));
-          a1[1] = fmaf(s10, d1[1] - q1.x, fmaf(b10, q1.y, a1[1]));
-          a1[2] = fmaf(s11, d1[2] - q0.x, fmaf(b11, q0.y, a1[2]));
-          a1[3] = fmaf(s11, d1[3] - q1.x, fmaf(b11, q1.y, a1[3]));
+          if constexpr (FMT == MOE_FORMAT_INT4) {
+            const float2 q0 = *pq0, q1 = *pq1;
+            // sv: ds of rows g, g + 8, g + 16, g + 24 (of the warp's 32), then db
+            const float s00 = bf(sv[0]), s01 = bf(sv[1]), s10 = bf(sv[2]), s11 = bf(sv[3]);
+            const float b00 = bf(sv[4]), b01 = bf(sv[5]), b10 = bf(sv[6]), b11 = bf(sv[7]);
+            float d0[4], d1[4];
+            group2(d0, d1, l0, h0, l1, h1, b, cv);
+            a0[0] = fmaf(s00, d0[0] - q0.x, fmaf(b00, q0.y, a0[0]));
+            a0[1] = fmaf(s00, d0[1] - q1.x, fmaf(b00, q1.y, a0[1]));
+            a0[2] = fmaf(s01, d0[2] - q0.x, fmaf(b01, q0.y, a0[2]));
+            a0[3] = fmaf(s01, d0[3] - q1.x, fmaf(b01, q1.y, a0[3]));
+            a1[0] = fmaf(s10, d1[0] - q0.x, fmaf(b10, q0.y, a1[0]));
+            a1[1] = fmaf(s10, d1[1] - q1.x, fmaf(b10, q1.y, a1[1]));
+            a1[2] = fmaf(s11, d1[2] - q0.x, fmaf(b11, q0.y, a1[2]));
+            a1[3] = fmaf(s11, d1[3] - q1.x, fmaf(b11, q1.y, a1[3]));
+          } else {
+            group2_fp4(a0, a1, l0, h0, l1, h1, fp4_scale2<FMT>(fsc[0]), fp4_scale2<FMT>(fsc[1]),
+                       fp4_scale2<FMT>(fsc[2]), fp4_scale2<FMT>(fsc[3]), b);
+          }
         }
         pb += sb;
         pq0 += sq0;
@@ -1023,13 +1206,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 static_assert(kSyncCtr + 4 + 8 * kMaxEnt <= MOE_CACHE_SYNC_WORDS, "sync words");
 
-template <bool FUSED>
+template <bool FUSED, int FMT>
 bool coop_attr_set(size_t smem) {
   static size_t done[64];
   int d = 0;
   if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) return false;
   if (done[d] >= smem) return true;
-  if (cudaFuncSetAttribute(ffn_coop_kernel<FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(ffn_coop_kernel<FUSED, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
     return false;
   done[d] = smem;
@@ -1046,8 +1229,8 @@ bool ffn_coop_supported(int H, int I, int k, int T, int has_shared) {
 
 namespace {
 
-template <bool FUSED>
-cudaError_t launch_coop(const FfnArgs& a, const LayerFuse& lf, cudaStream_t st) {
+template <bool FUSED, int FMT>
+cudaError_t launch_coop_fmt(const FfnArgs& a, const LayerFuse& lf, cudaStream_t st) {
   static int sms[64];
   if (!ffn_coop_supported(a.H, a.I, a.k, a.T, a.has_shared) || a.max_entries > kMaxEnt ||
       a.n_ctr < ffn_ctr_words(a.H, a.max_entries))
@@ -1064,6 +1247,8 @@ cudaError_t launch_coop(const FfnArgs& a, const LayerFuse& lf, cudaStream_t st) 
   CoopMaps maps;
   memset(&maps, 0, sizeof(maps));
   const BlobOffsets off = blob_offsets(a.H, a.I);
+  const Fp4Offsets foff = fp4_offsets(a.H, a.I, FMT);
+  const uint64_t blk = (uint64_t)foff.block;
   const uint8_t* bases[3] = {a.bank, a.pool, a.shared ? a.shared : a.bank};
   const uint64_t nblob[3] = {(uint64_t)a.n_bank, (uint64_t)a.n_pool,
                              a.shared ? 1ull : (uint64_t)a.n_bank};
@@ -1077,11 +1262,19 @@ cudaError_t launch_coop(const FfnArgs& a, const LayerFuse& lf, cudaStream_t st) 
                                 true)) != cudaSuccess)
         return e;
     }
-    {
+    if (FMT == MOE_FORMAT_INT4) {
       const uint64_t dims[4] = {H / 128, I, 4, nblob[i]};
       const uint64_t strides[3] = {H / 32, I * H / 32, B};
       const uint32_t box[4] = {8, 16, 4, 1};
       if ((e = encode_tiled_u32(&maps.gu_scale[i], bases[i] + off.gs, 4, dims, strides, box,
+                                false)) != cudaSuccess)
+        return e;
+    } else {
+      // one scale byte per block: [gate, up][row of I][H / block bytes]
+      const uint64_t dims[4] = {H / blk / 4, I, 2, nblob[i]};
+      const uint64_t strides[3] = {H / blk, I * H / blk, B};
+      const uint32_t box[4] = {(uint32_t)(kGuCols / blk / 4), 16, 2, 1};
+      if ((e = encode_tiled_u32(&maps.gu_scale[i], bases[i] + foff.gs, 4, dims, strides, box,
                                 false)) != cudaSuccess)
         return e;
     }
@@ -1093,16 +1286,24 @@ cudaError_t launch_coop(const FfnArgs& a, const LayerFuse& lf, cudaStream_t st) 
                                 true)) != cudaSuccess)
         return e;
     }
-    {
+    if (FMT == MOE_FORMAT_INT4) {
       const uint64_t dims[4] = {I / 128, H, 2, nblob[i]};
       const uint64_t strides[3] = {I / 32, H * I / 32, B};
       const uint32_t box[4] = {(uint32_t)(geo.KSD / 128), (uint32_t)geo.RD, 2, 1};
       if ((e = encode_tiled_u32(&maps.dn_scale[i], bases[i] + off.ds, 4, dims, strides, box,
                                 false)) != cudaSuccess)
         return e;
+    } else {
+      // [row of H][I / block bytes]
+      const uint64_t dims[3] = {I / blk / 4, H, nblob[i]};
+      const uint64_t strides[2] = {I / blk, B};
+      const uint32_t box[3] = {(uint32_t)(geo.KSD / blk / 4), (uint32_t)geo.RD, 1};
+      if ((e = encode_tiled_u32(&maps.dn_scale[i], bases[i] + foff.ds, 3, dims, strides, box,
+                                false)) != cudaSuccess)
+        return e;
     }
   }
-  if (!coop_attr_set<FUSED>(geo.smem)) return cudaErrorInvalidValue;
+  if (!coop_attr_set<FUSED, FMT>(geo.smem)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -1115,15 +1316,29 @@ cudaError_t launch_coop(const FfnArgs& a, const LayerFuse& lf, cudaStream_t st) 
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, ffn_coop_kernel<FUSED>, a, geo, maps, lf);
+  e = cudaLaunchKernelEx(&cfg, ffn_coop_kernel<FUSED, FMT>, a, geo, maps, lf);
   if (e == cudaErrorInvalidValue || e == cudaErrorNotSupported) {
     // a runtime that does not take both attributes together: launch it
     // cooperatively, after the previous kernel has completed
     (void)cudaGetLastError();
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, ffn_coop_kernel<FUSED>, a, geo, maps, lf);
+    e = cudaLaunchKernelEx(&cfg, ffn_coop_kernel<FUSED, FMT>, a, geo, maps, lf);
   }
   return e;
+}
+
+template <bool FUSED>
+cudaError_t launch_coop(const FfnArgs& a, const LayerFuse& lf, cudaStream_t st) {
+  switch (a.format) {
+    case MOE_FORMAT_INT4:
+      return launch_coop_fmt<FUSED, MOE_FORMAT_INT4>(a, lf, st);
+    case MOE_FORMAT_MXFP4:
+      return launch_coop_fmt<FUSED, MOE_FORMAT_MXFP4>(a, lf, st);
+    case MOE_FORMAT_NVFP4:
+      return launch_coop_fmt<FUSED, MOE_FORMAT_NVFP4>(a, lf, st);
+    default:
+      return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace

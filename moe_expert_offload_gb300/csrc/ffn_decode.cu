@@ -612,6 +612,7 @@ cudaError_t launch_ffn_decode(const FfnArgs& a, cudaStream_t st, bool ctr_zeroed
     }
     return launch_ffn_coop(a, st);
   }
+  if (a.format != MOE_FORMAT_INT4) return cudaErrorNotSupported;  // FP4: the cooperative kernel only
   static size_t done_a1[64], done_a2[64], done_b1[64], done_b2[64];
   const int nblk = (a.H + kRowsBlkB - 1) / kRowsBlkB;
   const int grid_a = a.max_entries * (a.I / 16);

@@ -37,6 +37,34 @@ __host__ __device__ inline BlobOffsets blob_offsets(int64_t H, int64_t I) {
   return o;
 }
 
+// FP4 expert blob (MOE_FORMAT_MXFP4 / NVFP4): E2M1 codes laid out as the
+// int4 codes, then one scale byte per block of each matrix, then (NVFP4) the
+// three fp32 matrix scales; the total rounded up to 256 bytes.
+struct Fp4Offsets {
+  int64_t gq, uq, dq, gs, us, ds, mat, total;
+  int block;  // elements per scale: 32 (MXFP4) or 16 (NVFP4)
+};
+
+__host__ __device__ inline Fp4Offsets fp4_offsets(int64_t H, int64_t I, int format) {
+  Fp4Offsets o;
+  o.block = format == MOE_FORMAT_NVFP4 ? 16 : 32;
+  const int64_t hi = H * I;
+  o.gq = 0;
+  o.uq = hi / 2;
+  o.dq = hi;
+  o.gs = hi / 2 * 3;
+  o.us = o.gs + hi / o.block;
+  o.ds = o.us + hi / o.block;
+  o.mat = o.ds + hi / o.block;
+  o.total = (o.mat + (format == MOE_FORMAT_NVFP4 ? 12 : 0) + 255) / 256 * 256;
+  return o;
+}
+
+// Bytes of one expert blob of the given format.
+inline int64_t expert_blob_bytes(int64_t H, int64_t I, int format) {
+  return format == MOE_FORMAT_INT4 ? blob_offsets(H, I).total : fp4_offsets(H, I, format).total;
+}
+
 // Programmatic dependent launch (the decode layer path).  A kernel launched
 // with launch_pdl may be scheduled while the previous kernel in the stream is
 // still running: it calls griddep_wait() before its first access to memory
@@ -132,6 +160,7 @@ struct FfnArgs {
   // every member has a zero default, so a caller that fills in only some
   // fields never hands a kernel an indeterminate flag or pointer
   int H = 0, I = 0, E = 0, k = 0, layer = 0, T = 0, has_shared = 0;
+  int format = 0;  // MOE_FORMAT_*
   int64_t blob_bytes = 0;
   const uint8_t* bank = nullptr;
   const uint8_t* pool = nullptr;

@@ -81,9 +81,11 @@ __device__ __forceinline__ float moe_exp(float x) {
   return __fmul_rn(p, __int_as_float((ni + 127) << 23));
 }
 
+// 1 / (1 + exp(-z)), the reciprocal correctly rounded (the same bits as the
+// IEEE division 1 / d).
 __device__ __forceinline__ float moe_sigmoid(float z) {
   const float d = __fadd_rn(1.0f, moe_exp(-z));
-  return __fdiv_rn(1.0f, d);
+  return __frcp_rn(d);
 }
 
 // (value, index) order used for every top-k: larger value first, lower
@@ -259,49 +261,50 @@ __device__ __forceinline__ void sigmoid_group_token(const float* __restrict__ lo
   uint32_t kept = 0;  // bit g: group g kept
   if (gsz % 32 == 0) {
     // group g = register rows i in [g gsz/32, (g+1) gsz/32) of every lane: the
-    // lane's two largest, then the warp's two largest (all lanes get every score)
+    // lane's two largest of each group, then an xor butterfly merging the
+    // lanes' pairs, all groups at once; every lane ends with every score
     const int rows = gsz >> 5;
-    float gs[EPL];  // n_groups <= EPL here
+    float t1[EPL], t2[EPL];  // n_groups <= EPL here
+    if (rows == 1) {
 #pragma unroll
-    for (int g = 0; g < EPL; ++g) {
-      gs[g] = -FLT_MAX;
-      if (g < n_groups) {
-        float t1 = -FLT_MAX, t2 = -FLT_MAX;
+      for (int g = 0; g < EPL; ++g) {
+        t1[g] = g < n_groups ? sel[g] : -FLT_MAX;
+        t2[g] = -FLT_MAX;
+      }
+    } else {
+#pragma unroll
+      for (int g = 0; g < EPL; ++g) {
+        t1[g] = -FLT_MAX;
+        t2[g] = -FLT_MAX;
 #pragma unroll
         for (int i = 0; i < EPL; ++i)
-          if (i >= g * rows && i < (g + 1) * rows) {
+          if (g < n_groups && i >= g * rows && i < (g + 1) * rows) {
             const float z = sel[i];
-            if (z > t1) {
-              t2 = t1;
-              t1 = z;
-            } else if (z > t2) {
-              t2 = z;
-            }
+            t2[g] = fmaxf(t2[g], fminf(t1[g], z));
+            t1[g] = fmaxf(t1[g], z);
           }
-        const uint32_t k1 = ord_key(t1), k2 = ord_key(t2);
-        const uint32_t m1 = __reduce_max_sync(0xffffffffu, k1);
-        const unsigned at = __ballot_sync(0xffffffffu, k1 == m1);
-        // second largest: m1 again when two lanes hold it, else the larger of the
-        // other lanes' first and the holder's second
-        const uint32_t c2 = k1 == m1 ? k2 : k1;
-        const uint32_t m2 = __popc(at) > 1 ? m1 : __reduce_max_sync(0xffffffffu, c2);
-        const float v1 = __shfl_sync(0xffffffffu, t1, __ffs(at) - 1);
-        const unsigned at2 = __ballot_sync(0xffffffffu, c2 == m2);
-        const float v2c = __shfl_sync(0xffffffffu, k1 == m1 ? t2 : t1, __ffs(at2) - 1);
-        gs[g] = __fadd_rn(v1, __popc(at) > 1 ? v1 : v2c);
       }
     }
-    // the topk_groups best groups, computed alike by every lane
-    for (int r = 0; r < topk_groups; ++r) {
-      float bvg = -FLT_MAX;
-      int bg = 0x7fffffff;
 #pragma unroll
-      for (int g = 0; g < EPL; ++g)
-        if (g < n_groups && !(kept >> g & 1u) && better(gs[g], g, bvg, bg)) {
-          bvg = gs[g];
-          bg = g;
-        }
-      kept |= 1u << bg;
+    for (int d = 16; d >= 1; d >>= 1)
+#pragma unroll
+      for (int g = 0; g < EPL; ++g) {
+        const float b1 = __shfl_xor_sync(0xffffffffu, t1[g], d);
+        const float b2 = __shfl_xor_sync(0xffffffffu, t2[g], d);
+        t2[g] = fmaxf(fminf(t1[g], b1), fmaxf(t2[g], b2));
+        t1[g] = fmaxf(t1[g], b1);
+      }
+    // the topk_groups best groups, computed alike by every lane: each group's
+    // rank is the number of groups ahead of it in the order of `better`
+#pragma unroll
+    for (int g = 0; g < EPL; ++g) t1[g] = __fadd_rn(t1[g], t2[g]);
+#pragma unroll
+    for (int g = 0; g < EPL; ++g) {
+      int ahead = 0;
+#pragma unroll
+      for (int h = 0; h < EPL; ++h)
+        ahead += (h < n_groups && better(t1[h], h, t1[g], g)) ? 1 : 0;
+      if (g < n_groups && ahead < topk_groups) kept |= 1u << g;
     }
   } else {
 #pragma unroll

@@ -206,6 +206,36 @@ def make_fp4_expert(rng, H: int, I: int, fmt: int) -> np.ndarray:
     return pack_fp4_blob(H, I, fmt, *q, *sc, mat=mat)
 
 
+def make_fp4_bank_torch(n_experts: int, H: int, I: int, fmt: int, seed: int, device):
+    """FP4 bank generated in device memory (torch's RNG), with the distributions of
+    make_fp4_expert: codes uniform over all 16, E8M0 bytes 118..124 (MXFP4) or E4M3
+    bytes with exponent field 1..5 (NVFP4), matrix scales U[0.5, 2) (NVFP4).
+    fmt: 0 MXFP4, 1 NVFP4.  Returns a uint8 tensor [n_experts, S_e]."""
+    import torch
+
+    off, sizes, total = fp4_blob_sections(H, I, fmt)
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    bank = torch.zeros((n_experts, total), dtype=torch.uint8, device=device)
+    chunk = max(1, min(n_experts, (1 << 30) // total))
+    for a in range(0, n_experts, chunk):
+        b = min(n_experts, a + chunk)
+        blk = bank[a:b]
+        blk[:, off["gq"]:off["gs"]].random_(0, 256, generator=g)
+        n_sc = off["mat"] - off["gs"]
+        if fmt == 0:
+            sc = torch.randint(118, 125, (b - a, n_sc), generator=g, device=device)
+        else:
+            e = torch.randint(1, 6, (b - a, n_sc), generator=g, device=device)
+            m = torch.randint(0, 8, (b - a, n_sc), generator=g, device=device)
+            sc = (e << 3) | m
+        blk[:, off["gs"]:off["mat"]] = sc.to(torch.uint8)
+        if fmt == 1:
+            mat = torch.rand((b - a, 3), generator=g, device=device) * 1.5 + 0.5
+            blk[:, off["mat"]:off["mat"] + 12].view(torch.float32).copy_(mat)
+    return bank
+
+
 def router_weights(seed: int, E: int, H: int, std: float = 0.02) -> np.ndarray:
     """bf16 bits [E][H], N(0, std)."""
     rng = np.random.default_rng(seed)

@@ -55,7 +55,27 @@ def test_expert_bytes_matches_layout(L):
     assert m.moe_expert_bytes(_spec(hidden=7168, inter=2048, num_experts=256, top_k=8)) == 24_772_608
 
 
+def test_fp4_expert_bytes_match_the_oracle_layout(L):
+    """The library's FP4 blob size agrees with the oracle's own layout (two
+    separate implementations of the same reading)."""
+    import oracle
+
+    oracle.build()
+    for fmt, ofmt in ((m.FORMAT_MXFP4, oracle.MXFP4), (m.FORMAT_NVFP4, oracle.NVFP4)):
+        for H, I in ((256, 128), (2048, 512), (7168, 2048), (1024, 192)):
+            got = m.moe_expert_bytes(_spec(hidden=H, inter=I, fmt=fmt))
+            assert got == oracle.fp4_blob_offsets(H, I, ofmt)["total"], (fmt, H, I)
+
+
+def test_fp4_prefill_is_unsupported(L):
+    s = _spec(hidden=1024, inter=512, fmt=m.FORMAT_NVFP4)
+    with pytest.raises(m.MoeError) as e:
+        m.moe_expert_ffn_prefill(s, 16, 16, 4, 16, 16, None, None, 256, 1 << 20, 16, stream=0)
+    assert e.value.code == m.MOE_EUNSUPPORTED
+
+
 @pytest.mark.parametrize("kw", [
+    dict(fmt=3), dict(fmt=-1),
     dict(hidden=100), dict(inter=96), dict(num_experts=0), dict(num_experts=2000),
     dict(top_k=0), dict(top_k=17), dict(num_layers=0),
     dict(router="sigmoid_group", n_groups=3), dict(router="sigmoid_group", n_groups=4, topk_groups=5),

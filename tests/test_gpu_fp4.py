@@ -1,0 +1,197 @@
+"""GPU parity of the FP4 decode path (MXFP4, NVFP4: the formats of the pages'
+deployed models, FreeToken summary "Key results" table) against the CPU
+oracle's FP4 expert (or_fp4_expert_forward), through the C ABI.
+
+The layer output is the routed experts' outputs weighted by the routing
+weights plus the shared expert's, summed here in float64 from the oracle's
+per-expert results; outputs must be within the Edge0 tolerance (relative L2
+<= 1e-2, |err| <= 2e-2 * max|y|).  Routing, plans and slot tables are format-
+independent and must match bit for bit; every resident slot must hold its
+bank blob byte for byte.
+"""
+import numpy as np
+import pytest
+
+import moe_expert_offload_gb300 as m
+from moe_expert_offload_gb300 import synth
+
+from gpu_util import assert_ffn_close, dev, dev_bits
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+# ABI format -> the oracle's FP4 format number (0 MXFP4, 1 NVFP4)
+ORACLE_FMT = {m.FORMAT_MXFP4: 0, m.FORMAT_NVFP4: 1}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from moe_expert_offload_gb300 import _build
+    import oracle
+
+    _build.build()
+    oracle.build()
+    m.lib()
+
+
+@pytest.fixture(scope="module")
+def oracle():
+    import oracle as o
+
+    return o
+
+
+def _fp4_bank(n, H, I, fmt, seed):
+    rng = np.random.default_rng(seed)
+    return np.stack([synth.make_fp4_expert(rng, H, I, ORACLE_FMT[fmt]) for _ in range(n)])
+
+
+def _reference(oracle, blobs, H, I, fmt, xb, ids, wts, shared_blob=None):
+    """y[t] = sum_j w[t][j] expert_{ids[t][j]}(x[t]) (+ shared(x[t])), float64; each
+    expert's output is the oracle's FP4 forward over all tokens at once."""
+    T = xb.shape[0]
+    y = np.zeros((T, H), dtype=np.float64)
+    of = ORACLE_FMT[fmt]
+    cache = {}
+    for e in np.unique(ids):
+        cache[int(e)] = oracle.fp4_expert_forward(blobs[int(e)], H, I, of, xb)
+    for t in range(T):
+        for j in range(ids.shape[1]):
+            y[t] += float(wts[t, j]) * cache[int(ids[t, j])][t]
+    if shared_blob is not None:
+        y += oracle.fp4_expert_forward(shared_blob, H, I, of, xb)
+    return y
+
+
+def test_fp4_blob_bytes_match_the_oracle_layout(oracle):
+    for fmt in (m.FORMAT_MXFP4, m.FORMAT_NVFP4):
+        for H, I in ((1024, 512), (2048, 512), (7168, 2048)):
+            spec = m.make_spec(1, H, I, 8, 2, fmt=fmt)
+            assert m.moe_expert_bytes(spec) == oracle.fp4_blob_offsets(H, I, ORACLE_FMT[fmt])[
+                "total"]
+
+
+@pytest.mark.parametrize("fmt", [m.FORMAT_MXFP4, m.FORMAT_NVFP4])
+@pytest.mark.parametrize("H,I,E,k,T,shared", [(1024, 512, 16, 4, 1, True),
+                                              (2048, 512, 16, 8, 4, False),
+                                              (2048, 1024, 12, 4, 8, True),
+                                              (3072, 512, 20, 6, 5, True)])
+def test_fp4_expert_ffn_matches_oracle(oracle, fmt, H, I, E, k, T, shared):
+    """moe_expert_ffn on FP4 experts: some resident in slots, the rest read from
+    the bank; the routed ids include repeats across tokens.  Both down-tile
+    geometries (inter % 1024 == 0 or not) and 1..8 tokens."""
+    bank_h = _fp4_bank(E + 1, H, I, fmt, seed=H + T + fmt)
+    bank = dev(bank_h, DEV)
+    spec = m.make_spec(1, H, I, E, k, has_shared=shared, fmt=fmt)
+    assert m.moe_expert_bytes(spec) == bank_h.shape[1]
+    S, K = max(2, E // 3), 2
+    cache = m.DeviceCache(spec, S, K, 52700, 77300, bank=bank[:E], device=DEV)
+    m.moe_cache_place(spec, cache.c, list(range(0, E, 3))[:S])
+    plan = m.DevicePlan(T * k, K, device=DEV)
+    rng = np.random.default_rng(T)
+    ids_h = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    wts_h = rng.uniform(0.05, 1.0, size=(T, k)).astype(np.float32)
+    xb = synth.bf16_bits(rng.normal(0, 1.5, (T, H)))
+    ids, wts = dev(ids_h, DEV), dev(wts_h, DEV)
+    sh = bank[E] if shared else None
+    # the step's plan (hits, fills, direct); the fill runs as a copy kernel here
+    m.moe_cache_step(spec, cache.c, 0, ids, T, plan.c, 1)
+    ws_b = m.moe_ffn_workspace_bytes(spec, T)
+    ws = torch.empty(ws_b, dtype=torch.uint8, device=DEV)
+    y = torch.empty((T, H), dtype=torch.float32, device=DEV)
+    m.moe_expert_ffn(spec, cache.c, 0, plan.c, dev_bits(xb, DEV), T, ids, wts, sh, ws, ws_b, y)
+    torch.cuda.synchronize()
+    assert int(plan.err[0].item()) == 0
+    ref = _reference(oracle, bank_h, H, I, fmt, xb, ids_h, wts_h, bank_h[E] if shared else None)
+    assert_ffn_close(y.cpu().numpy(), ref, f"fmt {fmt} H {H} I {I} T {T}")
+
+
+@pytest.mark.parametrize("fmt", [m.FORMAT_MXFP4, m.FORMAT_NVFP4])
+@pytest.mark.parametrize("sync", [True, False])
+def test_fp4_layer_forward_matches_oracle(oracle, fmt, sync):
+    """moe_layer_forward on FP4 experts over 10 steps with fills and evictions:
+    routing and plans bit for bit, outputs within tolerance, every resident slot
+    byte-equal to its bank blob (the fill written by the FFN kernel).  With the
+    cache's sync words the step is one kernel."""
+    L, H, I, E, k, T, S, K = 2, 1024, 512, 16, 4, 2, 6, 3
+    bank_h = _fp4_bank(L * E + 1, H, I, fmt, seed=7 + fmt)
+    bank = dev(bank_h, DEV)
+    spec = m.make_spec(L, H, I, E, k, has_shared=True, fmt=fmt)
+    cache = m.DeviceCache(spec, S, K, 52700, 77300, bank=bank[:L * E], device=DEV, sync=sync)
+    assert m.moe_layer_kernel_count(spec, cache.c, T) == (1 if sync else 3)
+    plan = m.DevicePlan(T * k, K, device=DEV)
+    wsb = m.moe_layer_workspace_bytes(spec, T)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    wts = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    y = torch.empty((T, H), dtype=torch.float32, device=DEV)
+    ost = oracle.CacheState(L * E, S)
+    rng = np.random.default_rng(11)
+    fills = 0
+    for step in range(10):
+        layer = step % L
+        wr_h = synth.router_weights(60 + layer, E, H)
+        xb = synth.bf16_bits(rng.normal(0, 1.5, (T, H)))
+        m.moe_layer_forward(spec, cache.c, layer, dev_bits(xb, DEV), T, dev_bits(wr_h, DEV),
+                            None, bank[L * E], plan.c, ids, wts, ws, wsb, y)
+        torch.cuda.synchronize()
+        oid, ow = oracle.route_softmax_topk(oracle.router_logits(xb, wr_h), k)
+        assert np.array_equal(ids.cpu().numpy(), oid)
+        op = oracle.cache_step(ost, E, layer, oid, K, 52700, 77300)
+        gp = plan.read(K)
+        for key in ("uniq", "hit_ids", "hit_slots", "fill_ids", "fill_slots", "evicted_ids",
+                    "direct_ids", "victims", "counts"):
+            assert np.array_equal(gp[key], op[key]), (step, key)
+        fills += op["n_fill"]
+        ref = _reference(oracle, bank_h[layer * E:(layer + 1) * E], H, I, fmt, xb, oid, ow,
+                         bank_h[L * E])
+        assert_ffn_close(y.cpu().numpy(), ref, f"step {step}")
+        pool = cache.pool.cpu().numpy()
+        for slot, eid in enumerate(ost.id_of_slot):
+            if eid >= 0:
+                assert np.array_equal(pool[slot], bank_h[eid]), f"step {step} slot {slot}"
+    assert fills > 0
+    assert int(plan.err[0].item()) == 0
+
+
+@pytest.mark.parametrize("fmt", [m.FORMAT_MXFP4, m.FORMAT_NVFP4])
+def test_fp4_qwen_shape_layer_steps(oracle, fmt):
+    """Qwen3.6-shaped FP4 layer (H=2048, I=512, E=256, top-8 + shared expert), 4
+    layers, 3 decode steps through the one-kernel step; every layer's output
+    checked on the last step, slot bytes equal to the bank's."""
+    L, H, I, E, k, S, K, T = 4, 2048, 512, 256, 8, 256, 8, 1
+    of = ORACLE_FMT[fmt]
+    bank = synth.make_fp4_bank_torch(L * E + 1, H, I, of, 21 + fmt, DEV)
+    spec = m.make_spec(L, H, I, E, k, has_shared=True, fmt=fmt)
+    cache = m.DeviceCache(spec, S, K, 52700, 77300, bank=bank[:L * E], device=DEV)
+    assert m.moe_layer_kernel_count(spec, cache.c, T) == 1
+    wr_h = [synth.router_weights(300 + l, E, H) for l in range(L)]
+    xs = [synth.ar1_stream(40 + l, 3, H) for l in range(L)]
+    plan = m.DevicePlan(T * k, K, device=DEV)
+    wsb = m.moe_layer_workspace_bytes(spec, T)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    wts = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    y = torch.empty((T, H), dtype=torch.float32, device=DEV)
+    shared_h = bank[L * E].cpu().numpy()
+    for step in range(3):
+        for layer in range(L):
+            xb = xs[layer][step]
+            m.moe_layer_forward(spec, cache.c, layer, dev_bits(xb, DEV), T,
+                                dev_bits(wr_h[layer], DEV), None, bank[L * E], plan.c, ids, wts,
+                                ws, wsb, y)
+            if step == 2:
+                torch.cuda.synchronize()
+                oid, ow = oracle.route_softmax_topk(oracle.router_logits(xb, wr_h[layer]), k)
+                assert np.array_equal(ids.cpu().numpy(), oid)
+                blobs = {int(e): bank[layer * E + int(e)].cpu().numpy() for e in oid.reshape(-1)}
+                ref = _reference(oracle, blobs, H, I, fmt, xb, oid, ow, shared_h)
+                assert_ffn_close(y.cpu().numpy(), ref, f"layer {layer}")
+    torch.cuda.synchronize()
+    assert int(plan.err[0].item()) == 0
+    ids_of = cache.id_of_slot.cpu().numpy()
+    for v in np.nonzero(ids_of >= 0)[0][:64]:
+        assert torch.equal(cache.pool[v], bank[int(ids_of[v])]), f"slot {v}"
