@@ -53,6 +53,16 @@ WORKLOADS = {
              "deepseek_decode_b1",
         L=8, H=7168, I=2048, E=256, k=8, T=8, shared=False, router="sigmoid_group", ng=8, G=4,
         scale=2.5, slots=307, K=8, bp=11800, bh=47500),
+    "qwen_decode_nvfp4": dict(
+        desc="qwen_decode with NVFP4 experts (E2M1 elements, one E4M3 scale per 16, fp32 "
+             "matrix scales), the format the pages deploy Qwen3.6 in",
+        L=40, H=2048, I=512, E=256, k=8, T=1, shared=True, router="softmax", slots=2560, K=8,
+        bp=52700, bh=77300, fmt=2),
+    "deepseek_decode_b1_mxfp4": dict(
+        desc="deepseek_decode_b1 with MXFP4 experts (E2M1 elements, one E8M0 scale per 32), "
+             "the format the pages deploy DeepSeek-V4-Flash in",
+        L=8, H=7168, I=2048, E=256, k=8, T=1, shared=False, router="sigmoid_group", ng=8, G=4,
+        scale=2.5, slots=307, K=8, bp=11800, bh=47500, fmt=1),
     "qwen_prefill": dict(
         desc="Whole-layer prefill, Qwen3.6-35B-A3B layer shape: H=2048, I=512, E=256, top-8 "
              "softmax + shared expert, 8192 tokens of N(0,1) bf16 hidden states with the router "
@@ -222,11 +232,21 @@ def make_inputs(w, n_steps, seed_base=0):
 def spec_of(w):
     import moe_expert_offload_gb300 as m
 
+    fmt = w.get("fmt", m.FORMAT_INT4)
     if w["router"] == "sigmoid_group":
         return m.make_spec(w["L"], w["H"], w["I"], w["E"], w["k"], router="sigmoid_group",
                            n_groups=w["ng"], topk_groups=w["G"], routed_scale=w["scale"],
-                           has_shared=w["shared"])
-    return m.make_spec(w["L"], w["H"], w["I"], w["E"], w["k"], has_shared=w["shared"])
+                           has_shared=w["shared"], fmt=fmt)
+    return m.make_spec(w["L"], w["H"], w["I"], w["E"], w["k"], has_shared=w["shared"], fmt=fmt)
+
+
+def make_bank(w, n, seed, dev):
+    """The workload's expert bank in device memory (int4 or FP4 blobs)."""
+    from moe_expert_offload_gb300 import synth
+
+    if w.get("fmt", 0):
+        return synth.make_fp4_bank_torch(n, w["H"], w["I"], w["fmt"] - 1, seed, dev)
+    return synth.make_bank_torch(n, w["H"], w["I"], seed, dev)
 
 
 # --------------------------------------------------------------- CPU oracle
@@ -244,16 +264,21 @@ class OracleRunner:
         self.xs, self.wr, self.bias = xs, wr, bias
         self.state = oracle.CacheState(w["L"] * w["E"], w["slots"])
         self.blobs = {}
+        self.fp4 = w.get("fmt", 0) - 1  # the oracle's FP4 format, or -1 for int4
         rng = np.random.default_rng(12345)
-        self.shared = synth.make_expert_bytes(rng, w["H"], w["I"]) if w["shared"] else None
+        self.shared = self.make(rng) if w["shared"] else None
         self.spent = 0.0
         self.tokens = 0
+
+    def make(self, rng):
+        if self.fp4 >= 0:
+            return self.synth.make_fp4_expert(rng, self.w["H"], self.w["I"], self.fp4)
+        return self.synth.make_expert_bytes(rng, self.w["H"], self.w["I"])
 
     def blob(self, gid):
         b = self.blobs.get(gid)
         if b is None:
-            b = self.synth.make_expert_bytes(np.random.default_rng(gid + 1), self.w["H"],
-                                             self.w["I"])
+            b = self.make(np.random.default_rng(gid + 1))
             self.blobs[gid] = b
         return b
 
@@ -271,11 +296,26 @@ class OracleRunner:
             o.cache_step(self.state, w["E"], l, ids, w["K"], w["bp"], w["bh"])
             self.spent += time.perf_counter() - t0
             need = {int(e) for e in ids.reshape(-1)}
-            full = [self.blob(l * w["E"] + (e if e in need else next(iter(need))))
-                    for e in range(w["E"])]
-            t0 = time.perf_counter()
-            o.moe_ffn(full, w["H"], w["I"], xb, ids, wt, self.shared, w["I"])
-            self.spent += time.perf_counter() - t0
+            if self.fp4 >= 0:
+                # FP4: the oracle's FP4 expert per routed expert, weighted sum in float64
+                blobs = {e: self.blob(l * w["E"] + e) for e in need}
+                t0 = time.perf_counter()
+                y = np.zeros((xb.shape[0], w["H"]))
+                for e in need:
+                    ye = o.fp4_expert_forward(blobs[e], w["H"], w["I"], self.fp4, xb)
+                    for t in range(xb.shape[0]):
+                        for j in range(ids.shape[1]):
+                            if ids[t, j] == e:
+                                y[t] += float(wt[t, j]) * ye[t]
+                if self.shared is not None:
+                    y += o.fp4_expert_forward(self.shared, w["H"], w["I"], self.fp4, xb)
+                self.spent += time.perf_counter() - t0
+            else:
+                full = [self.blob(l * w["E"] + (e if e in need else next(iter(need))))
+                        for e in range(w["E"])]
+                t0 = time.perf_counter()
+                o.moe_ffn(full, w["H"], w["I"], xb, ids, wt, self.shared, w["I"])
+                self.spent += time.perf_counter() - t0
         self.tokens += w["T"]
 
 
@@ -407,7 +447,7 @@ def run_gpu(args, w, rank, world, local_rank):
     se = m.moe_expert_bytes(spec)
     n_in = 2 * (args.warmup + args.steps)
     xs_h, wr_h, bias_h = make_inputs(w, n_in)
-    bank = synth.make_bank_torch(L * E + (1 if w["shared"] else 0), H, I, 7, dev)
+    bank = make_bank(w, L * E + (1 if w["shared"] else 0), 7, dev)
     shared = bank[L * E] if w["shared"] else None
     cache = m.DeviceCache(spec, w["slots"], w["K"], w["bp"], w["bh"], bank[:L * E], device=dev)
     plan = m.DevicePlan(T * k, w["K"], device=dev)
