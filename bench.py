@@ -146,10 +146,12 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload, experts_per_ffn):
-    """DRAM bytes per FFN launch from the committed ncu summary, if it was taken
-    on the current kernel source (else None).  An entry captured on another
-    workload of the same expert shape is scaled by the experts per launch."""
+def ncu_traffic(workload, experts_per_launch, router_bytes):
+    """DRAM bytes per launch of the timed kernel from the committed ncu summary,
+    if it was taken on the current kernel source (else None).  The summary holds
+    the bytes per expert of a smaller capture of the same expert shape (reads and
+    writes, less the router weights); they are scaled by the experts each launch
+    executes, plus this workload's router weights."""
     p = os.path.join(ROOT, "profiles", "ffn_decode_traffic.json")
     if not os.path.exists(p):
         return None
@@ -157,9 +159,7 @@ def ncu_traffic(workload, experts_per_ffn):
     e = d.get(workload)
     if not e or e.get("source_hash") != kernel_source_hash():
         return None
-    if e.get("scaled"):
-        return float(e["bytes_per_expert"]) * experts_per_ffn
-    return float(e["dram_bytes_per_ffn"])
+    return float(e["bytes_per_expert"]) * experts_per_launch + router_bytes
 
 
 class ClockSampler:
@@ -632,7 +632,8 @@ def run_gpu(args, w, rank, world, local_rank):
     value = tokens / (ms * 1e-3)
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
             "frac": achieved / hbm,
-            "traffic": ncu_traffic(args.workload, n_uniq / layer_steps + (1 if w["shared"] else 0)),
+            "traffic": ncu_traffic(args.workload, n_uniq / layer_steps + (1 if w["shared"] else 0),
+                                   E * H * 2 if one_kernel else 0),
             "kernel": ("decode layer step (moe_layer_forward as one cooperative kernel: router "
                        "logits, selection, control step, gate/up + down carrying the fill)"
                        if one_kernel else

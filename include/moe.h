@@ -368,8 +368,10 @@ int moe_layer_forward_prefill(const moe_spec* spec, const void* layer_experts, c
  *   - Sizes whose scratch need (moe_ffn_workspace_bytes(spec, T)) exceeds
  *     MOE_NOALLOC_SCRATCH_BYTES are rejected with MOE_ECAPACITY.
  *   - The first call on a device looks up the array's device address for the
- *     current device (cudaGetSymbolAddress); make that first call before any
- *     stream capture.
+ *     current device (cudaGetSymbolAddress) and keeps it; make that first call
+ *     before any stream capture.  A device reset (cudaDeviceReset) reloads the
+ *     library's device code and invalidates the kept address: do not use this
+ *     entry point on a device after resetting it.
  *   - All calls share the one array, which keeps the last call's contents
  *     (the arrival counters are cleared by every call).  Calls whose
  *     execution overlaps on the GPU (different streams, or different host

@@ -839,7 +839,11 @@ namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kNoAllocMaxDevices = 64;
-void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+// The array's device address per device, looked up on first use.  Atomic:
+// host threads may make their first call concurrently (each stores the same
+// address).  A device reset reloads the module and invalidates the address;
+// moe.h asks callers not to use this entry point across a reset.
+std::atomic<void*> g_noalloc_ptr[kNoAllocMaxDevices];
 
 int noalloc_scratch(void** out) {
   int dev = 0;
@@ -847,13 +851,13 @@ int noalloc_scratch(void** out) {
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= kNoAllocMaxDevices)
     return fail(MOE_EUNSUPPORTED, "device ordinal %d >= %d", dev, kNoAllocMaxDevices);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
+  void* p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+  if (!p) {
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || !p) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
-    g_noalloc_ptr[dev] = p;
+    g_noalloc_ptr[dev].store(p, std::memory_order_release);
   }
-  *out = g_noalloc_ptr[dev];
+  *out = p;
   return MOE_OK;
 }
 

@@ -29,12 +29,15 @@ def _built():
     m.lib()
 
 
-@pytest.mark.parametrize("T", [1, 4])
-def test_noalloc_matches_workspace_ffn_on_two_calls(T):
-    H, I, E, k, S, K = 2048, 512, 32, 8, 12, 4
+@pytest.mark.parametrize("H,I,E,T", [(2048, 512, 32, 1), (2048, 512, 32, 4),
+                                     (2048, 512, 32, 16), (7168, 2048, 16, 8)])
+def test_noalloc_matches_workspace_ffn_on_two_calls(H, I, E, T):
+    """Qwen-shaped experts at 1, 4 and 16 tokens (16: past the cooperative
+    kernel's 8, so the other FFN kernels run on the built-in array) and
+    DeepSeek-shaped experts at 8 tokens."""
+    k, S, K = 8, 12, 4
     spec = m.make_spec(1, H, I, E, k, has_shared=True)
-    bank_h = synth.make_bank(E + 1, H, I, seed=21)
-    bank = dev(bank_h, DEV)
+    bank = synth.make_bank_torch(E + 1, H, I, 21, DEV)
     shared = bank[E]
     cache = m.DeviceCache(spec, S, K, 52700, 77300, bank=bank[:E], device=DEV)
     plan = m.DevicePlan(T * k, K, device=DEV)
