@@ -280,16 +280,22 @@ size_t moe_layer_workspace_bytes(const moe_spec* spec, int32_t T);
  * moe_expert_ffn for one decode layer, no host sync.
  *   ids, weights  device out [T][k] (the routing decision, kept for the caller)
  *   workspace     >= moe_layer_workspace_bytes(spec, T)
- * The fill copies (bank -> slot of every F expert): when the decode FFN's
- * streaming kernels serve the shape (hidden % 512 == 0, inter % 256 == 0,
- * T <= 8, T*k + shared <= 128, and their shared-memory plan fits), those
- * kernels write each F expert's bytes into its slot as they read them from
- * the bank (FreeToken summary "method steps": the miss path fills the slot),
- * so no separate copy runs.  Otherwise a copy kernel runs beside the FFN on
- * a stream owned by the library and `stream` waits for it before any later
- * work.  Either way everything the call enqueues is complete, in order, from
- * the caller's stream's view (also when the stream is being captured into a
- * graph), and the slot contents are the same.
+ * One kernel: when `cache->sync` is set and the shape allows it (the
+ * cooperative FFN's shape: hidden % 1024 == 0, inter % 512 == 0, T <= 8; and
+ * T*k <= 32, k_victims <= 8, num_experts <= 256), the whole step -- router
+ * logits, selection, control step, FFN and fills -- is one cooperative kernel
+ * (moe_layer_kernel_count == 1); it uses the cache's sync words and leaves
+ * them zero.  Otherwise the step is a chain of kernels.
+ * The fill copies (bank -> slot of every F expert): when a decode FFN kernel
+ * carries them (the cooperative kernel; the streaming kernels for hidden %
+ * 512 == 0, inter % 256 == 0, T <= 8, T*k + shared <= 128), it writes each F
+ * expert's bytes into its slot as it reads them from the bank (FreeToken
+ * summary "method steps": the miss path fills the slot), so no separate copy
+ * runs.  Otherwise a copy kernel runs beside the FFN on a stream owned by the
+ * library and `stream` waits for it before any later work.  Either way
+ * everything the call enqueues is complete, in order, from the caller's
+ * stream's view (also when the stream is being captured into a graph), and
+ * the slot contents are the same.
  * ------------------------------------------------------------------------ */
 int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, const void* x,
                       int32_t T, const void* w_router, const float* bias, const void* shared,
@@ -298,12 +304,16 @@ int moe_layer_forward(const moe_spec* spec, moe_cache* cache, int32_t layer, con
 
 /* Test hook for failure detection without a GPU fault.  With on != 0 the
  * next decode FFN call of this process (moe_expert_ffn or moe_layer_forward,
- * on a shape the streaming kernels serve) issues no weight copies in its
- * gate/up kernel: that kernel's warps find their stages never filled, give
- * up after their bounded wait (one second of device time each), set
- * MOE_DERR_WAIT in plan->err and return; y of that call is undefined.  The
- * flag is cleared by that call (or by on == 0); the device context stays
- * usable and the next call runs normally.  Returns MOE_OK. */
+ * on a shape the cooperative or streaming kernels serve) issues no weight
+ * copies: the kernel's warps find their stages never filled, give up after
+ * their bounded wait (2^31 SM clock cycles after 1024 polling rounds, about a
+ * second at full clock), set MOE_DERR_WAIT in plan->err and return; y of that
+ * call is undefined.  When the call carried the step's fills (moe_layer_forward)
+ * the experts it filled are unmapped again (slot_of_id = -1, the slot empty,
+ * ts 0), so the cache never maps a partly written slot.  The flag is cleared
+ * by that call (or by on == 0); the device context stays usable and the next
+ * call runs normally.  Any bounded wait that runs out for another reason has
+ * the same effect.  Returns MOE_OK. */
 int moe_debug_inject_ffn_stall(int32_t on);
 
 /* Kernels one moe_layer_forward call on `cache` launches for T tokens (for
