@@ -164,24 +164,31 @@ def test_cache_step_matches_oracle_on_random_traces(oracle, L, E, S, K, bp, bh, 
         _tables_equal(cache, ost)
 
 
-@pytest.mark.parametrize("S", [512, 5120])
-def test_cache_step_zipf_trace_sweep_shape(oracle, S):
-    L, E, k, K, steps = 40, 256, 8, 8, 6
+@pytest.mark.parametrize("S,bp,bh", [(512, 52700, 77300), (5120, 52700, 77300),
+                                     (2560, 11800, 47500), (2560, 77300, 77300)])
+def test_cache_step_zipf_trace_sweep_shape(oracle, S, bp, bh):
+    """The cache sweep's shape (40 layers x 256 experts, top-8 Zipf traces with step
+    overlap, K=8) over 64 steps at each B_P/B_H pair of the sweep: plans every 13th layer
+    and all tables after every step, bit for bit."""
+    L, E, k, K, steps = 40, 256, 8, 8, 64
     spec = m.make_spec(L, 64, 64, E, k)
-    cache = m.DeviceCache(spec, S, K, 52700, 77300, bank=None, device=DEV, with_pool=False)
+    cache = m.DeviceCache(spec, S, K, bp, bh, bank=None, device=DEV, with_pool=False)
     plan = m.DevicePlan(k, K, device=DEV)
     ost = oracle.CacheState(L * E, S)
     traces = [synth.zipf_trace(1000 + l, steps, E, k) for l in range(L)]
+    fills = 0
     for s in range(steps):
         for layer in range(L):
             ids_h = traces[layer][s:s + 1]
             m.moe_cache_step(spec, cache.c, layer, dev(ids_h, DEV), 1, plan.c, do_fill=0)
-            op = oracle.cache_step(ost, E, layer, ids_h, K, 52700, 77300)
+            op = oracle.cache_step(ost, E, layer, ids_h, K, bp, bh)
+            fills += op["n_fill"]
             if layer % 13 == 0:
                 torch.cuda.synchronize()
                 _plans_equal(plan.read(K), op, K)
         torch.cuda.synchronize()
         _tables_equal(cache, ost)
+    assert fills > 0
 
 
 def test_cache_step_all_hits_then_duplicates(oracle):

@@ -101,8 +101,9 @@ def test_layer_prefetch_copies_the_layer():
 
 def test_full_size_qwen_prefill_layer(oracle):
     """One Qwen-shaped layer, 8192 tokens with router logits raised on expert t mod 256 so the
-    routing union covers all 256 experts; routing on sampled tokens bit-exact, sampled FFN rows
-    against the oracle."""
+    routing union covers all 256 experts; routing on sampled tokens bit-exact; against the
+    oracle, every output row of the two experts with the most assignments (several m-tiles
+    each) and a full 256-row m-tile of the shared expert."""
     H, I, E, k, T = 2048, 512, 256, 8, 8192
     spec = m.make_spec(1, H, I, E, k, has_shared=True)
     bank = synth.make_bank_torch(E + 1, H, I, 11, DEV)
@@ -125,13 +126,24 @@ def test_full_size_qwen_prefill_layer(oracle):
     oid, ow = oracle.route_softmax_topk(lg, k)
     assert np.array_equal(ids_g[sample], oid)
     assert np.array_equal(f32_bits(w_g[sample]), f32_bits(ow))
-    chk = sample[:12]
-    need = {int(e) for e in ids_g[chk].reshape(-1)}
-    blobs = {e: bank[e].cpu().numpy() for e in need}
-    anyb = blobs[next(iter(need))]
-    ref = oracle.moe_ffn([blobs.get(e, anyb) for e in range(E)], H, I, xb[chk], ids_g[chk],
-                         w_g[chk], bank[E].cpu().numpy(), I)
-    assert_ffn_close(y_g[chk], ref, "full-size prefill sample")
+    # every output row of the two experts with the most assignments (each spans two or more
+    # 256-row m-tiles of its group), and one full 256-row m-tile of the shared expert's group
+    # (the shared group takes the tokens in order)
+    counts = np.bincount(ids_g.reshape(-1), minlength=E)
+    top2 = np.argsort(-counts, kind="stable")[:2]
+    assert counts[top2].min() > 256, counts[top2]
+    rows = sorted(set(np.nonzero(np.isin(ids_g, top2).any(axis=1))[0].tolist()) |
+                  set(range(2048, 2048 + 256)))
+    rows = np.asarray(rows)
+    blobs = list(bank[:E].cpu().numpy())
+    import os
+    oracle.set_threads(os.cpu_count() or 1)
+    try:
+        ref = oracle.moe_ffn(blobs, H, I, xb[rows], ids_g[rows], w_g[rows],
+                             bank[E].cpu().numpy(), I)
+    finally:
+        oracle.set_threads(1)
+    assert_ffn_close(y_g[rows], ref, f"full-size prefill: {len(rows)} rows")
     assert np.all(np.isfinite(y_g))
     del bank
     torch.cuda.empty_cache()
