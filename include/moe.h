@@ -95,8 +95,10 @@ enum { MOE_ROUTER_SOFTMAX_TOPK = 0, MOE_ROUTER_SIGMOID_GROUP = 1 };
 enum { MOE_FORMAT_INT4 = 0, MOE_FORMAT_MXFP4 = 1, MOE_FORMAT_NVFP4 = 2 };
 
 /* Device-side error bits written to plan->err[0] (OR-ed, never cleared by the
- * library; the caller may zero it). */
-enum { MOE_DERR_BAD_ID = 1, MOE_DERR_WAIT = 2 };
+ * library; the caller may zero it).  MOE_DERR_RANGE: checked builds only
+ * (libmoe_checked.so, compiled with -DMOE_CHECKED): a cache-table entry read
+ * on the device lay outside its range and was treated as absent. */
+enum { MOE_DERR_BAD_ID = 1, MOE_DERR_WAIT = 2, MOE_DERR_RANGE = 4 };
 
 /* Model description (Edge0 §3 "MoESpec": expert count, routing family,
  * quantisation, layout). */

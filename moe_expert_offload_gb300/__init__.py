@@ -27,6 +27,7 @@ MOE_ROUTER_SOFTMAX_TOPK = 0
 MOE_ROUTER_SIGMOID_GROUP = 1
 MOE_DERR_BAD_ID = 1
 MOE_DERR_WAIT = 2
+MOE_DERR_RANGE = 4  # checked builds only (libmoe_checked.so)
 
 EXPORTED = (
     "moe_last_error", "moe_version", "moe_expert_bytes", "moe_route", "moe_cache_reset",
@@ -81,16 +82,20 @@ _lib = None
 
 
 def library_path() -> str:
-    return _build.LIB
+    """libmoe.so, or the library named by MOE_LIBRARY (e.g. the checked build,
+    libmoe_checked.so)."""
+    return os.environ.get("MOE_LIBRARY") or _build.LIB
 
 
 def lib():
     """Load libmoe.so; raise if it has not been built (no fallback path exists)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(_build.LIB):
-            raise RuntimeError("libmoe.so is not built; run __graft_entry__.build() first")
-        L = C.CDLL(_build.LIB)
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{os.path.basename(path)} is not built; run "
+                               "__graft_entry__.build() first")
+        L = C.CDLL(path)
         vp, i32, sz = C.c_void_p, C.c_int32, C.c_size_t
         sp, cp, pp = C.POINTER(MoeSpec), C.POINTER(MoeCache), C.POINTER(MoePlan)
         L.moe_last_error.restype = C.c_char_p

@@ -32,24 +32,30 @@ def _deps():
         os.path.join(ROOT, "include", "moe.h")]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+# The checked build (-DMOE_CHECKED): device-side range checks on cache-table
+# entries that OR MOE_DERR_RANGE into the error word (include/moe.h).
+LIB_CHECKED = os.path.join(HERE, "libmoe_checked.so")
+
+
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
-    out = os.path.join(HERE, "_build")
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    lib = LIB_CHECKED if checked else LIB
+    if not force and up_to_date(lib):
+        return lib
+    out = os.path.join(HERE, "_build_checked" if checked else "_build")
     os.makedirs(out, exist_ok=True)
     cc = nvcc()
-    objs = []
+    extra = ["-DMOE_CHECKED"] if checked else []
 
     def one(src):
         obj = os.path.join(out, os.path.basename(src)[:-3] + ".o")
-        cmd = [cc, *ARCH, *FLAGS, "-c", src, "-o", obj]
+        cmd = [cc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -59,12 +65,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
         objs = list(ex.map(one, _sources()))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

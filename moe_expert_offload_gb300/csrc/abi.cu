@@ -125,6 +125,8 @@ moe::CacheArgs cache_args(const moe_spec* spec, moe_cache* c, int32_t layer, con
   a.S0 = per_layer ? layer * a.S : 0;
   a.no_fill = c->policy == MOE_POLICY_STATIC;
   a.K = c->k_victims;
+  a.n_slots = c->num_slots;
+  a.n_bank = spec->num_layers * spec->num_experts;
   a.bp = c->bp_mbps;
   a.bh = c->bh_mbps;
   a.ids = ids;

@@ -120,7 +120,8 @@ __global__ void __launch_bounds__(kCtlThreads) cache_step_kernel(CacheArgs a, Se
       const int r = base + tid;
       const bool valid = r < n_uniq;
       const int32_t u = valid ? s.suniq[r] : 0;
-      const int32_t slot = valid ? a.slot_of_id[u] : -1;
+      int32_t slot = valid ? a.slot_of_id[u] : -1;
+      if (valid && !checked_ok(slot >= -1 && slot < a.n_slots, a.plan.err)) slot = -1;
       const bool hit = valid && slot >= 0, miss = valid && slot < 0;
       const unsigned hb = __ballot_sync(0xffffffffu, hit), mb = __ballot_sync(0xffffffffu, miss);
       if (lane == 0) {

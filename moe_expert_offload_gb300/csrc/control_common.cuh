@@ -142,7 +142,8 @@ __device__ __forceinline__ void ctl_classify_warp(const CacheArgs& a, CtlShared<
   // hit / miss in rank order, order-preserving compaction
   const bool valid = lane < nu;
   const int32_t u = valid ? s.suniq[lane] : 0;
-  const int32_t slot = valid ? slot_of(u) : -1;
+  int32_t slot = valid ? slot_of(u) : -1;
+  if (valid && !checked_ok(slot >= -1 && slot < a.n_slots, a.plan.err)) slot = -1;
   const bool hit = valid && slot >= 0, miss = valid && slot < 0;
   const unsigned hb = __ballot_sync(0xffffffffu, hit), mb = __ballot_sync(0xffffffffu, miss);
   if (valid) s.sslot[lane] = slot;
@@ -239,7 +240,8 @@ __device__ __forceinline__ void ctl_evict(const CacheArgs& a, CtlShared<KMAX, NT
     const int32_t v = a.S0 + (int32_t)(s.svict[tid] & 0xffffffffu);
     const int32_t f = s.smiss[tid];
     const int32_t known = s.sold[tid];  // -2: the slot's id was not prefetched
-    const int32_t old = known != -2 ? known : a.id_of_slot[v];
+    int32_t old = known != -2 ? known : a.id_of_slot[v];
+    if (!checked_ok(old >= -1 && old < a.n_bank, a.plan.err)) old = -1;
     if (old >= 0) a.slot_of_id[old] = -1;  // an evicted id is never one of F
     a.id_of_slot[v] = f;
     a.slot_of_id[f] = v;

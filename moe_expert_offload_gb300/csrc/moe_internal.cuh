@@ -65,6 +65,23 @@ inline int64_t expert_blob_bytes(int64_t H, int64_t I, int format) {
   return format == MOE_FORMAT_INT4 ? blob_offsets(H, I).total : fp4_offsets(H, I, format).total;
 }
 
+// Checked builds (-DMOE_CHECKED): cache-table entries read on the device are
+// range-checked before they index anything; an entry outside its range ORs
+// MOE_DERR_RANGE into the error word and is treated as absent.  In normal
+// builds the check compiles away.
+__device__ __forceinline__ bool checked_ok(bool in_range, int32_t* err) {
+#ifdef MOE_CHECKED
+  if (!in_range) {
+    if (err) atomicOr(err, MOE_DERR_RANGE);
+    return false;
+  }
+#else
+  (void)in_range;
+  (void)err;
+#endif
+  return true;
+}
+
 // Programmatic dependent launch (the decode layer path).  A kernel launched
 // with launch_pdl may be scheduled while the previous kernel in the stream is
 // still running: it calls griddep_wait() before its first access to memory
@@ -111,6 +128,7 @@ cudaError_t launch_router_select(const moe_spec& sp, const float* logits, const 
 // no_fill (static placement) makes q = 0.
 struct CacheArgs {
   int E = 0, layer = 0, n_ids = 0, S0 = 0, S = 0, K = 0, bp = 0, bh = 0, no_fill = 0;
+  int n_slots = 0, n_bank = 0;  // all slots of the pool; L * E (range checks)
   // words the step clears for the decode FFN that follows it (its counters)
   uint32_t* zero_words = nullptr;
   int n_zero = 0;
@@ -208,7 +226,8 @@ struct FfnArgs {
 // this sits on the FFN's start-up path.
 __device__ __forceinline__ int32_t ffn_slot(const FfnArgs& a, int32_t id,
                                             int32_t* fs = nullptr) {
-  const int32_t slot = a.slot_of_id[id];
+  int32_t slot = a.slot_of_id[id];
+  if (!checked_ok(slot >= -1 && slot < a.n_pool, a.err)) slot = -1;
   const int nf = a.counts[4];
   const bool want = fs != nullptr && a.fill_fused;
   bool filled = false;
