@@ -777,6 +777,13 @@ def run_prefill(args, w, rank, world, local_rank):
     for s in range(min(args.warmup, 3)):
         step_serial(s)
     ms_serial, _ = timed(step_serial, args.steps, False)
+    # the double buffer's parts: the layer copy alone, and the layer step with no
+    # copy anywhere (its FFN time against the FFN time beside the copy)
+    ms_copy, _ = timed(lambda s, ev=None: m.moe_layer_prefetch(spec, bank, (s + 1) % L, bufs[1],
+                                                              main.cuda_stream),
+                       args.steps, False)
+    ms_nocopy, evs_nc = timed(lambda s, ev=None: compute(s, bufs[0], ev), args.steps, True)
+    ffn_nocopy = statistics.mean(e[1].elapsed_time(e[2]) for e in evs_nc)
     assert int(err.cpu()[0]) == 0, "device error flag set"
 
     # end to end: hidden states in from pinned host memory, y back, every step
@@ -835,7 +842,8 @@ def run_prefill(args, w, rank, world, local_rank):
         "prefill_tok_s": tokens / (ms * 1e-3),
         "ffn_tflops": tflops,
         "layer_ms": {"overlapped_copy": step_ms, "serial_copy": ms_serial / args.steps,
-                     "route": route_ms, "ffn": ffn_ms},
+                     "copy_alone": ms_copy / args.steps, "without_copy": ms_nocopy / args.steps,
+                     "route": route_ms, "ffn": ffn_ms, "ffn_without_copy": ffn_nocopy},
         "e2e": {"value": flops * args.steps * world / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "tok_s": tokens / (ms_e2e * 1e-3),
                 "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 4},

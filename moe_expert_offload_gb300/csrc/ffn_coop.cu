@@ -362,14 +362,122 @@ struct ConsSync {
 // control step in the ring's shared memory (CTA 0 streams no weights).
 constexpr int kCtlK = 8;  // victims per step (KMAX of the victim lists)
 using CtlSh = ctl::CtlShared<kCtlK, kConsThreads>;
+constexpr int kWideK = 8;  // the wide (one-token) selection's largest k
 struct SelScratch {
   float a[kMaxTok][32 * 8];
   float b[kMaxTok][rsel::kMaxK], c[kMaxTok][rsel::kMaxK];
   float sum[kMaxTok];
   int32_t slot[256];  // slot_of_id of the layer's E experts before the step
+  // the wide selection: each warp's k best (order key, expert id, value) at
+  // position w k + r, and the group scores
+  uint32_t ckey[kCW * kWideK];
+  int32_t cid[kCW * kWideK];
+  float cval[kCW * kWideK];
+  float gs[kCW];
 };
 static_assert(sizeof(CtlSh) + sizeof(SelScratch) <= 3 * (size_t)kSlotBytes,
               "control step scratch must fit in the smallest ring");
+
+// Router selection of a single token by E / 32 warps (E % 32 == 0, E <= 512,
+// k <= 8): warp w holds experts 32 w + lane.  The same decisions and weights
+// as rsel::softmax_token / rsel::sigmoid_group_token (the order of rsel::better
+// everywhere): each warp takes its own k best, writes them at positions
+// w k + r (ascending expert id among equal scores), and warp 0 takes the k best
+// of those.  Sigmoid-group with one warp per group (E / n_groups == 32): the
+// group scores (sum of the two largest selection scores) meet in shared memory
+// first, and only the kept groups' warps put forward candidates.  All consumer
+// threads call it; warp 0 writes ids / weights.
+__device__ void select_wide(const LayerFuse& lf, int E, int k, int32_t* ids, float* wts,
+                            SelScratch& ss) {
+  const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
+  const int NW = E >> 5;
+  const bool sig = lf.router != MOE_ROUTER_SOFTMAX_TOPK;
+  float v = 0.0f, sv = 0.0f;  // this lane's logit (softmax) or sigmoid score
+  uint32_t key = 0u;
+  if (wid < NW) {
+    const int e = 32 * wid + lane;
+    const float l = __ldcg(lf.logits + e);
+    if (sig) {
+      const float bias = lf.sel_bias ? __ldg(lf.sel_bias + e) : 0.0f;
+      sv = rsel::moe_sigmoid(l);
+      v = __fadd_rn(sv, bias);  // selection score
+      // the group's two largest selection scores (t2 == t1 when it appears twice)
+      float t1 = v, t2 = -FLT_MAX;
+#pragma unroll
+      for (int d = 16; d >= 1; d >>= 1) {
+        const float b1 = __shfl_xor_sync(0xffffffffu, t1, d);
+        const float b2 = __shfl_xor_sync(0xffffffffu, t2, d);
+        t2 = fmaxf(fminf(t1, b1), fmaxf(t2, b2));
+        t1 = fmaxf(t1, b1);
+      }
+      if (lane == 0) ss.gs[wid] = __fadd_rn(t1, t2);
+    } else {
+      v = l;
+      sv = l;
+    }
+    key = rsel::ord_key(v);
+  }
+  if (sig) {
+    cons_sync();
+    // this warp's group kept: fewer than topk_groups groups ahead of it
+    if (wid < NW) {
+      const float mine = ss.gs[wid];
+      int ahead = 0;
+      for (int h = 0; h < NW; ++h) ahead += rsel::better(ss.gs[h], h, mine, wid) ? 1 : 0;
+      if (ahead >= lf.topk_groups) key = 0u;
+    }
+  }
+  if (wid < NW) {
+    // the warp's k best: a winner lane drops out; rank r goes to position w k + r
+    for (int r = 0; r < k; ++r) {
+      const uint32_t M = __reduce_max_sync(0xffffffffu, key);
+      const uint32_t me = (M != 0u && key == M) ? (uint32_t)lane : 0xffffffffu;
+      const uint32_t wl = __reduce_min_sync(0xffffffffu, me);
+      const float wv = __shfl_sync(0xffffffffu, sv, wl & 31);
+      if (lane == 0) {
+        ss.ckey[wid * kWideK + r] = M;
+        ss.cid[wid * kWideK + r] = M != 0u ? 32 * wid + (int)wl : 0x7fffffff;
+        ss.cval[wid * kWideK + r] = wv;
+      }
+      if ((uint32_t)lane == wl) key = 0u;
+    }
+  }
+  cons_sync();
+  if (wid == 0) {
+    // up to 16 x 8 candidates, four per lane at positions lane + 32 i
+    constexpr int CPL = kCW * kWideK / 32;
+    uint32_t ck[CPL], cs[CPL];
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int pos = lane + 32 * i, w = pos / kWideK, r = pos % kWideK;
+      ck[i] = (w < NW && r < k) ? ss.ckey[w * kWideK + r] : 0u;
+      cs[i] = (uint32_t)i;
+    }
+    rsel::lane_sort_desc<CPL>(ck, cs);
+    int rid[2];
+    rsel::warp_topk<CPL>(ck, cs, k, rid);  // positions w k' + r (k' = kWideK)
+    const int pos = rid[0];
+    const bool got = lane < k && pos != 0x7fffffff;
+    const int e = got ? ss.cid[pos] : 0x7fffffff;
+    const float val = got ? ss.cval[pos] : 0.0f;
+    float S = 0.0f;
+    if (sig) {
+      for (int r = 0; r < k; ++r) S = __fadd_rn(S, __shfl_sync(0xffffffffu, val, r));
+      if (lane < k) {
+        ids[lane] = e;
+        wts[lane] = __fmul_rn(__fdiv_rn(val, S), lf.scale);
+      }
+    } else {
+      const float top = __shfl_sync(0xffffffffu, val, 0);
+      const float ex = lane < k ? rsel::moe_exp(__fsub_rn(val, top)) : 0.0f;
+      for (int r = 0; r < k; ++r) S = __fadd_rn(S, __shfl_sync(0xffffffffu, ex, r));
+      if (lane < k) {
+        ids[lane] = e;
+        wts[lane] = __fdiv_rn(ex, S);
+      }
+    }
+  }
+}
 
 // Every CTA of the one-kernel layer step, consumer threads (tid < 512), once
 // every CTA's logits are stored: the router selection (one warp per token,
@@ -393,7 +501,11 @@ __device__ bool layer_route_classify(const FfnArgs& a, const LayerFuse& lf, CtlS
   }
   cons_sync();
   if (cs.nu < 0) return false;
-  if (wid < T) {
+  const bool wide = T == 1 && (E & 31) == 0 && E <= 32 * kCW && k <= kWideK &&
+                    (lf.router == MOE_ROUTER_SOFTMAX_TOPK || E / lf.n_groups == 32);
+  if (wide) {
+    select_wide(lf, E, k, s_ids, s_wts, ss);
+  } else if (wid < T) {
     if (lf.router == MOE_ROUTER_SOFTMAX_TOPK)
       rsel::softmax_token<8>(lf.logits, wid, E, k, s_ids, s_wts, ss.b[wid], ss.c[wid],
                              &ss.sum[wid]);
@@ -491,6 +603,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // x as fp16 B fragments of this CTA (scaled by a power of two per token),
   // the per-group sums O and X of the scaled, rounded values, and y = 0 on
   // this CTA's slice of the NY CTAs that run tiles (consumer threads)
+  auto zero_y = [&](unsigned yb, unsigned NY) {
+    const unsigned ny = (unsigned)T * H;
+    for (unsigned i = yb * ny / NY + tid; i < (yb + 1) * ny / NY; i += kConsThreads) a.y[i] = 0.0f;
+  };
   auto prep_x = [&](unsigned yb, unsigned NY) {
     const int ctid = tid;
     for (int t = 0; t < T; ++t) {
@@ -539,9 +655,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (in && q4 == 0) ox[G * kMaxTok + t] = make_float2(o, xs);
     }
     // y starts at zero (ordered before the down tiles' adds by the grid-wide
-    // gate/up count)
-    const unsigned ny = (unsigned)T * H;
-    for (unsigned i = yb * ny / NY + ctid; i < (yb + 1) * ny / NY; i += kConsThreads) a.y[i] = 0.0f;
+    // gate/up count; the one-kernel step zeroes it before its logits count)
+    if (!FUSED) zero_y(yb, NY);
     cons_sync();
   };
 
@@ -595,6 +710,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             rsel::router_dot_warp(a.x + (size_t)t * H, lf.w_router + (size_t)e * H, H);
         if (lane == 0) lf.logits[p] = v;
       }
+      // y starts at zero: ordered before every down tile's adds by the logits count,
+      // which every CTA waits for before its first tile
+      if (!ctl_cta) zero_y(b, G);
       cons_sync();
       if (tid == 0) red_release_gpu_add(sync + kSyncLogits);
       if (!ctl_cta) prep_x(b, G);
@@ -1027,29 +1145,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         // count); then entry r's h as B fragments, replacing the previous ones
         ntok = s_ntok[r];
         cons_sync();
-        if (ctid == 0) {
-          // every CTA's h rows (all entries) before the first down tile
-          if (cur < 0 && ok && !wait_count(gu_cnt, Gall)) s_fail = 1;
-          const int uid = s_uid[r];
-          for (int nn = 0; nn < ntok; ++nn) {
-            const float inv = inv_pow2_above(__uint_as_float(__ldcg(hmax + r * kMaxTok + nn)));
-            s_ih[nn] = inv;
-            // routing weight of this entry for the slot's token: the sum over the
-            // ranks j naming it (a token may list an expert twice); 1 for the
-            // shared expert
-            float wsum = 1.0f;
-            if (r < n_uniq) {
-              const int t = s_tok[r][nn];
-              wsum = 0.0f;
-              for (int j = 0; j < k; ++j)
-                if (base + s_ids[t * k + j] == uid) wsum += s_wts[t * k + j];
-            }
-            if constexpr (FMT != MOE_FORMAT_INT4) wsum *= s_fac[r][2];
-            s_wp[nn] = wsum / inv;
-          }
-        }
+        if (ctid == 0 && ok && cur < 0 && !wait_count(gu_cnt, Gall)) s_fail = 1;
         cur = r;
         cons_sync();
+        // h, its per-token maxima and the routing weights in one round of loads
+        if (ctid < ntok) {
+          const int nn = ctid;
+          const float inv = inv_pow2_above(__uint_as_float(__ldcg(hmax + r * kMaxTok + nn)));
+          s_ih[nn] = inv;
+          // routing weight of this entry for the slot's token: the sum over the
+          // ranks j naming it (a token may list an expert twice); 1 for the
+          // shared expert
+          float wsum = 1.0f;
+          if (r < n_uniq) {
+            const int t = s_tok[r][nn], uid = s_uid[r];
+            wsum = 0.0f;
+            for (int j = 0; j < k; ++j)
+              if (base + s_ids[t * k + j] == uid) wsum += s_wts[t * k + j];
+          }
+          if constexpr (FMT != MOE_FORMAT_INT4) wsum *= s_fac[r][2];
+          s_wp[nn] = wsum / inv;
+        }
         const float* hr = a.h + (int64_t)r * T * I;
         const int ngi = I / 64, n_items = ntok * ngi * 4;
         for (int b0 = 0; b0 < n_items; b0 += kConsThreads) {
@@ -1060,16 +1176,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           float v[16];
           float o = 0.0f, xs = 0.0f;
           if (in) {
-            const float sc = s_ih[nn];
             const float4* ph =
                 reinterpret_cast<const float4*>(hr + (int64_t)nn * I + G * 64 + q4 * 16);
+            float4 f[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) f[e] = __ldcg(ph + e);
+            const float sc =
+                inv_pow2_above(__uint_as_float(__ldcg(hmax + r * kMaxTok + nn)));
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float4 f = __ldcg(ph + e);
-              v[4 * e] = f.x * sc;
-              v[4 * e + 1] = f.y * sc;
-              v[4 * e + 2] = f.z * sc;
-              v[4 * e + 3] = f.w * sc;
+              v[4 * e] = f[e].x * sc;
+              v[4 * e + 1] = f[e].y * sc;
+              v[4 * e + 2] = f[e].z * sc;
+              v[4 * e + 3] = f[e].w * sc;
             }
             if constexpr (FMT == MOE_FORMAT_INT4)
               frag_item(v, frag + (size_t)nn * geo.frow + G * 128 + q4 * 32, o, xs);
