@@ -715,9 +715,10 @@ def run_prefill(args, w, rank, world, local_rank):
     side = torch.cuda.Stream()
     copy_done = [torch.cuda.Event() for _ in range(2)]
     comp_done = [torch.cuda.Event() for _ in range(2)]
+    route_done = torch.cuda.Event()
     fws = m.moe_prefill_workspace_bytes(spec, T)
 
-    def compute(s, buf, ev=None):
+    def compute(s, buf, ev=None, after_route=None):
         l = s % L
         sp = main.cuda_stream
         if ev is not None:
@@ -725,17 +726,26 @@ def run_prefill(args, w, rank, world, local_rank):
         m.moe_route(spec, xs[l], T, wr[l], None, logits, ids, wts, sp)
         if ev is not None:
             ev[1].record(main)
+        if after_route is not None:
+            after_route()
         m.moe_expert_ffn_prefill(spec, buf, xs[l], T, ids, wts, shared, err, ws, fws, y, sp)
         if ev is not None:
             ev[2].record(main)
 
     def step_overlap(s, ev=None):
-        # layer s % L computes from bufs[s % 2] while layer (s+1) % L streams into the other
+        # layer s % L computes from bufs[s % 2] while layer (s+1) % L streams into the
+        # other.  The copy starts once this step's routing is done, so that it runs
+        # beside the tensor-bound expert GEMMs, not beside the memory-bound routing
         main.wait_event(copy_done[s % 2])
-        side.wait_event(comp_done[(s + 1) % 2])
-        m.moe_layer_prefetch(spec, bank, (s + 1) % L, bufs[(s + 1) % 2], side.cuda_stream)
-        copy_done[(s + 1) % 2].record(side)
-        compute(s, bufs[s % 2], ev)
+
+        def start_copy():
+            route_done.record(main)
+            side.wait_event(route_done)
+            side.wait_event(comp_done[(s + 1) % 2])
+            m.moe_layer_prefetch(spec, bank, (s + 1) % L, bufs[(s + 1) % 2], side.cuda_stream)
+            copy_done[(s + 1) % 2].record(side)
+
+        compute(s, bufs[s % 2], ev, start_copy)
         comp_done[s % 2].record(main)
 
     def step_serial(s, ev=None):
