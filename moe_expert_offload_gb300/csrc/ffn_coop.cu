@@ -688,6 +688,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     CtlSh& cs = *reinterpret_cast<CtlSh*>(ring);
     SelScratch& ss = *reinterpret_cast<SelScratch*>(ring + sizeof(CtlSh));
     griddep_wait();  // x, the cache tables and the pool of the previous kernels
+    // the next kernel may be scheduled now: its CTAs start on SMs this grid
+    // frees and wait for its completion before reading anything
+    griddep_launch();
     if (wid < kCW) {
       const int E = a.E, np = T * E;
       if (ctl_cta) {
@@ -750,6 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     griddep_wait();  // the plan (and the cleared counters) of the previous kernels
+    griddep_launch();
     n_uniq = a.counts[0];
     n_exec = n_uniq + a.has_shared;
     for (int i = tid; i < n_ids; i += kThreads) {
@@ -1320,7 +1324,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (s_last)
       for (int i = tid; i < kSyncCtr + 4 + 8 * kMaxEnt; i += kThreads) lf.sync[i] = 0u;
   }
-  griddep_launch();
 }
 
 static_assert(kSyncCtr + 4 + 8 * kMaxEnt <= MOE_CACHE_SYNC_WORDS, "sync words");
