@@ -66,6 +66,10 @@ def lib():
                                     vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.or_cache_place.restype = i32
         L.or_cache_place.argtypes = [i32, i32, i32, i32, vp, i32, vp, vp, vp, vp]
+        L.or_slots_for_budget.restype = i64
+        L.or_slots_for_budget.argtypes = [i64, i64]
+        L.or_cache_resize.restype = i32
+        L.or_cache_resize.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
         L.or_expert_forward.argtypes = [vp, i32, i32, vp, i32, vp]
         f64 = C.c_double
         for name in ("or_e2m1", "or_e4m3", "or_e8m0"):
@@ -228,6 +232,39 @@ def cache_step(state: CacheState, E: int, layer: int, ids: np.ndarray, K: int, b
         "n_uniq": n_uniq, "n_hit": n_hit, "n_miss": n_miss, "q": q, "n_fill": n_fill,
         "n_direct": n_direct, "n_victims": n_vict, "now": now,
     }
+
+
+def slots_for_budget(free_bytes: int, slot_bytes: int) -> int:
+    """floor(free_bytes / slot_bytes): the slots a memory budget holds."""
+    n = int(lib().or_slots_for_budget(int(free_bytes), int(slot_bytes)))
+    if n < 0:
+        raise ValueError("slots_for_budget: bad sizes")
+    return n
+
+
+def cache_resize(state: CacheState, S_new: int) -> dict:
+    """Re-divide the slot pool of `state` into S_new slots (in place: the slot
+    arrays are replaced by arrays of S_new entries).  Returns the evicted ids,
+    the (from, to) blob moves and the counts."""
+    S = state.id_of_slot.size
+    cap = max(S, S_new)
+    ios = np.full(cap, -1, dtype=np.int32)
+    ios[:S] = state.id_of_slot
+    ts = np.zeros(cap, dtype=np.uint32)
+    ts[:S] = state.ts
+    ev = np.full(cap, -1, dtype=np.int32)
+    mf = np.full(cap, -1, dtype=np.int32)
+    mt = np.full(cap, -1, dtype=np.int32)
+    counts = np.zeros(3, dtype=np.int32)
+    rc = lib().or_cache_resize(state.slot_of_id.size, S, S_new, _vp(state.slot_of_id), _vp(ios),
+                               _vp(ts), _vp(ev), _vp(mf), _vp(mt), _vp(counts))
+    if rc:
+        raise ValueError("cache_resize: bad sizes or tables")
+    n_ev, n_mv, n_occ = (int(v) for v in counts)
+    state.id_of_slot = ios[:S_new].copy()
+    state.ts = ts[:S_new].copy()
+    return {"evicted_ids": ev[:n_ev].copy(), "move_from": mf[:n_mv].copy(),
+            "move_to": mt[:n_mv].copy(), "n_evicted": n_ev, "n_moved": n_mv, "n_occupied": n_occ}
 
 
 def expert_forward(blob: np.ndarray, H: int, I: int, x_bits: np.ndarray) -> np.ndarray:

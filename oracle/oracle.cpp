@@ -474,6 +474,82 @@ int or_cache_place(int E, int L, int S, int policy, const int32_t* ids, int n,
   return 0;
 }
 
+// ------------------------------------------------------ elastic slot pool
+// Slots a memory budget holds (reader "Elastic Memory Management": 10 slots
+// of 0.5 GB in 5 GB, 8 in 4 GB, 12 in 6 GB): floor(free_bytes / slot_bytes).
+// Returns -1 for slot_bytes <= 0 or free_bytes < 0.
+int64_t or_slots_for_budget(int64_t free_bytes, int64_t slot_bytes) {
+  if (slot_bytes <= 0 || free_bytes < 0) return -1;
+  return free_bytes / slot_bytes;
+}
+
+// Re-division of the shared slot pool from S to S_new slots at a safe point
+// between steps (reader "Elastic Memory Management": the excess slots are
+// evicted on a shrink, freed memory becomes new slots on a growth, and the
+// bank and the routing never change).  Readings where the page is silent:
+//   * which experts go on a shrink: the occupied slots past S_new can only
+//     stay if the most useful experts are kept, so the cache's own recency
+//     decides: the n_occ - S_new occupied slots with the smallest keys
+//     (ts, slot) -- the order of the victim scan -- are evicted;
+//   * where the kept experts past S_new go: in ascending slot order, to the
+//     free slots below S_new in ascending order, with their ts (their blob
+//     is copied there);
+//   * slots [S_new, S) are emptied (id -1, ts 0), and on a growth the new
+//     slots [S, S_new) start empty; the clock does not move.
+// Writes evicted ids in (ts, slot) order, the moves as (from, to) pairs and
+// counts = {n_evicted, n_moved, n_occupied after}.  Returns 0, or -1 for
+// S < 1, S_new < 1, or a table that is not a bijection.
+int or_cache_resize(int n_ids, int S, int S_new, int32_t* slot_of_id, int32_t* id_of_slot,
+                    uint32_t* ts, int32_t* evicted_ids, int32_t* move_from, int32_t* move_to,
+                    int32_t* counts) {
+  if (S < 1 || S_new < 1 || n_ids < 0) return -1;
+  for (int v = 0; v < S; ++v) {
+    const int32_t u = id_of_slot[v];
+    if (u >= n_ids || (u >= 0 && slot_of_id[u] != v)) return -1;
+  }
+  // 1. evict the oldest occupied slots until at most S_new remain
+  std::vector<std::pair<uint32_t, int32_t>> occ;
+  for (int v = 0; v < S; ++v)
+    if (id_of_slot[v] >= 0) occ.push_back({ts[v], v});
+  std::sort(occ.begin(), occ.end());
+  const int n_ev = std::max(0, (int)occ.size() - S_new);
+  for (int i = 0; i < n_ev; ++i) {
+    const int32_t v = occ[i].second;
+    evicted_ids[i] = id_of_slot[v];
+    slot_of_id[id_of_slot[v]] = -1;
+    id_of_slot[v] = -1;
+    ts[v] = 0;
+  }
+  // 2. the kept experts past S_new move to the free slots below it
+  std::vector<int32_t> from, to;
+  for (int v = S_new; v < S; ++v)
+    if (id_of_slot[v] >= 0) from.push_back(v);
+  for (int v = 0; v < S_new && v < S && to.size() < from.size(); ++v)
+    if (id_of_slot[v] < 0) to.push_back(v);
+  if (to.size() != from.size()) return -1;  // cannot happen: at most S_new kept
+  for (size_t i = 0; i < from.size(); ++i) {
+    const int32_t a = from[i], b = to[i], u = id_of_slot[a];
+    id_of_slot[b] = u;
+    ts[b] = ts[a];
+    slot_of_id[u] = b;
+    id_of_slot[a] = -1;
+    ts[a] = 0;
+    move_from[i] = a;
+    move_to[i] = b;
+  }
+  // 3. slots past both sizes' common part start (or are left) empty
+  for (int v = std::min(S, S_new); v < std::max(S, S_new); ++v) {
+    id_of_slot[v] = -1;
+    ts[v] = 0;
+  }
+  int n_occ = 0;
+  for (int v = 0; v < S_new; ++v) n_occ += id_of_slot[v] >= 0 ? 1 : 0;
+  counts[0] = n_ev;
+  counts[1] = (int32_t)from.size();
+  counts[2] = n_occ;
+  return 0;
+}
+
 // -------------------------------------------------------------- expert FFN
 }  // extern "C"
 
