@@ -16,6 +16,10 @@
  *                      or warm start); moe_cache.policy picks the shared LRU,
  *                      a per-layer LRU or static placement (the replacement
  *                      policies the pages compare)
+ *   moe_cache_resize   elastic re-division of the slot pool at a safe point
+ *                      between steps; moe_slots_for_budget gives the slot
+ *                      count of a memory budget (FreeToken reader "Elastic
+ *                      Memory Management")
  *   moe_expert_ffn     int4 affine group-64 SwiGLU experts down(silu(gate(x)) *
  *                      up(x)) over G = H u F (H from the slot pool; F, the
  *                      experts filled in this step, from their bank bytes,
@@ -230,6 +234,50 @@ int moe_cache_reset(const moe_spec* spec, moe_cache* cache, moe_stream_t stream)
  * ------------------------------------------------------------------------ */
 int moe_cache_place(const moe_spec* spec, moe_cache* cache, const int32_t* ids, int32_t n,
                     moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * moe_slots_for_budget -- slots of moe_expert_bytes(spec) that `free_bytes`
+ * of device memory hold: floor(free_bytes / S_e) (FreeToken reader "Elastic
+ * Memory Management": 10 slots of 0.5 GB in 5 GB, 8 in 4 GB, 12 in 6 GB).
+ * Returns -1 for an invalid spec or free_bytes < 0.
+ * ------------------------------------------------------------------------ */
+int64_t moe_slots_for_budget(const moe_spec* spec, int64_t free_bytes);
+
+/* Scratch bytes moe_cache_resize needs to go from cache->num_slots to
+ * new_slots slots: 4 * (8 + 3 * max(S, new_slots)).  0 for a NULL cache or
+ * new_slots < 1. */
+size_t moe_cache_resize_workspace_bytes(const moe_cache* cache, int32_t new_slots);
+
+/* ------------------------------------------------------------------------
+ * moe_cache_resize -- re-divide the shared slot pool from S = cache->num_slots
+ * to new_slots slots at a safe point between steps (FreeToken reader "Elastic
+ * Memory Management": the excess slots are evicted when the budget shrinks,
+ * new slots appear when it grows; the bank and the routing never change, so
+ * every later output is what it would have been with the same resident set).
+ *   Shrink: while more than new_slots slots are occupied, the occupied slot
+ *     with the smallest key (ts, slot) is evicted (the order of the victim
+ *     scan: the least recently routed expert goes first); then the kept
+ *     experts in slots >= new_slots move, blob and ts, to the free slots below
+ *     new_slots, both taken in ascending slot order.
+ *   Growth: slots [S, new_slots) start empty (id -1, ts 0); nothing moves.
+ *   Slots from min(S, new_slots) to max(S, new_slots) are left empty, and the
+ *   clock does not move.
+ * The caller guarantees that id_of_slot, ts and (if set) slot_pool hold
+ * max(S, new_slots) entries.  Policy MOE_POLICY_SHARED_LRU only
+ * (MOE_EUNSUPPORTED otherwise).  On success cache->num_slots = new_slots.
+ *   workspace  device, 4-byte aligned, >= moe_cache_resize_workspace_bytes:
+ *              int32 [0] evicted count, [1] moved count, [2] occupied slots
+ *              after, [3] MOE_DERR_RANGE if the tables were not a bijection
+ *              (then the tables are unchanged while cache->num_slots is
+ *              new_slots: moe_cache_reset or moe_cache_place the cache before
+ *              its next step); from word 8: the move sources, the move
+ *              destinations and the evicted ids (ascending slot order),
+ *              max(S, new_slots) words each.
+ * No step of this cache may run concurrently (a safe point); asynchronous on
+ * `stream`, two kernels (one for a growth or a cache without a pool).
+ * ------------------------------------------------------------------------ */
+int moe_cache_resize(const moe_spec* spec, moe_cache* cache, int32_t new_slots, void* workspace,
+                     size_t workspace_bytes, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * moe_cache_step -- one decode control step for layer `layer` (one CTA),

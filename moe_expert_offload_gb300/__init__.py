@@ -34,6 +34,7 @@ EXPORTED = (
     "moe_cache_step", "moe_ffn_workspace_bytes", "moe_expert_ffn", "moe_layer_workspace_bytes",
     "moe_layer_forward", "moe_expert_ffn_noalloc", "moe_prefill_workspace_bytes",
     "moe_layer_prefetch", "moe_expert_ffn_prefill", "moe_layer_forward_prefill",
+    "moe_slots_for_budget", "moe_cache_resize_workspace_bytes", "moe_cache_resize",
 )
 MOE_NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -112,6 +113,12 @@ def lib():
         L.moe_layer_kernel_count.argtypes = [sp, cp, i32]
         L.moe_cache_place.restype = C.c_int
         L.moe_cache_place.argtypes = [sp, cp, vp, i32, vp]
+        L.moe_slots_for_budget.restype = C.c_int64
+        L.moe_slots_for_budget.argtypes = [sp, C.c_int64]
+        L.moe_cache_resize_workspace_bytes.restype = sz
+        L.moe_cache_resize_workspace_bytes.argtypes = [cp, i32]
+        L.moe_cache_resize.restype = C.c_int
+        L.moe_cache_resize.argtypes = [sp, cp, i32, vp, sz, vp]
         L.moe_cache_step.restype = C.c_int
         L.moe_cache_step.argtypes = [sp, cp, i32, vp, i32, pp, i32, vp]
         L.moe_ffn_workspace_bytes.restype = sz
@@ -209,6 +216,23 @@ def moe_cache_place(spec, cache, ids, stream=None):
                                         _stream(stream)))
 
 
+def moe_slots_for_budget(spec, free_bytes) -> int:
+    n = int(lib().moe_slots_for_budget(C.byref(spec), int(free_bytes)))
+    if n < 0:
+        raise MoeError(MOE_EINVAL, moe_last_error())
+    return n
+
+
+def moe_cache_resize_workspace_bytes(cache, new_slots) -> int:
+    return int(lib().moe_cache_resize_workspace_bytes(C.byref(cache), new_slots))
+
+
+def moe_cache_resize(spec, cache, new_slots, workspace, workspace_bytes, stream=None):
+    """Re-divide the slot pool into new_slots slots (cache.num_slots follows)."""
+    return _check(lib().moe_cache_resize(C.byref(spec), C.byref(cache), new_slots,
+                                         _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
 def moe_cache_step(spec, cache, layer, ids, T, plan, do_fill=1, stream=None):
     return _check(lib().moe_cache_step(C.byref(spec), C.byref(cache), layer, _ptr(ids), T,
                                        C.byref(plan), do_fill, _stream(stream)))
@@ -300,16 +324,19 @@ class DeviceCache:
     """Slot tables and slot pool in device memory (torch tensors) + the C struct."""
 
     def __init__(self, spec: MoeSpec, num_slots, k_victims, bp_mbps, bh_mbps, bank, device="cuda",
-                 with_pool=True, policy=POLICY_SHARED_LRU, sync=True):
+                 with_pool=True, policy=POLICY_SHARED_LRU, sync=True, capacity=None):
         import torch
 
+        # capacity: slots the tables and the pool are allocated for (room for
+        # moe_cache_resize to grow into); num_slots of them are in use
+        cap = max(num_slots, capacity or 0)
         n_ids = spec.num_layers * spec.num_experts
         se = moe_expert_bytes(spec)
         self.slot_of_id = torch.full((n_ids,), -1, dtype=torch.int32, device=device)
-        self.id_of_slot = torch.full((num_slots,), -1, dtype=torch.int32, device=device)
-        self.ts = torch.zeros(num_slots, dtype=torch.int32, device=device)
+        self.id_of_slot = torch.full((cap,), -1, dtype=torch.int32, device=device)
+        self.ts = torch.zeros(cap, dtype=torch.int32, device=device)
         self.clock = torch.zeros(1, dtype=torch.int32, device=device)
-        self.pool = (torch.empty((num_slots, se), dtype=torch.uint8, device=device)
+        self.pool = (torch.empty((cap, se), dtype=torch.uint8, device=device)
                      if with_pool else None)
         self.bank = bank
         # sync words of the one-kernel decode layer step (None: the multi-kernel form)
@@ -320,10 +347,12 @@ class DeviceCache:
                           _ptr(self.pool), _ptr(bank), policy, _ptr(self.sync))
 
     def host_tables(self):
+        """slot_of_id, id_of_slot, ts, clock (the slots in use only)."""
         import numpy as np
 
-        return (self.slot_of_id.cpu().numpy().copy(), self.id_of_slot.cpu().numpy().copy(),
-                self.ts.cpu().numpy().view(np.uint32).copy(),
+        S = self.c.num_slots
+        return (self.slot_of_id.cpu().numpy().copy(), self.id_of_slot[:S].cpu().numpy().copy(),
+                self.ts[:S].cpu().numpy().view(np.uint32).copy(),
                 self.clock.cpu().numpy().view(np.uint32).copy())
 
 

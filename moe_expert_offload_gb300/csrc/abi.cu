@@ -366,6 +366,48 @@ int moe_cache_place(const moe_spec* spec, moe_cache* cache, const int32_t* ids, 
   return ok();
 }
 
+int64_t moe_slots_for_budget(const moe_spec* spec, int64_t free_bytes) {
+  if (check_spec(spec) != MOE_OK) return -1;
+  if (free_bytes < 0) {
+    fail(MOE_EINVAL, "moe_slots_for_budget: free_bytes < 0");
+    return -1;
+  }
+  ok();
+  return free_bytes / moe::expert_blob_bytes(spec->hidden, spec->inter, spec->format);
+}
+
+size_t moe_cache_resize_workspace_bytes(const moe_cache* cache, int32_t new_slots) {
+  if (!cache || cache->num_slots < 1 || new_slots < 1) return 0;
+  return moe::resize_workspace_bytes(cache->num_slots, new_slots);
+}
+
+int moe_cache_resize(const moe_spec* spec, moe_cache* cache, int32_t new_slots, void* workspace,
+                     size_t workspace_bytes, moe_stream_t stream) {
+  int rc = check_spec(spec);
+  if (rc) return rc;
+  rc = check_cache(spec, cache, false);
+  if (rc) return rc;
+  if (cache->policy != MOE_POLICY_SHARED_LRU)
+    return fail(MOE_EUNSUPPORTED, "moe_cache_resize: the shared LRU policy only");
+  if (new_slots < 1) return fail(MOE_EINVAL, "moe_cache_resize: new_slots must be >= 1");
+  if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 4)
+    return fail(MOE_EINVAL, "moe_cache_resize: workspace NULL or not 4-byte aligned");
+  const size_t need = moe::resize_workspace_bytes(cache->num_slots, new_slots);
+  if (workspace_bytes < need)
+    return fail(MOE_ECAPACITY, "moe_cache_resize: workspace %zu < %zu bytes", workspace_bytes,
+                need);
+  if (cache->slot_pool && reinterpret_cast<uintptr_t>(cache->slot_pool) % 16)
+    return fail(MOE_EINVAL, "moe_cache_resize: slot_pool must be 16-byte aligned");
+  const cudaError_t e = moe::launch_cache_resize(
+      cache->slot_of_id, spec->num_layers * spec->num_experts, cache->id_of_slot, cache->ts,
+      cache->num_slots, new_slots, static_cast<uint8_t*>(cache->slot_pool),
+      moe::expert_blob_bytes(spec->hidden, spec->inter, spec->format),
+      static_cast<int32_t*>(workspace), (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cache resize launch");
+  cache->num_slots = new_slots;
+  return ok();
+}
+
 int moe_cache_step(const moe_spec* spec, moe_cache* cache, int32_t layer, const int32_t* ids,
                    int32_t T, moe_plan* plan, int32_t do_fill, moe_stream_t stream) {
   int rc = check_spec(spec);

@@ -173,6 +173,11 @@ cudaError_t launch_cache_reset(int32_t* slot_of_id, int n_ids, int32_t* id_of_sl
                                int S, uint32_t* clock, uint32_t* sync, cudaStream_t st);
 cudaError_t launch_fill_copy(const moe_plan& plan, int K, const uint8_t* bank, uint8_t* pool,
                              int64_t blob_bytes, cudaStream_t st);
+// Elastic re-division of the shared slot pool from S to S_new slots (resize.cu).
+size_t resize_workspace_bytes(int S, int S_new);
+cudaError_t launch_cache_resize(int32_t* slot_of_id, int n_ids, int32_t* id_of_slot, uint32_t* ts,
+                                int S, int S_new, uint8_t* pool, int64_t blob_bytes, int32_t* ws,
+                                cudaStream_t st);
 
 struct FfnArgs {
   // every member has a zero default, so a caller that fills in only some

@@ -172,6 +172,46 @@ def test_cache_place_argument_checks(L):
     assert e.value.code == m.MOE_EINVAL
 
 
+def test_slots_for_budget_and_resize_workspace(L):
+    """floor(free / S_e) with the library's own blob size (the oracle's
+    restatement is pinned to the reader's 10 / 8 / 12 example)."""
+    import oracle
+
+    oracle.build()
+    for kw in (dict(), dict(hidden=2048, inter=512, num_experts=256, top_k=8),
+               dict(hidden=1024, inter=512, fmt=m.FORMAT_NVFP4)):
+        sp = _spec(**kw)
+        se = m.moe_expert_bytes(sp)
+        for free in (0, se - 1, se, 5 << 30, 4 << 30, 6 << 30):
+            assert m.moe_slots_for_budget(sp, free) == oracle.slots_for_budget(free, se)
+    with pytest.raises(m.MoeError):
+        m.moe_slots_for_budget(_spec(), -1)
+    with pytest.raises(m.MoeError):
+        m.moe_slots_for_budget(_spec(num_layers=0), 1 << 20)
+    c = _cache(num_slots=10)
+    assert m.moe_cache_resize_workspace_bytes(c, 8) == 4 * (8 + 3 * 10)
+    assert m.moe_cache_resize_workspace_bytes(c, 12) == 4 * (8 + 3 * 12)
+    assert m.moe_cache_resize_workspace_bytes(c, 0) == 0
+
+
+def test_cache_resize_argument_checks(L):
+    sp = _spec()
+    need = m.moe_cache_resize_workspace_bytes(_cache(), 4)
+    cases = [(_cache(policy=m.POLICY_LAYER_LRU), 4, 4096, need, m.MOE_EUNSUPPORTED),
+             (_cache(policy=m.POLICY_STATIC), 4, 4096, need, m.MOE_EUNSUPPORTED),
+             (_cache(), 0, 4096, need, m.MOE_EINVAL),
+             (_cache(), 4, None, need, m.MOE_EINVAL),
+             (_cache(), 4, 4098, need, m.MOE_EINVAL),
+             (_cache(), 4, 4096, need - 1, m.MOE_ECAPACITY),
+             (_cache(slot_pool=4100), 4, 4096, need, m.MOE_EINVAL),
+             (_cache(num_slots=0), 4, 4096, need, m.MOE_EINVAL)]
+    for c, n, ws, wsb, code in cases:
+        with pytest.raises(m.MoeError) as e:
+            m.moe_cache_resize(sp, c, n, ws, wsb, stream=0)
+        assert e.value.code == code
+        assert c.num_slots in (0, 8)  # unchanged on failure
+
+
 def test_ffn_argument_checks(L):
     s = _spec(has_shared=True)
     need = m.moe_ffn_workspace_bytes(s, 1)
