@@ -70,6 +70,15 @@ WORKLOADS = {
              "affine g64 dequantised to bf16 into tcgen05 grouped GEMMs; 2 layers alternating, "
              "the next layer copied bank -> buffer on a second stream (double buffer)",
         L=2, H=2048, I=512, E=256, k=8, T=8192, shared=True, router="softmax", prefill=True),
+    "elastic_resize": dict(
+        desc="Elastic slot pool on the qwen_decode shape and inputs (40 layers, H=2048, I=512, "
+             "E=256, top-8 + shared, int4 g64, K=8, B_P/B_H=52.7/77.3 GB/s): each step fills "
+             "the 2560-slot pool with a random resident set and runs one decode step through "
+             "all layers (both untimed), then the pool shrinks to 2048 slots (the KV cache takes "
+             "0.9 GB: the 512 least recently routed experts are evicted, the kept ones past slot "
+             "2048 move down) and grows back to 2560; the two re-divisions are timed",
+        L=40, H=2048, I=512, E=256, k=8, T=1, shared=True, router="softmax", slots=2560, K=8,
+        bp=52700, bh=77300, elastic=True, slots_lo=2048),
     "cache_sweep": dict(
         desc="Cache stress sweep: 40 layers x 256 experts, top-8, Zipf(1.1) routing traces of "
              "2048 steps per layer with 70% step-to-step overlap fed straight to the control "
@@ -405,6 +414,32 @@ def run_reference_sweep(args, w, world):
           flush=True)
 
 
+def run_reference_elastic(args, w, world):
+    """Each step is the oracle's shrink and growth of a full pool of the workload's
+    size (tables only: the oracle has no slot pool), on tables of random recency."""
+    import oracle
+
+    oracle.build()
+    n_ids = w["L"] * w["E"]
+    rng = np.random.default_rng(11)
+    spent = 0.0
+    for s in range(args.warmup + args.steps):
+        if s == args.warmup:
+            spent = 0.0
+        st = oracle.CacheState(n_ids, w["slots"])
+        oracle.cache_place(st, w["E"], w["L"], rng.choice(n_ids, w["slots"], replace=False))
+        st.ts[:] = rng.integers(1, 1000, w["slots"])
+        t0 = time.perf_counter()
+        oracle.cache_resize(st, w["slots_lo"])
+        oracle.cache_resize(st, w["slots"])
+        spent += time.perf_counter() - t0
+    val = 2 * args.steps / spent
+    sample = (f"{args.steps} shrink + growth pairs of a full {w['slots']}-slot pool, single "
+              f"thread, {spent:.3f} s of oracle time")
+    print(json.dumps(reference_line(args, w, world, val, "re-divisions/s", spent, sample,
+                                    "int32")), flush=True)
+
+
 def run_reference(args, w, rank, world):
     if rank != 0:
         return
@@ -412,6 +447,8 @@ def run_reference(args, w, rank, world):
         return run_reference_prefill(args, w, world)
     if w.get("sweep"):
         return run_reference_sweep(args, w, world)
+    if w.get("elastic"):
+        return run_reference_elastic(args, w, world)
     import oracle
 
     n = args.warmup + args.steps
@@ -950,6 +987,164 @@ def sweep_points(w):
             for cap in w["caps"] for bp, bh in w["ratios"]]
 
 
+def run_elastic(args, w, rank, world, local_rank):
+    """Re-divisions of the slot pool between decode steps (moe_cache_resize), each
+    bracketed by CUDA events; the decode steps between them are not timed.  The
+    first shrink's tables are checked against the oracle's re-division of the same
+    tables (the oracle's own time on them is the CPU baseline)."""
+    import torch
+
+    import moe_expert_offload_gb300 as m
+    from moe_expert_offload_gb300 import _build
+
+    _build.build()
+    m.lib()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    L, H, E, k, T = w["L"], w["H"], w["E"], w["k"], w["T"]
+    S_hi, S_lo = w["slots"], w["slots_lo"]
+    spec = spec_of(w)
+    se = m.moe_expert_bytes(spec)
+    n_in = args.warmup + args.steps
+    xs_h, wr_h, _ = make_inputs(w, n_in)
+    bank = make_bank(w, L * E + 1, 7, dev)
+    cache = m.DeviceCache(spec, S_hi, w["K"], w["bp"], w["bh"], bank[:L * E], device=dev)
+    plan = m.DevicePlan(T * k, w["K"], device=dev)
+    xs = torch.from_numpy(xs_h.view(np.int16)).to(dev)
+    wr = torch.from_numpy(wr_h.view(np.int16)).to(dev)
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    wts = torch.empty((T, k), dtype=torch.float32, device=dev)
+    y = torch.empty((T, H), dtype=torch.float32, device=dev)
+    lws = m.moe_layer_workspace_bytes(spec, T)
+    lw = torch.empty(lws, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    rwb = m.moe_cache_resize_workspace_bytes(cache.c, S_lo)
+    rws = torch.zeros((n_in, 2, rwb // 4), dtype=torch.int32, device=dev)
+    rng = np.random.default_rng(3)
+
+    def fill_pool():
+        # a full pool: a random resident set (ts 0); the decode step after it stamps
+        # the experts it routes (synchronises the stream)
+        m.moe_cache_place(spec, cache.c, rng.choice(L * E, S_hi, replace=False).astype(np.int32),
+                          sp)
+
+    def decode_step(s):
+        for l in range(L):
+            m.moe_layer_forward(spec, cache.c, l, xs[s, l], T, wr[l], None, bank[L * E], plan.c,
+                                ids, wts, lw, lws, y, sp)
+
+    def redivide(s, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        m.moe_cache_resize(spec, cache.c, S_lo, rws[s, 0], rwb, sp)
+        if ev is not None:
+            ev[1].record(stream)
+        m.moe_cache_resize(spec, cache.c, S_hi, rws[s, 1], rwb, sp)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for s in range(args.warmup):
+        fill_pool()
+        decode_step(s)
+        redivide(s)
+    torch.cuda.synchronize()
+    # parity of one shrink against the oracle, on the tables as they stand
+    import oracle
+
+    oracle.build()
+    fill_pool()
+    decode_step(args.warmup)
+    torch.cuda.synchronize()
+    soi, ios, ts, clk = cache.host_tables()
+    ost = oracle.CacheState(L * E, S_hi)
+    ost.slot_of_id[:], ost.id_of_slot[:], ost.ts[:], ost.clock[:] = soi, ios, ts, clk
+    t0 = time.perf_counter()
+    want = oracle.cache_resize(ost, S_lo)
+    cpu_s = time.perf_counter() - t0
+    m.moe_cache_resize(spec, cache.c, S_lo, rws[0, 0], rwb, sp)
+    torch.cuda.synchronize()
+    got = cache.host_tables()
+    if not (np.array_equal(got[0], ost.slot_of_id) and np.array_equal(got[1], ost.id_of_slot)
+            and np.array_equal(got[2], ost.ts) and int(rws[0, 0, 1]) == want["n_moved"]):
+        raise RuntimeError("elastic re-division differs from the oracle's")
+    m.moe_cache_resize(spec, cache.c, S_hi, rws[0, 1], rwb, sp)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    rank_barrier(world)
+    with ClockSampler(local_rank) as clk:
+        for j in range(args.steps):
+            s = args.warmup + j
+            fill_pool()
+            decode_step(s)
+            redivide(s, evs[j])
+        torch.cuda.synchronize()
+    rank_barrier(world)
+    shrink_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    grow_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    res_ms = max_over_ranks(sum(shrink_ms) + sum(grow_ms), world, dev)
+    r = rws[args.warmup:].cpu().numpy()
+    if np.any(r[:, :, 3] != 0):
+        raise RuntimeError("re-division reported inconsistent tables")
+    moved = r[:, 0, 1].astype(np.int64)
+    evicted = r[:, 0, 0].astype(np.int64)
+
+    # end to end through the public API: each re-division's counts read back to
+    # pinned host memory inside the timed region
+    cnt_host = torch.empty((args.steps, 2, 4), dtype=torch.int32).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    tot = 0.0
+    for j in range(args.steps):
+        fill_pool()
+        decode_step(args.warmup + j)
+        e0.record(stream)
+        m.moe_cache_resize(spec, cache.c, S_lo, rws[j, 0], rwb, sp)
+        cnt_host[j, 0].copy_(rws[j, 0, :4], non_blocking=True)
+        m.moe_cache_resize(spec, cache.c, S_hi, rws[j, 1], rwb, sp)
+        cnt_host[j, 1].copy_(rws[j, 1, :4], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        tot += e0.elapsed_time(e1)
+    ms_e2e = max_over_ranks(tot, world, dev)
+    if rank != 0:
+        return
+    hbm, _, peak_kind = peaks()
+    mv_bytes = 2.0 * float(moved.sum()) * se  # each moved blob read once and written once
+    t_shrink = sum(shrink_ms) * 1e-3
+    out = {
+        "metric": METRIC, "value": 2 * args.steps * world / (res_ms * 1e-3),
+        "unit": "re-divisions/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": res_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": run_config(args, w, world),
+        "roofline": {"bound": "hbm", "achieved": mv_bytes / t_shrink / 1e9, "peak": hbm,
+                     "unit": "GB/s", "frac": mv_bytes / t_shrink / 1e9 / hbm, "traffic": None,
+                     "kernel": "shrink (moe_cache_resize: one-CTA plan kernel + blob move "
+                               "kernel), moved blob bytes read + written per shrink",
+                     "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": mv_bytes / args.steps,
+                     "avg_launch_us": 1e6 * t_shrink / args.steps},
+        "elastic": {"slots": [S_hi, S_lo], "mean_evicted": float(evicted.mean()),
+                    "mean_moved": float(moved.mean()),
+                    "shrink_us": 1e3 * statistics.mean(shrink_ms),
+                    "grow_us": 1e3 * statistics.mean(grow_ms),
+                    "timing": "CUDA events around each moe_cache_resize call; decode steps "
+                              "between them untimed"},
+        "e2e": {"value": 2 * args.steps * world / (ms_e2e * 1e-3), "unit": "re-divisions/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 2 * 16},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if world == 1 and not args.no_cpu:
+        out["cpu_baseline"] = {
+            "value": 1.0 / cpu_s, "unit": "re-divisions/s", "cores": 1, "kind": "oracle",
+            "sample": f"one shrink {S_hi} -> {S_lo} of the GPU's own tables after a fill and "
+                      f"a decode step (tables only; the oracle has no slot pool), single thread, "
+                      f"{cpu_s * 1e3:.2f} ms", "host_cores": host_cores()}
+    print(json.dumps(out), flush=True)
+
+
 def run_sweep(args, w, rank, world, local_rank):
     """Config 5: every (capacity, B_P/B_H) point runs the 2048-step x 40-layer trace
     through moe_cache_step from a reset cache; one CUDA graph per 64 trace steps.
@@ -1184,6 +1379,8 @@ def main():
         run_prefill(args, w, rank, world, local_rank)
     elif w.get("sweep"):
         run_sweep(args, w, rank, world, local_rank)
+    elif w.get("elastic"):
+        run_elastic(args, w, rank, world, local_rank)
     else:
         run_gpu(args, w, rank, world, local_rank)
     if world > 1:
