@@ -79,6 +79,11 @@ WORKLOADS = {
              "2048 move down) and grows back to 2560; the two re-divisions are timed",
         L=40, H=2048, I=512, E=256, k=8, T=1, shared=True, router="softmax", slots=2560, K=8,
         bp=52700, bh=77300, elastic=True, slots_lo=2048),
+    "qwen_prefill_nvfp4": dict(
+        desc="qwen_prefill with NVFP4 experts (E2M1 elements, one E4M3 scale per 16, fp32 "
+             "matrix scales; dequantised exactly to bf16 inside the tcgen05 grouped GEMMs)",
+        L=2, H=2048, I=512, E=256, k=8, T=8192, shared=True, router="softmax", prefill=True,
+        fmt=2),
     "cache_sweep": dict(
         desc="Cache stress sweep: 40 layers x 256 experts, top-8, Zipf(1.1) routing traces of "
              "2048 steps per layer with 70% step-to-step overlap fed straight to the control "
@@ -734,7 +739,7 @@ def run_prefill(args, w, rank, world, local_rank):
     L, H, I, E, k, T = w["L"], w["H"], w["I"], w["E"], w["k"], w["T"]
     spec = spec_of(w)
     se = m.moe_expert_bytes(spec)
-    bank = synth.make_bank_torch(L * E + 1, H, I, 7, dev)
+    bank = make_bank(w, L * E + 1, 7, dev)
     shared = bank[L * E]
     bufs = [torch.empty((E, se), dtype=torch.uint8, device=dev) for _ in range(2)]
     wr_h = [synth.router_weights(100 + l, E, H) for l in range(L)]
@@ -922,9 +927,15 @@ class PrefillOracle:
         oracle.build()
         self.o, self.synth, self.w, self.x, self.wr = oracle, synth, w, x_h[0], wr_h[0]
         self.blobs = {}
-        self.shared = synth.make_expert_bytes(np.random.default_rng(12345), w["H"], w["I"])
+        self.fp4 = w.get("fmt", 0) - 1  # the oracle's FP4 format, or -1 for int4
+        self.shared = self.make(np.random.default_rng(12345))
         self.flops_per_token = 6.0 * w["H"] * w["I"] * (w["k"] + 1)
         self.spent, self.n = 0.0, 0
+
+    def make(self, rng):
+        if self.fp4 >= 0:
+            return self.synth.make_fp4_expert(rng, self.w["H"], self.w["I"], self.fp4)
+        return self.synth.make_expert_bytes(rng, self.w["H"], self.w["I"])
 
     def token(self, t):
         o, w = self.o, self.w
@@ -934,13 +945,21 @@ class PrefillOracle:
         self.spent += time.perf_counter() - t0
         for e in ids.reshape(-1):
             if int(e) not in self.blobs:
-                self.blobs[int(e)] = self.synth.make_expert_bytes(np.random.default_rng(int(e) + 1),
-                                                                  w["H"], w["I"])
-        anyb = self.blobs[int(ids[0, 0])]
-        full = [self.blobs.get(e, anyb) for e in range(w["E"])]
-        t0 = time.perf_counter()
-        o.moe_ffn(full, w["H"], w["I"], xb, ids, wt, self.shared, w["I"])
-        self.spent += time.perf_counter() - t0
+                self.blobs[int(e)] = self.make(np.random.default_rng(int(e) + 1))
+        if self.fp4 >= 0:
+            # the oracle's FP4 expert per routed expert, weighted sum in float64
+            t0 = time.perf_counter()
+            y = o.fp4_expert_forward(self.shared, w["H"], w["I"], self.fp4, xb)
+            for j in range(ids.shape[1]):
+                y += float(wt[0, j]) * o.fp4_expert_forward(self.blobs[int(ids[0, j])], w["H"],
+                                                            w["I"], self.fp4, xb)
+            self.spent += time.perf_counter() - t0
+        else:
+            anyb = self.blobs[int(ids[0, 0])]
+            full = [self.blobs.get(e, anyb) for e in range(w["E"])]
+            t0 = time.perf_counter()
+            o.moe_ffn(full, w["H"], w["I"], xb, ids, wt, self.shared, w["I"])
+            self.spent += time.perf_counter() - t0
         self.n += 1
 
 
@@ -966,11 +985,15 @@ def cpu_baseline_prefill(w, x_h, wr_h, budget_s=8.0):
                 f"{r.spent:.1f} s, {used} thread(s)")
 
     v1, _, s1 = run(1)
+    out = {"value": v1, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": s1,
+           "host_cores": ncores}
+    if w.get("fmt", 0):
+        # the oracle's FP4 expert is a single-threaded loop: no multi-core variant
+        return out
     vn, used, sn = run(ncores)
-    return {"value": v1, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": s1,
-            "host_cores": ncores,
-            "all_cores": {"value": vn, "unit": "TFLOP/s", "cores": used,
-                          "kind": "oracle, row loops on every host core", "sample": sn}}
+    out["all_cores"] = {"value": vn, "unit": "TFLOP/s", "cores": used,
+                        "kind": "oracle, row loops on every host core", "sample": sn}
+    return out
 
 
 # ------------------------------------------------------------- cache sweep

@@ -95,7 +95,10 @@ enum { MOE_ROUTER_SOFTMAX_TOPK = 0, MOE_ROUTER_SIGMOID_GROUP = 1 };
  * rounded up to 256 bytes.  FP4 experts run in the decode FFN where its
  * one-kernel form serves the shape (hidden % 1024 == 0, inter % 512 == 0,
  * T <= 8); MXFP4 block scales must lie in 2^-32 .. 2^7 (E8M0 bytes 95..134:
- * smaller ones contribute 0, larger ones overflow).  Prefill: int4 only. */
+ * smaller ones contribute 0, larger ones overflow).  Prefill takes all three
+ * formats: FP4 weights are dequantised exactly to bf16 (E2M1 times the block
+ * scale) for the tensor-core GEMMs, with no limit on the MXFP4 scales beyond
+ * bf16's own range. */
 enum { MOE_FORMAT_INT4 = 0, MOE_FORMAT_MXFP4 = 1, MOE_FORMAT_NVFP4 = 2 };
 
 /* Device-side error bits written to plan->err[0] (OR-ed, never cleared by the

@@ -772,7 +772,6 @@ int check_prefill(const moe_spec* s, int32_t T) {
   if (s->hidden % 256 || s->inter % 128)
     return fail(MOE_EUNSUPPORTED, "prefill needs hidden %% 256 == 0 and inter %% 128 == 0");
   if (s->num_experts > 1023) return fail(MOE_EUNSUPPORTED, "prefill supports num_experts <= 1023");
-  if (s->format != MOE_FORMAT_INT4) return fail(MOE_EUNSUPPORTED, "prefill supports int4 experts");
   if ((int64_t)T * (s->top_k + 1) > ((int64_t)1 << 30)) return fail(MOE_EINVAL, "T too large");
   return MOE_OK;
 }
@@ -802,7 +801,8 @@ int do_prefill(const moe_spec* spec, const void* experts, const void* x, int32_t
   a.E = spec->num_experts;
   a.k = spec->top_k;
   a.T = T;
-  a.blob_bytes = moe::blob_offsets(a.H, a.I).total;
+  a.format = spec->format;
+  a.blob_bytes = moe::expert_blob_bytes(a.H, a.I, a.format);
   a.experts = static_cast<const uint8_t*>(experts);
   a.shared = static_cast<const uint8_t*>(shared);
   a.weights = weights;

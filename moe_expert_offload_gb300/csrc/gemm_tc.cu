@@ -38,6 +38,12 @@
 //     every 8) because that is the order one LOP3 yields nibble pairs; A is
 //     stored in the same order (x is permuted once, GEMM1 writes h in it), so
 //     every dot product is unchanged.
+// FP4 experts (MXFP4, NVFP4) take the same path: each E2M1 code becomes its
+// bf16 value through two byte-permute lookups (hi and lo bytes of the eight
+// magnitudes) plus its sign bit, in the same (i, i + 4) column pairs, and is
+// multiplied by its block scale in bf16 -- exact, as an E2M1 value times an
+// E4M3 or power-of-two scale has at most six significant bits.  The NVFP4
+// per-matrix fp32 scales multiply the fp32 accumulators in the epilogue.
 // Every mbarrier wait is bounded: on time-out the CTA records MOE_DERR_WAIT,
 // every role leaves its loop, the loader drains its own copies, and the CTA
 // frees its TMEM and returns.
@@ -208,7 +214,41 @@ struct GemmMaps {
   CUtensorMap m[3];
 };
 
-template <int MODE, int BN>
+// bf16 of E2M1 codes: the high and low bytes of the eight magnitudes 0, 0.5,
+// 1, 1.5, 2, 3, 4, 6 (index = the code's low three bits), as byte-permute tables
+constexpr uint32_t kE2m1HiA = 0x3F3F3F00u, kE2m1HiB = 0x40404040u;
+constexpr uint32_t kE2m1LoA = 0xC0800000u, kE2m1LoB = 0xC0804000u;
+
+// One word of eight E2M1 codes (columns c0 .. c7, low nibble first) as the
+// bf16x2 pairs (c_i, c_{i+4}), i = 0..3: the order the int4 path yields.
+__device__ __forceinline__ void e2m1_pairs(uint32_t w, uint32_t (&o)[4]) {
+  const uint32_t sa = w & 0x7777u, sb = (w >> 16) & 0x7777u;
+  const uint32_t hia = __byte_perm(kE2m1HiA, kE2m1HiB, sa), loa = __byte_perm(kE2m1LoA, kE2m1LoB, sa);
+  const uint32_t hib = __byte_perm(kE2m1HiA, kE2m1HiB, sb), lob = __byte_perm(kE2m1LoA, kE2m1LoB, sb);
+  const uint32_t u = __byte_perm(loa, hia, 0x5140), v = __byte_perm(loa, hia, 0x7362);
+  const uint32_t ub = __byte_perm(lob, hib, 0x5140), vb = __byte_perm(lob, hib, 0x7362);
+  o[0] = __byte_perm(u, ub, 0x5410) | ((w << 12) & 0x80008000u);
+  o[1] = __byte_perm(u, ub, 0x7632) | ((w << 8) & 0x80008000u);
+  o[2] = __byte_perm(v, vb, 0x5410) | ((w << 4) & 0x80008000u);
+  o[3] = __byte_perm(v, vb, 0x7632) | (w & 0x80008000u);
+}
+
+// bf16 bits of one block scale byte: E4M3 (NVFP4; through fp16, both exact) or
+// E8M0 2^(e-127) (MXFP4; 0 is 2^-127, a bf16 subnormal; 255 is NaN).
+template <int FMT>
+__device__ __forceinline__ uint32_t fp4_scale_bf16(uint32_t byte) {
+  if constexpr (FMT == MOE_FORMAT_NVFP4) {
+    uint32_t r;
+    const uint16_t pair = (uint16_t)(byte | (byte << 8));  // both halves: e4m3(byte)
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(pair));
+    const float f = __half2float(__ushort_as_half((unsigned short)(r & 0xFFFFu)));
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
+  } else {
+    return byte == 0u ? 0x0040u : byte == 255u ? 0x7FC0u : byte << 7;
+  }
+}
+
+template <int MODE, int BN, int FMT>
 __global__ void __launch_bounds__(TileCfg<BN>::kThreads, TileCfg<BN>::kMinBlocks)
     grouped_gemm_kernel(GemmArgs g, const __grid_constant__ GemmMaps maps) {
   using C = TileCfg<BN>;
@@ -374,17 +414,18 @@ __global__ void __launch_bounds__(TileCfg<BN>::kThreads, TileCfg<BN>::kMinBlocks
     const int t = tid - kDqWarp0 * 32, w = wid - kDqWarp0;  // warp w: B rows 32w .. 32w+31
     const uint8_t* blob = (grp < g.E) ? g.experts + (int64_t)grp * g.blob_bytes : g.shared;
     const BlobOffsets off = blob_offsets(H, I);
+    const Fp4Offsets fo = fp4_offsets(H, I, FMT == MOE_FORMAT_INT4 ? MOE_FORMAT_NVFP4 : FMT);
     int64_t row, so, bo;
     int my;  // first row of this warp's code box in the map
     if (MODE == 1) {
       const bool up = t >= kBN / 2;
       row = (int64_t)nt * (kBN / 2) + (up ? t - kBN / 2 : t);
-      so = up ? off.us : off.gs;
+      so = FMT == MOE_FORMAT_INT4 ? (up ? off.us : off.gs) : (up ? fo.us : fo.gs);
       bo = up ? off.ub : off.gb;
       my = (up ? I : 0) + nt * (kBN / 2) + 32 * (w % (kDqWarps / 2));  // up rows follow the gate rows
     } else {
       row = (int64_t)nt * kBN + t;
-      so = off.ds;
+      so = FMT == MOE_FORMAT_INT4 ? off.ds : fo.ds;
       bo = off.db;
       my = nt * kBN + 32 * w;
     }
@@ -418,17 +459,36 @@ __global__ void __launch_bounds__(TileCfg<BN>::kThreads, TileCfg<BN>::kMinBlocks
         v.b0 = __ldg(reinterpret_cast<const uint32_t*>(brw + kb * 2));
       }
     };
+    // FP4: this row's block scale bytes of k-block kb (4 of 16 columns, or 2 of 32)
+    const uint8_t* frow = blob + so + row * (K / (FMT == MOE_FORMAT_NVFP4 ? 16 : 32));
+    auto load_fs = [&](int kb) -> uint32_t {
+      if constexpr (FMT == MOE_FORMAT_NVFP4)
+        return __ldg(reinterpret_cast<const uint32_t*>(frow + kb * 4));
+      else
+        return __ldg(reinterpret_cast<const uint16_t*>(frow + kb * 2));
+    };
     SB cur{}, nxt{};
-    load_sb(0, cur);
-    if (span < nk) load_sb(span, nxt);
+    uint32_t fs_cur = 0, fs_nxt = 0;
+    if constexpr (FMT == MOE_FORMAT_INT4) {
+      load_sb(0, cur);
+      if (span < nk) load_sb(span, nxt);
+    } else {
+      fs_cur = load_fs(0);
+      if (nk > 1) fs_nxt = load_fs(1);
+    }
     const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.0f, 128.0f);
     int kb = 0, consumed = 0;
     bool failed = false;
     for (; kb < nk; ++kb) {
       const int sb = kb % kStagesB, use = kb / kStagesB, cs = kb % kCodeStages;
-      if (kb > 0 && kb % span == 0) {
-        cur = nxt;
-        if (kb + span < nk) load_sb(kb + span, nxt);
+      if constexpr (FMT == MOE_FORMAT_INT4) {
+        if (kb > 0 && kb % span == 0) {
+          cur = nxt;
+          if (kb + span < nk) load_sb(kb + span, nxt);
+        }
+      } else if (kb > 0) {
+        fs_cur = fs_nxt;
+        if (kb + 1 < nk) fs_nxt = load_fs(kb + 1);
       }
       // the stage's previous MMAs are done (lane 0), this block's codes have landed (all lanes)
       if (lane == 0 && use > 0 && !mbar_wait(smem_u32(&empty_b[sb]), (use - 1) & 1)) s_fail = 1;
@@ -445,27 +505,51 @@ __global__ void __launch_bounds__(TileCfg<BN>::kThreads, TileCfg<BN>::kMinBlocks
       __syncwarp();
       consumed = kb + 1;
       if (lane == 0 && issued < nk) issue(issued++);
-      const int gi = kb % span;  // group within the fetched span
-      const uint32_t sw = gi < 2 ? cur.s0 : gi < 4 ? cur.s1 : gi < 6 ? cur.s2 : cur.s3;
-      const uint32_t bw = gi < 2 ? cur.b0 : gi < 4 ? cur.b1 : gi < 6 ? cur.b2 : cur.b3;
-      const uint32_t sh = (gi & 1) ? (sw >> 16) : (sw & 0xFFFFu);
-      const uint32_t bh = (gi & 1) ? (bw >> 16) : (bw & 0xFFFFu);
-      const uint32_t s2u = sh | (sh << 16), b2u = bh | (bh << 16);
-      const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162*>(&s2u);
-      const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&b2u);
       const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
       unsigned char* bb = b_ptr + sb * kBBytes;
+      if constexpr (FMT == MOE_FORMAT_INT4) {
+        const int gi = kb % span;  // group within the fetched span
+        const uint32_t sw = gi < 2 ? cur.s0 : gi < 4 ? cur.s1 : gi < 6 ? cur.s2 : cur.s3;
+        const uint32_t bw = gi < 2 ? cur.b0 : gi < 4 ? cur.b1 : gi < 6 ? cur.b2 : cur.b3;
+        const uint32_t sh = (gi & 1) ? (sw >> 16) : (sw & 0xFFFFu);
+        const uint32_t bh = (gi & 1) ? (bw >> 16) : (bw & 0xFFFFu);
+        const uint32_t s2u = sh | (sh << 16), b2u = bh | (bh << 16);
+        const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162*>(&s2u);
+        const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&b2u);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t o[4];
+        for (int c = 0; c < 8; ++c) {
+          uint32_t o[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint32_t v = ((words[c] >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
-          const __nv_bfloat162 q = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v), k128);
-          const __nv_bfloat162 wv = __hfma2(q, s2, b2);
-          o[i] = *reinterpret_cast<const uint32_t*>(&wv);
+          for (int i = 0; i < 4; ++i) {
+            uint32_t v = ((words[c] >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
+            const __nv_bfloat162 q = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v), k128);
+            const __nv_bfloat162 wv = __hfma2(q, s2, b2);
+            o[i] = *reinterpret_cast<const uint32_t*>(&wv);
+          }
+          *reinterpret_cast<uint4*>(bb + swz(t, c)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
-        *reinterpret_cast<uint4*>(bb + swz(t, c)) = make_uint4(o[0], o[1], o[2], o[3]);
+      } else {
+        // word c holds columns 8c .. 8c + 7: block c / 2 (16 columns) or c / 4 (32)
+        constexpr int kBlocks = FMT == MOE_FORMAT_NVFP4 ? 4 : 2;
+        uint32_t sc2[kBlocks];
+#pragma unroll
+        for (int j = 0; j < kBlocks; ++j) {
+          const uint32_t h = fp4_scale_bf16<FMT>((fs_cur >> (8 * j)) & 0xFFu);
+          sc2[j] = h | (h << 16);
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t o[4];
+          e2m1_pairs(words[c], o);
+          const __nv_bfloat162 s2 =
+              *reinterpret_cast<const __nv_bfloat162*>(&sc2[c / (8 / kBlocks)]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 wv = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&o[i]), s2);
+            o[i] = *reinterpret_cast<const uint32_t*>(&wv);
+          }
+          *reinterpret_cast<uint4*>(bb + swz(t, c)) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
       }
       fence_async_smem();
       __syncwarp();
@@ -485,6 +569,14 @@ __global__ void __launch_bounds__(TileCfg<BN>::kThreads, TileCfg<BN>::kMinBlocks
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (ok) {
       tc_fence_after();
+      // NVFP4: the fp32 matrix scales of gate, up and down multiply the sums
+      float sg = 1.0f, su = 1.0f, sd = 1.0f;
+      if constexpr (FMT == MOE_FORMAT_NVFP4) {
+        const float* mat = reinterpret_cast<const float*>(blob + fo.mat);
+        sg = __ldg(mat);
+        su = __ldg(mat + 1);
+        sd = __ldg(mat + 2);
+      }
       const int q = wid & 3, ch = (wid - kDqWarp0) >> 2;  // TMEM lane quarter, column half
       // Each warp stages its 32 rows x kRowBytes of output (bf16) in the idle A
       // ring, 16-byte chunks XOR-swizzled by the row within each 128-byte segment
@@ -514,7 +606,12 @@ __global__ void __launch_bounds__(TileCfg<BN>::kThreads, TileCfg<BN>::kMinBlocks
             for (int e = 0; e < 32; e += 8) {
               float h[8];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) h[i] = silu(gv[e + i]) * uv[e + i];
+              for (int i = 0; i < 8; ++i) {
+                if constexpr (FMT == MOE_FORMAT_NVFP4)
+                  h[i] = silu(gv[e + i] * sg) * (uv[e + i] * su);
+                else
+                  h[i] = silu(gv[e + i]) * uv[e + i];
+              }
               *reinterpret_cast<uint4*>(stg + sidx(lane, (c + e) >> 3)) = make_uint4(
                   bf2(h[0], h[4]), bf2(h[1], h[5]), bf2(h[2], h[6]), bf2(h[3], h[7]));
             }
@@ -531,6 +628,7 @@ __global__ void __launch_bounds__(TileCfg<BN>::kThreads, TileCfg<BN>::kMinBlocks
               dst_row = (int64_t)(a - Tk) * (g.k + 1) + g.k;
               wgt = 1.0f;
             }
+            wgt *= sd;
           }
 #pragma unroll
           for (int c = 0; c < kColsW; c += 32) {
@@ -573,8 +671,26 @@ __global__ void __launch_bounds__(TileCfg<BN>::kThreads, TileCfg<BN>::kMinBlocks
 
 }  // namespace
 
+// One (mode, tile width, format) instantiation: its shared-memory attribute once
+// per device, then the launch (n-tiles along x, m-tiles along y).
+template <int MODE, int BN, int FMT>
+cudaError_t launch_mode(const GemmArgs& a, const GemmMaps& maps, int max_tiles, int d,
+                        cudaStream_t st) {
+  using C = TileCfg<BN>;
+  static bool attr_done[64] = {};
+  if (!attr_done[d]) {
+    const cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, BN, FMT>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)C::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_done[d] = true;
+  }
+  const dim3 grid(MODE == 1 ? a.I / (BN / 2) : a.H / BN, max_tiles);
+  grouped_gemm_kernel<MODE, BN, FMT><<<grid, C::kThreads, C::kSmem, st>>>(a, maps);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_grouped_gemm(int mode, const GemmArgs& a, int max_tiles, cudaStream_t st) {
-  static bool attr_done[2][64] = {};
   int d = 0;
   cudaError_t e = cudaGetDevice(&d);
   if (e != cudaSuccess) return e;
@@ -606,27 +722,17 @@ cudaError_t launch_grouped_gemm(int mode, const GemmArgs& a, int max_tiles, cuda
       return e;
   }
   if (mode == 1) {
-    using C = TileCfg<kTileN1>;
-    if (!attr_done[0][d]) {
-      e = cudaFuncSetAttribute(grouped_gemm_kernel<1, kTileN1>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
-      if (e != cudaSuccess) return e;
-      attr_done[0][d] = true;
-    }
-    const dim3 grid(a.I / (kTileN1 / 2), max_tiles);
-    grouped_gemm_kernel<1, kTileN1><<<grid, C::kThreads, C::kSmem, st>>>(a, maps);
-  } else {
-    using C = TileCfg<kTileN2>;
-    if (!attr_done[1][d]) {
-      e = cudaFuncSetAttribute(grouped_gemm_kernel<2, kTileN2>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
-      if (e != cudaSuccess) return e;
-      attr_done[1][d] = true;
-    }
-    const dim3 grid(a.H / kTileN2, max_tiles);
-    grouped_gemm_kernel<2, kTileN2><<<grid, C::kThreads, C::kSmem, st>>>(a, maps);
+    if (a.format == MOE_FORMAT_MXFP4)
+      return launch_mode<1, kTileN1, MOE_FORMAT_MXFP4>(a, maps, max_tiles, d, st);
+    if (a.format == MOE_FORMAT_NVFP4)
+      return launch_mode<1, kTileN1, MOE_FORMAT_NVFP4>(a, maps, max_tiles, d, st);
+    return launch_mode<1, kTileN1, MOE_FORMAT_INT4>(a, maps, max_tiles, d, st);
   }
-  return cudaGetLastError();
+  if (a.format == MOE_FORMAT_MXFP4)
+    return launch_mode<2, kTileN2, MOE_FORMAT_MXFP4>(a, maps, max_tiles, d, st);
+  if (a.format == MOE_FORMAT_NVFP4)
+    return launch_mode<2, kTileN2, MOE_FORMAT_NVFP4>(a, maps, max_tiles, d, st);
+  return launch_mode<2, kTileN2, MOE_FORMAT_INT4>(a, maps, max_tiles, d, st);
 }
 
 }  // namespace moe

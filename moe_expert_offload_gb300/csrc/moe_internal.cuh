@@ -309,6 +309,7 @@ struct GemmArgs {
   uint16_t* h_out;          // mode 1 output: h_perm [R][I], K-permuted
   uint16_t* y_out;          // mode 2 output: y_assign [T][k+1][H]
   int32_t* err;             // device error bits (MOE_DERR_*), may be null
+  int format;               // MOE_FORMAT_* of the expert blobs
 };
 
 struct PrefillBufs {

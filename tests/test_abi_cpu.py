@@ -67,11 +67,14 @@ def test_fp4_expert_bytes_match_the_oracle_layout(L):
             assert got == oracle.fp4_blob_offsets(H, I, ofmt)["total"], (fmt, H, I)
 
 
-def test_fp4_prefill_is_unsupported(L):
-    s = _spec(hidden=1024, inter=512, fmt=m.FORMAT_NVFP4)
-    with pytest.raises(m.MoeError) as e:
-        m.moe_expert_ffn_prefill(s, 16, 16, 4, 16, 16, None, None, 256, 1 << 20, 16, stream=0)
-    assert e.value.code == m.MOE_EUNSUPPORTED
+def test_fp4_prefill_workspace_is_format_independent(L):
+    """The prefill path takes FP4 experts (dequantised to bf16 in the GEMM); its
+    scratch (permute, h, weighted outputs) does not depend on the weight format."""
+    for T in (1, 300, 8192):
+        want = m.moe_prefill_workspace_bytes(_spec(hidden=1024, inter=512), T)
+        assert want > 0
+        for fmt in (m.FORMAT_MXFP4, m.FORMAT_NVFP4):
+            assert m.moe_prefill_workspace_bytes(_spec(hidden=1024, inter=512, fmt=fmt), T) == want
 
 
 @pytest.mark.parametrize("kw", [

@@ -195,3 +195,85 @@ def test_fp4_qwen_shape_layer_steps(oracle, fmt):
     ids_of = cache.id_of_slot.cpu().numpy()
     for v in np.nonzero(ids_of >= 0)[0][:64]:
         assert torch.equal(cache.pool[v], bank[int(ids_of[v])]), f"slot {v}"
+
+
+# ------------------------------------------------------------------ prefill
+def _prefill_reference(oracle, blobs, H, I, fmt, xb, ids, wts, shared_blob=None):
+    """y[t] = sum_j w[t][j] expert_{ids[t][j]}(x[t]) (+ shared(x[t])), float64; each
+    expert's oracle FP4 forward runs on the rows routed to it only."""
+    T = xb.shape[0]
+    of = ORACLE_FMT[fmt]
+    y = np.zeros((T, H), dtype=np.float64)
+    for e in np.unique(ids):
+        rows = np.nonzero((ids == e).any(axis=1))[0]
+        ye = oracle.fp4_expert_forward(blobs[int(e)], H, I, of, xb[rows])
+        for n, t in enumerate(rows):
+            y[t] += float(wts[t][ids[t] == e].sum()) * ye[n]
+    if shared_blob is not None:
+        y += oracle.fp4_expert_forward(shared_blob, H, I, of, xb)
+    return y
+
+
+def _prefill(spec, experts, shared, xb, ids_h, w_h):
+    T, H = xb.shape[0], spec.hidden
+    wsb = m.moe_prefill_workspace_bytes(spec, T)
+    assert wsb > 0
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    y = torch.full((T, H), float("nan"), dtype=torch.float32, device=DEV)
+    m.moe_expert_ffn_prefill(spec, experts, dev_bits(xb, DEV), T, dev(ids_h, DEV), dev(w_h, DEV),
+                             shared, err, ws, wsb, y)
+    torch.cuda.synchronize()
+    assert int(err.cpu()[0]) == 0
+    return y.cpu().numpy()
+
+
+@pytest.mark.parametrize("fmt", [m.FORMAT_MXFP4, m.FORMAT_NVFP4])
+@pytest.mark.parametrize("H,I,E,k,T,shared", [(256, 128, 16, 2, 300, True),
+                                              (1024, 256, 32, 4, 400, False),
+                                              (2048, 512, 16, 4, 200, True)])
+def test_fp4_prefill_matches_oracle(oracle, fmt, H, I, E, k, T, shared):
+    """moe_expert_ffn_prefill on FP4 experts (the grouped tcgen05 GEMMs with the
+    weights dequantised to bf16 in the kernel) against the oracle's FP4 expert."""
+    spec = m.make_spec(1, H, I, E, k, has_shared=shared, fmt=fmt)
+    bank_h = _fp4_bank(E + 1, H, I, fmt, seed=H + T + 10 * fmt)
+    bank = dev(bank_h, DEV)
+    rng = np.random.default_rng(T + fmt)
+    xb = synth.bf16_bits(rng.normal(0, 1.5, (T, H)))
+    wr_h = synth.router_weights(E, E, H)
+    ids_h, w_h = oracle.route_softmax_topk(oracle.router_logits(xb, wr_h), k)
+    y = _prefill(spec, bank[:E], bank[E] if shared else None, xb, ids_h, w_h)
+    ref = _prefill_reference(oracle, bank_h, H, I, fmt, xb, ids_h, w_h,
+                             bank_h[E] if shared else None)
+    assert_ffn_close(y, ref, f"fp4 prefill fmt {fmt} H {H} T {T}")
+
+
+@pytest.mark.parametrize("fmt", [m.FORMAT_MXFP4, m.FORMAT_NVFP4])
+def test_fp4_prefill_wide_scales_and_multi_tile_experts(oracle, fmt):
+    """Block scales across a wide range (MXFP4 E8M0 bytes 100..150, i.e. 2^-27 ..
+    2^23, beyond what the decode kernel's fp16 products hold; NVFP4 E4M3 bytes
+    including subnormals and the largest finite value 448), and skewed routing:
+    two experts take most rows, so each spans several 256-row m-tiles."""
+    H, I, E, k, T = 256, 128, 8, 2, 700
+    of = ORACLE_FMT[fmt]
+    spec = m.make_spec(1, H, I, E, k, has_shared=False, fmt=fmt)
+    bank_h = _fp4_bank(E, H, I, fmt, seed=99 + fmt)
+    off = oracle.fp4_blob_offsets(H, I, of)
+    rng = np.random.default_rng(5 + fmt)
+    n_sc = off["mat"] - off["gs"]
+    if fmt == m.FORMAT_MXFP4:
+        bank_h[:, off["gs"]:off["mat"]] = rng.integers(100, 151, size=(E, n_sc), dtype=np.uint8)
+    else:
+        sc = rng.integers(0, 0x7F, size=(E, n_sc), dtype=np.uint8)  # no NaN (0x7F)
+        sc[:, ::17] = 0x7E                                           # 448
+        sc[:, 3::29] = rng.integers(1, 8, size=sc[:, 3::29].shape)  # subnormals
+        bank_h[:, off["gs"]:off["mat"]] = sc
+    bank = dev(bank_h, DEV)
+    xb = synth.bf16_bits(rng.normal(0, 1, (T, H)))
+    ids_h = np.zeros((T, k), np.int32)
+    ids_h[:, 0] = 3
+    ids_h[:, 1] = np.where(rng.random(T) < 0.9, 6, rng.integers(0, 3, T))
+    w_h = np.tile(np.array([[0.7, 0.3]], np.float32), (T, 1))
+    y = _prefill(spec, bank, None, xb, ids_h, w_h)
+    ref = _prefill_reference(oracle, bank_h, H, I, fmt, xb, ids_h, w_h)
+    assert_ffn_close(y, ref, f"fp4 prefill wide scales fmt {fmt}")
