@@ -108,9 +108,18 @@ int main() {
   CHECK(moe_expert_ffn_noalloc(&big, &cb, 0, &pb, dummy, 64, dummy, reinterpret_cast<float*>(dummy),
                                nullptr, reinterpret_cast<float*>(dummy), nullptr) ==
         MOE_ECAPACITY);
+  // FP4 prefill passes the format check; the stack buffer fails the 256-byte
+  // workspace alignment before anything is launched
+  CHECK(moe_prefill_workspace_bytes(&nv, 4) > 0);
   CHECK(moe_expert_ffn_prefill(&nv, dummy, dummy, 4, dummy, reinterpret_cast<float*>(dummy),
-                               nullptr, nullptr, dummy, 1 << 20, reinterpret_cast<float*>(dummy),
-                               nullptr) == MOE_EUNSUPPORTED);
+                               nullptr, nullptr, dummy + 1, 1 << 20,
+                               reinterpret_cast<float*>(dummy), nullptr) == MOE_EINVAL);
+  // elastic resize: host-side rejections
+  CHECK(moe_slots_for_budget(&nv, -1) == -1);
+  CHECK(moe_slots_for_budget(&nv, 0) == 0);
+  CHECK(moe_cache_resize_workspace_bytes(&cb, 0) == 0);
+  CHECK(moe_cache_resize(&nv, &cb, 0, dummy, 1 << 20, nullptr) == MOE_EINVAL);
+  CHECK(moe_cache_resize(&nv, &cb, 4, dummy, 4, nullptr) == MOE_ECAPACITY);
   if (g_fail) return 1;
   std::printf("abi sanitizer run: ok\n");
   return 0;
