@@ -277,3 +277,45 @@ def test_fp4_prefill_wide_scales_and_multi_tile_experts(oracle, fmt):
     y = _prefill(spec, bank, None, xb, ids_h, w_h)
     ref = _prefill_reference(oracle, bank_h, H, I, fmt, xb, ids_h, w_h)
     assert_ffn_close(y, ref, f"fp4 prefill wide scales fmt {fmt}")
+
+
+def test_fp4_full_size_prefill_layer(oracle):
+    """The qwen_prefill_nvfp4 shape: one Qwen-shaped NVFP4 layer, 8192 tokens whose
+    routing union covers all 256 experts, through moe_layer_forward_prefill.  Against
+    the oracle's FP4 expert: 64 rows spread over the m-tiles of the two experts with
+    the most assignments (each spans several 256-row m-tiles) and 16 rows of the
+    shared expert's group."""
+    H, I, E, k, T = 2048, 512, 256, 8, 8192
+    fmt = m.FORMAT_NVFP4
+    spec = m.make_spec(1, H, I, E, k, has_shared=True, fmt=fmt)
+    bank = synth.make_fp4_bank_torch(E + 1, H, I, ORACLE_FMT[fmt], 13, DEV)
+    wr_h = synth.router_weights(78, E, H)
+    xb = synth.prefill_hidden(4, T, H, wr_h)
+    wsb = m.moe_prefill_workspace_bytes(spec, T)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    wts = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    y = torch.empty((T, H), dtype=torch.float32, device=DEV)
+    m.moe_layer_forward_prefill(spec, bank[:E], dev_bits(xb, DEV), T, dev_bits(wr_h, DEV), None,
+                                bank[E], ids, wts, err, ws, wsb, y)
+    torch.cuda.synchronize()
+    assert int(err.cpu()[0]) == 0
+    ids_g, w_g, y_g = ids.cpu().numpy(), wts.cpu().numpy(), y.cpu().numpy()
+    assert len(np.unique(ids_g)) == E
+    assert np.all(np.isfinite(y_g))
+    counts = np.bincount(ids_g.reshape(-1), minlength=E)
+    top2 = np.argsort(-counts, kind="stable")[:2]
+    assert counts[top2].min() > 256, counts[top2]
+    rows = set()
+    for e in top2:
+        r = np.nonzero((ids_g == e).any(axis=1))[0]
+        rows |= set(r[np.linspace(0, len(r) - 1, 32).round().astype(int)].tolist())
+    rows |= set(range(4096, 4096 + 256, 16))
+    rows = np.asarray(sorted(rows))
+    blobs = {int(e): bank[int(e)].cpu().numpy() for e in np.unique(ids_g[rows])}
+    ref = _prefill_reference(oracle, blobs, H, I, fmt, xb[rows], ids_g[rows], w_g[rows],
+                             bank[E].cpu().numpy())
+    assert_ffn_close(y_g[rows], ref, f"full-size NVFP4 prefill: {len(rows)} rows")
+    del bank
+    torch.cuda.empty_cache()
