@@ -711,9 +711,11 @@ def run_gpu(args, w, rank, world, local_rank):
                   "direct_per_layer": n_direct / layer_steps,
                   "uniq_per_layer": n_uniq / layer_steps},
         "ffn_gbs": achieved,
-        # a fill carried by the FFN writes the slot (S_e) and reads nothing extra; a
-        # fill copy kernel reads and writes (2 S_e)
-        "step_gbs": (ffn_bytes + (1 if fused else 2) * se * n_fill / layer_steps) * L /
+        # per layer-step: the experts read, the router weights and the fills (a fill
+        # carried by the FFN writes the slot, S_e; a fill copy kernel reads and writes
+        # it, 2 S_e), over the graph-timed step
+        "step_gbs": ((n_uniq / layer_steps + (1 if w["shared"] else 0)) * se + E * H * 2 +
+                     (1 if fused else 2) * se * n_fill / layer_steps) * L /
                     (ms * 1e-3 / args.steps) / 1e9,
     }
     if cpu:
