@@ -562,6 +562,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ float s_ih[kMaxTok], s_wp[kMaxTok];
   __shared__ int s_fail;
   __shared__ __align__(16) uint32_t s_zero[8];  // B fragment and (O, X) of an absent token
+  __shared__ __align__(8) uint64_t s_lgbar;     // one-kernel step: the staged router rows
+  // the first ring slot that generic-proxy code used in this launch (routing
+  // scratch, staged rows): the producer fences once before its TMA reuses it
+  __shared__ int s_gen_slot;
   const int H = a.H, I = a.I, T = a.T, k = a.k;
   const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
   const int nst = geo.nst;
@@ -587,6 +591,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bar_init(su32(&rfull[i]), kCW);  // every consumer warp's partial is written
       bar_init(su32(&rfree[i]), 1);    // the tile's reducer has read them
     }
+    bar_init(su32(&s_lgbar), 1);
+    s_gen_slot = FUSED ? nst - 3 : nst;
     s_fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -685,8 +691,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* sync = lf.sync;
     uint32_t early[CtlSh::NE];
     int32_t early_id[CtlSh::NE];
-    CtlSh& cs = *reinterpret_cast<CtlSh*>(ring);
-    SelScratch& ss = *reinterpret_cast<SelScratch*>(ring + sizeof(CtlSh));
+    // the routing scratch in the ring's last three slots: the stream fills the
+    // first slots first, so its opening stages do not wait for a proxy fence
+    unsigned char* scr = ring + (size_t)(nst - 3) * kSlotBytes;
+    CtlSh& cs = *reinterpret_cast<CtlSh*>(scr);
+    SelScratch& ss = *reinterpret_cast<SelScratch*>(scr + sizeof(CtlSh));
     griddep_wait();  // x, the cache tables and the pool of the previous kernels
     // the next kernel may be scheduled now: its CTAs start on SMs this grid
     // frees and wait for its completion before reading anything
@@ -706,12 +715,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       // CTA 0 changes it only after every CTA has arrived there)
       for (int i = tid; i < E; i += kConsThreads) ss.slot[i] = lf.c.slot_of_id[a.layer * E + i];
       // router logits (the fixed order of every router path): pair p = (t, e)
-      // on CTA p % Gall, warp p / Gall
-      for (int p = (int)blockIdx.x + (int)Gall * wid; p < np; p += (int)Gall * kCW) {
-        const int t = p / E, e = p - t * E;
-        const float v =
-            rsel::router_dot_warp(a.x + (size_t)t * H, lf.w_router + (size_t)e * H, H);
-        if (lane == 0) lf.logits[p] = v;
+      // on CTA p % Gall, warp p / Gall.  Past 256 chunks per row (a warp would
+      // load its two rows in several rounds) the CTA's x rows and router rows
+      // are first staged in the ring's free slots by bulk copies: one round trip.
+      const int mine = np > (int)blockIdx.x ? (np - 1 - (int)blockIdx.x) / (int)Gall + 1 : 0;
+      const uint32_t rowb = (uint32_t)H * 2u;
+      const int nsl = (int)(((size_t)(T + mine) * rowb + kSlotBytes - 1) / kSlotBytes);
+      const bool staged = H > 2048 && mine <= kCW && nsl <= nst - 3;
+      unsigned char* stg = scr - (size_t)nsl * kSlotBytes;  // the slots before the scratch
+      if (staged) {
+        if (tid == 0) {
+          s_gen_slot = nst - 3 - nsl;
+          bar_expect(su32(&s_lgbar), (uint32_t)(T + mine) * rowb);
+          for (int t = 0; t < T; ++t)
+            bulk_g2s(su32(stg + (size_t)t * rowb), a.x + (size_t)t * H, rowb, su32(&s_lgbar));
+          for (int i = 0; i < mine; ++i) {
+            const int p = (int)blockIdx.x + (int)Gall * i, e = p % E;
+            bulk_g2s(su32(stg + (size_t)(T + i) * rowb), lf.w_router + (size_t)e * H, rowb,
+                     su32(&s_lgbar));
+          }
+        }
+        const bool got = warp_wait(su32(&s_lgbar), 0);
+        if (wid < mine && got) {
+          const int p = (int)blockIdx.x + (int)Gall * wid, t = p / E;
+          const float v = rsel::router_dot_smem(reinterpret_cast<const uint4*>(stg + (size_t)t * rowb),
+                                                reinterpret_cast<const uint4*>(stg + (size_t)(T + wid) * rowb), H);
+          if (lane == 0) lf.logits[p] = v;
+        }
+        if (!got && lane == 0) s_fail = 1;
+      } else {
+        for (int p = (int)blockIdx.x + (int)Gall * wid; p < np; p += (int)Gall * kCW) {
+          const int t = p / E, e = p - t * E;
+          const float v =
+              rsel::router_dot_warp(a.x + (size_t)t * H, lf.w_router + (size_t)e * H, H);
+          if (lane == 0) lf.logits[p] = v;
+        }
       }
       // y starts at zero: ordered before every down tile's adds by the logits count,
       // which every CTA waits for before its first tile
@@ -791,6 +829,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (wid == kProdW) {
     // ------------------------------------------------------------ producer
     int n = 0, s = 0, rnd = 0;  // stages issued; ring slot and round of stage n
+    // slots from gen_slot on held generic-proxy data (routing scratch, staged router
+    // rows): one proxy fence orders those accesses before the first TMA write there
+    const int gen_slot = s_gen_slot;
+    bool fenced = false;
     bool ok = !a.inject_stall;  // test hook: no copies, every wait runs out
     const uint64_t pol = l2_evict_first();  // weights are read once per call
     auto slot_ready = [&]() {
@@ -798,6 +840,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         r = rnd == 0 || bar_wait(su32(&empty[s]), (rnd - 1) & 1);
         if (r) bar_expect(su32(&full[s]), kCodeBytes + kSB);
+      }
+      if (!fenced && s >= gen_slot) {
+        fence_proxy_async_smem();
+        fenced = true;
       }
       return __shfl_sync(0xffffffffu, r, 0) != 0;
     };

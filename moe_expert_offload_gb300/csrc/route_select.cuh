@@ -59,6 +59,28 @@ __device__ __forceinline__ float router_dot_warp(const uint16_t* __restrict__ x,
   return acc;
 }
 
+// router_dot_warp on rows staged in shared memory (the same chunk-to-lane
+// assignment, the same fma order and butterfly): bit-identical logits.
+__device__ __forceinline__ float router_dot_smem(const uint4* xr, const uint4* wr, int H) {
+  const int lane = threadIdx.x & 31;
+  const int chunks = H >> 3;
+  float acc = 0.0f;
+  for (int c = lane; c < chunks; c += 32) {
+    const uint4 xv = xr[c], wv = wr[c];
+    acc = __fmaf_rn(bf_lo(xv.x), bf_lo(wv.x), acc);
+    acc = __fmaf_rn(bf_hi(xv.x), bf_hi(wv.x), acc);
+    acc = __fmaf_rn(bf_lo(xv.y), bf_lo(wv.y), acc);
+    acc = __fmaf_rn(bf_hi(xv.y), bf_hi(wv.y), acc);
+    acc = __fmaf_rn(bf_lo(xv.z), bf_lo(wv.z), acc);
+    acc = __fmaf_rn(bf_hi(xv.z), bf_hi(wv.z), acc);
+    acc = __fmaf_rn(bf_lo(xv.w), bf_lo(wv.w), acc);
+    acc = __fmaf_rn(bf_hi(xv.w), bf_hi(wv.w), acc);
+  }
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, d));
+  return acc;
+}
+
 // exp(x) in fp32: Cody-Waite reduction x = n ln2 + r (ln2 = 0x1.62e4p-1 +
 // 0x1.7f7d1cp-20, the high part short enough that n * hi is exact), the
 // degree-7 Taylor polynomial of e^r (coefficients 1/7! .. 1/0!) in Horner
