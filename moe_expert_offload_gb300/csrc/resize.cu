@@ -12,8 +12,8 @@
 // the two sizes are left empty (id -1, ts 0), so a later growth starts from
 // empty slots.  The clock does not move.
 //
-// Two kernels: one CTA plans and updates the tables (a 64-step bisection on
-// the 64-bit keys finds the eviction threshold with block-wide counts, then
+// Two kernels: one CTA plans and updates the tables (a radix select over the
+// 64-bit keys finds the eviction threshold in eight counting passes, then
 // block scans place the moves), and a grid copies the moved blobs.
 #include <cstdint>
 
@@ -29,6 +29,8 @@ struct RzShared {
   uint32_t warp[kRzWarps];
   uint32_t total;
   int bad;
+  uint32_t hist[256];  // radix select: keys per digit value
+  uint32_t digit, below;
 };
 
 // Sum of v over the block (all threads call it; two barriers).
@@ -109,22 +111,55 @@ __global__ void __launch_bounds__(kRzThreads, 1)
   }
   const uint32_t n_ev = n_occ > (uint32_t)S_new ? n_occ - (uint32_t)S_new : 0u;
 
-  // the eviction threshold: the smallest X with #{occupied keys <= X} >= n_ev
-  // (keys are distinct, so exactly n_ev keys lie at or below it)
+  // the eviction threshold: the n_ev-th smallest occupied key (keys are distinct,
+  // so exactly n_ev keys lie at or below it), by a radix select over the 64-bit
+  // keys, 8 bits per pass from the top: each pass counts the keys that share
+  // the digits found so far by their next digit and keeps the digit whose
+  // cumulative count first reaches the remaining rank
   uint64_t thr = 0;
   if (n_ev > 0) {
-    uint64_t lo = 0, hi = ~0ull;  // invariant: count(<= hi) >= n_ev
-    while (lo < hi) {
-      const uint64_t mid = lo + ((hi - lo) >> 1);
-      uint32_t c = 0;
-      for (int v = tid; v < S; v += kRzThreads)
-        c += (id_of_slot[v] >= 0 && slot_key(ts, v) <= mid) ? 1u : 0u;
-      if (block_sum(c, sh) >= n_ev)
-        hi = mid;
-      else
-        lo = mid + 1;
+    uint64_t prefix = 0, pmask = 0;
+    uint32_t rank = n_ev;  // 1-based rank among the keys that match prefix
+    for (int shift = 56; shift >= 0; shift -= 8) {
+      if (tid < 256) sh.hist[tid] = 0u;
+      __syncthreads();
+      for (int v = tid; v < S; v += kRzThreads) {
+        if (id_of_slot[v] < 0) continue;
+        const uint64_t key = slot_key(ts, v);
+        if ((key & pmask) == prefix) atomicAdd(&sh.hist[(key >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (tid < 32) {
+        // lane l holds digits 8 l .. 8 l + 7; an exclusive scan over the lanes
+        uint32_t c[8], sum = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          c[j] = sh.hist[8 * tid + j];
+          sum += c[j];
+        }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+          if (tid >= d) incl += o;
+        }
+        uint32_t run = incl - sum;  // keys with a smaller digit than 8 l
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (run < rank && rank <= run + c[j]) {
+            sh.digit = 8u * tid + j;
+            sh.below = run;
+          }
+          run += c[j];
+        }
+      }
+      __syncthreads();
+      prefix |= (uint64_t)sh.digit << shift;
+      pmask |= (uint64_t)255u << shift;
+      rank -= sh.below;
+      __syncthreads();  // hist, digit and below are rewritten by the next pass
     }
-    thr = lo;
+    thr = prefix;
   }
   // evict (the list in ascending slot order)
   uint32_t base = 0;
