@@ -615,50 +615,75 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   auto prep_x = [&](unsigned yb, unsigned NY) {
     const int ctid = tid;
-    for (int t = 0; t < T; ++t) {
-      uint32_t m = 0u;
-      const uint4* xp = reinterpret_cast<const uint4*>(a.x + (int64_t)t * H);
-      for (int i = ctid; i < H / 8; i += kConsThreads) {
-        const uint4 v = __ldg(xp + i);
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+    // max |x| per token: a warp's lanes read 32 consecutive 8-element chunks of x
+    // (one token: H / 8 is a multiple of 32), four chunks per lane in flight
+    const int cpt = H / 8, nch = T * cpt;
+    const uint4* xq = reinterpret_cast<const uint4*>(a.x);
+    for (int i0 = ctid; i0 < nch; i0 += 4 * kConsThreads) {
+      uint4 v4[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int idx = i0 + u * kConsThreads;
+        v4[u] = idx < nch ? __ldg(xq + idx) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int idx = i0 + u * kConsThreads;
+        if (idx >= nch) break;  // (the same for every lane of the warp)
+        const uint32_t w4[4] = {v4[u].x, v4[u].y, v4[u].z, v4[u].w};
+        uint32_t m = 0u;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           m = max(m, (w4[q] << 16) & 0x7FFFFFFFu);
           m = max(m, w4[q] & 0x7FFF0000u);
         }
+        m = __reduce_max_sync(0xffffffffu, m);
+        if (lane == 0) atomicMax(&s_vmax[idx / cpt], m);
       }
-      m = __reduce_max_sync(0xffffffffu, m);
-      if (lane == 0) atomicMax(&s_vmax[t], m);
     }
     cons_sync();
     if (ctid < T) s_px[ctid] = 1.0f / inv_pow2_above(__uint_as_float(s_vmax[ctid]));
+    // the fragments, two items per thread with both items' loads in flight
     const int ng = H / 64, n_items = T * ng * 4;
-    for (int b0 = 0; b0 < n_items; b0 += kConsThreads) {
-      const int it = b0 + ctid;
-      const bool in = it < n_items;
-      const int t = in ? it / (ng * 4) : 0, rem = it - t * ng * 4, G = rem >> 2, q4 = rem & 3;
-      float v[16];
-      float o = 0.0f, xs = 0.0f;
-      if (in) {
-        const float sc = inv_pow2_above(__uint_as_float(s_vmax[t]));
-        const uint4* px = reinterpret_cast<const uint4*>(a.x + (int64_t)t * H + G * 64 + q4 * 16);
-        const uint4 p0 = __ldg(px), p1 = __ldg(px + 1);
-        const uint32_t wv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    for (int b0 = 0; b0 < n_items; b0 += 2 * kConsThreads) {
+      uint4 pv[2][2];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          v[2 * i] = __uint_as_float(wv[i] << 16) * sc;
-          v[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u) * sc;
+      for (int u = 0; u < 2; ++u) {
+        const int it = b0 + u * kConsThreads + ctid;
+        if (it < n_items) {
+          const int t = it / (ng * 4), rem = it - t * ng * 4, G = rem >> 2, q4 = rem & 3;
+          const uint4* px = reinterpret_cast<const uint4*>(a.x + (int64_t)t * H + G * 64 + q4 * 16);
+          pv[u][0] = __ldg(px);
+          pv[u][1] = __ldg(px + 1);
         }
-        if constexpr (FMT == MOE_FORMAT_INT4)
-          frag_item(v, frag + (size_t)t * geo.frow + G * 128 + q4 * 32, o, xs);
-        else
-          frag_plain(v, frag + (size_t)t * geo.frow + G * 128 + q4 * 32);
       }
-      o += __shfl_xor_sync(0xffffffffu, o, 1);
-      o += __shfl_xor_sync(0xffffffffu, o, 2);
-      xs += __shfl_xor_sync(0xffffffffu, xs, 1);
-      xs += __shfl_xor_sync(0xffffffffu, xs, 2);
-      if (in && q4 == 0) ox[G * kMaxTok + t] = make_float2(o, xs);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int it = b0 + u * kConsThreads + ctid;
+        const bool in = it < n_items;
+        const int t = in ? it / (ng * 4) : 0, rem = it - t * ng * 4, G = rem >> 2, q4 = rem & 3;
+        float v[16];
+        float o = 0.0f, xs = 0.0f;
+        if (in) {
+          const float sc = inv_pow2_above(__uint_as_float(s_vmax[t]));
+          const uint4 p0 = pv[u][0], p1 = pv[u][1];
+          const uint32_t wv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            v[2 * i] = __uint_as_float(wv[i] << 16) * sc;
+            v[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u) * sc;
+          }
+          if constexpr (FMT == MOE_FORMAT_INT4)
+            frag_item(v, frag + (size_t)t * geo.frow + G * 128 + q4 * 32, o, xs);
+          else
+            frag_plain(v, frag + (size_t)t * geo.frow + G * 128 + q4 * 32);
+        }
+        o += __shfl_xor_sync(0xffffffffu, o, 1);
+        o += __shfl_xor_sync(0xffffffffu, o, 2);
+        xs += __shfl_xor_sync(0xffffffffu, xs, 1);
+        xs += __shfl_xor_sync(0xffffffffu, xs, 2);
+        if (in && q4 == 0) ox[G * kMaxTok + t] = make_float2(o, xs);
+      }
     }
     // y starts at zero (ordered before the down tiles' adds by the grid-wide
     // gate/up count; the one-kernel step zeroes it before its logits count)
