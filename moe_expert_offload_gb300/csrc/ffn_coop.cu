@@ -1,9 +1,11 @@
 // Decode expert FFN as one persistent, cooperative kernel:
 //   y[t] = sum_j w[t][j] * Wd_e (silu(Wg_e x_t) * (Wu_e x_t))  (+ shared(x_t))
-// with int4 affine group-64 weights (Edge0 §3.1 "math convention"), every
-// executed expert's term added in the fixed rank order j (FreeToken summary
+// with int4 affine group-64 weights (Edge0 §3.1 "math convention") or MXFP4 /
+// NVFP4 weights, every executed expert's term added once (FreeToken summary
 // "core method": the partial sums of the cached and the direct sets merge
-// exactly).
+// exactly -- no term dropped or counted twice).  The same kernel, instantiated
+// with FUSED, is the whole decode layer step: router logits, selection, the
+// control step (CTA 0) and this FFN in one launch (below).
 //
 // Decode streams megabytes of packed weights against a few KB of
 // activations; the kernel keeps HBM streaming and spends few SM
