@@ -756,13 +756,12 @@ def run_prefill(args, w, rank, world, local_rank):
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     y = torch.empty((T, H), dtype=torch.float32, device=dev)
     main = torch.cuda.current_stream()
-    side = torch.cuda.Stream()
+    side = torch.cuda.Stream(priority=-1)  # the layer copy's CTAs are placed first
     copy_done = [torch.cuda.Event() for _ in range(2)]
     comp_done = [torch.cuda.Event() for _ in range(2)]
-    route_done = torch.cuda.Event()
     fws = m.moe_prefill_workspace_bytes(spec, T)
 
-    def compute(s, buf, ev=None, after_route=None):
+    def compute(s, buf, ev=None):
         l = s % L
         sp = main.cuda_stream
         if ev is not None:
@@ -770,26 +769,20 @@ def run_prefill(args, w, rank, world, local_rank):
         m.moe_route(spec, xs[l], T, wr[l], None, logits, ids, wts, sp)
         if ev is not None:
             ev[1].record(main)
-        if after_route is not None:
-            after_route()
         m.moe_expert_ffn_prefill(spec, buf, xs[l], T, ids, wts, shared, err, ws, fws, y, sp)
         if ev is not None:
             ev[2].record(main)
 
     def step_overlap(s, ev=None):
         # layer s % L computes from bufs[s % 2] while layer (s+1) % L streams into the
-        # other.  The copy starts once this step's routing is done, so that it runs
-        # beside the tensor-bound expert GEMMs, not beside the memory-bound routing
+        # other.  The copy starts with the step, beside the routing: the router's
+        # FMA-bound CTAs leave room on every SM for the copy kernel's, while the
+        # expert GEMMs that follow would lose HBM bandwidth to it
         main.wait_event(copy_done[s % 2])
-
-        def start_copy():
-            route_done.record(main)
-            side.wait_event(route_done)
-            side.wait_event(comp_done[(s + 1) % 2])
-            m.moe_layer_prefetch(spec, bank, (s + 1) % L, bufs[(s + 1) % 2], side.cuda_stream)
-            copy_done[(s + 1) % 2].record(side)
-
-        compute(s, bufs[s % 2], ev, start_copy)
+        side.wait_event(comp_done[(s + 1) % 2])
+        m.moe_layer_prefetch(spec, bank, (s + 1) % L, bufs[(s + 1) % 2], side.cuda_stream)
+        copy_done[(s + 1) % 2].record(side)
+        compute(s, bufs[s % 2], ev)
         comp_done[s % 2].record(main)
 
     def step_serial(s, ev=None):
@@ -901,7 +894,7 @@ def run_prefill(args, w, rank, world, local_rank):
         "e2e": {"value": flops * args.steps * world / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "tok_s": tokens / (ms_e2e * 1e-3),
                 "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 4},
-        "gpu_launches": 9 * args.steps,  # logits, select, 7 FFN kernels (the copy is a memcpy)
+        "gpu_launches": 10 * args.steps,  # logits, select, 7 FFN kernels, the layer copy
         "clocks": clk.summary(),
     }
     if world == 1 and not args.no_cpu:

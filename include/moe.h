@@ -387,8 +387,13 @@ int32_t moe_layer_kernel_count(const moe_spec* spec, const moe_cache* cache, int
 size_t moe_prefill_workspace_bytes(const moe_spec* spec, int32_t T);
 
 /* Copy the E expert blobs of `layer` (E * S_e bytes, contiguous in the bank)
- * into `dst` (device, 16-byte aligned) on `stream`: the whole-layer fill of the
- * double buffer.  Issue it on a second stream to overlap the previous layer. */
+ * into `dst` (device) on `stream`: the whole-layer fill of the double buffer.
+ * Issue it on a second stream to overlap another layer's compute.  With bank
+ * and dst 16-byte aligned the copy is one kernel of one 256-thread CTA per SM
+ * (streaming loads and stores, no shared memory), small enough to share each
+ * SM with the routing kernels of moe_route / moe_layer_forward_prefill, which
+ * is where it overlaps best; otherwise it is a cudaMemcpyAsync.
+ * MOE_EINVAL for a NULL pointer or a layer out of range. */
 int moe_layer_prefetch(const moe_spec* spec, const void* bank, int32_t layer, void* dst,
                        moe_stream_t stream);
 

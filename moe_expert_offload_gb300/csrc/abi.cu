@@ -10,6 +10,13 @@
 
 #include "moe_internal.cuh"
 
+namespace moe {
+// The double buffer's whole-layer copy (prefill.cu): a copy kernel of one
+// 256-thread CTA per SM, or cudaMemcpyAsync when an address or the size is not
+// a multiple of 16 bytes.
+cudaError_t launch_layer_copy(const void* src, void* dst, size_t bytes, cudaStream_t st);
+}  // namespace moe
+
 namespace {
 
 thread_local char g_err[512] = "";
@@ -829,7 +836,7 @@ extern "C" int moe_layer_prefetch(const moe_spec* spec, const void* bank, int32_
   const size_t se = (size_t)moe::expert_blob_bytes(spec->hidden, spec->inter, spec->format);
   const size_t bytes = se * spec->num_experts;
   const uint8_t* src = static_cast<const uint8_t*>(bank) + (size_t)layer * bytes;
-  cudaError_t e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, (cudaStream_t)stream);
+  cudaError_t e = moe::launch_layer_copy(src, dst, bytes, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "layer copy");
   return ok();
 }

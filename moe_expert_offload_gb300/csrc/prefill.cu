@@ -215,6 +215,26 @@ __global__ void combine_kernel(const uint16_t* __restrict__ ya, const int32_t* _
   }
 }
 
+// The double buffer's whole-layer copy (bank -> layer buffer), n 16-byte words:
+// one CTA of 256 threads per SM, each thread with eight streaming loads in
+// flight before its eight stores (L2 evict-first on both sides: the layer
+// passes through once).  It holds no shared memory and few registers, so it
+// shares every SM with the routing kernels it runs beside (their CTAs leave
+// room for it) instead of taking SMs from them.
+__global__ void __launch_bounds__(256) layer_copy_kernel(const uint4* __restrict__ src,
+                                                         uint4* __restrict__ dst, int64_t n) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + 7 * stride < n; i += 8 * stride) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = __ldcs(src + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) __stcs(dst + i + u * stride, v[u]);
+  }
+  for (; i < n; i += stride) __stcs(dst + i, __ldcs(src + i));
+}
+
 size_t al256(size_t b) { return (b + 255) / 256 * 256; }
 
 int max_tiles_for(int E, int k, int T) {
@@ -288,6 +308,19 @@ cudaError_t launch_prefill_ffn(const GemmArgs& base, const PrefillBufs& b, const
   const int64_t nc = (int64_t)T * H / 8;
   combine_kernel<<<(int)((nc + 255) / 256 < 8192 ? (nc + 255) / 256 : 8192), 256, 0, st>>>(
       b.y_assign, ids, T, k, E, H, has_shared, y);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_layer_copy(const void* src, void* dst, size_t bytes, cudaStream_t st) {
+  if (bytes == 0) return cudaSuccess;
+  if (((uintptr_t)src | (uintptr_t)dst | bytes) & 15u)
+    return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, st);
+  int d = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d);
+  if (e != cudaSuccess) return e;
+  layer_copy_kernel<<<sms, 256, 0, st>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst),
+                                         (int64_t)(bytes / 16));
   return cudaGetLastError();
 }
 

@@ -87,16 +87,53 @@ def test_prefill_skewed_routing_and_empty_experts(oracle):
     assert_ffn_close(y, ref, "skewed")
 
 
-def test_layer_prefetch_copies_the_layer():
+@pytest.mark.parametrize("offset", [0, 16, 4])
+def test_layer_prefetch_copies_the_layer(offset):
+    """The layer copy lands byte for byte and writes nothing around dst: the
+    copy kernel at 16-byte aligned destinations, the plain copy at offset 4."""
     H, I, E, L = 256, 128, 16, 3
     spec = m.make_spec(L, H, I, E, 2)
     se = m.moe_expert_bytes(spec)
     bank = dev(synth.make_bank(L * E, H, I, seed=2), DEV)
-    dst = torch.zeros((E, se), dtype=torch.uint8, device=DEV)
+    buf = torch.zeros(E * se + 64, dtype=torch.uint8, device=DEV)
+    dst = buf[offset:offset + E * se]
     side = torch.cuda.Stream()
     m.moe_layer_prefetch(spec, bank, 2, dst, side)
     side.synchronize()
-    assert torch.equal(dst, bank[2 * E:3 * E])
+    assert torch.equal(dst, bank[2 * E:3 * E].reshape(-1))
+    assert not buf[:offset].any() and not buf[offset + E * se:].any()
+
+
+def test_layer_prefetch_beside_routing_full_layer():
+    """A whole Qwen-shaped layer (256 experts, 453 MB) copied on a second stream
+    while moe_route runs on the first: the copy is exact and the routing equals
+    the routing run alone."""
+    L, H, I, E, k, T = 2, 2048, 512, 256, 8, 4096
+    spec = m.make_spec(L, H, I, E, k)
+    se = m.moe_expert_bytes(spec)
+    bank = torch.randint(0, 256, (L * E, se), dtype=torch.uint8, device=DEV)
+    dst = torch.empty((E, se), dtype=torch.uint8, device=DEV)
+    rng = np.random.default_rng(11)
+    xb = torch.from_numpy(synth.bf16_bits(rng.normal(0, 1, (T, H))).view(np.int16)).to(DEV)
+    wr = torch.from_numpy(synth.router_weights(3, E, H).view(np.int16)).to(DEV)
+
+    def route(stream):
+        logits = torch.empty((T, E), dtype=torch.float32, device=DEV)
+        ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
+        wts = torch.empty((T, k), dtype=torch.float32, device=DEV)
+        m.moe_route(spec, xb, T, wr, None, logits, ids, wts, stream.cuda_stream)
+        return logits, ids, wts
+
+    main = torch.cuda.current_stream()
+    want = route(main)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream(priority=-1)
+    m.moe_layer_prefetch(spec, bank, 1, dst, side.cuda_stream)
+    got = route(main)
+    torch.cuda.synchronize()
+    assert torch.equal(dst, bank[E:2 * E])
+    for a, b in zip(got, want):
+        assert torch.equal(a, b)
 
 
 def test_full_size_qwen_prefill_layer(oracle):
