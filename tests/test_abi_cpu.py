@@ -265,9 +265,10 @@ def test_prefill_argument_checks(L):
         m.moe_expert_ffn_prefill(s2, None, 4096, 16, 256, 256, None, None, 4096, 1 << 30, 4096,
                                  stream=0)
     assert e.value.code == m.MOE_EINVAL
-    with pytest.raises(m.MoeError) as e:
-        m.moe_layer_prefetch(s2, 4096, 7, 4096, stream=0)
-    assert e.value.code == m.MOE_EINVAL
+    for bank, layer, dst in ((4096, 7, 4096), (4096, -1, 4096), (None, 0, 4096), (4096, 0, None)):
+        with pytest.raises(m.MoeError) as e:  # layer out of range, NULL bank or destination
+            m.moe_layer_prefetch(s2, bank, layer, dst, stream=0)
+        assert e.value.code == m.MOE_EINVAL
     assert m.moe_expert_ffn_prefill(s2, None, None, 0, None, None, None, None, None, 0, None,
                                     stream=0) == m.MOE_OK
 
