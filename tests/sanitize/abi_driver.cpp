@@ -120,6 +120,11 @@ int main() {
   CHECK(moe_cache_resize_workspace_bytes(&cb, 0) == 0);
   CHECK(moe_cache_resize(&nv, &cb, 0, dummy, 1 << 20, nullptr) == MOE_EINVAL);
   CHECK(moe_cache_resize(&nv, &cb, 4, dummy, 4, nullptr) == MOE_ECAPACITY);
+  // layer prefetch: a layer out of range and NULL pointers are refused before the copy
+  CHECK(moe_layer_prefetch(&nv, dummy, nv.num_layers, dummy, nullptr) == MOE_EINVAL);
+  CHECK(moe_layer_prefetch(&nv, dummy, -1, dummy, nullptr) == MOE_EINVAL);
+  CHECK(moe_layer_prefetch(&nv, nullptr, 0, dummy, nullptr) == MOE_EINVAL);
+  CHECK(moe_layer_prefetch(&nv, dummy, 0, nullptr, nullptr) == MOE_EINVAL);
   if (g_fail) return 1;
   std::printf("abi sanitizer run: ok\n");
   return 0;
